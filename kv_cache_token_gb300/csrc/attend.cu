@@ -1,0 +1,516 @@
+// D1: split-K GQA decode attention over a paged, token-table-indexed KV pool.
+//
+// For every lane (sequence b, KV head h) the g query heads of the group
+// attend the lane's kept tokens (read through their slots, vToken review
+// Eq. (2)) and the new token (read from the call's k_new/v_new).  The work
+// is the concatenation of every lane's 16-token tiles, cut into equal
+// contiguous ranges, one per warp of a persistent grid (stream-K), so every
+// warp streams the same number of bytes whatever the lanes' lengths.  A warp
+// writes, per lane segment it covers, the running max / sum / unnormalised
+// output of the segment (split-K partials) and, for every token, its base-2
+// scaled logits, which the epilogue turns into weights once the lane's
+// log-sum-exp is known (H2O Guide, "Formulating Cumulative Attention
+// Scores": the weights are the ones the attention pass already computes).
+//
+// bf16: K/V rows move HBM -> shared memory with one cp.async.bulk per row,
+// completing on a per-stage mbarrier (3 stages per warp, L2 evict_first);
+// QK^T and PV run on the tensor cores with the warp-level bf16 MMA
+// (m16n8k16; the 16 M rows are the group's query heads), fp32 accumulation;
+// P enters the PV product as a hi + lo pair of bf16 values so the output
+// keeps ~16 bits of weight precision.
+// fp32: one thread per token on the CUDA cores (small heads only).
+#include "kvevict_internal.cuh"
+
+namespace kve {
+
+namespace {
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16(float* c, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// p -> (hi, lo) bf16 pairs with hi + lo == p to ~16 significant bits
+__device__ __forceinline__ void split_bf16(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
+  float2 hf = __bfloat1622float2(h);
+  __nv_bfloat162 l = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+  hi = *reinterpret_cast<uint32_t*>(&h);
+  lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+struct AttendArgs {
+  const void* k_pool; const void* v_pool;
+  const int32_t* slot; const int32_t* count;
+  const void* q; const void* k_new; const void* v_new;
+  float* logits; float* part_o; float* part_ml; int32_t* lane_nseg;
+  uint32_t* status;
+  int lanes, g, Hkv, Hq, cap, lcap, P;
+  float scale2;   // log2(e) / sqrt(d)
+};
+
+constexpr int kMaxLanesSmem = 1024;   // lanes per layer (validated at create)
+
+// ---------------------------------------------------------------------------
+// bf16 tensor-core kernel
+// ---------------------------------------------------------------------------
+template <int D>
+struct Bf16Cfg {
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kRowStride = kRowBytes + 16;            // +16 B: conflict-free ldmatrix
+  static constexpr int kStageBytes = 2 * 16 * kRowStride;      // K rows then V rows
+  static constexpr int kWarpBytes = kStages * kStageBytes;
+  static constexpr int kSmem = kAttendWarps * kWarpBytes;
+  static constexpr int kKs = D / 16;                           // k-steps over d
+  static constexpr int kDn = D / 8;                            // 8-wide output column tiles
+};
+
+template <int D>
+__global__ void __launch_bounds__(kAttendWarps * 32, 2) attend_bf16_kernel(AttendArgs a) {
+  using C = Bf16Cfg<D>;
+  extern __shared__ __align__(128) unsigned char smem[];
+  __shared__ int sh_prefix[kMaxLanesSmem + 1];
+  __shared__ int sh_scan[40];
+  __shared__ uint64_t sh_bar[kAttendWarps][kStages];
+
+  const int tid = threadIdx.x, lane_id = tid & 31, warp = tid >> 5;
+  const int lanes = a.lanes;
+
+  // --- lane tile prefix (every CTA computes the same table) ---------------
+  int my_max = 0;
+  {
+    int carry = 0;
+    for (int base = 0; base < lanes; base += blockDim.x) {
+      int l = base + tid;
+      int t = 0;
+      if (l < lanes) {
+        int n = a.count[l];
+        if (n < 0 || n >= a.cap) { set_status(a.status, ST_BAD_INDEX); n = n < 0 ? 0 : a.cap - 1; }
+        t = (n + 1 + 15) >> 4;
+      }
+      my_max = max(my_max, t);
+      int tot;
+      int ex = block_excl_scan(t, sh_scan, &tot);
+      if (l < lanes) sh_prefix[l] = carry + ex;
+      carry += tot;
+    }
+    if (tid == 0) sh_prefix[lanes] = carry;
+  }
+  my_max = warp_max(my_max);
+  if (lane_id == 0) sh_scan[warp] = my_max;
+  __syncthreads();
+  int max_tiles = 0;
+  for (int w = 0; w < kAttendWarps; ++w) max_tiles = max(max_tiles, sh_scan[w]);
+  const int total = sh_prefix[lanes];
+  const int warps_total = gridDim.x * kAttendWarps;
+  int tp = (total + warps_total - 1) / warps_total;
+  tp = max(tp, (max_tiles + kMaxSeg - 2) / (kMaxSeg - 1));
+  tp = max(tp, 1);
+  if (blockIdx.x == 0) {
+    for (int l = tid; l < lanes; l += blockDim.x) {
+      int s = sh_prefix[l], e = sh_prefix[l + 1];
+      a.lane_nseg[l] = (e - 1) / tp - s / tp + 1;
+    }
+  }
+
+  const int gw = blockIdx.x * kAttendWarps + warp;
+  const int t_begin = gw * tp;
+  const int t_end = min(total, t_begin + tp);
+  if (t_begin >= t_end) return;
+
+  unsigned char* wbuf = smem + warp * C::kWarpBytes;
+  uint64_t* bars = sh_bar[warp];
+  if (lane_id == 0) {
+    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncwarp();
+  const uint64_t pol = policy_evict_first();
+
+  const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(a.k_pool);
+  const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v_pool);
+  const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(a.k_new);
+  const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(a.v_new);
+  const size_t pool_rows = static_cast<size_t>(a.P) * kBlock;
+
+  // find the lane of a tile (monotone walk)
+  auto lane_of = [&](int t, int hint) {
+    int l = hint;
+    while (sh_prefix[l + 1] <= t) ++l;
+    return l;
+  };
+
+  // --- producer: issue the copies of tile t into stage st ------------------
+  int issue_lane = lane_of(t_begin, 0);
+  auto issue = [&](int t, int st) {
+    issue_lane = lane_of(t, issue_lane);
+    const int l = issue_lane;
+    const int n = min(max(a.count[l], 0), a.cap - 1);
+    const int i0 = (t - sh_prefix[l]) * 16;
+    const int valid = min(16, n + 1 - i0);
+    unsigned char* sbuf = wbuf + st * C::kStageBytes;
+    fence_proxy_async();
+    if (lane_id == 0) mbar_arrive_expect_tx(&bars[st], (uint32_t)(valid * 2 * C::kRowBytes));
+    __syncwarp();
+    const int r = lane_id & 15;
+    const bool isv = lane_id >= 16;
+    unsigned char* dst = sbuf + (isv ? 16 * C::kRowStride : 0) + r * C::kRowStride;
+    const int i = i0 + r;
+    if (r < valid) {
+      const __nv_bfloat16* src;
+      if (i < n) {
+        int s = a.slot[static_cast<size_t>(l) * a.cap + i];
+        if (s < 0 || static_cast<size_t>(s) >= pool_rows) { set_status(a.status, ST_BAD_INDEX); s = 0; }
+        src = (isv ? vp : kp) + static_cast<size_t>(s) * D;
+      } else {
+        src = (isv ? vn : kn) + static_cast<size_t>(l) * D;
+      }
+      bulk_g2s(dst, src, C::kRowBytes, &bars[st], pol);
+    } else {
+      uint4 z = make_uint4(0, 0, 0, 0);
+#pragma unroll
+      for (int o = 0; o < C::kRowBytes; o += 16) *reinterpret_cast<uint4*>(dst + o) = z;
+    }
+  };
+
+  // --- consumer state -------------------------------------------------------
+  const int gq = lane_id >> 2, cq = lane_id & 3;   // MMA group / thread-in-group
+  const int h0 = gq, h1 = gq + 8;
+  const bool v0 = h0 < a.g, v1 = h1 < a.g;
+  uint32_t qa[C::kKs][4];
+  float o_acc[C::kDn][4];
+  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  int cur_lane = -1, seg = 0, cur_n = 0;
+
+  auto load_q = [&](int l) {
+    const int b = l / a.Hkv, kh = l % a.Hkv;
+    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q) +
+                              (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kh) * a.g) * D;
+#pragma unroll
+    for (int ks = 0; ks < C::kKs; ++ks) {
+      const int c0 = ks * 16 + cq * 2;
+      qa[ks][0] = v0 ? *reinterpret_cast<const uint32_t*>(qb + h0 * D + c0) : 0u;
+      qa[ks][1] = v1 ? *reinterpret_cast<const uint32_t*>(qb + h1 * D + c0) : 0u;
+      qa[ks][2] = v0 ? *reinterpret_cast<const uint32_t*>(qb + h0 * D + c0 + 8) : 0u;
+      qa[ks][3] = v1 ? *reinterpret_cast<const uint32_t*>(qb + h1 * D + c0 + 8) : 0u;
+    }
+#pragma unroll
+    for (int dn = 0; dn < C::kDn; ++dn) o_acc[dn][0] = o_acc[dn][1] = o_acc[dn][2] = o_acc[dn][3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+  };
+
+  auto flush = [&]() {
+    float s0 = l0, s1 = l1;
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
+    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
+    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
+    const size_t base = (static_cast<size_t>(cur_lane) * kMaxSeg + seg) * a.g;
+    if (v0) {
+      float* po = a.part_o + (base + h0) * D;
+#pragma unroll
+      for (int dn = 0; dn < C::kDn; ++dn)
+        *reinterpret_cast<float2*>(po + dn * 8 + cq * 2) = make_float2(o_acc[dn][0], o_acc[dn][1]);
+      if (cq == 0) *reinterpret_cast<float2*>(a.part_ml + (base + h0) * 2) = make_float2(m0, s0);
+    }
+    if (v1) {
+      float* po = a.part_o + (base + h1) * D;
+#pragma unroll
+      for (int dn = 0; dn < C::kDn; ++dn)
+        *reinterpret_cast<float2*>(po + dn * 8 + cq * 2) = make_float2(o_acc[dn][2], o_acc[dn][3]);
+      if (cq == 0) *reinterpret_cast<float2*>(a.part_ml + (base + h1) * 2) = make_float2(m1, s1);
+    }
+  };
+
+  // --- pipeline ---------------------------------------------------------------
+  for (int s = 0; s < kStages - 1; ++s)
+    if (t_begin + s < t_end) issue(t_begin + s, s);
+
+  int cons_lane = lane_of(t_begin, 0);
+  for (int t = t_begin, u = 0; t < t_end; ++t, ++u) {
+    if (t + kStages - 1 < t_end) issue(t + kStages - 1, (u + kStages - 1) % kStages);
+    const int st = u % kStages;
+    const uint32_t par = (u / kStages) & 1;
+    {
+      int spins = 0;
+      while (!mbar_try_wait(&bars[st], par)) {
+        if (++spins > (1 << 22)) { set_status(a.status, ST_TIMEOUT); return; }
+      }
+    }
+    __syncwarp();
+
+    cons_lane = lane_of(t, cons_lane);
+    if (cons_lane != cur_lane) {
+      if (cur_lane >= 0) flush();
+      cur_lane = cons_lane;
+      seg = gw - sh_prefix[cur_lane] / tp;
+      cur_n = min(max(a.count[cur_lane], 0), a.cap - 1);
+      load_q(cur_lane);
+    }
+    const int i0 = (t - sh_prefix[cur_lane]) * 16;
+    const unsigned char* kb = wbuf + st * C::kStageBytes;
+    const unsigned char* vb = kb + 16 * C::kRowStride;
+
+    // S = Q K^T for 16 tokens (two 8-token column tiles)
+    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    {
+      const int tok = (lane_id & 7) + ((lane_id >> 4) << 3);
+      const int colb = ((lane_id >> 3) & 1) * 16;   // bytes
+      const uint32_t rowaddr = smem_u32(kb + tok * C::kRowStride + colb);
+#pragma unroll
+      for (int ks = 0; ks < C::kKs; ++ks) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(rowaddr + ks * 32, b0, b1, b2, b3);
+        mma_bf16(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+        mma_bf16(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+      }
+    }
+    // scale, mask, store logits, online softmax
+    float p[2][4];
+    float tmax0 = -INFINITY, tmax1 = -INFINITY;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int i = i0 + nt * 8 + cq * 2 + e;
+        const bool ok = i <= cur_n;
+        sacc[nt][e] = ok ? sacc[nt][e] * a.scale2 : -INFINITY;
+        sacc[nt][2 + e] = ok ? sacc[nt][2 + e] * a.scale2 : -INFINITY;
+        tmax0 = fmaxf(tmax0, sacc[nt][e]);
+        tmax1 = fmaxf(tmax1, sacc[nt][2 + e]);
+      }
+      const int i = i0 + nt * 8 + cq * 2;
+      if (v0)
+        *reinterpret_cast<float2*>(a.logits + (static_cast<size_t>(cur_lane) * a.g + h0) * a.lcap + i) =
+            make_float2(sacc[nt][0], sacc[nt][1]);
+      if (v1)
+        *reinterpret_cast<float2*>(a.logits + (static_cast<size_t>(cur_lane) * a.g + h1) * a.lcap + i) =
+            make_float2(sacc[nt][2], sacc[nt][3]);
+    }
+    tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 1));
+    tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 2));
+    tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 1));
+    tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 2));
+    const float mn0 = fmaxf(m0, tmax0), mn1 = fmaxf(m1, tmax1);
+    const float c0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - mn0);
+    const float c1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - mn1);
+    m0 = mn0;
+    m1 = mn1;
+    float ps0 = 0.f, ps1 = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        p[nt][e] = v0 ? exp2f(sacc[nt][e] - mn0) : 0.f;
+        p[nt][2 + e] = v1 ? exp2f(sacc[nt][2 + e] - mn1) : 0.f;
+        ps0 += p[nt][e];
+        ps1 += p[nt][2 + e];
+      }
+    }
+    l0 = l0 * c0 + ps0;
+    l1 = l1 * c1 + ps1;
+#pragma unroll
+    for (int dn = 0; dn < C::kDn; ++dn) {
+      o_acc[dn][0] *= c0; o_acc[dn][1] *= c0;
+      o_acc[dn][2] *= c1; o_acc[dn][3] *= c1;
+    }
+    // P as the A operand (rows = heads, k = tokens): hi and lo parts
+    uint32_t ah[4], al[4];
+    split_bf16(p[0][0], p[0][1], ah[0], al[0]);   // row h0, tokens 2c, 2c+1
+    split_bf16(p[0][2], p[0][3], ah[1], al[1]);   // row h1
+    split_bf16(p[1][0], p[1][1], ah[2], al[2]);   // row h0, tokens 2c+8, 2c+9
+    split_bf16(p[1][2], p[1][3], ah[3], al[3]);   // row h1
+    {
+      const int tok = (lane_id & 7) + (((lane_id >> 3) & 1) << 3);
+      const int colsel = lane_id >> 4;
+      const uint32_t rowaddr = smem_u32(vb + tok * C::kRowStride) + colsel * 16;
+#pragma unroll
+      for (int dn = 0; dn < C::kDn; dn += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4_t(rowaddr + dn * 16, b0, b1, b2, b3);
+        mma_bf16(o_acc[dn], ah[0], ah[1], ah[2], ah[3], b0, b1);
+        mma_bf16(o_acc[dn], al[0], al[1], al[2], al[3], b0, b1);
+        mma_bf16(o_acc[dn + 1], ah[0], ah[1], ah[2], ah[3], b2, b3);
+        mma_bf16(o_acc[dn + 1], al[0], al[1], al[2], al[3], b2, b3);
+      }
+    }
+    __syncwarp();
+  }
+  flush();
+}
+
+// ---------------------------------------------------------------------------
+// fp32 CUDA-core kernel: grid (chunks, lanes), one thread per token
+// ---------------------------------------------------------------------------
+constexpr int kF32Chunk = 128;
+
+__global__ void __launch_bounds__(kF32Chunk) attend_f32_kernel(AttendArgs a, int D) {
+  extern __shared__ float fsm[];
+  float* sq = fsm;                       // [g][D]
+  float* sp = sq + a.g * D;              // [g][kF32Chunk]
+  float* sred = sp + a.g * kF32Chunk;    // [g][2]
+  const int l = blockIdx.y, chunk = blockIdx.x, tid = threadIdx.x;
+  int n = a.count[l];
+  if (n < 0 || n >= a.cap) { if (tid == 0) set_status(a.status, ST_BAD_INDEX); n = max(0, min(n, a.cap - 1)); }
+  const int nchunks = (n + 1 + kF32Chunk - 1) / kF32Chunk;
+  if (chunk == 0 && tid == 0) a.lane_nseg[l] = nchunks;
+  if (chunk >= nchunks) return;
+  const int b = l / a.Hkv, kh = l % a.Hkv;
+  const float* qb = static_cast<const float*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kh) * a.g) * D;
+  for (int i = tid; i < a.g * D; i += blockDim.x) sq[i] = qb[i];
+  __syncthreads();
+  const int i = chunk * kF32Chunk + tid;
+  const bool ok = i <= n;
+  const float* krow = nullptr;
+  const size_t pool_rows = static_cast<size_t>(a.P) * kBlock;
+  if (ok) {
+    if (i < n) {
+      int s = a.slot[static_cast<size_t>(l) * a.cap + i];
+      if (s < 0 || static_cast<size_t>(s) >= pool_rows) { set_status(a.status, ST_BAD_INDEX); s = 0; }
+      krow = static_cast<const float*>(a.k_pool) + static_cast<size_t>(s) * D;
+    } else {
+      krow = static_cast<const float*>(a.k_new) + static_cast<size_t>(l) * D;
+    }
+  }
+  __shared__ float swarp[kF32Chunk / 32];
+  for (int h = 0; h < a.g; ++h) {
+    float s = -INFINITY;
+    if (ok) {
+      float acc = 0.f;
+      for (int e = 0; e < D; ++e) acc = fmaf(sq[h * D + e], krow[e], acc);
+      s = acc * a.scale2;
+      a.logits[(static_cast<size_t>(l) * a.g + h) * a.lcap + i] = s;
+    }
+    float m = warp_max(s);
+    if ((tid & 31) == 0) swarp[tid >> 5] = m;
+    __syncthreads();
+    m = swarp[0];
+    for (int w = 1; w < kF32Chunk / 32; ++w) m = fmaxf(m, swarp[w]);
+    __syncthreads();
+    const float pv = ok ? exp2f(s - m) : 0.f;
+    sp[h * kF32Chunk + tid] = pv;
+    float ps = pv;
+    for (int o = 16; o > 0; o >>= 1) ps += __shfl_xor_sync(0xffffffffu, ps, o);
+    if ((tid & 31) == 0) swarp[tid >> 5] = ps;
+    __syncthreads();
+    if (tid == 0) {
+      float tot = 0.f;
+      for (int w = 0; w < kF32Chunk / 32; ++w) tot += swarp[w];
+      sred[h * 2 + 0] = m;
+      sred[h * 2 + 1] = tot;
+    }
+    __syncthreads();
+  }
+  // O[h][e] = sum_i p[h][i] v_i[e]
+  const size_t base = (static_cast<size_t>(l) * kMaxSeg + chunk) * a.g;
+  for (int he = tid; he < a.g * D; he += blockDim.x) {
+    const int h = he / D, e = he % D;
+    float acc = 0.f;
+    const int cnt = min(kF32Chunk, n + 1 - chunk * kF32Chunk);
+    for (int t = 0; t < cnt; ++t) {
+      const int it = chunk * kF32Chunk + t;
+      const float* vr;
+      if (it < n) {
+        int s = a.slot[static_cast<size_t>(l) * a.cap + it];
+        if (s < 0 || static_cast<size_t>(s) >= pool_rows) s = 0;
+        vr = static_cast<const float*>(a.v_pool) + static_cast<size_t>(s) * D;
+      } else {
+        vr = static_cast<const float*>(a.v_new) + static_cast<size_t>(l) * D;
+      }
+      acc = fmaf(sp[h * kF32Chunk + t], vr[e], acc);
+    }
+    a.part_o[(base + h) * D + e] = acc;
+  }
+  if (tid < a.g) {
+    a.part_ml[(base + tid) * 2 + 0] = sred[tid * 2 + 0];
+    a.part_ml[(base + tid) * 2 + 1] = sred[tid * 2 + 1];
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_attend(const Ctx& ctx, int layer, const void* q, const void* k_new, const void* v_new,
+                          cudaStream_t stream) {
+  const Dims& dm = ctx.dims;
+  LayerState ls = layer_state(ctx, layer);
+  AttendArgs a;
+  a.k_pool = ls.k_pool; a.v_pool = ls.v_pool; a.slot = ls.slot; a.count = ls.count;
+  a.q = q; a.k_new = k_new; a.v_new = v_new;
+  a.logits = ctx.ws.logits; a.part_o = ctx.ws.part_o; a.part_ml = ctx.ws.part_ml;
+  a.lane_nseg = ctx.ws.lane_nseg; a.status = ctx.ws.status;
+  a.lanes = dm.lanes; a.g = dm.g; a.Hkv = dm.Hkv; a.Hq = dm.Hq; a.cap = dm.cap; a.lcap = dm.lcap;
+  a.P = dm.P;
+  a.scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(dm.d));
+  if (dm.dtype == KVEVICT_BF16) {
+    if (dm.lanes > kMaxLanesSmem) return cudaErrorInvalidValue;
+    const int grid = ctx.sm_count * 2;
+    if (dm.d == 128) {
+      auto k = attend_bf16_kernel<128>;
+      const int sm = Bf16Cfg<128>::kSmem;
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+      k<<<grid, kAttendWarps * 32, sm, stream>>>(a);
+    } else {
+      auto k = attend_bf16_kernel<64>;
+      const int sm = Bf16Cfg<64>::kSmem;
+      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
+      k<<<grid, kAttendWarps * 32, sm, stream>>>(a);
+    }
+  } else {
+    const int chunks = (dm.cap + kF32Chunk) / kF32Chunk;   // enough for n = cap - 1 plus the new token
+    if (chunks > kMaxSeg) return cudaErrorInvalidValue;
+    dim3 grid(chunks, dm.lanes);
+    const size_t sm = (static_cast<size_t>(dm.g) * dm.d + dm.g * kF32Chunk + 2 * dm.g) * sizeof(float);
+    attend_f32_kernel<<<grid, kF32Chunk, sm, stream>>>(a, dm.d);
+  }
+  return cudaGetLastError();
+}
+
+}  // namespace kve

@@ -1,0 +1,444 @@
+// Decode-step epilogue (one CTA per lane) and the layer allocator.
+//
+// epilogue: combines the split-K partials into the lane's log-sum-exp and
+// output; turns every kept token's logits into its group weight
+// w_j = sum_h exp(s_hj - LSE_h) and writes it straight into the policy's
+// score state (H2O: S_j += w_j; SnapKV: history[j][slot] = w_j); builds the
+// eviction keys (SnapKV: float64 window sums in slot order 0 upward, then a
+// warp-shuffle sliding max over kept neighbours, clamped); selects the
+// budgeted bottom-k outside the recent window (radix descent on (key,
+// position)); removes the victims from the token table in place; admits the
+// new token into the lowest free slot of the lane's blocks; and sizes the
+// lane's relocation plan.
+// allocate: one CTA hands out the lowest free block ids, ascending lanes,
+// first to admissions that found no slot, then to relocation destinations.
+// apply: one CTA per lane writes those admissions and runs the relocation
+// (vToken review, Sec. 3.3 Stage 3: fill each destination completely, in
+// ascending position, and release the sources).
+#include "lane_ops.cuh"
+
+namespace kve {
+namespace {
+
+constexpr int kEpiThreads = 512;
+constexpr float kLn2 = 0.6931471805599453f;
+
+struct EpiArgs {
+  LayerState ls;
+  Workspace ws;
+  Dims dm;
+  int has_q, new_pos;
+  const void* k_new; const void* v_new;
+  float* out; float* lse; int32_t* victims; int32_t* n_victims;
+};
+
+template <typename KT>
+__device__ __forceinline__ void copy_row(KT* dst, const KT* src, int d) {
+  for (int e = threadIdx.x; e < d; e += blockDim.x) dst[e] = src[e];
+}
+
+template <typename KT>
+__global__ void __launch_bounds__(kEpiThreads) decode_epilogue_kernel(EpiArgs A) {
+  __shared__ float sh_M[kMaxG], sh_L[kMaxG], sh_lse2[kMaxG];
+  __shared__ int sh_hist[256];
+  __shared__ int sh_misc[40];
+  __shared__ int sh_scan[40];
+  __shared__ int sh_idx[kEpiThreads];
+  __shared__ unsigned sh_min[32];
+  __shared__ __align__(16) float sh_rows[128 * kMaxW];
+
+  const Dims& dm = A.dm;
+  const int l = blockIdx.x, tid = threadIdx.x;
+  LaneRefs L = lane_refs(A.ls, dm, l);
+  const int n = A.ls.count[l];
+  bool bad = n < 0 || n >= dm.cap;
+  if (!bad && n > 0 && L.pos[n - 1] >= A.new_pos) {
+    if (tid == 0) set_status(A.ws.status, ST_POSITION);
+    bad = true;
+  } else if (bad && tid == 0) {
+    set_status(A.ws.status, ST_CAPACITY);
+  }
+  if (bad) {
+    if (tid == 0) { A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0; }
+    return;
+  }
+  const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
+
+  // ---- combine the split-K partials --------------------------------------
+  if (A.has_q) {
+    const int nseg = min(A.ws.lane_nseg[l], kMaxSeg);
+    const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml) + static_cast<size_t>(l) * kMaxSeg * g;
+    if (tid < g) {
+      float M = -INFINITY;
+      for (int s = 0; s < nseg; ++s) M = fmaxf(M, ml[s * g + tid].x);
+      float Ls = 0.f;
+      for (int s = 0; s < nseg; ++s) {
+        const float2 v = ml[s * g + tid];
+        if (v.x != -INFINITY) Ls += v.y * exp2f(v.x - M);
+      }
+      sh_M[tid] = M;
+      sh_L[tid] = Ls;
+      const float lse2 = M + log2f(Ls);
+      sh_lse2[tid] = lse2;
+      A.lse[static_cast<size_t>(b) * dm.Hq + kh * g + tid] = lse2 * kLn2;
+    }
+    __syncthreads();
+    const float* po = A.ws.part_o + static_cast<size_t>(l) * kMaxSeg * g * d;
+    for (int he = tid; he < g * d; he += blockDim.x) {
+      const int h = he / d, e = he - h * d;
+      float acc = 0.f;
+      for (int s = 0; s < nseg; ++s) {
+        const float m = ml[s * g + h].x;
+        if (m != -INFINITY) acc += po[(static_cast<size_t>(s) * g + h) * d + e] * exp2f(m - sh_M[h]);
+      }
+      A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = acc / sh_L[h];
+    }
+  }
+
+  // ---- weights -> score state; SnapKV window sums ----------------------------
+  const int policy = dm.policy;
+  const int W = dm.W;
+  const int rs = policy == KVEVICT_SNAPKV ? A.ls.ring_slot[l] : 0;
+  double* keys64 = A.ws.keys64 ? A.ws.keys64 + static_cast<size_t>(l) * dm.cap : nullptr;
+  double* pooled64 = A.ws.pooled64 ? A.ws.pooled64 + static_cast<size_t>(l) * dm.cap : nullptr;
+  const float* lg = A.ws.logits + static_cast<size_t>(l) * g * dm.lcap;
+  int nan_count = 0;
+  for (int i = tid; i < n; i += blockDim.x) {
+    float w = 0.f;
+    if (A.has_q) {
+      for (int h = 0; h < g; ++h) w += exp2f(lg[static_cast<size_t>(h) * dm.lcap + i] - sh_lse2[h]);
+    }
+    if (policy == KVEVICT_SNAPKV) {
+      float* row = L.ring + static_cast<size_t>(i) * W;
+      if (A.has_q) row[rs] = w;
+      double sum = 0.0;
+      for (int t = 0; t < W; ++t) sum += static_cast<double>((A.has_q && t == rs) ? w : row[t]);
+      keys64[i] = sum;
+      if (sum != sum) ++nan_count;
+    } else {
+      float sc = L.score[i];
+      if (A.has_q) {
+        sc += w;
+        L.score[i] = sc;
+      }
+      if (sc != sc) ++nan_count;
+    }
+  }
+  if (policy == KVEVICT_SNAPKV && tid == 0) keys64[n] = 0.0;
+  __syncthreads();
+  if (policy == KVEVICT_SNAPKV) {
+    if (A.has_q && tid == 0) A.ls.ring_slot[l] = (rs + 1) % W;
+    // sliding max over kept neighbours [i-r, i+r], clamped to [0, n]
+    const int r = (dm.pool_kernel - 1) / 2;
+    const int span = 32 - 2 * r;
+    const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
+    const int nn = n + 1;
+    for (int base = warp * span; base < nn; base += nwarps * span) {
+      const int idx = base - r + lane;
+      const double v = (idx >= 0 && idx < nn) ? keys64[idx] : -INFINITY;
+      double m = v;
+      for (int o = 1; o <= r; ++o) {
+        m = fmax(m, __shfl_down_sync(0xffffffffu, v, o));
+        m = fmax(m, __shfl_up_sync(0xffffffffu, v, o));
+      }
+      if (lane >= r && lane < 32 - r && idx >= 0 && idx < nn) pooled64[idx] = m;
+    }
+    __syncthreads();
+  }
+
+  // ---- bottom-k selection ------------------------------------------------------
+  const int k = max(0, n + 1 - dm.budget);
+  const int cut = A.new_pos - dm.R + 1;
+  auto candf = [&](int i) { return L.pos[i] < cut; };
+  auto posf = [&](int i) { return static_cast<uint32_t>(L.pos[i]); };
+  SelectResult sel;
+  int vcount, dead = 0;
+  int32_t* vout = A.victims + static_cast<size_t>(l) * dm.cap;
+  if (policy == KVEVICT_SNAPKV) {
+    auto keyf = [&](int i) { return mono_key(pooled64[i]); };
+    sel = block_bottom_k(n, k, 64, keyf, posf, candf, sh_hist, sh_misc);
+    auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
+    vcount = lane_remove(L, n, isv, vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx, sh_rows);
+  } else {
+    auto keyf = [&](int i) { return mono_key(L.score[i]); };
+    sel = block_bottom_k(n, k, 32, keyf, posf, candf, sh_hist, sh_misc);
+    auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
+    vcount = lane_remove(L, n, isv, vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx, sh_rows);
+  }
+  const int m = n - vcount;
+  const int nb = lane_prune_blocks(L, l, sh_scan);
+
+  // ---- admission: lowest free slot among the lane's blocks --------------------
+  unsigned best = 0xFFFFFFFFu;
+  for (int j = tid; j < nb; j += blockDim.x) {
+    const int blk = L.blocks[j];
+    const int mk = L.mask[blk] & 0xFFFF;
+    if (mk != 0xFFFF) best = min(best, static_cast<unsigned>(blk * kBlock + (__ffs(~mk) - 1)));
+  }
+  best = warp_min(best);
+  if ((tid & 31) == 0) sh_min[tid >> 5] = best;
+  __syncthreads();
+  best = 0xFFFFFFFFu;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) best = min(best, sh_min[w]);
+  const bool need = best == 0xFFFFFFFFu;
+  if (!need) {
+    KT* kp = static_cast<KT*>(A.ls.k_pool);
+    KT* vp = static_cast<KT*>(A.ls.v_pool);
+    copy_row(kp + static_cast<size_t>(best) * d, static_cast<const KT*>(A.k_new) + static_cast<size_t>(l) * d, d);
+    copy_row(vp + static_cast<size_t>(best) * d, static_cast<const KT*>(A.v_new) + static_cast<size_t>(l) * d, d);
+    if (tid == 0) atomicOr(&L.mask[best >> 4], 1 << (best & 15));
+  }
+  if (tid == 0) {
+    L.pos[m] = A.new_pos;
+    L.slot[m] = need ? -1 : static_cast<int>(best);
+    if (L.score) L.score[m] = 0.f;
+    A.ls.count[l] = m + 1;
+    if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
+    A.n_victims[l] = vcount;
+  }
+  if (L.ring)
+    for (int t = tid; t < W; t += blockDim.x) L.ring[static_cast<size_t>(m) * W + t] = 0.f;
+  __syncthreads();
+
+  // ---- relocation plan ---------------------------------------------------------
+  int t_live = 0;
+  const int ndst = lane_plan(L, nb, m + 1, false, dm.theta_f, need, &t_live, sh_scan);
+  int nan_tot;
+  (void)block_excl_scan(nan_count, sh_scan, &nan_tot);
+  if (tid == 0) {
+    A.ws.need_admit[l] = need ? 1 : 0;
+    A.ws.want_dst[l] = ndst;
+    A.ws.plan_tlive[l] = t_live;
+    if (need || ndst > 0) atomicOr(A.ws.work_flag, 1);
+    atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_VICTIMS]), (unsigned long long)vcount);
+    if (dead) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_FREED_DEAD]), (unsigned long long)dead);
+    if (nan_tot) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_NAN_KEYS]), (unsigned long long)nan_tot);
+    if (l == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_STEPS]), 1ull);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// allocator: one CTA
+// ---------------------------------------------------------------------------
+constexpr int kAllocThreads = 1024;
+
+__global__ void __launch_bounds__(kAllocThreads) allocate_kernel(LayerState ls, Workspace ws, Dims dm) {
+  __shared__ int sh_scan[40];
+  __shared__ int sh_flag;
+  const int tid = threadIdx.x;
+  if (tid == 0) {
+    sh_flag = *ws.work_flag;
+    *ws.work_flag = 0;
+  }
+  __syncthreads();
+  if (sh_flag == 0) {
+    if (tid == 0) { ws.counters[1] = 0; ws.counters[2] = 0; }
+    return;
+  }
+  // exclusive prefixes over lanes: admissions, destinations, moved tokens
+  int totA = 0, totD = 0, totM = 0;
+  for (int base = 0; base < dm.lanes; base += blockDim.x) {
+    const int l = base + tid;
+    const int a = l < dm.lanes ? ws.need_admit[l] : 0;
+    const int dd = l < dm.lanes ? ws.want_dst[l] : 0;
+    const int mm = (l < dm.lanes && dd > 0) ? ws.plan_tlive[l] : 0;
+    int ta, td, tm;
+    const int ea = block_excl_scan(a, sh_scan, &ta);
+    const int ed = block_excl_scan(dd, sh_scan, &td);
+    const int em = block_excl_scan(mm, sh_scan, &tm);
+    if (l < dm.lanes) {
+      ws.admit_block[l] = totA + ea;
+      ws.dst_begin[l] = totD + ed;
+      ws.move_begin[l] = totM + em;
+    }
+    totA += ta; totD += td; totM += tm;
+  }
+  const int need_total = totA + totD;
+  // the lowest free block ids, ascending
+  int found = 0;
+  for (int base = 0; base < dm.P && found < need_total; base += blockDim.x) {
+    const int blk = base + tid;
+    const int fr = (blk < dm.P && ls.owner[blk] < 0) ? 1 : 0;
+    int tot;
+    const int ex = block_excl_scan(fr, sh_scan, &tot);
+    if (fr && found + ex < need_total) ws.alloc_ids[found + ex] = blk;
+    found += tot;
+  }
+  found = min(found, need_total);
+  __syncthreads();
+  const int gotA = min(found, totA);
+  const bool deferred = totD > found - gotA;
+  for (int l = tid; l < dm.lanes; l += blockDim.x) {
+    if (ws.need_admit[l]) {
+      const int idx = ws.admit_block[l];
+      if (idx < gotA) {
+        const int blk = ws.alloc_ids[idx];
+        ws.admit_block[l] = blk;
+        ls.owner[blk] = l;
+      } else {
+        // no block: the new token is not stored (its table entry is dropped)
+        ws.admit_block[l] = -1;
+        ws.need_admit[l] = 0;
+        ls.count[l] -= 1;
+        set_status(ws.status, ST_NO_BLOCKS);
+      }
+    }
+    const int nd = ws.want_dst[l];
+    if (nd > 0) {
+      if (deferred) {
+        ws.want_dst[l] = 0;
+      } else {
+        const int beg = totA + ws.dst_begin[l];
+        ws.dst_begin[l] = beg;
+        for (int j = 0; j < nd; ++j) ls.owner[ws.alloc_ids[beg + j]] = l;
+      }
+    }
+  }
+  if (tid == 0) {
+    ws.counters[1] = 1;
+    ws.counters[2] = deferred ? 0 : totM;
+    if (deferred && totD > 0)
+      atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_DEFERRED]), 1ull);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// apply: one CTA per lane
+// ---------------------------------------------------------------------------
+template <typename KT>
+__global__ void __launch_bounds__(kEpiThreads) apply_kernel(LayerState ls, Workspace ws, Dims dm,
+                                                           const void* k_new, const void* v_new,
+                                                           int mark_freed, int32_t* moves) {
+  __shared__ int sh_scan[40];
+  const int l = blockIdx.x, tid = threadIdx.x;
+  if (ws.counters[1] == 0) return;
+  const int need = ws.need_admit[l];
+  const int ndst = ws.want_dst[l];
+  if (!need && ndst == 0) return;
+  LaneRefs L = lane_refs(ls, dm, l);
+  const int d = dm.d;
+  KT* kp = static_cast<KT*>(ls.k_pool);
+  KT* vp = static_cast<KT*>(ls.v_pool);
+  const int m = ls.count[l];
+  if (need) {
+    const int blk = ws.admit_block[l];
+    const size_t s = static_cast<size_t>(blk) * kBlock;
+    copy_row(kp + s * d, static_cast<const KT*>(k_new) + static_cast<size_t>(l) * d, d);
+    copy_row(vp + s * d, static_cast<const KT*>(v_new) + static_cast<size_t>(l) * d, d);
+    if (tid == 0) {
+      L.mask[blk] = 1;
+      L.slot[m - 1] = blk * kBlock;
+      const int nb = *L.nblocks;
+      L.blocks[nb] = blk;
+      *L.nblocks = nb + 1;
+      ws.need_admit[l] = 0;
+      atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_ADMIT_NEW_BLOCK]), 1ull);
+    }
+    __syncthreads();
+  }
+  if (ndst > 0) {
+    const int nb = *L.nblocks;
+    int nsrc = 0;
+    for (int j = tid; j < nb; j += blockDim.x) {
+      const int blk = L.blocks[j];
+      const int c = __popc(L.mask[blk] & 0xFFFF);
+      if (c > 0 && c < kBlock) { ws.blk_tag[blk] = 1; ++nsrc; }
+    }
+    int nsrc_tot;
+    (void)block_excl_scan(nsrc, sh_scan, &nsrc_tot);
+    const int dbeg = ws.dst_begin[l];
+    const int mbeg = ws.move_begin[l];
+    int q_total = 0;
+    for (int base = 0; base < m; base += blockDim.x) {
+      const int i = base + tid;
+      int old = -1;
+      bool src = false;
+      if (i < m) {
+        old = L.slot[i];
+        src = old >= 0 && ws.blk_tag[old >> 4] == 1;
+      }
+      int tot;
+      const int ex = block_excl_scan(src ? 1 : 0, sh_scan, &tot);
+      if (src && (q_total + ex) / kBlock >= ndst) {
+        set_status(ws.status, ST_BAD_INDEX);   // plan and tables disagree: leave the token in place
+      } else if (src) {
+        const int q = q_total + ex;
+        const int db = ws.alloc_ids[dbeg + q / kBlock];
+        const int dof = q % kBlock;
+        const int ns = db * kBlock + dof;
+        const KT* ks = kp + static_cast<size_t>(old) * d;
+        const KT* vs = vp + static_cast<size_t>(old) * d;
+        KT* kd = kp + static_cast<size_t>(ns) * d;
+        KT* vd = vp + static_cast<size_t>(ns) * d;
+        for (int e = 0; e < d; ++e) { kd[e] = ks[e]; vd[e] = vs[e]; }
+        L.slot[i] = ns;
+        if (moves) {
+          int32_t* mv = moves + static_cast<size_t>(mbeg + q) * 6;
+          mv[0] = l; mv[1] = L.pos[i]; mv[2] = old >> 4; mv[3] = old & 15; mv[4] = db; mv[5] = dof;
+        }
+      }
+      q_total += tot;
+    }
+    __syncthreads();
+    for (int j = tid; j < ndst; j += blockDim.x) {
+      const int db = ws.alloc_ids[dbeg + j];
+      const int filled = min(kBlock, q_total - j * kBlock);
+      L.mask[db] = filled >= kBlock ? 0xFFFF : ((1 << filled) - 1);
+    }
+    for (int j = tid; j < nb; j += blockDim.x) {
+      const int blk = L.blocks[j];
+      if (ws.blk_tag[blk] == 1) {
+        ws.blk_tag[blk] = 0;
+        L.mask[blk] = 0;
+        L.owner[blk] = -1;
+        if (mark_freed) ws.freed_flag[blk] = 1;
+      }
+    }
+    __syncthreads();
+    const int nb2 = lane_prune_blocks(L, l, sh_scan);
+    for (int j = tid; j < ndst; j += blockDim.x) L.blocks[nb2 + j] = ws.alloc_ids[dbeg + j];
+    __syncthreads();
+    if (tid == 0) {
+      *L.nblocks = nb2 + ndst;
+      ws.want_dst[l] = 0;
+      atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_PLANS]), 1ull);
+      atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_MOVED]), (unsigned long long)q_total);
+      atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_FREED_RELOC]), (unsigned long long)nsrc_tot);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, const void* k_new,
+                            const void* v_new, float* out, float* lse, int32_t* victims,
+                            int32_t* n_victims, cudaStream_t stream) {
+  EpiArgs A;
+  A.ls = layer_state(ctx, layer);
+  A.ws = ctx.ws;
+  A.dm = ctx.dims;
+  A.has_q = has_q ? 1 : 0;
+  A.new_pos = new_pos;
+  A.k_new = k_new; A.v_new = v_new;
+  A.out = out; A.lse = lse; A.victims = victims; A.n_victims = n_victims;
+  if (ctx.dims.dtype == KVEVICT_BF16)
+    decode_epilogue_kernel<__nv_bfloat16><<<ctx.dims.lanes, kEpiThreads, 0, stream>>>(A);
+  else
+    decode_epilogue_kernel<float><<<ctx.dims.lanes, kEpiThreads, 0, stream>>>(A);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_allocate_apply(const Ctx& ctx, int layer, const void* k_new, const void* v_new,
+                                  bool mark_freed, int32_t* moves, cudaStream_t stream) {
+  LayerState ls = layer_state(ctx, layer);
+  allocate_kernel<<<1, kAllocThreads, 0, stream>>>(ls, ctx.ws, ctx.dims);
+  if (ctx.dims.dtype == KVEVICT_BF16)
+    apply_kernel<__nv_bfloat16><<<ctx.dims.lanes, kEpiThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, k_new, v_new,
+                                                                            mark_freed ? 1 : 0, moves);
+  else
+    apply_kernel<float><<<ctx.dims.lanes, kEpiThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, k_new, v_new,
+                                                                   mark_freed ? 1 : 0, moves);
+  return cudaGetLastError();
+}
+
+}  // namespace kve

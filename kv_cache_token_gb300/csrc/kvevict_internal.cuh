@@ -1,0 +1,294 @@
+// Internal declarations of the eviction engine: data layout, workspace
+// layout, status bits, PTX helpers and block-level primitives shared by the
+// kernels.  Not part of the public C ABI (include/kvevict.h).
+#pragma once
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+
+#include "../../include/kvevict.h"
+
+namespace kve {
+
+constexpr int kBlock = 16;          // tokens per paged block (vToken review, Sec. 4.5 default)
+constexpr int kMaxSeg = 64;         // split-K segments per lane in the decode kernel
+constexpr int kMaxW = 64;           // largest SnapKV obsWindow supported
+constexpr int kMaxG = 16;           // largest GQA group
+constexpr int kAttendWarps = 4;     // warps per CTA of the decode kernel
+constexpr int kStages = 3;          // copy stages per warp of the decode kernel
+
+// device status bits (read and cleared by kvevict_last_error)
+enum : uint32_t {
+  ST_NO_BLOCKS = 1u << 0,     // a mandatory admission found no free block
+  ST_BAD_INDEX = 1u << 1,     // an index read from the tables was out of range
+  ST_TIMEOUT = 1u << 2,       // a bounded wait gave up
+  ST_CAPACITY = 1u << 3,      // a lane's token table is full
+  ST_POSITION = 1u << 4,      // the new position is not after the lane's last
+};
+
+// per-layer cumulative counters (int64), index into stats[layer][...]
+enum : int {
+  SC_STEPS = 0, SC_VICTIMS, SC_ADMIT_NEW_BLOCK, SC_FREED_DEAD, SC_FREED_RELOC,
+  SC_MOVED, SC_PLANS, SC_DEFERRED, SC_NAN_KEYS, SC_NCOUNTERS
+};
+
+struct Dims {
+  int policy, L, B, Hq, Hkv, g, d, dtype, P, cap, lanes, W, budget, R, pool_kernel;
+  float theta_f;
+  int lcap;          // logits row capacity (cap + 1 rounded up to 16)
+  int max_window;    // DropKV window queries per head the workspace holds
+};
+
+// One layer's slice of the engine state.
+struct LayerState {
+  void* k_pool; void* v_pool;      // [P][16][d]
+  int32_t* pos; int32_t* slot;     // [lanes][cap]
+  int32_t* count;                  // [lanes]
+  float* score;                    // [lanes][cap]
+  float* ring;                     // [lanes][cap][W] or null
+  int32_t* ring_slot;              // [lanes]
+  int32_t* owner; int32_t* mask;   // [P]
+  int32_t* lane_blocks;            // [lanes][cap]
+  int32_t* lane_nblocks;           // [lanes]
+  long long* stats;                // [SC_NCOUNTERS]
+};
+
+// Library scratch, carved out of the caller's workspace.
+struct Workspace {
+  uint32_t* status;                // 1 word
+  int32_t* work_flag;              // 1 word: any lane needs the allocator this call
+  float* logits;                   // [lanes][g][lcap] base-2 scaled logits
+  float* part_o;                   // [lanes][kMaxSeg][g][d]
+  float* part_ml;                  // [lanes][kMaxSeg][g][2]  (max, sum), base 2
+  int32_t* lane_nseg;              // [lanes]
+  double* keys64;                  // [lanes][cap]  SnapKV window sums
+  double* pooled64;                // [lanes][cap]  SnapKV pooled keys
+  int32_t* need_admit;             // [lanes]
+  int32_t* want_dst;               // [lanes]
+  int32_t* admit_block;            // [lanes]
+  int32_t* dst_begin;              // [lanes]  index into alloc_ids
+  int32_t* move_begin;             // [lanes]  index into the moves output
+  int32_t* plan_tlive;             // [lanes]  tokens a relocation plan moves
+  int32_t* alloc_ids;              // [P]
+  int32_t* freed_flag;             // [P]  1 = released during this call
+  int32_t* blk_tag;                // [P]  1 = source block of a running plan
+  int32_t* counters;               // [8] per-call scalars
+  // DropKV prefill-window scorer
+  float* d3_part;                  // [lanes][chunks][rows_cap][d + 2]
+  __nv_bfloat16* d3_ahi;           // [lanes][rows][d]
+  __nv_bfloat16* d3_alo;           // [lanes][rows][d]
+  float* d3_rowc;                  // [lanes][rows][2]  (lse2, |a|^2)
+  float* d3_score_part;            // [2][lanes][cap]
+};
+
+struct Ctx {
+  kvevict_config cfg;
+  kvevict_buffers buf;
+  Dims dims;
+  Workspace ws;
+  int sm_count;
+  int device;
+  size_t ws_bytes;
+};
+
+// workspace layout (host)
+size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base);
+Dims make_dims(const kvevict_config& c);
+LayerState layer_state(const Ctx& ctx, int layer);
+int d3_chunks(const Dims& dm, int sm_count);
+int d3_rows_max(const Dims& dm);
+
+// kernel launchers (host)
+cudaError_t launch_reset(const Ctx&, cudaStream_t);
+cudaError_t launch_prefill(const Ctx&, int layer, const void* k, const void* v, int n, cudaStream_t);
+cudaError_t launch_decode(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
+                          int new_pos, float* out, float* lse, int32_t* victims, int32_t* n_victims,
+                          cudaStream_t);
+cudaError_t launch_select(const Ctx&, const void* keys, int key_dtype, const int32_t* positions,
+                          const int32_t* counts, int n_lanes, int stride, int budget, int recent,
+                          int32_t* victims, int32_t* n_victims, cudaStream_t);
+cudaError_t launch_compact(const Ctx&, int layer, const int32_t* victims, const int32_t* n_victims,
+                           int32_t* freed, int32_t* n_freed, int32_t* moves, int32_t* n_moves,
+                           cudaStream_t);
+cudaError_t launch_score(const Ctx&, int layer, const void* q_win, int w, const int32_t* q_pos,
+                         float* lse, float* a_out, float* scores, cudaStream_t);
+cudaError_t launch_stats(const Ctx&, int layer, long long* out, cudaStream_t);
+cudaError_t launch_attend(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
+                          cudaStream_t);
+cudaError_t launch_epilogue(const Ctx&, int layer, bool has_q, int new_pos, const void* k_new,
+                            const void* v_new, float* out, float* lse, int32_t* victims,
+                            int32_t* n_victims, cudaStream_t);
+cudaError_t launch_allocate_apply(const Ctx&, int layer, const void* k_new, const void* v_new,
+                                  bool mark_freed, int32_t* moves, cudaStream_t);
+
+// ---------------------------------------------------------------------------
+// device helpers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) { atomicOr(st, bits); }
+
+// Monotone unsigned images of float keys: a < b  <=>  mono(a) < mono(b).
+// -0.0 maps to +0.0; every NaN maps above +inf (a NaN-scored token is the
+// last to be evicted).
+__device__ __forceinline__ unsigned long long mono_key(float x) {
+  if (x == 0.0f) x = 0.0f;
+  uint32_t u = __float_as_uint(x);
+  if (x != x) return 0xFFFFFFFFull;
+  u = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+  return u;
+}
+__device__ __forceinline__ unsigned long long mono_key(double x) {
+  if (x == 0.0) x = 0.0;
+  unsigned long long u = static_cast<unsigned long long>(__double_as_longlong(x));
+  if (x != x) return 0xFFFFFFFFFFFFFFFFull;
+  u = (u & 0x8000000000000000ull) ? ~u : (u | 0x8000000000000000ull);
+  return u;
+}
+
+// warp/block reductions and scans
+__device__ __forceinline__ int warp_incl_scan(int v) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    int t = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += t;
+  }
+  return v;
+}
+
+// Block-wide exclusive scan of one int per thread; returns the exclusive
+// prefix and writes the block total.  sh must hold 33 ints.  All threads of
+// the block must call it.
+__device__ __forceinline__ int block_excl_scan(int v, int* sh, int* total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5, nw = (blockDim.x + 31) >> 5;
+  int inc = warp_incl_scan(v);
+  if (lane == 31) sh[wid] = inc;
+  __syncthreads();
+  if (wid == 0) {
+    int x = lane < nw ? sh[lane] : 0;
+    int xs = warp_incl_scan(x);
+    if (lane < nw) sh[lane] = xs - x;
+    if (lane == nw - 1) sh[32] = xs;
+  }
+  __syncthreads();
+  int r = sh[wid] + inc - v;
+  *total = sh[32];
+  __syncthreads();
+  return r;
+}
+
+template <typename T>
+__device__ __forceinline__ T warp_max(T v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = max(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+template <typename T>
+__device__ __forceinline__ T warp_min(T v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = min(v, __shfl_xor_sync(0xffffffffu, v, o));
+  return v;
+}
+__device__ __forceinline__ int warp_sum(int v) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// ---------------------------------------------------------------------------
+// Bottom-k selection over one lane (one CTA): the k candidates with the
+// smallest (key, position), found by an MSB-first radix descent over the
+// composite key (monotone key bits, then the position).  The result is a
+// threshold such that a candidate is a victim iff its composite, restricted
+// to the resolved bits, is below the prefix (or equal to it when inclusive).
+// ---------------------------------------------------------------------------
+struct SelectResult {
+  unsigned long long key_prefix, key_mask;
+  uint32_t pos_prefix, pos_mask;
+  int inclusive;   // candidates equal to the prefix on the resolved bits are victims
+  int k;           // number of victims (0 = none)
+};
+
+__device__ __forceinline__ bool select_is_victim(const SelectResult& r, unsigned long long key,
+                                                 uint32_t pos) {
+  if (r.k <= 0) return false;
+  unsigned long long kk = key & r.key_mask;
+  if (kk != r.key_prefix) return kk < r.key_prefix;
+  uint32_t pp = pos & r.pos_mask;
+  if (pp != r.pos_prefix) return pp < r.pos_prefix;
+  return r.inclusive != 0;
+}
+
+// KeyFn(i) -> unsigned long long monotone key of entry i; PosFn(i) -> uint32
+// position; CandFn(i) -> bool.  key_bits = 32 or 64.  sh_hist: 256 ints,
+// sh_misc: 40 ints.  Returns the same SelectResult in every thread.
+template <typename KeyFn, typename PosFn, typename CandFn>
+__device__ SelectResult block_bottom_k(int n, int k, int key_bits, KeyFn keyf, PosFn posf,
+                                       CandFn candf, int* sh_hist, int* sh_misc) {
+  SelectResult r;
+  r.key_prefix = 0; r.key_mask = 0; r.pos_prefix = 0; r.pos_mask = 0; r.inclusive = 0; r.k = k;
+  if (k <= 0) { r.k = 0; return r; }
+  const int total_bits = key_bits + 32;
+  int k_rem = k;
+  for (int shift = total_bits - 8; shift >= 0; shift -= 8) {
+    for (int i = threadIdx.x; i < 256; i += blockDim.x) sh_hist[i] = 0;
+    __syncthreads();
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      if (!candf(i)) continue;
+      unsigned long long key = keyf(i);
+      uint32_t pos = posf(i);
+      if ((key & r.key_mask) != r.key_prefix || (pos & r.pos_mask) != r.pos_prefix) continue;
+      int digit = shift >= 32 ? (int)((key >> (shift - 32)) & 0xFF) : (int)((pos >> shift) & 0xFF);
+      atomicAdd(&sh_hist[digit], 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < 32) {
+      // find the bucket where the cumulative count reaches k_rem
+      const int lane = threadIdx.x;
+      int c[8];
+      int s = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { c[j] = sh_hist[lane * 8 + j]; s += c[j]; }
+      int inc = warp_incl_scan(s);
+      int exc = inc - s;
+      int found = -1, below = 0, cnt = 0;
+      if (exc < k_rem && inc >= k_rem) {
+        int acc = exc;
+        for (int j = 0; j < 8; ++j) {
+          if (acc + c[j] >= k_rem) { found = lane * 8 + j; below = acc; cnt = c[j]; break; }
+          acc += c[j];
+        }
+      }
+      unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
+      int src = ball ? __ffs(ball) - 1 : 0;
+      found = __shfl_sync(0xffffffffu, found, src);
+      below = __shfl_sync(0xffffffffu, below, src);
+      cnt = __shfl_sync(0xffffffffu, cnt, src);
+      if (lane == 0) { sh_misc[0] = ball ? found : -1; sh_misc[1] = below; sh_misc[2] = cnt; }
+    }
+    __syncthreads();
+    int b = sh_misc[0], below = sh_misc[1], cnt = sh_misc[2];
+    __syncthreads();
+    if (b < 0) {   // fewer candidates than k: everything matching the prefix is a victim
+      r.inclusive = 1;
+      return r;
+    }
+    if (shift >= 32) {
+      r.key_prefix |= (unsigned long long)b << (shift - 32);
+      r.key_mask |= 0xFFull << (shift - 32);
+    } else {
+      r.pos_prefix |= (uint32_t)b << shift;
+      r.pos_mask |= 0xFFu << shift;
+    }
+    k_rem -= below;
+    if (cnt == k_rem) { r.inclusive = 1; return r; }
+  }
+  r.inclusive = 1;   // fully resolved: exactly one entry equals the prefix
+  return r;
+}
+
+}  // namespace kve

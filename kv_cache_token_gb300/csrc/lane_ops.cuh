@@ -1,0 +1,160 @@
+// Lane-level device routines shared by the decode epilogue and the forced
+// compaction: in-place stable removal of victims from a token table,
+// release of emptied blocks, pruning of the lane's block list, and the
+// relocation plan (vToken review, Sec. 3.3 Stages 1 and 3).  Each routine is
+// executed by all threads of one CTA that owns the lane.
+#pragma once
+#include "kvevict_internal.cuh"
+
+namespace kve {
+
+struct LaneRefs {
+  int32_t* pos; int32_t* slot; float* score; float* ring;   // lane slices
+  int32_t* blocks; int32_t* nblocks;                        // lane block list
+  int32_t* owner; int32_t* mask;                            // layer pool
+  int W;
+};
+
+__device__ __forceinline__ LaneRefs lane_refs(const LayerState& ls, const Dims& dm, int l) {
+  LaneRefs r;
+  const size_t off = static_cast<size_t>(l) * dm.cap;
+  r.pos = ls.pos + off;
+  r.slot = ls.slot + off;
+  r.score = ls.score ? ls.score + off : nullptr;
+  r.ring = ls.ring ? ls.ring + off * dm.W : nullptr;
+  r.blocks = ls.lane_blocks + off;
+  r.nblocks = ls.lane_nblocks + l;
+  r.owner = ls.owner;
+  r.mask = ls.mask;
+  r.W = dm.W;
+  return r;
+}
+
+// Removes the entries i < n for which is_victim(i) holds, keeping the order
+// of the survivors.  Victim positions are appended (ascending) to vout (if
+// not null).  Each victim's live bit is cleared; a block whose last live bit
+// clears is released (owner -1) and, if freed_flag is given, flagged.
+// Returns the number of victims.  sh_scan: 40 ints, sh_idx: blockDim ints.
+template <typename VictimFn>
+__device__ __forceinline__ int lane_remove(const LaneRefs& L, int n, VictimFn is_victim, int32_t* vout,
+                           int32_t* freed_flag, int* n_dead, int P, uint32_t* status,
+                           int* sh_scan, int* sh_idx, float* sh_rows) {
+  int kept_total = 0, vict_total = 0, dead = 0;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    int p = 0, s = 0;
+    float sc = 0.f;
+    bool isv = false, keep = false;
+    if (i < n) {
+      p = L.pos[i];
+      s = L.slot[i];
+      if (L.score) sc = L.score[i];
+      isv = is_victim(i);
+      keep = !isv;
+    }
+    int ktot, vtot;
+    const int kex = block_excl_scan(keep ? 1 : 0, sh_scan, &ktot);
+    const int vex = block_excl_scan(isv ? 1 : 0, sh_scan, &vtot);
+    const int ni = kept_total + kex;
+    sh_idx[threadIdx.x] = keep ? ni : -1;
+    // every read of this chunk happened before the scans' barriers
+    if (keep) {
+      L.pos[ni] = p;
+      L.slot[ni] = s;
+      if (L.score) L.score[ni] = sc;
+    }
+    if (isv) {
+      if (vout) vout[vict_total + vex] = p;
+      if (s >= 0 && s < P * kBlock) {
+        const int b = s >> 4;
+        const int bit = 1 << (s & 15);
+        const int old = atomicAnd(&L.mask[b], ~bit);
+        if ((old & ~bit) == 0 && (old & bit)) {
+          L.owner[b] = -1;
+          if (freed_flag) freed_flag[b] = 1;
+          ++dead;
+        }
+      } else if (s >= 0) {
+        set_status(status, ST_BAD_INDEX);
+      }
+    }
+    __syncthreads();
+    if (L.ring) {
+      // move history rows of survivors: read a group of rows, barrier, write
+      const int W = L.W;
+      const int cnt = min(static_cast<int>(blockDim.x), n - base);
+      for (int g0 = 0; g0 < cnt; g0 += 128) {
+        const int rows = min(128, cnt - g0);
+        for (int e = threadIdx.x; e < rows * W; e += blockDim.x)
+          sh_rows[e] = L.ring[static_cast<size_t>(base + g0) * W + e];
+        __syncthreads();
+        for (int e = threadIdx.x; e < rows * W; e += blockDim.x) {
+          const int dst = sh_idx[g0 + e / W];
+          if (dst >= 0) L.ring[static_cast<size_t>(dst) * W + e % W] = sh_rows[e];
+        }
+        __syncthreads();
+      }
+    }
+    kept_total += ktot;
+    vict_total += vtot;
+  }
+  if (n_dead) {
+    int d = dead;
+    // block-wide sum via the scan helper
+    int tot;
+    (void)block_excl_scan(d, sh_scan, &tot);
+    *n_dead = tot;
+  }
+  return vict_total;
+}
+
+// Drops released blocks (owner != l) from the lane's block list, stably.
+__device__ __forceinline__ int lane_prune_blocks(const LaneRefs& L, int l, int* sh_scan) {
+  const int nb = *L.nblocks;
+  int out = 0;
+  for (int base = 0; base < nb; base += blockDim.x) {
+    const int j = base + threadIdx.x;
+    int b = -1;
+    bool keep = false;
+    if (j < nb) {
+      b = L.blocks[j];
+      keep = b >= 0 && L.owner[b] == l;
+    }
+    int tot;
+    const int ex = block_excl_scan(keep ? 1 : 0, sh_scan, &tot);
+    if (keep) L.blocks[out + ex] = b;
+    __syncthreads();
+    out += tot;
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) *L.nblocks = out;
+  __syncthreads();
+  return out;
+}
+
+// Relocation plan of a lane after its evictions and admission; a pending
+// admission counts as one more block holding one token.
+// Returns the number of destination blocks (0 = no plan); *t_live = tokens to move.
+__device__ __forceinline__ int lane_plan(const LaneRefs& L, int nb, int n_live, bool forced, float theta_f,
+                         bool pending_admit, int* t_live_out, int* sh_scan) {
+  const int N = nb + (pending_admit ? 1 : 0);
+  if (N == 0) { *t_live_out = 0; return 0; }
+  // Eq. (1) over the lane's blocks, in double (theta_f is widened exactly)
+  const double Fd = 1.0 - static_cast<double>(n_live) / (static_cast<double>(N) * kBlock);
+  if (!forced && !(Fd > static_cast<double>(theta_f))) { *t_live_out = 0; return 0; }
+  int src = 0, tl = 0;
+  for (int j = threadIdx.x; j < nb; j += blockDim.x) {
+    const int c = __popc(L.mask[L.blocks[j]] & 0xFFFF);
+    if (c > 0 && c < kBlock) { ++src; tl += c; }
+  }
+  int src_tot, tl_tot;
+  (void)block_excl_scan(src, sh_scan, &src_tot);
+  (void)block_excl_scan(tl, sh_scan, &tl_tot);
+  if (pending_admit) { src_tot += 1; tl_tot += 1; }
+  const int ndst = (tl_tot + kBlock - 1) / kBlock;
+  if (!(src_tot > ndst)) { *t_live_out = 0; return 0; }
+  *t_live_out = tl_tot;
+  return ndst;
+}
+
+}  // namespace kve

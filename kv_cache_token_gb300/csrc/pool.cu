@@ -1,0 +1,296 @@
+// Pool management: reset, prompt admission, standalone bottom-k selection,
+// forced compaction with its freed-block / move outputs, and the layer
+// metrics (vToken review, Eq. (1) and Fig. 1's share of blocks at <= 50%
+// utilisation).
+#include "lane_ops.cuh"
+
+namespace kve {
+namespace {
+
+constexpr int kThreads = 512;
+constexpr int kSelThreads = 1024;
+
+// ---------------------------------------------------------------------------
+// prompt admission
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) prefill_alloc_kernel(LayerState ls, Workspace ws, Dims dm, int n) {
+  __shared__ int sh_scan[40];
+  __shared__ int sh_bad;
+  const int tid = threadIdx.x;
+  const int need = (n + kBlock - 1) / kBlock;
+  const int total = need * dm.lanes;
+  if (tid == 0) sh_bad = 0;
+  __syncthreads();
+  for (int l = tid; l < dm.lanes; l += blockDim.x)
+    if (ls.count[l] != 0) sh_bad = 1;
+  __syncthreads();
+  if (sh_bad || n > dm.cap - 1) {
+    if (tid == 0) { ws.counters[4] = 0; set_status(ws.status, ST_CAPACITY); }
+    return;
+  }
+  int found = 0;
+  for (int base = 0; base < dm.P && found < total; base += blockDim.x) {
+    const int blk = base + tid;
+    const int fr = (blk < dm.P && ls.owner[blk] < 0) ? 1 : 0;
+    int tot;
+    const int ex = block_excl_scan(fr, sh_scan, &tot);
+    if (fr && found + ex < total) ws.alloc_ids[found + ex] = blk;
+    found += tot;
+  }
+  __syncthreads();
+  if (found < total) {
+    if (tid == 0) { ws.counters[4] = 0; set_status(ws.status, ST_NO_BLOCKS); }
+    return;
+  }
+  for (int j = tid; j < total; j += blockDim.x) {
+    const int blk = ws.alloc_ids[j];
+    const int l = j / need, jb = j % need;
+    ls.owner[blk] = l;
+    const int filled = min(kBlock, n - jb * kBlock);
+    ls.mask[blk] = filled >= kBlock ? 0xFFFF : ((1 << filled) - 1);
+    ls.lane_blocks[static_cast<size_t>(l) * dm.cap + jb] = blk;
+  }
+  for (int l = tid; l < dm.lanes; l += blockDim.x) {
+    ls.lane_nblocks[l] = need;
+    ls.count[l] = n;
+    ls.ring_slot[l] = 0;
+  }
+  if (tid == 0) ws.counters[4] = 1;
+}
+
+// grid (token chunks, lanes): table entries and K/V rows (16-byte pieces)
+template <typename KT>
+__global__ void __launch_bounds__(kThreads) prefill_fill_kernel(LayerState ls, Workspace ws, Dims dm, int n,
+                                                               const KT* kc, const KT* vc) {
+  if (ws.counters[4] == 0) return;
+  const int l = blockIdx.y;
+  const int need = (n + kBlock - 1) / kBlock;
+  const int per = 256;   // tokens per CTA
+  const int t0 = blockIdx.x * per;
+  if (t0 >= n) return;
+  const int t1 = min(n, t0 + per);
+  const size_t lo = static_cast<size_t>(l) * dm.cap;
+  for (int i = t0 + threadIdx.x; i < t1; i += blockDim.x) {
+    const int blk = ws.alloc_ids[l * need + i / kBlock];
+    ls.pos[lo + i] = i;
+    ls.slot[lo + i] = blk * kBlock + (i % kBlock);
+    if (ls.score) ls.score[lo + i] = 0.f;
+  }
+  if (ls.ring) {
+    float* r = ls.ring + lo * dm.W;
+    for (size_t e = static_cast<size_t>(t0) * dm.W + threadIdx.x; e < static_cast<size_t>(t1) * dm.W; e += blockDim.x)
+      r[e] = 0.f;
+  }
+  const int vec = 16 / sizeof(KT);               // elements per 16-byte piece
+  const int per_row = dm.d / vec;
+  const size_t src_lane = static_cast<size_t>(l) * n * dm.d;
+  const uint4* ks = reinterpret_cast<const uint4*>(kc + src_lane);
+  const uint4* vs = reinterpret_cast<const uint4*>(vc + src_lane);
+  uint4* kd = reinterpret_cast<uint4*>(ls.k_pool);
+  uint4* vd = reinterpret_cast<uint4*>(ls.v_pool);
+  for (int e = threadIdx.x; e < (t1 - t0) * per_row; e += blockDim.x) {
+    const int i = t0 + e / per_row, c = e % per_row;
+    const int blk = ws.alloc_ids[l * need + i / kBlock];
+    const size_t slot = static_cast<size_t>(blk) * kBlock + (i % kBlock);
+    kd[slot * per_row + c] = ks[static_cast<size_t>(i) * per_row + c];
+    vd[slot * per_row + c] = vs[static_cast<size_t>(i) * per_row + c];
+  }
+}
+
+// ---------------------------------------------------------------------------
+// standalone selection
+// ---------------------------------------------------------------------------
+template <typename KeyT>
+__global__ void __launch_bounds__(kSelThreads) select_kernel(const KeyT* keys, const int32_t* positions,
+                                                            const int32_t* counts, int stride, int budget, int R,
+                                                            int32_t* victims, int32_t* n_victims) {
+  __shared__ int sh_hist[256];
+  __shared__ int sh_misc[40];
+  __shared__ int sh_scan[40];
+  const int l = blockIdx.x;
+  const int n = max(0, min(counts[l], stride));
+  const KeyT* kk = keys + static_cast<size_t>(l) * stride;
+  const int32_t* pp = positions + static_cast<size_t>(l) * stride;
+  if (n == 0) {
+    if (threadIdx.x == 0) n_victims[l] = 0;
+    return;
+  }
+  const int newest = pp[n - 1];
+  const int cut = newest - R + 1;
+  const int k = max(0, n - budget);
+  auto candf = [&](int i) { return pp[i] < cut; };
+  auto posf = [&](int i) { return static_cast<uint32_t>(pp[i]); };
+  auto keyf = [&](int i) { return mono_key(kk[i]); };
+  const SelectResult sel = block_bottom_k(n, k, sizeof(KeyT) * 8, keyf, posf, candf, sh_hist, sh_misc);
+  int total = 0;
+  int32_t* vo = victims + static_cast<size_t>(l) * stride;
+  for (int base = 0; base < n; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    const bool v = i < n && candf(i) && select_is_victim(sel, keyf(i), posf(i));
+    int tot;
+    const int ex = block_excl_scan(v ? 1 : 0, sh_scan, &tot);
+    if (v) vo[total + ex] = pp[i];
+    total += tot;
+  }
+  if (threadIdx.x == 0) n_victims[l] = total;
+}
+
+// ---------------------------------------------------------------------------
+// forced compaction
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(kThreads) compact_evict_kernel(LayerState ls, Workspace ws, Dims dm,
+                                                                const int32_t* victims,
+                                                                const int32_t* n_victims) {
+  __shared__ int sh_scan[40];
+  __shared__ int sh_idx[kThreads];
+  __shared__ __align__(16) float sh_rows[128 * kMaxW];
+  const int l = blockIdx.x, tid = threadIdx.x;
+  LaneRefs L = lane_refs(ls, dm, l);
+  const int n = ls.count[l];
+  if (n < 0 || n > dm.cap) {
+    if (tid == 0) { set_status(ws.status, ST_BAD_INDEX); ws.want_dst[l] = 0; ws.need_admit[l] = 0; }
+    return;
+  }
+  const int k = max(0, min(n_victims[l], n));
+  const int32_t* vl = victims + static_cast<size_t>(l) * dm.cap;
+  auto isv = [&](int i) {
+    const int p = L.pos[i];
+    int lo = 0, hi = k;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (vl[mid] < p) lo = mid + 1; else hi = mid;
+    }
+    return lo < k && vl[lo] == p;
+  };
+  int dead = 0;
+  const int vcount = lane_remove(L, n, isv, nullptr, ws.freed_flag, &dead, dm.P, ws.status, sh_scan, sh_idx,
+                                 sh_rows);
+  const int m = n - vcount;
+  if (tid == 0) ls.count[l] = m;
+  const int nb = lane_prune_blocks(L, l, sh_scan);
+  int t_live = 0;
+  const int ndst = lane_plan(L, nb, m, true, dm.theta_f, false, &t_live, sh_scan);
+  if (tid == 0) {
+    ws.need_admit[l] = 0;
+    ws.want_dst[l] = ndst;
+    ws.plan_tlive[l] = t_live;
+    if (ndst > 0) atomicOr(ws.work_flag, 1);
+    atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_VICTIMS]), (unsigned long long)vcount);
+    if (dead) atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_FREED_DEAD]), (unsigned long long)dead);
+  }
+}
+
+__global__ void __launch_bounds__(1024) compact_finalize_kernel(Workspace ws, Dims dm, int32_t* freed,
+                                                               int32_t* n_freed, int32_t* n_moves) {
+  __shared__ int sh_scan[40];
+  int total = 0;
+  for (int base = 0; base < dm.P; base += blockDim.x) {
+    const int blk = base + threadIdx.x;
+    const int f = (blk < dm.P && ws.freed_flag[blk]) ? 1 : 0;
+    int tot;
+    const int ex = block_excl_scan(f, sh_scan, &tot);
+    if (f) {
+      if (freed) freed[total + ex] = blk;
+      ws.freed_flag[blk] = 0;
+    }
+    total += tot;
+  }
+  if (threadIdx.x == 0) {
+    if (n_freed) *n_freed = total;
+    if (n_moves) *n_moves = ws.counters[1] ? ws.counters[2] : 0;
+  }
+}
+
+// ---------------------------------------------------------------------------
+// metrics
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(1024) stats_kernel(LayerState ls, Dims dm, long long* out) {
+  __shared__ unsigned long long sh[3][32];
+  unsigned long long N = 0, live = 0, half = 0;
+  for (int blk = threadIdx.x; blk < dm.P; blk += blockDim.x) {
+    if (ls.owner[blk] >= 0) {
+      const int c = __popc(ls.mask[blk] & 0xFFFF);
+      ++N;
+      live += c;
+      if (c <= kBlock / 2) ++half;
+    }
+  }
+  for (int o = 16; o > 0; o >>= 1) {
+    N += __shfl_xor_sync(0xffffffffu, N, o);
+    live += __shfl_xor_sync(0xffffffffu, live, o);
+    half += __shfl_xor_sync(0xffffffffu, half, o);
+  }
+  const int w = threadIdx.x >> 5;
+  if ((threadIdx.x & 31) == 0) { sh[0][w] = N; sh[1][w] = live; sh[2][w] = half; }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    unsigned long long a = 0, b = 0, c = 0;
+    for (int i = 0; i < (int)(blockDim.x >> 5); ++i) { a += sh[0][i]; b += sh[1][i]; c += sh[2][i]; }
+    for (int i = 0; i < SC_NCOUNTERS; ++i) out[i] = ls.stats[i];
+    out[KVEVICT_STAT_BLOCKS] = (long long)a;
+    out[KVEVICT_STAT_LIVE] = (long long)b;
+    out[KVEVICT_STAT_HALF_EMPTY] = (long long)c;
+    out[KVEVICT_STAT_LANES] = dm.lanes;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_prefill(const Ctx& ctx, int layer, const void* k, const void* v, int n, cudaStream_t stream) {
+  LayerState ls = layer_state(ctx, layer);
+  prefill_alloc_kernel<<<1, 1024, 0, stream>>>(ls, ctx.ws, ctx.dims, n);
+  dim3 grid((n + 255) / 256, ctx.dims.lanes);
+  if (ctx.dims.dtype == KVEVICT_BF16)
+    prefill_fill_kernel<__nv_bfloat16><<<grid, kThreads, 0, stream>>>(
+        ls, ctx.ws, ctx.dims, n, static_cast<const __nv_bfloat16*>(k), static_cast<const __nv_bfloat16*>(v));
+  else
+    prefill_fill_kernel<float><<<grid, kThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, n,
+                                                             static_cast<const float*>(k),
+                                                             static_cast<const float*>(v));
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select(const Ctx& ctx, const void* keys, int key_dtype, const int32_t* positions,
+                          const int32_t* counts, int n_lanes, int stride, int budget, int recent,
+                          int32_t* victims, int32_t* n_victims, cudaStream_t stream) {
+  (void)ctx;
+  if (key_dtype == KVEVICT_KEY_F64)
+    select_kernel<double><<<n_lanes, kSelThreads, 0, stream>>>(static_cast<const double*>(keys), positions, counts,
+                                                              stride, budget, recent, victims, n_victims);
+  else
+    select_kernel<float><<<n_lanes, kSelThreads, 0, stream>>>(static_cast<const float*>(keys), positions, counts,
+                                                             stride, budget, recent, victims, n_victims);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_compact(const Ctx& ctx, int layer, const int32_t* victims, const int32_t* n_victims,
+                           int32_t* freed, int32_t* n_freed, int32_t* moves, int32_t* n_moves,
+                           cudaStream_t stream) {
+  LayerState ls = layer_state(ctx, layer);
+  compact_evict_kernel<<<ctx.dims.lanes, kThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, victims, n_victims);
+  cudaError_t e = launch_allocate_apply(ctx, layer, nullptr, nullptr, true, moves, stream);
+  if (e != cudaSuccess) return e;
+  compact_finalize_kernel<<<1, 1024, 0, stream>>>(ctx.ws, ctx.dims, freed, n_freed, n_moves);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_stats(const Ctx& ctx, int layer, long long* out, cudaStream_t stream) {
+  LayerState ls = layer_state(ctx, layer);
+  stats_kernel<<<1, 1024, 0, stream>>>(ls, ctx.dims, out);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_decode(const Ctx& ctx, int layer, const void* q, const void* k_new, const void* v_new,
+                          int new_pos, float* out, float* lse, int32_t* victims, int32_t* n_victims,
+                          cudaStream_t stream) {
+  cudaError_t e;
+  if (q) {
+    e = launch_attend(ctx, layer, q, k_new, v_new, stream);
+    if (e != cudaSuccess) return e;
+  }
+  e = launch_epilogue(ctx, layer, q != nullptr, new_pos, k_new, v_new, out, lse, victims, n_victims, stream);
+  if (e != cudaSuccess) return e;
+  return launch_allocate_apply(ctx, layer, k_new, v_new, false, nullptr, stream);
+}
+
+}  // namespace kve

@@ -77,7 +77,7 @@ class Engine:
         g = self.g
         out = np.zeros((c.batch, c.num_q_heads, c.head_dim))
         lse = np.zeros((c.batch, c.num_q_heads))
-        victims, freed, pending, new_rows = [], [], [], {}
+        victims, freed, pending, new_rows, all_keys, all_pos = [], [], [], {}, [], []
         for lane in range(self.n_lanes):
             b, h = divmod(lane, c.num_kv_heads)
             L = PL.lanes[lane]
@@ -99,6 +99,8 @@ class Engine:
             pos_all = np.append(L.pos, np.int64(new_pos))
             vict = select_lane(keys, pos_all, c.budget, c.recent_window)
             assert new_pos not in vict
+            all_keys.append(keys)
+            all_pos.append(pos_all)
             freed += PL.evict(lane, vict)
             if not PL.admit(lane, new_pos, kn, vn):
                 pending.append(lane)
@@ -106,7 +108,7 @@ class Engine:
             victims.append(vict)
         moves, freed2, deferred = self._finish_layer(PL, pending, new_rows, forced=False)
         return dict(out=out, lse=lse, victims=victims, moves=moves,
-                    freed=sorted(freed + freed2), deferred=deferred)
+                    freed=sorted(freed + freed2), deferred=deferred, keys=all_keys, pos=all_pos)
 
     def _finish_layer(self, PL, pending, new_rows, forced):
         """Layer-level end of a step: admissions that need a block, then the

@@ -1,0 +1,85 @@
+"""Decode-step parity: the CUDA engine (attention, scoring, selection,
+eviction, admission, relocation) against the oracle, step by step, on the
+full H2O toy workload and on scaled copies of the SnapKV and 70B-shaped
+workloads (several tiles per lane, ragged tails, mass eviction at step 1)."""
+import numpy as np
+import pytest
+import torch
+
+from tests.gpu_helpers import (assert_rows_close, compare_states, gpu_state, make_pair, near_tie,
+                               oracle_state, prefill_both, victim_lists)
+from workloads import Workload, scaled, shape
+
+pytestmark = pytest.mark.gpu
+
+
+def run_decode(shp, steps, layers=(0,), check_state_every=1, null_steps=()):
+    wl = Workload(shp)
+    eng, orc = make_pair(shp, layers=list(layers))
+    for layer in layers:
+        prefill_both(eng, orc, wl, layer)
+        compare_states(gpu_state(eng, layer), oracle_state(orc, layer), shp.policy, "prefill")
+    for t in range(steps):
+        for layer in layers:
+            q, kn, vn, pos = wl.step(layer, t)
+            null = t in null_steps
+            qg = None if null else q.cuda()
+            out, lse, vic, nv = eng.decode_step(layer, qg, kn.cuda(), vn.cuda(), pos)
+            ref = orc.decode_step(layer, None if null else q.double().numpy(), kn.double().numpy(),
+                                  vn.double().numpy(), pos)
+            torch.cuda.synchronize()
+            if not null:
+                assert_rows_close(out.cpu().numpy(), ref["out"], "step %d out" % t)
+                assert_rows_close(lse.cpu().numpy()[..., None], ref["lse"][..., None], "step %d lse" % t)
+            got = victim_lists(nv, vic)
+            for l in range(eng.lanes):
+                if not np.array_equal(got[l], ref["victims"][l]):
+                    assert near_tie(ref["keys"][l], ref["pos"][l], got[l], ref["victims"][l]), \
+                        "step %d lane %d victims differ beyond a tie" % (t, l)
+                    pytest.fail("step %d lane %d: near-tie swap (trajectories would diverge)" % (t, l))
+            if t % check_state_every == 0 or t == steps - 1:
+                compare_states(gpu_state(eng, layer), oracle_state(orc, layer), shp.policy,
+                               "step %d layer %d" % (t, layer))
+    code, msg = eng.last_error()
+    assert code == 0, msg
+    return eng, orc
+
+
+def test_h2o_toy_full():
+    """The H2O toy workload as specified: fp32, d=64, 512 + 32 steps, budget 128."""
+    run_decode(shape("h2o_toy"), 32)
+
+
+def test_snapkv_scaled():
+    shp = scaled("snapkv_decode", batch=2, num_kv_heads=4, num_q_heads=16, ctx=700, steps=12,
+                 budget=200, recent_window=40, obs_window=8, pool_kernel=5)
+    run_decode(shp, 12)
+
+
+def test_snapkv_window_and_pool_as_specified_short_context():
+    """obsWindow 32 and poolKernel 7 as in the SnapKV workload, on a short prompt."""
+    shp = scaled("snapkv_decode", batch=1, ctx=1500, steps=40, budget=1024, recent_window=256)
+    run_decode(shp, 40, check_state_every=8)
+
+
+def test_h2o_group8_scaled():
+    shp = scaled("h2o_70b", num_layers=2, batch=2, num_kv_heads=2, num_q_heads=16, ctx=1000, steps=6,
+                 budget=200, recent_window=100)
+    run_decode(shp, 6, layers=(0, 1))
+
+
+def test_h2o_group8_below_budget_growth():
+    """Lanes below the budget grow: admissions append, fill the tail block,
+    then take new blocks; no eviction happens until the budget is reached."""
+    shp = scaled("h2o_70b", num_layers=1, batch=1, num_kv_heads=3, num_q_heads=24, ctx=100, steps=40,
+                 budget=120, recent_window=30)
+    run_decode(shp, 40)
+
+
+def test_null_query_is_inert():
+    shp = scaled("snapkv_decode", batch=1, num_kv_heads=2, num_q_heads=8, ctx=300, steps=6,
+                 budget=200, recent_window=20, obs_window=4, pool_kernel=3)
+    run_decode(shp, 6, null_steps=(1, 4))
+    shp = scaled("h2o_70b", num_layers=1, batch=1, num_kv_heads=2, num_q_heads=16, ctx=300, steps=4,
+                 budget=200, recent_window=20)
+    run_decode(shp, 4, null_steps=(0, 2))

@@ -14,7 +14,7 @@ Workloads (shapes from the task's five configs; the constructions marked
 2. snapkv_decode: B=4, Hq=32, Hkv=8, d=128, bf16, context 4096; K ~ N(0,1);
    per (b, kvh) a direction u = q*/|q*| with q* ~ N(0,I) (chosen); 40
    non-overlapping runs of U{8..32} tokens at uniform starts (redrawn on
-   overlap) get k += 3u; decode queries q_h = q* + N(0,I) (chosen) so a run
+   overlap; scaled copies plant 40 * ctx / 4096 runs) get k += 3u; decode queries q_h = q* + N(0,I) (chosen) so a run
    token's logit is lifted by about 3; V ~ N(0,1); obsWindow 32,
    poolKernel 7, recentWindow 256, budget 1024, 256 steps.
 3. dropkv_prefill: B=1, Hq=32, Hkv=8, d=128, bf16, context 32768; q/K/V ~
@@ -159,14 +159,18 @@ class Workload:
         return u, qstar
 
     def _runs(self, layer):
-        """40 non-overlapping runs per (b, kvh): list of (start, length)."""
+        """Non-overlapping planted runs per (b, kvh): 40 at context 4096,
+        scaled with the context for shorter prompts; list of (start, length)."""
         s = self.s
+        n_runs = max(1, round(40 * s.ctx / 4096))
         g = self._gen("runs", layer)
         out = []
         for _ in range(s.lanes):
             taken = torch.zeros(s.ctx, dtype=torch.bool)
             runs = []
-            while len(runs) < 40:
+            tries = 0
+            while len(runs) < n_runs and tries < 100000:
+                tries += 1
                 ln = int(torch.randint(8, 33, (1,), generator=g))
                 st = int(torch.randint(0, s.ctx - ln + 1, (1,), generator=g))
                 if taken[st:st + ln].any():
