@@ -1,0 +1,433 @@
+#!/usr/bin/env python
+"""Benchmark of the per-decode-step KV-cache eviction engine.
+
+One step = one decode step of every layer of the 70B-shaped H2O workload
+(80 layers, 16 sequences x 8 KV heads, group 8, d=128, bf16, 16384-token
+prompts = 86 GB of K/V, budget 3276 = 1638 heavy + 1638 recent): split-K
+attention + score epilogue, bottom-k selection, eviction, admission and
+gated relocation, through the C ABI.  The prompt is prefilled and the first
+(mass-eviction) decode step runs inside the warm-up; the timed steps are the
+steady state.  Every layer call streams ~215 MB of K/V, more than the 129 MB
+L2, so no L2 flush is needed between steps.
+
+Metric: KV bytes scored + evicted per step (K/V rows read by the attention,
+the H2O score read-modify-write, 1 KB per relocated token) / step time, in
+GB/s, as in the task's metric; tokens scored per second alongside.
+"""
+import argparse
+import contextlib
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "KV GB/s scored+evicted per decode step (frac. of HBM peak); tokens scored/s"
+UNIT = "GB/s"
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=48)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--workload", default="h2o_70b")
+    ap.add_argument("--e2e-steps", type=int, default=8)
+    ap.add_argument("--cpu-lanes", type=int, default=32)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# clocks
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        self.p = None
+
+    def start(self):
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + self.FIELDS,
+                                       "--format=csv,noheader,nounits", "-lms", "100"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+        time.sleep(0.3)
+
+    def stop(self):
+        if self.p is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"], "samples": 0}
+        time.sleep(0.25)
+        self.p.terminate()
+        self.p.wait()
+        rows = [r.split(",") for r in open(self.f.name).read().strip().splitlines() if r.strip()]
+        os.unlink(self.f.name)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for r in rows:
+            try:
+                sm.append(float(r[2]))
+                smax.append(float(r[3]))
+                for nm, v in zip(names, r[6:10]):
+                    if v.strip().lower() == "active":
+                        reasons.add(nm)
+            except (ValueError, IndexError):
+                continue
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# oracle baseline (CPU) on a bounded sample of lanes
+# ---------------------------------------------------------------------------
+def _oracle_lane_job(job):
+    import types
+    import numpy as np
+    from oracle.engine import Engine as Oracle
+    K, V, steps, f = job
+    cfg = types.SimpleNamespace(policy=f["policy"], num_layers=1, batch=1, num_q_heads=f["g"], num_kv_heads=1,
+                                head_dim=f["d"], blocks_per_pool=f["blocks"], budget=f["budget"],
+                                recent_window=f["R"], obs_window=f["W"], pool_kernel=f["pk"],
+                                theta_f=f["theta"])
+    o = Oracle(cfg)
+    o.prefill(0, K[None, None].astype(np.float64), V[None, None].astype(np.float64))
+    q, kn, vn, pos = steps[0]
+    o.decode_step(0, q[None].astype(np.float64), kn[None, None].astype(np.float64),
+                  vn[None, None].astype(np.float64), pos)         # mass eviction: warm-up
+    t0 = time.perf_counter()
+    nbytes = tokens = 0
+    for q, kn, vn, pos in steps[1:]:
+        n = o.layers[0].lanes[0].pos.size
+        r = o.decode_step(0, q[None].astype(np.float64), kn[None, None].astype(np.float64),
+                          vn[None, None].astype(np.float64), pos)
+        tokens += n + 1
+        nbytes += (n + 1) * 2 * f["d"] * 2 + n * 8 + len(r["moves"]) * 4 * f["d"] * 2
+    return time.perf_counter() - t0, nbytes, tokens
+
+
+def oracle_baseline(lane_inputs, f, workers):
+    """Times the oracle's steady-state decode steps on the sampled lanes in a
+    spawn pool of single-threaded workers; returns (GB/s, tokens/s, seconds)."""
+    import multiprocessing as mp
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    jobs = [(K, V, steps, f) for K, V, steps in lane_inputs]
+    t0 = time.perf_counter()
+    with mp.get_context("spawn").Pool(workers) as pool:
+        res = pool.map(_oracle_lane_job, jobs)
+    wall = time.perf_counter() - t0
+    busy = sum(r[0] for r in res)
+    nbytes = sum(r[1] for r in res)
+    tokens = sum(r[2] for r in res)
+    # per-core throughput x cores used (the workers run concurrently)
+    gbs = nbytes / busy * workers / 1e9
+    return gbs, tokens / busy * workers, busy, wall
+
+
+def lane_sample_inputs(wl, shp, n_lanes, n_steps, device):
+    """Context and step inputs of the first n_lanes lanes of layer 0, as
+    float32 numpy arrays (bf16 values are exact in float32)."""
+    import torch
+    K, V = wl.context(0, device=device)
+    g = shp.group
+    out = []
+    steps_all = [wl.step(0, t, device=device) for t in range(n_steps)]
+    for lane in range(n_lanes):
+        b, h = divmod(lane, shp.num_kv_heads)
+        steps = [(q[b, h * g:(h + 1) * g].float().cpu().numpy(), kn[b, h].float().cpu().numpy(),
+                  vn[b, h].float().cpu().numpy(), pos) for q, kn, vn, pos in steps_all]
+        out.append((K[b, h].float().cpu().numpy(), V[b, h].float().cpu().numpy(), steps))
+    del K, V
+    if device != "cpu":
+        torch.cuda.empty_cache()
+    return out
+
+
+def oracle_fields(shp):
+    per_lane = -(-shp.max_tokens // 16) + -(-shp.budget // 16) + 2
+    return dict(policy=shp.policy, g=shp.group, d=shp.head_dim, blocks=per_lane, budget=shp.budget,
+                R=shp.recent_window, W=shp.obs_window, pk=shp.pool_kernel, theta=float(shp.theta_f))
+
+
+# ---------------------------------------------------------------------------
+# measured peaks and committed counters
+# ---------------------------------------------------------------------------
+def hbm_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            return float(json.load(open(p))["hbm_gbs"]), "measured"
+        except (KeyError, ValueError):
+            pass
+    return 6800.0, "fallback"
+
+
+def committed_traffic():
+    """DRAM bytes per launch of the decode attention kernel from the
+    committed ncu summary, if it was taken on the current kernel source."""
+    p = os.path.join(ROOT, "profiles", "d1_attend_h2o70b.json")
+    src = os.path.join(ROOT, "kv_cache_token_gb300", "csrc", "attend.cu")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+        h = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        if d.get("attend_cu_sha256_16") != h:
+            return None
+        return d.get("dram_bytes_per_launch_full_size")
+    except (ValueError, OSError):
+        return None
+
+
+# ---------------------------------------------------------------------------
+# GPU arm
+# ---------------------------------------------------------------------------
+def run_gpu(args):
+    import numpy as np
+    import torch
+    import torch.distributed as dist
+    import __graft_entry__
+    __graft_entry__.build()
+    from kv_cache_token_gb300 import Engine, config_from
+    from workloads import Workload, shape
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    if world > 1:
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    shp = shape(args.workload)
+    assert shp.kind == "decode"
+    assert args.warmup >= 1 and args.warmup + args.steps + args.e2e_steps <= shp.steps, "the workload has %d decode steps" % shp.steps
+    wl = Workload(shp)
+    eng = Engine(config_from(shp))
+    eng.reset()
+    cpu_lanes = None
+    t_setup = time.time()
+    for layer in range(shp.num_layers):
+        if layer == 0 and rank == 0 and not args.no_cpu_baseline:
+            cpu_lanes = lane_sample_inputs(wl, shp, args.cpu_lanes, args.warmup + args.steps, "cuda")
+        K, V = wl.context(layer, device="cuda")
+        eng.prefill(layer, K, V)
+        del K, V
+    torch.cuda.synchronize()
+    code, msg = eng.last_error()
+    assert code == 0, msg
+    total_steps = args.warmup + args.steps + args.e2e_steps
+    inputs = [[wl.step(layer, t, device="cuda")[:3] for layer in range(shp.num_layers)]
+              for t in range(args.warmup + args.steps)]
+    L, B, Hq, d = shp.num_layers, shp.batch, shp.num_q_heads, shp.head_dim
+    outs = [torch.empty((B, Hq, d), dtype=torch.float32, device="cuda") for _ in range(L)]
+    lses = [torch.empty((B, Hq), dtype=torch.float32, device="cuda") for _ in range(L)]
+    vics = [torch.empty((eng.lanes, shp.max_tokens), dtype=torch.int32, device="cuda") for _ in range(L)]
+    nvs = [torch.empty((eng.lanes,), dtype=torch.int32, device="cuda") for _ in range(L)]
+    stream = torch.cuda.current_stream()
+
+    def step(t, timed_events=None):
+        pos = shp.ctx + t
+        for layer in range(L):
+            q, kn, vn = inputs[t][layer]
+            if timed_events is not None:
+                timed_events[layer][0].record(stream)
+            eng.attend(layer, q, kn, vn)
+            if timed_events is not None:
+                timed_events[layer][1].record(stream)
+            eng.finish_step(layer, q, kn, vn, pos, outs[layer], lses[layer], vics[layer], nvs[layer])
+
+    for t in range(args.warmup):
+        step(t)
+    torch.cuda.synchronize()
+    code, msg = eng.last_error()
+    assert code == 0, msg
+    counts_before = eng.counts.sum(dim=1).cpu().numpy().astype(np.int64)          # per layer
+    stats_before = eng.stats_buf.sum(dim=0).cpu().numpy()
+    setup_s = time.time() - t_setup
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
+           for _ in range(args.steps)]
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for i in range(args.steps):
+        step(args.warmup + i, evs[i])
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    clocks = sampler.stop()
+    elapsed_ms = e0.elapsed_time(e1)
+    code, msg = eng.last_error()
+    assert code == 0, msg
+    counts_after = eng.counts.sum(dim=1).cpu().numpy().astype(np.int64)
+    stats_after = eng.stats_buf.sum(dim=0).cpu().numpy()
+    assert np.array_equal(counts_before, counts_after), "timed steps are not in steady state"
+    lanes = eng.lanes
+    attended = int((counts_before + lanes).sum()) * args.steps             # kept + new, every layer
+    kv_bytes = attended * 2 * d * 2
+    score_bytes = int(counts_before.sum()) * 8 * args.steps
+    moved = int(stats_after[5] - stats_before[5])
+    move_bytes = moved * 4 * d * 2
+    step_bytes = (kv_bytes + score_bytes + move_bytes) / args.steps
+    ms_per_step = elapsed_ms / args.steps
+    # dominant kernel: the split-K attention, timed by events around each launch
+    d1 = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(args.steps) for l in range(L)]
+    d1_ms = statistics.mean(d1)
+    d1_bytes = int((counts_before + lanes).mean()) * 2 * d * 2   # K/V rows per launch (one layer)
+    peak, peak_kind = hbm_peak()
+    d1_gbs = d1_bytes / (d1_ms * 1e-3) / 1e9
+
+    # end to end through the public call, host buffers, copies in the timed region
+    e2e = None
+    if args.e2e_steps > 0:
+        base = args.warmup + args.steps
+        host_in = [[tuple(x.cpu().pin_memory() for x in wl.step(layer, base + t)[:3]) for layer in range(L)]
+                   for t in range(args.e2e_steps)]
+        dev_in = [tuple(torch.empty_like(x, device="cuda") for x in host_in[0][0]) for _ in range(L)]
+        kread = 16
+        host_out = [(torch.empty((B, Hq, d), dtype=torch.float32).pin_memory(),
+                     torch.empty((B, Hq), dtype=torch.float32).pin_memory(),
+                     torch.empty((lanes,), dtype=torch.int32).pin_memory(),
+                     torch.empty((lanes, kread), dtype=torch.int32).pin_memory()) for _ in range(L)]
+        h2d = sum(x.numel() * x.element_size() for x in host_in[0][0]) * L
+        d2h = sum(x.numel() * x.element_size() for x in host_out[0]) * L
+        ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier()
+        torch.cuda.synchronize()
+        ea.record(stream)
+        for t in range(args.e2e_steps):
+            pos = shp.ctx + base + t
+            for layer in range(L):
+                for dst, src in zip(dev_in[layer], host_in[t][layer]):
+                    dst.copy_(src, non_blocking=True)
+                q, kn, vn = dev_in[layer]
+                eng.decode_step(layer, q, kn, vn, pos, outs[layer], lses[layer], vics[layer], nvs[layer])
+                ho = host_out[layer]
+                ho[0].copy_(outs[layer], non_blocking=True)
+                ho[1].copy_(lses[layer], non_blocking=True)
+                ho[2].copy_(nvs[layer], non_blocking=True)
+                ho[3].copy_(vics[layer][:, :kread], non_blocking=True)
+        eb.record(stream)
+        torch.cuda.synchronize()
+        barrier()
+        e2e_ms = ea.elapsed_time(eb) / args.e2e_steps
+        counts_e2e = eng.counts.sum(dim=1).cpu().numpy().astype(np.int64)
+        e2e_bytes = (int((counts_e2e + lanes).sum()) * 2 * d * 2 + int(counts_e2e.sum()) * 8)
+        e2e = {"value": round(e2e_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h), "ms_per_step": round(e2e_ms, 4)}
+        code, msg = eng.last_error()
+        assert code == 0, msg
+
+    # aggregate over ranks: units processed by all / max time
+    value = step_bytes / (ms_per_step * 1e-3) / 1e9
+    tokens_s = attended / args.steps / (ms_per_step * 1e-3)
+    if world > 1:
+        t = torch.tensor([ms_per_step, step_bytes, attended / args.steps], dtype=torch.float64, device="cuda")
+        mx = t.clone()
+        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+        sm = t.clone()
+        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+        ms_per_step = float(mx[0])
+        value = float(sm[1]) / (ms_per_step * 1e-3) / 1e9
+        tokens_s = float(sm[2]) / (ms_per_step * 1e-3)
+
+    cpu = None
+    if rank == 0 and cpu_lanes is not None:
+        workers = max(1, min(len(cpu_lanes), os.cpu_count() or 1, 16))
+        gbs, tps, busy, wall = oracle_baseline(cpu_lanes, oracle_fields(shp), workers)
+        cpu = {"value": round(gbs, 4), "unit": UNIT, "cores": workers, "kind": "oracle",
+               "tokens_scored_per_s": round(tps, 1),
+               "sample": "%d lanes of layer 0 x %d steady-state decode steps (after the mass-eviction step), "
+                         "numpy float64 oracle, %d single-threaded processes, %.1f s of CPU work"
+                         % (len(cpu_lanes), args.warmup + args.steps - 1, workers, busy)}
+
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "tokens_scored_per_s": round(tokens_s, 1),
+        "config": {"workload": "h2o_70b: 80 layers, batch 16, 64 q / 8 KV heads, d 128, bf16, context 16384 "
+                               "(86 GB K/V), H2O budget 3276 (1638 recent), steady-state decode steps",
+                   "global_batch": B * world, "seq_len": shp.ctx, "parallelism": "replica per GPU" if world > 1 else "1 GPU",
+                   "l2": "no flush: every layer call streams ~215 MB of K/V, above the 129 MB L2",
+                   "bytes_per_step": int(step_bytes), "moved_tokens_timed": moved,
+                   "setup_s": round(setup_s, 1)},
+        "roofline": {"bound": "hbm", "kernel": "attend_bf16_kernel (split-K decode attention)",
+                     "achieved": round(d1_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": round(d1_gbs / peak, 4), "traffic": committed_traffic(),
+                     "algorithmic_bytes_per_launch": d1_bytes, "avg_launch_ms": round(d1_ms, 5)},
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "clocks": clocks,
+        "gpu_launches": 4 * L * args.steps,
+    }
+    if rank == 0:
+        print(json.dumps(line))
+    if world > 1:
+        dist.destroy_process_group()
+
+
+# ---------------------------------------------------------------------------
+# reference arm: the oracle on host cores
+# ---------------------------------------------------------------------------
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    from workloads import Workload, shape
+    shp = shape(args.workload)
+    wl = Workload(shp)
+    lanes = max(1, args.cpu_lanes)
+    steps = min(args.warmup + args.steps, shp.steps)
+    t0 = time.time()
+    inputs = lane_sample_inputs(wl, shp, lanes, steps, "cpu")
+    workers = max(1, min(lanes, os.cpu_count() or 1, 16))
+    gbs, tps, busy, wall = oracle_baseline(inputs, oracle_fields(shp), workers)
+    bytes_per_step = None
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic", "tokens_scored_per_s": round(tps, 1),
+        "config": {"workload": "h2o_70b: 80 layers, batch 16, 64 q / 8 KV heads, d 128, bf16, context 16384 "
+                               "(86 GB K/V), H2O budget 3276 (1638 recent), steady-state decode steps",
+                   "seq_len": shp.ctx, "bytes_per_step": bytes_per_step},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": UNIT, "cores": workers, "kind": "oracle",
+                         "sample": "%d lanes of layer 0 x %d steady-state decode steps, numpy float64 oracle, "
+                                   "%d single-threaded processes (%.1f s CPU, %.1f s total)"
+                                   % (lanes, steps - 1, workers, busy, time.time() - t0)},
+        "e2e": {"value": round(gbs, 4), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_gpu(args)
+
+
+if __name__ == "__main__":
+    main()

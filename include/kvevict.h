@@ -204,6 +204,19 @@ kvevict_status kvevict_decode_step(kvevict_ctx* ctx, int layer, const void* q, c
                                    const void* v_new, int32_t new_pos, float* out, float* lse,
                                    int32_t* victims, int32_t* n_victims, void* stream);
 
+/* The two halves of kvevict_decode_step, for callers that schedule or time
+ * them separately: decode_step(...) == attend(...) then finish_step(...) on
+ * the same stream with the same arguments.  kvevict_attend runs the split-K
+ * attention kernel only (it writes library scratch, no engine state, so it
+ * may be repeated); kvevict_finish_step runs the rest of the step (combine,
+ * scores, keys, select, evict, admit, reclaim).  With q == NULL, attend does
+ * nothing and finish_step is the inert step described above. */
+kvevict_status kvevict_attend(kvevict_ctx* ctx, int layer, const void* q, const void* k_new,
+                              const void* v_new, void* stream);
+kvevict_status kvevict_finish_step(kvevict_ctx* ctx, int layer, const void* q, const void* k_new,
+                                   const void* v_new, int32_t new_pos, float* out, float* lse,
+                                   int32_t* victims, int32_t* n_victims, void* stream);
+
 /* DropKV prefill-window scoring of one layer (DropKV explainer: Lemma 1 and
  * the fused scoring paragraph).  q_win [B][Hq][w][d] (kv_dtype, device) are
  * the last w prompt queries at positions q_pos[w] (int32, device); every

@@ -67,12 +67,15 @@ def lib():
         L.kvevict_reset.argtypes = [V, V]
         L.kvevict_prefill.argtypes = [V, ctypes.c_int, V, V, I, V]
         L.kvevict_decode_step.argtypes = [V, ctypes.c_int, V, V, V, I, V, V, V, V, V]
+        L.kvevict_attend.argtypes = [V, ctypes.c_int, V, V, V, V]
+        L.kvevict_finish_step.argtypes = [V, ctypes.c_int, V, V, V, I, V, V, V, V, V]
         L.kvevict_score.argtypes = [V, ctypes.c_int, V, I, V, V, V, V, V]
         L.kvevict_select.argtypes = [V, V, I, V, V, I, I, I, I, V, V, V]
         L.kvevict_compact.argtypes = [V, ctypes.c_int, V, V, V, V, V, V, V]
         L.kvevict_stats.argtypes = [V, ctypes.c_int, V, V]
         L.kvevict_last_error.argtypes = [V, ctypes.c_char_p, ctypes.c_size_t]
-        for f in ("validate", "create", "reset", "prefill", "decode_step", "score", "select",
+        for f in ("validate", "create", "reset", "prefill", "decode_step", "attend", "finish_step",
+                  "score", "select",
                   "compact", "stats", "last_error"):
             getattr(L, "kvevict_" + f).restype = ctypes.c_int
         _LIB = L
@@ -199,6 +202,24 @@ class Engine:
         _check(lib().kvevict_decode_step(self.h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), int(new_pos),
                                          _ptr(out), _ptr(lse), _ptr(victims), _ptr(n_victims),
                                          _stream(stream)), "kvevict_decode_step")
+        return out, lse, victims, n_victims
+
+    def attend(self, layer, q, k_new, v_new, stream=None):
+        _check(lib().kvevict_attend(self.h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _stream(stream)),
+               "kvevict_attend")
+
+    def finish_step(self, layer, q, k_new, v_new, new_pos, out=None, lse=None, victims=None, n_victims=None,
+                    stream=None):
+        c = self.cfg
+        if q is not None and out is None:
+            out = torch.empty((c.batch, c.num_q_heads, c.head_dim), dtype=torch.float32, device=self.device)
+        if q is not None and lse is None:
+            lse = torch.empty((c.batch, c.num_q_heads), dtype=torch.float32, device=self.device)
+        victims = self.victims if victims is None else victims
+        n_victims = self.n_victims if n_victims is None else n_victims
+        _check(lib().kvevict_finish_step(self.h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), int(new_pos),
+                                         _ptr(out), _ptr(lse), _ptr(victims), _ptr(n_victims),
+                                         _stream(stream)), "kvevict_finish_step")
         return out, lse, victims, n_victims
 
     def score(self, layer, q_win, q_pos, lse=None, a_out=None, scores=None, stream=None):

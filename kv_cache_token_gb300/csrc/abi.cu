@@ -222,6 +222,10 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   ctx->c.sm_count = sms;
   ctx->c.device = dev;
   ctx->c.ws_bytes = kve::workspace_layout(*cfg, &ctx->c.ws, static_cast<char*>(bufs->workspace));
+  if (kve::prepare_kernels(ctx->c) != cudaSuccess) {
+    delete ctx;
+    return KVEVICT_E_CUDA;
+  }
   *out = ctx;
   return KVEVICT_OK;
 }
@@ -251,6 +255,28 @@ kvevict_status kvevict_decode_step(kvevict_ctx* ctx, int layer, const void* q, c
   if (ctx->c.dims.policy == KVEVICT_DROPKV) return KVEVICT_E_INVALID_ARG;
   return cuda_status(kve::launch_decode(ctx->c, layer, q, k_new, v_new, new_pos, out, lse, victims, n_victims,
                                         static_cast<cudaStream_t>(stream)));
+}
+
+kvevict_status kvevict_attend(kvevict_ctx* ctx, int layer, const void* q, const void* k_new, const void* v_new,
+                              void* stream) {
+  if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !k_new || !v_new) return KVEVICT_E_INVALID_ARG;
+  if (ctx->c.dims.policy == KVEVICT_DROPKV) return KVEVICT_E_INVALID_ARG;
+  if (!q) return KVEVICT_OK;
+  return cuda_status(kve::launch_attend(ctx->c, layer, q, k_new, v_new, static_cast<cudaStream_t>(stream)));
+}
+
+kvevict_status kvevict_finish_step(kvevict_ctx* ctx, int layer, const void* q, const void* k_new, const void* v_new,
+                                   int32_t new_pos, float* out, float* lse, int32_t* victims, int32_t* n_victims,
+                                   void* stream) {
+  if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !k_new || !v_new || !victims || !n_victims || new_pos < 0)
+    return KVEVICT_E_INVALID_ARG;
+  if (q && (!out || !lse)) return KVEVICT_E_INVALID_ARG;
+  if (ctx->c.dims.policy == KVEVICT_DROPKV) return KVEVICT_E_INVALID_ARG;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  cudaError_t e = kve::launch_epilogue(ctx->c, layer, q != nullptr, new_pos, k_new, v_new, out, lse, victims,
+                                       n_victims, st);
+  if (e == cudaSuccess) e = kve::launch_allocate_apply(ctx->c, layer, k_new, v_new, false, nullptr, st);
+  return cuda_status(e);
 }
 
 kvevict_status kvevict_score(kvevict_ctx* ctx, int layer, const void* q_win, int32_t w, const int32_t* q_pos,

@@ -477,6 +477,16 @@ __global__ void __launch_bounds__(kF32Chunk) attend_f32_kernel(AttendArgs a, int
 
 }  // namespace
 
+cudaError_t prepare_kernels(const Ctx& ctx) {
+  (void)ctx;
+  cudaError_t e = cudaFuncSetAttribute(attend_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Bf16Cfg<128>::kSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attend_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Bf16Cfg<64>::kSmem);
+  return e;
+}
+
 cudaError_t launch_attend(const Ctx& ctx, int layer, const void* q, const void* k_new, const void* v_new,
                           cudaStream_t stream) {
   const Dims& dm = ctx.dims;
@@ -492,17 +502,10 @@ cudaError_t launch_attend(const Ctx& ctx, int layer, const void* q, const void* 
   if (dm.dtype == KVEVICT_BF16) {
     if (dm.lanes > kMaxLanesSmem) return cudaErrorInvalidValue;
     const int grid = ctx.sm_count * 2;
-    if (dm.d == 128) {
-      auto k = attend_bf16_kernel<128>;
-      const int sm = Bf16Cfg<128>::kSmem;
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-      k<<<grid, kAttendWarps * 32, sm, stream>>>(a);
-    } else {
-      auto k = attend_bf16_kernel<64>;
-      const int sm = Bf16Cfg<64>::kSmem;
-      cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, sm);
-      k<<<grid, kAttendWarps * 32, sm, stream>>>(a);
-    }
+    if (dm.d == 128)
+      attend_bf16_kernel<128><<<grid, kAttendWarps * 32, Bf16Cfg<128>::kSmem, stream>>>(a);
+    else
+      attend_bf16_kernel<64><<<grid, kAttendWarps * 32, Bf16Cfg<64>::kSmem, stream>>>(a);
   } else {
     const int chunks = (dm.cap + kF32Chunk) / kF32Chunk;   // enough for n = cap - 1 plus the new token
     if (chunks > kMaxSeg) return cudaErrorInvalidValue;

@@ -322,6 +322,26 @@ __global__ void __launch_bounds__(256) d3_combine_kernel(D3Args A) {
   }
 }
 
+// One (row, key) term of the DropKV score: p / (1 - p) * ||a - v||, with
+// x = log2 p.  ||a - v||^2 comes from the expansion r2 = |a|^2 + |v|^2 - 2<a,v>
+// except where p > 1/2: there a is within (1 - p) of v and the expansion
+// cancels, so the distance is taken directly from the fp32 a and the staged v
+// row (at most one key per row can have p > 1/2).  1 - p uses expm1 near 1.
+__device__ __forceinline__ float residual_term(float x, float r2, const float* arow, const unsigned char* vrow) {
+  const float p = exp2f(x);
+  if (!(p > 0.f)) return 0.f;
+  if (p <= 0.5f) return p / (1.f - p) * sqrtf(fmaxf(0.f, r2));
+  const float om = -expm1f(x * kLn2);
+  if (!(om > 0.f)) return INFINITY;
+  const __nv_bfloat16* v = reinterpret_cast<const __nv_bfloat16*>(vrow);
+  float acc = 0.f;
+  for (int e = 0; e < kD; ++e) {
+    const float df = arow[e] - __bfloat162float(v[e]);
+    acc = fmaf(df, df, acc);
+  }
+  return p / om * sqrtf(acc);
+}
+
 // ---------------------------------------------------------------------------
 // pass 2
 // ---------------------------------------------------------------------------
@@ -350,6 +370,13 @@ __global__ void __launch_bounds__(kWarps * 32) d3_pass2_kernel(D3Args A) {
   const float ana = oka ? A.ws.d3_rowc[(wbase + ra) * 2 + 1] : 0.f;
   const float anb = okb ? A.ws.d3_rowc[(wbase + rb) * 2 + 1] : 0.f;
   float* out = A.ws.d3_score_part + (static_cast<size_t>(rg) * A.dm.lanes + l) * A.dm.cap;
+  auto arow_of = [&](int r, bool ok) -> const float* {
+    if (!ok) return A.a_out;
+    const int h = r / A.w, i = r % A.w;
+    return A.a_out + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i) * kD;
+  };
+  const float* arow_a = arow_of(ra, oka);
+  const float* arow_b = arow_of(rb, okb);
 
   const int ntiles = (j_end - j_begin + kKeyTile - 1) / kKeyTile;
   load_tile(tiles[0], A, l, n, j_begin);
@@ -389,23 +416,10 @@ __global__ void __launch_bounds__(kWarps * 32) d3_pass2_kernel(D3Args A) {
         const int kp = T.pos[key];
         const float vn = T.vn[key];
         float term = 0.f;
-        // row a
-        if (kp <= qpa) {
-          const float pr = exp2f(s[nt][e] * A.scale2 - lsa);
-          if (pr > 0.f) {
-            const float om = 1.f - pr;
-            const float r2 = fmaxf(0.f, ana + vn - 2.f * g[nt][e]);
-            term += om > 0.f ? pr / om * sqrtf(r2) : INFINITY;
-          }
-        }
-        if (kp <= qpb) {
-          const float pr = exp2f(s[nt][2 + e] * A.scale2 - lsb);
-          if (pr > 0.f) {
-            const float om = 1.f - pr;
-            const float r2 = fmaxf(0.f, anb + vn - 2.f * g[nt][2 + e]);
-            term += om > 0.f ? pr / om * sqrtf(r2) : INFINITY;
-          }
-        }
+        if (kp <= qpa) term += residual_term(s[nt][e] * A.scale2 - lsa, ana + vn - 2.f * g[nt][e], arow_a,
+                                             T.v + key * kRowStride);
+        if (kp <= qpb) term += residual_term(s[nt][2 + e] * A.scale2 - lsb, anb + vn - 2.f * g[nt][2 + e], arow_b,
+                                             T.v + key * kRowStride);
         // sum over the 8 row groups of the warp (lanes with equal cq)
         term += __shfl_xor_sync(0xffffffffu, term, 4);
         term += __shfl_xor_sync(0xffffffffu, term, 8);

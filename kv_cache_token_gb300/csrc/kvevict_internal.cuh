@@ -114,6 +114,7 @@ cudaError_t launch_compact(const Ctx&, int layer, const int32_t* victims, const 
 cudaError_t launch_score(const Ctx&, int layer, const void* q_win, int w, const int32_t* q_pos,
                          float* lse, float* a_out, float* scores, cudaStream_t);
 cudaError_t launch_stats(const Ctx&, int layer, long long* out, cudaStream_t);
+cudaError_t prepare_kernels(const Ctx&);   // one-time kernel attributes (not stream work)
 cudaError_t launch_attend(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
                           cudaStream_t);
 cudaError_t launch_epilogue(const Ctx&, int layer, bool has_q, int new_pos, const void* k_new,
