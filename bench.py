@@ -43,6 +43,8 @@ def parse():
     ap.add_argument("--e2e-steps", type=int, default=8)
     ap.add_argument("--cpu-lanes", type=int, default=32)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-layers", type=int, default=0,
+                    help="profiling only: run the workload with this many layers (not a bench number)")
     return ap.parse_args()
 
 
@@ -217,6 +219,9 @@ def run_gpu(args):
             dist.barrier()
 
     shp = shape(args.workload)
+    if args.profile_layers:
+        import dataclasses
+        shp = dataclasses.replace(shp, num_layers=args.profile_layers)
     assert shp.kind == "decode"
     assert args.warmup >= 1 and args.warmup + args.steps + args.e2e_steps <= shp.steps, "the workload has %d decode steps" % shp.steps
     wl = Workload(shp)
@@ -382,6 +387,8 @@ def run_gpu(args):
         "clocks": clocks,
         "gpu_launches": 4 * L * args.steps,
     }
+    if args.profile_layers:
+        line["profile_only"] = "%d layers: for profiling, not a bench number" % L
     if rank == 0:
         print(json.dumps(line))
     if world > 1:
