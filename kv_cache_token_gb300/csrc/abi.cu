@@ -72,6 +72,7 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base) {
   w.freed_flag = reinterpret_cast<int32_t*>(take(P * 4));
   w.blk_tag = reinterpret_cast<int32_t*>(take(P * 4));
   w.counters = reinterpret_cast<int32_t*>(take(64));
+  w.epi_done = reinterpret_cast<int32_t*>(take(4));
   if (dm.max_window > 0 && dm.dtype == KVEVICT_BF16 && dm.d == 128) {
     const size_t rows = static_cast<size_t>(d3_rows_max(dm));
     const size_t chunks = static_cast<size_t>(d3_chunks(dm, 0));
@@ -139,6 +140,7 @@ cudaError_t launch_reset(const Ctx& ctx, cudaStream_t st) {
   ms(w.freed_flag, 0, P * 4);
   ms(w.blk_tag, 0, P * 4);
   ms(w.counters, 0, 64);
+  ms(w.epi_done, 0, 4);
   return e;
 }
 
@@ -222,7 +224,7 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   ctx->c.sm_count = sms;
   ctx->c.device = dev;
   ctx->c.ws_bytes = kve::workspace_layout(*cfg, &ctx->c.ws, static_cast<char*>(bufs->workspace));
-  if (kve::prepare_kernels(ctx->c) != cudaSuccess) {
+  if (kve::prepare_kernels(ctx->c) != cudaSuccess || ctx->c.attend_ctas_per_sm < 1) {
     delete ctx;
     return KVEVICT_E_CUDA;
   }
@@ -275,7 +277,7 @@ kvevict_status kvevict_finish_step(kvevict_ctx* ctx, int layer, const void* q, c
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = kve::launch_epilogue(ctx->c, layer, q != nullptr, new_pos, k_new, v_new, out, lse, victims,
                                        n_victims, st);
-  if (e == cudaSuccess) e = kve::launch_allocate_apply(ctx->c, layer, k_new, v_new, false, nullptr, st);
+  if (e == cudaSuccess) e = kve::launch_allocate_apply(ctx->c, layer, k_new, v_new, false, nullptr, st, false);
   return cuda_status(e);
 }
 

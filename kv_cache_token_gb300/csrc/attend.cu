@@ -100,25 +100,45 @@ constexpr int kMaxLanesSmem = 1024;   // lanes per layer (validated at create)
 
 // ---------------------------------------------------------------------------
 // bf16 tensor-core kernel
+//
+// Per 16-token tile a warp computes S^T = K Q^T (M = 16 tokens, N = 8 query
+// heads of the group, K = d) and O^T += V^T P^T (M = 16 rows of d, N = 8
+// heads, K = 16 tokens), so a group of 8 heads fills the MMA with no padding.
+// P^T reaches the B operand through a shared-memory transpose (stmatrix.trans
+// then ldmatrix), as a hi + lo pair of bf16 values.
 // ---------------------------------------------------------------------------
-template <int D>
+constexpr int kAttStages = 2;      // copy stages per warp
+
+template <int D, int NT>
 struct Bf16Cfg {
   static constexpr int kRowBytes = D * 2;
   static constexpr int kRowStride = kRowBytes + 16;            // +16 B: conflict-free ldmatrix
   static constexpr int kStageBytes = 2 * 16 * kRowStride;      // K rows then V rows
-  static constexpr int kWarpBytes = kStages * kStageBytes;
+  static constexpr int kPBytes = NT * 2 * 8 * 32;              // [NT][hi, lo][8 heads][16 tokens] bf16
+  static constexpr int kWarpBytes = kAttStages * kStageBytes + kPBytes;
   static constexpr int kSmem = kAttendWarps * kWarpBytes;
-  static constexpr int kKs = D / 16;                           // k-steps over d
-  static constexpr int kDn = D / 8;                            // 8-wide output column tiles
+  static constexpr int kKs = D / 16;                           // k-steps over d (QK^T)
+  static constexpr int kDt = D / 16;                           // 16-row tiles of d (PV)
 };
 
-template <int D>
-__global__ void __launch_bounds__(kAttendWarps * 32, 2) attend_bf16_kernel(AttendArgs a) {
-  using C = Bf16Cfg<D>;
+__device__ __forceinline__ void stsm_x2_t(uint32_t addr, uint32_t r0, uint32_t r1) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x2.trans.shared.b16 [%0], {%1, %2};" ::"r"(addr), "r"(r0), "r"(r1)
+               : "memory");
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t& r0, uint32_t& r1) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0,%1}, [%2];" : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void mma_bf16a(float* c, const uint32_t* a, uint32_t b0, uint32_t b1) {
+  mma_bf16(c, a[0], a[1], a[2], a[3], b0, b1);
+}
+
+template <int D, int NT>
+__global__ void __launch_bounds__(kAttendWarps * 32, 3) attend_bf16_kernel(AttendArgs a) {
+  using C = Bf16Cfg<D, NT>;
   extern __shared__ __align__(128) unsigned char smem[];
   __shared__ int sh_prefix[kMaxLanesSmem + 1];
   __shared__ int sh_scan[40];
-  __shared__ uint64_t sh_bar[kAttendWarps][kStages];
+  __shared__ uint64_t sh_bar[kAttendWarps][kAttStages];
 
   const int tid = threadIdx.x, lane_id = tid & 31, warp = tid >> 5;
   const int lanes = a.lanes;
@@ -166,9 +186,10 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 2) attend_bf16_kernel(Atten
   if (t_begin >= t_end) return;
 
   unsigned char* wbuf = smem + warp * C::kWarpBytes;
+  unsigned char* pbuf = wbuf + kAttStages * C::kStageBytes;
   uint64_t* bars = sh_bar[warp];
   if (lane_id == 0) {
-    for (int s = 0; s < kStages; ++s) mbar_init(&bars[s], 1);
+    for (int s = 0; s < kAttStages; ++s) mbar_init(&bars[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncwarp();
@@ -178,107 +199,132 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 2) attend_bf16_kernel(Atten
   const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(a.v_pool);
   const __nv_bfloat16* kn = static_cast<const __nv_bfloat16*>(a.k_new);
   const __nv_bfloat16* vn = static_cast<const __nv_bfloat16*>(a.v_new);
-  const size_t pool_rows = static_cast<size_t>(a.P) * kBlock;
+  const int pool_rows = a.P * kBlock;
+  const int r = lane_id & 15;          // the row (token) this thread copies
+  const bool isv = lane_id >= 16;      // K row (lanes 0-15) or V row (16-31)
 
-  // find the lane of a tile (monotone walk)
-  auto lane_of = [&](int t, int hint) {
-    int l = hint;
-    while (sh_prefix[l + 1] <= t) ++l;
-    return l;
+  // --- producer: slot indices are fetched one issue ahead -----------------
+  int pf_lane = 0, pf_n = 0;
+  {
+    int l = 0;
+    while (sh_prefix[l + 1] <= t_begin) ++l;
+    pf_lane = l;
+    pf_n = min(max(a.count[l], 0), a.cap - 1);
+  }
+  int iss_lane = pf_lane, iss_n = pf_n;
+  auto fetch_slot = [&](int t) -> int {
+    if (t >= t_end) return -1;
+    while (sh_prefix[pf_lane + 1] <= t) {
+      ++pf_lane;
+      pf_n = min(max(a.count[pf_lane], 0), a.cap - 1);
+    }
+    const int i = (t - sh_prefix[pf_lane]) * 16 + r;
+    return i < pf_n ? a.slot[static_cast<size_t>(pf_lane) * a.cap + i] : -1;
   };
-
-  // --- producer: issue the copies of tile t into stage st ------------------
-  int issue_lane = lane_of(t_begin, 0);
-  auto issue = [&](int t, int st) {
-    issue_lane = lane_of(t, issue_lane);
-    const int l = issue_lane;
-    const int n = min(max(a.count[l], 0), a.cap - 1);
+  auto issue = [&](int t, int st, int slot) {
+    while (sh_prefix[iss_lane + 1] <= t) {
+      ++iss_lane;
+      iss_n = min(max(a.count[iss_lane], 0), a.cap - 1);
+    }
+    const int l = iss_lane, n = iss_n;
     const int i0 = (t - sh_prefix[l]) * 16;
     const int valid = min(16, n + 1 - i0);
     unsigned char* sbuf = wbuf + st * C::kStageBytes;
     fence_proxy_async();
-    if (lane_id == 0) mbar_arrive_expect_tx(&bars[st], (uint32_t)(valid * 2 * C::kRowBytes));
+    if (lane_id == 0) mbar_arrive_expect_tx(&bars[st], static_cast<uint32_t>(valid * 2 * C::kRowBytes));
     __syncwarp();
-    const int r = lane_id & 15;
-    const bool isv = lane_id >= 16;
     unsigned char* dst = sbuf + (isv ? 16 * C::kRowStride : 0) + r * C::kRowStride;
     const int i = i0 + r;
     if (r < valid) {
       const __nv_bfloat16* src;
       if (i < n) {
-        int s = a.slot[static_cast<size_t>(l) * a.cap + i];
-        if (s < 0 || static_cast<size_t>(s) >= pool_rows) { set_status(a.status, ST_BAD_INDEX); s = 0; }
+        int s = slot;
+        if (s < 0 || s >= pool_rows) { set_status(a.status, ST_BAD_INDEX); s = 0; }
         src = (isv ? vp : kp) + static_cast<size_t>(s) * D;
       } else {
         src = (isv ? vn : kn) + static_cast<size_t>(l) * D;
       }
       bulk_g2s(dst, src, C::kRowBytes, &bars[st], pol);
     } else {
-      uint4 z = make_uint4(0, 0, 0, 0);
+      const uint4 z = make_uint4(0, 0, 0, 0);
 #pragma unroll
       for (int o = 0; o < C::kRowBytes; o += 16) *reinterpret_cast<uint4*>(dst + o) = z;
     }
   };
 
   // --- consumer state -------------------------------------------------------
-  const int gq = lane_id >> 2, cq = lane_id & 3;   // MMA group / thread-in-group
-  const int h0 = gq, h1 = gq + 8;
-  const bool v0 = h0 < a.g, v1 = h1 < a.g;
-  uint32_t qa[C::kKs][4];
-  float o_acc[C::kDn][4];
-  float m0 = -INFINITY, m1 = -INFINITY, l0 = 0.f, l1 = 0.f;
+  const int gq = lane_id >> 2, cq = lane_id & 3;
+  uint32_t qb[NT][C::kKs][2];
+  float o_acc[NT][C::kDt][4];
+  float m_run[NT][2], l_run[NT][2];
   int cur_lane = -1, seg = 0, cur_n = 0;
 
   auto load_q = [&](int l) {
     const int b = l / a.Hkv, kh = l % a.Hkv;
-    const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q) +
-                              (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kh) * a.g) * D;
+    const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(a.q) +
+                                 (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kh) * a.g) * D;
 #pragma unroll
-    for (int ks = 0; ks < C::kKs; ++ks) {
-      const int c0 = ks * 16 + cq * 2;
-      qa[ks][0] = v0 ? *reinterpret_cast<const uint32_t*>(qb + h0 * D + c0) : 0u;
-      qa[ks][1] = v1 ? *reinterpret_cast<const uint32_t*>(qb + h1 * D + c0) : 0u;
-      qa[ks][2] = v0 ? *reinterpret_cast<const uint32_t*>(qb + h0 * D + c0 + 8) : 0u;
-      qa[ks][3] = v1 ? *reinterpret_cast<const uint32_t*>(qb + h1 * D + c0 + 8) : 0u;
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = nt * 8 + gq;
+      const bool ok = h < a.g;
+#pragma unroll
+      for (int ks = 0; ks < C::kKs; ++ks) {
+        const int c0 = ks * 16 + cq * 2;
+        qb[nt][ks][0] = ok ? *reinterpret_cast<const uint32_t*>(qbase + h * D + c0) : 0u;
+        qb[nt][ks][1] = ok ? *reinterpret_cast<const uint32_t*>(qbase + h * D + c0 + 8) : 0u;
+      }
+#pragma unroll
+      for (int dt = 0; dt < C::kDt; ++dt) o_acc[nt][dt][0] = o_acc[nt][dt][1] = o_acc[nt][dt][2] = o_acc[nt][dt][3] = 0.f;
+      m_run[nt][0] = m_run[nt][1] = -INFINITY;
+      l_run[nt][0] = l_run[nt][1] = 0.f;
     }
-#pragma unroll
-    for (int dn = 0; dn < C::kDn; ++dn) o_acc[dn][0] = o_acc[dn][1] = o_acc[dn][2] = o_acc[dn][3] = 0.f;
-    m0 = m1 = -INFINITY;
-    l0 = l1 = 0.f;
   };
 
   auto flush = [&]() {
-    float s0 = l0, s1 = l1;
-    s0 += __shfl_xor_sync(0xffffffffu, s0, 1);
-    s0 += __shfl_xor_sync(0xffffffffu, s0, 2);
-    s1 += __shfl_xor_sync(0xffffffffu, s1, 1);
-    s1 += __shfl_xor_sync(0xffffffffu, s1, 2);
     const size_t base = (static_cast<size_t>(cur_lane) * kMaxSeg + seg) * a.g;
-    if (v0) {
-      float* po = a.part_o + (base + h0) * D;
 #pragma unroll
-      for (int dn = 0; dn < C::kDn; ++dn)
-        *reinterpret_cast<float2*>(po + dn * 8 + cq * 2) = make_float2(o_acc[dn][0], o_acc[dn][1]);
-      if (cq == 0) *reinterpret_cast<float2*>(a.part_ml + (base + h0) * 2) = make_float2(m0, s0);
-    }
-    if (v1) {
-      float* po = a.part_o + (base + h1) * D;
+    for (int nt = 0; nt < NT; ++nt) {
 #pragma unroll
-      for (int dn = 0; dn < C::kDn; ++dn)
-        *reinterpret_cast<float2*>(po + dn * 8 + cq * 2) = make_float2(o_acc[dn][2], o_acc[dn][3]);
-      if (cq == 0) *reinterpret_cast<float2*>(a.part_ml + (base + h1) * 2) = make_float2(m1, s1);
+      for (int e = 0; e < 2; ++e) {
+        float s = l_run[nt][e];
+        s += __shfl_xor_sync(0xffffffffu, s, 4);
+        s += __shfl_xor_sync(0xffffffffu, s, 8);
+        s += __shfl_xor_sync(0xffffffffu, s, 16);
+        const int h = nt * 8 + cq * 2 + e;
+        if (h < a.g) {
+          float* po = a.part_o + (base + h) * D;
+#pragma unroll
+          for (int dt = 0; dt < C::kDt; ++dt) {
+            po[dt * 16 + gq] = o_acc[nt][dt][e];
+            po[dt * 16 + gq + 8] = o_acc[nt][dt][2 + e];
+          }
+          if (gq == 0) *reinterpret_cast<float2*>(a.part_ml + (base + h) * 2) = make_float2(m_run[nt][e], s);
+        }
+      }
     }
   };
 
   // --- pipeline ---------------------------------------------------------------
-  for (int s = 0; s < kStages - 1; ++s)
-    if (t_begin + s < t_end) issue(t_begin + s, s);
+  int next_slot = fetch_slot(t_begin);
+  issue(t_begin, 0, next_slot);
+  next_slot = fetch_slot(t_begin + 1);
 
-  int cons_lane = lane_of(t_begin, 0);
+  // smem lane addresses
+  const int ktok = (lane_id & 7) + (((lane_id >> 3) & 1) << 3);
+  const int kcol = (lane_id >> 4) * 16;                  // bytes
+  const int vtok = (lane_id & 7) + ((lane_id >> 4) << 3);
+  const int vcol = ((lane_id >> 3) & 1) * 16;            // bytes
+  const int prow = (lane_id & 7) * 32 + ((lane_id >> 3) & 1) * 16;   // stmatrix / ldmatrix.x2 rows
+
+  int cons_lane = 0;
+  while (sh_prefix[cons_lane + 1] <= t_begin) ++cons_lane;
   for (int t = t_begin, u = 0; t < t_end; ++t, ++u) {
-    if (t + kStages - 1 < t_end) issue(t + kStages - 1, (u + kStages - 1) % kStages);
-    const int st = u % kStages;
-    const uint32_t par = (u / kStages) & 1;
+    if (t + 1 < t_end) {
+      issue(t + 1, (u + 1) % kAttStages, next_slot);
+      next_slot = fetch_slot(t + 2);
+    }
+    const int st = u % kAttStages;
+    const uint32_t par = (u / kAttStages) & 1;
     {
       int spins = 0;
       while (!mbar_try_wait(&bars[st], par)) {
@@ -287,7 +333,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 2) attend_bf16_kernel(Atten
     }
     __syncwarp();
 
-    cons_lane = lane_of(t, cons_lane);
+    while (sh_prefix[cons_lane + 1] <= t) ++cons_lane;
     if (cons_lane != cur_lane) {
       if (cur_lane >= 0) flush();
       cur_lane = cons_lane;
@@ -299,87 +345,92 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 2) attend_bf16_kernel(Atten
     const unsigned char* kb = wbuf + st * C::kStageBytes;
     const unsigned char* vb = kb + 16 * C::kRowStride;
 
-    // S = Q K^T for 16 tokens (two 8-token column tiles)
-    float sacc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    // S^T = K Q^T : two accumulators per head tile (even / odd k-steps)
+    float sa[NT][4], sb[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
     {
-      const int tok = (lane_id & 7) + ((lane_id >> 4) << 3);
-      const int colb = ((lane_id >> 3) & 1) * 16;   // bytes
-      const uint32_t rowaddr = smem_u32(kb + tok * C::kRowStride + colb);
+      const uint32_t addr = smem_u32(kb + ktok * C::kRowStride + kcol);
 #pragma unroll
       for (int ks = 0; ks < C::kKs; ++ks) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4(rowaddr + ks * 32, b0, b1, b2, b3);
-        mma_bf16(sacc[0], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-        mma_bf16(sacc[1], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b2, b3);
+        uint32_t af[4];
+        ldsm_x4(addr + ks * 32, af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) mma_bf16a((ks & 1) ? sb[nt] : sa[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
       }
     }
-    // scale, mask, store logits, online softmax
-    float p[2][4];
-    float tmax0 = -INFINITY, tmax1 = -INFINITY;
+    const bool ok0 = i0 + gq <= cur_n, ok1 = i0 + gq + 8 <= cur_n;
+    uint32_t ph[NT][2], pl[NT][2];
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+    for (int nt = 0; nt < NT; ++nt) {
+      float sv[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const bool ok = (e < 2) ? ok0 : ok1;
+        sv[e] = ok ? (sa[nt][e] + sb[nt][e]) * a.scale2 : -INFINITY;
+      }
+      // logits of the valid heads: [lane][head][token]
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int i = i0 + nt * 8 + cq * 2 + e;
-        const bool ok = i <= cur_n;
-        sacc[nt][e] = ok ? sacc[nt][e] * a.scale2 : -INFINITY;
-        sacc[nt][2 + e] = ok ? sacc[nt][2 + e] * a.scale2 : -INFINITY;
-        tmax0 = fmaxf(tmax0, sacc[nt][e]);
-        tmax1 = fmaxf(tmax1, sacc[nt][2 + e]);
+        const int h = nt * 8 + cq * 2 + e;
+        if (h < a.g) {
+          float* lrow = a.logits + (static_cast<size_t>(cur_lane) * a.g + h) * a.lcap + i0;
+          lrow[gq] = sv[e];
+          lrow[gq + 8] = sv[2 + e];
+        }
       }
-      const int i = i0 + nt * 8 + cq * 2;
-      if (v0)
-        *reinterpret_cast<float2*>(a.logits + (static_cast<size_t>(cur_lane) * a.g + h0) * a.lcap + i) =
-            make_float2(sacc[nt][0], sacc[nt][1]);
-      if (v1)
-        *reinterpret_cast<float2*>(a.logits + (static_cast<size_t>(cur_lane) * a.g + h1) * a.lcap + i) =
-            make_float2(sacc[nt][2], sacc[nt][3]);
-    }
-    tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 1));
-    tmax0 = fmaxf(tmax0, __shfl_xor_sync(0xffffffffu, tmax0, 2));
-    tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 1));
-    tmax1 = fmaxf(tmax1, __shfl_xor_sync(0xffffffffu, tmax1, 2));
-    const float mn0 = fmaxf(m0, tmax0), mn1 = fmaxf(m1, tmax1);
-    const float c0 = (m0 == -INFINITY) ? 0.f : exp2f(m0 - mn0);
-    const float c1 = (m1 == -INFINITY) ? 0.f : exp2f(m1 - mn1);
-    m0 = mn0;
-    m1 = mn1;
-    float ps0 = 0.f, ps1 = 0.f;
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
+      float pv[4];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        p[nt][e] = v0 ? exp2f(sacc[nt][e] - mn0) : 0.f;
-        p[nt][2 + e] = v1 ? exp2f(sacc[nt][2 + e] - mn1) : 0.f;
-        ps0 += p[nt][e];
-        ps1 += p[nt][2 + e];
-      }
-    }
-    l0 = l0 * c0 + ps0;
-    l1 = l1 * c1 + ps1;
+        float tm = fmaxf(sv[e], sv[2 + e]);
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+        const float mo = m_run[nt][e];
+        const float mn = fmaxf(mo, tm);
+        const float corr = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
+        m_run[nt][e] = mn;
+        pv[e] = exp2f(sv[e] - mn);
+        pv[2 + e] = exp2f(sv[2 + e] - mn);
+        l_run[nt][e] = l_run[nt][e] * corr + pv[e] + pv[2 + e];
 #pragma unroll
-    for (int dn = 0; dn < C::kDn; ++dn) {
-      o_acc[dn][0] *= c0; o_acc[dn][1] *= c0;
-      o_acc[dn][2] *= c1; o_acc[dn][3] *= c1;
+        for (int dt = 0; dt < C::kDt; ++dt) {
+          o_acc[nt][dt][e] *= corr;
+          o_acc[nt][dt][2 + e] *= corr;
+        }
+      }
+      split_bf16(pv[0], pv[1], ph[nt][0], pl[nt][0]);   // token gq,     heads 2c, 2c+1
+      split_bf16(pv[2], pv[3], ph[nt][1], pl[nt][1]);   // token gq + 8
     }
-    // P as the A operand (rows = heads, k = tokens): hi and lo parts
-    uint32_t ah[4], al[4];
-    split_bf16(p[0][0], p[0][1], ah[0], al[0]);   // row h0, tokens 2c, 2c+1
-    split_bf16(p[0][2], p[0][3], ah[1], al[1]);   // row h1
-    split_bf16(p[1][0], p[1][1], ah[2], al[2]);   // row h0, tokens 2c+8, 2c+9
-    split_bf16(p[1][2], p[1][3], ah[3], al[3]);   // row h1
+    // P -> [head][token] in shared memory (transposed store), then B fragments
+    uint32_t bh[NT][2], bl[NT][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      unsigned char* pb = pbuf + nt * 2 * 8 * 32;
+      stsm_x2_t(smem_u32(pb + prow), ph[nt][0], ph[nt][1]);
+      stsm_x2_t(smem_u32(pb + 256 + prow), pl[nt][0], pl[nt][1]);
+    }
+    __syncwarp();
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const unsigned char* pb = pbuf + nt * 2 * 8 * 32;
+      ldsm_x2(smem_u32(pb + prow), bh[nt][0], bh[nt][1]);
+      ldsm_x2(smem_u32(pb + 256 + prow), bl[nt][0], bl[nt][1]);
+    }
+    // O^T += V^T P^T
     {
-      const int tok = (lane_id & 7) + (((lane_id >> 3) & 1) << 3);
-      const int colsel = lane_id >> 4;
-      const uint32_t rowaddr = smem_u32(vb + tok * C::kRowStride) + colsel * 16;
+      const uint32_t addr = smem_u32(vb + vtok * C::kRowStride + vcol);
 #pragma unroll
-      for (int dn = 0; dn < C::kDn; dn += 2) {
-        uint32_t b0, b1, b2, b3;
-        ldsm_x4_t(rowaddr + dn * 16, b0, b1, b2, b3);
-        mma_bf16(o_acc[dn], ah[0], ah[1], ah[2], ah[3], b0, b1);
-        mma_bf16(o_acc[dn], al[0], al[1], al[2], al[3], b0, b1);
-        mma_bf16(o_acc[dn + 1], ah[0], ah[1], ah[2], ah[3], b2, b3);
-        mma_bf16(o_acc[dn + 1], al[0], al[1], al[2], al[3], b2, b3);
+      for (int dt = 0; dt < C::kDt; ++dt) {
+        uint32_t af[4];
+        ldsm_x4_t(addr + dt * 32, af[0], af[1], af[2], af[3]);
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          mma_bf16a(o_acc[nt][dt], af, bh[nt][0], bh[nt][1]);
+          mma_bf16a(o_acc[nt][dt], af, bl[nt][0], bl[nt][1]);
+        }
       }
     }
     __syncwarp();
@@ -477,14 +528,35 @@ __global__ void __launch_bounds__(kF32Chunk) attend_f32_kernel(AttendArgs a, int
 
 }  // namespace
 
-cudaError_t prepare_kernels(const Ctx& ctx) {
-  (void)ctx;
-  cudaError_t e = cudaFuncSetAttribute(attend_bf16_kernel<128>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Bf16Cfg<128>::kSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(attend_bf16_kernel<64>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Bf16Cfg<64>::kSmem);
-  return e;
+template <int D, int NT>
+static cudaError_t set_attr() {
+  return cudaFuncSetAttribute(attend_bf16_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              Bf16Cfg<D, NT>::kSmem);
+}
+
+template <int D, int NT>
+static int ctas_per_sm() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_bf16_kernel<D, NT>, kAttendWarps * 32,
+                                                    Bf16Cfg<D, NT>::kSmem) != cudaSuccess)
+    return 0;
+  return n;
+}
+
+cudaError_t prepare_kernels(Ctx& ctx) {
+  cudaError_t e = set_attr<128, 1>();
+  if (e == cudaSuccess) e = set_attr<128, 2>();
+  if (e == cudaSuccess) e = set_attr<64, 1>();
+  if (e == cudaSuccess) e = set_attr<64, 2>();
+  if (e != cudaSuccess) return e;
+  const Dims& dm = ctx.dims;
+  const int nt = dm.g > 8 ? 2 : 1;
+  ctx.attend_ctas_per_sm = 1;
+  if (dm.dtype == KVEVICT_BF16) {
+    if (dm.d == 128) ctx.attend_ctas_per_sm = nt == 1 ? ctas_per_sm<128, 1>() : ctas_per_sm<128, 2>();
+    else ctx.attend_ctas_per_sm = nt == 1 ? ctas_per_sm<64, 1>() : ctas_per_sm<64, 2>();
+  }
+  return cudaGetLastError();
 }
 
 cudaError_t launch_attend(const Ctx& ctx, int layer, const void* q, const void* k_new, const void* v_new,
@@ -501,11 +573,16 @@ cudaError_t launch_attend(const Ctx& ctx, int layer, const void* q, const void* 
   a.scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(dm.d));
   if (dm.dtype == KVEVICT_BF16) {
     if (dm.lanes > kMaxLanesSmem) return cudaErrorInvalidValue;
-    const int grid = ctx.sm_count * 2;
-    if (dm.d == 128)
-      attend_bf16_kernel<128><<<grid, kAttendWarps * 32, Bf16Cfg<128>::kSmem, stream>>>(a);
+    const int grid = ctx.sm_count * ctx.attend_ctas_per_sm;
+    const int nt = dm.g > 8 ? 2 : 1;
+    if (dm.d == 128 && nt == 1)
+      attend_bf16_kernel<128, 1><<<grid, kAttendWarps * 32, Bf16Cfg<128, 1>::kSmem, stream>>>(a);
+    else if (dm.d == 128)
+      attend_bf16_kernel<128, 2><<<grid, kAttendWarps * 32, Bf16Cfg<128, 2>::kSmem, stream>>>(a);
+    else if (nt == 1)
+      attend_bf16_kernel<64, 1><<<grid, kAttendWarps * 32, Bf16Cfg<64, 1>::kSmem, stream>>>(a);
     else
-      attend_bf16_kernel<64><<<grid, kAttendWarps * 32, Bf16Cfg<64>::kSmem, stream>>>(a);
+      attend_bf16_kernel<64, 2><<<grid, kAttendWarps * 32, Bf16Cfg<64, 2>::kSmem, stream>>>(a);
   } else {
     const int chunks = (dm.cap + kF32Chunk) / kF32Chunk;   // enough for n = cap - 1 plus the new token
     if (chunks > kMaxSeg) return cudaErrorInvalidValue;

@@ -20,7 +20,8 @@
 namespace kve {
 namespace {
 
-constexpr int kEpiThreads = 512;
+constexpr int kEpiThreads = 1024;
+constexpr int kApplyThreads = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct EpiArgs {
@@ -38,15 +39,13 @@ __device__ __forceinline__ void copy_row(KT* dst, const KT* src, int d) {
 }
 
 template <typename KT>
-__global__ void __launch_bounds__(kEpiThreads) decode_epilogue_kernel(EpiArgs A) {
-  __shared__ float sh_M[kMaxG], sh_L[kMaxG], sh_lse2[kMaxG];
-  __shared__ int sh_hist[256];
-  __shared__ int sh_misc[40];
-  __shared__ int sh_scan[40];
-  __shared__ int sh_idx[kEpiThreads];
-  __shared__ unsigned sh_min[32];
-  __shared__ __align__(16) float sh_rows[128 * kMaxW];
+__device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n);
+__device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const Dims& dm, int* sh_scan,
+                               int* sh_flag);
 
+template <typename KT>
+__global__ void __launch_bounds__(kEpiThreads) decode_epilogue_kernel(EpiArgs A) {
+  __shared__ int sh_scan[40];
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   LaneRefs L = lane_refs(A.ls, dm, l);
@@ -60,9 +59,39 @@ __global__ void __launch_bounds__(kEpiThreads) decode_epilogue_kernel(EpiArgs A)
   }
   if (bad) {
     if (tid == 0) { A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0; }
-    return;
+  } else {
+    lane_step<KT>(A, L, n);
   }
+  // the last CTA of the grid to finish runs the layer allocator
+  __shared__ int sh_last, sh_flag;
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    sh_last = atomicAdd(A.ws.epi_done, 1) == static_cast<int>(gridDim.x) - 1;
+  }
+  __syncthreads();
+  if (sh_last) {
+    if (tid == 0) *A.ws.epi_done = 0;
+    __threadfence();
+    allocate_layer(A.ls, A.ws, dm, sh_scan, &sh_flag);
+  }
+}
+
+// One lane's step after the attention kernel (all threads of the CTA).
+template <typename KT>
+__device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n) {
+  __shared__ float sh_M[kMaxG], sh_L[kMaxG], sh_lse2[kMaxG];
+  __shared__ int sh_hist[256];
+  __shared__ int sh_misc[40];
+  __shared__ int sh_scan[40];
+  __shared__ int sh_idx[kEpiThreads];
+  __shared__ unsigned sh_min[32];
+  __shared__ int sh_nan;
+  __shared__ __align__(16) float sh_rows[128 * kMaxW];
+  const Dims& dm = A.dm;
+  const int l = blockIdx.x, tid = threadIdx.x;
   const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
+  if (tid == 0) sh_nan = 0;
 
   // ---- combine the split-K partials --------------------------------------
   if (A.has_q) {
@@ -203,8 +232,9 @@ __global__ void __launch_bounds__(kEpiThreads) decode_epilogue_kernel(EpiArgs A)
   // ---- relocation plan ---------------------------------------------------------
   int t_live = 0;
   const int ndst = lane_plan(L, nb, m + 1, false, dm.theta_f, need, &t_live, sh_scan);
-  int nan_tot;
-  (void)block_excl_scan(nan_count, sh_scan, &nan_tot);
+  if (nan_count) atomicAdd(&sh_nan, nan_count);
+  __syncthreads();
+  const int nan_tot = sh_nan;
   if (tid == 0) {
     A.ws.need_admit[l] = need ? 1 : 0;
     A.ws.want_dst[l] = ndst;
@@ -218,20 +248,19 @@ __global__ void __launch_bounds__(kEpiThreads) decode_epilogue_kernel(EpiArgs A)
 }
 
 // ---------------------------------------------------------------------------
-// allocator: one CTA
+// allocator: run by one CTA (the last epilogue CTA of a decode step, or its
+// own launch in the forced compaction).  Per-lane requests written by other
+// CTAs of the same grid are read with ld.global.cg (L2), after their
+// __threadfence().
 // ---------------------------------------------------------------------------
-constexpr int kAllocThreads = 1024;
-
-__global__ void __launch_bounds__(kAllocThreads) allocate_kernel(LayerState ls, Workspace ws, Dims dm) {
-  __shared__ int sh_scan[40];
-  __shared__ int sh_flag;
+__device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const Dims& dm, int* sh_scan,
+                               int* sh_flag) {
   const int tid = threadIdx.x;
   if (tid == 0) {
-    sh_flag = *ws.work_flag;
-    *ws.work_flag = 0;
+    *sh_flag = atomicExch(ws.work_flag, 0);
   }
   __syncthreads();
-  if (sh_flag == 0) {
+  if (*sh_flag == 0) {
     if (tid == 0) { ws.counters[1] = 0; ws.counters[2] = 0; }
     return;
   }
@@ -239,9 +268,9 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(LayerState ls, 
   int totA = 0, totD = 0, totM = 0;
   for (int base = 0; base < dm.lanes; base += blockDim.x) {
     const int l = base + tid;
-    const int a = l < dm.lanes ? ws.need_admit[l] : 0;
-    const int dd = l < dm.lanes ? ws.want_dst[l] : 0;
-    const int mm = (l < dm.lanes && dd > 0) ? ws.plan_tlive[l] : 0;
+    const int a = l < dm.lanes ? __ldcg(ws.need_admit + l) : 0;
+    const int dd = l < dm.lanes ? __ldcg(ws.want_dst + l) : 0;
+    const int mm = (l < dm.lanes && dd > 0) ? __ldcg(ws.plan_tlive + l) : 0;
     int ta, td, tm;
     const int ea = block_excl_scan(a, sh_scan, &ta);
     const int ed = block_excl_scan(dd, sh_scan, &td);
@@ -258,7 +287,7 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(LayerState ls, 
   int found = 0;
   for (int base = 0; base < dm.P && found < need_total; base += blockDim.x) {
     const int blk = base + tid;
-    const int fr = (blk < dm.P && ls.owner[blk] < 0) ? 1 : 0;
+    const int fr = (blk < dm.P && __ldcg(ls.owner + blk) < 0) ? 1 : 0;
     int tot;
     const int ex = block_excl_scan(fr, sh_scan, &tot);
     if (fr && found + ex < need_total) ws.alloc_ids[found + ex] = blk;
@@ -269,7 +298,7 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(LayerState ls, 
   const int gotA = min(found, totA);
   const bool deferred = totD > found - gotA;
   for (int l = tid; l < dm.lanes; l += blockDim.x) {
-    if (ws.need_admit[l]) {
+    if (__ldcg(ws.need_admit + l)) {
       const int idx = ws.admit_block[l];
       if (idx < gotA) {
         const int blk = ws.alloc_ids[idx];
@@ -279,11 +308,11 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(LayerState ls, 
         // no block: the new token is not stored (its table entry is dropped)
         ws.admit_block[l] = -1;
         ws.need_admit[l] = 0;
-        ls.count[l] -= 1;
+        ls.count[l] = __ldcg(ls.count + l) - 1;
         set_status(ws.status, ST_NO_BLOCKS);
       }
     }
-    const int nd = ws.want_dst[l];
+    const int nd = __ldcg(ws.want_dst + l);
     if (nd > 0) {
       if (deferred) {
         ws.want_dst[l] = 0;
@@ -302,11 +331,17 @@ __global__ void __launch_bounds__(kAllocThreads) allocate_kernel(LayerState ls, 
   }
 }
 
+__global__ void __launch_bounds__(1024) allocate_kernel(LayerState ls, Workspace ws, Dims dm) {
+  __shared__ int sh_scan[40];
+  __shared__ int sh_flag;
+  allocate_layer(ls, ws, dm, sh_scan, &sh_flag);
+}
+
 // ---------------------------------------------------------------------------
 // apply: one CTA per lane
 // ---------------------------------------------------------------------------
 template <typename KT>
-__global__ void __launch_bounds__(kEpiThreads) apply_kernel(LayerState ls, Workspace ws, Dims dm,
+__global__ void __launch_bounds__(kApplyThreads) apply_kernel(LayerState ls, Workspace ws, Dims dm,
                                                            const void* k_new, const void* v_new,
                                                            int mark_freed, int32_t* moves) {
   __shared__ int sh_scan[40];
@@ -429,15 +464,15 @@ cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, 
 }
 
 cudaError_t launch_allocate_apply(const Ctx& ctx, int layer, const void* k_new, const void* v_new,
-                                  bool mark_freed, int32_t* moves, cudaStream_t stream) {
+                                  bool mark_freed, int32_t* moves, cudaStream_t stream, bool with_allocate) {
   LayerState ls = layer_state(ctx, layer);
-  allocate_kernel<<<1, kAllocThreads, 0, stream>>>(ls, ctx.ws, ctx.dims);
+  if (with_allocate) allocate_kernel<<<1, 1024, 0, stream>>>(ls, ctx.ws, ctx.dims);
   if (ctx.dims.dtype == KVEVICT_BF16)
-    apply_kernel<__nv_bfloat16><<<ctx.dims.lanes, kEpiThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, k_new, v_new,
-                                                                            mark_freed ? 1 : 0, moves);
+    apply_kernel<__nv_bfloat16><<<ctx.dims.lanes, kApplyThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, k_new, v_new,
+                                                                              mark_freed ? 1 : 0, moves);
   else
-    apply_kernel<float><<<ctx.dims.lanes, kEpiThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, k_new, v_new,
-                                                                   mark_freed ? 1 : 0, moves);
+    apply_kernel<float><<<ctx.dims.lanes, kApplyThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, k_new, v_new,
+                                                                     mark_freed ? 1 : 0, moves);
   return cudaGetLastError();
 }
 

@@ -74,6 +74,7 @@ struct Workspace {
   int32_t* freed_flag;             // [P]  1 = released during this call
   int32_t* blk_tag;                // [P]  1 = source block of a running plan
   int32_t* counters;               // [8] per-call scalars
+  int32_t* epi_done;               // 1 word: epilogue CTAs finished this call
   // DropKV prefill-window scorer
   float* d3_part;                  // [lanes][chunks][rows_cap][d + 2]
   __nv_bfloat16* d3_ahi;           // [lanes][rows][d]
@@ -90,6 +91,7 @@ struct Ctx {
   int sm_count;
   int device;
   size_t ws_bytes;
+  int attend_ctas_per_sm;
 };
 
 // workspace layout (host)
@@ -114,14 +116,14 @@ cudaError_t launch_compact(const Ctx&, int layer, const int32_t* victims, const 
 cudaError_t launch_score(const Ctx&, int layer, const void* q_win, int w, const int32_t* q_pos,
                          float* lse, float* a_out, float* scores, cudaStream_t);
 cudaError_t launch_stats(const Ctx&, int layer, long long* out, cudaStream_t);
-cudaError_t prepare_kernels(const Ctx&);   // one-time kernel attributes (not stream work)
+cudaError_t prepare_kernels(Ctx&);   // one-time kernel attributes and occupancy (not stream work)
 cudaError_t launch_attend(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
                           cudaStream_t);
 cudaError_t launch_epilogue(const Ctx&, int layer, bool has_q, int new_pos, const void* k_new,
                             const void* v_new, float* out, float* lse, int32_t* victims,
                             int32_t* n_victims, cudaStream_t);
 cudaError_t launch_allocate_apply(const Ctx&, int layer, const void* k_new, const void* v_new,
-                                  bool mark_freed, int32_t* moves, cudaStream_t);
+                                  bool mark_freed, int32_t* moves, cudaStream_t, bool with_allocate);
 
 // ---------------------------------------------------------------------------
 // device helpers
@@ -226,13 +228,48 @@ __device__ __forceinline__ bool select_is_victim(const SelectResult& r, unsigned
 
 // KeyFn(i) -> unsigned long long monotone key of entry i; PosFn(i) -> uint32
 // position; CandFn(i) -> bool.  key_bits = 32 or 64.  sh_hist: 256 ints,
-// sh_misc: 40 ints.  Returns the same SelectResult in every thread.
+// sh_misc: 40 ints (blockDim <= 1024).  Returns the same SelectResult in
+// every thread.  k == 1 (the steady state of a full cache) takes one pass.
 template <typename KeyFn, typename PosFn, typename CandFn>
 __device__ SelectResult block_bottom_k(int n, int k, int key_bits, KeyFn keyf, PosFn posf,
                                        CandFn candf, int* sh_hist, int* sh_misc) {
   SelectResult r;
   r.key_prefix = 0; r.key_mask = 0; r.pos_prefix = 0; r.pos_mask = 0; r.inclusive = 0; r.k = k;
   if (k <= 0) { r.k = 0; return r; }
+  if (k == 1) {
+    // a single victim: block-wide minimum of (key, position)
+    unsigned long long bk = ~0ull;
+    uint32_t bp = 0xFFFFFFFFu;
+    int any = 0;
+    for (int i = threadIdx.x; i < n; i += blockDim.x) {
+      if (!candf(i)) continue;
+      const unsigned long long kk = keyf(i);
+      const uint32_t pp = posf(i);
+      any = 1;
+      if (kk < bk || (kk == bk && pp < bp)) { bk = kk; bp = pp; }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const unsigned long long ok = __shfl_xor_sync(0xffffffffu, bk, o);
+      const uint32_t op = __shfl_xor_sync(0xffffffffu, bp, o);
+      any |= __shfl_xor_sync(0xffffffffu, any, o);
+      if (ok < bk || (ok == bk && op < bp)) { bk = ok; bp = op; }
+    }
+    unsigned long long* shk = reinterpret_cast<unsigned long long*>(sh_hist);   // 32 x 8 bytes
+    uint32_t* shp = reinterpret_cast<uint32_t*>(sh_hist + 64);
+    const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    if ((threadIdx.x & 31) == 0) { shk[wid] = bk; shp[wid] = bp; sh_misc[wid] = any; }
+    __syncthreads();
+    bk = ~0ull; bp = 0xFFFFFFFFu; any = 0;
+    for (int w = 0; w < nw; ++w) {
+      any |= sh_misc[w];
+      if (shk[w] < bk || (shk[w] == bk && shp[w] < bp)) { bk = shk[w]; bp = shp[w]; }
+    }
+    __syncthreads();
+    if (!any) { r.k = 0; return r; }
+    r.key_prefix = bk; r.key_mask = ~0ull; r.pos_prefix = bp; r.pos_mask = 0xFFFFFFFFu; r.inclusive = 1;
+    return r;
+  }
   const int total_bits = key_bits + 32;
   int k_rem = k;
   for (int shift = total_bits - 8; shift >= 0; shift -= 8) {

@@ -52,9 +52,11 @@ __device__ __forceinline__ int lane_remove(const LaneRefs& L, int n, VictimFn is
       isv = is_victim(i);
       keep = !isv;
     }
-    int ktot, vtot;
-    const int kex = block_excl_scan(keep ? 1 : 0, sh_scan, &ktot);
-    const int vex = block_excl_scan(isv ? 1 : 0, sh_scan, &vtot);
+    // one scan of both counts: survivors in the low half-word, victims in the high
+    int tot2;
+    const int ex2 = block_excl_scan((keep ? 1 : 0) | (isv ? 0x10000 : 0), sh_scan, &tot2);
+    const int kex = ex2 & 0xFFFF, vex = ex2 >> 16;
+    const int ktot = tot2 & 0xFFFF, vtot = tot2 >> 16;
     const int ni = kept_total + kex;
     sh_idx[threadIdx.x] = keep ? ni : -1;
     // every read of this chunk happened before the scans' barriers

@@ -268,7 +268,7 @@ cudaError_t launch_compact(const Ctx& ctx, int layer, const int32_t* victims, co
                            cudaStream_t stream) {
   LayerState ls = layer_state(ctx, layer);
   compact_evict_kernel<<<ctx.dims.lanes, kThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, victims, n_victims);
-  cudaError_t e = launch_allocate_apply(ctx, layer, nullptr, nullptr, true, moves, stream);
+  cudaError_t e = launch_allocate_apply(ctx, layer, nullptr, nullptr, true, moves, stream, true);
   if (e != cudaSuccess) return e;
   compact_finalize_kernel<<<1, 1024, 0, stream>>>(ctx.ws, ctx.dims, freed, n_freed, n_moves);
   return cudaGetLastError();
@@ -290,7 +290,7 @@ cudaError_t launch_decode(const Ctx& ctx, int layer, const void* q, const void* 
   }
   e = launch_epilogue(ctx, layer, q != nullptr, new_pos, k_new, v_new, out, lse, victims, n_victims, stream);
   if (e != cudaSuccess) return e;
-  return launch_allocate_apply(ctx, layer, k_new, v_new, false, nullptr, stream);
+  return launch_allocate_apply(ctx, layer, k_new, v_new, false, nullptr, stream, false);
 }
 
 }  // namespace kve
