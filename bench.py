@@ -258,6 +258,8 @@ def run_gpu(args):
             if timed_events is not None:
                 timed_events[layer][1].record(stream)
             eng.finish_step(layer, q, kn, vn, pos, outs[layer], lses[layer], vics[layer], nvs[layer])
+            if timed_events is not None:
+                timed_events[layer][2].record(stream)
 
     for t in range(args.warmup):
         step(t)
@@ -270,7 +272,7 @@ def run_gpu(args):
 
     sampler = ClockSampler(local)
     sampler.start()
-    evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
+    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)]
            for _ in range(args.steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
@@ -299,6 +301,7 @@ def run_gpu(args):
     # dominant kernel: the split-K attention, timed by events around each launch
     d1 = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(args.steps) for l in range(L)]
     d1_ms = statistics.mean(d1)
+    fin_ms = statistics.mean(evs[i][l][1].elapsed_time(evs[i][l][2]) for i in range(args.steps) for l in range(L))
     d1_bytes = int((counts_before + lanes).mean()) * 2 * d * 2   # K/V rows per launch (one layer)
     peak, peak_kind = hbm_peak()
     d1_gbs = d1_bytes / (d1_ms * 1e-3) / 1e9
@@ -377,6 +380,7 @@ def run_gpu(args):
                    "global_batch": B * world, "seq_len": shp.ctx, "parallelism": "replica per GPU" if world > 1 else "1 GPU",
                    "l2": "no flush: every layer call streams ~215 MB of K/V, above the 129 MB L2",
                    "bytes_per_step": int(step_bytes), "moved_tokens_timed": moved,
+                   "attend_ms_per_layer": round(d1_ms, 5), "finish_ms_per_layer": round(fin_ms, 5),
                    "setup_s": round(setup_s, 1)},
         "roofline": {"bound": "hbm", "kernel": "attend_bf16_kernel (split-K decode attention)",
                      "achieved": round(d1_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
@@ -385,7 +389,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clocks,
-        "gpu_launches": 4 * L * args.steps,
+        "gpu_launches": 3 * L * args.steps,
     }
     if args.profile_layers:
         line["profile_only"] = "%d layers: for profiling, not a bench number" % L

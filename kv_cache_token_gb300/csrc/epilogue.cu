@@ -131,6 +131,13 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   double* keys64 = A.ws.keys64 ? A.ws.keys64 + static_cast<size_t>(l) * dm.cap : nullptr;
   double* pooled64 = A.ws.pooled64 ? A.ws.pooled64 + static_cast<size_t>(l) * dm.cap : nullptr;
   const float* lg = A.ws.logits + static_cast<size_t>(l) * g * dm.lcap;
+  const int k = max(0, n + 1 - dm.budget);
+  const int cut = A.new_pos - dm.R + 1;
+  // k == 1 (a full cache in steady state): the minimum candidate (key,
+  // position) is tracked in the same pass that produces the keys.
+  unsigned long long best_k = ~0ull;
+  uint32_t best_p = 0xFFFFFFFFu;
+  int best_i = -1;
   int nan_count = 0;
   for (int i = tid; i < n; i += blockDim.x) {
     float w = 0.f;
@@ -151,6 +158,13 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
         L.score[i] = sc;
       }
       if (sc != sc) ++nan_count;
+      if (k == 1) {
+        const int p = L.pos[i];
+        const unsigned long long kk = mono_key(sc);
+        if (p < cut && (kk < best_k || (kk == best_k && static_cast<uint32_t>(p) < best_p))) {
+          best_k = kk; best_p = static_cast<uint32_t>(p); best_i = i;
+        }
+      }
     }
   }
   if (policy == KVEVICT_SNAPKV && tid == 0) keys64[n] = 0.0;
@@ -170,32 +184,47 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
         m = fmax(m, __shfl_down_sync(0xffffffffu, v, o));
         m = fmax(m, __shfl_up_sync(0xffffffffu, v, o));
       }
-      if (lane >= r && lane < 32 - r && idx >= 0 && idx < nn) pooled64[idx] = m;
+      if (lane >= r && lane < 32 - r && idx >= 0 && idx < nn) {
+        pooled64[idx] = m;
+        if (k == 1 && idx < n) {
+          const int p = L.pos[idx];
+          const unsigned long long kk = mono_key(m);
+          if (p < cut && (kk < best_k || (kk == best_k && static_cast<uint32_t>(p) < best_p))) {
+            best_k = kk; best_p = static_cast<uint32_t>(p); best_i = idx;
+          }
+        }
+      }
     }
     __syncthreads();
   }
 
-  // ---- bottom-k selection ------------------------------------------------------
-  const int k = max(0, n + 1 - dm.budget);
-  const int cut = A.new_pos - dm.R + 1;
+  // ---- bottom-k selection and eviction ------------------------------------------
   auto candf = [&](int i) { return L.pos[i] < cut; };
   auto posf = [&](int i) { return static_cast<uint32_t>(L.pos[i]); };
-  SelectResult sel;
-  int vcount, dead = 0;
+  int vcount = 0, dead = 0;
   int32_t* vout = A.victims + static_cast<size_t>(l) * dm.cap;
-  if (policy == KVEVICT_SNAPKV) {
-    auto keyf = [&](int i) { return mono_key(pooled64[i]); };
-    sel = block_bottom_k(n, k, 64, keyf, posf, candf, sh_hist, sh_misc);
-    auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
-    vcount = lane_remove(L, n, isv, vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx, sh_rows);
-  } else {
-    auto keyf = [&](int i) { return mono_key(L.score[i]); };
-    sel = block_bottom_k(n, k, 32, keyf, posf, candf, sh_hist, sh_misc);
-    auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
-    vcount = lane_remove(L, n, isv, vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx, sh_rows);
+  if (k == 1) {
+    const int v = block_argmin3(best_k, best_p, best_i, sh_hist, sh_misc);
+    if (v >= 0) {
+      vcount = 1;
+      dead = lane_remove_one(L, n, v, vout, dm.P, A.ws.status, sh_misc, sh_rows);
+    }
+  } else if (k > 1) {
+    SelectResult sel;
+    if (policy == KVEVICT_SNAPKV) {
+      auto keyf = [&](int i) { return mono_key(pooled64[i]); };
+      sel = block_bottom_k(n, k, 64, keyf, posf, candf, sh_hist, sh_misc);
+      auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
+      vcount = lane_remove(L, n, isv, vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx, sh_rows);
+    } else {
+      auto keyf = [&](int i) { return mono_key(L.score[i]); };
+      sel = block_bottom_k(n, k, 32, keyf, posf, candf, sh_hist, sh_misc);
+      auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
+      vcount = lane_remove(L, n, isv, vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx, sh_rows);
+    }
   }
   const int m = n - vcount;
-  const int nb = lane_prune_blocks(L, l, sh_scan);
+  const int nb = (k > 1 && dead > 0) ? lane_prune_blocks(L, l, sh_scan) : *L.nblocks;
 
   // ---- admission: lowest free slot among the lane's blocks --------------------
   unsigned best = 0xFFFFFFFFu;

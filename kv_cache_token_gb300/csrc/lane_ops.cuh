@@ -110,6 +110,96 @@ __device__ __forceinline__ int lane_remove(const LaneRefs& L, int n, VictimFn is
   return vict_total;
 }
 
+// Block-wide minimum of (key, position) with the entry index; returns the
+// index of the minimum (-1 if no thread had a candidate).  Every thread
+// returns the same value.  sh_a: 256 ints of scratch, sh_b: 40 ints.
+__device__ __forceinline__ int block_argmin3(unsigned long long bk, uint32_t bp, int bi, int* sh_a, int* sh_b) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const unsigned long long ok = __shfl_xor_sync(0xffffffffu, bk, o);
+    const uint32_t op = __shfl_xor_sync(0xffffffffu, bp, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+    if (oi >= 0 && (bi < 0 || ok < bk || (ok == bk && op < bp))) { bk = ok; bp = op; bi = oi; }
+  }
+  unsigned long long* shk = reinterpret_cast<unsigned long long*>(sh_a);   // 32 x 8 bytes
+  uint32_t* shp = reinterpret_cast<uint32_t*>(sh_a + 64);
+  const int wid = threadIdx.x >> 5, nw = blockDim.x >> 5;
+  if ((threadIdx.x & 31) == 0) { shk[wid] = bk; shp[wid] = bp; sh_b[wid] = bi; }
+  __syncthreads();
+  bk = ~0ull; bp = 0xFFFFFFFFu; bi = -1;
+  for (int w = 0; w < nw; ++w) {
+    const int oi = sh_b[w];
+    if (oi >= 0 && (bi < 0 || shk[w] < bk || (shk[w] == bk && shp[w] < bp))) { bk = shk[w]; bp = shp[w]; bi = oi; }
+  }
+  __syncthreads();
+  return bi;
+}
+
+// Removes the single entry v (the step's only victim): its position goes to
+// vout[0], its live bit clears (an emptied block is released and dropped
+// from the lane's block list by swapping in the last entry), and entries
+// v+1 .. n-1 shift down by one.  Returns 1 if a block was released.
+__device__ __forceinline__ int lane_remove_one(const LaneRefs& L, int n, int v, int32_t* vout, int P,
+                                               uint32_t* status, int* sh_b, float* sh_rows) {
+  if (threadIdx.x == 0) {
+    const int s = L.slot[v];
+    vout[0] = L.pos[v];
+    int dead_blk = -1;
+    if (s >= 0 && s < P * kBlock) {
+      const int b = s >> 4, bit = 1 << (s & 15);
+      const int old = atomicAnd(&L.mask[b], ~bit);
+      if ((old & ~bit) == 0 && (old & bit)) {
+        L.owner[b] = -1;
+        dead_blk = b;
+      }
+    } else if (s >= 0) {
+      set_status(status, ST_BAD_INDEX);
+    }
+    sh_b[0] = dead_blk;
+  }
+  // shift the table: every read of a chunk precedes the barrier, the chunk's
+  // writes (one index lower) follow it
+  for (int base = v + 1; base < n; base += blockDim.x) {
+    const int i = base + threadIdx.x;
+    int p = 0, s = 0;
+    float sc = 0.f;
+    if (i < n) {
+      p = L.pos[i];
+      s = L.slot[i];
+      if (L.score) sc = L.score[i];
+    }
+    __syncthreads();
+    if (i < n) {
+      L.pos[i - 1] = p;
+      L.slot[i - 1] = s;
+      if (L.score) L.score[i - 1] = sc;
+    }
+  }
+  if (L.ring) {
+    const int W = L.W;
+    for (int base = v + 1; base < n; base += 128) {
+      const int rows = min(128, n - base);
+      __syncthreads();
+      for (int e = threadIdx.x; e < rows * W; e += blockDim.x) sh_rows[e] = L.ring[static_cast<size_t>(base) * W + e];
+      __syncthreads();
+      for (int e = threadIdx.x; e < rows * W; e += blockDim.x) L.ring[static_cast<size_t>(base - 1) * W + e] = sh_rows[e];
+    }
+  }
+  __syncthreads();
+  const int dead_blk = sh_b[0];
+  if (dead_blk >= 0) {
+    const int nb = *L.nblocks;
+    for (int j = threadIdx.x; j < nb; j += blockDim.x) {
+      if (L.blocks[j] == dead_blk) {
+        L.blocks[j] = L.blocks[nb - 1];
+        *L.nblocks = nb - 1;
+      }
+    }
+    __syncthreads();
+  }
+  return dead_blk >= 0 ? 1 : 0;
+}
+
 // Drops released blocks (owner != l) from the lane's block list, stably.
 __device__ __forceinline__ int lane_prune_blocks(const LaneRefs& L, int l, int* sh_scan) {
   const int nb = *L.nblocks;
