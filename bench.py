@@ -248,18 +248,11 @@ def run_gpu(args):
     nvs = [torch.empty((eng.lanes,), dtype=torch.int32, device="cuda") for _ in range(L)]
     stream = torch.cuda.current_stream()
 
-    def step(t, timed_events=None):
+    def step(t):
         pos = shp.ctx + t
         for layer in range(L):
             q, kn, vn = inputs[t][layer]
-            if timed_events is not None:
-                timed_events[layer][0].record(stream)
-            eng.attend(layer, q, kn, vn)
-            if timed_events is not None:
-                timed_events[layer][1].record(stream)
-            eng.finish_step(layer, q, kn, vn, pos, outs[layer], lses[layer], vics[layer], nvs[layer])
-            if timed_events is not None:
-                timed_events[layer][2].record(stream)
+            eng.decode_step(layer, q, kn, vn, pos, outs[layer], lses[layer], vics[layer], nvs[layer])
 
     for t in range(args.warmup):
         step(t)
@@ -272,19 +265,32 @@ def run_gpu(args):
 
     sampler = ClockSampler(local)
     sampler.start()
-    evs = [[[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(L)]
-           for _ in range(args.steps)]
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     barrier()
     torch.cuda.synchronize()
     e0.record(stream)
     for i in range(args.steps):
-        step(args.warmup + i, evs[i])
+        step(args.warmup + i)
     e1.record(stream)
     torch.cuda.synchronize()
     barrier()
     clocks = sampler.stop()
     elapsed_ms = e0.elapsed_time(e1)
+    # dominant kernel: the split-K attention of every layer, replayed on the
+    # steady-state tables (it changes no engine state), each launch
+    # bracketed by CUDA events on the launching stream
+    reps = 3
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps * L)]
+    tlast = args.warmup + args.steps - 1
+    torch.cuda.synchronize()
+    for rep in range(reps):
+        for layer in range(L):
+            q, kn, vn = inputs[tlast][layer]
+            ev = evs[rep * L + layer]
+            ev[0].record(stream)
+            eng.attend(layer, q, kn, vn)
+            ev[1].record(stream)
+    torch.cuda.synchronize()
     code, msg = eng.last_error()
     assert code == 0, msg
     counts_after = eng.counts.sum(dim=1).cpu().numpy().astype(np.int64)
@@ -299,9 +305,9 @@ def run_gpu(args):
     step_bytes = (kv_bytes + score_bytes + move_bytes) / args.steps
     ms_per_step = elapsed_ms / args.steps
     # dominant kernel: the split-K attention, timed by events around each launch
-    d1 = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(args.steps) for l in range(L)]
+    d1 = [ev[0].elapsed_time(ev[1]) for ev in evs]
     d1_ms = statistics.mean(d1)
-    fin_ms = statistics.mean(evs[i][l][1].elapsed_time(evs[i][l][2]) for i in range(args.steps) for l in range(L))
+    fin_ms = ms_per_step / L - d1_ms
     d1_bytes = int((counts_before + lanes).mean()) * 2 * d * 2   # K/V rows per launch (one layer)
     peak, peak_kind = hbm_peak()
     d1_gbs = d1_bytes / (d1_ms * 1e-3) / 1e9
@@ -380,7 +386,7 @@ def run_gpu(args):
                    "global_batch": B * world, "seq_len": shp.ctx, "parallelism": "replica per GPU" if world > 1 else "1 GPU",
                    "l2": "no flush: every layer call streams ~215 MB of K/V, above the 129 MB L2",
                    "bytes_per_step": int(step_bytes), "moved_tokens_timed": moved,
-                   "attend_ms_per_layer": round(d1_ms, 5), "finish_ms_per_layer": round(fin_ms, 5),
+                   "attend_ms_per_layer": round(d1_ms, 5), "rest_of_step_ms_per_layer": round(fin_ms, 5),
                    "setup_s": round(setup_s, 1)},
         "roofline": {"bound": "hbm", "kernel": "attend_bf16_kernel (split-K decode attention)",
                      "achieved": round(d1_gbs, 1), "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",

@@ -55,10 +55,12 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base) {
   Workspace w;
   w.status = reinterpret_cast<uint32_t*>(take(4));
   w.work_flag = reinterpret_cast<int32_t*>(take(4));
-  w.logits = reinterpret_cast<float*>(take(lanes * g * dm.lcap * 4));
-  w.part_o = reinterpret_cast<float*>(take(lanes * kMaxSeg * g * d * 4));
-  w.part_ml = reinterpret_cast<float*>(take(lanes * kMaxSeg * g * 2 * 4));
-  w.lane_nseg = reinterpret_cast<int32_t*>(take(lanes * 4));
+  for (int c = 0; c < 2; ++c) {
+    w.logits_buf[c] = reinterpret_cast<float*>(take(lanes * g * dm.lcap * 4));
+    w.part_o_buf[c] = reinterpret_cast<float*>(take(lanes * kMaxSeg * g * d * 4));
+    w.part_ml_buf[c] = reinterpret_cast<float*>(take(lanes * kMaxSeg * g * 2 * 4));
+    w.lane_nseg_buf[c] = reinterpret_cast<int32_t*>(take(lanes * 4));
+  }
   const bool snap = c.policy == KVEVICT_SNAPKV;
   w.keys64 = snap ? reinterpret_cast<double*>(take(lanes * cap * 8)) : nullptr;
   w.pooled64 = snap ? reinterpret_cast<double*>(take(lanes * cap * 8)) : nullptr;

@@ -133,6 +133,11 @@ __device__ __forceinline__ void mma_bf16a(float* c, const uint32_t* a, uint32_t 
 }
 
 template <int D, int NT>
+__device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_prefix, const int tp, const int gw,
+                                            const int t_begin, const int t_end, unsigned char* wbuf,
+                                            uint64_t* bars);
+
+template <int D, int NT>
 __global__ void __launch_bounds__(kAttendWarps * 32, 3) attend_bf16_kernel(AttendArgs a) {
   using C = Bf16Cfg<D, NT>;
   extern __shared__ __align__(128) unsigned char smem[];
@@ -183,11 +188,22 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) attend_bf16_kernel(Atten
   const int gw = blockIdx.x * kAttendWarps + warp;
   const int t_begin = gw * tp;
   const int t_end = min(total, t_begin + tp);
-  if (t_begin >= t_end) return;
+  if (t_begin < t_end) attend_warp<D, NT>(a, sh_prefix, tp, gw, t_begin, t_end, smem + warp * C::kWarpBytes,
+                                          sh_bar[warp]);
+  // the next kernel in the stream may start now; this grid completes only
+  // after its predecessor did (so completion orders everything before it)
+  grid_dep_wait();
+  grid_dep_launch();
+}
 
-  unsigned char* wbuf = smem + warp * C::kWarpBytes;
+// One warp's range of tiles [t_begin, t_end) (stream-K split of the layer).
+template <int D, int NT>
+__device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_prefix, const int tp, const int gw,
+                                            const int t_begin, const int t_end, unsigned char* wbuf,
+                                            uint64_t* bars) {
+  using C = Bf16Cfg<D, NT>;
+  const int lane_id = threadIdx.x & 31;
   unsigned char* pbuf = wbuf + kAttStages * C::kStageBytes;
-  uint64_t* bars = sh_bar[warp];
   if (lane_id == 0) {
     for (int s = 0; s < kAttStages; ++s) mbar_init(&bars[s], 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -453,7 +469,10 @@ __global__ void __launch_bounds__(kF32Chunk) attend_f32_kernel(AttendArgs a, int
   if (n < 0 || n >= a.cap) { if (tid == 0) set_status(a.status, ST_BAD_INDEX); n = max(0, min(n, a.cap - 1)); }
   const int nchunks = (n + 1 + kF32Chunk - 1) / kF32Chunk;
   if (chunk == 0 && tid == 0) a.lane_nseg[l] = nchunks;
-  if (chunk >= nchunks) return;
+  if (chunk >= nchunks) {
+    grid_dep_wait();
+    return;
+  }
   const int b = l / a.Hkv, kh = l % a.Hkv;
   const float* qb = static_cast<const float*>(a.q) + (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kh) * a.g) * D;
   for (int i = tid; i < a.g * D; i += blockDim.x) sq[i] = qb[i];
@@ -524,6 +543,8 @@ __global__ void __launch_bounds__(kF32Chunk) attend_f32_kernel(AttendArgs a, int
     a.part_ml[(base + tid) * 2 + 0] = sred[tid * 2 + 0];
     a.part_ml[(base + tid) * 2 + 1] = sred[tid * 2 + 1];
   }
+  grid_dep_wait();
+  grid_dep_launch();
 }
 
 }  // namespace
@@ -566,8 +587,9 @@ cudaError_t launch_attend(const Ctx& ctx, int layer, const void* q, const void* 
   AttendArgs a;
   a.k_pool = ls.k_pool; a.v_pool = ls.v_pool; a.slot = ls.slot; a.count = ls.count;
   a.q = q; a.k_new = k_new; a.v_new = v_new;
-  a.logits = ctx.ws.logits; a.part_o = ctx.ws.part_o; a.part_ml = ctx.ws.part_ml;
-  a.lane_nseg = ctx.ws.lane_nseg; a.status = ctx.ws.status;
+  const int c = layer & 1;
+  a.logits = ctx.ws.logits_buf[c]; a.part_o = ctx.ws.part_o_buf[c]; a.part_ml = ctx.ws.part_ml_buf[c];
+  a.lane_nseg = ctx.ws.lane_nseg_buf[c]; a.status = ctx.ws.status;
   a.lanes = dm.lanes; a.g = dm.g; a.Hkv = dm.Hkv; a.Hq = dm.Hq; a.cap = dm.cap; a.lcap = dm.lcap;
   a.P = dm.P;
   a.scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(dm.d));
@@ -575,20 +597,21 @@ cudaError_t launch_attend(const Ctx& ctx, int layer, const void* q, const void* 
     if (dm.lanes > kMaxLanesSmem) return cudaErrorInvalidValue;
     const int grid = ctx.sm_count * ctx.attend_ctas_per_sm;
     const int nt = dm.g > 8 ? 2 : 1;
+    const dim3 blk(kAttendWarps * 32);
     if (dm.d == 128 && nt == 1)
-      attend_bf16_kernel<128, 1><<<grid, kAttendWarps * 32, Bf16Cfg<128, 1>::kSmem, stream>>>(a);
+      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, Bf16Cfg<128, 1>::kSmem, stream, true, a);
     else if (dm.d == 128)
-      attend_bf16_kernel<128, 2><<<grid, kAttendWarps * 32, Bf16Cfg<128, 2>::kSmem, stream>>>(a);
+      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, Bf16Cfg<128, 2>::kSmem, stream, true, a);
     else if (nt == 1)
-      attend_bf16_kernel<64, 1><<<grid, kAttendWarps * 32, Bf16Cfg<64, 1>::kSmem, stream>>>(a);
+      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, Bf16Cfg<64, 1>::kSmem, stream, true, a);
     else
-      attend_bf16_kernel<64, 2><<<grid, kAttendWarps * 32, Bf16Cfg<64, 2>::kSmem, stream>>>(a);
+      return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, Bf16Cfg<64, 2>::kSmem, stream, true, a);
   } else {
     const int chunks = (dm.cap + kF32Chunk) / kF32Chunk;   // enough for n = cap - 1 plus the new token
     if (chunks > kMaxSeg) return cudaErrorInvalidValue;
     dim3 grid(chunks, dm.lanes);
     const size_t sm = (static_cast<size_t>(dm.g) * dm.d + dm.g * kF32Chunk + 2 * dm.g) * sizeof(float);
-    attend_f32_kernel<<<grid, kF32Chunk, sm, stream>>>(a, dm.d);
+    return launch_k(attend_f32_kernel, grid, dim3(kF32Chunk), sm, stream, true, a, dm.d);
   }
   return cudaGetLastError();
 }

@@ -28,7 +28,7 @@ struct EpiArgs {
   LayerState ls;
   Workspace ws;
   Dims dm;
-  int has_q, new_pos;
+  int has_q, new_pos, layer;
   const void* k_new; const void* v_new;
   float* out; float* lse; int32_t* victims; int32_t* n_victims;
 };
@@ -46,6 +46,8 @@ __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const 
 template <typename KT>
 __global__ void __launch_bounds__(kEpiThreads) decode_epilogue_kernel(EpiArgs A) {
   __shared__ int sh_scan[40];
+  grid_dep_wait();      // the attention kernel's results are complete and visible
+  grid_dep_launch();
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   LaneRefs L = lane_refs(A.ls, dm, l);
@@ -94,32 +96,40 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   if (tid == 0) sh_nan = 0;
 
   // ---- combine the split-K partials --------------------------------------
+  const int cbuf = A.layer & 1;
   if (A.has_q) {
-    const int nseg = min(A.ws.lane_nseg[l], kMaxSeg);
-    const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml) + static_cast<size_t>(l) * kMaxSeg * g;
-    if (tid < g) {
-      float M = -INFINITY;
-      for (int s = 0; s < nseg; ++s) M = fmaxf(M, ml[s * g + tid].x);
-      float Ls = 0.f;
-      for (int s = 0; s < nseg; ++s) {
-        const float2 v = ml[s * g + tid];
-        if (v.x != -INFINITY) Ls += v.y * exp2f(v.x - M);
+    __shared__ float sh_scale[kMaxSeg][kMaxG];
+    const int nseg = min(A.ws.lane_nseg_buf[cbuf][l], kMaxSeg);
+    const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp < g) {
+      // one warp per head; lanes hold segments lane and lane + 32
+      const int h = warp;
+      const float2 v0 = lane < nseg ? ml[lane * g + h] : make_float2(-INFINITY, 0.f);
+      const float2 v1 = lane + 32 < nseg ? ml[(lane + 32) * g + h] : make_float2(-INFINITY, 0.f);
+      const float M = warp_max(fmaxf(v0.x, v1.x));
+      const float s0 = v0.x == -INFINITY ? 0.f : exp2f(v0.x - M);
+      const float s1 = v1.x == -INFINITY ? 0.f : exp2f(v1.x - M);
+      if (lane < nseg) sh_scale[lane][h] = s0;
+      if (lane + 32 < nseg) sh_scale[lane + 32][h] = s1;
+      float Ls = v0.y * s0 + v1.y * s1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+      if (lane == 0) {
+        sh_M[h] = M;
+        sh_L[h] = Ls;
+        const float lse2 = M + log2f(Ls);
+        sh_lse2[h] = lse2;
+        A.lse[static_cast<size_t>(b) * dm.Hq + kh * g + h] = lse2 * kLn2;
       }
-      sh_M[tid] = M;
-      sh_L[tid] = Ls;
-      const float lse2 = M + log2f(Ls);
-      sh_lse2[tid] = lse2;
-      A.lse[static_cast<size_t>(b) * dm.Hq + kh * g + tid] = lse2 * kLn2;
     }
     __syncthreads();
-    const float* po = A.ws.part_o + static_cast<size_t>(l) * kMaxSeg * g * d;
+    const float* po = A.ws.part_o_buf[cbuf] + static_cast<size_t>(l) * kMaxSeg * g * d;
     for (int he = tid; he < g * d; he += blockDim.x) {
       const int h = he / d, e = he - h * d;
       float acc = 0.f;
-      for (int s = 0; s < nseg; ++s) {
-        const float m = ml[s * g + h].x;
-        if (m != -INFINITY) acc += po[(static_cast<size_t>(s) * g + h) * d + e] * exp2f(m - sh_M[h]);
-      }
+#pragma unroll 8
+      for (int s = 0; s < nseg; ++s) acc = fmaf(po[(static_cast<size_t>(s) * g + h) * d + e], sh_scale[s][h], acc);
       A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = acc / sh_L[h];
     }
   }
@@ -130,7 +140,7 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   const int rs = policy == KVEVICT_SNAPKV ? A.ls.ring_slot[l] : 0;
   double* keys64 = A.ws.keys64 ? A.ws.keys64 + static_cast<size_t>(l) * dm.cap : nullptr;
   double* pooled64 = A.ws.pooled64 ? A.ws.pooled64 + static_cast<size_t>(l) * dm.cap : nullptr;
-  const float* lg = A.ws.logits + static_cast<size_t>(l) * g * dm.lcap;
+  const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
   const int k = max(0, n + 1 - dm.budget);
   const int cut = A.new_pos - dm.R + 1;
   // k == 1 (a full cache in steady state): the minimum candidate (key,
@@ -374,6 +384,8 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(LayerState ls, Wor
                                                            const void* k_new, const void* v_new,
                                                            int mark_freed, int32_t* moves) {
   __shared__ int sh_scan[40];
+  grid_dep_launch();    // the next layer's attention may start (it touches other state)
+  grid_dep_wait();      // the epilogue and its allocator are complete
   const int l = blockIdx.x, tid = threadIdx.x;
   if (ws.counters[1] == 0) return;
   const int need = ws.need_admit[l];
@@ -483,26 +495,25 @@ cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, 
   A.dm = ctx.dims;
   A.has_q = has_q ? 1 : 0;
   A.new_pos = new_pos;
+  A.layer = layer;
   A.k_new = k_new; A.v_new = v_new;
   A.out = out; A.lse = lse; A.victims = victims; A.n_victims = n_victims;
   if (ctx.dims.dtype == KVEVICT_BF16)
-    decode_epilogue_kernel<__nv_bfloat16><<<ctx.dims.lanes, kEpiThreads, 0, stream>>>(A);
-  else
-    decode_epilogue_kernel<float><<<ctx.dims.lanes, kEpiThreads, 0, stream>>>(A);
-  return cudaGetLastError();
+    return launch_k(decode_epilogue_kernel<__nv_bfloat16>, dim3(ctx.dims.lanes), dim3(kEpiThreads), 0, stream, true, A);
+  return launch_k(decode_epilogue_kernel<float>, dim3(ctx.dims.lanes), dim3(kEpiThreads), 0, stream, true, A);
 }
 
 cudaError_t launch_allocate_apply(const Ctx& ctx, int layer, const void* k_new, const void* v_new,
                                   bool mark_freed, int32_t* moves, cudaStream_t stream, bool with_allocate) {
   LayerState ls = layer_state(ctx, layer);
   if (with_allocate) allocate_kernel<<<1, 1024, 0, stream>>>(ls, ctx.ws, ctx.dims);
+  const bool pdl = !with_allocate;   // in a decode step apply follows the epilogue directly
+  const int mf = mark_freed ? 1 : 0;
   if (ctx.dims.dtype == KVEVICT_BF16)
-    apply_kernel<__nv_bfloat16><<<ctx.dims.lanes, kApplyThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, k_new, v_new,
-                                                                              mark_freed ? 1 : 0, moves);
-  else
-    apply_kernel<float><<<ctx.dims.lanes, kApplyThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, k_new, v_new,
-                                                                     mark_freed ? 1 : 0, moves);
-  return cudaGetLastError();
+    return launch_k(apply_kernel<__nv_bfloat16>, dim3(ctx.dims.lanes), dim3(kApplyThreads), 0, stream, pdl, ls,
+                    ctx.ws, ctx.dims, k_new, v_new, mf, moves);
+  return launch_k(apply_kernel<float>, dim3(ctx.dims.lanes), dim3(kApplyThreads), 0, stream, pdl, ls, ctx.ws,
+                  ctx.dims, k_new, v_new, mf, moves);
 }
 
 }  // namespace kve

@@ -58,10 +58,12 @@ struct LayerState {
 struct Workspace {
   uint32_t* status;                // 1 word
   int32_t* work_flag;              // 1 word: any lane needs the allocator this call
-  float* logits;                   // [lanes][g][lcap] base-2 scaled logits
-  float* part_o;                   // [lanes][kMaxSeg][g][d]
-  float* part_ml;                  // [lanes][kMaxSeg][g][2]  (max, sum), base 2
-  int32_t* lane_nseg;              // [lanes]
+  // split-K scratch, two copies: layer l uses copy l & 1, so the attention of
+  // layer l+1 may overlap the epilogue of layer l
+  float* logits_buf[2];            // [lanes][g][lcap] base-2 scaled logits
+  float* part_o_buf[2];            // [lanes][kMaxSeg][g][d]
+  float* part_ml_buf[2];           // [lanes][kMaxSeg][g][2]  (max, sum), base 2
+  int32_t* lane_nseg_buf[2];       // [lanes]
   double* keys64;                  // [lanes][cap]  SnapKV window sums
   double* pooled64;                // [lanes][cap]  SnapKV pooled keys
   int32_t* need_admit;             // [lanes]
@@ -125,9 +127,30 @@ cudaError_t launch_epilogue(const Ctx&, int layer, bool has_q, int new_pos, cons
 cudaError_t launch_allocate_apply(const Ctx&, int layer, const void* k_new, const void* v_new,
                                   bool mark_freed, int32_t* moves, cudaStream_t, bool with_allocate);
 
+// Kernel launch with programmatic dependent launch allowed (the kernel may
+// start before its predecessor in the stream completes; it orders itself
+// with griddepcontrol.wait where it consumes the predecessor's results).
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_k(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                            bool pdl, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = pdl ? attr : nullptr;
+  cfg.numAttrs = pdl ? 1 : 0;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // ---------------------------------------------------------------------------
 // device helpers
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }
