@@ -20,7 +20,8 @@
 namespace kve {
 namespace {
 
-constexpr int kEpiThreads = 1024;
+constexpr int kEpiThreads = 512;
+constexpr int kFastPer = 8;     // tokens per thread on the one-victim H2O path
 constexpr int kApplyThreads = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -44,7 +45,7 @@ __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const 
                                int* sh_flag);
 
 template <typename KT>
-__global__ void __launch_bounds__(kEpiThreads) decode_epilogue_kernel(EpiArgs A) {
+__global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs A) {
   __shared__ int sh_scan[40];
   grid_dep_wait();      // the attention kernel's results are complete and visible
   grid_dep_launch();
@@ -132,6 +133,147 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       for (int s = 0; s < nseg; ++s) acc = fmaf(po[(static_cast<size_t>(s) * g + h) * d + e], sh_scale[s][h], acc);
       A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = acc / sh_L[h];
     }
+  }
+
+  // ---- H2O with at most one victim and a short lane: one batched pass ---------
+  // Every thread loads its tokens' logits, scores, positions and slots in
+  // one batch, computes the new scores and the candidate minimum from
+  // registers, and after the block-wide argmin writes each survivor straight
+  // to its index after the removal (one lower past the victim).
+  if (dm.policy == KVEVICT_H2O && n + 1 - dm.budget <= 1 && n <= kFastPer * static_cast<int>(blockDim.x) &&
+      g <= 8) {
+    const int k = max(0, n + 1 - dm.budget);
+    const int cut = A.new_pos - dm.R + 1;
+    const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
+    float lv[kFastPer][8];
+    float sc[kFastPer];
+    int ps[kFastPer], sl[kFastPer];
+#pragma unroll
+    for (int j = 0; j < kFastPer; ++j) {
+      const int i = tid + j * static_cast<int>(blockDim.x);
+      const bool ok = i < n;
+#pragma unroll
+      for (int h = 0; h < 8; ++h) lv[j][h] = (ok && A.has_q && h < g) ? __ldcs(lg + static_cast<size_t>(h) * dm.lcap + i) : -INFINITY;
+      sc[j] = ok ? L.score[i] : 0.f;
+      ps[j] = ok ? L.pos[i] : 0x7FFFFFFF;
+      sl[j] = ok ? L.slot[i] : -1;
+    }
+    unsigned long long best_k = ~0ull;
+    uint32_t best_p = 0xFFFFFFFFu;
+    int best_i = -1, nan_count = 0;
+#pragma unroll
+    for (int j = 0; j < kFastPer; ++j) {
+      const int i = tid + j * static_cast<int>(blockDim.x);
+      if (i < n) {
+        float w = 0.f;
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+          if (h < g) w += exp2f(lv[j][h] - sh_lse2[h]);
+        if (A.has_q) sc[j] += w;
+        if (sc[j] != sc[j]) ++nan_count;
+        if (k == 1 && ps[j] < cut) {
+          const unsigned long long kk = mono_key(sc[j]);
+          if (kk < best_k || (kk == best_k && static_cast<uint32_t>(ps[j]) < best_p)) {
+            best_k = kk; best_p = static_cast<uint32_t>(ps[j]); best_i = i;
+          }
+        }
+      }
+    }
+    const int v = (k == 1) ? block_argmin3(best_k, best_p, best_i, sh_hist, sh_misc) : -1;
+    if (tid == 0) { sh_misc[0] = -1; sh_misc[1] = -1; }
+    __syncthreads();
+    // scatter the survivors; the victim's owner releases its slot
+#pragma unroll
+    for (int j = 0; j < kFastPer; ++j) {
+      const int i = tid + j * static_cast<int>(blockDim.x);
+      if (i < n) {
+        if (i == v) {
+          A.victims[static_cast<size_t>(l) * dm.cap] = ps[j];
+          const int s = sl[j];
+          int dead_blk = -1;
+          if (s >= 0 && s < dm.P * kBlock) {
+            const int bb = s >> 4, bit = 1 << (s & 15);
+            const int old = atomicAnd(&L.mask[bb], ~bit);
+            if ((old & ~bit) == 0 && (old & bit)) {
+              L.owner[bb] = -1;
+              dead_blk = bb;
+            }
+          } else if (s >= 0) {
+            set_status(A.ws.status, ST_BAD_INDEX);
+          }
+          sh_misc[0] = dead_blk;
+          sh_misc[1] = s;
+        } else {
+          const int ni = (v >= 0 && i > v) ? i - 1 : i;
+          if (ni != i) {
+            L.pos[ni] = ps[j];
+            L.slot[ni] = sl[j];
+          }
+          L.score[ni] = sc[j];
+        }
+      }
+    }
+    if (nan_count) atomicAdd(&sh_nan, nan_count);
+    __syncthreads();
+    const int vcount = v >= 0 ? 1 : 0;
+    const int dead_blk = sh_misc[0], vslot = sh_misc[1];
+    int nb = *L.nblocks;
+    if (dead_blk >= 0) {
+      for (int j = tid; j < nb; j += blockDim.x) {
+        if (L.blocks[j] == dead_blk) {
+          L.blocks[j] = L.blocks[nb - 1];
+          *L.nblocks = nb - 1;
+        }
+      }
+      __syncthreads();
+      nb -= 1;
+    }
+    const int m = n - vcount;
+    // admission: the lowest free slot of the lane's blocks; with exactly one
+    // hole left and it being the victim's, no scan is needed
+    const int holes = nb * kBlock - m;
+    unsigned best = 0xFFFFFFFFu;
+    if (holes == 1 && vcount == 1 && dead_blk < 0 && vslot >= 0) {
+      best = static_cast<unsigned>(vslot);
+    } else if (holes > 0) {
+      for (int j = tid; j < nb; j += blockDim.x) {
+        const int blk = L.blocks[j];
+        const int mk = L.mask[blk] & 0xFFFF;
+        if (mk != 0xFFFF) best = min(best, static_cast<unsigned>(blk * kBlock + (__ffs(~mk) - 1)));
+      }
+      best = warp_min(best);
+      if ((tid & 31) == 0) sh_min[tid >> 5] = best;
+      __syncthreads();
+      best = 0xFFFFFFFFu;
+      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) best = min(best, sh_min[w]);
+    }
+    const bool need = best == 0xFFFFFFFFu;
+    if (!need) {
+      KT* kp = static_cast<KT*>(A.ls.k_pool);
+      KT* vp = static_cast<KT*>(A.ls.v_pool);
+      copy_row(kp + static_cast<size_t>(best) * d, static_cast<const KT*>(A.k_new) + static_cast<size_t>(l) * d, d);
+      copy_row(vp + static_cast<size_t>(best) * d, static_cast<const KT*>(A.v_new) + static_cast<size_t>(l) * d, d);
+    }
+    int t_live = 0;
+    const int ndst = lane_plan(L, nb, m + 1, false, dm.theta_f, need, &t_live, sh_scan);
+    if (tid == 0) {
+      if (!need) atomicOr(&L.mask[best >> 4], 1 << (best & 15));
+      L.pos[m] = A.new_pos;
+      L.slot[m] = need ? -1 : static_cast<int>(best);
+      L.score[m] = 0.f;
+      A.ls.count[l] = m + 1;
+      if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
+      A.n_victims[l] = vcount;
+      A.ws.need_admit[l] = need ? 1 : 0;
+      A.ws.want_dst[l] = ndst;
+      A.ws.plan_tlive[l] = t_live;
+      if (need || ndst > 0) atomicOr(A.ws.work_flag, 1);
+      if (vcount) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_VICTIMS]), 1ull);
+      if (dead_blk >= 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_FREED_DEAD]), 1ull);
+      if (sh_nan) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_NAN_KEYS]), (unsigned long long)sh_nan);
+      if (l == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_STEPS]), 1ull);
+    }
+    return;
   }
 
   // ---- weights -> score state; SnapKV window sums ----------------------------
