@@ -55,7 +55,9 @@ typedef enum {
   KVEVICT_E_DTYPE = 6,             /* unsupported kv or key dtype / head_dim */
   KVEVICT_E_CUDA = 7,              /* a CUDA runtime call failed */
   KVEVICT_E_TIMEOUT = 8,           /* a device-side bounded wait gave up */
-  KVEVICT_E_DEVICE = 9             /* the device status word has fault bits set */
+  KVEVICT_E_DEVICE = 9,            /* the device status word has fault bits set */
+  KVEVICT_E_SCRATCH_LIMIT = 10     /* kvevict_attend_static: the layer needs more scratch
+                                      than KVEVICT_STATIC_SCRATCH_BYTES */
 } kvevict_status;
 
 typedef enum { KVEVICT_H2O = 0, KVEVICT_SNAPKV = 1, KVEVICT_DROPKV = 2 } kvevict_policy;
@@ -254,6 +256,28 @@ kvevict_status kvevict_select(kvevict_ctx* ctx, const void* keys, int32_t key_dt
 kvevict_status kvevict_compact(kvevict_ctx* ctx, int layer, const int32_t* victims,
                                const int32_t* n_victims, int32_t* freed, int32_t* n_freed,
                                int32_t* moves, int32_t* n_moves, void* stream);
+
+/* Attention output and log-sum-exp of one layer without any scratch from the
+ * caller.  The pages have no counterpart to this call; it exists for callers
+ * that cannot allocate device memory: code running during CUDA-graph stream
+ * capture (cudaMalloc cannot be captured), hosts whose own allocator owns all
+ * device memory, and serving loops that ban allocation on the hot path
+ * because cudaMalloc synchronises the device.
+ * Computes, for every lane, what kvevict_decode_step writes to out
+ * [B][Hq][d] (fp32) and lse [B][Hq] (fp32) for the same q [B][Hq][d] and new
+ * token k_new/v_new [B][Hkv][d] (kv_dtype, all device pointers), and changes
+ * no engine state (no scores, no eviction, no admission).  Its scratch is
+ * one array of KVEVICT_STATIC_SCRATCH_BYTES compiled into the library, held
+ * on every GPU that loads the library until the process exits; a layer
+ * needing more returns KVEVICT_E_SCRATCH_LIMIT before anything is enqueued.
+ * It calls no cudaMalloc and no allocating routine.  The first call on a
+ * device looks up that array's device address (cudaGetSymbolAddress) with
+ * the device current; make that first call before any stream capture.
+ * Every call shares the array and it keeps the last call's contents (no
+ * part of it needs to start at zero); calls that overlap on the GPU race. */
+#define KVEVICT_STATIC_SCRATCH_BYTES (16u << 20)
+kvevict_status kvevict_attend_static(kvevict_ctx* ctx, int layer, const void* q, const void* k_new,
+                                     const void* v_new, float* out, float* lse, void* stream);
 
 /* Writes KVEVICT_NSTATS int64 counters of one layer to out (device). */
 kvevict_status kvevict_stats(kvevict_ctx* ctx, int layer, int64_t* out, void* stream);

@@ -16,7 +16,7 @@ KEY_F32, KEY_F64 = 0, 1
 
 STATUS = {0: "OK", 1: "E_INVALID_ARG", 2: "E_POOL_KERNEL_EVEN", 3: "E_RECENT_GE_BUDGET",
           4: "E_OBS_WINDOW_ZERO", 5: "E_NO_BLOCKS", 6: "E_DTYPE", 7: "E_CUDA", 8: "E_TIMEOUT",
-          9: "E_DEVICE"}
+          9: "E_DEVICE", 10: "E_SCRATCH_LIMIT"}
 STAT_NAMES = ["steps", "victims", "admit_new_block", "freed_dead", "freed_reloc", "moved", "plans",
               "deferred", "nan_keys", "blocks", "live", "half_empty", "lanes"]
 NSTATS = len(STAT_NAMES)
@@ -70,11 +70,13 @@ def lib():
         L.kvevict_attend.argtypes = [V, ctypes.c_int, V, V, V, V]
         L.kvevict_finish_step.argtypes = [V, ctypes.c_int, V, V, V, I, V, V, V, V, V]
         L.kvevict_score.argtypes = [V, ctypes.c_int, V, I, V, V, V, V, V]
+        L.kvevict_attend_static.argtypes = [V, ctypes.c_int, V, V, V, V, V, V]
         L.kvevict_select.argtypes = [V, V, I, V, V, I, I, I, I, V, V, V]
         L.kvevict_compact.argtypes = [V, ctypes.c_int, V, V, V, V, V, V, V]
         L.kvevict_stats.argtypes = [V, ctypes.c_int, V, V]
         L.kvevict_last_error.argtypes = [V, ctypes.c_char_p, ctypes.c_size_t]
         for f in ("validate", "create", "reset", "prefill", "decode_step", "attend", "finish_step",
+                  "attend_static",
                   "score", "select",
                   "compact", "stats", "last_error"):
             getattr(L, "kvevict_" + f).restype = ctypes.c_int
@@ -221,6 +223,18 @@ class Engine:
                                          _ptr(out), _ptr(lse), _ptr(victims), _ptr(n_victims),
                                          _stream(stream)), "kvevict_finish_step")
         return out, lse, victims, n_victims
+
+    def attend_static(self, layer, q, k_new, v_new, out=None, lse=None, stream=None):
+        """kvevict_attend_static: attention output and LSE of one layer using the
+        library's built-in scratch array (no workspace, no allocation inside)."""
+        c = self.cfg
+        if out is None:
+            out = torch.empty((c.batch, c.num_q_heads, c.head_dim), dtype=torch.float32, device=self.device)
+        if lse is None:
+            lse = torch.empty((c.batch, c.num_q_heads), dtype=torch.float32, device=self.device)
+        _check(lib().kvevict_attend_static(self.h, layer, _ptr(q), _ptr(k_new), _ptr(v_new), _ptr(out), _ptr(lse),
+                                           _stream(stream)), "kvevict_attend_static")
+        return out, lse
 
     def score(self, layer, q_win, q_pos, lse=None, a_out=None, scores=None, stream=None):
         c = self.cfg

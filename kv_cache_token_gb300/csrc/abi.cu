@@ -7,10 +7,6 @@
 
 #include "kvevict_internal.cuh"
 
-struct kvevict_ctx {
-  kve::Ctx c;
-};
-
 namespace kve {
 
 namespace {

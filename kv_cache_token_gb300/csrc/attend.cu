@@ -616,4 +616,38 @@ cudaError_t launch_attend(const Ctx& ctx, int layer, const void* q, const void* 
   return cudaGetLastError();
 }
 
+// The same attention kernels writing their split-K scratch to caller-chosen
+// buffers (used by the entry point that allocates nothing); ordinary launch.
+cudaError_t launch_attend_into(const Ctx& ctx, int layer, const void* q, const void* k_new, const void* v_new,
+                               float* logits, float* part_o, float* part_ml, int32_t* lane_nseg,
+                               cudaStream_t stream) {
+  const Dims& dm = ctx.dims;
+  LayerState ls = layer_state(ctx, layer);
+  AttendArgs a;
+  a.k_pool = ls.k_pool; a.v_pool = ls.v_pool; a.slot = ls.slot; a.count = ls.count;
+  a.q = q; a.k_new = k_new; a.v_new = v_new;
+  a.logits = logits; a.part_o = part_o; a.part_ml = part_ml; a.lane_nseg = lane_nseg;
+  a.status = ctx.ws.status;
+  a.lanes = dm.lanes; a.g = dm.g; a.Hkv = dm.Hkv; a.Hq = dm.Hq; a.cap = dm.cap; a.lcap = dm.lcap;
+  a.P = dm.P;
+  a.scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(dm.d));
+  if (dm.dtype == KVEVICT_BF16) {
+    if (dm.lanes > kMaxLanesSmem) return cudaErrorInvalidValue;
+    const int grid = ctx.sm_count * ctx.attend_ctas_per_sm;
+    const int nt = dm.g > 8 ? 2 : 1;
+    const dim3 blk(kAttendWarps * 32);
+    if (dm.d == 128 && nt == 1)
+      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, Bf16Cfg<128, 1>::kSmem, stream, false, a);
+    else if (dm.d == 128)
+      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, Bf16Cfg<128, 2>::kSmem, stream, false, a);
+    else if (nt == 1)
+      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, Bf16Cfg<64, 1>::kSmem, stream, false, a);
+    return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, Bf16Cfg<64, 2>::kSmem, stream, false, a);
+  }
+  const int chunks = (dm.cap + kF32Chunk) / kF32Chunk;
+  if (chunks > kMaxSeg) return cudaErrorInvalidValue;
+  const size_t sm = (static_cast<size_t>(dm.g) * dm.d + dm.g * kF32Chunk + 2 * dm.g) * sizeof(float);
+  return launch_k(attend_f32_kernel, dim3(chunks, dm.lanes), dim3(kF32Chunk), sm, stream, false, a, dm.d);
+}
+
 }  // namespace kve

@@ -118,6 +118,8 @@ cudaError_t launch_compact(const Ctx&, int layer, const int32_t* victims, const 
 cudaError_t launch_score(const Ctx&, int layer, const void* q_win, int w, const int32_t* q_pos,
                          float* lse, float* a_out, float* scores, cudaStream_t);
 cudaError_t launch_stats(const Ctx&, int layer, long long* out, cudaStream_t);
+cudaError_t launch_attend_into(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
+                               float* logits, float* part_o, float* part_ml, int32_t* lane_nseg, cudaStream_t);
 cudaError_t prepare_kernels(Ctx&);   // one-time kernel attributes and occupancy (not stream work)
 cudaError_t launch_attend(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
                           cudaStream_t);
@@ -353,3 +355,8 @@ __device__ SelectResult block_bottom_k(int n, int k, int key_bits, KeyFn keyf, P
 }
 
 }  // namespace kve
+
+// The opaque handle of the C ABI.
+struct kvevict_ctx {
+  kve::Ctx c;
+};
