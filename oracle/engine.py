@@ -55,8 +55,8 @@ class Engine:
     def prefill(self, layer, K, V):
         """K, V [B, Hkv, n, d]."""
         B, H = self.cfg.batch, self.cfg.num_kv_heads
-        Ks = [np.asarray(K[b, h], dtype=np.float64) for b in range(B) for h in range(H)]
-        Vs = [np.asarray(V[b, h], dtype=np.float64) for b in range(B) for h in range(H)]
+        Ks = [np.asarray(K[b, h]) for b in range(B) for h in range(H)]
+        Vs = [np.asarray(V[b, h]) for b in range(B) for h in range(H)]
         self.layers[layer].prefill(Ks, Vs)
 
     def lane_keys(self, L, n_new=1):

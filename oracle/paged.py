@@ -133,13 +133,14 @@ class PagedLayer:
             L = self.lanes[lane]
             for b in blocks:
                 self.assign(b, lane)
-            for i in range(n):
-                slot = slot_of(blocks[i // BLOCK], i % BLOCK)
-                self.live[slot // BLOCK, slot % BLOCK] = True
-                self.write_row(slot, Kctx[lane][i], Vctx[lane][i])
-            L.pos = np.arange(n, dtype=np.int64)
-            L.slot = np.array([slot_of(blocks[i // BLOCK], i % BLOCK) for i in range(n)],
-                              dtype=np.int64)
+            i = np.arange(n)
+            blk, off = blocks[i // BLOCK], i % BLOCK          # Eq. (2): slot = block * S + offset
+            self.live[blk, off] = True
+            if self.store_kv:
+                self.K[blk, off] = Kctx[lane]
+                self.V[blk, off] = Vctx[lane]
+            L.pos = i.astype(np.int64)
+            L.slot = (blk * BLOCK + off).astype(np.int64)
             L.score = np.zeros(n)
             L.hist = np.zeros((n, L.hist.shape[1]), np.float32)
             L.ring_slot = 0
