@@ -137,14 +137,11 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
                                             const int t_begin, const int t_end, unsigned char* wbuf,
                                             uint64_t* bars);
 
-// __launch_bounds__(.., 4) caps the kernel at 128 registers so that one CTA
-// of the (small) epilogue kernel fits beside three of these on an SM: the
-// epilogue of layer l then runs while layer l+1 streams.
 template <int D, int NT>
-__global__ void __launch_bounds__(kAttendWarps * 32, 4) attend_bf16_kernel(AttendArgs a) {
+__global__ void __launch_bounds__(kAttendWarps * 32, 3) attend_bf16_kernel(AttendArgs a) {
   using C = Bf16Cfg<D, NT>;
   extern __shared__ __align__(128) unsigned char smem[];
-  int* sh_prefix = reinterpret_cast<int*>(smem + C::kSmem);     // lanes + 1 entries after the warp buffers
+  __shared__ int sh_prefix[kMaxLanesSmem + 1];
   __shared__ int sh_scan[40];
   __shared__ uint64_t sh_bar[kAttendWarps][kAttStages];
 
@@ -553,21 +550,16 @@ __global__ void __launch_bounds__(kF32Chunk) attend_f32_kernel(AttendArgs a, int
 }  // namespace
 
 template <int D, int NT>
-static size_t attend_smem(int lanes) {
-  return Bf16Cfg<D, NT>::kSmem + static_cast<size_t>(lanes + 1) * sizeof(int);
-}
-
-template <int D, int NT>
 static cudaError_t set_attr() {
   return cudaFuncSetAttribute(attend_bf16_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              attend_smem<D, NT>(kMaxLanesSmem));
+                              Bf16Cfg<D, NT>::kSmem);
 }
 
 template <int D, int NT>
-static int ctas_per_sm(int lanes) {
+static int ctas_per_sm() {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_bf16_kernel<D, NT>, kAttendWarps * 32,
-                                                    attend_smem<D, NT>(lanes)) != cudaSuccess)
+                                                    Bf16Cfg<D, NT>::kSmem) != cudaSuccess)
     return 0;
   return n;
 }
@@ -582,9 +574,8 @@ cudaError_t prepare_kernels(Ctx& ctx) {
   const int nt = dm.g > 8 ? 2 : 1;
   ctx.attend_ctas_per_sm = 1;
   if (dm.dtype == KVEVICT_BF16) {
-    const int L = dm.lanes;
-    if (dm.d == 128) ctx.attend_ctas_per_sm = nt == 1 ? ctas_per_sm<128, 1>(L) : ctas_per_sm<128, 2>(L);
-    else ctx.attend_ctas_per_sm = nt == 1 ? ctas_per_sm<64, 1>(L) : ctas_per_sm<64, 2>(L);
+    if (dm.d == 128) ctx.attend_ctas_per_sm = nt == 1 ? ctas_per_sm<128, 1>() : ctas_per_sm<128, 2>();
+    else ctx.attend_ctas_per_sm = nt == 1 ? ctas_per_sm<64, 1>() : ctas_per_sm<64, 2>();
   }
   return cudaGetLastError();
 }
@@ -608,13 +599,13 @@ cudaError_t launch_attend(const Ctx& ctx, int layer, const void* q, const void* 
     const int nt = dm.g > 8 ? 2 : 1;
     const dim3 blk(kAttendWarps * 32);
     if (dm.d == 128 && nt == 1)
-      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, attend_smem<128, 1>(dm.lanes), stream, true, a);
+      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, Bf16Cfg<128, 1>::kSmem, stream, true, a);
     else if (dm.d == 128)
-      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, attend_smem<128, 2>(dm.lanes), stream, true, a);
+      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, Bf16Cfg<128, 2>::kSmem, stream, true, a);
     else if (nt == 1)
-      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, attend_smem<64, 1>(dm.lanes), stream, true, a);
+      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, Bf16Cfg<64, 1>::kSmem, stream, true, a);
     else
-      return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, attend_smem<64, 2>(dm.lanes), stream, true, a);
+      return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, Bf16Cfg<64, 2>::kSmem, stream, true, a);
   } else {
     const int chunks = (dm.cap + kF32Chunk) / kF32Chunk;   // enough for n = cap - 1 plus the new token
     if (chunks > kMaxSeg) return cudaErrorInvalidValue;
@@ -646,12 +637,12 @@ cudaError_t launch_attend_into(const Ctx& ctx, int layer, const void* q, const v
     const int nt = dm.g > 8 ? 2 : 1;
     const dim3 blk(kAttendWarps * 32);
     if (dm.d == 128 && nt == 1)
-      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, attend_smem<128, 1>(dm.lanes), stream, false, a);
+      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, Bf16Cfg<128, 1>::kSmem, stream, false, a);
     else if (dm.d == 128)
-      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, attend_smem<128, 2>(dm.lanes), stream, false, a);
+      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, Bf16Cfg<128, 2>::kSmem, stream, false, a);
     else if (nt == 1)
-      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, attend_smem<64, 1>(dm.lanes), stream, false, a);
-    return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, attend_smem<64, 2>(dm.lanes), stream, false, a);
+      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, Bf16Cfg<64, 1>::kSmem, stream, false, a);
+    return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, Bf16Cfg<64, 2>::kSmem, stream, false, a);
   }
   const int chunks = (dm.cap + kF32Chunk) / kF32Chunk;
   if (chunks > kMaxSeg) return cudaErrorInvalidValue;

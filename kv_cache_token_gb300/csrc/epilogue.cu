@@ -20,14 +20,9 @@
 namespace kve {
 namespace {
 
-// The epilogue is small on purpose (4 warps, <= 128 registers, ~6 KB of
-// static shared memory): one of its CTAs fits beside three CTAs of the
-// attention kernel, so with programmatic dependent launch the bookkeeping of
-// layer l runs while layer l+1 streams its K/V.
-constexpr int kEpiThreads = 128;
-constexpr int kFastPer = 4;     // tokens per thread per batch on the one-victim H2O path
-constexpr int kApplyThreads = 128;
-constexpr int kApplyCtas = 16;   // CTAs of the apply kernel; they loop over the lanes
+constexpr int kEpiThreads = 512;
+constexpr int kFastPer = 8;     // tokens per thread on the one-victim H2O path
+constexpr int kApplyThreads = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct EpiArgs {
@@ -50,7 +45,7 @@ __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const 
                                int* sh_flag);
 
 template <typename KT>
-__global__ void __launch_bounds__(kEpiThreads, 4) decode_epilogue_kernel(EpiArgs A) {
+__global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs A) {
   __shared__ int sh_scan[40];
   grid_dep_wait();      // the attention kernel's results are complete and visible
   grid_dep_launch();
@@ -95,7 +90,7 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   __shared__ int sh_idx[kEpiThreads];
   __shared__ unsigned sh_min[32];
   __shared__ int sh_nan;
-  extern __shared__ __align__(16) float sh_rows[];   // SnapKV history staging: 128 rows x W floats
+  __shared__ __align__(16) float sh_rows[128 * kMaxW];
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
@@ -108,8 +103,9 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
     const int nseg = min(A.ws.lane_nseg_buf[cbuf][l], kMaxSeg);
     const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
     const int warp = tid >> 5, lane = tid & 31;
-    for (int h = warp; h < g; h += blockDim.x >> 5) {
+    if (warp < g) {
       // one warp per head; lanes hold segments lane and lane + 32
+      const int h = warp;
       const float2 v0 = lane < nseg ? ml[lane * g + h] : make_float2(-INFINITY, 0.f);
       const float2 v1 = lane + 32 < nseg ? ml[(lane + 32) * g + h] : make_float2(-INFINITY, 0.f);
       const float M = warp_max(fmaxf(v0.x, v1.x));
@@ -139,105 +135,88 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
     }
   }
 
-  // ---- H2O with at most one victim (the steady state of a full cache) --------
-  // Pass 1 reads every token's logits, score and position in batches of
-  // kFastPer tokens per thread (all loads of a batch in flight together),
-  // writes the new scores and keeps the candidate minimum in registers; after
-  // the block-wide argmin, pass 2 moves the entries behind the victim one
-  // index down.
-  if (dm.policy == KVEVICT_H2O && n + 1 - dm.budget <= 1 && g <= 8) {
+  // ---- H2O with at most one victim and a short lane: one batched pass ---------
+  // Every thread loads its tokens' logits, scores, positions and slots in
+  // one batch, computes the new scores and the candidate minimum from
+  // registers, and after the block-wide argmin writes each survivor straight
+  // to its index after the removal (one lower past the victim).
+  if (dm.policy == KVEVICT_H2O && n + 1 - dm.budget <= 1 && n <= kFastPer * static_cast<int>(blockDim.x) &&
+      g <= 8) {
     const int k = max(0, n + 1 - dm.budget);
     const int cut = A.new_pos - dm.R + 1;
     const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
-    const int step = kFastPer * static_cast<int>(blockDim.x);
+    float lv[kFastPer][8];
+    float sc[kFastPer];
+    int ps[kFastPer], sl[kFastPer];
+#pragma unroll
+    for (int j = 0; j < kFastPer; ++j) {
+      const int i = tid + j * static_cast<int>(blockDim.x);
+      const bool ok = i < n;
+#pragma unroll
+      for (int h = 0; h < 8; ++h) lv[j][h] = (ok && A.has_q && h < g) ? __ldcs(lg + static_cast<size_t>(h) * dm.lcap + i) : -INFINITY;
+      sc[j] = ok ? L.score[i] : 0.f;
+      ps[j] = ok ? L.pos[i] : 0x7FFFFFFF;
+      sl[j] = ok ? L.slot[i] : -1;
+    }
     unsigned long long best_k = ~0ull;
     uint32_t best_p = 0xFFFFFFFFu;
     int best_i = -1, nan_count = 0;
-    for (int base = 0; base < n; base += step) {
-      float lv[kFastPer][8];
-      float sc[kFastPer];
-      int ps[kFastPer];
 #pragma unroll
-      for (int j = 0; j < kFastPer; ++j) {
-        const int i = base + tid + j * static_cast<int>(blockDim.x);
-        const bool ok = i < n;
+    for (int j = 0; j < kFastPer; ++j) {
+      const int i = tid + j * static_cast<int>(blockDim.x);
+      if (i < n) {
+        float w = 0.f;
 #pragma unroll
         for (int h = 0; h < 8; ++h)
-          lv[j][h] = (ok && A.has_q && h < g) ? __ldcs(lg + static_cast<size_t>(h) * dm.lcap + i) : -INFINITY;
-        sc[j] = ok ? L.score[i] : 0.f;
-        ps[j] = ok ? L.pos[i] : 0x7FFFFFFF;
-      }
-#pragma unroll
-      for (int j = 0; j < kFastPer; ++j) {
-        const int i = base + tid + j * static_cast<int>(blockDim.x);
-        if (i < n) {
-          if (A.has_q) {
-            float w = 0.f;
-#pragma unroll
-            for (int h = 0; h < 8; ++h)
-              if (h < g) w += exp2f(lv[j][h] - sh_lse2[h]);
-            sc[j] += w;
-            L.score[i] = sc[j];
-          }
-          if (sc[j] != sc[j]) ++nan_count;
-          if (k == 1 && ps[j] < cut) {
-            const unsigned long long kk = mono_key(sc[j]);
-            if (kk < best_k || (kk == best_k && static_cast<uint32_t>(ps[j]) < best_p)) {
-              best_k = kk; best_p = static_cast<uint32_t>(ps[j]); best_i = i;
-            }
+          if (h < g) w += exp2f(lv[j][h] - sh_lse2[h]);
+        if (A.has_q) sc[j] += w;
+        if (sc[j] != sc[j]) ++nan_count;
+        if (k == 1 && ps[j] < cut) {
+          const unsigned long long kk = mono_key(sc[j]);
+          if (kk < best_k || (kk == best_k && static_cast<uint32_t>(ps[j]) < best_p)) {
+            best_k = kk; best_p = static_cast<uint32_t>(ps[j]); best_i = i;
           }
         }
       }
     }
     const int v = (k == 1) ? block_argmin3(best_k, best_p, best_i, sh_hist, sh_misc) : -1;
-    int vcount = 0, dead_blk = -1, vslot = -1;
-    if (v >= 0) {
-      vcount = 1;
-      // the victim's slot and position are read before the shift overwrites index v
-      if (tid == 0) {
-        const int s = L.slot[v];
-        A.victims[static_cast<size_t>(l) * dm.cap] = L.pos[v];
-        if (s >= 0 && s < dm.P * kBlock) {
-          const int bb = s >> 4, bit = 1 << (s & 15);
-          const int old = atomicAnd(&L.mask[bb], ~bit);
-          if ((old & ~bit) == 0 && (old & bit)) {
-            L.owner[bb] = -1;
-            dead_blk = bb;
-          }
-        } else if (s >= 0) {
-          set_status(A.ws.status, ST_BAD_INDEX);
-        }
-        sh_misc[0] = dead_blk;
-        sh_misc[1] = s;
-      }
-      for (int base = v + 1; base < n; base += step) {
-        int ps[kFastPer], sl[kFastPer];
-        float sc[kFastPer];
+    if (tid == 0) { sh_misc[0] = -1; sh_misc[1] = -1; }
+    __syncthreads();
+    // scatter the survivors; the victim's owner releases its slot
 #pragma unroll
-        for (int j = 0; j < kFastPer; ++j) {
-          const int i = base + tid + j * static_cast<int>(blockDim.x);
-          if (i < n) {
-            ps[j] = L.pos[i];
-            sl[j] = L.slot[i];
-            sc[j] = L.score[i];
+    for (int j = 0; j < kFastPer; ++j) {
+      const int i = tid + j * static_cast<int>(blockDim.x);
+      if (i < n) {
+        if (i == v) {
+          A.victims[static_cast<size_t>(l) * dm.cap] = ps[j];
+          const int s = sl[j];
+          int dead_blk = -1;
+          if (s >= 0 && s < dm.P * kBlock) {
+            const int bb = s >> 4, bit = 1 << (s & 15);
+            const int old = atomicAnd(&L.mask[bb], ~bit);
+            if ((old & ~bit) == 0 && (old & bit)) {
+              L.owner[bb] = -1;
+              dead_blk = bb;
+            }
+          } else if (s >= 0) {
+            set_status(A.ws.status, ST_BAD_INDEX);
           }
-        }
-        __syncthreads();
-#pragma unroll
-        for (int j = 0; j < kFastPer; ++j) {
-          const int i = base + tid + j * static_cast<int>(blockDim.x);
-          if (i < n) {
-            L.pos[i - 1] = ps[j];
-            L.slot[i - 1] = sl[j];
-            L.score[i - 1] = sc[j];
+          sh_misc[0] = dead_blk;
+          sh_misc[1] = s;
+        } else {
+          const int ni = (v >= 0 && i > v) ? i - 1 : i;
+          if (ni != i) {
+            L.pos[ni] = ps[j];
+            L.slot[ni] = sl[j];
           }
+          L.score[ni] = sc[j];
         }
       }
-      __syncthreads();
-      dead_blk = sh_misc[0];
-      vslot = sh_misc[1];
     }
     if (nan_count) atomicAdd(&sh_nan, nan_count);
+    __syncthreads();
+    const int vcount = v >= 0 ? 1 : 0;
+    const int dead_blk = sh_misc[0], vslot = sh_misc[1];
     int nb = *L.nblocks;
     if (dead_blk >= 0) {
       for (int j = tid; j < nb; j += blockDim.x) {
@@ -246,9 +225,9 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
           *L.nblocks = nb - 1;
         }
       }
+      __syncthreads();
       nb -= 1;
     }
-    __syncthreads();
     const int m = n - vcount;
     // admission: the lowest free slot of the lane's blocks; with exactly one
     // hole left and it being the victim's, no scan is needed
@@ -543,30 +522,14 @@ __global__ void __launch_bounds__(1024) allocate_kernel(LayerState ls, Workspace
 // apply: one CTA per lane
 // ---------------------------------------------------------------------------
 template <typename KT>
-__device__ __forceinline__ void apply_lane(const LayerState& ls, const Workspace& ws, const Dims& dm, const void* k_new,
-                                           const void* v_new, int mark_freed, int32_t* moves, const int l,
-                                           int* sh_scan);
-
-template <typename KT>
 __global__ void __launch_bounds__(kApplyThreads) apply_kernel(LayerState ls, Workspace ws, Dims dm,
                                                            const void* k_new, const void* v_new,
                                                            int mark_freed, int32_t* moves) {
   __shared__ int sh_scan[40];
   grid_dep_launch();    // the next layer's attention may start (it touches other state)
   grid_dep_wait();      // the epilogue and its allocator are complete
+  const int l = blockIdx.x, tid = threadIdx.x;
   if (ws.counters[1] == 0) return;
-  for (int l = blockIdx.x; l < dm.lanes; l += gridDim.x) {
-    apply_lane<KT>(ls, ws, dm, k_new, v_new, mark_freed, moves, l, sh_scan);
-    __syncthreads();
-  }
-}
-
-// Admission into a fresh block and the relocation plan of one lane.
-template <typename KT>
-__device__ __forceinline__ void apply_lane(const LayerState& ls, const Workspace& ws, const Dims& dm, const void* k_new,
-                                           const void* v_new, int mark_freed, int32_t* moves, const int l,
-                                           int* sh_scan) {
-  const int tid = threadIdx.x;
   const int need = ws.need_admit[l];
   const int ndst = ws.want_dst[l];
   if (!need && ndst == 0) return;
@@ -675,13 +638,11 @@ cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, 
   A.has_q = has_q ? 1 : 0;
   A.new_pos = new_pos;
   A.layer = layer;
-  const size_t rows_smem = ctx.dims.policy == KVEVICT_SNAPKV ? static_cast<size_t>(128) * ctx.dims.W * sizeof(float) : 0;
   A.k_new = k_new; A.v_new = v_new;
   A.out = out; A.lse = lse; A.victims = victims; A.n_victims = n_victims;
   if (ctx.dims.dtype == KVEVICT_BF16)
-    return launch_k(decode_epilogue_kernel<__nv_bfloat16>, dim3(ctx.dims.lanes), dim3(kEpiThreads), rows_smem, stream,
-                    true, A);
-  return launch_k(decode_epilogue_kernel<float>, dim3(ctx.dims.lanes), dim3(kEpiThreads), rows_smem, stream, true, A);
+    return launch_k(decode_epilogue_kernel<__nv_bfloat16>, dim3(ctx.dims.lanes), dim3(kEpiThreads), 0, stream, true, A);
+  return launch_k(decode_epilogue_kernel<float>, dim3(ctx.dims.lanes), dim3(kEpiThreads), 0, stream, true, A);
 }
 
 cudaError_t launch_allocate_apply(const Ctx& ctx, int layer, const void* k_new, const void* v_new,
@@ -690,11 +651,10 @@ cudaError_t launch_allocate_apply(const Ctx& ctx, int layer, const void* k_new, 
   if (with_allocate) allocate_kernel<<<1, 1024, 0, stream>>>(ls, ctx.ws, ctx.dims);
   const bool pdl = !with_allocate;   // in a decode step apply follows the epilogue directly
   const int mf = mark_freed ? 1 : 0;
-  const dim3 grid(ctx.dims.lanes < kApplyCtas ? ctx.dims.lanes : kApplyCtas);
   if (ctx.dims.dtype == KVEVICT_BF16)
-    return launch_k(apply_kernel<__nv_bfloat16>, grid, dim3(kApplyThreads), 0, stream, pdl, ls,
+    return launch_k(apply_kernel<__nv_bfloat16>, dim3(ctx.dims.lanes), dim3(kApplyThreads), 0, stream, pdl, ls,
                     ctx.ws, ctx.dims, k_new, v_new, mf, moves);
-  return launch_k(apply_kernel<float>, grid, dim3(kApplyThreads), 0, stream, pdl, ls, ctx.ws,
+  return launch_k(apply_kernel<float>, dim3(ctx.dims.lanes), dim3(kApplyThreads), 0, stream, pdl, ls, ctx.ws,
                   ctx.dims, k_new, v_new, mf, moves);
 }
 
