@@ -21,7 +21,7 @@ namespace kve {
 namespace {
 
 constexpr int kEpiThreads = 512;
-constexpr int kFastPer = 8;     // tokens per thread on the one-victim H2O path
+constexpr int kFastPer = 7;     // tokens per thread on the one-victim H2O path
 constexpr int kApplyThreads = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -90,61 +90,35 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   __shared__ int sh_idx[kEpiThreads];
   __shared__ unsigned sh_min[32];
   __shared__ int sh_nan;
+  __shared__ float sh_scale[kMaxSeg][kMaxG];
   __shared__ __align__(16) float sh_rows[128 * kMaxW];
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
   if (tid == 0) sh_nan = 0;
 
-  // ---- combine the split-K partials --------------------------------------
+  // ---- H2O with at most one victim (the steady state of a full cache) --------
+  // One batched pass with every independent load issued up front: the
+  // split-K statistics (read for all kMaxSeg segments, masked afterwards),
+  // each thread's kFastPer tokens (logits, score, position, slot) and the
+  // lane's block count.  Weights, new scores and the candidate minimum come
+  // from registers; the partial outputs for `out` are loaded while the
+  // argmin's barriers run; survivors are written straight to their index
+  // after the removal.
   const int cbuf = A.layer & 1;
-  if (A.has_q) {
-    __shared__ float sh_scale[kMaxSeg][kMaxG];
-    const int nseg = min(A.ws.lane_nseg_buf[cbuf][l], kMaxSeg);
-    const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
-    const int warp = tid >> 5, lane = tid & 31;
-    if (warp < g) {
-      // one warp per head; lanes hold segments lane and lane + 32
-      const int h = warp;
-      const float2 v0 = lane < nseg ? ml[lane * g + h] : make_float2(-INFINITY, 0.f);
-      const float2 v1 = lane + 32 < nseg ? ml[(lane + 32) * g + h] : make_float2(-INFINITY, 0.f);
-      const float M = warp_max(fmaxf(v0.x, v1.x));
-      const float s0 = v0.x == -INFINITY ? 0.f : exp2f(v0.x - M);
-      const float s1 = v1.x == -INFINITY ? 0.f : exp2f(v1.x - M);
-      if (lane < nseg) sh_scale[lane][h] = s0;
-      if (lane + 32 < nseg) sh_scale[lane + 32][h] = s1;
-      float Ls = v0.y * s0 + v1.y * s1;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-      if (lane == 0) {
-        sh_M[h] = M;
-        sh_L[h] = Ls;
-        const float lse2 = M + log2f(Ls);
-        sh_lse2[h] = lse2;
-        A.lse[static_cast<size_t>(b) * dm.Hq + kh * g + h] = lse2 * kLn2;
-      }
-    }
-    __syncthreads();
-    const float* po = A.ws.part_o_buf[cbuf] + static_cast<size_t>(l) * kMaxSeg * g * d;
-    for (int he = tid; he < g * d; he += blockDim.x) {
-      const int h = he / d, e = he - h * d;
-      float acc = 0.f;
-#pragma unroll 8
-      for (int s = 0; s < nseg; ++s) acc = fmaf(po[(static_cast<size_t>(s) * g + h) * d + e], sh_scale[s][h], acc);
-      A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = acc / sh_L[h];
-    }
-  }
-
-  // ---- H2O with at most one victim and a short lane: one batched pass ---------
-  // Every thread loads its tokens' logits, scores, positions and slots in
-  // one batch, computes the new scores and the candidate minimum from
-  // registers, and after the block-wide argmin writes each survivor straight
-  // to its index after the removal (one lower past the victim).
   if (dm.policy == KVEVICT_H2O && n + 1 - dm.budget <= 1 && n <= kFastPer * static_cast<int>(blockDim.x) &&
       g <= 8) {
     const int k = max(0, n + 1 - dm.budget);
     const int cut = A.new_pos - dm.R + 1;
+    const int warp = tid >> 5, lane = tid & 31;
     const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
+    const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
+    const int nseg = A.has_q ? min(A.ws.lane_nseg_buf[cbuf][l], kMaxSeg) : 0;
+    float2 m0 = make_float2(-INFINITY, 0.f), m1 = make_float2(-INFINITY, 0.f);
+    if (A.has_q && warp < g) {
+      m0 = ml[lane * g + warp];
+      m1 = ml[(lane + 32) * g + warp];
+    }
     float lv[kFastPer][8];
     float sc[kFastPer];
     int ps[kFastPer], sl[kFastPer];
@@ -158,6 +132,28 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       ps[j] = ok ? L.pos[i] : 0x7FFFFFFF;
       sl[j] = ok ? L.slot[i] : -1;
     }
+    int nb = *L.nblocks;
+    // per-head log-sum-exp of the split-K segments (one warp per head)
+    if (A.has_q && warp < g) {
+      const int h = warp;
+      if (lane >= nseg) m0 = make_float2(-INFINITY, 0.f);
+      if (lane + 32 >= nseg) m1 = make_float2(-INFINITY, 0.f);
+      const float M = warp_max(fmaxf(m0.x, m1.x));
+      const float s0 = m0.x == -INFINITY ? 0.f : exp2f(m0.x - M);
+      const float s1 = m1.x == -INFINITY ? 0.f : exp2f(m1.x - M);
+      sh_scale[lane][h] = s0;
+      sh_scale[lane + 32][h] = s1;
+      float Ls = m0.y * s0 + m1.y * s1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+      if (lane == 0) {
+        sh_L[h] = Ls;
+        const float lse2 = M + log2f(Ls);
+        sh_lse2[h] = lse2;
+        A.lse[static_cast<size_t>(b) * dm.Hq + kh * g + h] = lse2 * kLn2;
+      }
+    }
+    __syncthreads();
     unsigned long long best_k = ~0ull;
     uint32_t best_p = 0xFFFFFFFFu;
     int best_i = -1, nan_count = 0;
@@ -179,7 +175,33 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
         }
       }
     }
+    // partial outputs of the split-K segments, in flight during the argmin
+    const float* po = A.ws.part_o_buf[cbuf] + static_cast<size_t>(l) * kMaxSeg * g * d;
+    constexpr int kOutPer = 2;          // outputs per thread (g * d <= 1024)
+    float pov[kOutPer][16];
+#pragma unroll
+    for (int u = 0; u < kOutPer; ++u) {
+      const int he = tid + u * static_cast<int>(blockDim.x);
+      const int h = he / d, e = he - (he / d) * d;
+#pragma unroll
+      for (int s2 = 0; s2 < 16; ++s2)
+        pov[u][s2] = (A.has_q && he < g * d && s2 < nseg) ? po[(static_cast<size_t>(s2) * g + h) * d + e] : 0.f;
+    }
     const int v = (k == 1) ? block_argmin3(best_k, best_p, best_i, sh_hist, sh_misc) : -1;
+    if (A.has_q) {
+#pragma unroll
+      for (int u = 0; u < kOutPer; ++u) {
+        const int he = tid + u * static_cast<int>(blockDim.x);
+        if (he < g * d) {
+          const int h = he / d, e = he - h * d;
+          float acc = 0.f;
+#pragma unroll
+          for (int s2 = 0; s2 < 16; ++s2) acc = fmaf(pov[u][s2], sh_scale[s2][h], acc);
+          for (int s2 = 16; s2 < nseg; ++s2) acc = fmaf(po[(static_cast<size_t>(s2) * g + h) * d + e], sh_scale[s2][h], acc);
+          A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = acc / sh_L[h];
+        }
+      }
+    }
     if (tid == 0) { sh_misc[0] = -1; sh_misc[1] = -1; }
     __syncthreads();
     // scatter the survivors; the victim's owner releases its slot
@@ -217,7 +239,6 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
     __syncthreads();
     const int vcount = v >= 0 ? 1 : 0;
     const int dead_blk = sh_misc[0], vslot = sh_misc[1];
-    int nb = *L.nblocks;
     if (dead_blk >= 0) {
       for (int j = tid; j < nb; j += blockDim.x) {
         if (L.blocks[j] == dead_blk) {
@@ -274,6 +295,43 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       if (l == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_STEPS]), 1ull);
     }
     return;
+  }
+
+  // ---- combine the split-K partials --------------------------------------
+  if (A.has_q) {
+    const int nseg = min(A.ws.lane_nseg_buf[cbuf][l], kMaxSeg);
+    const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
+    const int warp = tid >> 5, lane = tid & 31;
+    if (warp < g) {
+      // one warp per head; lanes hold segments lane and lane + 32
+      const int h = warp;
+      const float2 v0 = lane < nseg ? ml[lane * g + h] : make_float2(-INFINITY, 0.f);
+      const float2 v1 = lane + 32 < nseg ? ml[(lane + 32) * g + h] : make_float2(-INFINITY, 0.f);
+      const float M = warp_max(fmaxf(v0.x, v1.x));
+      const float s0 = v0.x == -INFINITY ? 0.f : exp2f(v0.x - M);
+      const float s1 = v1.x == -INFINITY ? 0.f : exp2f(v1.x - M);
+      if (lane < nseg) sh_scale[lane][h] = s0;
+      if (lane + 32 < nseg) sh_scale[lane + 32][h] = s1;
+      float Ls = v0.y * s0 + v1.y * s1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+      if (lane == 0) {
+        sh_M[h] = M;
+        sh_L[h] = Ls;
+        const float lse2 = M + log2f(Ls);
+        sh_lse2[h] = lse2;
+        A.lse[static_cast<size_t>(b) * dm.Hq + kh * g + h] = lse2 * kLn2;
+      }
+    }
+    __syncthreads();
+    const float* po = A.ws.part_o_buf[cbuf] + static_cast<size_t>(l) * kMaxSeg * g * d;
+    for (int he = tid; he < g * d; he += blockDim.x) {
+      const int h = he / d, e = he - h * d;
+      float acc = 0.f;
+#pragma unroll 8
+      for (int s = 0; s < nseg; ++s) acc = fmaf(po[(static_cast<size_t>(s) * g + h) * d + e], sh_scale[s][h], acc);
+      A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = acc / sh_L[h];
+    }
   }
 
   // ---- weights -> score state; SnapKV window sums ----------------------------
