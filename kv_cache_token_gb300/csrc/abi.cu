@@ -221,6 +221,7 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   ctx->c.dims = kve::make_dims(*cfg);
   ctx->c.sm_count = sms;
   ctx->c.device = dev;
+  ctx->c.last_layer = -1;
   ctx->c.ws_bytes = kve::workspace_layout(*cfg, &ctx->c.ws, static_cast<char*>(bufs->workspace));
   if (kve::prepare_kernels(ctx->c) != cudaSuccess || ctx->c.attend_ctas_per_sm < 1) {
     delete ctx;
@@ -253,8 +254,10 @@ kvevict_status kvevict_decode_step(kvevict_ctx* ctx, int layer, const void* q, c
     return KVEVICT_E_INVALID_ARG;
   if (q && (!out || !lse)) return KVEVICT_E_INVALID_ARG;
   if (ctx->c.dims.policy == KVEVICT_DROPKV) return KVEVICT_E_INVALID_ARG;
-  return cuda_status(kve::launch_decode(ctx->c, layer, q, k_new, v_new, new_pos, out, lse, victims, n_victims,
-                                        static_cast<cudaStream_t>(stream)));
+  const cudaError_t e = kve::launch_decode(ctx->c, layer, q, k_new, v_new, new_pos, out, lse, victims, n_victims,
+                                           static_cast<cudaStream_t>(stream));
+  ctx->c.last_layer = layer;
+  return cuda_status(e);
 }
 
 kvevict_status kvevict_attend(kvevict_ctx* ctx, int layer, const void* q, const void* k_new, const void* v_new,
@@ -262,7 +265,9 @@ kvevict_status kvevict_attend(kvevict_ctx* ctx, int layer, const void* q, const 
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !k_new || !v_new) return KVEVICT_E_INVALID_ARG;
   if (ctx->c.dims.policy == KVEVICT_DROPKV) return KVEVICT_E_INVALID_ARG;
   if (!q) return KVEVICT_OK;
-  return cuda_status(kve::launch_attend(ctx->c, layer, q, k_new, v_new, static_cast<cudaStream_t>(stream)));
+  const cudaError_t e = kve::launch_attend(ctx->c, layer, q, k_new, v_new, static_cast<cudaStream_t>(stream));
+  ctx->c.last_layer = layer;
+  return cuda_status(e);
 }
 
 kvevict_status kvevict_finish_step(kvevict_ctx* ctx, int layer, const void* q, const void* k_new, const void* v_new,
@@ -276,6 +281,7 @@ kvevict_status kvevict_finish_step(kvevict_ctx* ctx, int layer, const void* q, c
   cudaError_t e = kve::launch_epilogue(ctx->c, layer, q != nullptr, new_pos, k_new, v_new, out, lse, victims,
                                        n_victims, st);
   if (e == cudaSuccess) e = kve::launch_allocate_apply(ctx->c, layer, k_new, v_new, false, nullptr, st, false);
+  ctx->c.last_layer = layer;
   return cuda_status(e);
 }
 

@@ -25,38 +25,6 @@ namespace kve {
 
 namespace {
 
-__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
-  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
-}
-__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
-               : "memory");
-}
-__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
-  uint32_t ok;
-  asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-      : "=r"(ok)
-      : "r"(smem_u32(bar)), "r"(parity)
-      : "memory");
-  return ok != 0;
-}
-__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
-                                         uint64_t policy) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
-          smem_u32(dst)),
-      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
-      : "memory");
-}
-__device__ __forceinline__ uint64_t policy_evict_first() {
-  uint64_t p;
-  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-  return p;
-}
-__device__ __forceinline__ void fence_proxy_async() {
-  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
 __device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
                                         uint32_t& r3) {
   asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
@@ -108,6 +76,7 @@ constexpr int kMaxLanesSmem = 1024;   // lanes per layer (validated at create)
 // then ldmatrix), as a hi + lo pair of bf16 values.
 // ---------------------------------------------------------------------------
 constexpr int kAttStages = 2;      // copy stages per warp
+constexpr float kRescaleLog2 = 8.f;  // lazy-rescale threshold (log2 units)
 
 template <int D, int NT>
 struct Bf16Cfg {
@@ -237,10 +206,36 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
     const int i = (t - sh_prefix[pf_lane]) * 16 + r;
     return i < pf_n ? a.slot[static_cast<size_t>(pf_lane) * a.cap + i] : -1;
   };
+  // --- query fragments -------------------------------------------------------
+  // qb holds the query of the lane being consumed; with one head tile, qn
+  // receives the next lane's query as soon as the copy of that lane's first
+  // tile is issued, so a lane change does not wait on a global load.
+  const int gq = lane_id >> 2, cq = lane_id & 3;
+  constexpr bool kQAhead = NT == 1;
+  uint32_t qb[NT][C::kKs][2];
+  uint32_t qn[kQAhead ? NT : 1][kQAhead ? C::kKs : 1][2];
+  auto fetch_q = [&](int l, uint32_t (*dst)[C::kKs][2]) {
+    const int b = l / a.Hkv, kh = l % a.Hkv;
+    const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(a.q) +
+                                 (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kh) * a.g) * D;
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int h = nt * 8 + gq;
+      const bool ok = h < a.g;
+#pragma unroll
+      for (int ks = 0; ks < C::kKs; ++ks) {
+        const int c0 = ks * 16 + cq * 2;
+        dst[nt][ks][0] = ok ? *reinterpret_cast<const uint32_t*>(qbase + h * D + c0) : 0u;
+        dst[nt][ks][1] = ok ? *reinterpret_cast<const uint32_t*>(qbase + h * D + c0 + 8) : 0u;
+      }
+    }
+  };
+
   auto issue = [&](int t, int st, int slot) {
     while (sh_prefix[iss_lane + 1] <= t) {
       ++iss_lane;
       iss_n = min(max(a.count[iss_lane], 0), a.cap - 1);
+      if constexpr (kQAhead) fetch_q(iss_lane, reinterpret_cast<uint32_t (*)[C::kKs][2]>(qn));
     }
     const int l = iss_lane, n = iss_n;
     const int i0 = (t - sh_prefix[l]) * 16;
@@ -269,26 +264,13 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
   };
 
   // --- consumer state -------------------------------------------------------
-  const int gq = lane_id >> 2, cq = lane_id & 3;
-  uint32_t qb[NT][C::kKs][2];
   float o_acc[NT][C::kDt][4];
   float m_run[NT][2], l_run[NT][2];
   int cur_lane = -1, seg = 0, cur_n = 0;
 
-  auto load_q = [&](int l) {
-    const int b = l / a.Hkv, kh = l % a.Hkv;
-    const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(a.q) +
-                                 (static_cast<size_t>(b) * a.Hq + static_cast<size_t>(kh) * a.g) * D;
+  auto reset_acc = [&]() {
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
-      const int h = nt * 8 + gq;
-      const bool ok = h < a.g;
-#pragma unroll
-      for (int ks = 0; ks < C::kKs; ++ks) {
-        const int c0 = ks * 16 + cq * 2;
-        qb[nt][ks][0] = ok ? *reinterpret_cast<const uint32_t*>(qbase + h * D + c0) : 0u;
-        qb[nt][ks][1] = ok ? *reinterpret_cast<const uint32_t*>(qbase + h * D + c0 + 8) : 0u;
-      }
 #pragma unroll
       for (int dt = 0; dt < C::kDt; ++dt) o_acc[nt][dt][0] = o_acc[nt][dt][1] = o_acc[nt][dt][2] = o_acc[nt][dt][3] = 0.f;
       m_run[nt][0] = m_run[nt][1] = -INFINITY;
@@ -322,6 +304,7 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
 
   // --- pipeline ---------------------------------------------------------------
   int next_slot = fetch_slot(t_begin);
+  fetch_q(iss_lane, qb);
   issue(t_begin, 0, next_slot);
   next_slot = fetch_slot(t_begin + 1);
 
@@ -335,6 +318,26 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
   int cons_lane = 0;
   while (sh_prefix[cons_lane + 1] <= t_begin) ++cons_lane;
   for (int t = t_begin, u = 0; t < t_end; ++t, ++u) {
+    // lane change of the consumer first: issuing tile t + 1 may refill qn
+    while (sh_prefix[cons_lane + 1] <= t) ++cons_lane;
+    if (cons_lane != cur_lane) {
+      if (cur_lane >= 0) {
+        flush();
+        if constexpr (kQAhead) {
+#pragma unroll
+          for (int ks = 0; ks < C::kKs; ++ks) {
+            qb[0][ks][0] = qn[0][ks][0];
+            qb[0][ks][1] = qn[0][ks][1];
+          }
+        } else {
+          fetch_q(cons_lane, qb);
+        }
+      }
+      cur_lane = cons_lane;
+      seg = gw - sh_prefix[cur_lane] / tp;
+      cur_n = min(max(a.count[cur_lane], 0), a.cap - 1);
+      reset_acc();
+    }
     if (t + 1 < t_end) {
       issue(t + 1, (u + 1) % kAttStages, next_slot);
       next_slot = fetch_slot(t + 2);
@@ -348,25 +351,20 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
       }
     }
     __syncwarp();
-
-    while (sh_prefix[cons_lane + 1] <= t) ++cons_lane;
-    if (cons_lane != cur_lane) {
-      if (cur_lane >= 0) flush();
-      cur_lane = cons_lane;
-      seg = gw - sh_prefix[cur_lane] / tp;
-      cur_n = min(max(a.count[cur_lane], 0), a.cap - 1);
-      load_q(cur_lane);
-    }
     const int i0 = (t - sh_prefix[cur_lane]) * 16;
     const unsigned char* kb = wbuf + st * C::kStageBytes;
     const unsigned char* vb = kb + 16 * C::kRowStride;
 
-    // S^T = K Q^T : two accumulators per head tile (even / odd k-steps)
-    float sa[NT][4], sb[NT][4];
+    // S^T = K Q^T : kSAcc independent accumulators per head tile (k-steps
+    // round robin), summed at the end, to keep the dependent MMA chain short
+    constexpr int kSAcc = C::kKs >= 4 ? 4 : C::kKs;
+    float sacc[kSAcc][NT][4];
 #pragma unroll
-    for (int nt = 0; nt < NT; ++nt)
+    for (int c = 0; c < kSAcc; ++c)
 #pragma unroll
-      for (int e = 0; e < 4; ++e) sa[nt][e] = sb[nt][e] = 0.f;
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sacc[c][nt][e] = 0.f;
     {
       const uint32_t addr = smem_u32(kb + ktok * C::kRowStride + kcol);
 #pragma unroll
@@ -374,7 +372,7 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
         uint32_t af[4];
         ldsm_x4(addr + ks * 32, af[0], af[1], af[2], af[3]);
 #pragma unroll
-        for (int nt = 0; nt < NT; ++nt) mma_bf16a((ks & 1) ? sb[nt] : sa[nt], af, qb[nt][ks][0], qb[nt][ks][1]);
+        for (int nt = 0; nt < NT; ++nt) mma_bf16a(sacc[ks % kSAcc][nt], af, qb[nt][ks][0], qb[nt][ks][1]);
       }
     }
     const bool ok0 = i0 + gq <= cur_n, ok1 = i0 + gq + 8 <= cur_n;
@@ -385,7 +383,10 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const bool ok = (e < 2) ? ok0 : ok1;
-        sv[e] = ok ? (sa[nt][e] + sb[nt][e]) * a.scale2 : -INFINITY;
+        float acc = sacc[0][nt][e];
+#pragma unroll
+        for (int c = 1; c < kSAcc; ++c) acc += sacc[c][nt][e];
+        sv[e] = ok ? acc * a.scale2 : -INFINITY;
       }
       // logits of the valid heads: [lane][head][token]
 #pragma unroll
@@ -397,25 +398,39 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
           lrow[gq + 8] = sv[2 + e];
         }
       }
+      // Lazy rescaling: the running max m_run only moves when some logit
+      // of the tile exceeds it by more than kRescaleLog2 (a warp vote), so
+      // the cross-lane max and the rescale of o_acc are skipped on most
+      // tiles.  Weights are then at most 2^kRescaleLog2, far inside fp32;
+      // (m_run, l_run) stay a consistent pair for the split-K combine.
+      bool grow = false;
+#pragma unroll
+      for (int e = 0; e < 2; ++e) grow |= fmaxf(sv[e], sv[2 + e]) > m_run[nt][e] + kRescaleLog2;
+      if (__any_sync(0xffffffffu, grow)) {
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          float tm = fmaxf(sv[e], sv[2 + e]);
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
+          tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
+          const float mo = m_run[nt][e];
+          const float mn = fmaxf(mo, tm);
+          const float corr = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
+          m_run[nt][e] = mn;
+          l_run[nt][e] *= corr;
+#pragma unroll
+          for (int dt = 0; dt < C::kDt; ++dt) {
+            o_acc[nt][dt][e] *= corr;
+            o_acc[nt][dt][2 + e] *= corr;
+          }
+        }
+      }
       float pv[4];
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        float tm = fmaxf(sv[e], sv[2 + e]);
-        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 4));
-        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 8));
-        tm = fmaxf(tm, __shfl_xor_sync(0xffffffffu, tm, 16));
-        const float mo = m_run[nt][e];
-        const float mn = fmaxf(mo, tm);
-        const float corr = (mo == -INFINITY) ? 0.f : exp2f(mo - mn);
-        m_run[nt][e] = mn;
-        pv[e] = exp2f(sv[e] - mn);
-        pv[2 + e] = exp2f(sv[2 + e] - mn);
-        l_run[nt][e] = l_run[nt][e] * corr + pv[e] + pv[2 + e];
-#pragma unroll
-        for (int dt = 0; dt < C::kDt; ++dt) {
-          o_acc[nt][dt][e] *= corr;
-          o_acc[nt][dt][2 + e] *= corr;
-        }
+        pv[e] = exp2f(sv[e] - m_run[nt][e]);
+        pv[2 + e] = exp2f(sv[2 + e] - m_run[nt][e]);
+        l_run[nt][e] += pv[e] + pv[2 + e];
       }
       split_bf16(pv[0], pv[1], ph[nt][0], pl[nt][0]);   // token gq,     heads 2c, 2c+1
       split_bf16(pv[2], pv[3], ph[nt][1], pl[nt][1]);   // token gq + 8
@@ -569,6 +584,7 @@ cudaError_t prepare_kernels(Ctx& ctx) {
   if (e == cudaSuccess) e = set_attr<128, 2>();
   if (e == cudaSuccess) e = set_attr<64, 1>();
   if (e == cudaSuccess) e = set_attr<64, 2>();
+  if (e == cudaSuccess) e = prepare_epilogue();
   if (e != cudaSuccess) return e;
   const Dims& dm = ctx.dims;
   const int nt = dm.g > 8 ? 2 : 1;
@@ -593,25 +609,29 @@ cudaError_t launch_attend(const Ctx& ctx, int layer, const void* q, const void* 
   a.lanes = dm.lanes; a.g = dm.g; a.Hkv = dm.Hkv; a.Hq = dm.Hq; a.cap = dm.cap; a.lcap = dm.lcap;
   a.P = dm.P;
   a.scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(dm.d));
+  // The previous attention, epilogue and apply launches may still run when
+  // this kernel starts early: allowed only when they work on the other
+  // scratch parity (and so on another layer).
+  const bool pdl = ctx.last_layer < 0 || ((ctx.last_layer ^ layer) & 1) != 0;
   if (dm.dtype == KVEVICT_BF16) {
     if (dm.lanes > kMaxLanesSmem) return cudaErrorInvalidValue;
     const int grid = ctx.sm_count * ctx.attend_ctas_per_sm;
     const int nt = dm.g > 8 ? 2 : 1;
     const dim3 blk(kAttendWarps * 32);
     if (dm.d == 128 && nt == 1)
-      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, Bf16Cfg<128, 1>::kSmem, stream, true, a);
+      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, Bf16Cfg<128, 1>::kSmem, stream, pdl, a);
     else if (dm.d == 128)
-      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, Bf16Cfg<128, 2>::kSmem, stream, true, a);
+      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, Bf16Cfg<128, 2>::kSmem, stream, pdl, a);
     else if (nt == 1)
-      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, Bf16Cfg<64, 1>::kSmem, stream, true, a);
+      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, Bf16Cfg<64, 1>::kSmem, stream, pdl, a);
     else
-      return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, Bf16Cfg<64, 2>::kSmem, stream, true, a);
+      return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, Bf16Cfg<64, 2>::kSmem, stream, pdl, a);
   } else {
     const int chunks = (dm.cap + kF32Chunk) / kF32Chunk;   // enough for n = cap - 1 plus the new token
     if (chunks > kMaxSeg) return cudaErrorInvalidValue;
     dim3 grid(chunks, dm.lanes);
     const size_t sm = (static_cast<size_t>(dm.g) * dm.d + dm.g * kF32Chunk + 2 * dm.g) * sizeof(float);
-    return launch_k(attend_f32_kernel, grid, dim3(kF32Chunk), sm, stream, true, a, dm.d);
+    return launch_k(attend_f32_kernel, grid, dim3(kF32Chunk), sm, stream, pdl, a, dm.d);
   }
   return cudaGetLastError();
 }

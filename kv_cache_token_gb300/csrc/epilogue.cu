@@ -22,6 +22,14 @@ namespace {
 
 constexpr int kEpiThreads = 512;
 constexpr int kFastPer = 7;     // tokens per thread on the one-victim H2O path
+constexpr int kFastN = kFastPer * kEpiThreads;   // tokens a lane may hold on that path
+constexpr int kPoSeg = 16;      // split-K partial outputs staged in shared memory on that path
+constexpr int kWorkShift = 16;  // done counter: arrivals below, lanes asking for blocks above
+constexpr int kWorkUnit = 1 << kWorkShift;
+// dynamic shared memory of the epilogue: the fast path's logits [8][kFastN]
+// and partial outputs [kPoSeg][8][128]; the general path's row buffer
+constexpr size_t kEpiDynSmem = (static_cast<size_t>(8) * kFastN + static_cast<size_t>(kPoSeg) * 8 * 128) * 4;
+static_assert(kEpiDynSmem >= static_cast<size_t>(128) * kMaxW * 4, "row buffer fits");
 constexpr int kApplyThreads = 512;
 constexpr float kLn2 = 0.6931471805599453f;
 
@@ -40,104 +48,140 @@ __device__ __forceinline__ void copy_row(KT* dst, const KT* src, int d) {
 }
 
 template <typename KT>
-__device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n);
+__device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n, unsigned char* dsm,
+                                          int* sh_work);
 __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const Dims& dm, int* sh_scan,
                                int* sh_flag);
 
 template <typename KT>
 __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs A) {
+  extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ int sh_scan[40];
-  grid_dep_wait();      // the attention kernel's results are complete and visible
-  grid_dep_launch();
+  __shared__ int sh_work, sh_last, sh_flag;
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   LaneRefs L = lane_refs(A.ls, dm, l);
-  const int n = A.ls.count[l];
-  bool bad = n < 0 || n >= dm.cap;
-  if (!bad && n > 0 && L.pos[n - 1] >= A.new_pos) {
-    if (tid == 0) set_status(A.ws.status, ST_POSITION);
-    bad = true;
-  } else if (bad && tid == 0) {
-    set_status(A.ws.status, ST_CAPACITY);
-  }
-  if (bad) {
-    if (tid == 0) { A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0; }
+  // The token count (and, on the fast path, the token table) is not written
+  // by the attention kernel: it is read before the dependency wait, while
+  // the attention kernel drains.
+  const int n = __ldcg(A.ls.count + l);
+  if (tid == 0) sh_work = 0;
+  if (n < 0 || n >= dm.cap) {
+    grid_dep_wait();
+    grid_dep_launch();
+    if (tid == 0) {
+      set_status(A.ws.status, ST_CAPACITY);
+      A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
+    }
   } else {
-    lane_step<KT>(A, L, n);
+    lane_step<KT>(A, L, n, dsm, &sh_work);
   }
-  // the last CTA of the grid to finish runs the layer allocator
-  __shared__ int sh_last, sh_flag;
+  // The last CTA of the grid to finish runs the layer allocator, if any lane
+  // asked for blocks: the done counter carries the number of such lanes in
+  // its upper bits, so the common no-work case needs no further atomic.
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    sh_last = atomicAdd(A.ws.epi_done, 1) == static_cast<int>(gridDim.x) - 1;
+    const int old = atomicAdd(A.ws.epi_done, 1 + (sh_work ? kWorkUnit : 0));
+    sh_last = (old & (kWorkUnit - 1)) == static_cast<int>(gridDim.x) - 1;
+    sh_flag = (old >> kWorkShift) + (sh_work ? 1 : 0);
   }
   __syncthreads();
   if (sh_last) {
-    if (tid == 0) *A.ws.epi_done = 0;
-    __threadfence();
-    allocate_layer(A.ls, A.ws, dm, sh_scan, &sh_flag);
+    if (sh_flag == 0) {
+      if (tid == 0) { *A.ws.epi_done = 0; A.ws.counters[1] = 0; A.ws.counters[2] = 0; }
+    } else {
+      if (tid == 0) *A.ws.epi_done = 0;
+      __threadfence();
+      allocate_layer(A.ls, A.ws, dm, sh_scan, &sh_flag);
+    }
   }
 }
 
 // One lane's step after the attention kernel (all threads of the CTA).
 template <typename KT>
-__device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n) {
+__device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n, unsigned char* dsm,
+                                          int* sh_work) {
   __shared__ float sh_M[kMaxG], sh_L[kMaxG], sh_lse2[kMaxG];
-  __shared__ int sh_hist[256];
+  __shared__ __align__(16) int sh_hist[256];   // also read as 64-bit words
   __shared__ int sh_misc[40];
   __shared__ int sh_scan[40];
   __shared__ int sh_idx[kEpiThreads];
   __shared__ unsigned sh_min[32];
   __shared__ int sh_nan;
   __shared__ float sh_scale[kMaxSeg][kMaxG];
-  __shared__ __align__(16) float sh_rows[128 * kMaxW];
+  __shared__ uint64_t sh_bar;
+  float* sh_rows = reinterpret_cast<float*>(dsm);      // general path: 128 * kMaxW floats
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
-  if (tid == 0) sh_nan = 0;
+  const int cbuf = A.layer & 1;
 
   // ---- H2O with at most one victim (the steady state of a full cache) --------
-  // One batched pass with every independent load issued up front: the
-  // split-K statistics (read for all kMaxSeg segments, masked afterwards),
-  // each thread's kFastPer tokens (logits, score, position, slot) and the
-  // lane's block count.  Weights, new scores and the candidate minimum come
-  // from registers; the partial outputs for `out` are loaded while the
-  // argmin's barriers run; survivors are written straight to their index
-  // after the removal.
-  const int cbuf = A.layer & 1;
-  if (dm.policy == KVEVICT_H2O && n + 1 - dm.budget <= 1 && n <= kFastPer * static_cast<int>(blockDim.x) &&
-      g <= 8) {
+  // Before the dependency wait: the lane's token table (kFastPer tokens a
+  // thread), its block count and the new token's K/V row, none of which the
+  // attention kernel writes.  After it: the logits and the split-K partial
+  // outputs arrive in shared memory by bulk copy (one mbarrier), the split-K
+  // statistics by plain loads.  Weights, new scores and the candidate minimum
+  // come from registers and shared memory; survivors are written straight to
+  // their index after the removal.
+  if (dm.policy == KVEVICT_H2O && n + 1 - dm.budget <= 1 && n <= kFastN && g <= 8 && d <= 128) {
     const int k = max(0, n + 1 - dm.budget);
     const int cut = A.new_pos - dm.R + 1;
     const int warp = tid >> 5, lane = tid & 31;
-    const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
-    const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
-    const int nseg = A.has_q ? min(A.ws.lane_nseg_buf[cbuf][l], kMaxSeg) : 0;
-    float2 m0 = make_float2(-INFINITY, 0.f), m1 = make_float2(-INFINITY, 0.f);
-    if (A.has_q && warp < g) {
-      m0 = ml[lane * g + warp];
-      m1 = ml[(lane + 32) * g + warp];
-    }
-    float lv[kFastPer][8];
     float sc[kFastPer];
     int ps[kFastPer], sl[kFastPer];
 #pragma unroll
     for (int j = 0; j < kFastPer; ++j) {
-      const int i = tid + j * static_cast<int>(blockDim.x);
+      const int i = tid + j * kEpiThreads;
       const bool ok = i < n;
-#pragma unroll
-      for (int h = 0; h < 8; ++h) lv[j][h] = (ok && A.has_q && h < g) ? __ldcs(lg + static_cast<size_t>(h) * dm.lcap + i) : -INFINITY;
-      sc[j] = ok ? L.score[i] : 0.f;
-      ps[j] = ok ? L.pos[i] : 0x7FFFFFFF;
-      sl[j] = ok ? L.slot[i] : -1;
+      sc[j] = ok ? __ldcg(L.score + i) : 0.f;
+      ps[j] = ok ? __ldcg(L.pos + i) : 0x7FFFFFFF;
+      sl[j] = ok ? __ldcg(L.slot + i) : -1;
     }
-    int nb = *L.nblocks;
+    int nb = __ldcg(L.nblocks);
+    KT knv{}, vnv{};
+    if (tid < d) {
+      knv = static_cast<const KT*>(A.k_new)[static_cast<size_t>(l) * d + tid];
+      vnv = static_cast<const KT*>(A.v_new)[static_cast<size_t>(l) * d + tid];
+    }
+    if (tid == 0) {
+      sh_nan = 0;
+      mbar_init(&sh_bar, 1);
+      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    }
+    // the last kept token must precede the new one
+    bool late = false;
+#pragma unroll
+    for (int j = 0; j < kFastPer; ++j) late |= (tid + j * kEpiThreads == n - 1) && ps[j] >= A.new_pos;
+    grid_dep_wait();      // the attention kernel's results are complete and visible
+    grid_dep_launch();
+    if (__syncthreads_or(late)) {
+      if (tid == 0) {
+        set_status(A.ws.status, ST_POSITION);
+        A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
+      }
+      return;
+    }
+    float* lg_s = reinterpret_cast<float*>(dsm);                 // [g][kFastN]
+    float* po_s = lg_s + 8 * kFastN;                             // [kPoSeg][g][d]
+    const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
+    const float* po = A.ws.part_o_buf[cbuf] + static_cast<size_t>(l) * kMaxSeg * g * d;
+    if (A.has_q && tid == 0) {
+      const uint32_t row = static_cast<uint32_t>((n + 3) & ~3) * 4u;   // 16-byte multiple, inside lcap
+      const uint32_t pob = static_cast<uint32_t>(kPoSeg * g * d) * 4u;
+      mbar_arrive_expect_tx(&sh_bar, row * g + pob);
+      if (row)
+        for (int h = 0; h < g; ++h) bulk_g2s(lg_s + h * kFastN, lg + static_cast<size_t>(h) * dm.lcap, row, &sh_bar);
+      bulk_g2s(po_s, po, pob, &sh_bar);
+    }
+    const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
+    const int nseg = A.has_q ? min(__ldcg(A.ws.lane_nseg_buf[cbuf] + l), kMaxSeg) : 0;
     // per-head log-sum-exp of the split-K segments (one warp per head)
     if (A.has_q && warp < g) {
       const int h = warp;
-      if (lane >= nseg) m0 = make_float2(-INFINITY, 0.f);
-      if (lane + 32 >= nseg) m1 = make_float2(-INFINITY, 0.f);
+      const float2 m0 = lane < nseg ? __ldcg(ml + lane * g + h) : make_float2(-INFINITY, 0.f);
+      const float2 m1 = lane + 32 < nseg ? __ldcg(ml + (lane + 32) * g + h) : make_float2(-INFINITY, 0.f);
       const float M = warp_max(fmaxf(m0.x, m1.x));
       const float s0 = m0.x == -INFINITY ? 0.f : exp2f(m0.x - M);
       const float s1 = m1.x == -INFINITY ? 0.f : exp2f(m1.x - M);
@@ -154,18 +198,21 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       }
     }
     __syncthreads();
+    if (A.has_q && !mbar_wait_bounded(&sh_bar, 0, A.ws.status)) (void)mbar_wait_bounded(&sh_bar, 0, A.ws.status);
     unsigned long long best_k = ~0ull;
     uint32_t best_p = 0xFFFFFFFFu;
     int best_i = -1, nan_count = 0;
 #pragma unroll
     for (int j = 0; j < kFastPer; ++j) {
-      const int i = tid + j * static_cast<int>(blockDim.x);
+      const int i = tid + j * kEpiThreads;
       if (i < n) {
-        float w = 0.f;
+        if (A.has_q) {
+          float w = 0.f;
 #pragma unroll
-        for (int h = 0; h < 8; ++h)
-          if (h < g) w += exp2f(lv[j][h] - sh_lse2[h]);
-        if (A.has_q) sc[j] += w;
+          for (int h = 0; h < 8; ++h)
+            if (h < g) w += exp2f(lg_s[h * kFastN + i] - sh_lse2[h]);
+          sc[j] += w;
+        }
         if (sc[j] != sc[j]) ++nan_count;
         if (k == 1 && ps[j] < cut) {
           const unsigned long long kk = mono_key(sc[j]);
@@ -175,39 +222,25 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
         }
       }
     }
-    // partial outputs of the split-K segments, in flight during the argmin
-    const float* po = A.ws.part_o_buf[cbuf] + static_cast<size_t>(l) * kMaxSeg * g * d;
-    constexpr int kOutPer = 2;          // outputs per thread (g * d <= 1024)
-    float pov[kOutPer][16];
-#pragma unroll
-    for (int u = 0; u < kOutPer; ++u) {
-      const int he = tid + u * static_cast<int>(blockDim.x);
-      const int h = he / d, e = he - (he / d) * d;
-#pragma unroll
-      for (int s2 = 0; s2 < 16; ++s2)
-        pov[u][s2] = (A.has_q && he < g * d && s2 < nseg) ? po[(static_cast<size_t>(s2) * g + h) * d + e] : 0.f;
-    }
-    const int v = (k == 1) ? block_argmin3(best_k, best_p, best_i, sh_hist, sh_misc) : -1;
+    // output: combine the split-K partial outputs (the first kPoSeg from
+    // shared memory); its loads overlap the argmin's barriers
     if (A.has_q) {
-#pragma unroll
-      for (int u = 0; u < kOutPer; ++u) {
-        const int he = tid + u * static_cast<int>(blockDim.x);
-        if (he < g * d) {
-          const int h = he / d, e = he - h * d;
-          float acc = 0.f;
-#pragma unroll
-          for (int s2 = 0; s2 < 16; ++s2) acc = fmaf(pov[u][s2], sh_scale[s2][h], acc);
-          for (int s2 = 16; s2 < nseg; ++s2) acc = fmaf(po[(static_cast<size_t>(s2) * g + h) * d + e], sh_scale[s2][h], acc);
-          A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = acc / sh_L[h];
-        }
+      for (int he = tid; he < g * d; he += kEpiThreads) {
+        const int h = he / d, e = he - h * d;
+        float acc = 0.f;
+        const int ns = min(nseg, kPoSeg);
+        for (int s2 = 0; s2 < ns; ++s2) acc = fmaf(po_s[(s2 * g + h) * d + e], sh_scale[s2][h], acc);
+        for (int s2 = kPoSeg; s2 < nseg; ++s2) acc = fmaf(__ldcg(po + (static_cast<size_t>(s2) * g + h) * d + e), sh_scale[s2][h], acc);
+        A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = acc / sh_L[h];
       }
     }
+    const int v = (k == 1) ? block_argmin3(best_k, best_p, best_i, sh_hist, sh_misc) : -1;
     if (tid == 0) { sh_misc[0] = -1; sh_misc[1] = -1; }
     __syncthreads();
     // scatter the survivors; the victim's owner releases its slot
 #pragma unroll
     for (int j = 0; j < kFastPer; ++j) {
-      const int i = tid + j * static_cast<int>(blockDim.x);
+      const int i = tid + j * kEpiThreads;
       if (i < n) {
         if (i == v) {
           A.victims[static_cast<size_t>(l) * dm.cap] = ps[j];
@@ -240,7 +273,7 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
     const int vcount = v >= 0 ? 1 : 0;
     const int dead_blk = sh_misc[0], vslot = sh_misc[1];
     if (dead_blk >= 0) {
-      for (int j = tid; j < nb; j += blockDim.x) {
+      for (int j = tid; j < nb; j += kEpiThreads) {
         if (L.blocks[j] == dead_blk) {
           L.blocks[j] = L.blocks[nb - 1];
           *L.nblocks = nb - 1;
@@ -257,7 +290,7 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
     if (holes == 1 && vcount == 1 && dead_blk < 0 && vslot >= 0) {
       best = static_cast<unsigned>(vslot);
     } else if (holes > 0) {
-      for (int j = tid; j < nb; j += blockDim.x) {
+      for (int j = tid; j < nb; j += kEpiThreads) {
         const int blk = L.blocks[j];
         const int mk = L.mask[blk] & 0xFFFF;
         if (mk != 0xFFFF) best = min(best, static_cast<unsigned>(blk * kBlock + (__ffs(~mk) - 1)));
@@ -266,14 +299,12 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       if ((tid & 31) == 0) sh_min[tid >> 5] = best;
       __syncthreads();
       best = 0xFFFFFFFFu;
-      for (int w = 0; w < static_cast<int>(blockDim.x >> 5); ++w) best = min(best, sh_min[w]);
+      for (int w = 0; w < kEpiThreads / 32; ++w) best = min(best, sh_min[w]);
     }
     const bool need = best == 0xFFFFFFFFu;
-    if (!need) {
-      KT* kp = static_cast<KT*>(A.ls.k_pool);
-      KT* vp = static_cast<KT*>(A.ls.v_pool);
-      copy_row(kp + static_cast<size_t>(best) * d, static_cast<const KT*>(A.k_new) + static_cast<size_t>(l) * d, d);
-      copy_row(vp + static_cast<size_t>(best) * d, static_cast<const KT*>(A.v_new) + static_cast<size_t>(l) * d, d);
+    if (!need && tid < d) {
+      static_cast<KT*>(A.ls.k_pool)[static_cast<size_t>(best) * d + tid] = knv;
+      static_cast<KT*>(A.ls.v_pool)[static_cast<size_t>(best) * d + tid] = vnv;
     }
     int t_live = 0;
     const int ndst = lane_plan(L, nb, m + 1, false, dm.theta_f, need, &t_live, sh_scan);
@@ -288,11 +319,26 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       A.ws.need_admit[l] = need ? 1 : 0;
       A.ws.want_dst[l] = ndst;
       A.ws.plan_tlive[l] = t_live;
-      if (need || ndst > 0) atomicOr(A.ws.work_flag, 1);
+      if (need || ndst > 0) {
+        atomicOr(A.ws.work_flag, 1);
+        *sh_work = 1;
+      }
       if (vcount) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_VICTIMS]), 1ull);
       if (dead_blk >= 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_FREED_DEAD]), 1ull);
       if (sh_nan) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_NAN_KEYS]), (unsigned long long)sh_nan);
       if (l == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_STEPS]), 1ull);
+    }
+    return;
+  }
+
+  // ---- general path ------------------------------------------------------------
+  grid_dep_wait();      // the attention kernel's results are complete and visible
+  grid_dep_launch();
+  if (tid == 0) sh_nan = 0;
+  if (n > 0 && L.pos[n - 1] >= A.new_pos) {
+    if (tid == 0) {
+      set_status(A.ws.status, ST_POSITION);
+      A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
     }
     return;
   }
@@ -478,7 +524,10 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
     A.ws.need_admit[l] = need ? 1 : 0;
     A.ws.want_dst[l] = ndst;
     A.ws.plan_tlive[l] = t_live;
-    if (need || ndst > 0) atomicOr(A.ws.work_flag, 1);
+    if (need || ndst > 0) {
+      atomicOr(A.ws.work_flag, 1);
+      *sh_work = 1;
+    }
     atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_VICTIMS]), (unsigned long long)vcount);
     if (dead) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_FREED_DEAD]), (unsigned long long)dead);
     if (nan_tot) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_NAN_KEYS]), (unsigned long long)nan_tot);
@@ -698,9 +747,25 @@ cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, 
   A.layer = layer;
   A.k_new = k_new; A.v_new = v_new;
   A.out = out; A.lse = lse; A.victims = victims; A.n_victims = n_victims;
+  // After this layer's attention launch the predecessor triggers only once
+  // its own predecessors are complete; without one, the predecessor may be
+  // the last step's apply, whose epilogue may still be writing that layer's
+  // tables, which this kernel reads before its dependency wait.
+  const bool pdl = has_q || ctx.last_layer != layer;
   if (ctx.dims.dtype == KVEVICT_BF16)
-    return launch_k(decode_epilogue_kernel<__nv_bfloat16>, dim3(ctx.dims.lanes), dim3(kEpiThreads), 0, stream, true, A);
-  return launch_k(decode_epilogue_kernel<float>, dim3(ctx.dims.lanes), dim3(kEpiThreads), 0, stream, true, A);
+    return launch_k(decode_epilogue_kernel<__nv_bfloat16>, dim3(ctx.dims.lanes), dim3(kEpiThreads), kEpiDynSmem,
+                    stream, pdl, A);
+  return launch_k(decode_epilogue_kernel<float>, dim3(ctx.dims.lanes), dim3(kEpiThreads), kEpiDynSmem, stream,
+                  pdl, A);
+}
+
+cudaError_t prepare_epilogue() {
+  cudaError_t e = cudaFuncSetAttribute(decode_epilogue_kernel<__nv_bfloat16>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kEpiDynSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(decode_epilogue_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             static_cast<int>(kEpiDynSmem));
+  return e;
 }
 
 cudaError_t launch_allocate_apply(const Ctx& ctx, int layer, const void* k_new, const void* v_new,

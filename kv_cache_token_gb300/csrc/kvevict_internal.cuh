@@ -94,6 +94,11 @@ struct Ctx {
   int device;
   size_t ws_bytes;
   int attend_ctas_per_sm;
+  // Layer of the most recent attention or decode-step launch (-1: none).
+  // Those kernels may still run when the next kernel starts under
+  // programmatic dependent launch, so a launch that would touch that layer's
+  // tables or its parity's scratch is not launched early.
+  int last_layer;
 };
 
 // workspace layout (host)
@@ -120,6 +125,7 @@ cudaError_t launch_score(const Ctx&, int layer, const void* q_win, int w, const 
 cudaError_t launch_stats(const Ctx&, int layer, long long* out, cudaStream_t);
 cudaError_t launch_attend_into(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
                                float* logits, float* part_o, float* part_ml, int32_t* lane_nseg, cudaStream_t);
+cudaError_t prepare_epilogue();     // one-time attributes of the epilogue kernels
 cudaError_t prepare_kernels(Ctx&);   // one-time kernel attributes and occupancy (not stream work)
 cudaError_t launch_attend(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
                           cudaStream_t);
@@ -158,6 +164,57 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) { atomicOr(st, bits); }
+
+// mbarrier and bulk-copy (TMA, untiled) primitives
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)), "r"(bytes)
+               : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Waits for phase `parity` of the barrier; gives up after a bounded number
+// of polls (each try_wait itself suspends for a while), records ST_TIMEOUT
+// and returns false.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* status) {
+  for (int spins = 0; spins < (1 << 22); ++spins)
+    if (mbar_try_wait(bar, parity)) return true;
+  set_status(status, ST_TIMEOUT);
+  return false;
+}
+// global -> shared bulk copy completing on `bar`; dst, src and bytes are
+// multiples of 16 bytes
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+          smem_u32(dst)),
+      "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar) {
+  asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+                   smem_u32(dst)),
+               "l"(src), "r"(bytes), "r"(smem_u32(bar))
+               : "memory");
+}
+__device__ __forceinline__ uint64_t policy_evict_first() {
+  uint64_t p;
+  asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+  return p;
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
 
 // Monotone unsigned images of float keys: a < b  <=>  mono(a) < mono(b).
 // -0.0 maps to +0.0; every NaN maps above +inf (a NaN-scored token is the
@@ -253,7 +310,7 @@ __device__ __forceinline__ bool select_is_victim(const SelectResult& r, unsigned
 
 // KeyFn(i) -> unsigned long long monotone key of entry i; PosFn(i) -> uint32
 // position; CandFn(i) -> bool.  key_bits = 32 or 64.  sh_hist: 256 ints,
-// sh_misc: 40 ints (blockDim <= 1024).  Returns the same SelectResult in
+// 8-byte aligned (it also holds 64-bit keys), sh_misc: 40 ints (blockDim <= 1024).  Returns the same SelectResult in
 // every thread.  k == 1 (the steady state of a full cache) takes one pass.
 template <typename KeyFn, typename PosFn, typename CandFn>
 __device__ SelectResult block_bottom_k(int n, int k, int key_bits, KeyFn keyf, PosFn posf,

@@ -112,7 +112,8 @@ __device__ __forceinline__ int lane_remove(const LaneRefs& L, int n, VictimFn is
 
 // Block-wide minimum of (key, position) with the entry index; returns the
 // index of the minimum (-1 if no thread had a candidate).  Every thread
-// returns the same value.  sh_a: 256 ints of scratch, sh_b: 40 ints.
+// returns the same value.  sh_a: 256 ints of scratch, 8-byte aligned (it
+// also holds 64-bit keys), sh_b: 40 ints.
 __device__ __forceinline__ int block_argmin3(unsigned long long bk, uint32_t bp, int bi, int* sh_a, int* sh_b) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {

@@ -104,7 +104,7 @@ template <typename KeyT>
 __global__ void __launch_bounds__(kSelThreads) select_kernel(const KeyT* keys, const int32_t* positions,
                                                             const int32_t* counts, int stride, int budget, int R,
                                                             int32_t* victims, int32_t* n_victims) {
-  __shared__ int sh_hist[256];
+  __shared__ __align__(16) int sh_hist[256];   // also read as 64-bit words
   __shared__ int sh_misc[40];
   __shared__ int sh_scan[40];
   const int l = blockIdx.x;

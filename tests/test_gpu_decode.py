@@ -83,3 +83,44 @@ def test_null_query_is_inert():
     shp = scaled("h2o_70b", num_layers=1, batch=1, num_kv_heads=2, num_q_heads=16, ctx=300, steps=4,
                  budget=200, recent_window=20)
     run_decode(shp, 4, null_steps=(0, 2))
+
+
+@pytest.mark.parametrize("order", [(0, 0, 0, 0, 0, 0), (0, 2, 0, 2, 2, 0, 1, 1, 2), (1, 0, 2, 2, 1, 0, 0)])
+def test_steps_enqueued_without_host_sync(order):
+    """Decode steps enqueued back to back with no host synchronisation, in
+    orders that revisit a layer or its scratch parity immediately (the
+    second step's kernels must not start on tables or scratch the first is
+    still writing).  Step 1 of every layer is a mass eviction followed by
+    relocation, so the apply kernel has work.  Every call's outputs and the
+    final tables match the oracle run in the same order."""
+    shp = scaled("h2o_70b", num_layers=3, batch=2, num_kv_heads=2, num_q_heads=16, ctx=1000, steps=12,
+                 budget=200, recent_window=100)
+    wl = Workload(shp)
+    layers = sorted(set(order))
+    eng, orc = make_pair(shp, layers=layers)
+    for layer in layers:
+        prefill_both(eng, orc, wl, layer)
+    torch.cuda.synchronize()
+    t_of = {l: 0 for l in layers}
+    calls = []
+    for layer in order:
+        t = t_of[layer]
+        t_of[layer] += 1
+        q, kn, vn, pos = wl.step(layer, t)
+        vic = torch.zeros((eng.lanes, shp.max_tokens), dtype=torch.int32, device="cuda")
+        nv = torch.zeros((eng.lanes,), dtype=torch.int32, device="cuda")
+        out, lse, _, _ = eng.decode_step(layer, q.cuda(), kn.cuda(), vn.cuda(), pos, victims=vic, n_victims=nv)
+        calls.append((layer, t, q, kn, vn, pos, out, lse, vic, nv))
+    torch.cuda.synchronize()
+    for layer, t, q, kn, vn, pos, out, lse, vic, nv in calls:
+        ref = orc.decode_step(layer, q.double().numpy(), kn.double().numpy(), vn.double().numpy(), pos)
+        what = "layer %d step %d" % (layer, t)
+        assert_rows_close(out.cpu().numpy(), ref["out"], what + " out")
+        assert_rows_close(lse.cpu().numpy()[..., None], ref["lse"][..., None], what + " lse")
+        got = victim_lists(nv, vic)
+        for l in range(eng.lanes):
+            np.testing.assert_array_equal(got[l], ref["victims"][l], err_msg=what + " lane %d victims" % l)
+    for layer in layers:
+        compare_states(gpu_state(eng, layer), oracle_state(orc, layer), shp.policy, "final layer %d" % layer)
+    code, msg = eng.last_error()
+    assert code == 0, msg
