@@ -53,19 +53,343 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
 __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const Dims& dm, int* sh_scan,
                                int* sh_flag);
 
+// Marks this lane's epilogue done (thread 0 only).  The per-lane requests
+// the allocator reads (need_admit, want_dst, plan_tlive, count, released
+// block owners) are written before; the fence makes them visible to the
+// last CTA.  The done counter carries the number of lanes asking for blocks
+// in its upper bits, so the common no-work case needs no further atomic.
+__device__ __forceinline__ void signal_done(const Workspace& ws, bool work, int* sh_last, int* sh_flag) {
+  __threadfence();
+  const int old = atomicAdd(ws.epi_done, 1 + (work ? kWorkUnit : 0));
+  *sh_last = (old & (kWorkUnit - 1)) == static_cast<int>(gridDim.x) - 1;
+  *sh_flag = (old >> kWorkShift) + (work ? 1 : 0);
+}
+
+// H2O with at most one victim (the steady state of a full cache), all
+// threads of the CTA.  Before the dependency wait: the lane's token table
+// (kFastPer tokens a thread), its block list with the live masks (kFastPer
+// blocks a thread) and the new token's K/V row, none of which the attention
+// kernel writes; from the masks, each warp's lowest free slot.  After it:
+// logits and split-K partial outputs by bulk copy into shared memory,
+// split-K statistics by plain loads.  The minimum (key, position) and its
+// slot come from three warp reductions and one barrier; the holder of the
+// victim's block decides from the mask it already holds whether the block
+// empties.  The allocator's requests and the done counter go out before
+// the table is rewritten, so the counter's fence does not wait for those
+// stores.
+template <typename KT>
+__device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& L, const int n, unsigned char* dsm,
+                                              int* sh_sig, int* sh_last, int* sh_flag) {
+  __shared__ float sh_L[8], sh_lse2[8];
+  __shared__ float sh_scale[kMaxSeg][8];
+  __shared__ unsigned sh_wkey[kEpiThreads / 32], sh_wpos[kEpiThreads / 32], sh_wslot[kEpiThreads / 32];
+  __shared__ unsigned sh_wfree[kEpiThreads / 32];
+  __shared__ int sh_nan, sh_dead, sh_tail;
+  __shared__ int sh_scan2[40];
+  __shared__ uint64_t sh_bar;
+  constexpr unsigned kNone = 0xFFFFFFFFu;
+  const Dims& dm = A.dm;
+  const int l = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
+  const int cbuf = A.layer & 1;
+  const int k = max(0, n + 1 - dm.budget);          // 0 or 1
+  const int cut = A.new_pos - dm.R + 1;
+
+  // ---- before the dependency wait -----------------------------------------------
+  float sc[kFastPer];
+  int ps[kFastPer], sl[kFastPer];
+#pragma unroll
+  for (int j = 0; j < kFastPer; ++j) {
+    const int i = tid + j * kEpiThreads;
+    const bool ok = i < n;
+    sc[j] = ok ? __ldcg(L.score + i) : 0.f;
+    ps[j] = ok ? __ldcg(L.pos + i) : 0x7FFFFFFF;
+    sl[j] = ok ? __ldcg(L.slot + i) : -1;
+  }
+  KT knv{}, vnv{};
+  if (tid < d) {
+    knv = static_cast<const KT*>(A.k_new)[static_cast<size_t>(l) * d + tid];
+    vnv = static_cast<const KT*>(A.v_new)[static_cast<size_t>(l) * d + tid];
+  }
+  const int nb = min(__ldcg(L.nblocks), kFastN);   // every block holds a live token, so nb <= n
+  int bk[kFastPer], bm[kFastPer];
+#pragma unroll
+  for (int j = 0; j < kFastPer; ++j) {
+    const int jj = tid + j * kEpiThreads;
+    bk[j] = jj < nb ? __ldcg(L.blocks + jj) : -1;
+  }
+  bool bad_blk = false;
+#pragma unroll
+  for (int j = 0; j < kFastPer; ++j) {
+    if (bk[j] >= dm.P) { bad_blk = true; bk[j] = -1; }
+    bm[j] = bk[j] >= 0 ? (__ldcg(L.mask + bk[j]) & 0xFFFF) : 0xFFFF;
+  }
+  if (bad_blk) set_status(A.ws.status, ST_BAD_INDEX);
+  if (tid == 0) {
+    sh_nan = 0;
+    sh_dead = -1;
+    mbar_init(&sh_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  {
+    // lowest free slot of the lane's blocks before this step's eviction
+    unsigned fr = kNone;
+#pragma unroll
+    for (int j = 0; j < kFastPer; ++j)
+      if (bk[j] >= 0 && bm[j] != 0xFFFF) fr = min(fr, static_cast<unsigned>(bk[j] * kBlock + (__ffs(~bm[j]) - 1)));
+    fr = __reduce_min_sync(0xffffffffu, fr);
+    if (lane == 0) sh_wfree[warp] = fr;
+  }
+  // the last kept token must precede the new one
+  bool late = false;
+#pragma unroll
+  for (int j = 0; j < kFastPer; ++j) late |= (tid + j * kEpiThreads == n - 1) && ps[j] >= A.new_pos;
+
+  grid_dep_wait();      // the attention kernel's results are complete and visible
+  grid_dep_launch();
+
+  // split-K statistics of all kMaxSeg segments (in bounds), masked below
+  const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
+  float2 m0 = make_float2(-INFINITY, 0.f), m1 = make_float2(-INFINITY, 0.f);
+  if (A.has_q && warp < g) {
+    m0 = __ldcg(ml + lane * g + warp);
+    m1 = __ldcg(ml + (lane + 32) * g + warp);
+  }
+  const int nseg = A.has_q ? min(__ldcg(A.ws.lane_nseg_buf[cbuf] + l), kMaxSeg) : 0;
+  if (__syncthreads_or(late)) {
+    if (tid == 0) {
+      set_status(A.ws.status, ST_POSITION);
+      A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
+    }
+    return;
+  }
+  float* lg_s = reinterpret_cast<float*>(dsm);                 // [g][kFastN]
+  float* po_s = lg_s + 8 * kFastN;                             // [kPoSeg][g][d]
+  const float* po = A.ws.part_o_buf[cbuf] + static_cast<size_t>(l) * kMaxSeg * g * d;
+  if (A.has_q && tid == 0) {
+    const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
+    const uint32_t row = static_cast<uint32_t>((n + 3) & ~3) * 4u;   // 16-byte multiple, inside lcap
+    const uint32_t pob = static_cast<uint32_t>(kPoSeg * g * d) * 4u;
+    mbar_arrive_expect_tx(&sh_bar, row * g + pob);
+    if (row)
+      for (int h = 0; h < g; ++h) bulk_g2s(lg_s + h * kFastN, lg + static_cast<size_t>(h) * dm.lcap, row, &sh_bar);
+    bulk_g2s(po_s, po, pob, &sh_bar);
+  }
+  // per-head log-sum-exp of the split-K segments (one warp per head)
+  if (A.has_q && warp < g) {
+    const int h = warp;
+    if (lane >= nseg) m0 = make_float2(-INFINITY, 0.f);
+    if (lane + 32 >= nseg) m1 = make_float2(-INFINITY, 0.f);
+    const float M = warp_max(fmaxf(m0.x, m1.x));
+    const float s0 = m0.x == -INFINITY ? 0.f : exp2f(m0.x - M);
+    const float s1 = m1.x == -INFINITY ? 0.f : exp2f(m1.x - M);
+    sh_scale[lane][h] = s0;
+    sh_scale[lane + 32][h] = s1;
+    float Ls = m0.y * s0 + m1.y * s1;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+    if (lane == 0) {
+      sh_L[h] = Ls;
+      const float lse2 = M + log2f(Ls);
+      sh_lse2[h] = lse2;
+      A.lse[static_cast<size_t>(b) * dm.Hq + kh * g + h] = lse2 * kLn2;
+    }
+  }
+  __syncthreads();
+  unsigned pre_free = lane < kEpiThreads / 32 ? sh_wfree[lane] : kNone;
+  pre_free = __reduce_min_sync(0xffffffffu, pre_free);
+  if (A.has_q && !mbar_wait_bounded(&sh_bar, 0, A.ws.status)) (void)mbar_wait_bounded(&sh_bar, 0, A.ws.status);
+
+  // ---- weights -> scores; candidate minimum (key, position) -------------------------
+  if (A.has_q) {
+    float w[kFastPer];
+#pragma unroll
+    for (int j = 0; j < kFastPer; ++j) w[j] = 0.f;
+    if (g == 8) {
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        const float lse2 = sh_lse2[h];
+        const float* row = lg_s + h * kFastN + tid;
+#pragma unroll
+        for (int j = 0; j < kFastPer; ++j) w[j] += exp2f(row[j * kEpiThreads] - lse2);
+      }
+    } else {
+      for (int h = 0; h < g; ++h) {
+        const float lse2 = sh_lse2[h];
+        const float* row = lg_s + h * kFastN + tid;
+#pragma unroll
+        for (int j = 0; j < kFastPer; ++j) w[j] += exp2f(row[j * kEpiThreads] - lse2);
+      }
+    }
+#pragma unroll
+    for (int j = 0; j < kFastPer; ++j) sc[j] += w[j];
+  }
+  unsigned ck = kNone, cp = kNone;
+  int cs = -1, nan_count = 0;
+#pragma unroll
+  for (int j = 0; j < kFastPer; ++j) {
+    const int i = tid + j * kEpiThreads;
+    if (i < n) {
+      if (sc[j] != sc[j]) ++nan_count;
+      if (k == 1 && ps[j] < cut) {
+        const unsigned kk = static_cast<unsigned>(mono_key(sc[j]));
+        const unsigned pp = static_cast<unsigned>(ps[j]);
+        if (kk < ck || (kk == ck && pp < cp)) { ck = kk; cp = pp; cs = sl[j]; }
+      }
+    }
+  }
+  {
+    const unsigned wk = __reduce_min_sync(0xffffffffu, ck);
+    const unsigned wp = __reduce_min_sync(0xffffffffu, ck == wk ? cp : kNone);
+    const unsigned ws = __reduce_min_sync(0xffffffffu, (ck == wk && cp == wp) ? static_cast<unsigned>(cs) : kNone);
+    if (lane == 0) { sh_wkey[warp] = wk; sh_wpos[warp] = wp; sh_wslot[warp] = ws; }
+  }
+  if (nan_count) atomicAdd(&sh_nan, nan_count);
+  __syncthreads();
+  unsigned vkey, vpos, vslot_u;
+  {
+    const bool in = lane < kEpiThreads / 32;
+    const unsigned k1 = in ? sh_wkey[lane] : kNone, p1 = in ? sh_wpos[lane] : kNone;
+    const unsigned s1 = in ? sh_wslot[lane] : kNone;
+    vkey = __reduce_min_sync(0xffffffffu, k1);
+    vpos = __reduce_min_sync(0xffffffffu, k1 == vkey ? p1 : kNone);
+    vslot_u = __reduce_min_sync(0xffffffffu, (k1 == vkey && p1 == vpos) ? s1 : kNone);
+  }
+  const bool has_victim = k == 1 && vpos != kNone;   // positions are below 2^31
+  const int vslot = static_cast<int>(vslot_u);
+  const int vcount = has_victim ? 1 : 0;
+  // ---- eviction: the victim's slot is released; an emptied block is freed ---------
+  bool vslot_ok = false;
+  if (has_victim) {
+    if (vslot >= 0 && vslot < dm.P * kBlock) {
+      vslot_ok = true;
+      const int vb = vslot >> 4, vbit = 1 << (vslot & 15);
+#pragma unroll
+      for (int j = 0; j < kFastPer; ++j) {
+        if (bk[j] == vb) {
+          atomicAnd(&L.mask[vb], ~vbit);
+          if ((bm[j] & ~vbit) == 0) {
+            L.owner[vb] = -1;
+            sh_dead = tid + j * kEpiThreads;     // index of the block in the lane's list
+          }
+        }
+      }
+    } else if (vslot >= 0 && tid == 0) {
+      set_status(A.ws.status, ST_BAD_INDEX);
+    }
+  }
+  __syncthreads();
+  const int dead_j = sh_dead;
+  int nb2 = nb;
+  unsigned best;
+  if (dead_j < 0) {
+    // the victim's slot is now free too
+    best = min(pre_free, vslot_ok ? static_cast<unsigned>(vslot) : kNone);
+  } else {
+    // rare: the victim emptied its block; drop it from the list (the last
+    // entry moves into its place) and look for a free slot in the others
+    const int vb = vslot >> 4;
+    if (tid == 0) sh_tail = __ldcg(L.blocks + nb - 1);
+    unsigned fr = kNone;
+#pragma unroll
+    for (int j = 0; j < kFastPer; ++j)
+      if (bk[j] >= 0 && bk[j] != vb && bm[j] != 0xFFFF)
+        fr = min(fr, static_cast<unsigned>(bk[j] * kBlock + (__ffs(~bm[j]) - 1)));
+    fr = __reduce_min_sync(0xffffffffu, fr);
+    if (lane == 0) sh_wfree[warp] = fr;
+    __syncthreads();
+    if (tid == 0) {
+      L.blocks[dead_j] = sh_tail;
+      *L.nblocks = nb - 1;
+    }
+    best = lane < kEpiThreads / 32 ? sh_wfree[lane] : kNone;
+    best = __reduce_min_sync(0xffffffffu, best);
+    nb2 = nb - 1;
+    __syncthreads();
+  }
+  const bool need = best == kNone;
+  const int m = n - vcount;
+  // ---- admission into the lowest free slot; relocation plan --------------------------
+  if (!need && tid == 0) atomicOr(&L.mask[best >> 4], 1 << (best & 15));
+  __syncthreads();
+  int t_live = 0;
+  const int ndst = lane_plan(L, nb2, m + 1, false, dm.theta_f, need, &t_live, sh_scan2);
+  const bool work = need || ndst > 0;
+  if (tid == 0) {
+    A.ls.count[l] = m + 1;
+    if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
+    A.ws.need_admit[l] = need ? 1 : 0;
+    A.ws.want_dst[l] = ndst;
+    A.ws.plan_tlive[l] = t_live;
+    if (work) atomicOr(A.ws.work_flag, 1);
+    signal_done(A.ws, work, sh_last, sh_flag);
+    *sh_sig = 1;
+  }
+  // ---- the table: survivors shift over the victim; the new token goes last -----------
+#pragma unroll
+  for (int j = 0; j < kFastPer; ++j) {
+    const int i = tid + j * kEpiThreads;
+    if (i < n) {
+      const unsigned pp = static_cast<unsigned>(ps[j]);
+      if (has_victim && pp == vpos) {
+        A.victims[static_cast<size_t>(l) * dm.cap] = ps[j];
+      } else {
+        const int ni = (has_victim && pp > vpos) ? i - 1 : i;
+        if (ni != i) {
+          L.pos[ni] = ps[j];
+          L.slot[ni] = sl[j];
+        }
+        L.score[ni] = sc[j];
+      }
+    }
+  }
+  if (!need && tid < d) {
+    static_cast<KT*>(A.ls.k_pool)[static_cast<size_t>(best) * d + tid] = knv;
+    static_cast<KT*>(A.ls.v_pool)[static_cast<size_t>(best) * d + tid] = vnv;
+  }
+  if (tid == 0) {
+    L.pos[m] = A.new_pos;
+    L.slot[m] = need ? -1 : static_cast<int>(best);
+    L.score[m] = 0.f;
+    A.n_victims[l] = vcount;
+    if (vcount) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_VICTIMS]), 1ull);
+    if (dead_j >= 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_FREED_DEAD]), 1ull);
+    if (sh_nan) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_NAN_KEYS]), (unsigned long long)sh_nan);
+    if (l == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_STEPS]), 1ull);
+  }
+  // ---- output: combine the split-K partial outputs (the first kPoSeg from
+  // shared memory), two interleaved chains per output ---------------------------------
+  if (A.has_q) {
+    const int ns = min(nseg, kPoSeg);
+    for (int he = tid; he < g * d; he += kEpiThreads) {
+      const int h = he / d, e = he - h * d;
+      float a0 = 0.f, a1 = 0.f;
+      int s2 = 0;
+      for (; s2 + 1 < ns; s2 += 2) {
+        a0 = fmaf(po_s[(s2 * g + h) * d + e], sh_scale[s2][h], a0);
+        a1 = fmaf(po_s[((s2 + 1) * g + h) * d + e], sh_scale[s2 + 1][h], a1);
+      }
+      if (s2 < ns) a0 = fmaf(po_s[(s2 * g + h) * d + e], sh_scale[s2][h], a0);
+      for (s2 = kPoSeg; s2 < nseg; ++s2)
+        a1 = fmaf(__ldcg(po + (static_cast<size_t>(s2) * g + h) * d + e), sh_scale[s2][h], a1);
+      A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = (a0 + a1) / sh_L[h];
+    }
+  }
+}
+
 template <typename KT>
 __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs A) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ int sh_scan[40];
-  __shared__ int sh_work, sh_last, sh_flag;
+  __shared__ int sh_work, sh_last, sh_flag, sh_sig;
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   LaneRefs L = lane_refs(A.ls, dm, l);
-  // The token count (and, on the fast path, the token table) is not written
-  // by the attention kernel: it is read before the dependency wait, while
-  // the attention kernel drains.
+  // The token count (and, on the fast path, the token table and the block
+  // list) is not written by the attention kernel: it is read before the
+  // dependency wait, while the attention kernel drains.
   const int n = __ldcg(A.ls.count + l);
-  if (tid == 0) sh_work = 0;
+  if (tid == 0) { sh_work = 0; sh_sig = 0; }
   if (n < 0 || n >= dm.cap) {
     grid_dep_wait();
     grid_dep_launch();
@@ -73,20 +397,18 @@ __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs
       set_status(A.ws.status, ST_CAPACITY);
       A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
     }
+  } else if (dm.policy == KVEVICT_H2O && n + 1 - dm.budget <= 1 && n <= kFastN && dm.g <= 8 && dm.d <= 128) {
+    h2o_fast_step<KT>(A, L, n, dsm, &sh_sig, &sh_last, &sh_flag);
   } else {
     lane_step<KT>(A, L, n, dsm, &sh_work);
   }
-  // The last CTA of the grid to finish runs the layer allocator, if any lane
-  // asked for blocks: the done counter carries the number of such lanes in
-  // its upper bits, so the common no-work case needs no further atomic.
   __syncthreads();
-  if (tid == 0) {
-    __threadfence();
-    const int old = atomicAdd(A.ws.epi_done, 1 + (sh_work ? kWorkUnit : 0));
-    sh_last = (old & (kWorkUnit - 1)) == static_cast<int>(gridDim.x) - 1;
-    sh_flag = (old >> kWorkShift) + (sh_work ? 1 : 0);
+  if (!sh_sig) {
+    if (tid == 0) signal_done(A.ws, sh_work != 0, &sh_last, &sh_flag);
+    __syncthreads();
   }
-  __syncthreads();
+  // The last CTA of the grid to finish runs the layer allocator, if any lane
+  // asked for blocks.
   if (sh_last) {
     if (sh_flag == 0) {
       if (tid == 0) { *A.ws.epi_done = 0; A.ws.counters[1] = 0; A.ws.counters[2] = 0; }
@@ -110,226 +432,11 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   __shared__ unsigned sh_min[32];
   __shared__ int sh_nan;
   __shared__ float sh_scale[kMaxSeg][kMaxG];
-  __shared__ uint64_t sh_bar;
   float* sh_rows = reinterpret_cast<float*>(dsm);      // general path: 128 * kMaxW floats
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
   const int cbuf = A.layer & 1;
-
-  // ---- H2O with at most one victim (the steady state of a full cache) --------
-  // Before the dependency wait: the lane's token table (kFastPer tokens a
-  // thread), its block count and the new token's K/V row, none of which the
-  // attention kernel writes.  After it: the logits and the split-K partial
-  // outputs arrive in shared memory by bulk copy (one mbarrier), the split-K
-  // statistics by plain loads.  Weights, new scores and the candidate minimum
-  // come from registers and shared memory; survivors are written straight to
-  // their index after the removal.
-  if (dm.policy == KVEVICT_H2O && n + 1 - dm.budget <= 1 && n <= kFastN && g <= 8 && d <= 128) {
-    const int k = max(0, n + 1 - dm.budget);
-    const int cut = A.new_pos - dm.R + 1;
-    const int warp = tid >> 5, lane = tid & 31;
-    float sc[kFastPer];
-    int ps[kFastPer], sl[kFastPer];
-#pragma unroll
-    for (int j = 0; j < kFastPer; ++j) {
-      const int i = tid + j * kEpiThreads;
-      const bool ok = i < n;
-      sc[j] = ok ? __ldcg(L.score + i) : 0.f;
-      ps[j] = ok ? __ldcg(L.pos + i) : 0x7FFFFFFF;
-      sl[j] = ok ? __ldcg(L.slot + i) : -1;
-    }
-    int nb = __ldcg(L.nblocks);
-    KT knv{}, vnv{};
-    if (tid < d) {
-      knv = static_cast<const KT*>(A.k_new)[static_cast<size_t>(l) * d + tid];
-      vnv = static_cast<const KT*>(A.v_new)[static_cast<size_t>(l) * d + tid];
-    }
-    if (tid == 0) {
-      sh_nan = 0;
-      mbar_init(&sh_bar, 1);
-      asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    }
-    // the last kept token must precede the new one
-    bool late = false;
-#pragma unroll
-    for (int j = 0; j < kFastPer; ++j) late |= (tid + j * kEpiThreads == n - 1) && ps[j] >= A.new_pos;
-    grid_dep_wait();      // the attention kernel's results are complete and visible
-    grid_dep_launch();
-    if (__syncthreads_or(late)) {
-      if (tid == 0) {
-        set_status(A.ws.status, ST_POSITION);
-        A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
-      }
-      return;
-    }
-    float* lg_s = reinterpret_cast<float*>(dsm);                 // [g][kFastN]
-    float* po_s = lg_s + 8 * kFastN;                             // [kPoSeg][g][d]
-    const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
-    const float* po = A.ws.part_o_buf[cbuf] + static_cast<size_t>(l) * kMaxSeg * g * d;
-    if (A.has_q && tid == 0) {
-      const uint32_t row = static_cast<uint32_t>((n + 3) & ~3) * 4u;   // 16-byte multiple, inside lcap
-      const uint32_t pob = static_cast<uint32_t>(kPoSeg * g * d) * 4u;
-      mbar_arrive_expect_tx(&sh_bar, row * g + pob);
-      if (row)
-        for (int h = 0; h < g; ++h) bulk_g2s(lg_s + h * kFastN, lg + static_cast<size_t>(h) * dm.lcap, row, &sh_bar);
-      bulk_g2s(po_s, po, pob, &sh_bar);
-    }
-    const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
-    const int nseg = A.has_q ? min(__ldcg(A.ws.lane_nseg_buf[cbuf] + l), kMaxSeg) : 0;
-    // per-head log-sum-exp of the split-K segments (one warp per head)
-    if (A.has_q && warp < g) {
-      const int h = warp;
-      const float2 m0 = lane < nseg ? __ldcg(ml + lane * g + h) : make_float2(-INFINITY, 0.f);
-      const float2 m1 = lane + 32 < nseg ? __ldcg(ml + (lane + 32) * g + h) : make_float2(-INFINITY, 0.f);
-      const float M = warp_max(fmaxf(m0.x, m1.x));
-      const float s0 = m0.x == -INFINITY ? 0.f : exp2f(m0.x - M);
-      const float s1 = m1.x == -INFINITY ? 0.f : exp2f(m1.x - M);
-      sh_scale[lane][h] = s0;
-      sh_scale[lane + 32][h] = s1;
-      float Ls = m0.y * s0 + m1.y * s1;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-      if (lane == 0) {
-        sh_L[h] = Ls;
-        const float lse2 = M + log2f(Ls);
-        sh_lse2[h] = lse2;
-        A.lse[static_cast<size_t>(b) * dm.Hq + kh * g + h] = lse2 * kLn2;
-      }
-    }
-    __syncthreads();
-    if (A.has_q && !mbar_wait_bounded(&sh_bar, 0, A.ws.status)) (void)mbar_wait_bounded(&sh_bar, 0, A.ws.status);
-    unsigned long long best_k = ~0ull;
-    uint32_t best_p = 0xFFFFFFFFu;
-    int best_i = -1, nan_count = 0;
-#pragma unroll
-    for (int j = 0; j < kFastPer; ++j) {
-      const int i = tid + j * kEpiThreads;
-      if (i < n) {
-        if (A.has_q) {
-          float w = 0.f;
-#pragma unroll
-          for (int h = 0; h < 8; ++h)
-            if (h < g) w += exp2f(lg_s[h * kFastN + i] - sh_lse2[h]);
-          sc[j] += w;
-        }
-        if (sc[j] != sc[j]) ++nan_count;
-        if (k == 1 && ps[j] < cut) {
-          const unsigned long long kk = mono_key(sc[j]);
-          if (kk < best_k || (kk == best_k && static_cast<uint32_t>(ps[j]) < best_p)) {
-            best_k = kk; best_p = static_cast<uint32_t>(ps[j]); best_i = i;
-          }
-        }
-      }
-    }
-    // output: combine the split-K partial outputs (the first kPoSeg from
-    // shared memory); its loads overlap the argmin's barriers
-    if (A.has_q) {
-      for (int he = tid; he < g * d; he += kEpiThreads) {
-        const int h = he / d, e = he - h * d;
-        float acc = 0.f;
-        const int ns = min(nseg, kPoSeg);
-        for (int s2 = 0; s2 < ns; ++s2) acc = fmaf(po_s[(s2 * g + h) * d + e], sh_scale[s2][h], acc);
-        for (int s2 = kPoSeg; s2 < nseg; ++s2) acc = fmaf(__ldcg(po + (static_cast<size_t>(s2) * g + h) * d + e), sh_scale[s2][h], acc);
-        A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = acc / sh_L[h];
-      }
-    }
-    const int v = (k == 1) ? block_argmin3(best_k, best_p, best_i, sh_hist, sh_misc) : -1;
-    if (tid == 0) { sh_misc[0] = -1; sh_misc[1] = -1; }
-    __syncthreads();
-    // scatter the survivors; the victim's owner releases its slot
-#pragma unroll
-    for (int j = 0; j < kFastPer; ++j) {
-      const int i = tid + j * kEpiThreads;
-      if (i < n) {
-        if (i == v) {
-          A.victims[static_cast<size_t>(l) * dm.cap] = ps[j];
-          const int s = sl[j];
-          int dead_blk = -1;
-          if (s >= 0 && s < dm.P * kBlock) {
-            const int bb = s >> 4, bit = 1 << (s & 15);
-            const int old = atomicAnd(&L.mask[bb], ~bit);
-            if ((old & ~bit) == 0 && (old & bit)) {
-              L.owner[bb] = -1;
-              dead_blk = bb;
-            }
-          } else if (s >= 0) {
-            set_status(A.ws.status, ST_BAD_INDEX);
-          }
-          sh_misc[0] = dead_blk;
-          sh_misc[1] = s;
-        } else {
-          const int ni = (v >= 0 && i > v) ? i - 1 : i;
-          if (ni != i) {
-            L.pos[ni] = ps[j];
-            L.slot[ni] = sl[j];
-          }
-          L.score[ni] = sc[j];
-        }
-      }
-    }
-    if (nan_count) atomicAdd(&sh_nan, nan_count);
-    __syncthreads();
-    const int vcount = v >= 0 ? 1 : 0;
-    const int dead_blk = sh_misc[0], vslot = sh_misc[1];
-    if (dead_blk >= 0) {
-      for (int j = tid; j < nb; j += kEpiThreads) {
-        if (L.blocks[j] == dead_blk) {
-          L.blocks[j] = L.blocks[nb - 1];
-          *L.nblocks = nb - 1;
-        }
-      }
-      __syncthreads();
-      nb -= 1;
-    }
-    const int m = n - vcount;
-    // admission: the lowest free slot of the lane's blocks; with exactly one
-    // hole left and it being the victim's, no scan is needed
-    const int holes = nb * kBlock - m;
-    unsigned best = 0xFFFFFFFFu;
-    if (holes == 1 && vcount == 1 && dead_blk < 0 && vslot >= 0) {
-      best = static_cast<unsigned>(vslot);
-    } else if (holes > 0) {
-      for (int j = tid; j < nb; j += kEpiThreads) {
-        const int blk = L.blocks[j];
-        const int mk = L.mask[blk] & 0xFFFF;
-        if (mk != 0xFFFF) best = min(best, static_cast<unsigned>(blk * kBlock + (__ffs(~mk) - 1)));
-      }
-      best = warp_min(best);
-      if ((tid & 31) == 0) sh_min[tid >> 5] = best;
-      __syncthreads();
-      best = 0xFFFFFFFFu;
-      for (int w = 0; w < kEpiThreads / 32; ++w) best = min(best, sh_min[w]);
-    }
-    const bool need = best == 0xFFFFFFFFu;
-    if (!need && tid < d) {
-      static_cast<KT*>(A.ls.k_pool)[static_cast<size_t>(best) * d + tid] = knv;
-      static_cast<KT*>(A.ls.v_pool)[static_cast<size_t>(best) * d + tid] = vnv;
-    }
-    int t_live = 0;
-    const int ndst = lane_plan(L, nb, m + 1, false, dm.theta_f, need, &t_live, sh_scan);
-    if (tid == 0) {
-      if (!need) atomicOr(&L.mask[best >> 4], 1 << (best & 15));
-      L.pos[m] = A.new_pos;
-      L.slot[m] = need ? -1 : static_cast<int>(best);
-      L.score[m] = 0.f;
-      A.ls.count[l] = m + 1;
-      if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
-      A.n_victims[l] = vcount;
-      A.ws.need_admit[l] = need ? 1 : 0;
-      A.ws.want_dst[l] = ndst;
-      A.ws.plan_tlive[l] = t_live;
-      if (need || ndst > 0) {
-        atomicOr(A.ws.work_flag, 1);
-        *sh_work = 1;
-      }
-      if (vcount) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_VICTIMS]), 1ull);
-      if (dead_blk >= 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_FREED_DEAD]), 1ull);
-      if (sh_nan) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_NAN_KEYS]), (unsigned long long)sh_nan);
-      if (l == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_STEPS]), 1ull);
-    }
-    return;
-  }
 
   // ---- general path ------------------------------------------------------------
   grid_dep_wait();      // the attention kernel's results are complete and visible

@@ -232,9 +232,15 @@ __device__ __forceinline__ int lane_plan(const LaneRefs& L, int nb, int n_live, 
                          bool pending_admit, int* t_live_out, int* sh_scan) {
   const int N = nb + (pending_admit ? 1 : 0);
   if (N == 0) { *t_live_out = 0; return 0; }
-  // Eq. (1) over the lane's blocks, in double (theta_f is widened exactly)
-  const double Fd = 1.0 - static_cast<double>(n_live) / (static_cast<double>(N) * kBlock);
-  if (!forced && !(Fd > static_cast<double>(theta_f))) { *t_live_out = 0; return 0; }
+  // Eq. (1) over the lane's blocks, in double (theta_f is widened exactly);
+  // one lane of each warp divides (double arithmetic is slow on this part)
+  int over = 0;
+  if ((threadIdx.x & 31) == 0) {
+    const double Fd = 1.0 - static_cast<double>(n_live) / (static_cast<double>(N) * kBlock);
+    over = Fd > static_cast<double>(theta_f) ? 1 : 0;
+  }
+  over = __shfl_sync(0xffffffffu, over, 0);
+  if (!forced && !over) { *t_live_out = 0; return 0; }
   int src = 0, tl = 0;
   for (int j = threadIdx.x; j < nb; j += blockDim.x) {
     const int c = __popc(L.mask[L.blocks[j]] & 0xFFFF);
