@@ -45,6 +45,12 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-layers", type=int, default=0,
                     help="profiling only: run the workload with this many layers (not a bench number)")
+    ap.add_argument("--kernel-table", action="store_true",
+                    help="time the engine's other kernels on their own workloads (DropKV window scoring at "
+                         "32K and 128K, selection, forced compaction, the SnapKV and toy decode steps), one "
+                         "JSON line each, instead of the decode-step bench line")
+    ap.add_argument("--only", default="",
+                    help="with --kernel-table: comma-separated subset of d3_32k, d3_128k, snapkv, toy")
     return ap.parse_args()
 
 
@@ -478,10 +484,168 @@ def run_reference(args):
     print(json.dumps(line))
 
 
+# ---------------------------------------------------------------------------
+# kernel table: the other kernels, each on its own workload
+# ---------------------------------------------------------------------------
+def tensor_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        try:
+            return float(json.load(open(p))["bf16_tflops"]), "measured"
+        except (KeyError, ValueError):
+            pass
+    return 1900.0, "fallback"
+
+
+def run_kernel_table(args):
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    from kv_cache_token_gb300 import Engine, config_from
+    from workloads import Workload, shape
+
+    hbm, hbm_kind = hbm_peak()
+    tc, tc_kind = tensor_peak()
+    only = set(x for x in args.only.split(",") if x)
+    stream = torch.cuda.current_stream()
+
+    def timed(fn, reps, warm=2):
+        for _ in range(warm):
+            fn()
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+        torch.cuda.synchronize()
+        for a, b in evs:
+            a.record(stream)
+            fn()
+            b.record(stream)
+        torch.cuda.synchronize()
+        ms = sorted(a.elapsed_time(b) for a, b in evs)
+        return ms[len(ms) // 2], ms[max(0, len(ms) // 10)], ms[min(len(ms) - 1, (9 * len(ms)) // 10)]
+
+    def emit(row, workload, ms, p10, p90, nbytes=None, flops=None, extra=None):
+        line = {"kernel_table": row, "workload": workload, "ms_median": round(ms, 4), "ms_p10": round(p10, 4),
+                "ms_p90": round(p90, 4)}
+        fr = {}
+        if nbytes is not None:
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            line["hbm"] = {"algorithmic_bytes": int(nbytes), "achieved_gbs": round(gbs, 1), "peak_gbs": hbm,
+                           "peak_kind": hbm_kind, "frac": round(gbs / hbm, 4)}
+            fr["hbm"] = gbs / hbm
+        if flops is not None:
+            tf = flops / (ms * 1e-3) / 1e12
+            line["tensor"] = {"flops": int(flops), "achieved_tflops": round(tf, 1), "peak_tflops": tc,
+                              "peak_kind": tc_kind, "frac": round(tf / tc, 4)}
+            fr["tensor"] = tf / tc
+        if fr:
+            line["bound"] = max(fr, key=fr.get)
+        if extra:
+            line.update(extra)
+        print(json.dumps(line), flush=True)
+
+    # D3 window scoring, selection and (128K) forced compaction
+    for tag, name in (("d3_32k", "dropkv_prefill"), ("d3_128k", "paged_128k")):
+        if only and tag not in only:
+            continue
+        shp = shape(name)
+        wl = Workload(shp)
+        eng = Engine(config_from(shp))
+        eng.reset()
+        K, V = wl.context(0, device="cuda")
+        eng.prefill(0, K, V)
+        del K, V
+        q, qp = wl.window(0, device="cuda")
+        lanes, w, g, d, n = eng.lanes, shp.window, shp.group, shp.head_dim, shp.ctx
+        lse = torch.empty((shp.batch, shp.num_q_heads, w), dtype=torch.float32, device="cuda")
+        a_out = torch.empty((shp.batch, shp.num_q_heads, w, d), dtype=torch.float32, device="cuda")
+        scores = torch.zeros((lanes, shp.max_tokens), dtype=torch.float32, device="cuda")
+        ms, p10, p90 = timed(lambda: eng.score(0, q, qp, lse, a_out, scores), reps=10)
+        # K and V read once per pass; QK^T and PV (pass 1), QK^T and a V^T (pass 2), full key range per row
+        rows = g * w
+        emit("D3 DropKV window scoring (pass 1, combine, pass 2, finalize)", name, ms, p10, p90,
+             nbytes=2 * lanes * n * 2 * d * 2, flops=4 * 2 * lanes * rows * n * d)
+        pos, cnt = eng.positions[0], eng.counts[0]
+        victims = torch.full((lanes, shp.max_tokens), -1, dtype=torch.int32, device="cuda")
+        nvic = torch.zeros((lanes,), dtype=torch.int32, device="cuda")
+        ms, p10, p90 = timed(lambda: eng.select(scores, pos, cnt, shp.budget, shp.recent_window, victims, nvic),
+                             reps=10)
+        emit("D4 bottom-k selection (radix descent on (key, position))", name, ms, p10, p90,
+             nbytes=lanes * n * (4 + 4))
+        if tag == "d3_128k":
+            samples = []
+            for rep in range(3):
+                if rep:
+                    eng.reset()
+                    K, V = wl.context(0, device="cuda")
+                    eng.prefill(0, K, V)
+                    del K, V
+                    eng.score(0, q, qp, lse, a_out, scores)
+                    eng.select(scores, pos, cnt, shp.budget, shp.recent_window, victims, nvic)
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                freed, n_freed, moves, n_moves = eng.compact(0, victims, nvic)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                samples.append(e0.elapsed_time(e1))
+            moved, nf = int(n_moves.item()), int(n_freed.item())
+            st = eng.stats(0).cpu().tolist()
+            samples.sort()
+            emit("D5 token-level compaction (plan, allocate, gather, release)", name, samples[1], samples[0],
+                 samples[-1], nbytes=moved * 2 * d * 2 * 2 + int(nvic.sum().item()) * 3 * 4,
+                 extra={"moved_tokens": moved, "freed_blocks": nf, "blocks_after": st[9], "live_after": st[10]})
+        code, msg = eng.last_error()
+        assert code == 0, msg
+        del eng
+        torch.cuda.empty_cache()
+
+    # decode steps of the SnapKV workload and of the H2O toy (latency-bound)
+    for tag, name, first in (("snapkv", "snapkv_decode", 1), ("toy", "h2o_toy", 1)):
+        if only and tag not in only:
+            continue
+        shp = shape(name)
+        wl = Workload(shp)
+        eng = Engine(config_from(shp))
+        eng.reset()
+        K, V = wl.context(0, device="cuda")
+        eng.prefill(0, K, V)
+        del K, V
+        steps = [wl.step(0, t, device="cuda") for t in range(shp.steps)]
+        B, Hq, d = shp.batch, shp.num_q_heads, shp.head_dim
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        for t in range(first):
+            q, kn, vn, p = steps[t]
+            eng.decode_step(0, q, kn, vn, p, out, lse)
+        torch.cuda.synchronize()
+        n_before = int(eng.counts[0].sum().item())
+        timed_steps = list(range(first, shp.steps))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for t in timed_steps:
+            q, kn, vn, p = steps[t]
+            eng.decode_step(0, q, kn, vn, p, out, lse)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1) / len(timed_steps)
+        lanes = eng.lanes
+        es = 2 if shp.kv_dtype == "bf16" else 4
+        per_tok = 2 * d * es + (4 + 4 * shp.obs_window + 8 if shp.policy == 1 else 8)
+        emit("decode step (attention, score epilogue, selection, eviction, admission)", name, ms, ms, ms,
+             nbytes=(n_before + lanes) * per_tok,
+             extra={"steps_timed": len(timed_steps), "us_per_step": round(ms * 1e3, 2),
+                    "note": "back-to-back steps through the C ABI; small per-step work, launch-latency bound"})
+        code, msg = eng.last_error()
+        assert code == 0, msg
+        del eng
+        torch.cuda.empty_cache()
+
+
 def main():
     args = parse()
     if args.impl == "reference":
         run_reference(args)
+    elif args.kernel_table:
+        run_kernel_table(args)
     else:
         run_gpu(args)
 
