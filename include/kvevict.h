@@ -226,6 +226,7 @@ kvevict_status kvevict_finish_step(kvevict_ctx* ctx, int layer, const void* q, c
  * Writes lse [B][Hq][w] (fp32, natural log), a_out [B][Hq][w][d] (fp32 attention
  * outputs) and scores[lane][j] (fp32, [B*Hkv][max_tokens], kept order) =
  * sum over the group's rows of p/(1-p) * ||a - v_j|| (+inf where 1-p <= 0).
+ * q_win and a_out must be 16-byte aligned (KVEVICT_E_INVALID_ARG otherwise).
  * q_win == NULL is inert: nothing is written. */
 kvevict_status kvevict_score(kvevict_ctx* ctx, int layer, const void* q_win, int32_t w,
                              const int32_t* q_pos, float* lse, float* a_out, float* scores,

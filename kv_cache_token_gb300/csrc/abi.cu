@@ -290,6 +290,8 @@ kvevict_status kvevict_score(kvevict_ctx* ctx, int layer, const void* q_win, int
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L) return KVEVICT_E_INVALID_ARG;
   if (!q_win) return KVEVICT_OK;   // null attention is inert
   if (w < 1 || w > ctx->c.dims.max_window || !q_pos || !lse || !a_out || !scores) return KVEVICT_E_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(q_win) % 16 || reinterpret_cast<uintptr_t>(a_out) % 16)
+    return KVEVICT_E_INVALID_ARG;   // 16-byte row copies and stores
   if (ctx->c.dims.dtype != KVEVICT_BF16 || ctx->c.dims.d != 128) return KVEVICT_E_DTYPE;
   return cuda_status(kve::launch_score(ctx->c, layer, q_win, w, q_pos, lse, a_out, scores,
                                        static_cast<cudaStream_t>(stream)));

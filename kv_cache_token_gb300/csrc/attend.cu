@@ -585,6 +585,7 @@ cudaError_t prepare_kernels(Ctx& ctx) {
   if (e == cudaSuccess) e = set_attr<64, 1>();
   if (e == cudaSuccess) e = set_attr<64, 2>();
   if (e == cudaSuccess) e = prepare_epilogue();
+  if (e == cudaSuccess) e = prepare_dropkv();
   if (e != cudaSuccess) return e;
   const Dims& dm = ctx.dims;
   const int nt = dm.g > 8 ? 2 : 1;

@@ -14,6 +14,7 @@
 //   CTA's rows -> one partial per row group.
 // finalize: scores = sum of the row-group partials.
 #include "kvevict_internal.cuh"
+#include "tcgen05.cuh"
 
 namespace kve {
 namespace {
@@ -273,52 +274,67 @@ __global__ void __launch_bounds__(kWarps * 32) d3_pass1_kernel(D3Args A) {
 }
 
 // ---------------------------------------------------------------------------
-// combine: grid (lanes), one warp per row
+// combine: grid (row groups of 8, lanes), one warp per row; the chunks'
+// (max, sum) in lanes of the warp, then each lane accumulates 4 of the d
+// columns over the chunks.
 // ---------------------------------------------------------------------------
 __global__ void __launch_bounds__(256) d3_combine_kernel(D3Args A) {
-  const int l = blockIdx.x;
+  const int l = blockIdx.y;
+  const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
+  if (r >= A.rows) return;
   const int n = min(max(A.ls.count[l], 0), A.dm.cap);
   const int nch = (n + kChunk - 1) / kChunk;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
   const size_t stride = kD + 2;
   const size_t chunk_stride = static_cast<size_t>(A.rows_cap) * stride;
-  for (int r = warp; r < A.rows; r += blockDim.x >> 5) {
-    const int h = r / A.w, i = r % A.w;
-    const float* base = A.ws.d3_part + static_cast<size_t>(l) * A.chunks * chunk_stride + static_cast<size_t>(r) * stride;
-    float M = -INFINITY;
-    for (int c = 0; c < nch; ++c) M = fmaxf(M, base[c * chunk_stride + kD]);
-    float Ls = 0.f;
-    float acc[4] = {0.f, 0.f, 0.f, 0.f};
-    for (int c = 0; c < nch; ++c) {
-      const float m = base[c * chunk_stride + kD];
-      if (m == -INFINITY) continue;
-      const float sc = exp2f(m - M);
-      Ls += base[c * chunk_stride + kD + 1] * sc;
+  const int h = r / A.w, i = r % A.w;
+  const float* base = A.ws.d3_part + static_cast<size_t>(l) * A.chunks * chunk_stride + static_cast<size_t>(r) * stride;
+  float M = -INFINITY;
+  for (int c = lane; c < nch; c += 32) M = fmaxf(M, base[c * chunk_stride + kD]);
+  M = warp_max(M);
+  float Lp = 0.f;
+  for (int c = lane; c < nch; c += 32) {
+    const float m = base[c * chunk_stride + kD];
+    if (m != -INFINITY) Lp += base[c * chunk_stride + kD + 1] * exp2f(m - M);
+  }
+  for (int o = 16; o > 0; o >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, o);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+  for (int c = 0; c < nch; ++c) {
+    const float m = base[c * chunk_stride + kD];
+    const float sc = m == -INFINITY ? 0.f : exp2f(m - M);
+    // partial rows are 130 floats: 8-byte aligned, so two float2 loads
+    const float2 x0 = *reinterpret_cast<const float2*>(base + c * chunk_stride + lane * 4);
+    const float2 x1 = *reinterpret_cast<const float2*>(base + c * chunk_stride + lane * 4 + 2);
+    acc[0] = fmaf(x0.x, sc, acc[0]);
+    acc[1] = fmaf(x0.y, sc, acc[1]);
+    acc[2] = fmaf(x1.x, sc, acc[2]);
+    acc[3] = fmaf(x1.y, sc, acc[3]);
+  }
+  const float lse2 = M + log2f(Lp);
+  const size_t orow = (static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i;
+  const size_t wrow = static_cast<size_t>(l) * A.rows_cap + r;
+  float nrm = 0.f;
+  float av[4];
 #pragma unroll
-      for (int u = 0; u < 4; ++u) acc[u] += base[c * chunk_stride + lane + 32 * u] * sc;
-    }
-    const float lse2 = M + log2f(Ls);
-    const size_t orow = (static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i;
-    float nrm = 0.f;
-    const size_t wrow = static_cast<size_t>(l) * A.rows_cap + r;
+  for (int u = 0; u < 4; ++u) {
+    av[u] = acc[u] / Lp;
+    nrm += av[u] * av[u];
+  }
+  *reinterpret_cast<float4*>(A.a_out + orow * kD + lane * 4) = make_float4(av[0], av[1], av[2], av[3]);
 #pragma unroll
-    for (int u = 0; u < 4; ++u) {
-      const float a = acc[u] / Ls;
-      const int e = lane + 32 * u;
-      A.a_out[orow * kD + e] = a;
-      nrm += a * a;
-      const __nv_bfloat16 hi = __float2bfloat16_rn(a);
-      const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
-      A.ws.d3_ahi[wrow * kD + e] = hi;
-      A.ws.d3_alo[wrow * kD + e] = lo;
-    }
-    for (int o = 16; o > 0; o >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o);
-    if (lane == 0) {
-      A.lse_out[orow] = lse2 * kLn2;
-      A.ws.d3_rowc[wrow * 2 + 0] = lse2;
-      A.ws.d3_rowc[wrow * 2 + 1] = nrm;
-    }
+  for (int u = 0; u < 4; u += 2) {
+    const __nv_bfloat162 hi = __floats2bfloat162_rn(av[u], av[u + 1]);
+    const float2 hf = __bfloat1622float2(hi);
+    const __nv_bfloat162 lo = __floats2bfloat162_rn(av[u] - hf.x, av[u + 1] - hf.y);
+    *reinterpret_cast<__nv_bfloat162*>(A.ws.d3_ahi + wrow * kD + lane * 4 + u) = hi;
+    *reinterpret_cast<__nv_bfloat162*>(A.ws.d3_alo + wrow * kD + lane * 4 + u) = lo;
+  }
+  for (int o = 16; o > 0; o >>= 1) nrm += __shfl_xor_sync(0xffffffffu, nrm, o);
+  if (lane == 0) {
+    A.lse_out[orow] = lse2 * kLn2;
+    A.ws.d3_rowc[wrow * 2 + 0] = lse2;
+    A.ws.d3_rowc[wrow * 2 + 1] = nrm;
   }
 }
 
@@ -456,9 +472,537 @@ __global__ void __launch_bounds__(256) d3_finalize_kernel(D3Args A, int groups) 
   }
 }
 
+// ---------------------------------------------------------------------------
+// tcgen05 path: all window rows of a lane (up to 256 = two 128-row tiles) per
+// CTA, one thread per row, accumulators in tensor memory.
+//
+// pass 1, per 64-key tile:  S = Q K^T (Q and K in shared memory, 128-byte
+//   swizzle); each thread masks and exponentiates its row (lazy rescale of
+//   the running max), writes P as bf16 hi + lo over S in tensor memory, and
+//   O += P V takes P from tensor memory and V (MN-major) from shared memory.
+//   Tensor-memory columns: O of tile 0 / 1 at 0 / 128; S-P double buffer at
+//   256 + 128 * (t & 1) (+ 64 for row tile 1).
+// pass 2, per 64-key tile:  S = Q K^T and G = a V^T (a as bf16 hi + lo held
+//   in tensor memory); the next tile's MMAs run while each thread turns its
+//   row of S and G into residual terms; the 256 rows are summed per key by a
+//   warp butterfly and shared memory, and the CTA writes the final scores.
+//   Tensor-memory columns: a hi 0 / 64, a lo 128 / 192, S 256 / 320,
+//   G 384 / 448.
+// K/V tiles arrive by 16-byte cp.async into a three-stage ring, each chunk
+// placed at its swizzled position.
+// ---------------------------------------------------------------------------
+constexpr int kTcKeys = 64;
+constexpr int kTcStages = 3;
+constexpr int kTcThreads = 256;
+constexpr int kTcRows = 256;
+constexpr int kTcHalf = kTcKeys * 128;                 // one d half of a K or V tile (8 KB)
+constexpr int kTcKV = 4 * kTcHalf;                     // K (2 halves) then V (2 halves)
+constexpr int kTcQ = 2 * 2 * 128 * 128;                // [row tile][d half][128 rows][128 B]
+constexpr int kTcSmem = kTcQ + kTcStages * kTcKV + 1024;
+constexpr uint32_t kTcCols = 512;
+constexpr float kTcRescale = 8.f;
+constexpr uint32_t kIdS = tc::idesc_bf16(128, kTcKeys, 0);
+constexpr uint32_t kIdPV = tc::idesc_bf16(128, kD, 1);
+static_assert(kChunk % kTcKeys == 0, "chunks hold whole tiles");
+
+// Hardware approximations (PTX ex2/rcp/sqrt .approx.ftz, relative error
+// about 2^-22; results below 2^-126 flush to zero).
+__device__ __forceinline__ float hw_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float hw_rcp(float x) {
+  float y;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float hw_sqrt(float x) {
+  float y;
+  asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
+  const uint32_t a = smem_u32(p);
+  return p + (((a + 1023u) & ~1023u) - a);
+}
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+// byte offset of bf16 element e of key row k in a swizzled K or V tile
+__device__ __forceinline__ int sw_off(int k, int e) {
+  return (e >> 6) * kTcHalf + k * 128 + ((((e & 63) >> 3) ^ (k & 7)) << 4) + (e & 7) * 2;
+}
+
+// Loads (cp.async) and zero fills of one CTA's Q rows and K/V tiles.
+struct TcLoader {
+  const D3Args& A;
+  unsigned char* kv;
+  int (*pos)[kTcKeys];
+  size_t lo;
+  int j_begin, j_end, ntiles, key, part;
+  int nx_slot, nx_pos;
+  __device__ TcLoader(const D3Args& a, unsigned char* kv_, int (*pos_)[kTcKeys], int l, int jb, int je, int nt)
+      : A(a), kv(kv_), pos(pos_), lo(static_cast<size_t>(l) * a.dm.cap), j_begin(jb), j_end(je), ntiles(nt),
+        key(threadIdx.x >> 2), part(threadIdx.x & 3), nx_slot(-1), nx_pos(0x7FFFFFFF) {}
+  // slot and position of this thread's key in `tile` (consumed by the next issue)
+  __device__ void fetch(int tile) {
+    const int j = j_begin + tile * kTcKeys + key;
+    nx_slot = -1;
+    nx_pos = 0x7FFFFFFF;
+    if (tile < ntiles && j < j_end) {
+      int s = A.ls.slot[lo + j];
+      if (s < 0 || s >= A.dm.P * kBlock) { set_status(A.ws.status, ST_BAD_INDEX); s = 0; }
+      nx_slot = s;
+      nx_pos = A.ls.pos[lo + j];
+    }
+  }
+  __device__ void issue(int tile) {
+    if (tile >= ntiles) return;
+    const int st = tile % kTcStages;
+    unsigned char* kb = kv + st * kTcKV;
+    unsigned char* vb = kb + 2 * kTcHalf;
+    const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(A.ls.k_pool) + static_cast<size_t>(nx_slot) * kD;
+    const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(A.ls.v_pool) + static_cast<size_t>(nx_slot) * kD;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int c = part * 4 + i, half = c >> 3, cc = c & 7;
+      const int off = half * kTcHalf + key * 128 + ((cc ^ (key & 7)) << 4);
+      if (nx_slot >= 0) {
+        cp_async16(kb + off, kp + c * 8);
+        cp_async16(vb + off, vp + c * 8);
+      } else {
+        *reinterpret_cast<uint4*>(kb + off) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(vb + off) = make_uint4(0, 0, 0, 0);
+      }
+    }
+    if (part == 0) pos[st][key] = nx_pos;
+  }
+};
+
+// Q rows of the lane into [row tile][d half][row][128 B], rows >= A.rows zero.
+__device__ __forceinline__ void tc_load_q(const D3Args& A, unsigned char* sq, int b, int kh) {
+  const int r = threadIdx.x, rr = r & 127;
+  unsigned char* row = sq + (r >> 7) * 32768 + rr * 128;
+  if (r < A.rows) {
+    const int h = r / A.w, i = r % A.w;
+    const __nv_bfloat16* src = A.q + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i) * kD;
+#pragma unroll
+    for (int c = 0; c < 16; ++c) cp_async16(row + (c >> 3) * 16384 + (((c & 7) ^ (rr & 7)) << 4), src + c * 8);
+  } else {
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      *reinterpret_cast<uint4*>(row + (c >> 3) * 16384 + (((c & 7) ^ (rr & 7)) << 4)) = make_uint4(0, 0, 0, 0);
+  }
+}
+
+// S[row tile mm] = Q K^T for stage st into tensor-memory column dS (thread 0)
+__device__ __forceinline__ void tc_issue_s(uint32_t dS, const unsigned char* sq, const unsigned char* kst, int mm) {
+#pragma unroll
+  for (int ks = 0; ks < 8; ++ks) {
+    const int half = ks >> 2, kin = ks & 3;
+    const uint64_t ad = tc::desc_sw128(smem_u32(sq + mm * 32768 + half * 16384) + kin * 32, 16, 1024);
+    const uint64_t bd = tc::desc_sw128(smem_u32(kst + half * kTcHalf) + kin * 32, 16, 1024);
+    tc::mma_ss(dS, ad, bd, kIdS, ks > 0 ? 1u : 0u);
+  }
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) d3_tc_pass1_kernel(D3Args A) {
+  extern __shared__ unsigned char d3_dsm[];
+  __shared__ int sh_pos[kTcStages][kTcKeys];
+  __shared__ __align__(8) uint64_t sh_bar;
+  __shared__ uint32_t sh_taddr;
+  const int chunk = blockIdx.x, l = blockIdx.y;
+  const int n = min(max(A.ls.count[l], 0), A.dm.cap);
+  const int j_begin = chunk * kChunk;
+  if (j_begin >= n) return;
+  const int j_end = min(n, j_begin + kChunk);
+  const int ntiles = (j_end - j_begin + kTcKeys - 1) / kTcKeys;
+  unsigned char* sq = align1024(d3_dsm);
+  unsigned char* skv = sq + kTcQ;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
+  const int r = tid, m = r >> 7;
+  const bool row_ok = r < A.rows;
+  const int qp = row_ok ? A.qpos[r % A.w] : -1;
+
+  if (warp == 0) tc::alloc(&sh_taddr, kTcCols);
+  if (tid == 0) {
+    mbar_init(&sh_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  TcLoader ld(A, skv, sh_pos, l, j_begin, j_end, ntiles);
+  tc_load_q(A, sq, b, kh);
+  ld.fetch(0);
+#pragma unroll
+  for (int T = 0; T < kTcStages - 1; ++T) {
+    ld.issue(T);
+    cp_commit();
+    ld.fetch(T + 1);
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tl = sh_taddr;
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+
+  float m_run = -INFINITY, l_run = 0.f;
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t % kTcStages, buf = t & 1;
+    unsigned char* kst = skv + st * kTcKV;
+    cp_wait<kTcStages - 2>();
+    fence_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (tid == 0) {
+      tc_issue_s(tl + 256 + buf * 128, sq, kst, 0);
+      tc_issue_s(tl + 256 + buf * 128 + 64, sq, kst, 1);
+      tc::commit(&sh_bar);
+    }
+    (void)mbar_wait_bounded(&sh_bar, t & 1, A.ws.status);
+    tc::fence_after();
+    // S(t) complete, hence the P V of tile t - 1: its stage is free again
+    ld.issue(t + kTcStages - 1);
+    cp_commit();
+    ld.fetch(t + kTcStages);
+
+    const uint32_t aS = tl + lane_off + 256 + buf * 128 + m * 64;
+    float s[kTcKeys];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t v[16];
+      tc::ld16(aS + q4 * 16, v);
+      tc::wait_ld();
+#pragma unroll
+      for (int k = 0; k < 16; ++k) s[q4 * 16 + k] = __uint_as_float(v[k]);
+    }
+    float tmax = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kTcKeys; ++k) {
+      const bool ok = row_ok && sh_pos[st][k] <= qp;
+      s[k] = ok ? s[k] * A.scale2 : -INFINITY;
+      tmax = fmaxf(tmax, s[k]);
+    }
+    // lazy rescale: the running max moves only by more than kTcRescale
+    float factor = 1.f;
+    if (tmax > m_run + kTcRescale) {
+      factor = (m_run == -INFINITY) ? 0.f : exp2f(m_run - tmax);
+      m_run = tmax;
+      l_run *= factor;
+    }
+    if (t > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+      const uint32_t aO = tl + lane_off + m * 128;
+#pragma unroll
+      for (int q8 = 0; q8 < 8; ++q8) {
+        uint32_t v[16];
+        tc::ld16(aO + q8 * 16, v);
+        tc::wait_ld();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * factor);
+        tc::st16(aO + q8 * 16, v);
+      }
+      tc::wait_st();
+    }
+    float psum = 0.f;
+    uint32_t hi[32], lo[32];
+#pragma unroll
+    for (int k2 = 0; k2 < 32; ++k2) {
+      const float p0 = s[2 * k2] == -INFINITY ? 0.f : hw_exp2(s[2 * k2] - m_run);
+      const float p1 = s[2 * k2 + 1] == -INFINITY ? 0.f : hw_exp2(s[2 * k2 + 1] - m_run);
+      psum += p0 + p1;
+      split_bf16(p0, p1, hi[k2], lo[k2]);
+    }
+    l_run += psum;
+    {
+      uint32_t v[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = hi[k];
+      tc::st16(aS, v);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = hi[16 + k];
+      tc::st16(aS + 16, v);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = lo[k];
+      tc::st16(aS + 32, v);
+#pragma unroll
+      for (int k = 0; k < 16; ++k) v[k] = lo[16 + k];
+      tc::st16(aS + 48, v);
+    }
+    tc::wait_st();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (tid == 0) {
+      const uint32_t vbase = smem_u32(kst + 2 * kTcHalf);
+#pragma unroll
+      for (int mm = 0; mm < 2; ++mm) {
+        const uint32_t aP = tl + 256 + buf * 128 + mm * 64;
+#pragma unroll
+        for (int ks = 0; ks < 4; ++ks) {
+          const uint64_t bd = tc::desc_sw128(vbase + ks * 2048, kTcHalf, 1024);
+          tc::mma_ts(tl + mm * 128, aP + ks * 8, bd, kIdPV, (t > 0 || ks > 0) ? 1u : 0u);
+          tc::mma_ts(tl + mm * 128, aP + 32 + ks * 8, bd, kIdPV, 1u);
+        }
+      }
+    }
+  }
+  if (tid == 0) tc::commit(&sh_bar);
+  (void)mbar_wait_bounded(&sh_bar, ntiles & 1, A.ws.status);
+  tc::fence_after();
+  const size_t stride = kD + 2;
+  float* part = A.ws.d3_part + (static_cast<size_t>(l) * A.chunks + chunk) * static_cast<size_t>(A.rows_cap) * stride +
+                static_cast<size_t>(r) * stride;
+  const uint32_t aO = tl + lane_off + m * 128;
+#pragma unroll
+  for (int q8 = 0; q8 < 8; ++q8) {
+    uint32_t v[16];
+    tc::ld16(aO + q8 * 16, v);
+    tc::wait_ld();
+    if (row_ok) {
+#pragma unroll
+      for (int k = 0; k < 16; k += 2)
+        *reinterpret_cast<float2*>(part + q8 * 16 + k) = make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+    }
+  }
+  if (row_ok) {
+    part[kD] = m_run;
+    part[kD + 1] = l_run;
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tl, kTcCols);
+}
+
+// p / (1 - p) * ||a - v|| for the one key of a row with p > 1/2, x = log2 p:
+// the distance directly from the fp32 a row and the swizzled V tile (the
+// expansion would cancel), 1 - p from expm1.
+__device__ __noinline__ float residual_direct(float x, const float* arow, const unsigned char* vtile, int key) {
+  const float p = exp2f(x);
+  const float om = -expm1f(x * kLn2);
+  if (!(om > 0.f)) return INFINITY;
+  const float4* a4 = reinterpret_cast<const float4*>(arow);
+  float acc = 0.f;
+#pragma unroll 4
+  for (int c = 0; c < kD / 8; ++c) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(vtile + sw_off(key, c * 8));
+    const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
+    const float4 x0 = a4[c * 2], x1 = a4[c * 2 + 1];
+    const float2 v0 = __bfloat1622float2(pr[0]), v1 = __bfloat1622float2(pr[1]);
+    const float2 v2 = __bfloat1622float2(pr[2]), v3 = __bfloat1622float2(pr[3]);
+    float d;
+    d = x0.x - v0.x; acc = fmaf(d, d, acc);
+    d = x0.y - v0.y; acc = fmaf(d, d, acc);
+    d = x0.z - v1.x; acc = fmaf(d, d, acc);
+    d = x0.w - v1.y; acc = fmaf(d, d, acc);
+    d = x1.x - v2.x; acc = fmaf(d, d, acc);
+    d = x1.y - v2.y; acc = fmaf(d, d, acc);
+    d = x1.z - v3.x; acc = fmaf(d, d, acc);
+    d = x1.w - v3.y; acc = fmaf(d, d, acc);
+  }
+  return p / om * sqrtf(acc);
+}
+
+__global__ void __launch_bounds__(kTcThreads, 1) d3_tc_pass2_kernel(D3Args A) {
+  extern __shared__ unsigned char d3_dsm[];
+  __shared__ int sh_pos[kTcStages][kTcKeys];
+  __shared__ float sh_vn[kTcKeys];
+  __shared__ float sh_col[kTcThreads / 32][kTcKeys];
+  __shared__ __align__(8) uint64_t sh_bar;
+  __shared__ uint32_t sh_taddr;
+  const int chunk = blockIdx.x, l = blockIdx.y;
+  const int n = min(max(A.ls.count[l], 0), A.dm.cap);
+  const int j_begin = chunk * kChunk;
+  if (j_begin >= n) return;
+  const int j_end = min(n, j_begin + kChunk);
+  const int ntiles = (j_end - j_begin + kTcKeys - 1) / kTcKeys;
+  unsigned char* sq = align1024(d3_dsm);
+  unsigned char* skv = sq + kTcQ;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
+  const int r = tid, m = r >> 7;
+  const bool row_ok = r < A.rows;
+  const int qp = row_ok ? A.qpos[r % A.w] : -1;
+  const size_t wrow = static_cast<size_t>(l) * A.rows_cap + r;
+  const float lse2 = row_ok ? A.ws.d3_rowc[wrow * 2] : 0.f;
+  const float an = row_ok ? A.ws.d3_rowc[wrow * 2 + 1] : 0.f;
+  const float* arow = A.a_out;
+  if (row_ok) {
+    const int h = r / A.w, i = r % A.w;
+    arow = A.a_out + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i) * kD;
+  }
+
+  if (warp == 0) tc::alloc(&sh_taddr, kTcCols);
+  if (tid == 0) {
+    mbar_init(&sh_bar, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  TcLoader ld(A, skv, sh_pos, l, j_begin, j_end, ntiles);
+  tc_load_q(A, sq, b, kh);
+  ld.fetch(0);
+#pragma unroll
+  for (int T = 0; T < kTcStages - 1; ++T) {
+    ld.issue(T);
+    cp_commit();
+    ld.fetch(T + 1);
+  }
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  const uint32_t tl = sh_taddr;
+  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+  // a of this row (bf16 hi and lo) into tensor memory
+  {
+    const uint4* hsrc = reinterpret_cast<const uint4*>(A.ws.d3_ahi + wrow * kD);
+    const uint4* lsrc = reinterpret_cast<const uint4*>(A.ws.d3_alo + wrow * kD);
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t vh[16], vl[16];
+#pragma unroll
+      for (int u = 0; u < 4; ++u) {
+        const uint4 x = row_ok ? hsrc[q4 * 4 + u] : make_uint4(0, 0, 0, 0);
+        const uint4 y = row_ok ? lsrc[q4 * 4 + u] : make_uint4(0, 0, 0, 0);
+        vh[u * 4 + 0] = x.x; vh[u * 4 + 1] = x.y; vh[u * 4 + 2] = x.z; vh[u * 4 + 3] = x.w;
+        vl[u * 4 + 0] = y.x; vl[u * 4 + 1] = y.y; vl[u * 4 + 2] = y.z; vl[u * 4 + 3] = y.w;
+      }
+      tc::st16(tl + lane_off + m * 64 + q4 * 16, vh);
+      tc::st16(tl + lane_off + 128 + m * 64 + q4 * 16, vl);
+    }
+    tc::wait_st();
+  }
+  auto issue_mma = [&](int t) {
+    const int st = t % kTcStages;
+    const unsigned char* kst = skv + st * kTcKV;
+    const unsigned char* vst = kst + 2 * kTcHalf;
+#pragma unroll
+    for (int mm = 0; mm < 2; ++mm) {
+      tc_issue_s(tl + 256 + mm * 64, sq, kst, mm);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const int half = ks >> 2, kin = ks & 3;
+        const uint64_t bd = tc::desc_sw128(smem_u32(vst + half * kTcHalf) + kin * 32, 16, 1024);
+        tc::mma_ts(tl + 384 + mm * 64, tl + mm * 64 + ks * 8, bd, kIdS, ks > 0 ? 1u : 0u);
+        tc::mma_ts(tl + 384 + mm * 64, tl + 128 + mm * 64 + ks * 8, bd, kIdS, 1u);
+      }
+    }
+    tc::commit(&sh_bar);
+  };
+  cp_wait<kTcStages - 2>();
+  fence_async_smem();
+  tc::fence_before();
+  __syncthreads();
+  tc::fence_after();
+  if (tid == 0) issue_mma(0);
+
+  float* out = A.scores + static_cast<size_t>(l) * A.dm.cap;
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t % kTcStages;
+    const unsigned char* vst = skv + st * kTcKV + 2 * kTcHalf;
+    (void)mbar_wait_bounded(&sh_bar, t & 1, A.ws.status);
+    tc::fence_after();
+    // the MMAs of tile t - 1 and their smem reads are complete: refill its stage
+    ld.issue(t + kTcStages - 1);
+    cp_commit();
+    ld.fetch(t + kTcStages);
+    float s[kTcKeys], g[kTcKeys];
+#pragma unroll
+    for (int q4 = 0; q4 < 4; ++q4) {
+      uint32_t v[16], w[16];
+      tc::ld16(tl + lane_off + 256 + m * 64 + q4 * 16, v);
+      tc::ld16(tl + lane_off + 384 + m * 64 + q4 * 16, w);
+      tc::wait_ld();
+#pragma unroll
+      for (int k = 0; k < 16; ++k) {
+        s[q4 * 16 + k] = __uint_as_float(v[k]);
+        g[q4 * 16 + k] = __uint_as_float(w[k]);
+      }
+    }
+    // |v|^2 of the tile's keys: four threads per key, 32 elements each
+    {
+      const int key = tid >> 2, part = tid & 3;
+      float acc = 0.f;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        const int e0 = (part * 4 + c) * 8;
+        const uint4 x = *reinterpret_cast<const uint4*>(vst + sw_off(key, e0));
+        const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const float2 f = __bfloat1622float2(pr[u]);
+          acc = fmaf(f.x, f.x, fmaf(f.y, f.y, acc));
+        }
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      if (part == 0) sh_vn[key] = acc;
+    }
+    cp_wait<kTcStages - 2>();
+    fence_async_smem();
+    tc::fence_before();
+    __syncthreads();
+    tc::fence_after();
+    if (tid == 0 && t + 1 < ntiles) issue_mma(t + 1);
+    // residual terms of this row over the tile's keys: the expansion
+    // |a|^2 + |v|^2 - 2<a, v> for p <= 1/2; the key with p > 1/2 (at most
+    // one per row, the weights summing to 1) takes the direct distance
+    int xk = -1;
+    float xx = 0.f;
+#pragma unroll
+    for (int k = 0; k < kTcKeys; ++k) {
+      const bool ok = row_ok && sh_pos[st][k] <= qp;
+      const float x = s[k] * A.scale2 - lse2;
+      const float p = ok ? hw_exp2(x) : 0.f;
+      const float r2 = fmaxf(0.f, an + sh_vn[k] - 2.f * g[k]);
+      float term = p * hw_rcp(1.f - p) * hw_sqrt(r2);
+      if (p > 0.5f) { xk = k; xx = x; term = 0.f; }
+      s[k] = p > 0.f ? term : 0.f;
+    }
+    if (xk >= 0) {
+      const float dterm = residual_direct(xx, arow, vst, xk);
+#pragma unroll
+      for (int k = 0; k < kTcKeys; ++k)
+        if (k == xk) s[k] = dterm;
+    }
+    // butterfly: each lane ends with the warp's sums of two keys
+#pragma unroll
+    for (int o = 16, cnt = kTcKeys; o >= 1; o >>= 1, cnt >>= 1) {
+      const bool up = (lane & o) != 0;
+#pragma unroll
+      for (int i = 0; i < cnt / 2; ++i) {
+        const float send = up ? s[i] : s[cnt / 2 + i];
+        const float keep = up ? s[cnt / 2 + i] : s[i];
+        s[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+      }
+    }
+    {
+      const int k0 = ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4 +
+                     (lane & 1) * 2;
+      sh_col[warp][k0] = s[0];
+      sh_col[warp][k0 + 1] = s[1];
+    }
+    __syncthreads();
+    if (tid < kTcKeys) {
+      const int j = j_begin + t * kTcKeys + tid;
+      float tot = 0.f;
+#pragma unroll
+      for (int w = 0; w < kTcThreads / 32; ++w) tot += sh_col[w][tid];
+      if (j < j_end) out[j] = tot;
+    }
+  }
+  tc::fence_before();
+  __syncthreads();
+  if (warp == 0) tc::dealloc(tl, kTcCols);
+}
+
 }  // namespace
 
 int d3_rows_max(const Dims& dm) { return dm.g * dm.max_window; }
+
+cudaError_t prepare_dropkv() {
+  cudaError_t e = cudaFuncSetAttribute(d3_tc_pass1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(d3_tc_pass2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  return e;
+}
 int d3_chunks(const Dims& dm, int) { return (dm.cap + kChunk - 1) / kChunk; }
 
 cudaError_t launch_score(const Ctx& ctx, int layer, const void* q_win, int w, const int32_t* q_pos,
@@ -478,10 +1022,17 @@ cudaError_t launch_score(const Ctx& ctx, int layer, const void* q_win, int w, co
   A.scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(dm.d));
   if (A.rows > A.rows_cap || A.rows > kMaxRowGroups * kRowsPerCta || dm.d != kD || dm.dtype != KVEVICT_BF16)
     return cudaErrorInvalidValue;
+  if (A.rows <= kTcRows) {
+    const dim3 grid(A.chunks, dm.lanes);
+    d3_tc_pass1_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(A);
+    d3_combine_kernel<<<dim3((A.rows + 7) / 8, dm.lanes), 256, 0, stream>>>(A);
+    d3_tc_pass2_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(A);
+    return cudaGetLastError();
+  }
   const int groups = (A.rows + kRowsPerCta - 1) / kRowsPerCta;
   dim3 grid(A.chunks, dm.lanes, groups);
   d3_pass1_kernel<<<grid, kWarps * 32, 0, stream>>>(A);
-  d3_combine_kernel<<<dm.lanes, 256, 0, stream>>>(A);
+  d3_combine_kernel<<<dim3((A.rows + 7) / 8, dm.lanes), 256, 0, stream>>>(A);
   d3_pass2_kernel<<<grid, kWarps * 32, 0, stream>>>(A);
   dim3 fgrid((dm.cap + 255) / 256 < 64 ? (dm.cap + 255) / 256 : 64, dm.lanes);
   d3_finalize_kernel<<<fgrid, 256, 0, stream>>>(A, groups);

@@ -33,6 +33,21 @@ def test_window_scores_scaled():
     run_score(shp)
 
 
+def test_window_scores_many_rows():
+    """384 window rows per lane (group 8 x 48 positions): more rows than the
+    two 128-row tensor-memory tiles, so the general kernel scores them."""
+    shp = scaled("dropkv_prefill", ctx=1500, num_kv_heads=2, num_q_heads=16, window=48, budget=80,
+                 recent_window=48)
+    run_score(shp)
+
+
+def test_window_scores_single_partial_tile():
+    """A lane shorter than one 64-key tile, with window rows before every key."""
+    shp = scaled("dropkv_prefill", ctx=40, num_kv_heads=1, num_q_heads=4, window=16, budget=20,
+                 recent_window=16)
+    run_score(shp)
+
+
 def test_window_scores_short_window_group8():
     shp = scaled("dropkv_prefill", ctx=2100, num_kv_heads=1, num_q_heads=8, window=20, budget=105,
                  recent_window=20)
