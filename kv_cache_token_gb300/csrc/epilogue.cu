@@ -578,12 +578,14 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       auto keyf = [&](int i) { return mono_key(pooled64[i]); };
       sel = block_bottom_k(n, k, 64, keyf, posf, candf, sh_hist, sh_misc);
       auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
-      vcount = lane_remove(L, n, isv, vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx, sh_rows);
+      vcount = lane_remove(L, n, plain_victims(isv), vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx,
+                           sh_rows);
     } else {
       auto keyf = [&](int i) { return mono_key(L.score[i]); };
       sel = block_bottom_k(n, k, 32, keyf, posf, candf, sh_hist, sh_misc);
       auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
-      vcount = lane_remove(L, n, isv, vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx, sh_rows);
+      vcount = lane_remove(L, n, plain_victims(isv), vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx,
+                           sh_rows);
     }
   }
   const int m = n - vcount;
@@ -740,6 +742,7 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(LayerState ls, Wor
                                                            const void* k_new, const void* v_new,
                                                            int mark_freed, int32_t* moves) {
   __shared__ int sh_scan[40];
+  __shared__ int sh_mv_src[kApplyThreads], sh_mv_dst[kApplyThreads];
   grid_dep_launch();    // the next layer's attention may start (it touches other state)
   grid_dep_wait();      // the epilogue and its allocator are complete
   const int l = blockIdx.x, tid = threadIdx.x;
@@ -780,6 +783,10 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(LayerState ls, Wor
     (void)block_excl_scan(nsrc, sh_scan, &nsrc_tot);
     const int dbeg = ws.dst_begin[l];
     const int mbeg = ws.move_begin[l];
+    const int cpr = d * static_cast<int>(sizeof(KT)) / 16;     // 16-byte pieces per K or V row
+    const size_t row_bytes = static_cast<size_t>(d) * sizeof(KT);
+    unsigned char* kpb = reinterpret_cast<unsigned char*>(kp);
+    unsigned char* vpb = reinterpret_cast<unsigned char*>(vp);
     int q_total = 0;
     for (int base = 0; base < m; base += blockDim.x) {
       const int i = base + tid;
@@ -793,22 +800,33 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(LayerState ls, Wor
       const int ex = block_excl_scan(src ? 1 : 0, sh_scan, &tot);
       if (src && (q_total + ex) / kBlock >= ndst) {
         set_status(ws.status, ST_BAD_INDEX);   // plan and tables disagree: leave the token in place
+        sh_mv_src[ex] = -1;
       } else if (src) {
         const int q = q_total + ex;
         const int db = ws.alloc_ids[dbeg + q / kBlock];
         const int dof = q % kBlock;
         const int ns = db * kBlock + dof;
-        const KT* ks = kp + static_cast<size_t>(old) * d;
-        const KT* vs = vp + static_cast<size_t>(old) * d;
-        KT* kd = kp + static_cast<size_t>(ns) * d;
-        KT* vd = vp + static_cast<size_t>(ns) * d;
-        for (int e = 0; e < d; ++e) { kd[e] = ks[e]; vd[e] = vs[e]; }
+        sh_mv_src[ex] = old;
+        sh_mv_dst[ex] = ns;
         L.slot[i] = ns;
         if (moves) {
           int32_t* mv = moves + static_cast<size_t>(mbeg + q) * 6;
           mv[0] = l; mv[1] = L.pos[i]; mv[2] = old >> 4; mv[3] = old & 15; mv[4] = db; mv[5] = dof;
         }
       }
+      __syncthreads();
+      // the chunk's K and V rows, 16 bytes per thread (destinations are
+      // fresh blocks, never a source of the same plan)
+      for (int e = tid; e < tot * 2 * cpr; e += blockDim.x) {
+        const int mvi = e / (2 * cpr), rem = e - mvi * 2 * cpr;
+        const int so = sh_mv_src[mvi];
+        if (so < 0) continue;
+        unsigned char* base = rem < cpr ? kpb : vpb;
+        const size_t c16 = static_cast<size_t>(rem < cpr ? rem : rem - cpr) * 16;
+        *reinterpret_cast<uint4*>(base + static_cast<size_t>(sh_mv_dst[mvi]) * row_bytes + c16) =
+            *reinterpret_cast<const uint4*>(base + static_cast<size_t>(so) * row_bytes + c16);
+      }
+      __syncthreads();
       q_total += tot;
     }
     __syncthreads();

@@ -30,17 +30,31 @@ __device__ __forceinline__ LaneRefs lane_refs(const LayerState& ls, const Dims& 
   return r;
 }
 
+// A victim predicate without per-chunk preparation.
+template <typename F>
+struct PlainVictims {
+  F f;
+  __device__ __forceinline__ void prepare(int) {}
+  __device__ __forceinline__ bool operator()(int i) const { return f(i); }
+};
+template <typename F>
+__device__ __forceinline__ PlainVictims<F> plain_victims(F f) { return PlainVictims<F>{f}; }
+
 // Removes the entries i < n for which is_victim(i) holds, keeping the order
 // of the survivors.  Victim positions are appended (ascending) to vout (if
-// not null).  Each victim's live bit is cleared; a block whose last live bit
-// clears is released (owner -1) and, if freed_flag is given, flagged.
+// not null).  Each victim's live bit is cleared (fire-and-forget atomics);
+// afterwards every block of the lane's list left without a live bit (each
+// held one before) is released (owner -1) and, if freed_flag is given,
+// flagged.  is_victim.prepare(base) runs on every thread at the start of each
+// chunk of blockDim entries, before any entry of the chunk is tested.
 // Returns the number of victims.  sh_scan: 40 ints, sh_idx: blockDim ints.
 template <typename VictimFn>
 __device__ __forceinline__ int lane_remove(const LaneRefs& L, int n, VictimFn is_victim, int32_t* vout,
                            int32_t* freed_flag, int* n_dead, int P, uint32_t* status,
                            int* sh_scan, int* sh_idx, float* sh_rows) {
-  int kept_total = 0, vict_total = 0, dead = 0;
+  int kept_total = 0, vict_total = 0;
   for (int base = 0; base < n; base += blockDim.x) {
+    is_victim.prepare(base);
     const int i = base + threadIdx.x;
     int p = 0, s = 0;
     float sc = 0.f;
@@ -68,14 +82,7 @@ __device__ __forceinline__ int lane_remove(const LaneRefs& L, int n, VictimFn is
     if (isv) {
       if (vout) vout[vict_total + vex] = p;
       if (s >= 0 && s < P * kBlock) {
-        const int b = s >> 4;
-        const int bit = 1 << (s & 15);
-        const int old = atomicAnd(&L.mask[b], ~bit);
-        if ((old & ~bit) == 0 && (old & bit)) {
-          L.owner[b] = -1;
-          if (freed_flag) freed_flag[b] = 1;
-          ++dead;
-        }
+        atomicAnd(&L.mask[s >> 4], ~(1 << (s & 15)));
       } else if (s >= 0) {
         set_status(status, ST_BAD_INDEX);
       }
@@ -100,13 +107,22 @@ __device__ __forceinline__ int lane_remove(const LaneRefs& L, int n, VictimFn is
     kept_total += ktot;
     vict_total += vtot;
   }
-  if (n_dead) {
-    int d = dead;
-    // block-wide sum via the scan helper
-    int tot;
-    (void)block_excl_scan(d, sh_scan, &tot);
-    *n_dead = tot;
+  // blocks emptied by the removal
+  __threadfence();
+  __syncthreads();
+  int dead = 0;
+  const int nb = *L.nblocks;
+  for (int j = threadIdx.x; j < nb; j += blockDim.x) {
+    const int b = L.blocks[j];
+    if (b >= 0 && b < P && (__ldcg(L.mask + b) & 0xFFFF) == 0 && L.owner[b] >= 0) {
+      L.owner[b] = -1;
+      if (freed_flag) freed_flag[b] = 1;
+      ++dead;
+    }
   }
+  int tot;
+  (void)block_excl_scan(dead, sh_scan, &tot);
+  if (n_dead) *n_dead = tot;
   return vict_total;
 }
 

@@ -138,10 +138,53 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const KeyT* keys, c
 // ---------------------------------------------------------------------------
 // forced compaction
 // ---------------------------------------------------------------------------
+// Victim test against an ascending victim list: per chunk of table entries
+// the list's slice that can match (it starts at the first victim position
+// not below the chunk's first position) is staged in shared memory, and
+// each entry is looked up there.  The slice start only moves forward.
+struct SegVictims {
+  const int32_t* vl;
+  int k;
+  const int32_t* pos;
+  int* seg;
+  int* sh_len;
+  int start, len;
+  __device__ void prepare(int base) {
+    if (base > 0) {
+      // drop the slice entries below this chunk's first position
+      const int p0 = pos[base];
+      for (;;) {
+        const int c = __syncthreads_count(static_cast<int>(threadIdx.x) < len && seg[threadIdx.x] < p0);
+        start += c;
+        if (c < len || start >= k) break;
+        // the whole slice was below p0 (victims not in the table): next slice
+        len = min(static_cast<int>(blockDim.x), k - start);
+        if (static_cast<int>(threadIdx.x) < len) seg[threadIdx.x] = vl[start + threadIdx.x];
+        __syncthreads();
+      }
+    }
+    len = min(static_cast<int>(blockDim.x), max(0, k - start));
+    __syncthreads();
+    if (static_cast<int>(threadIdx.x) < len) seg[threadIdx.x] = vl[start + threadIdx.x];
+    __syncthreads();
+  }
+  __device__ bool operator()(int i) const {
+    const int p = pos[i];
+    int lo = 0, hi = len;
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (seg[mid] < p) lo = mid + 1; else hi = mid;
+    }
+    return lo < len && seg[lo] == p;
+  }
+};
+
 __global__ void __launch_bounds__(kThreads) compact_evict_kernel(LayerState ls, Workspace ws, Dims dm,
                                                                 const int32_t* victims,
                                                                 const int32_t* n_victims) {
   __shared__ int sh_scan[40];
+  __shared__ int sh_seg[kThreads];
+  __shared__ int sh_seg_len;
   __shared__ int sh_idx[kThreads];
   __shared__ __align__(16) float sh_rows[128 * kMaxW];
   const int l = blockIdx.x, tid = threadIdx.x;
@@ -152,16 +195,14 @@ __global__ void __launch_bounds__(kThreads) compact_evict_kernel(LayerState ls, 
     return;
   }
   const int k = max(0, min(n_victims[l], n));
-  const int32_t* vl = victims + static_cast<size_t>(l) * dm.cap;
-  auto isv = [&](int i) {
-    const int p = L.pos[i];
-    int lo = 0, hi = k;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (vl[mid] < p) lo = mid + 1; else hi = mid;
-    }
-    return lo < k && vl[lo] == p;
-  };
+  SegVictims isv;
+  isv.vl = victims + static_cast<size_t>(l) * dm.cap;
+  isv.k = k;
+  isv.pos = L.pos;
+  isv.seg = sh_seg;
+  isv.sh_len = &sh_seg_len;
+  isv.start = 0;
+  isv.len = 0;
   int dead = 0;
   const int vcount = lane_remove(L, n, isv, nullptr, ws.freed_flag, &dead, dm.P, ws.status, sh_scan, sh_idx,
                                  sh_rows);
