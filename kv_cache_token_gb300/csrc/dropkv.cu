@@ -493,7 +493,6 @@ __global__ void __launch_bounds__(256) d3_finalize_kernel(D3Args A, int groups) 
 // ---------------------------------------------------------------------------
 constexpr int kTcKeys = 64;
 constexpr int kTcStages = 3;
-constexpr int kTcThreads = 256;
 constexpr int kTcRows = 256;
 constexpr int kTcHalf = kTcKeys * 128;                 // one d half of a K or V tile (8 KB)
 constexpr int kTcKV = 4 * kTcHalf;                     // K (2 halves) then V (2 halves)
@@ -527,72 +526,9 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
   const uint32_t a = smem_u32(p);
   return p + (((a + 1023u) & ~1023u) - a);
 }
-__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 // byte offset of bf16 element e of key row k in a swizzled K or V tile
 __device__ __forceinline__ int sw_off(int k, int e) {
   return (e >> 6) * kTcHalf + k * 128 + ((((e & 63) >> 3) ^ (k & 7)) << 4) + (e & 7) * 2;
-}
-
-// Loads (cp.async) and zero fills of one CTA's Q rows and K/V tiles.
-struct TcLoader {
-  const D3Args& A;
-  unsigned char* kv;
-  int (*pos)[kTcKeys];
-  size_t lo;
-  int j_begin, j_end, ntiles, key, part;
-  int nx_slot, nx_pos;
-  __device__ TcLoader(const D3Args& a, unsigned char* kv_, int (*pos_)[kTcKeys], int l, int jb, int je, int nt)
-      : A(a), kv(kv_), pos(pos_), lo(static_cast<size_t>(l) * a.dm.cap), j_begin(jb), j_end(je), ntiles(nt),
-        key(threadIdx.x >> 2), part(threadIdx.x & 3), nx_slot(-1), nx_pos(0x7FFFFFFF) {}
-  // slot and position of this thread's key in `tile` (consumed by the next issue)
-  __device__ void fetch(int tile) {
-    const int j = j_begin + tile * kTcKeys + key;
-    nx_slot = -1;
-    nx_pos = 0x7FFFFFFF;
-    if (tile < ntiles && j < j_end) {
-      int s = A.ls.slot[lo + j];
-      if (s < 0 || s >= A.dm.P * kBlock) { set_status(A.ws.status, ST_BAD_INDEX); s = 0; }
-      nx_slot = s;
-      nx_pos = A.ls.pos[lo + j];
-    }
-  }
-  __device__ void issue(int tile) {
-    if (tile >= ntiles) return;
-    const int st = tile % kTcStages;
-    unsigned char* kb = kv + st * kTcKV;
-    unsigned char* vb = kb + 2 * kTcHalf;
-    const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(A.ls.k_pool) + static_cast<size_t>(nx_slot) * kD;
-    const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(A.ls.v_pool) + static_cast<size_t>(nx_slot) * kD;
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const int c = part * 4 + i, half = c >> 3, cc = c & 7;
-      const int off = half * kTcHalf + key * 128 + ((cc ^ (key & 7)) << 4);
-      if (nx_slot >= 0) {
-        cp_async16(kb + off, kp + c * 8);
-        cp_async16(vb + off, vp + c * 8);
-      } else {
-        *reinterpret_cast<uint4*>(kb + off) = make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(vb + off) = make_uint4(0, 0, 0, 0);
-      }
-    }
-    if (part == 0) pos[st][key] = nx_pos;
-  }
-};
-
-// Q rows of the lane into [row tile][d half][row][128 B], rows >= A.rows zero.
-__device__ __forceinline__ void tc_load_q(const D3Args& A, unsigned char* sq, int b, int kh) {
-  const int r = threadIdx.x, rr = r & 127;
-  unsigned char* row = sq + (r >> 7) * 32768 + rr * 128;
-  if (r < A.rows) {
-    const int h = r / A.w, i = r % A.w;
-    const __nv_bfloat16* src = A.q + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i) * kD;
-#pragma unroll
-    for (int c = 0; c < 16; ++c) cp_async16(row + (c >> 3) * 16384 + (((c & 7) ^ (rr & 7)) << 4), src + c * 8);
-  } else {
-#pragma unroll
-    for (int c = 0; c < 16; ++c)
-      *reinterpret_cast<uint4*>(row + (c >> 3) * 16384 + (((c & 7) ^ (rr & 7)) << 4)) = make_uint4(0, 0, 0, 0);
-  }
 }
 
 // S[row tile mm] = Q K^T for stage st into tensor-memory column dS (thread 0)
@@ -606,10 +542,118 @@ __device__ __forceinline__ void tc_issue_s(uint32_t dS, const unsigned char* sq,
   }
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) d3_tc_pass1_kernel(D3Args A) {
+// Warp roles of the tcgen05 passes: warps 0-7 own one window row per thread,
+// warp 8 produces (Q, then K/V tiles into the stage ring by 16-byte cp.async
+// at the swizzled positions, each lane's copies completing on the stage's
+// full barrier), warp 9 lane 0 issues the MMAs.  Hand-offs are mbarriers;
+// the row warps synchronise among themselves on named barrier 1.
+constexpr int kWsRowThreads = 256;
+constexpr int kWsThreads = kWsRowThreads + 64;
+constexpr int kWsProducer = 8, kWsIssuer = 9;
+
+__device__ __forceinline__ void cp_async16_zf(void* dst, const void* src, bool ok) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async4_zf(void* dst, const void* src, bool ok) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 4 : 0)
+               : "memory");
+}
+// one arrival on the barrier once this thread's earlier cp.async copies land
+__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void rows_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+struct WsBars {
+  uint64_t qfull;
+  uint64_t full[kTcStages], empty[kTcStages];
+  uint64_t x_full[2], x_free[2], pv_done[2];
+};
+
+// Producer warp: Q rows (8 per lane), then tile t's keys 2 lane and 2 lane + 1.
+__device__ __forceinline__ void ws_produce(const D3Args& A, int l, int j_begin, int j_end, int ntiles,
+                                           unsigned char* sq, unsigned char* skv, int (*pos)[kTcKeys], WsBars& bar) {
+  const int lane = threadIdx.x & 31;
+  const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
+#pragma unroll 1
+  for (int q = 0; q < 8; ++q) {
+    const int r = lane * 8 + q, rr = r & 127;
+    unsigned char* row = sq + (r >> 7) * 32768 + rr * 128;
+    const bool ok = r < A.rows;
+    const int h = ok ? r / A.w : 0, i = ok ? r % A.w : 0;
+    const __nv_bfloat16* src = A.q + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i) * kD;
+#pragma unroll
+    for (int c = 0; c < 16; ++c)
+      cp_async16_zf(row + (c >> 3) * 16384 + (((c & 7) ^ (rr & 7)) << 4), ok ? src + c * 8 : A.q, ok);
+  }
+  cp_async_arrive(&bar.qfull);
+  const size_t lo = static_cast<size_t>(l) * A.dm.cap;
+  const __nv_bfloat16* kpool = static_cast<const __nv_bfloat16*>(A.ls.k_pool);
+  const __nv_bfloat16* vpool = static_cast<const __nv_bfloat16*>(A.ls.v_pool);
+  const int rows_max = A.dm.P * kBlock;
+  auto slot_of = [&](int t, int key) -> int {
+    const int j = j_begin + t * kTcKeys + key;
+    if (t >= ntiles || j >= j_end) return -1;
+    int sl = A.ls.slot[lo + j];
+    if (sl < 0 || sl >= rows_max) { set_status(A.ws.status, ST_BAD_INDEX); sl = 0; }
+    return sl;
+  };
+  int s0 = slot_of(0, 2 * lane), s1 = slot_of(0, 2 * lane + 1);
+#pragma unroll 1
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t % kTcStages;
+    if (t >= kTcStages) (void)mbar_wait_bounded(&bar.empty[st], ((t / kTcStages) - 1) & 1, A.ws.status);
+    unsigned char* kb = skv + st * kTcKV;
+    unsigned char* vb = kb + 2 * kTcHalf;
+#pragma unroll
+    for (int kk = 0; kk < 2; ++kk) {
+      const int key = 2 * lane + kk;
+      const int sl = kk ? s1 : s0;
+      const bool ok = sl >= 0;
+      const __nv_bfloat16* ks = kpool + static_cast<size_t>(ok ? sl : 0) * kD;
+      const __nv_bfloat16* vs = vpool + static_cast<size_t>(ok ? sl : 0) * kD;
+#pragma unroll
+      for (int c = 0; c < 16; ++c) {
+        const int off = (c >> 3) * kTcHalf + key * 128 + (((c & 7) ^ (key & 7)) << 4);
+        cp_async16_zf(kb + off, ks + c * 8, ok);
+        cp_async16_zf(vb + off, vs + c * 8, ok);
+      }
+      cp_async4_zf(&pos[st][key], A.ls.pos + lo + (ok ? j_begin + t * kTcKeys + key : 0), ok);
+    }
+    cp_async_arrive(&bar.full[st]);
+    s0 = slot_of(t + 1, 2 * lane);
+    s1 = slot_of(t + 1, 2 * lane + 1);
+  }
+  asm volatile("cp.async.wait_all;" ::: "memory");
+}
+
+__device__ __forceinline__ void ws_init_bars(WsBars& bar, uint32_t full_count, uint32_t empty_count,
+                                             uint32_t free_count) {
+  mbar_init(&bar.qfull, 32);
+  for (int s = 0; s < kTcStages; ++s) {
+    mbar_init(&bar.full[s], full_count);
+    mbar_init(&bar.empty[s], empty_count);
+  }
+  for (int b = 0; b < 2; ++b) {
+    mbar_init(&bar.x_full[b], 1);
+    mbar_init(&bar.x_free[b], free_count);
+    mbar_init(&bar.pv_done[b], 1);
+  }
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// pass 1.  Issue order S(0), then per tile S(t+1), P V(t): the tensor core
+// computes the next scores while the row warps exponentiate.  x_full[b]:
+// S(t) done (b = t & 1); x_free[b]: P(t) written by the 8 row warps;
+// pv_done[b]: P V(t) done; empty[s]: the stage's last reader (P V) done.
+__global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass1_kernel(D3Args A) {
   extern __shared__ unsigned char d3_dsm[];
   __shared__ int sh_pos[kTcStages][kTcKeys];
-  __shared__ __align__(8) uint64_t sh_bar;
+  __shared__ __align__(8) WsBars bar;
   __shared__ uint32_t sh_taddr;
   const int chunk = blockIdx.x, l = blockIdx.y;
   const int n = min(max(A.ls.count[l], 0), A.dm.cap);
@@ -620,157 +664,156 @@ __global__ void __launch_bounds__(kTcThreads, 1) d3_tc_pass1_kernel(D3Args A) {
   unsigned char* sq = align1024(d3_dsm);
   unsigned char* skv = sq + kTcQ;
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
-  const int r = tid, m = r >> 7;
-  const bool row_ok = r < A.rows;
-  const int qp = row_ok ? A.qpos[r % A.w] : -1;
-
-  if (warp == 0) tc::alloc(&sh_taddr, kTcCols);
-  if (tid == 0) {
-    mbar_init(&sh_bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  TcLoader ld(A, skv, sh_pos, l, j_begin, j_end, ntiles);
-  tc_load_q(A, sq, b, kh);
-  ld.fetch(0);
-#pragma unroll
-  for (int T = 0; T < kTcStages - 1; ++T) {
-    ld.issue(T);
-    cp_commit();
-    ld.fetch(T + 1);
-  }
+  if (warp == kWsIssuer) tc::alloc(&sh_taddr, kTcCols);
+  if (tid == 0) ws_init_bars(bar, 32, 1, kWsRowThreads / 32);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tl = sh_taddr;
-  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
 
-  float m_run = -INFINITY, l_run = 0.f;
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t % kTcStages, buf = t & 1;
-    unsigned char* kst = skv + st * kTcKV;
-    cp_wait<kTcStages - 2>();
-    fence_async_smem();
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    if (tid == 0) {
-      tc_issue_s(tl + 256 + buf * 128, sq, kst, 0);
-      tc_issue_s(tl + 256 + buf * 128 + 64, sq, kst, 1);
-      tc::commit(&sh_bar);
-    }
-    (void)mbar_wait_bounded(&sh_bar, t & 1, A.ws.status);
-    tc::fence_after();
-    // S(t) complete, hence the P V of tile t - 1: its stage is free again
-    ld.issue(t + kTcStages - 1);
-    cp_commit();
-    ld.fetch(t + kTcStages);
-
-    const uint32_t aS = tl + lane_off + 256 + buf * 128 + m * 64;
-    float s[kTcKeys];
+  if (warp == kWsProducer) {
+    ws_produce(A, l, j_begin, j_end, ntiles, sq, skv, sh_pos, bar);
+  } else if (warp == kWsIssuer) {
+    if ((tid & 31) == 0) {
+      (void)mbar_wait_bounded(&bar.qfull, 0, A.ws.status);
+      auto issue_s = [&](int t) {
+        const int st = t % kTcStages, buf = t & 1;
+        (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);
+        tc::fence_after();
+        const unsigned char* kst = skv + st * kTcKV;
+        tc_issue_s(tl + 256 + buf * 128, sq, kst, 0);
+        tc_issue_s(tl + 256 + buf * 128 + 64, sq, kst, 1);
+        tc::commit(&bar.x_full[buf]);
+      };
+      issue_s(0);
+#pragma unroll 1
+      for (int t = 0; t < ntiles; ++t) {
+        if (t + 1 < ntiles) issue_s(t + 1);
+        const int st = t % kTcStages, buf = t & 1;
+        (void)mbar_wait_bounded(&bar.x_free[buf], (t >> 1) & 1, A.ws.status);
+        tc::fence_after();
+        const uint32_t vbase = smem_u32(skv + st * kTcKV + 2 * kTcHalf);
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      uint32_t v[16];
-      tc::ld16(aS + q4 * 16, v);
-      tc::wait_ld();
+        for (int mm = 0; mm < 2; ++mm) {
+          const uint32_t aP = tl + 256 + buf * 128 + mm * 64;
 #pragma unroll
-      for (int k = 0; k < 16; ++k) s[q4 * 16 + k] = __uint_as_float(v[k]);
+          for (int ks = 0; ks < 4; ++ks) {
+            const uint64_t bd = tc::desc_sw128(vbase + ks * 2048, kTcHalf, 1024);
+            tc::mma_ts(tl + mm * 128, aP + ks * 8, bd, kIdPV, (t > 0 || ks > 0) ? 1u : 0u);
+            tc::mma_ts(tl + mm * 128, aP + 32 + ks * 8, bd, kIdPV, 1u);
+          }
+        }
+        tc::commit(&bar.empty[st]);
+        tc::commit(&bar.pv_done[buf]);
+      }
     }
-    float tmax = -INFINITY;
+  } else {
+    // row warps: one window row per thread
+    const int r = tid, m = r >> 7;
+    const bool row_ok = r < A.rows;
+    const int qp = row_ok ? A.qpos[r % A.w] : -1;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int nkeys = j_end - j_begin;
+    float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll 1
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t % kTcStages, buf = t & 1;
+      (void)mbar_wait_bounded(&bar.x_full[buf], (t >> 1) & 1, A.ws.status);
+      (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);   // key positions
+      tc::fence_after();
+      const uint32_t aS = tl + lane_off + 256 + buf * 128 + m * 64;
+      float s[kTcKeys];
 #pragma unroll
-    for (int k = 0; k < kTcKeys; ++k) {
-      const bool ok = row_ok && sh_pos[st][k] <= qp;
-      s[k] = ok ? s[k] * A.scale2 : -INFINITY;
-      tmax = fmaxf(tmax, s[k]);
-    }
-    // lazy rescale: the running max moves only by more than kTcRescale
-    float factor = 1.f;
-    if (tmax > m_run + kTcRescale) {
-      factor = (m_run == -INFINITY) ? 0.f : exp2f(m_run - tmax);
-      m_run = tmax;
-      l_run *= factor;
-    }
-    if (t > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
-      const uint32_t aO = tl + lane_off + m * 128;
-#pragma unroll
-      for (int q8 = 0; q8 < 8; ++q8) {
+      for (int q4 = 0; q4 < 4; ++q4) {
         uint32_t v[16];
-        tc::ld16(aO + q8 * 16, v);
+        tc::ld16(aS + q4 * 16, v);
         tc::wait_ld();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * factor);
-        tc::st16(aO + q8 * 16, v);
+        for (int k = 0; k < 16; ++k) s[q4 * 16 + k] = __uint_as_float(v[k]);
       }
-      tc::wait_st();
-    }
-    float psum = 0.f;
-    uint32_t hi[32], lo[32];
+      float tmax = -INFINITY;
 #pragma unroll
-    for (int k2 = 0; k2 < 32; ++k2) {
-      const float p0 = s[2 * k2] == -INFINITY ? 0.f : hw_exp2(s[2 * k2] - m_run);
-      const float p1 = s[2 * k2 + 1] == -INFINITY ? 0.f : hw_exp2(s[2 * k2 + 1] - m_run);
-      psum += p0 + p1;
-      split_bf16(p0, p1, hi[k2], lo[k2]);
-    }
-    l_run += psum;
-    {
-      uint32_t v[16];
+      for (int k = 0; k < kTcKeys; ++k) {
+        const bool ok = row_ok && t * kTcKeys + k < nkeys && sh_pos[st][k] <= qp;
+        s[k] = ok ? s[k] * A.scale2 : -INFINITY;
+        tmax = fmaxf(tmax, s[k]);
+      }
+      float factor = 1.f;
+      if (tmax > m_run + kTcRescale) {
+        factor = (m_run == -INFINITY) ? 0.f : exp2f(m_run - tmax);
+        m_run = tmax;
+        l_run *= factor;
+      }
+      if (t > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+        // P V(t - 1) must be complete before O is rescaled
+        (void)mbar_wait_bounded(&bar.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, A.ws.status);
+        tc::fence_after();
+        const uint32_t aO = tl + lane_off + m * 128;
+#pragma unroll 1
+        for (int q8 = 0; q8 < 8; ++q8) {
+          uint32_t v[16];
+          tc::ld16(aO + q8 * 16, v);
+          tc::wait_ld();
 #pragma unroll
-      for (int k = 0; k < 16; ++k) v[k] = hi[k];
-      tc::st16(aS, v);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) v[k] = hi[16 + k];
-      tc::st16(aS + 16, v);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) v[k] = lo[k];
-      tc::st16(aS + 32, v);
-#pragma unroll
-      for (int k = 0; k < 16; ++k) v[k] = lo[16 + k];
-      tc::st16(aS + 48, v);
-    }
-    tc::wait_st();
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    if (tid == 0) {
-      const uint32_t vbase = smem_u32(kst + 2 * kTcHalf);
-#pragma unroll
-      for (int mm = 0; mm < 2; ++mm) {
-        const uint32_t aP = tl + 256 + buf * 128 + mm * 64;
-#pragma unroll
-        for (int ks = 0; ks < 4; ++ks) {
-          const uint64_t bd = tc::desc_sw128(vbase + ks * 2048, kTcHalf, 1024);
-          tc::mma_ts(tl + mm * 128, aP + ks * 8, bd, kIdPV, (t > 0 || ks > 0) ? 1u : 0u);
-          tc::mma_ts(tl + mm * 128, aP + 32 + ks * 8, bd, kIdPV, 1u);
+          for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * factor);
+          tc::st16(aO + q8 * 16, v);
         }
       }
-    }
-  }
-  if (tid == 0) tc::commit(&sh_bar);
-  (void)mbar_wait_bounded(&sh_bar, ntiles & 1, A.ws.status);
-  tc::fence_after();
-  const size_t stride = kD + 2;
-  float* part = A.ws.d3_part + (static_cast<size_t>(l) * A.chunks + chunk) * static_cast<size_t>(A.rows_cap) * stride +
-                static_cast<size_t>(r) * stride;
-  const uint32_t aO = tl + lane_off + m * 128;
+      float psum = 0.f;
+      uint32_t hi[32], lo[32];
 #pragma unroll
-  for (int q8 = 0; q8 < 8; ++q8) {
-    uint32_t v[16];
-    tc::ld16(aO + q8 * 16, v);
-    tc::wait_ld();
+      for (int k2 = 0; k2 < 32; ++k2) {
+        const float p0 = s[2 * k2] == -INFINITY ? 0.f : hw_exp2(s[2 * k2] - m_run);
+        const float p1 = s[2 * k2 + 1] == -INFINITY ? 0.f : hw_exp2(s[2 * k2 + 1] - m_run);
+        psum += p0 + p1;
+        split_bf16(p0, p1, hi[k2], lo[k2]);
+      }
+      l_run += psum;
+      {
+        uint32_t v[16];
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = hi[k];
+        tc::st16(aS, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = hi[16 + k];
+        tc::st16(aS + 16, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = lo[k];
+        tc::st16(aS + 32, v);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) v[k] = lo[16 + k];
+        tc::st16(aS + 48, v);
+      }
+      tc::wait_st();
+      tc::fence_before();
+      __syncwarp();
+      if ((tid & 31) == 0) mbar_arrive1(&bar.x_free[buf]);
+    }
+    (void)mbar_wait_bounded(&bar.pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, A.ws.status);
+    tc::fence_after();
+    const size_t stride = kD + 2;
+    float* part = A.ws.d3_part + (static_cast<size_t>(l) * A.chunks + chunk) * static_cast<size_t>(A.rows_cap) * stride +
+                  static_cast<size_t>(r) * stride;
+    const uint32_t aO = tl + lane_off + m * 128;
+#pragma unroll
+    for (int q8 = 0; q8 < 8; ++q8) {
+      uint32_t v[16];
+      tc::ld16(aO + q8 * 16, v);
+      tc::wait_ld();
+      if (row_ok) {
+#pragma unroll
+        for (int k = 0; k < 16; k += 2)
+          *reinterpret_cast<float2*>(part + q8 * 16 + k) = make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+      }
+    }
     if (row_ok) {
-#pragma unroll
-      for (int k = 0; k < 16; k += 2)
-        *reinterpret_cast<float2*>(part + q8 * 16 + k) = make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+      part[kD] = m_run;
+      part[kD + 1] = l_run;
     }
-  }
-  if (row_ok) {
-    part[kD] = m_run;
-    part[kD + 1] = l_run;
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 0) tc::dealloc(tl, kTcCols);
+  if (warp == kWsIssuer) tc::dealloc(tl, kTcCols);
 }
 
 // p / (1 - p) * ||a - v|| for the one key of a row with p > 1/2, x = log2 p:
@@ -802,12 +845,15 @@ __device__ __noinline__ float residual_direct(float x, const float* arow, const 
   return p / om * sqrtf(acc);
 }
 
-__global__ void __launch_bounds__(kTcThreads, 1) d3_tc_pass2_kernel(D3Args A) {
+// pass 2.  x_full[0]: S(t) and G(t) done; x_free[0]: the 8 row warps have
+// read them (the buffer may be overwritten); empty[s]: the MMAs and the 8 row
+// warps are done with the stage.
+__global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass2_kernel(D3Args A) {
   extern __shared__ unsigned char d3_dsm[];
   __shared__ int sh_pos[kTcStages][kTcKeys];
   __shared__ float sh_vn[kTcKeys];
-  __shared__ float sh_col[kTcThreads / 32][kTcKeys];
-  __shared__ __align__(8) uint64_t sh_bar;
+  __shared__ float sh_col[kWsRowThreads / 32][kTcKeys];
+  __shared__ __align__(8) WsBars bar;
   __shared__ uint32_t sh_taddr;
   const int chunk = blockIdx.x, l = blockIdx.y;
   const int n = min(max(A.ls.count[l], 0), A.dm.cap);
@@ -818,40 +864,19 @@ __global__ void __launch_bounds__(kTcThreads, 1) d3_tc_pass2_kernel(D3Args A) {
   unsigned char* sq = align1024(d3_dsm);
   unsigned char* skv = sq + kTcQ;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
-  const int r = tid, m = r >> 7;
-  const bool row_ok = r < A.rows;
-  const int qp = row_ok ? A.qpos[r % A.w] : -1;
-  const size_t wrow = static_cast<size_t>(l) * A.rows_cap + r;
-  const float lse2 = row_ok ? A.ws.d3_rowc[wrow * 2] : 0.f;
-  const float an = row_ok ? A.ws.d3_rowc[wrow * 2 + 1] : 0.f;
-  const float* arow = A.a_out;
-  if (row_ok) {
-    const int h = r / A.w, i = r % A.w;
-    arow = A.a_out + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i) * kD;
-  }
-
-  if (warp == 0) tc::alloc(&sh_taddr, kTcCols);
-  if (tid == 0) {
-    mbar_init(&sh_bar, 1);
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-  }
-  TcLoader ld(A, skv, sh_pos, l, j_begin, j_end, ntiles);
-  tc_load_q(A, sq, b, kh);
-  ld.fetch(0);
-#pragma unroll
-  for (int T = 0; T < kTcStages - 1; ++T) {
-    ld.issue(T);
-    cp_commit();
-    ld.fetch(T + 1);
-  }
+  if (warp == kWsIssuer) tc::alloc(&sh_taddr, kTcCols);
+  if (tid == 0) ws_init_bars(bar, 32, 1 + kWsRowThreads / 32, kWsRowThreads / 32);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tl = sh_taddr;
+  const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
+  const int r = tid, m = r >> 7;
+  const bool row_ok = r < A.rows;
+  const size_t wrow = static_cast<size_t>(l) * A.rows_cap + (row_ok ? r : 0);
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  // a of this row (bf16 hi and lo) into tensor memory
-  {
+  if (warp < kWsProducer) {
+    // a of this row (bf16 hi and lo) into tensor memory
     const uint4* hsrc = reinterpret_cast<const uint4*>(A.ws.d3_ahi + wrow * kD);
     const uint4* lsrc = reinterpret_cast<const uint4*>(A.ws.d3_alo + wrow * kD);
 #pragma unroll
@@ -869,128 +894,143 @@ __global__ void __launch_bounds__(kTcThreads, 1) d3_tc_pass2_kernel(D3Args A) {
     }
     tc::wait_st();
   }
-  auto issue_mma = [&](int t) {
-    const int st = t % kTcStages;
-    const unsigned char* kst = skv + st * kTcKV;
-    const unsigned char* vst = kst + 2 * kTcHalf;
-#pragma unroll
-    for (int mm = 0; mm < 2; ++mm) {
-      tc_issue_s(tl + 256 + mm * 64, sq, kst, mm);
-#pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const int half = ks >> 2, kin = ks & 3;
-        const uint64_t bd = tc::desc_sw128(smem_u32(vst + half * kTcHalf) + kin * 32, 16, 1024);
-        tc::mma_ts(tl + 384 + mm * 64, tl + mm * 64 + ks * 8, bd, kIdS, ks > 0 ? 1u : 0u);
-        tc::mma_ts(tl + 384 + mm * 64, tl + 128 + mm * 64 + ks * 8, bd, kIdS, 1u);
-      }
-    }
-    tc::commit(&sh_bar);
-  };
-  cp_wait<kTcStages - 2>();
-  fence_async_smem();
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
-  if (tid == 0) issue_mma(0);
 
-  float* out = A.scores + static_cast<size_t>(l) * A.dm.cap;
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t % kTcStages;
-    const unsigned char* vst = skv + st * kTcKV + 2 * kTcHalf;
-    (void)mbar_wait_bounded(&sh_bar, t & 1, A.ws.status);
-    tc::fence_after();
-    // the MMAs of tile t - 1 and their smem reads are complete: refill its stage
-    ld.issue(t + kTcStages - 1);
-    cp_commit();
-    ld.fetch(t + kTcStages);
-    float s[kTcKeys], g[kTcKeys];
+  if (warp == kWsProducer) {
+    ws_produce(A, l, j_begin, j_end, ntiles, sq, skv, sh_pos, bar);
+  } else if (warp == kWsIssuer) {
+    if (lane == 0) {
+      (void)mbar_wait_bounded(&bar.qfull, 0, A.ws.status);
+#pragma unroll 1
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t % kTcStages;
+        (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);
+        if (t > 0) (void)mbar_wait_bounded(&bar.x_free[0], (t - 1) & 1, A.ws.status);
+        tc::fence_after();
+        const unsigned char* kst = skv + st * kTcKV;
+        const unsigned char* vst = kst + 2 * kTcHalf;
 #pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      uint32_t v[16], w[16];
-      tc::ld16(tl + lane_off + 256 + m * 64 + q4 * 16, v);
-      tc::ld16(tl + lane_off + 384 + m * 64 + q4 * 16, w);
-      tc::wait_ld();
+        for (int mm = 0; mm < 2; ++mm) {
+          tc_issue_s(tl + 256 + mm * 64, sq, kst, mm);
 #pragma unroll
-      for (int k = 0; k < 16; ++k) {
-        s[q4 * 16 + k] = __uint_as_float(v[k]);
-        g[q4 * 16 + k] = __uint_as_float(w[k]);
+          for (int ks = 0; ks < 8; ++ks) {
+            const int half = ks >> 2, kin = ks & 3;
+            const uint64_t bd = tc::desc_sw128(smem_u32(vst + half * kTcHalf) + kin * 32, 16, 1024);
+            tc::mma_ts(tl + 384 + mm * 64, tl + mm * 64 + ks * 8, bd, kIdS, ks > 0 ? 1u : 0u);
+            tc::mma_ts(tl + 384 + mm * 64, tl + 128 + mm * 64 + ks * 8, bd, kIdS, 1u);
+          }
+        }
+        tc::commit(&bar.x_full[0]);
+        tc::commit(&bar.empty[st]);
       }
     }
-    // |v|^2 of the tile's keys: four threads per key, 32 elements each
-    {
-      const int key = tid >> 2, part = tid & 3;
-      float acc = 0.f;
+  } else {
+    const int qp = row_ok ? A.qpos[r % A.w] : -1;
+    const float lse2 = row_ok ? A.ws.d3_rowc[wrow * 2] : 0.f;
+    const float an = row_ok ? A.ws.d3_rowc[wrow * 2 + 1] : 0.f;
+    const float* arow = A.a_out;
+    if (row_ok) {
+      const int h = r / A.w, i = r % A.w;
+      arow = A.a_out + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i) * kD;
+    }
+    const int nkeys = j_end - j_begin;
+    float* out = A.scores + static_cast<size_t>(l) * A.dm.cap;
+#pragma unroll 1
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t % kTcStages;
+      const unsigned char* vst = skv + st * kTcKV + 2 * kTcHalf;
+      (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);
+      // |v|^2 of the tile's keys: four threads per key, 32 elements each
+      {
+        const int key = tid >> 2, part = tid & 3;
+        float acc = 0.f;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        const int e0 = (part * 4 + c) * 8;
-        const uint4 x = *reinterpret_cast<const uint4*>(vst + sw_off(key, e0));
-        const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&x);
+        for (int c = 0; c < 4; ++c) {
+          const uint4 x = *reinterpret_cast<const uint4*>(vst + sw_off(key, (part * 4 + c) * 8));
+          const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&x);
 #pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const float2 f = __bfloat1622float2(pr[u]);
-          acc = fmaf(f.x, f.x, fmaf(f.y, f.y, acc));
+          for (int u = 0; u < 4; ++u) {
+            const float2 f = __bfloat1622float2(pr[u]);
+            acc = fmaf(f.x, f.x, fmaf(f.y, f.y, acc));
+          }
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        if (part == 0) sh_vn[key] = acc;
+      }
+      rows_sync();
+      (void)mbar_wait_bounded(&bar.x_full[0], t & 1, A.ws.status);
+      tc::fence_after();
+      float sv[kTcKeys / 2][2], gv[kTcKeys / 2][2];   // [key within half][half]
+      uint32_t v[16], w[16];
+#pragma unroll
+      for (int q4 = 0; q4 < 4; ++q4) {
+        tc::ld16(tl + lane_off + 256 + m * 64 + q4 * 16, v);
+        tc::ld16(tl + lane_off + 384 + m * 64 + q4 * 16, w);
+        tc::wait_ld();
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const int key = q4 * 16 + k;
+          sv[key & 31][key >> 5] = __uint_as_float(v[k]);
+          gv[key & 31][key >> 5] = __uint_as_float(w[k]);
         }
       }
-      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-      if (part == 0) sh_vn[key] = acc;
-    }
-    cp_wait<kTcStages - 2>();
-    fence_async_smem();
-    tc::fence_before();
-    __syncthreads();
-    tc::fence_after();
-    if (tid == 0 && t + 1 < ntiles) issue_mma(t + 1);
-    // residual terms of this row over the tile's keys: the expansion
-    // |a|^2 + |v|^2 - 2<a, v> for p <= 1/2; the key with p > 1/2 (at most
-    // one per row, the weights summing to 1) takes the direct distance
-    int xk = -1;
-    float xx = 0.f;
+      tc::fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&bar.x_free[0]);   // the next tile's MMAs may overwrite S and G
+      int xk = -1;
+      float xx = 0.f;
 #pragma unroll
-    for (int k = 0; k < kTcKeys; ++k) {
-      const bool ok = row_ok && sh_pos[st][k] <= qp;
-      const float x = s[k] * A.scale2 - lse2;
-      const float p = ok ? hw_exp2(x) : 0.f;
-      const float r2 = fmaxf(0.f, an + sh_vn[k] - 2.f * g[k]);
-      float term = p * hw_rcp(1.f - p) * hw_sqrt(r2);
-      if (p > 0.5f) { xk = k; xx = x; term = 0.f; }
-      s[k] = p > 0.f ? term : 0.f;
-    }
-    if (xk >= 0) {
-      const float dterm = residual_direct(xx, arow, vst, xk);
+      for (int hf = 0; hf < 2; ++hf) {
+        float term[kTcKeys / 2];
 #pragma unroll
-      for (int k = 0; k < kTcKeys; ++k)
-        if (k == xk) s[k] = dterm;
-    }
-    // butterfly: each lane ends with the warp's sums of two keys
+        for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
+          const int k = hf * 32 + k2;
+          const bool ok = row_ok && t * kTcKeys + k < nkeys && sh_pos[st][k] <= qp;
+          const float x = sv[k2][hf] * A.scale2 - lse2;
+          const float p = ok ? hw_exp2(x) : 0.f;
+          const float r2 = fmaxf(0.f, an + sh_vn[k] - 2.f * gv[k2][hf]);
+          float tm = p * hw_rcp(1.f - p) * hw_sqrt(r2);
+          if (p > 0.5f) { xk = k; xx = x; tm = 0.f; }
+          term[k2] = p > 0.f ? tm : 0.f;
+        }
+        // the one key of the row with p > 1/2: direct distance, out of line
+        if (xk >= hf * 32 && xk < hf * 32 + 32) {
+          const float dterm = residual_direct(xx, arow, vst, xk);
 #pragma unroll
-    for (int o = 16, cnt = kTcKeys; o >= 1; o >>= 1, cnt >>= 1) {
-      const bool up = (lane & o) != 0;
+          for (int k2 = 0; k2 < kTcKeys / 2; ++k2)
+            if (hf * 32 + k2 == xk) term[k2] = dterm;
+        }
+        // butterfly: each lane ends with the warp's sum of one key
 #pragma unroll
-      for (int i = 0; i < cnt / 2; ++i) {
-        const float send = up ? s[i] : s[cnt / 2 + i];
-        const float keep = up ? s[cnt / 2 + i] : s[i];
-        s[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+        for (int o = 16, cnt = kTcKeys / 2; o >= 1; o >>= 1, cnt >>= 1) {
+          const bool up = (lane & o) != 0;
+#pragma unroll
+          for (int i = 0; i < cnt / 2; ++i) {
+            const float send = up ? term[i] : term[cnt / 2 + i];
+            const float keep = up ? term[cnt / 2 + i] : term[i];
+            term[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+          }
+        }
+        sh_col[warp][hf * 32 + lane] = term[0];
       }
-    }
-    {
-      const int k0 = ((lane >> 4) & 1) * 32 + ((lane >> 3) & 1) * 16 + ((lane >> 2) & 1) * 8 + ((lane >> 1) & 1) * 4 +
-                     (lane & 1) * 2;
-      sh_col[warp][k0] = s[0];
-      sh_col[warp][k0 + 1] = s[1];
-    }
-    __syncthreads();
-    if (tid < kTcKeys) {
-      const int j = j_begin + t * kTcKeys + tid;
-      float tot = 0.f;
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&bar.empty[st]);    // this warp is done with the stage
+      rows_sync();
+      if (tid < kTcKeys) {
+        const int j = j_begin + t * kTcKeys + tid;
+        float tot = 0.f;
 #pragma unroll
-      for (int w = 0; w < kTcThreads / 32; ++w) tot += sh_col[w][tid];
-      if (j < j_end) out[j] = tot;
+        for (int w8 = 0; w8 < kWsRowThreads / 32; ++w8) tot += sh_col[w8][tid];
+        if (j < j_end) out[j] = tot;
+      }
     }
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == 0) tc::dealloc(tl, kTcCols);
+  if (warp == kWsIssuer) tc::dealloc(tl, kTcCols);
 }
 
 }  // namespace
@@ -1024,9 +1064,9 @@ cudaError_t launch_score(const Ctx& ctx, int layer, const void* q_win, int w, co
     return cudaErrorInvalidValue;
   if (A.rows <= kTcRows) {
     const dim3 grid(A.chunks, dm.lanes);
-    d3_tc_pass1_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(A);
+    d3_tc_pass1_kernel<<<grid, kWsThreads, kTcSmem, stream>>>(A);
     d3_combine_kernel<<<dim3((A.rows + 7) / 8, dm.lanes), 256, 0, stream>>>(A);
-    d3_tc_pass2_kernel<<<grid, kTcThreads, kTcSmem, stream>>>(A);
+    d3_tc_pass2_kernel<<<grid, kWsThreads, kTcSmem, stream>>>(A);
     return cudaGetLastError();
   }
   const int groups = (A.rows + kRowsPerCta - 1) / kRowsPerCta;
