@@ -731,12 +731,22 @@ __global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass1_kernel(D3Args A) {
 #pragma unroll
         for (int k = 0; k < 16; ++k) s[q4 * 16 + k] = __uint_as_float(v[k]);
       }
+      // a full tile whose last (largest) position precedes the row is wholly visible
+      const bool all_vis = row_ok && (t + 1) * kTcKeys <= nkeys && sh_pos[st][kTcKeys - 1] <= qp;
       float tmax = -INFINITY;
+      if (all_vis) {
 #pragma unroll
-      for (int k = 0; k < kTcKeys; ++k) {
-        const bool ok = row_ok && t * kTcKeys + k < nkeys && sh_pos[st][k] <= qp;
-        s[k] = ok ? s[k] * A.scale2 : -INFINITY;
-        tmax = fmaxf(tmax, s[k]);
+        for (int k = 0; k < kTcKeys; ++k) {
+          s[k] *= A.scale2;
+          tmax = fmaxf(tmax, s[k]);
+        }
+      } else {
+#pragma unroll
+        for (int k = 0; k < kTcKeys; ++k) {
+          const bool ok = row_ok && t * kTcKeys + k < nkeys && sh_pos[st][k] <= qp;
+          s[k] = ok ? s[k] * A.scale2 : -INFINITY;
+          tmax = fmaxf(tmax, s[k]);
+        }
       }
       float factor = 1.f;
       if (tmax > m_run + kTcRescale) {
@@ -982,19 +992,34 @@ __global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass2_kernel(D3Args A) {
       if (lane == 0) mbar_arrive1(&bar.x_free[0]);   // the next tile's MMAs may overwrite S and G
       int xk = -1;
       float xx = 0.f;
+      // a full tile whose last (largest) position precedes the row is wholly visible
+      const bool all_vis = row_ok && (t + 1) * kTcKeys <= nkeys && sh_pos[st][kTcKeys - 1] <= qp;
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         float term[kTcKeys / 2];
+        if (all_vis) {
 #pragma unroll
-        for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
-          const int k = hf * 32 + k2;
-          const bool ok = row_ok && t * kTcKeys + k < nkeys && sh_pos[st][k] <= qp;
-          const float x = sv[k2][hf] * A.scale2 - lse2;
-          const float p = ok ? hw_exp2(x) : 0.f;
-          const float r2 = fmaxf(0.f, an + sh_vn[k] - 2.f * gv[k2][hf]);
-          float tm = p * hw_rcp(1.f - p) * hw_sqrt(r2);
-          if (p > 0.5f) { xk = k; xx = x; tm = 0.f; }
-          term[k2] = p > 0.f ? tm : 0.f;
+          for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
+            const int k = hf * 32 + k2;
+            const float x = fmaf(sv[k2][hf], A.scale2, -lse2);
+            const float p = hw_exp2(x);
+            const float r2 = fmaxf(0.f, fmaf(-2.f, gv[k2][hf], an + sh_vn[k]));
+            float tm = p * hw_rcp(1.f - p) * hw_sqrt(r2);
+            if (p > 0.5f) { xk = k; xx = x; tm = 0.f; }
+            term[k2] = tm;
+          }
+        } else {
+#pragma unroll
+          for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
+            const int k = hf * 32 + k2;
+            const bool ok = row_ok && t * kTcKeys + k < nkeys && sh_pos[st][k] <= qp;
+            const float x = fmaf(sv[k2][hf], A.scale2, -lse2);
+            const float p = ok ? hw_exp2(x) : 0.f;
+            const float r2 = fmaxf(0.f, fmaf(-2.f, gv[k2][hf], an + sh_vn[k]));
+            float tm = p * hw_rcp(1.f - p) * hw_sqrt(r2);
+            if (p > 0.5f) { xk = k; xx = x; tm = 0.f; }
+            term[k2] = p > 0.f ? tm : 0.f;
+          }
         }
         // the one key of the row with p > 1/2: direct distance, out of line
         if (xk >= hf * 32 && xk < hf * 32 + 32) {
