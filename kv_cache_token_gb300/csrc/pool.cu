@@ -2,6 +2,8 @@
 // forced compaction with its freed-block / move outputs, and the layer
 // metrics (vToken review, Eq. (1) and Fig. 1's share of blocks at <= 50%
 // utilisation).
+#include <cooperative_groups.h>
+
 #include "lane_ops.cuh"
 
 namespace kve {
@@ -133,6 +135,147 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const KeyT* keys, c
     total += tot;
   }
   if (threadIdx.x == 0) n_victims[l] = total;
+}
+
+// Selection by a cluster of kSelCluster CTAs per lane: each CTA takes a
+// contiguous slice of the lane's entries; every radix pass merges the CTAs'
+// 256-bin histograms into the leader CTA's shared memory (distributed shared
+// memory atomics) and the leader's bucket choice is read back by all; the
+// victims are written ascending, each CTA at the offset of the lower ranks'
+// counts.  Same result as select_kernel.
+constexpr int kSelCluster = 8;
+constexpr int kSelClThreads = 512;
+
+struct SelState {
+  unsigned long long key_prefix, key_mask;
+  uint32_t pos_prefix, pos_mask;
+  int k_rem, done, inclusive;
+};
+
+template <typename KeyT>
+__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelClThreads)
+    select_cluster_kernel(const KeyT* keys, const int32_t* positions, const int32_t* counts, int stride,
+                          int budget, int R, int32_t* victims, int32_t* n_victims) {
+  namespace cg = cooperative_groups;
+  cg::cluster_group cluster = cg::this_cluster();
+  __shared__ int sh_hist[256];       // leader: merged histogram
+  __shared__ int sh_local[256];      // this CTA's histogram
+  __shared__ SelState sh_state;      // leader: the descent so far
+  __shared__ int sh_count;           // this CTA's number of victims
+  __shared__ int sh_scan[40];
+  const int rank = static_cast<int>(cluster.block_rank());
+  const int l = blockIdx.x / kSelCluster;
+  const int tid = threadIdx.x;
+  const int n = max(0, min(counts[l], stride));
+  const int k = max(0, n - budget);
+  if (n == 0 || k == 0) {               // uniform over the cluster
+    if (rank == 0 && tid == 0) n_victims[l] = 0;
+    return;
+  }
+  const KeyT* kk = keys + static_cast<size_t>(l) * stride;
+  const int32_t* pp = positions + static_cast<size_t>(l) * stride;
+  const int cut = pp[n - 1] - R + 1;
+  const int chunk = (n + kSelCluster - 1) / kSelCluster;
+  const int i_begin = min(n, rank * chunk), i_end = min(n, i_begin + chunk);
+  int* lead_hist = cluster.map_shared_rank(sh_hist, 0);
+  SelState* lead = cluster.map_shared_rank(&sh_state, 0);
+  if (rank == 0 && tid == 0) {
+    sh_state.key_prefix = 0; sh_state.key_mask = 0; sh_state.pos_prefix = 0; sh_state.pos_mask = 0;
+    sh_state.k_rem = k; sh_state.done = 0; sh_state.inclusive = 0;
+  }
+  const int key_bits = static_cast<int>(sizeof(KeyT)) * 8;
+  SelectResult r;
+  r.key_prefix = 0; r.key_mask = 0; r.pos_prefix = 0; r.pos_mask = 0; r.inclusive = 0; r.k = k;
+  for (int shift = key_bits + 32 - 8; shift >= 0; shift -= 8) {
+    if (rank == 0 && tid < 256) sh_hist[tid] = 0;
+    if (tid < 256) sh_local[tid] = 0;
+    cluster.sync();
+    for (int i = i_begin + tid; i < i_end; i += blockDim.x) {
+      const int p = pp[i];
+      if (p >= cut) continue;
+      const unsigned long long key = mono_key(kk[i]);
+      if ((key & r.key_mask) != r.key_prefix || (static_cast<uint32_t>(p) & r.pos_mask) != r.pos_prefix) continue;
+      const int digit = shift >= 32 ? static_cast<int>((key >> (shift - 32)) & 0xFF)
+                                    : static_cast<int>((static_cast<uint32_t>(p) >> shift) & 0xFF);
+      atomicAdd(&sh_local[digit], 1);
+    }
+    __syncthreads();
+    if (tid < 256 && sh_local[tid]) atomicAdd(&lead_hist[tid], sh_local[tid]);
+    cluster.sync();
+    if (rank == 0 && tid < 32) {
+      // the bucket where the cumulative count reaches k_rem
+      const int k_rem = sh_state.k_rem;
+      int c[8], sum = 0;
+#pragma unroll
+      for (int j = 0; j < 8; ++j) { c[j] = sh_hist[tid * 8 + j]; sum += c[j]; }
+      const int inc = warp_incl_scan(sum), exc = inc - sum;
+      int found = -1, below = 0, cnt = 0;
+      if (exc < k_rem && inc >= k_rem) {
+        int acc = exc;
+        for (int j = 0; j < 8; ++j) {
+          if (acc + c[j] >= k_rem) { found = tid * 8 + j; below = acc; cnt = c[j]; break; }
+          acc += c[j];
+        }
+      }
+      const unsigned ball = __ballot_sync(0xffffffffu, found >= 0);
+      const int src = ball ? __ffs(ball) - 1 : 0;
+      found = __shfl_sync(0xffffffffu, found, src);
+      below = __shfl_sync(0xffffffffu, below, src);
+      cnt = __shfl_sync(0xffffffffu, cnt, src);
+      if (tid == 0) {
+        if (!ball) {
+          sh_state.done = 1; sh_state.inclusive = 1;    // fewer candidates than k: all matching are victims
+        } else {
+          if (shift >= 32) {
+            sh_state.key_prefix |= static_cast<unsigned long long>(found) << (shift - 32);
+            sh_state.key_mask |= 0xFFull << (shift - 32);
+          } else {
+            sh_state.pos_prefix |= static_cast<uint32_t>(found) << shift;
+            sh_state.pos_mask |= 0xFFu << shift;
+          }
+          sh_state.k_rem = k_rem - below;
+          if (cnt == k_rem - below || shift == 0) { sh_state.done = 1; sh_state.inclusive = 1; }
+        }
+      }
+    }
+    cluster.sync();
+    const SelState st = *lead;
+    r.key_prefix = st.key_prefix; r.key_mask = st.key_mask;
+    r.pos_prefix = st.pos_prefix; r.pos_mask = st.pos_mask; r.inclusive = st.inclusive;
+    if (st.done) break;
+  }
+  // victims of this CTA's slice, counted, then written at the cluster offset
+  int mine = 0;
+  for (int i = i_begin + tid; i < i_end; i += blockDim.x) {
+    const int p = pp[i];
+    mine += (p < cut && select_is_victim(r, mono_key(kk[i]), static_cast<uint32_t>(p))) ? 1 : 0;
+  }
+  int tot;
+  (void)block_excl_scan(mine, sh_scan, &tot);
+  if (tid == 0) sh_count = tot;
+  cluster.sync();
+  int offset = 0, all = 0;
+  for (int q = 0; q < kSelCluster; ++q) {
+    const int cq = *cluster.map_shared_rank(&sh_count, q);
+    if (q < rank) offset += cq;
+    all += cq;
+  }
+  int32_t* vo = victims + static_cast<size_t>(l) * stride;
+  for (int base = i_begin; base < i_end; base += blockDim.x) {
+    const int i = base + tid;
+    bool v = false;
+    int p = 0;
+    if (i < i_end) {
+      p = pp[i];
+      v = p < cut && select_is_victim(r, mono_key(kk[i]), static_cast<uint32_t>(p));
+    }
+    int t2;
+    const int ex = block_excl_scan(v ? 1 : 0, sh_scan, &t2);
+    if (v) vo[offset + ex] = p;
+    offset += t2;
+  }
+  if (rank == 0 && tid == 0) n_victims[l] = all;
+  cluster.sync();    // no CTA leaves while another may still read its shared memory
 }
 
 // ---------------------------------------------------------------------------
@@ -295,12 +438,13 @@ cudaError_t launch_select(const Ctx& ctx, const void* keys, int key_dtype, const
                           const int32_t* counts, int n_lanes, int stride, int budget, int recent,
                           int32_t* victims, int32_t* n_victims, cudaStream_t stream) {
   (void)ctx;
+  if (n_lanes <= 0) return cudaSuccess;
   if (key_dtype == KVEVICT_KEY_F64)
-    select_kernel<double><<<n_lanes, kSelThreads, 0, stream>>>(static_cast<const double*>(keys), positions, counts,
-                                                              stride, budget, recent, victims, n_victims);
+    select_cluster_kernel<double><<<n_lanes * kSelCluster, kSelClThreads, 0, stream>>>(
+        static_cast<const double*>(keys), positions, counts, stride, budget, recent, victims, n_victims);
   else
-    select_kernel<float><<<n_lanes, kSelThreads, 0, stream>>>(static_cast<const float*>(keys), positions, counts,
-                                                             stride, budget, recent, victims, n_victims);
+    select_cluster_kernel<float><<<n_lanes * kSelCluster, kSelClThreads, 0, stream>>>(
+        static_cast<const float*>(keys), positions, counts, stride, budget, recent, victims, n_victims);
   return cudaGetLastError();
 }
 
