@@ -144,7 +144,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const KeyT* keys, c
 // victims are written ascending, each CTA at the offset of the lower ranks'
 // counts.  Same result as select_kernel.
 constexpr int kSelCluster = 8;
-constexpr int kSelClThreads = 512;
+constexpr int kSelClThreads = 1024;
 
 struct SelState {
   unsigned long long key_prefix, key_mask;
@@ -186,10 +186,11 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelClThre
   const int key_bits = static_cast<int>(sizeof(KeyT)) * 8;
   SelectResult r;
   r.key_prefix = 0; r.key_mask = 0; r.pos_prefix = 0; r.pos_mask = 0; r.inclusive = 0; r.k = k;
+  if (rank == 0 && tid < 256) sh_hist[tid] = 0;
+  cluster.sync();
   for (int shift = key_bits + 32 - 8; shift >= 0; shift -= 8) {
-    if (rank == 0 && tid < 256) sh_hist[tid] = 0;
     if (tid < 256) sh_local[tid] = 0;
-    cluster.sync();
+    __syncthreads();
     for (int i = i_begin + tid; i < i_end; i += blockDim.x) {
       const int p = pp[i];
       if (p >= cut) continue;
@@ -222,6 +223,8 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelClThre
       found = __shfl_sync(0xffffffffu, found, src);
       below = __shfl_sync(0xffffffffu, below, src);
       cnt = __shfl_sync(0xffffffffu, cnt, src);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) sh_hist[tid * 8 + j] = 0;   // ready for the next pass
       if (tid == 0) {
         if (!ball) {
           sh_state.done = 1; sh_state.inclusive = 1;    // fewer candidates than k: all matching are victims
