@@ -41,7 +41,7 @@ def parse():
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--workload", default="h2o_70b")
     ap.add_argument("--e2e-steps", type=int, default=8)
-    ap.add_argument("--cpu-lanes", type=int, default=32)
+    ap.add_argument("--cpu-lanes", type=int, default=96)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-layers", type=int, default=0,
                     help="profiling only: run the workload with this many layers (not a bench number)")
