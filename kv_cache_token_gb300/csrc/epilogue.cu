@@ -53,6 +53,14 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
 __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const Dims& dm, int* sh_scan,
                                int* sh_flag);
 
+// 2^x by the hardware approximation (PTX ex2.approx.ftz, relative error
+// about 2^-22; results below 2^-126 flush to zero).
+__device__ __forceinline__ float hw_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
 // Marks this lane's epilogue done (thread 0 only).  The per-lane requests
 // the allocator reads (need_admit, want_dst, plan_tlive, count, released
 // block owners) are written before; the fence makes them visible to the
@@ -211,14 +219,14 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
         const float lse2 = sh_lse2[h];
         const float* row = lg_s + h * kFastN + tid;
 #pragma unroll
-        for (int j = 0; j < kFastPer; ++j) w[j] += exp2f(row[j * kEpiThreads] - lse2);
+        for (int j = 0; j < kFastPer; ++j) w[j] += hw_exp2(row[j * kEpiThreads] - lse2);
       }
     } else {
       for (int h = 0; h < g; ++h) {
         const float lse2 = sh_lse2[h];
         const float* row = lg_s + h * kFastN + tid;
 #pragma unroll
-        for (int j = 0; j < kFastPer; ++j) w[j] += exp2f(row[j * kEpiThreads] - lse2);
+        for (int j = 0; j < kFastPer; ++j) w[j] += hw_exp2(row[j * kEpiThreads] - lse2);
       }
     }
 #pragma unroll
@@ -315,6 +323,9 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
   int t_live = 0;
   const int ndst = lane_plan(L, nb2, m + 1, false, dm.theta_f, need, &t_live, sh_scan2);
   const bool work = need || ndst > 0;
+  // the done counter's old value is only needed at the end: its round trip
+  // overlaps the table rewrite and the output combine
+  int done_old = 0;
   if (tid == 0) {
     A.ls.count[l] = m + 1;
     if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
@@ -322,8 +333,8 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
     A.ws.want_dst[l] = ndst;
     A.ws.plan_tlive[l] = t_live;
     if (work) atomicOr(A.ws.work_flag, 1);
-    signal_done(A.ws, work, sh_last, sh_flag);
-    *sh_sig = 1;
+    __threadfence();
+    done_old = atomicAdd(A.ws.epi_done, 1 + (work ? kWorkUnit : 0));
   }
   // ---- the table: survivors shift over the victim; the new token goes last -----------
 #pragma unroll
@@ -374,6 +385,11 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
         a1 = fmaf(__ldcg(po + (static_cast<size_t>(s2) * g + h) * d + e), sh_scale[s2][h], a1);
       A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = (a0 + a1) / sh_L[h];
     }
+  }
+  if (tid == 0) {
+    *sh_last = (done_old & (kWorkUnit - 1)) == static_cast<int>(gridDim.x) - 1;
+    *sh_flag = (done_old >> kWorkShift) + (work ? 1 : 0);
+    *sh_sig = 1;
   }
 }
 
