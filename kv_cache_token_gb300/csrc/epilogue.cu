@@ -63,12 +63,11 @@ __device__ __forceinline__ float hw_exp2(float x) {
 
 // Marks this lane's epilogue done (thread 0 only).  The per-lane requests
 // the allocator reads (need_admit, want_dst, plan_tlive, count, released
-// block owners) are written before; the fence makes them visible to the
-// last CTA.  The done counter carries the number of lanes asking for blocks
+// block owners) are written before (by any thread of the CTA, ordered by a
+// barrier before this call); the release makes them visible to the last CTA.  The done counter carries the number of lanes asking for blocks
 // in its upper bits, so the common no-work case needs no further atomic.
 __device__ __forceinline__ void signal_done(const Workspace& ws, bool work, int* sh_last, int* sh_flag) {
-  __threadfence();
-  const int old = atomicAdd(ws.epi_done, 1 + (work ? kWorkUnit : 0));
+  const int old = atomic_add_release(ws.epi_done, 1 + (work ? kWorkUnit : 0));
   *sh_last = (old & (kWorkUnit - 1)) == static_cast<int>(gridDim.x) - 1;
   *sh_flag = (old >> kWorkShift) + (work ? 1 : 0);
 }
@@ -82,14 +81,17 @@ __device__ __forceinline__ void signal_done(const Workspace& ws, bool work, int*
 // split-K statistics by plain loads.  The minimum (key, position) and its
 // slot come from three warp reductions and one barrier; the holder of the
 // victim's block decides from the mask it already holds whether the block
-// empties.  The allocator's requests and the done counter go out before
-// the table is rewritten, so the counter's fence does not wait for those
-// stores.
+// empties.  The fragmentation test of Eq. (1) is evaluated before the wait
+// for each of the eight outcomes the scoring can have (double division is
+// slow on this part).  The allocator's requests and the done counter go out
+// before the table is rewritten, so the counter's release does not wait for
+// those stores, and the counter's old value is read only at the end.
 template <typename KT>
 __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& L, const int n, unsigned char* dsm,
                                               int* sh_sig, int* sh_last, int* sh_flag) {
-  __shared__ float sh_L[8], sh_lse2[8];
-  __shared__ float sh_scale[kMaxSeg][8];
+  __shared__ float sh_rL[8], sh_lse2[8];
+  __shared__ __align__(16) float sh_scale[8][kMaxSeg];   // per head, per split-K segment
+  __shared__ unsigned sh_over;
   __shared__ unsigned sh_wkey[kEpiThreads / 32], sh_wpos[kEpiThreads / 32], sh_wslot[kEpiThreads / 32];
   __shared__ unsigned sh_wfree[kEpiThreads / 32];
   __shared__ int sh_nan, sh_dead, sh_tail;
@@ -133,6 +135,8 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
     bm[j] = bk[j] >= 0 ? (__ldcg(L.mask + bk[j]) & 0xFFFF) : 0xFFFF;
   }
   if (bad_blk) set_status(A.ws.status, ST_BAD_INDEX);
+  // a request of this lane left non-zero (the invariant is that none is)
+  const bool stale_req = tid == 0 && (__ldcg(A.ws.need_admit + l) | __ldcg(A.ws.want_dst + l)) != 0;
   if (tid == 0) {
     sh_nan = 0;
     sh_dead = -1;
@@ -147,6 +151,16 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
       if (bk[j] >= 0 && bm[j] != 0xFFFF) fr = min(fr, static_cast<unsigned>(bk[j] * kBlock + (__ffs(~bm[j]) - 1)));
     fr = __reduce_min_sync(0xffffffffu, fr);
     if (lane == 0) sh_wfree[warp] = fr;
+  }
+  // Eq. (1)'s test for each outcome the scoring has yet to decide: a victim
+  // or none (bit 0), its block emptied or not (bit 1), the new token waiting
+  // for a fresh block or not (bit 2); one lane per outcome
+  if (warp == 0) {
+    const int vc = lane & 1, dead = (lane >> 1) & 1, fresh = (lane >> 2) & 1;
+    const int N = nb - dead + fresh;
+    const bool o = lane < 8 && N > 0 && frag_over(n - vc + 1, N, dm.theta_f);
+    const unsigned bits = __ballot_sync(0xffffffffu, o);
+    if (lane == 0) sh_over = bits;
   }
   // the last kept token must precede the new one
   bool late = false;
@@ -191,13 +205,13 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
     const float M = warp_max(fmaxf(m0.x, m1.x));
     const float s0 = m0.x == -INFINITY ? 0.f : exp2f(m0.x - M);
     const float s1 = m1.x == -INFINITY ? 0.f : exp2f(m1.x - M);
-    sh_scale[lane][h] = s0;
-    sh_scale[lane + 32][h] = s1;
+    sh_scale[h][lane] = s0;
+    sh_scale[h][lane + 32] = s1;
     float Ls = m0.y * s0 + m1.y * s1;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
     if (lane == 0) {
-      sh_L[h] = Ls;
+      sh_rL[h] = 1.f / Ls;
       const float lse2 = M + log2f(Ls);
       sh_lse2[h] = lse2;
       A.lse[static_cast<size_t>(b) * dm.Hq + kh * g + h] = lse2 * kLn2;
@@ -321,7 +335,8 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
   if (!need && tid == 0) atomicOr(&L.mask[best >> 4], 1 << (best & 15));
   __syncthreads();
   int t_live = 0;
-  const int ndst = lane_plan(L, nb2, m + 1, false, dm.theta_f, need, &t_live, sh_scan2);
+  const int outcome = vcount | (dead_j >= 0 ? 2 : 0) | (need ? 4 : 0);
+  const int ndst = lane_plan_given(L, nb2, ((sh_over >> outcome) & 1u) != 0, false, need, &t_live, sh_scan2);
   const bool work = need || ndst > 0;
   // the done counter's old value is only needed at the end: its round trip
   // overlaps the table rewrite and the output combine
@@ -329,12 +344,20 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
   if (tid == 0) {
     A.ls.count[l] = m + 1;
     if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
-    A.ws.need_admit[l] = need ? 1 : 0;
-    A.ws.want_dst[l] = ndst;
-    A.ws.plan_tlive[l] = t_live;
+    // The allocator reads a lane's requests (and its count) only when they
+    // are non-zero; between steps they hold zero (the apply kernel clears
+    // what it consumed).  A lane that asks for blocks, released a block or
+    // clears a request left over publishes with release semantics; the
+    // writes of the others are of no concern to the allocator.
+    const bool publish = work || dead_j >= 0 || stale_req;
+    if (work || stale_req) {
+      A.ws.need_admit[l] = need ? 1 : 0;
+      A.ws.want_dst[l] = ndst;
+      A.ws.plan_tlive[l] = t_live;
+    }
     if (work) atomicOr(A.ws.work_flag, 1);
-    __threadfence();
-    done_old = atomicAdd(A.ws.epi_done, 1 + (work ? kWorkUnit : 0));
+    const int inc = 1 + (work ? kWorkUnit : 0);
+    done_old = publish ? atomic_add_release(A.ws.epi_done, inc) : atomicAdd(A.ws.epi_done, inc);
   }
   // ---- the table: survivors shift over the victim; the new token goes last -----------
 #pragma unroll
@@ -369,21 +392,43 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
     if (l == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_STEPS]), 1ull);
   }
   // ---- output: combine the split-K partial outputs (the first kPoSeg from
-  // shared memory), two interleaved chains per output ---------------------------------
+  // shared memory); a thread owns two adjacent elements of one head, so the
+  // segment scales are warp-uniform and read four at a time -------------------------
   if (A.has_q) {
     const int ns = min(nseg, kPoSeg);
-    for (int he = tid; he < g * d; he += kEpiThreads) {
-      const int h = he / d, e = he - h * d;
-      float a0 = 0.f, a1 = 0.f;
-      int s2 = 0;
-      for (; s2 + 1 < ns; s2 += 2) {
-        a0 = fmaf(po_s[(s2 * g + h) * d + e], sh_scale[s2][h], a0);
-        a1 = fmaf(po_s[((s2 + 1) * g + h) * d + e], sh_scale[s2 + 1][h], a1);
+    const bool out8 = (reinterpret_cast<uintptr_t>(A.out) & 7) == 0;
+    for (int q2 = tid; q2 < (g * d) >> 1; q2 += kEpiThreads) {
+      const int he = q2 * 2, h = he / d, e = he - h * d;
+      const float4* sc4 = reinterpret_cast<const float4*>(sh_scale[h]);
+      float2 a0 = make_float2(0.f, 0.f), a1 = make_float2(0.f, 0.f);
+#pragma unroll
+      for (int s4 = 0; s4 < kPoSeg / 4; ++s4) {
+        const float4 c4 = sc4[s4];
+        const float cs[4] = {c4.x, c4.y, c4.z, c4.w};
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          const int s2 = s4 * 4 + u;
+          if (s2 < ns) {
+            const float2 pv = *reinterpret_cast<const float2*>(po_s + (s2 * g + h) * d + e);
+            float2& a = (u & 1) ? a1 : a0;
+            a.x = fmaf(pv.x, cs[u], a.x);
+            a.y = fmaf(pv.y, cs[u], a.y);
+          }
+        }
       }
-      if (s2 < ns) a0 = fmaf(po_s[(s2 * g + h) * d + e], sh_scale[s2][h], a0);
-      for (s2 = kPoSeg; s2 < nseg; ++s2)
-        a1 = fmaf(__ldcg(po + (static_cast<size_t>(s2) * g + h) * d + e), sh_scale[s2][h], a1);
-      A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = (a0 + a1) / sh_L[h];
+      for (int s2 = kPoSeg; s2 < nseg; ++s2) {
+        const float2 pv = __ldcg(reinterpret_cast<const float2*>(po + (static_cast<size_t>(s2) * g + h) * d + e));
+        a0.x = fmaf(pv.x, sh_scale[h][s2], a0.x);
+        a0.y = fmaf(pv.y, sh_scale[h][s2], a0.y);
+      }
+      const float r = sh_rL[h];
+      float* o = A.out + (static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e;
+      if (out8) {
+        *reinterpret_cast<float2*>(o) = make_float2((a0.x + a1.x) * r, (a0.y + a1.y) * r);
+      } else {
+        o[0] = (a0.x + a1.x) * r;
+        o[1] = (a0.y + a1.y) * r;
+      }
     }
   }
   if (tid == 0) {
@@ -413,7 +458,8 @@ __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs
       set_status(A.ws.status, ST_CAPACITY);
       A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
     }
-  } else if (dm.policy == KVEVICT_H2O && n + 1 - dm.budget <= 1 && n <= kFastN && dm.g <= 8 && dm.d <= 128) {
+  } else if (dm.policy == KVEVICT_H2O && n + 1 - dm.budget <= 1 && n <= kFastN && dm.g <= 8 && dm.d <= 128 &&
+             (dm.d & 1) == 0) {
     h2o_fast_step<KT>(A, L, n, dsm, &sh_sig, &sh_last, &sh_flag);
   } else {
     lane_step<KT>(A, L, n, dsm, &sh_work);

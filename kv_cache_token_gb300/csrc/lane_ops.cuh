@@ -241,22 +241,21 @@ __device__ __forceinline__ int lane_prune_blocks(const LaneRefs& L, int l, int* 
   return out;
 }
 
-// Relocation plan of a lane after its evictions and admission; a pending
-// admission counts as one more block holding one token.
+// Eq. (1)'s fragmentation test F > theta for N blocks holding n_live tokens,
+// in double (theta_f is widened exactly); N > 0.
+__device__ __forceinline__ bool frag_over(int n_live, int N, float theta_f) {
+  const double Fd = 1.0 - static_cast<double>(n_live) / (static_cast<double>(N) * kBlock);
+  return Fd > static_cast<double>(theta_f);
+}
+
+// Relocation plan of a lane after its evictions and admission, given the
+// outcome of the fragmentation test (over); a pending admission counts as
+// one more block holding one token.
 // Returns the number of destination blocks (0 = no plan); *t_live = tokens to move.
-__device__ __forceinline__ int lane_plan(const LaneRefs& L, int nb, int n_live, bool forced, float theta_f,
-                         bool pending_admit, int* t_live_out, int* sh_scan) {
+__device__ __forceinline__ int lane_plan_given(const LaneRefs& L, int nb, bool over, bool forced, bool pending_admit,
+                                               int* t_live_out, int* sh_scan) {
   const int N = nb + (pending_admit ? 1 : 0);
-  if (N == 0) { *t_live_out = 0; return 0; }
-  // Eq. (1) over the lane's blocks, in double (theta_f is widened exactly);
-  // one lane of each warp divides (double arithmetic is slow on this part)
-  int over = 0;
-  if ((threadIdx.x & 31) == 0) {
-    const double Fd = 1.0 - static_cast<double>(n_live) / (static_cast<double>(N) * kBlock);
-    over = Fd > static_cast<double>(theta_f) ? 1 : 0;
-  }
-  over = __shfl_sync(0xffffffffu, over, 0);
-  if (!forced && !over) { *t_live_out = 0; return 0; }
+  if (N == 0 || (!forced && !over)) { *t_live_out = 0; return 0; }
   int src = 0, tl = 0;
   for (int j = threadIdx.x; j < nb; j += blockDim.x) {
     const int c = __popc(L.mask[L.blocks[j]] & 0xFFFF);
@@ -270,6 +269,17 @@ __device__ __forceinline__ int lane_plan(const LaneRefs& L, int nb, int n_live, 
   if (!(src_tot > ndst)) { *t_live_out = 0; return 0; }
   *t_live_out = tl_tot;
   return ndst;
+}
+
+// The same with the test evaluated here: one lane of each warp divides
+// (double arithmetic is slow on this part).
+__device__ __forceinline__ int lane_plan(const LaneRefs& L, int nb, int n_live, bool forced, float theta_f,
+                         bool pending_admit, int* t_live_out, int* sh_scan) {
+  const int N = nb + (pending_admit ? 1 : 0);
+  int over = 0;
+  if ((threadIdx.x & 31) == 0 && N > 0) over = frag_over(n_live, N, theta_f) ? 1 : 0;
+  over = __shfl_sync(0xffffffffu, over, 0);
+  return lane_plan_given(L, nb, over != 0, forced, pending_admit, t_live_out, sh_scan);
 }
 
 }  // namespace kve

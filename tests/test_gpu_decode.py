@@ -124,3 +124,55 @@ def test_steps_enqueued_without_host_sync(order):
         compare_states(gpu_state(eng, layer), oracle_state(orc, layer), shp.policy, "final layer %d" % layer)
     code, msg = eng.last_error()
     assert code == 0, msg
+
+
+def test_decode_steps_captured_in_a_cuda_graph():
+    """The library never allocates or synchronises inside a step, so decode
+    steps can be captured into a CUDA graph (programmatic-dependent launches
+    included) and replayed.  Four steps over two layers are captured once and
+    replayed once; every captured call's outputs, victims and the final
+    tables match the oracle run in the same order."""
+    shp = scaled("h2o_70b", num_layers=2, batch=2, num_kv_heads=2, num_q_heads=16, ctx=900, steps=6,
+                 budget=200, recent_window=100)
+    wl = Workload(shp)
+    layers = [0, 1]
+    eng, orc = make_pair(shp, layers=layers)
+    for layer in layers:
+        prefill_both(eng, orc, wl, layer)
+    # one eager step per layer first (mass eviction and relocation)
+    for layer in layers:
+        q, kn, vn, pos = wl.step(layer, 0)
+        eng.decode_step(layer, q.cuda(), kn.cuda(), vn.cuda(), pos)
+        orc.decode_step(layer, q.double().numpy(), kn.double().numpy(), vn.double().numpy(), pos)
+    torch.cuda.synchronize()
+    calls = []
+    for t in (1, 2):
+        for layer in layers:
+            q, kn, vn, pos = wl.step(layer, t)
+            calls.append(dict(layer=layer, t=t, q=q, kn=kn, vn=vn, pos=pos, qg=q.cuda(), kg=kn.cuda(),
+                              vg=vn.cuda(),
+                              out=torch.empty((shp.batch, shp.num_q_heads, shp.head_dim), dtype=torch.float32,
+                                              device="cuda"),
+                              lse=torch.empty((shp.batch, shp.num_q_heads), dtype=torch.float32, device="cuda"),
+                              vic=torch.zeros((eng.lanes, shp.max_tokens), dtype=torch.int32, device="cuda"),
+                              nv=torch.zeros((eng.lanes,), dtype=torch.int32, device="cuda")))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        for c in calls:
+            eng.decode_step(c["layer"], c["qg"], c["kg"], c["vg"], c["pos"], c["out"], c["lse"], c["vic"], c["nv"])
+    graph.replay()
+    torch.cuda.synchronize()
+    for c in calls:
+        ref = orc.decode_step(c["layer"], c["q"].double().numpy(), c["kn"].double().numpy(),
+                              c["vn"].double().numpy(), c["pos"])
+        what = "layer %d step %d (graph)" % (c["layer"], c["t"])
+        assert_rows_close(c["out"].cpu().numpy(), ref["out"], what + " out")
+        assert_rows_close(c["lse"].cpu().numpy()[..., None], ref["lse"][..., None], what + " lse")
+        got = victim_lists(c["nv"], c["vic"])
+        for l in range(eng.lanes):
+            np.testing.assert_array_equal(got[l], ref["victims"][l], err_msg=what + " lane %d victims" % l)
+    for layer in layers:
+        compare_states(gpu_state(eng, layer), oracle_state(orc, layer), shp.policy, "final layer %d" % layer)
+    code, msg = eng.last_error()
+    assert code == 0, msg
