@@ -153,7 +153,12 @@ size_t kvevict_buffer_size(const kvevict_config* cfg, int which);
 size_t kvevict_workspace_size(const kvevict_config* cfg);
 
 /* Validates cfg, records the buffer pointers (no copy, no allocation) and
- * queries the current CUDA device.  *out is NULL on failure. */
+ * queries the current CUDA device.  k_pool and v_pool must be 16-byte aligned
+ * and the workspace 256-byte aligned (KVEVICT_E_INVALID_ARG otherwise).  With
+ * a scoring window (max_window > 0, bf16, head_dim 128) it also encodes, on
+ * the host, TMA tensor maps over every layer's K and V pool for the window
+ * scoring's row gathers (KVEVICT_E_CUDA if the driver refuses).  *out is
+ * NULL on failure. */
 kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* bufs,
                               kvevict_ctx** out);
 void kvevict_destroy(kvevict_ctx* ctx);

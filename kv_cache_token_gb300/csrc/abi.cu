@@ -79,8 +79,10 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base) {
     w.d3_alo = reinterpret_cast<__nv_bfloat16*>(take(lanes * rows * d * 2));
     w.d3_rowc = reinterpret_cast<float*>(take(lanes * rows * 2 * 4));
     w.d3_score_part = reinterpret_cast<float*>(take(4 * lanes * cap * 4));
+    w.d3_vn = reinterpret_cast<float*>(take(lanes * cap * 4));
   } else {
     w.d3_part = nullptr; w.d3_ahi = nullptr; w.d3_alo = nullptr; w.d3_rowc = nullptr; w.d3_score_part = nullptr;
+    w.d3_vn = nullptr;
   }
   if (ws) *ws = w;
   return off;
@@ -222,8 +224,11 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   ctx->c.sm_count = sms;
   ctx->c.device = dev;
   ctx->c.last_layer = -1;
+  ctx->c.tmaps = nullptr;
   ctx->c.ws_bytes = kve::workspace_layout(*cfg, &ctx->c.ws, static_cast<char*>(bufs->workspace));
-  if (kve::prepare_kernels(ctx->c) != cudaSuccess || ctx->c.attend_ctas_per_sm < 1) {
+  if (kve::prepare_kernels(ctx->c) != cudaSuccess || ctx->c.attend_ctas_per_sm < 1 ||
+      kve::prepare_tensor_maps(ctx->c) != cudaSuccess) {
+    delete[] ctx->c.tmaps;
     delete ctx;
     return KVEVICT_E_CUDA;
   }
@@ -231,7 +236,11 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   return KVEVICT_OK;
 }
 
-void kvevict_destroy(kvevict_ctx* ctx) { delete ctx; }
+void kvevict_destroy(kvevict_ctx* ctx) {
+  if (!ctx) return;
+  delete[] ctx->c.tmaps;
+  delete ctx;
+}
 
 static kvevict_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVEVICT_OK : KVEVICT_E_CUDA; }
 

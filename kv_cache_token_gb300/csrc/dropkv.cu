@@ -13,6 +13,9 @@
 //   ||a||^2 + ||v||^2 - 2 G)) (+inf where 1 - p <= 0); column sums over the
 //   CTA's rows -> one partial per row group.
 // finalize: scores = sum of the row-group partials.
+#include <cudaTypedefs.h>
+#include <new>
+
 #include "kvevict_internal.cuh"
 #include "tcgen05.cuh"
 
@@ -481,18 +484,25 @@ __global__ void __launch_bounds__(256) d3_finalize_kernel(D3Args A, int groups) 
 //   the running max), writes P as bf16 hi + lo over S in tensor memory, and
 //   O += P V takes P from tensor memory and V (MN-major) from shared memory.
 //   Tensor-memory columns: O of tile 0 / 1 at 0 / 128; S-P double buffer at
-//   256 + 128 * (t & 1) (+ 64 for row tile 1).
+//   256 + 128 * (t & 1) (+ 64 for row tile 1).  The row warps also take
+//   |v|^2 of every key for pass 2.
 // pass 2, per 64-key tile:  S = Q K^T and G = a V^T (a as bf16 hi + lo held
-//   in tensor memory); the next tile's MMAs run while each thread turns its
-//   row of S and G into residual terms; the 256 rows are summed per key by a
-//   warp butterfly and shared memory, and the CTA writes the final scores.
+//   in tensor memory); each thread copies its row of S and G to registers,
+//   which frees the buffer for the next tile's MMAs, and turns them into
+//   residual terms (32 keys at a time through one copy of the code); each warp sums its 32 rows per key
+//   by a butterfly, and the producer adds the 8 warp sums in a fixed order
+//   when the tile's stage is recycled and writes the final scores.  While
+//   every weight of a warp's rows is below 2^-7, p / (1 - p) is the series
+//   p (1 + p (1 + p)) instead of a reciprocal.
 //   Tensor-memory columns: a hi 0 / 64, a lo 128 / 192, S 256 / 320,
-//   G 384 / 448.
-// K/V tiles arrive by 16-byte cp.async into a three-stage ring, each chunk
-// placed at its swizzled position.
+//   G 384 / 448 (row tile 0 / 1).  (MMAs of 32 keys, which would let two
+//   buffers fit, re-read Q from shared memory for half the keys and ran
+//   at a fraction of the rate.)
+// K/V rows arrive by TMA gathers (four pool rows per copy, 128-byte swizzle
+// applied by the copy engine) into a four-stage ring.
 // ---------------------------------------------------------------------------
 constexpr int kTcKeys = 64;
-constexpr int kTcStages = 3;
+constexpr int kTcStages = 4;
 constexpr int kTcRows = 256;
 constexpr int kTcHalf = kTcKeys * 128;                 // one d half of a K or V tile (8 KB)
 constexpr int kTcKV = 4 * kTcHalf;                     // K (2 halves) then V (2 halves)
@@ -521,6 +531,13 @@ __device__ __forceinline__ float hw_sqrt(float x) {
   asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
+// sqrt(x) for finite x >= 0 as x * rsqrt(x): one special-function operation
+// (rsqrt.approx.ftz, relative error about 2^-22), 0 at 0
+__device__ __forceinline__ float hw_sqrt_fin(float x) {
+  float y;
+  asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return x > 0.f ? x * y : 0.f;
+}
 
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
   const uint32_t a = smem_u32(p);
@@ -543,20 +560,14 @@ __device__ __forceinline__ void tc_issue_s(uint32_t dS, const unsigned char* sq,
 }
 
 // Warp roles of the tcgen05 passes: warps 0-7 own one window row per thread,
-// warp 8 produces (Q, then K/V tiles into the stage ring by 16-byte cp.async
-// at the swizzled positions, each lane's copies completing on the stage's
-// full barrier), warp 9 lane 0 issues the MMAs.  Hand-offs are mbarriers;
-// the row warps synchronise among themselves on named barrier 1.
+// warp 8 produces (Q, then K/V tiles into the stage ring by TMA row gathers),
+// warp 9 lane 0 issues the MMAs.  Hand-offs are mbarriers only.
 constexpr int kWsRowThreads = 256;
 constexpr int kWsThreads = kWsRowThreads + 64;
 constexpr int kWsProducer = 8, kWsIssuer = 9;
 
 __device__ __forceinline__ void cp_async16_zf(void* dst, const void* src, bool ok) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async4_zf(void* dst, const void* src, bool ok) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 4 : 0)
                : "memory");
 }
 // one arrival on the barrier once this thread's earlier cp.async copies land
@@ -566,17 +577,60 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
 __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-__device__ __forceinline__ void rows_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
-
 struct WsBars {
   uint64_t qfull;
   uint64_t full[kTcStages], empty[kTcStages];
   uint64_t x_full[2], x_free[2], pv_done[2];
 };
 
-// Producer warp: Q rows (8 per lane), then tile t's keys 2 lane and 2 lane + 1.
-__device__ __forceinline__ void ws_produce(const D3Args& A, int l, int j_begin, int j_end, int ntiles,
-                                           unsigned char* sq, unsigned char* skv, int (*pos)[kTcKeys], WsBars& bar) {
+// The K and V pool tensor maps of one layer (see kTmapsPerLayer).
+struct D3Maps {
+  CUtensorMap m[kTmapsPerLayer];   // K gather, V gather, K 16 rows, V 16 rows, K 64 rows, V 64 rows
+};
+
+// One tiled TMA copy: rows y .. y + box - 1 of the 64-element half row at
+// column x into consecutive 128-byte rows at dst (128-byte swizzle), the box
+// bytes completing on bar.
+__device__ __forceinline__ void tma_rows(void* dst, const CUtensorMap* map, int x, int y, uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];" ::"r"(
+          smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// One TMA gather: the 64-element half rows at column x of four pool rows
+// (slots r0..r3) into four consecutive 128-byte rows at dst, swizzled by
+// their shared-memory address (the UMMA 128-byte K-major layout when dst
+// lies in a 1024-byte aligned tile); 512 bytes complete on bar.  A row past
+// the pool reads as zeros.
+__device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, int x, int r0, int r1, int r2, int r3,
+                                            uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Producer warp.  Q rows first (8 per lane, 16-byte cp.async, once); then per
+// tile the K and V rows of its 64 keys by TMA, after the keys' positions
+// (and in pass 2 their |v|^2), loaded one tile ahead, are stored to the
+// stage and lane 0 has armed the stage's full barrier with the tile's bytes.
+// A tile whose 64 slots are consecutive (the layout a prefill leaves) takes
+// one 64-row copy per tensor and row half; otherwise each group of 16 keys
+// in consecutive slots takes a 16-row copy, and the other keys are gathered
+// four rows per copy (lanes 0-15, four keys each; a key past the chunk
+// gathers a row past the pool, which reads as zeros).  A TMA instruction
+// costs tens of nanoseconds to issue, so the fewer the better.
+// In pass 2 it also retires each tile's column sums: once the tile's stage
+// is empty (its MMAs and the 8 row warps are done with it), the 8 warps'
+// partial sums are added in warp order and stored.
+template <bool kPass2>
+__device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, int l,
+                                           int j_begin, int j_end, int ntiles, unsigned char* sq, unsigned char* skv,
+                                           int (*pos)[kTcKeys], float (*vn)[kTcKeys],
+                                           float (*col)[kWsRowThreads / 32][kTcKeys], WsBars& bar) {
   const int lane = threadIdx.x & 31;
   const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
 #pragma unroll 1
@@ -592,43 +646,103 @@ __device__ __forceinline__ void ws_produce(const D3Args& A, int l, int j_begin, 
   }
   cp_async_arrive(&bar.qfull);
   const size_t lo = static_cast<size_t>(l) * A.dm.cap;
-  const __nv_bfloat16* kpool = static_cast<const __nv_bfloat16*>(A.ls.k_pool);
-  const __nv_bfloat16* vpool = static_cast<const __nv_bfloat16*>(A.ls.v_pool);
   const int rows_max = A.dm.P * kBlock;
-  auto slot_of = [&](int t, int key) -> int {
+  auto fetch = [&](int t, int key, int& sl, int& ps, float& v) {
     const int j = j_begin + t * kTcKeys + key;
-    if (t >= ntiles || j >= j_end) return -1;
-    int sl = A.ls.slot[lo + j];
-    if (sl < 0 || sl >= rows_max) { set_status(A.ws.status, ST_BAD_INDEX); sl = 0; }
-    return sl;
+    sl = rows_max;
+    ps = 0x7FFFFFFF;
+    v = 0.f;
+    if (t >= ntiles || j >= j_end) return;
+    int s = A.ls.slot[lo + j];
+    if (s < 0 || s >= rows_max) { set_status(A.ws.status, ST_BAD_INDEX); s = 0; }
+    sl = s;
+    ps = A.ls.pos[lo + j];
+    if (kPass2) v = A.ws.d3_vn[lo + j];
   };
-  int s0 = slot_of(0, 2 * lane), s1 = slot_of(0, 2 * lane + 1);
-#pragma unroll 1
-  for (int t = 0; t < ntiles; ++t) {
-    const int st = t % kTcStages;
-    if (t >= kTcStages) (void)mbar_wait_bounded(&bar.empty[st], ((t / kTcStages) - 1) & 1, A.ws.status);
-    unsigned char* kb = skv + st * kTcKV;
-    unsigned char* vb = kb + 2 * kTcHalf;
+  auto retire = [&](int u) {
+    const int su = u % kTcStages;
 #pragma unroll
     for (int kk = 0; kk < 2; ++kk) {
       const int key = 2 * lane + kk;
-      const int sl = kk ? s1 : s0;
-      const bool ok = sl >= 0;
-      const __nv_bfloat16* ks = kpool + static_cast<size_t>(ok ? sl : 0) * kD;
-      const __nv_bfloat16* vs = vpool + static_cast<size_t>(ok ? sl : 0) * kD;
+      float tot = 0.f;
 #pragma unroll
-      for (int c = 0; c < 16; ++c) {
-        const int off = (c >> 3) * kTcHalf + key * 128 + (((c & 7) ^ (key & 7)) << 4);
-        cp_async16_zf(kb + off, ks + c * 8, ok);
-        cp_async16_zf(vb + off, vs + c * 8, ok);
-      }
-      cp_async4_zf(&pos[st][key], A.ls.pos + lo + (ok ? j_begin + t * kTcKeys + key : 0), ok);
+      for (int w8 = 0; w8 < kWsRowThreads / 32; ++w8) tot += col[su][w8][key];
+      const int j = j_begin + u * kTcKeys + key;
+      if (j < j_end) A.scores[lo + j] = tot;
     }
-    cp_async_arrive(&bar.full[st]);
-    s0 = slot_of(t + 1, 2 * lane);
-    s1 = slot_of(t + 1, 2 * lane + 1);
+  };
+  int s0, s1, p0, p1;
+  float v0, v1;
+  fetch(0, 2 * lane, s0, p0, v0);
+  fetch(0, 2 * lane + 1, s1, p1, v1);
+#pragma unroll 1
+  for (int t = 0; t < ntiles; ++t) {
+    const int st = t % kTcStages;
+    if (t >= kTcStages) {
+      (void)mbar_wait_bounded(&bar.empty[st], ((t / kTcStages) - 1) & 1, A.ws.status);
+      if (kPass2) retire(t - kTcStages);
+    }
+    pos[st][2 * lane] = p0;
+    pos[st][2 * lane + 1] = p1;
+    if (kPass2) {
+      vn[st][2 * lane] = v0;
+      vn[st][2 * lane + 1] = v1;
+    }
+    // lane g < 16 takes keys 4g .. 4g + 3, held by lanes 2g and 2g + 1
+    const int g0 = __shfl_sync(0xffffffffu, s0, (2 * lane) & 31);
+    const int g1 = __shfl_sync(0xffffffffu, s1, (2 * lane) & 31);
+    const int g2 = __shfl_sync(0xffffffffu, s0, (2 * lane + 1) & 31);
+    const int g3 = __shfl_sync(0xffffffffu, s1, (2 * lane + 1) & 31);
+    // consecutive slots: the whole tile (lane 0's key 0 first), and each
+    // 16-key group q (keys 16q.., held by lanes 8q .. 8q + 7)
+    const int tbase = __shfl_sync(0xffffffffu, s0, 0);
+    const bool tile_run = __all_sync(0xffffffffu, s0 == tbase + 2 * lane && s1 == tbase + 2 * lane + 1) &&
+                          tbase + kTcKeys <= rows_max;
+    const int qbase = __shfl_sync(0xffffffffu, s0, lane & ~7);
+    const unsigned qrun = __ballot_sync(0xffffffffu, s0 == qbase + 2 * (lane & 7) && s1 == qbase + 2 * (lane & 7) + 1);
+    const int grp = (lane >> 2) & 3;                                  // the group of lane g < 16
+    const int gbase = __shfl_sync(0xffffffffu, qbase, 8 * grp);
+    const bool grp_run = ((qrun >> (8 * grp)) & 0xFFu) == 0xFFu && gbase + 16 <= rows_max;
+    __syncwarp();
+    if (lane == 0) mbar_arrive_expect_tx(&bar.full[st], static_cast<uint32_t>(kTcKV));
+    __syncwarp();
+    unsigned char* kst = skv + st * kTcKV;
+    unsigned char* vst = kst + 2 * kTcHalf;
+    if (tile_run) {
+      if (lane == 0) {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_rows(kst + hf * kTcHalf, &mp.m[4], hf * 64, tbase, &bar.full[st]);
+          tma_rows(vst + hf * kTcHalf, &mp.m[5], hf * 64, tbase, &bar.full[st]);
+        }
+      }
+    } else if (lane < kTcKeys / 4) {
+      if (grp_run) {
+        if ((lane & 3) == 0) {
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            tma_rows(kst + hf * kTcHalf + grp * 2048, &mp.m[2], hf * 64, gbase, &bar.full[st]);
+            tma_rows(vst + hf * kTcHalf + grp * 2048, &mp.m[3], hf * 64, gbase, &bar.full[st]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int hf = 0; hf < 2; ++hf) {
+          tma_gather4(kst + hf * kTcHalf + lane * 512, &mp.m[0], hf * 64, g0, g1, g2, g3, &bar.full[st]);
+          tma_gather4(vst + hf * kTcHalf + lane * 512, &mp.m[1], hf * 64, g0, g1, g2, g3, &bar.full[st]);
+        }
+      }
+    }
+    fetch(t + 1, 2 * lane, s0, p0, v0);
+    fetch(t + 1, 2 * lane + 1, s1, p1, v1);
   }
-  asm volatile("cp.async.wait_all;" ::: "memory");
+  if (kPass2) {
+#pragma unroll 1
+    for (int u = ntiles > kTcStages ? ntiles - kTcStages : 0; u < ntiles; ++u) {
+      (void)mbar_wait_bounded(&bar.empty[u % kTcStages], (u / kTcStages) & 1, A.ws.status);
+      retire(u);
+    }
+  }
 }
 
 __device__ __forceinline__ void ws_init_bars(WsBars& bar, uint32_t full_count, uint32_t empty_count,
@@ -649,8 +763,10 @@ __device__ __forceinline__ void ws_init_bars(WsBars& bar, uint32_t full_count, u
 // pass 1.  Issue order S(0), then per tile S(t+1), P V(t): the tensor core
 // computes the next scores while the row warps exponentiate.  x_full[b]:
 // S(t) done (b = t & 1); x_free[b]: P(t) written by the 8 row warps;
-// pv_done[b]: P V(t) done; empty[s]: the stage's last reader (P V) done.
-__global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass1_kernel(D3Args A) {
+// pv_done[b]: P V(t) done; empty[s]: P V and the 8 row warps (which also
+// take |v|^2 of the tile's keys for pass 2) are done with the stage.
+__global__ void __launch_bounds__(kWsThreads, 1)
+    d3_tc_pass1_kernel(D3Args A, const __grid_constant__ D3Maps mp) {
   extern __shared__ unsigned char d3_dsm[];
   __shared__ int sh_pos[kTcStages][kTcKeys];
   __shared__ __align__(8) WsBars bar;
@@ -665,14 +781,14 @@ __global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass1_kernel(D3Args A) {
   unsigned char* skv = sq + kTcQ;
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == kWsIssuer) tc::alloc(&sh_taddr, kTcCols);
-  if (tid == 0) ws_init_bars(bar, 32, 1, kWsRowThreads / 32);
+  if (tid == 0) ws_init_bars(bar, 1, 1 + kWsRowThreads / 32, kWsRowThreads / 32);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tl = sh_taddr;
 
   if (warp == kWsProducer) {
-    ws_produce(A, l, j_begin, j_end, ntiles, sq, skv, sh_pos, bar);
+    ws_produce<false>(A, mp, l, j_begin, j_end, ntiles, sq, skv, sh_pos, nullptr, nullptr, bar);
   } else if (warp == kWsIssuer) {
     if ((tid & 31) == 0) {
       (void)mbar_wait_bounded(&bar.qfull, 0, A.ws.status);
@@ -723,13 +839,15 @@ __global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass1_kernel(D3Args A) {
       tc::fence_after();
       const uint32_t aS = tl + lane_off + 256 + buf * 128 + m * 64;
       float s[kTcKeys];
+      {
+        uint32_t v[4][16];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        uint32_t v[16];
-        tc::ld16(aS + q4 * 16, v);
+        for (int q4 = 0; q4 < 4; ++q4) tc::ld16(aS + q4 * 16, v[q4]);
         tc::wait_ld();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) s[q4 * 16 + k] = __uint_as_float(v[k]);
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) s[q4 * 16 + k] = __uint_as_float(v[q4][k]);
       }
       // a full tile whose last (largest) position precedes the row is wholly visible
       const bool all_vis = row_ok && (t + 1) * kTcKeys <= nkeys && sh_pos[st][kTcKeys - 1] <= qp;
@@ -798,6 +916,28 @@ __global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass1_kernel(D3Args A) {
       tc::fence_before();
       __syncwarp();
       if ((tid & 31) == 0) mbar_arrive1(&bar.x_free[buf]);
+      // |v|^2 of the tile's keys for pass 2: four threads per key, 32 elements each
+      {
+        const int key = tid >> 2, part = tid & 3;
+        const unsigned char* vst = skv + st * kTcKV + 2 * kTcHalf;
+        float acc = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          const uint4 x = *reinterpret_cast<const uint4*>(vst + sw_off(key, (part * 4 + c) * 8));
+          const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float2 f = __bfloat1622float2(pr[u]);
+            acc = fmaf(f.x, f.x, fmaf(f.y, f.y, acc));
+          }
+        }
+        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+        const int j = j_begin + t * kTcKeys + key;
+        if (part == 0 && j < j_end) A.ws.d3_vn[static_cast<size_t>(l) * A.dm.cap + j] = acc;
+      }
+      __syncwarp();
+      if ((tid & 31) == 0) mbar_arrive1(&bar.empty[st]);
     }
     (void)mbar_wait_bounded(&bar.pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, A.ws.status);
     tc::fence_after();
@@ -857,12 +997,17 @@ __device__ __noinline__ float residual_direct(float x, const float* arow, const 
 
 // pass 2.  x_full[0]: S(t) and G(t) done; x_free[0]: the 8 row warps have
 // read them (the buffer may be overwritten); empty[s]: the MMAs and the 8 row
-// warps are done with the stage.
-__global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass2_kernel(D3Args A) {
+// warps are done with the stage.  Each row warp leaves its 32 rows' sum per
+// key of the tile in col[stage][warp]; the producer adds the 8 when it
+// recycles the stage.
+constexpr float kSmallLog2 = -7.f;   // p < 2^-7: p / (1 - p) = p (1 + p (1 + p)) within 2^-21
+
+__global__ void __launch_bounds__(kWsThreads, 1)
+    d3_tc_pass2_kernel(D3Args A, const __grid_constant__ D3Maps mp) {
   extern __shared__ unsigned char d3_dsm[];
   __shared__ int sh_pos[kTcStages][kTcKeys];
-  __shared__ float sh_vn[kTcKeys];
-  __shared__ float sh_col[kWsRowThreads / 32][kTcKeys];
+  __shared__ float sh_vn[kTcStages][kTcKeys];
+  __shared__ float sh_col[kTcStages][kWsRowThreads / 32][kTcKeys];
   __shared__ __align__(8) WsBars bar;
   __shared__ uint32_t sh_taddr;
   const int chunk = blockIdx.x, l = blockIdx.y;
@@ -875,7 +1020,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass2_kernel(D3Args A) {
   unsigned char* skv = sq + kTcQ;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (warp == kWsIssuer) tc::alloc(&sh_taddr, kTcCols);
-  if (tid == 0) ws_init_bars(bar, 32, 1 + kWsRowThreads / 32, kWsRowThreads / 32);
+  if (tid == 0) ws_init_bars(bar, 1, 1 + kWsRowThreads / 32, kWsRowThreads / 32);
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
@@ -909,7 +1054,7 @@ __global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass2_kernel(D3Args A) {
   tc::fence_after();
 
   if (warp == kWsProducer) {
-    ws_produce(A, l, j_begin, j_end, ntiles, sq, skv, sh_pos, bar);
+    ws_produce<true>(A, mp, l, j_begin, j_end, ntiles, sq, skv, sh_pos, sh_vn, sh_col, bar);
   } else if (warp == kWsIssuer) {
     if (lane == 0) {
       (void)mbar_wait_bounded(&bar.qfull, 0, A.ws.status);
@@ -946,87 +1091,93 @@ __global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass2_kernel(D3Args A) {
       arow = A.a_out + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i) * kD;
     }
     const int nkeys = j_end - j_begin;
-    float* out = A.scores + static_cast<size_t>(l) * A.dm.cap;
 #pragma unroll 1
     for (int t = 0; t < ntiles; ++t) {
       const int st = t % kTcStages;
       const unsigned char* vst = skv + st * kTcKV + 2 * kTcHalf;
-      (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);
-      // |v|^2 of the tile's keys: four threads per key, 32 elements each
-      {
-        const int key = tid >> 2, part = tid & 3;
-        float acc = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 x = *reinterpret_cast<const uint4*>(vst + sw_off(key, (part * 4 + c) * 8));
-          const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 f = __bfloat1622float2(pr[u]);
-            acc = fmaf(f.x, f.x, fmaf(f.y, f.y, acc));
-          }
-        }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        if (part == 0) sh_vn[key] = acc;
-      }
-      rows_sync();
+      (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);   // positions, |v|^2, V
+      // S and G of the tile's 64 keys; once read, the next tile's MMAs may
+      // overwrite them
       (void)mbar_wait_bounded(&bar.x_full[0], t & 1, A.ws.status);
       tc::fence_after();
-      float sv[kTcKeys / 2][2], gv[kTcKeys / 2][2];   // [key within half][half]
-      uint32_t v[16], w[16];
+      float sv[kTcKeys], gv[kTcKeys];
+      {
+        uint32_t v[4][16], w[4][16];
 #pragma unroll
-      for (int q4 = 0; q4 < 4; ++q4) {
-        tc::ld16(tl + lane_off + 256 + m * 64 + q4 * 16, v);
-        tc::ld16(tl + lane_off + 384 + m * 64 + q4 * 16, w);
+        for (int q4 = 0; q4 < 4; ++q4) {
+          tc::ld16(tl + lane_off + 256 + m * 64 + q4 * 16, v[q4]);
+          tc::ld16(tl + lane_off + 384 + m * 64 + q4 * 16, w[q4]);
+        }
         tc::wait_ld();
 #pragma unroll
-        for (int k = 0; k < 16; ++k) {
-          const int key = q4 * 16 + k;
-          sv[key & 31][key >> 5] = __uint_as_float(v[k]);
-          gv[key & 31][key >> 5] = __uint_as_float(w[k]);
-        }
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            sv[q4 * 16 + k] = __uint_as_float(v[q4][k]);
+            gv[q4 * 16 + k] = __uint_as_float(w[q4][k]);
+          }
       }
       tc::fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive1(&bar.x_free[0]);   // the next tile's MMAs may overwrite S and G
-      int xk = -1;
-      float xx = 0.f;
-      // a full tile whose last (largest) position precedes the row is wholly visible
-      const bool all_vis = row_ok && (t + 1) * kTcKeys <= nkeys && sh_pos[st][kTcKeys - 1] <= qp;
-#pragma unroll
+      if (lane == 0) mbar_arrive1(&bar.x_free[0]);
+      // keys visible to the row: positions ascend within the tile, so they
+      // are a prefix (binary search of the row's query position)
+      int vis = 0;
+      if (row_ok) {
+        const int lim = min(kTcKeys, nkeys - t * kTcKeys);
+        if (lim > 0 && sh_pos[st][lim - 1] <= qp) {
+          vis = lim;
+        } else {
+          int lo = 0, hi = lim;   // first key with position > qp lies in [lo, hi)
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sh_pos[st][mid] <= qp) lo = mid + 1; else hi = mid;
+          }
+          vis = lo;
+        }
+      }
+      // the two halves go through one copy of the code (the row loop is long
+      // and instruction fetch stalls when it is duplicated); after the first,
+      // the second half's registers move down
+#pragma unroll 1
       for (int hf = 0; hf < 2; ++hf) {
-        float term[kTcKeys / 2];
-        if (all_vis) {
+        const int kv = vis - hf * 32;   // visible keys of this half: k2 < kv
+        // weights p = 2^x of the half's keys in place of S (x = -inf, p = 0
+        // where not visible), and the largest x
+        float xmax = -INFINITY;
+#pragma unroll
+        for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
+          const float x = k2 < kv ? fmaf(sv[k2], A.scale2, -lse2) : -INFINITY;
+          xmax = fmaxf(xmax, x);
+          sv[k2] = hw_exp2(x);
+        }
+        if (!__any_sync(0xffffffffu, xmax >= kSmallLog2)) {
+          // every weight of the warp's rows is small: no reciprocal (r2 is
+          // finite, so a key that is not visible, p = 0, gives 0)
 #pragma unroll
           for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
-            const int k = hf * 32 + k2;
-            const float x = fmaf(sv[k2][hf], A.scale2, -lse2);
-            const float p = hw_exp2(x);
-            const float r2 = fmaxf(0.f, fmaf(-2.f, gv[k2][hf], an + sh_vn[k]));
-            float tm = p * hw_rcp(1.f - p) * hw_sqrt(r2);
-            if (p > 0.5f) { xk = k; xx = x; tm = 0.f; }
-            term[k2] = tm;
+            const float p = sv[k2];
+            const float r2 = fmaxf(0.f, fmaf(-2.f, gv[k2], an + sh_vn[st][hf * 32 + k2]));
+            sv[k2] = p * fmaf(p, 1.f + p, 1.f) * hw_sqrt_fin(r2);
           }
         } else {
+          int xk = -1;
 #pragma unroll
           for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
-            const int k = hf * 32 + k2;
-            const bool ok = row_ok && t * kTcKeys + k < nkeys && sh_pos[st][k] <= qp;
-            const float x = fmaf(sv[k2][hf], A.scale2, -lse2);
-            const float p = ok ? hw_exp2(x) : 0.f;
-            const float r2 = fmaxf(0.f, fmaf(-2.f, gv[k2][hf], an + sh_vn[k]));
+            const float p = sv[k2];
+            const float r2 = fmaxf(0.f, fmaf(-2.f, gv[k2], an + sh_vn[st][hf * 32 + k2]));
             float tm = p * hw_rcp(1.f - p) * hw_sqrt(r2);
-            if (p > 0.5f) { xk = k; xx = x; tm = 0.f; }
-            term[k2] = p > 0.f ? tm : 0.f;
+            if (p > 0.5f) { xk = k2; tm = 0.f; }
+            sv[k2] = p > 0.f ? tm : 0.f;
           }
-        }
-        // the one key of the row with p > 1/2: direct distance, out of line
-        if (xk >= hf * 32 && xk < hf * 32 + 32) {
-          const float dterm = residual_direct(xx, arow, vst, xk);
+          // the one key of the row with p > 1/2 (the largest x): direct
+          // distance, out of line
+          if (xk >= 0) {
+            const float dterm = residual_direct(xmax, arow, vst, hf * 32 + xk);
 #pragma unroll
-          for (int k2 = 0; k2 < kTcKeys / 2; ++k2)
-            if (hf * 32 + k2 == xk) term[k2] = dterm;
+            for (int k2 = 0; k2 < kTcKeys / 2; ++k2)
+              if (k2 == xk) sv[k2] = dterm;
+          }
         }
         // butterfly: each lane ends with the warp's sum of one key
 #pragma unroll
@@ -1034,23 +1185,20 @@ __global__ void __launch_bounds__(kWsThreads, 1) d3_tc_pass2_kernel(D3Args A) {
           const bool up = (lane & o) != 0;
 #pragma unroll
           for (int i = 0; i < cnt / 2; ++i) {
-            const float send = up ? term[i] : term[cnt / 2 + i];
-            const float keep = up ? term[cnt / 2 + i] : term[i];
-            term[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            const float send = up ? sv[i] : sv[cnt / 2 + i];
+            const float keep = up ? sv[cnt / 2 + i] : sv[i];
+            sv[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
           }
         }
-        sh_col[warp][hf * 32 + lane] = term[0];
+        sh_col[st][warp][hf * 32 + lane] = sv[0];
+#pragma unroll
+        for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
+          sv[k2] = sv[kTcKeys / 2 + k2];
+          gv[k2] = gv[kTcKeys / 2 + k2];
+        }
       }
       __syncwarp();
       if (lane == 0) mbar_arrive1(&bar.empty[st]);    // this warp is done with the stage
-      rows_sync();
-      if (tid < kTcKeys) {
-        const int j = j_begin + t * kTcKeys + tid;
-        float tot = 0.f;
-#pragma unroll
-        for (int w8 = 0; w8 < kWsRowThreads / 32; ++w8) tot += sh_col[w8][tid];
-        if (j < j_end) out[j] = tot;
-      }
     }
   }
   tc::fence_before();
@@ -1069,6 +1217,37 @@ cudaError_t prepare_dropkv() {
   return e;
 }
 int d3_chunks(const Dims& dm, int) { return (dm.cap + kChunk - 1) / kChunk; }
+
+cudaError_t prepare_tensor_maps(Ctx& ctx) {
+  const Dims& dm = ctx.dims;
+  if (!(dm.max_window > 0 && dm.dtype == KVEVICT_BF16 && dm.d == kD)) return cudaSuccess;
+  void* fn = nullptr;
+  cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+  cudaError_t e = cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q);
+  if (e != cudaSuccess) return e;
+  if (q != cudaDriverEntryPointSuccess || !fn) return cudaErrorNotSupported;
+  const auto encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  ctx.tmaps = new (std::nothrow) CUtensorMap[kTmapsPerLayer * static_cast<size_t>(dm.L)];
+  if (!ctx.tmaps) return cudaErrorMemoryAllocation;
+  // [P * 16 rows][d] bf16, rows 2 d bytes apart; boxes of 64 elements (128
+  // bytes) by 1, 16 or 64 rows
+  const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(dm.P) * kBlock};
+  const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kD) * 2};
+  const cuuint32_t box_rows[3] = {1, 16, static_cast<cuuint32_t>(kTcKeys)};
+  const cuuint32_t estride[2] = {1, 1};
+  for (int layer = 0; layer < dm.L; ++layer) {
+    const LayerState ls = layer_state(ctx, layer);
+    for (int i = 0; i < kTmapsPerLayer; ++i) {
+      const cuuint32_t box[2] = {64, box_rows[i / 2]};
+      const CUresult r = encode(&ctx.tmaps[static_cast<size_t>(layer) * kTmapsPerLayer + i],
+                                CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, (i & 1) ? ls.v_pool : ls.k_pool, gdim, gstride,
+                                box, estride, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+      if (r != CUDA_SUCCESS) return cudaErrorInvalidValue;
+    }
+  }
+  return cudaSuccess;
+}
 
 cudaError_t launch_score(const Ctx& ctx, int layer, const void* q_win, int w, const int32_t* q_pos,
                          float* lse, float* a_out, float* scores, cudaStream_t stream) {
@@ -1089,9 +1268,12 @@ cudaError_t launch_score(const Ctx& ctx, int layer, const void* q_win, int w, co
     return cudaErrorInvalidValue;
   if (A.rows <= kTcRows) {
     const dim3 grid(A.chunks, dm.lanes);
-    d3_tc_pass1_kernel<<<grid, kWsThreads, kTcSmem, stream>>>(A);
+    if (!ctx.tmaps) return cudaErrorInvalidValue;
+    D3Maps mp;
+    for (int i = 0; i < kTmapsPerLayer; ++i) mp.m[i] = ctx.tmaps[static_cast<size_t>(layer) * kTmapsPerLayer + i];
+    d3_tc_pass1_kernel<<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
     d3_combine_kernel<<<dim3((A.rows + 7) / 8, dm.lanes), 256, 0, stream>>>(A);
-    d3_tc_pass2_kernel<<<grid, kWsThreads, kTcSmem, stream>>>(A);
+    d3_tc_pass2_kernel<<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
     return cudaGetLastError();
   }
   const int groups = (A.rows + kRowsPerCta - 1) / kRowsPerCta;

@@ -4,6 +4,7 @@
 #pragma once
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>           // CUtensorMap (the type only; encoding goes through the runtime's driver entry point)
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 
@@ -83,6 +84,7 @@ struct Workspace {
   __nv_bfloat16* d3_alo;           // [lanes][rows][d]
   float* d3_rowc;                  // [lanes][rows][2]  (lse2, |a|^2)
   float* d3_score_part;            // [2][lanes][cap]
+  float* d3_vn;                    // [lanes][cap]  |v|^2 of each kept key (scoring pass 1 -> pass 2)
 };
 
 struct Ctx {
@@ -99,6 +101,11 @@ struct Ctx {
   // programmatic dependent launch, so a launch that would touch that layer's
   // tables or its parity's scratch is not launched early.
   int last_layer;
+  // TMA tensor maps over each layer's K and V pool ([P * 16 rows][d], bf16,
+  // 128-byte swizzle, boxes of one 64-element half row x 1, 16 or 64 rows),
+  // kTmapsPerLayer per layer, for the window scoring's row copies; null when
+  // the configuration has no scoring window.
+  CUtensorMap* tmaps;
 };
 
 // workspace layout (host)
@@ -107,6 +114,10 @@ Dims make_dims(const kvevict_config& c);
 LayerState layer_state(const Ctx& ctx, int layer);
 int d3_chunks(const Dims& dm, int sm_count);
 int d3_rows_max(const Dims& dm);
+// tensor maps per layer: {K, V} x {1-row gather box, 16-row box, 64-row box}
+constexpr int kTmapsPerLayer = 6;
+// Encodes ctx.tmaps (host); cudaSuccess when the configuration needs none.
+cudaError_t prepare_tensor_maps(Ctx& ctx);
 
 // kernel launchers (host)
 cudaError_t launch_reset(const Ctx&, cudaStream_t);
