@@ -90,3 +90,49 @@ def test_score_select_compact_pipeline():
     np.testing.assert_array_equal(freed[:int(n_freed.item())].cpu().numpy(), np.array(cref["freed"], np.int32))
     assert int(n_moves.item()) == len(cref["moves"])
     compare_states(gpu_state(eng, 0), oracle_state(orc, 0), shp.policy, "after compaction")
+
+
+def test_window_scores_scattered_slots():
+    """The scores depend on each kept token's position and K/V rows, not on
+    where the rows sit in the pool.  After a prefill, each lane's slots are
+    permuted among themselves (K/V rows moved along): the first 128 tokens
+    keep consecutive slots (whole-tile copies), the next 256 keep in-order
+    16-token blocks in shuffled block order (16-row copies), the rest are
+    scattered token by token (four-row gathers), with ragged ends.  The
+    scores must equal the oracle's on the unpermuted tokens."""
+    shp = scaled("dropkv_prefill", ctx=3000, num_kv_heads=2, num_q_heads=8)
+    wl = Workload(shp)
+    eng, orc = make_pair(shp)
+    prefill_both(eng, orc, wl, 0)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(11)
+    n = shp.ctx
+    slots = eng.slots[0].cpu().numpy()
+    kp = eng.k_pool[0].reshape(-1, shp.head_dim).clone()
+    vp = eng.v_pool[0].reshape(-1, shp.head_dim).clone()
+    for l in range(eng.lanes):
+        old = slots[l, :n].copy()
+        order = np.arange(n)
+        blocks = np.arange(128, 384).reshape(16, 16)
+        order[128:384] = blocks[rng.permutation(16)].reshape(-1)
+        order[384:] = 384 + rng.permutation(n - 384)
+        new = old[order]                  # token i now lives where token order[i] lived
+        src = torch.as_tensor(old, dtype=torch.long, device="cuda")
+        dst = torch.as_tensor(new, dtype=torch.long, device="cuda")
+        kp[dst] = eng.k_pool[0].reshape(-1, shp.head_dim)[src]
+        vp[dst] = eng.v_pool[0].reshape(-1, shp.head_dim)[src]
+        slots[l, :n] = new
+    eng.k_pool[0].copy_(kp.reshape(eng.k_pool[0].shape))
+    eng.v_pool[0].copy_(vp.reshape(eng.v_pool[0].shape))
+    eng.slots[0].copy_(torch.as_tensor(slots))
+    torch.cuda.synchronize()
+    q, qp = wl.window(0)
+    lse, a, sc = eng.score(0, q.cuda(), qp.cuda())
+    ref = orc.score(0, q.double().numpy(), qp.numpy())
+    torch.cuda.synchronize()
+    assert_rows_close(lse.cpu().numpy()[..., None], ref["lse"][..., None], "lse")
+    assert_rows_close(a.cpu().numpy(), ref["a"], "window outputs")
+    for l in range(eng.lanes):
+        assert_scores_close(sc[l, :n].cpu().numpy(), ref["scores"][l], "lane %d scores" % l)
+    code, msg = eng.last_error()
+    assert code == 0, msg
