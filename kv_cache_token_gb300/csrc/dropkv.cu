@@ -25,7 +25,7 @@ namespace {
 constexpr int kD = 128;
 constexpr int kRowStride = kD * 2 + 16;         // bytes per staged row
 constexpr int kKeyTile = 32;                    // keys per tile
-constexpr int kChunk = 1024;                    // keys per CTA
+constexpr int kChunkMin = 1024;                 // keys per CTA, at least (the workspace holds cap / kChunkMin chunks)
 constexpr int kWarps = 8;                       // 8 x 16 = 128 rows per CTA
 constexpr int kRowsPerCta = kWarps * 16;
 constexpr int kMaxRowGroups = 4;
@@ -68,7 +68,7 @@ struct D3Args {
   Dims dm;
   const __nv_bfloat16* q;   // [B][Hq][w][d]
   const int32_t* qpos;      // [w]
-  int w, rows, rows_cap, chunks;
+  int w, rows, rows_cap, chunks, chunk_keys;   // chunk_keys: keys per CTA, a multiple of 64
   float* lse_out; float* a_out; float* scores;
   float scale2;
 };
@@ -166,9 +166,9 @@ __global__ void __launch_bounds__(kWarps * 32) d3_pass1_kernel(D3Args A) {
   __shared__ __align__(128) Tile tiles[2];
   const int chunk = blockIdx.x, l = blockIdx.y, rg = blockIdx.z;
   const int n = min(max(A.ls.count[l], 0), A.dm.cap);
-  const int j_begin = chunk * kChunk;
+  const int j_begin = chunk * A.chunk_keys;
   if (j_begin >= n) return;
-  const int j_end = min(n, j_begin + kChunk);
+  const int j_end = min(n, j_begin + A.chunk_keys);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
   const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
   const int r0 = rg * kRowsPerCta + warp * 16;
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(256) d3_combine_kernel(D3Args A) {
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (r >= A.rows) return;
   const int n = min(max(A.ls.count[l], 0), A.dm.cap);
-  const int nch = (n + kChunk - 1) / kChunk;
+  const int nch = (n + A.chunk_keys - 1) / A.chunk_keys;
   const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
   const size_t stride = kD + 2;
   const size_t chunk_stride = static_cast<size_t>(A.rows_cap) * stride;
@@ -296,24 +296,29 @@ __global__ void __launch_bounds__(256) d3_combine_kernel(D3Args A) {
   for (int c = lane; c < nch; c += 32) M = fmaxf(M, base[c * chunk_stride + kD]);
   M = warp_max(M);
   float Lp = 0.f;
-  for (int c = lane; c < nch; c += 32) {
-    const float m = base[c * chunk_stride + kD];
-    if (m != -INFINITY) Lp += base[c * chunk_stride + kD + 1] * exp2f(m - M);
+  float acc[4] = {0.f, 0.f, 0.f, 0.f};
+  // 32 chunks at a time: lane c holds chunk c's scale, broadcast by shuffle,
+  // so the partial rows' loads do not wait on one another
+  for (int c0 = 0; c0 < nch; c0 += 32) {
+    const int c = c0 + lane;
+    const float m = c < nch ? base[c * chunk_stride + kD] : -INFINITY;
+    const float sc_mine = m == -INFINITY ? 0.f : exp2f(m - M);
+    if (c < nch) Lp += base[c * chunk_stride + kD + 1] * sc_mine;
+    const int cnt = min(32, nch - c0);
+    const float* bc = base + static_cast<size_t>(c0) * chunk_stride + lane * 4;
+#pragma unroll 8
+    for (int u = 0; u < cnt; ++u) {
+      const float sc = __shfl_sync(0xffffffffu, sc_mine, u);
+      // partial rows are 130 floats: 8-byte aligned, so two float2 loads
+      const float2 x0 = *reinterpret_cast<const float2*>(bc + u * chunk_stride);
+      const float2 x1 = *reinterpret_cast<const float2*>(bc + u * chunk_stride + 2);
+      acc[0] = fmaf(x0.x, sc, acc[0]);
+      acc[1] = fmaf(x0.y, sc, acc[1]);
+      acc[2] = fmaf(x1.x, sc, acc[2]);
+      acc[3] = fmaf(x1.y, sc, acc[3]);
+    }
   }
   for (int o = 16; o > 0; o >>= 1) Lp += __shfl_xor_sync(0xffffffffu, Lp, o);
-  float acc[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-  for (int c = 0; c < nch; ++c) {
-    const float m = base[c * chunk_stride + kD];
-    const float sc = m == -INFINITY ? 0.f : exp2f(m - M);
-    // partial rows are 130 floats: 8-byte aligned, so two float2 loads
-    const float2 x0 = *reinterpret_cast<const float2*>(base + c * chunk_stride + lane * 4);
-    const float2 x1 = *reinterpret_cast<const float2*>(base + c * chunk_stride + lane * 4 + 2);
-    acc[0] = fmaf(x0.x, sc, acc[0]);
-    acc[1] = fmaf(x0.y, sc, acc[1]);
-    acc[2] = fmaf(x1.x, sc, acc[2]);
-    acc[3] = fmaf(x1.y, sc, acc[3]);
-  }
   const float lse2 = M + log2f(Lp);
   const size_t orow = (static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i;
   const size_t wrow = static_cast<size_t>(l) * A.rows_cap + r;
@@ -369,9 +374,9 @@ __global__ void __launch_bounds__(kWarps * 32) d3_pass2_kernel(D3Args A) {
   __shared__ float colsum[kWarps][kKeyTile];
   const int chunk = blockIdx.x, l = blockIdx.y, rg = blockIdx.z;
   const int n = min(max(A.ls.count[l], 0), A.dm.cap);
-  const int j_begin = chunk * kChunk;
+  const int j_begin = chunk * A.chunk_keys;
   if (j_begin >= n) return;
-  const int j_end = min(n, j_begin + kChunk);
+  const int j_end = min(n, j_begin + A.chunk_keys);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, cq = lane & 3;
   const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
   const int r0 = rg * kRowsPerCta + warp * 16;
@@ -512,7 +517,7 @@ constexpr uint32_t kTcCols = 512;
 constexpr float kTcRescale = 8.f;
 constexpr uint32_t kIdS = tc::idesc_bf16(128, kTcKeys, 0);
 constexpr uint32_t kIdPV = tc::idesc_bf16(128, kD, 1);
-static_assert(kChunk % kTcKeys == 0, "chunks hold whole tiles");
+static_assert(kChunkMin % kTcKeys == 0, "chunks hold whole tiles");
 
 // Hardware approximations (PTX ex2/rcp/sqrt .approx.ftz, relative error
 // about 2^-22; results below 2^-126 flush to zero).
@@ -773,9 +778,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   __shared__ uint32_t sh_taddr;
   const int chunk = blockIdx.x, l = blockIdx.y;
   const int n = min(max(A.ls.count[l], 0), A.dm.cap);
-  const int j_begin = chunk * kChunk;
+  const int j_begin = chunk * A.chunk_keys;
   if (j_begin >= n) return;
-  const int j_end = min(n, j_begin + kChunk);
+  const int j_end = min(n, j_begin + A.chunk_keys);
   const int ntiles = (j_end - j_begin + kTcKeys - 1) / kTcKeys;
   unsigned char* sq = align1024(d3_dsm);
   unsigned char* skv = sq + kTcQ;
@@ -1012,9 +1017,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   __shared__ uint32_t sh_taddr;
   const int chunk = blockIdx.x, l = blockIdx.y;
   const int n = min(max(A.ls.count[l], 0), A.dm.cap);
-  const int j_begin = chunk * kChunk;
+  const int j_begin = chunk * A.chunk_keys;
   if (j_begin >= n) return;
-  const int j_end = min(n, j_begin + kChunk);
+  const int j_end = min(n, j_begin + A.chunk_keys);
   const int ntiles = (j_end - j_begin + kTcKeys - 1) / kTcKeys;
   unsigned char* sq = align1024(d3_dsm);
   unsigned char* skv = sq + kTcQ;
@@ -1216,7 +1221,18 @@ cudaError_t prepare_dropkv() {
     e = cudaFuncSetAttribute(d3_tc_pass2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
   return e;
 }
-int d3_chunks(const Dims& dm, int) { return (dm.cap + kChunk - 1) / kChunk; }
+// Keys per CTA: each lane's keys split over floor(SMs / lanes) CTAs (one
+// wave when the lanes are few), in whole 64-key tiles, at least kChunkMin.
+// sm_count 0 gives the most chunks any device can use (workspace sizing).
+static int d3_chunk_keys(const Dims& dm, int sm_count) {
+  const int per_lane = sm_count > 0 ? max(1, sm_count / max(1, dm.lanes)) : 1 << 30;
+  const int k = (dm.cap + per_lane - 1) / per_lane;
+  return max(kChunkMin, (k + kTcKeys - 1) / kTcKeys * kTcKeys);
+}
+int d3_chunks(const Dims& dm, int sm_count) {
+  const int ck = d3_chunk_keys(dm, sm_count);
+  return (dm.cap + ck - 1) / ck;
+}
 
 cudaError_t prepare_tensor_maps(Ctx& ctx) {
   const Dims& dm = ctx.dims;
@@ -1261,6 +1277,7 @@ cudaError_t launch_score(const Ctx& ctx, int layer, const void* q_win, int w, co
   A.w = w;
   A.rows = dm.g * w;
   A.rows_cap = d3_rows_max(dm);
+  A.chunk_keys = d3_chunk_keys(dm, ctx.sm_count);
   A.chunks = d3_chunks(dm, ctx.sm_count);
   A.lse_out = lse; A.a_out = a_out; A.scores = scores;
   A.scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(dm.d));
