@@ -536,12 +536,10 @@ __device__ __forceinline__ float hw_sqrt(float x) {
   asm("sqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-// sqrt(x) for finite x >= 0 as x * rsqrt(x): one special-function operation
-// (rsqrt.approx.ftz, relative error about 2^-22), 0 at 0
-__device__ __forceinline__ float hw_sqrt_fin(float x) {
+__device__ __forceinline__ float hw_rsqrt(float x) {
   float y;
   asm("rsqrt.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
-  return x > 0.f ? x * y : 0.f;
+  return y;
 }
 
 __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
@@ -856,21 +854,21 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       }
       // a full tile whose last (largest) position precedes the row is wholly visible
       const bool all_vis = row_ok && (t + 1) * kTcKeys <= nkeys && sh_pos[st][kTcKeys - 1] <= qp;
+      // the largest raw score of the tile (scale2 > 0 keeps the order; the
+      // scale is applied once, and inside the exponent's FMA below)
       float tmax = -INFINITY;
       if (all_vis) {
 #pragma unroll
-        for (int k = 0; k < kTcKeys; ++k) {
-          s[k] *= A.scale2;
-          tmax = fmaxf(tmax, s[k]);
-        }
+        for (int k = 0; k < kTcKeys; ++k) tmax = fmaxf(tmax, s[k]);
       } else {
 #pragma unroll
         for (int k = 0; k < kTcKeys; ++k) {
           const bool ok = row_ok && t * kTcKeys + k < nkeys && sh_pos[st][k] <= qp;
-          s[k] = ok ? s[k] * A.scale2 : -INFINITY;
+          s[k] = ok ? s[k] : -INFINITY;
           tmax = fmaxf(tmax, s[k]);
         }
       }
+      tmax *= A.scale2;
       float factor = 1.f;
       if (tmax > m_run + kTcRescale) {
         factor = (m_run == -INFINITY) ? 0.f : exp2f(m_run - tmax);
@@ -892,12 +890,15 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           tc::st16(aO + q8 * 16, v);
         }
       }
+      // p = 2^(s scale2 - m); a masked key (s = -inf) gives 0, and so does
+      // every key while the row has seen none (m = -inf, offset taken as 0)
+      const float negm = m_run == -INFINITY ? 0.f : -m_run;
       float psum = 0.f;
       uint32_t hi[32], lo[32];
 #pragma unroll
       for (int k2 = 0; k2 < 32; ++k2) {
-        const float p0 = s[2 * k2] == -INFINITY ? 0.f : hw_exp2(s[2 * k2] - m_run);
-        const float p1 = s[2 * k2 + 1] == -INFINITY ? 0.f : hw_exp2(s[2 * k2 + 1] - m_run);
+        const float p0 = hw_exp2(fmaf(s[2 * k2], A.scale2, negm));
+        const float p1 = hw_exp2(fmaf(s[2 * k2 + 1], A.scale2, negm));
         psum += p0 + p1;
         split_bf16(p0, p1, hi[k2], lo[k2]);
       }
@@ -1005,13 +1006,14 @@ __device__ __noinline__ float residual_direct(float x, const float* arow, const 
 // warps are done with the stage.  Each row warp leaves its 32 rows' sum per
 // key of the tile in col[stage][warp]; the producer adds the 8 when it
 // recycles the stage.
-constexpr float kSmallLog2 = -7.f;   // p < 2^-7: p / (1 - p) = p (1 + p (1 + p)) within 2^-21
+constexpr float kSmallLog2 = -7.f;   // p < 2^-7: p / (1 - p) = p + p^2 + p^3 within 2^-21
+constexpr float kR2Floor = 1e-30f;   // r2 floor: sqrt(r2) = r2 rsqrt(r2) stays finite (1e-15 for r2 = 0)
 
 __global__ void __launch_bounds__(kWsThreads, 1)
     d3_tc_pass2_kernel(D3Args A, const __grid_constant__ D3Maps mp) {
   extern __shared__ unsigned char d3_dsm[];
   __shared__ int sh_pos[kTcStages][kTcKeys];
-  __shared__ float sh_vn[kTcStages][kTcKeys];
+  __shared__ __align__(16) float sh_vn[kTcStages][kTcKeys];
   __shared__ float sh_col[kTcStages][kWsRowThreads / 32][kTcKeys];
   __shared__ __align__(8) WsBars bar;
   __shared__ uint32_t sh_taddr;
@@ -1150,20 +1152,37 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         // weights p = 2^x of the half's keys in place of S (x = -inf, p = 0
         // where not visible), and the largest x
         float xmax = -INFINITY;
-#pragma unroll
-        for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
-          const float x = k2 < kv ? fmaf(sv[k2], A.scale2, -lse2) : -INFINITY;
-          xmax = fmaxf(xmax, x);
-          sv[k2] = hw_exp2(x);
-        }
-        if (!__any_sync(0xffffffffu, xmax >= kSmallLog2)) {
-          // every weight of the warp's rows is small: no reciprocal (r2 is
-          // finite, so a key that is not visible, p = 0, gives 0)
+        if (__all_sync(0xffffffffu, kv >= kTcKeys / 2)) {
 #pragma unroll
           for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
-            const float p = sv[k2];
-            const float r2 = fmaxf(0.f, fmaf(-2.f, gv[k2], an + sh_vn[st][hf * 32 + k2]));
-            sv[k2] = p * fmaf(p, 1.f + p, 1.f) * hw_sqrt_fin(r2);
+            const float x = fmaf(sv[k2], A.scale2, -lse2);
+            xmax = fmaxf(xmax, x);
+            sv[k2] = hw_exp2(x);
+          }
+        } else {
+#pragma unroll
+          for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
+            const float x = k2 < kv ? fmaf(sv[k2], A.scale2, -lse2) : -INFINITY;
+            xmax = fmaxf(xmax, x);
+            sv[k2] = hw_exp2(x);
+          }
+        }
+        if (!__any_sync(0xffffffffu, xmax >= kSmallLog2)) {
+          // every weight of the warp's rows is small: no reciprocal, and
+          // sqrt(r2) = r2 rsqrt(r2) (a key that is not visible has p = 0)
+          const float4* vn4 = reinterpret_cast<const float4*>(&sh_vn[st][hf * 32]);
+#pragma unroll
+          for (int k4 = 0; k4 < kTcKeys / 8; ++k4) {
+            const float4 vq = vn4[k4];
+            const float vv[4] = {vq.x, vq.y, vq.z, vq.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int k2 = k4 * 4 + u;
+              const float p = sv[k2];
+              const float r2 = fmaxf(kR2Floor, fmaf(-2.f, gv[k2], an + vv[u]));
+              const float q = fmaf(fmaf(p, p, p), p, p);   // p + p^2 + p^3
+              sv[k2] = q * r2 * hw_rsqrt(r2);
+            }
           }
         } else {
           int xk = -1;
