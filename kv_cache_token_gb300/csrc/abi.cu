@@ -70,6 +70,10 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base) {
   w.freed_flag = reinterpret_cast<int32_t*>(take(P * 4));
   w.blk_tag = reinterpret_cast<int32_t*>(take(P * 4));
   w.counters = reinterpret_cast<int32_t*>(take(64));
+  w.cmp_pos = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
+  w.cmp_slot = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
+  w.cmp_score = reinterpret_cast<float*>(take(lanes * cap * 4));
+  w.cmp_cnt = reinterpret_cast<int32_t*>(take(lanes * static_cast<size_t>(cmp_ctas_per_lane(dm) + 1) * 4));
   w.epi_done = reinterpret_cast<int32_t*>(take(4));
   if (dm.max_window > 0 && dm.dtype == KVEVICT_BF16 && dm.d == 128) {
     const size_t rows = static_cast<size_t>(d3_rows_max(dm));

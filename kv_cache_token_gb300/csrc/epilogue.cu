@@ -31,6 +31,7 @@ constexpr int kWorkUnit = 1 << kWorkShift;
 constexpr size_t kEpiDynSmem = (static_cast<size_t>(8) * kFastN + static_cast<size_t>(kPoSeg) * 8 * 128) * 4;
 static_assert(kEpiDynSmem >= static_cast<size_t>(128) * kMaxW * 4, "row buffer fits");
 constexpr int kApplyThreads = 512;
+constexpr int kCopyBatch = 8;   // relocation: 16-byte loads in flight per thread
 constexpr float kLn2 = 0.6931471805599453f;
 
 struct EpiArgs {
@@ -772,14 +773,23 @@ __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const 
       }
     }
     const int nd = __ldcg(ws.want_dst + l);
-    if (nd > 0) {
-      if (deferred) {
-        ws.want_dst[l] = 0;
-      } else {
-        const int beg = totA + ws.dst_begin[l];
-        ws.dst_begin[l] = beg;
-        for (int j = 0; j < nd; ++j) ls.owner[ws.alloc_ids[beg + j]] = l;
+    if (deferred) {
+      if (nd > 0) ws.want_dst[l] = 0;
+    } else {
+      ws.dst_begin[l] = totA + ws.dst_begin[l];
+    }
+  }
+  if (!deferred && totD > 0) {
+    // destination q belongs to the last lane whose first destination is at
+    // or before it (lanes without destinations share the next one's start)
+    __syncthreads();
+    for (int q = tid; q < totD; q += blockDim.x) {
+      int lo = 0, hi = dm.lanes;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldcg(ws.dst_begin + mid) <= totA + q) lo = mid + 1; else hi = mid;
       }
+      ls.owner[ws.alloc_ids[totA + q]] = lo - 1;
     }
   }
   if (tid == 0) {
@@ -877,16 +887,31 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(LayerState ls, Wor
         }
       }
       __syncthreads();
-      // the chunk's K and V rows, 16 bytes per thread (destinations are
-      // fresh blocks, never a source of the same plan)
-      for (int e = tid; e < tot * 2 * cpr; e += blockDim.x) {
-        const int mvi = e / (2 * cpr), rem = e - mvi * 2 * cpr;
-        const int so = sh_mv_src[mvi];
-        if (so < 0) continue;
-        unsigned char* base = rem < cpr ? kpb : vpb;
-        const size_t c16 = static_cast<size_t>(rem < cpr ? rem : rem - cpr) * 16;
-        *reinterpret_cast<uint4*>(base + static_cast<size_t>(sh_mv_dst[mvi]) * row_bytes + c16) =
-            *reinterpret_cast<const uint4*>(base + static_cast<size_t>(so) * row_bytes + c16);
+      // the chunk's K and V rows in 16-byte pieces, eight loads in flight per
+      // thread before their stores (destinations are fresh blocks, never a
+      // source of the same plan)
+      const int npieces = tot * 2 * cpr;
+      for (int e0 = tid; e0 < npieces; e0 += blockDim.x * kCopyBatch) {
+        uint4 v[kCopyBatch];
+        unsigned char* dst[kCopyBatch];
+#pragma unroll
+        for (int u = 0; u < kCopyBatch; ++u) {
+          const int e = e0 + u * static_cast<int>(blockDim.x);
+          dst[u] = nullptr;
+          if (e < npieces) {
+            const int mvi = e / (2 * cpr), rem = e - mvi * 2 * cpr;
+            const int so = sh_mv_src[mvi];
+            if (so >= 0) {
+              unsigned char* base = rem < cpr ? kpb : vpb;
+              const size_t c16 = static_cast<size_t>(rem < cpr ? rem : rem - cpr) * 16;
+              v[u] = *reinterpret_cast<const uint4*>(base + static_cast<size_t>(so) * row_bytes + c16);
+              dst[u] = base + static_cast<size_t>(sh_mv_dst[mvi]) * row_bytes + c16;
+            }
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kCopyBatch; ++u)
+          if (dst[u]) *reinterpret_cast<uint4*>(dst[u]) = v[u];
       }
       __syncthreads();
       q_total += tot;
@@ -953,6 +978,11 @@ cudaError_t prepare_epilogue() {
     e = cudaFuncSetAttribute(decode_epilogue_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              static_cast<int>(kEpiDynSmem));
   return e;
+}
+
+cudaError_t launch_allocate(const Ctx& ctx, int layer, cudaStream_t stream) {
+  allocate_kernel<<<1, 1024, 0, stream>>>(layer_state(ctx, layer), ctx.ws, ctx.dims);
+  return cudaGetLastError();
 }
 
 cudaError_t launch_allocate_apply(const Ctx& ctx, int layer, const void* k_new, const void* v_new,

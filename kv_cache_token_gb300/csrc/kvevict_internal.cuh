@@ -85,6 +85,10 @@ struct Workspace {
   float* d3_rowc;                  // [lanes][rows][2]  (lse2, |a|^2)
   float* d3_score_part;            // [2][lanes][cap]
   float* d3_vn;                    // [lanes][cap]  |v|^2 of each kept key (scoring pass 1 -> pass 2)
+  int32_t* cmp_pos;                // [lanes][cap]  forced compaction: survivors of each CTA's range,
+  int32_t* cmp_slot;               //               compacted at the range start
+  float* cmp_score;                // [lanes][cap]
+  int32_t* cmp_cnt;                // [lanes][cmp_ctas_per_lane + 1]  survivors per CTA, entries before
 };
 
 struct Ctx {
@@ -114,6 +118,10 @@ Dims make_dims(const kvevict_config& c);
 LayerState layer_state(const Ctx& ctx, int layer);
 int d3_chunks(const Dims& dm, int sm_count);
 int d3_rows_max(const Dims& dm);
+// CTAs per lane of the forced compaction's removal (each takes at most
+// kCmpPerCta table entries).
+constexpr int kCmpPerCta = 4096;
+inline int cmp_ctas_per_lane(const Dims& dm) { return (dm.cap + kCmpPerCta - 1) / kCmpPerCta; }
 // tensor maps per layer: {K, V} x {1-row gather box, 16-row box, 64-row box}
 constexpr int kTmapsPerLayer = 6;
 // Encodes ctx.tmaps (host); cudaSuccess when the configuration needs none.
@@ -144,6 +152,7 @@ cudaError_t launch_attend(const Ctx&, int layer, const void* q, const void* k_ne
 cudaError_t launch_epilogue(const Ctx&, int layer, bool has_q, int new_pos, const void* k_new,
                             const void* v_new, float* out, float* lse, int32_t* victims,
                             int32_t* n_victims, cudaStream_t);
+cudaError_t launch_allocate(const Ctx&, int layer, cudaStream_t);
 cudaError_t launch_allocate_apply(const Ctx&, int layer, const void* k_new, const void* v_new,
                                   bool mark_freed, int32_t* moves, cudaStream_t, bool with_allocate);
 

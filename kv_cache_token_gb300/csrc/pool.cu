@@ -367,18 +367,459 @@ __global__ void __launch_bounds__(kThreads) compact_evict_kernel(LayerState ls, 
   }
 }
 
+// Removal for tables without history rows, cmp_ctas_per_lane CTAs per lane
+// over contiguous ranges of the table (one wave at 128K instead of one CTA
+// per lane).  compact_remove_kernel: each CTA finds the slice of the
+// ascending victim list that can match its range (positions between its
+// first and last entry; extra positions match nothing, as in the oracle's
+// membership test), stages it in shared memory when it fits, tests each
+// entry by binary search, clears the victims' live bits and writes its
+// survivors, in order, to scratch at the range start, with their count.
+// compact_place_kernel: each CTA copies its survivors to their final index
+// (the counts of the lane's earlier CTAs before it; the lane's entry count
+// before the removal comes from scratch).
+constexpr int kCmpThreads = 512;
+constexpr int kCmpStage = 4096;     // victim-slice entries staged in shared memory
+
+// cmp_cnt per lane: cpl survivor counts, then the entry count before the
+// removal (-1 for a count out of range)
+
+// First index of the ascending a[0..k) whose value is >= x (strict: > x),
+// by one warp: 32 probes per round narrow the interval 32-fold, so a
+// search costs a few dependent loads instead of one per halving.
+template <bool kStrict>
+__device__ __forceinline__ int warp_lower_bound(const int32_t* a, int k, int x) {
+  const int lane = threadIdx.x & 31;
+  int lo = 0, hi = k;   // the answer lies in [lo, hi]
+  while (hi - lo > 32) {
+    const int step = (hi - lo + 31) / 32;
+    const int idx = lo + lane * step;
+    const int v = idx < hi ? a[idx] : 0x7FFFFFFF;
+    const bool ge = idx >= hi || (kStrict ? v > x : v >= x);
+    const unsigned bal = __ballot_sync(0xffffffffu, ge);
+    const int f = __ffs(bal) - 1;        // first probe at or past the answer (lane 31 at worst... or none)
+    if (bal == 0u) {
+      lo = lo + 31 * step + 1;
+    } else {
+      const int nhi = min(hi, lo + f * step);
+      lo = f == 0 ? lo : lo + (f - 1) * step + 1;
+      hi = nhi;
+    }
+  }
+  const int idx = lo + lane;
+  const bool ge = idx >= hi || (kStrict ? a[idx] > x : a[idx] >= x);
+  const unsigned bal = __ballot_sync(0xffffffffu, ge);
+  return bal ? lo + __ffs(bal) - 1 : hi;
+}
+
+__global__ void __launch_bounds__(kCmpThreads) compact_remove_kernel(LayerState ls, Workspace ws, Dims dm,
+                                                                    const int32_t* victims,
+                                                                    const int32_t* n_victims, int cpl) {
+  __shared__ int sh_vic[kCmpStage];
+  __shared__ int sh_scan[40];
+  __shared__ int sh_v0, sh_v1;
+  const int l = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  LaneRefs L = lane_refs(ls, dm, l);
+  const int n = ls.count[l];
+  const bool lane_ok = n >= 0 && n <= dm.cap;
+  if (c == 0 && tid == 0) ws.cmp_cnt[static_cast<size_t>(l) * (cpl + 1) + cpl] = lane_ok ? n : -1;
+  if (!lane_ok) return;
+  const int per = (n + cpl - 1) / cpl;
+  const int s = min(n, c * per), e = min(n, s + per);
+  const int k = max(0, min(n_victims[l], n));
+  const int32_t* vl = victims + static_cast<size_t>(l) * dm.cap;
+  // the victims between the range's first and last position: warp 0 finds
+  // the first >= the first position, warp 1 the first > the last
+  if (tid < 64) {
+    int v = 0;
+    if (s < e && k > 0) {
+      v = tid < 32 ? warp_lower_bound<false>(vl, k, L.pos[s]) : warp_lower_bound<true>(vl, k, L.pos[e - 1]);
+    }
+    if ((tid & 31) == 0) {
+      if (tid == 0) sh_v0 = v; else sh_v1 = v;
+    }
+  }
+  __syncthreads();
+  const int v0 = sh_v0, len = sh_v1 - sh_v0;
+  const bool staged = len <= kCmpStage;
+  if (staged)
+    for (int i = tid; i < len; i += blockDim.x) sh_vic[i] = vl[v0 + i];
+  __syncthreads();
+  const int* slice = staged ? sh_vic : vl + v0;
+  const size_t lo_off = static_cast<size_t>(l) * dm.cap;
+  int kept_total = 0, vict_total = 0;
+  for (int base = s; base < e; base += blockDim.x) {
+    const int i = base + tid;
+    int p = 0, sl = 0;
+    float sc = 0.f;
+    bool isv = false, keep = false;
+    if (i < e) {
+      p = L.pos[i];
+      sl = L.slot[i];
+      if (L.score) sc = L.score[i];
+      int lo = 0, hi = len;
+      while (lo < hi) { const int mid = (lo + hi) >> 1; if (slice[mid] < p) lo = mid + 1; else hi = mid; }
+      isv = lo < len && slice[lo] == p;
+      keep = !isv;
+    }
+    int tot2;
+    const int ex2 = block_excl_scan((keep ? 1 : 0) | (isv ? 0x10000 : 0), sh_scan, &tot2);
+    if (keep) {
+      const size_t o = lo_off + s + kept_total + (ex2 & 0xFFFF);
+      ws.cmp_pos[o] = p;
+      ws.cmp_slot[o] = sl;
+      ws.cmp_score[o] = sc;
+    }
+    if (isv) {
+      if (sl >= 0 && sl < dm.P * kBlock) {
+        atomicAnd(&L.mask[sl >> 4], ~(1 << (sl & 15)));
+      } else if (sl >= 0) {
+        set_status(ws.status, ST_BAD_INDEX);
+      }
+    }
+    kept_total += tot2 & 0xFFFF;
+    vict_total += tot2 >> 16;
+  }
+  if (tid == 0) {
+    ws.cmp_cnt[static_cast<size_t>(l) * (cpl + 1) + c] = kept_total;
+    if (vict_total) atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_VICTIMS]), (unsigned long long)vict_total);
+  }
+}
+
+__global__ void __launch_bounds__(kCmpThreads) compact_place_kernel(LayerState ls, Workspace ws, Dims dm, int cpl) {
+  __shared__ int sh_off;
+  const int l = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  LaneRefs L = lane_refs(ls, dm, l);
+  const int32_t* cnt = ws.cmp_cnt + static_cast<size_t>(l) * (cpl + 1);
+  const int n = cnt[cpl];
+  if (n < 0) {
+    if (c == 0 && tid == 0) { set_status(ws.status, ST_BAD_INDEX); ws.want_dst[l] = 0; ws.need_admit[l] = 0; }
+    return;
+  }
+  const int per = (n + cpl - 1) / cpl;
+  const int s = min(n, c * per);
+  if (tid < 32) {
+    int before = 0;
+    for (int j = tid; j < c; j += 32) before += cnt[j];
+    for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+    if (tid == 0) sh_off = before;
+  }
+  __syncthreads();
+  const int off = sh_off, mine = cnt[c];
+  const size_t lo_off = static_cast<size_t>(l) * dm.cap;
+  for (int j = tid; j < mine; j += blockDim.x) {
+    L.pos[off + j] = ws.cmp_pos[lo_off + s + j];
+    L.slot[off + j] = ws.cmp_slot[lo_off + s + j];
+    if (L.score) L.score[off + j] = ws.cmp_score[lo_off + s + j];
+  }
+}
+
+// One CTA per lane after the removal, kBlkPer consecutive entries of the
+// lane's block list per thread, all loads of a pass issued together: sets
+// the count, releases the blocks the removal emptied (every live bit was
+// cleared by the removal kernel), drops them from the list (stably), and
+// sizes the forced relocation plan from the remaining blocks' live counts
+// (vToken review, Sec. 3.3 Stage 1).
+constexpr int kBlkPer = 8;
+
+__global__ void __launch_bounds__(1024) compact_blocks_kernel(LayerState ls, Workspace ws, Dims dm, int cpl) {
+  __shared__ int sh_scan[40];
+  __shared__ int sh_m;
+  const int l = blockIdx.x, tid = threadIdx.x;
+  LaneRefs L = lane_refs(ls, dm, l);
+  const int32_t* cnt = ws.cmp_cnt + static_cast<size_t>(l) * (cpl + 1);
+  if (cnt[cpl] < 0) {
+    if (tid == 0) { set_status(ws.status, ST_BAD_INDEX); ws.want_dst[l] = 0; ws.need_admit[l] = 0; }
+    return;
+  }
+  if (tid < 32) {
+    int all = 0;
+    for (int j = tid; j < cpl; j += 32) all += cnt[j];
+    for (int o = 16; o > 0; o >>= 1) all += __shfl_xor_sync(0xffffffffu, all, o);
+    if (tid == 0) sh_m = all;
+  }
+  const int nb = *L.nblocks;
+  int out = 0, dead_tot = 0, src_tot = 0, tl_tot = 0;
+  for (int base = 0; base < nb; base += blockDim.x * kBlkPer) {
+    const int j0 = base + tid * kBlkPer;
+    int b[kBlkPer], mk[kBlkPer], ow[kBlkPer];
+#pragma unroll
+    for (int u = 0; u < kBlkPer; ++u) {
+      b[u] = j0 + u < nb ? L.blocks[j0 + u] : -1;
+      if (b[u] >= dm.P) b[u] = -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kBlkPer; ++u) {
+      mk[u] = b[u] >= 0 ? (__ldcg(L.mask + b[u]) & 0xFFFF) : 0;
+      ow[u] = b[u] >= 0 ? L.owner[b[u]] : -1;
+    }
+    int keep = 0, dead = 0, src = 0, tl = 0;
+#pragma unroll
+    for (int u = 0; u < kBlkPer; ++u) {
+      if (b[u] < 0) continue;
+      if (mk[u] == 0) {
+        if (ow[u] >= 0) {
+          L.owner[b[u]] = -1;
+          ws.freed_flag[b[u]] = 1;
+          ++dead;
+        }
+      } else if (ow[u] == l) {
+        ++keep;
+        const int c = __popc(mk[u]);
+        if (c < kBlock) { ++src; tl += c; }
+      }
+    }
+    int tot;
+    int ex = block_excl_scan(keep, sh_scan, &tot);
+    int tot2, tot3;
+    (void)block_excl_scan(dead | (src << 16), sh_scan, &tot2);
+    (void)block_excl_scan(tl, sh_scan, &tot3);
+    // every read of this pass precedes the scans' barriers; writes go below
+    // the next pass's entries
+#pragma unroll
+    for (int u = 0; u < kBlkPer; ++u)
+      if (b[u] >= 0 && mk[u] != 0 && ow[u] == l) L.blocks[out + ex++] = b[u];
+    out += tot;
+    dead_tot += tot2 & 0xFFFF;
+    src_tot += tot2 >> 16;
+    tl_tot += tot3;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    const int m = sh_m;
+    *L.nblocks = out;
+    ls.count[l] = m;
+    const int ndst = (tl_tot + kBlock - 1) / kBlock;
+    const int plan = (out > 0 && src_tot > ndst) ? ndst : 0;
+    ws.need_admit[l] = 0;
+    ws.want_dst[l] = plan;
+    ws.plan_tlive[l] = plan ? tl_tot : 0;
+    if (plan > 0) atomicOr(ws.work_flag, 1);
+    if (dead_tot)
+      atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_FREED_DEAD]), (unsigned long long)dead_tot);
+  }
+}
+
+// Relocation of the forced compaction (vToken review, Sec. 3.3 Stage 3),
+// cmp_ctas_per_lane CTAs per lane over contiguous ranges of the table.  A
+// token moves when its block holds between 1 and 15 live tokens (a source;
+// the live masks are final after the removal and untouched until
+// compact_reloc_finish_kernel); the q-th moving token of the lane in table
+// order goes to destination q / 16, offset q % 16.  count: sources per
+// range.  move: each CTA ranks its sources after the lane's earlier CTAs,
+// points their table slots at the destinations, writes the move tuples and
+// copies the K and V rows (eight 16-byte loads in flight per thread).
+// finish (one CTA per lane): releases the sources, sets the destinations'
+// masks, rebuilds the block list.
+__device__ __forceinline__ bool reloc_src(const LaneRefs& L, int old, int P) {
+  if (old < 0 || old >= P * kBlock) return false;
+  const int c = __popc(__ldcg(L.mask + (old >> 4)) & 0xFFFF);
+  return c > 0 && c < kBlock;
+}
+
+__global__ void __launch_bounds__(kCmpThreads) compact_reloc_count_kernel(LayerState ls, Workspace ws, Dims dm,
+                                                                         int cpl) {
+  __shared__ int sh_scan[40];
+  const int l = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  if (__ldcg(ws.counters + 1) == 0 || __ldcg(ws.want_dst + l) <= 0) return;
+  LaneRefs L = lane_refs(ls, dm, l);
+  const int m = min(max(__ldcg(ls.count + l), 0), dm.cap);
+  const int per = (m + cpl - 1) / cpl;
+  const int s = min(m, c * per), e = min(m, s + per);
+  int cnt = 0;
+  for (int i = s + tid; i < e; i += blockDim.x) cnt += reloc_src(L, L.slot[i], dm.P) ? 1 : 0;
+  int tot;
+  (void)block_excl_scan(cnt, sh_scan, &tot);
+  if (tid == 0) ws.cmp_cnt[static_cast<size_t>(l) * (cpl + 1) + c] = tot;
+}
+
+template <typename KT>
+__global__ void __launch_bounds__(kCmpThreads) compact_reloc_move_kernel(LayerState ls, Workspace ws, Dims dm,
+                                                                        int cpl, int32_t* moves) {
+  constexpr int kBatch = 8;
+  __shared__ int sh_scan[40];
+  __shared__ int sh_off;
+  __shared__ int sh_src[kCmpThreads], sh_dst[kCmpThreads];
+  const int l = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
+  const int ndst = __ldcg(ws.want_dst + l);
+  if (__ldcg(ws.counters + 1) == 0 || ndst <= 0) return;
+  LaneRefs L = lane_refs(ls, dm, l);
+  const int m = min(max(__ldcg(ls.count + l), 0), dm.cap);
+  const int per = (m + cpl - 1) / cpl;
+  const int s = min(m, c * per), e = min(m, s + per);
+  const int32_t* cnt = ws.cmp_cnt + static_cast<size_t>(l) * (cpl + 1);
+  if (tid < 32) {
+    int before = 0;
+    for (int j = tid; j < c; j += 32) before += cnt[j];
+    for (int o = 16; o > 0; o >>= 1) before += __shfl_xor_sync(0xffffffffu, before, o);
+    if (tid == 0) sh_off = before;
+  }
+  __syncthreads();
+  const int dbeg = ws.dst_begin[l], mbeg = ws.move_begin[l];
+  const int d = dm.d;
+  const int cpr = d * static_cast<int>(sizeof(KT)) / 16;     // 16-byte pieces per K or V row
+  const size_t row_bytes = static_cast<size_t>(d) * sizeof(KT);
+  unsigned char* kpb = static_cast<unsigned char*>(ls.k_pool);
+  unsigned char* vpb = static_cast<unsigned char*>(ls.v_pool);
+  int q_run = sh_off;
+  for (int base = s; base < e; base += blockDim.x) {
+    const int i = base + tid;
+    int old = -1;
+    bool src = false;
+    if (i < e) {
+      old = L.slot[i];
+      src = reloc_src(L, old, dm.P);
+    }
+    int tot;
+    const int ex = block_excl_scan(src ? 1 : 0, sh_scan, &tot);
+    if (src) {
+      const int q = q_run + ex;
+      if (q / kBlock >= ndst) {
+        set_status(ws.status, ST_BAD_INDEX);   // plan and tables disagree: leave the token in place
+        sh_src[ex] = -1;
+      } else {
+        const int db = ws.alloc_ids[dbeg + q / kBlock];
+        const int dof = q % kBlock;
+        const int ns = db * kBlock + dof;
+        sh_src[ex] = old;
+        sh_dst[ex] = ns;
+        L.slot[i] = ns;
+        if (moves) {
+          int32_t* mv = moves + static_cast<size_t>(mbeg + q) * 6;
+          mv[0] = l; mv[1] = L.pos[i]; mv[2] = old >> 4; mv[3] = old & 15; mv[4] = db; mv[5] = dof;
+        }
+      }
+    }
+    __syncthreads();
+    const int npieces = tot * 2 * cpr;
+    for (int e0 = tid; e0 < npieces; e0 += blockDim.x * kBatch) {
+      uint4 v[kBatch];
+      unsigned char* dst[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int pe = e0 + u * static_cast<int>(blockDim.x);
+        dst[u] = nullptr;
+        if (pe < npieces) {
+          const int mvi = pe / (2 * cpr), rem = pe - mvi * 2 * cpr;
+          const int so = sh_src[mvi];
+          if (so >= 0) {
+            unsigned char* pool = rem < cpr ? kpb : vpb;
+            const size_t c16 = static_cast<size_t>(rem < cpr ? rem : rem - cpr) * 16;
+            v[u] = *reinterpret_cast<const uint4*>(pool + static_cast<size_t>(so) * row_bytes + c16);
+            dst[u] = pool + static_cast<size_t>(sh_dst[mvi]) * row_bytes + c16;
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u)
+        if (dst[u]) *reinterpret_cast<uint4*>(dst[u]) = v[u];
+    }
+    __syncthreads();
+    q_run += tot;
+  }
+}
+
+__global__ void __launch_bounds__(1024) compact_reloc_finish_kernel(LayerState ls, Workspace ws, Dims dm, int cpl) {
+  __shared__ int sh_scan[40];
+  __shared__ int sh_moved;
+  const int l = blockIdx.x, tid = threadIdx.x;
+  const int ndst = __ldcg(ws.want_dst + l);
+  if (__ldcg(ws.counters + 1) == 0 || ndst <= 0) return;
+  LaneRefs L = lane_refs(ls, dm, l);
+  if (tid < 32) {
+    int all = 0;
+    for (int j = tid; j < cpl; j += 32) all += ws.cmp_cnt[static_cast<size_t>(l) * (cpl + 1) + j];
+    for (int o = 16; o > 0; o >>= 1) all += __shfl_xor_sync(0xffffffffu, all, o);
+    if (tid == 0) sh_moved = all;
+  }
+  const int dbeg = ws.dst_begin[l];
+  // sources (1 to 15 live tokens) are released; the full blocks stay, in order
+  const int nb = *L.nblocks;
+  int out = 0, nsrc_tot = 0;
+  for (int base = 0; base < nb; base += blockDim.x * kBlkPer) {
+    const int j0 = base + tid * kBlkPer;
+    int b[kBlkPer], c[kBlkPer], ow[kBlkPer];
+#pragma unroll
+    for (int u = 0; u < kBlkPer; ++u) {
+      b[u] = j0 + u < nb ? L.blocks[j0 + u] : -1;
+      if (b[u] >= dm.P) b[u] = -1;
+    }
+#pragma unroll
+    for (int u = 0; u < kBlkPer; ++u) {
+      c[u] = b[u] >= 0 ? __popc(L.mask[b[u]] & 0xFFFF) : 0;
+      ow[u] = b[u] >= 0 ? L.owner[b[u]] : -1;
+    }
+    int keep = 0, nsrc = 0;
+#pragma unroll
+    for (int u = 0; u < kBlkPer; ++u) {
+      if (b[u] < 0) continue;
+      if (c[u] > 0 && c[u] < kBlock) {
+        L.mask[b[u]] = 0;
+        L.owner[b[u]] = -1;
+        ws.freed_flag[b[u]] = 1;
+        ++nsrc;
+      } else if (c[u] > 0 && ow[u] == l) {
+        ++keep;
+      }
+    }
+    int tot, tot2;
+    int ex = block_excl_scan(keep, sh_scan, &tot);
+    (void)block_excl_scan(nsrc, sh_scan, &tot2);
+#pragma unroll
+    for (int u = 0; u < kBlkPer; ++u)
+      if (b[u] >= 0 && c[u] == kBlock && ow[u] == l) L.blocks[out + ex++] = b[u];
+    out += tot;
+    nsrc_tot += tot2;
+  }
+  __syncthreads();
+  const int moved = min(sh_moved, ndst * kBlock);
+  for (int j = tid; j < ndst; j += blockDim.x) {
+    const int db = ws.alloc_ids[dbeg + j];
+    const int filled = min(kBlock, moved - j * kBlock);
+    L.mask[db] = filled >= kBlock ? 0xFFFF : (filled > 0 ? (1 << filled) - 1 : 0);
+    L.blocks[out + j] = db;
+  }
+  if (tid == 0) {
+    *L.nblocks = out + ndst;
+    ws.want_dst[l] = 0;
+    atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_PLANS]), 1ull);
+    atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_MOVED]), (unsigned long long)sh_moved);
+    atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_FREED_RELOC]), (unsigned long long)nsrc_tot);
+  }
+}
+
+// The freed list: block ids with a set flag, ascending; each warp takes 512
+// consecutive flags per pass, 32 per coalesced load, and places its set
+// flags by ballot; one scan of the 32 warp counts per pass.  The flags are
+// cleared.
 __global__ void __launch_bounds__(1024) compact_finalize_kernel(Workspace ws, Dims dm, int32_t* freed,
                                                                int32_t* n_freed, int32_t* n_moves) {
   __shared__ int sh_scan[40];
+  constexpr int kPer = 16;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const unsigned lt = (1u << lane) - 1u;
   int total = 0;
-  for (int base = 0; base < dm.P; base += blockDim.x) {
-    const int blk = base + threadIdx.x;
-    const int f = (blk < dm.P && ws.freed_flag[blk]) ? 1 : 0;
+  for (int base = 0; base < dm.P; base += blockDim.x * kPer) {
+    const int wb = base + warp * 32 * kPer;
+    unsigned bal[kPer];
+    int wtot = 0;
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const int idx = wb + u * 32 + lane;
+      bal[u] = __ballot_sync(0xffffffffu, idx < dm.P && ws.freed_flag[idx] != 0);
+      wtot += __popc(bal[u]);
+    }
     int tot;
-    const int ex = block_excl_scan(f, sh_scan, &tot);
-    if (f) {
-      if (freed) freed[total + ex] = blk;
-      ws.freed_flag[blk] = 0;
+    const int wex = block_excl_scan(lane == 0 ? wtot : 0, sh_scan, &tot);
+    int off = total + __shfl_sync(0xffffffffu, wex, 0);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      if ((bal[u] >> lane) & 1u) {
+        const int idx = wb + u * 32 + lane;
+        if (freed) freed[off + __popc(bal[u] & lt)] = idx;
+        ws.freed_flag[idx] = 0;
+      }
+      off += __popc(bal[u]);
     }
     total += tot;
   }
@@ -455,9 +896,27 @@ cudaError_t launch_compact(const Ctx& ctx, int layer, const int32_t* victims, co
                            int32_t* freed, int32_t* n_freed, int32_t* moves, int32_t* n_moves,
                            cudaStream_t stream) {
   LayerState ls = layer_state(ctx, layer);
-  compact_evict_kernel<<<ctx.dims.lanes, kThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, victims, n_victims);
-  cudaError_t e = launch_allocate_apply(ctx, layer, nullptr, nullptr, true, moves, stream, true);
+  if (ls.ring) {
+    compact_evict_kernel<<<ctx.dims.lanes, kThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, victims, n_victims);
+  } else {
+    const int cpl = cmp_ctas_per_lane(ctx.dims);
+    const dim3 grid(cpl, ctx.dims.lanes);
+    compact_remove_kernel<<<grid, kCmpThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, victims, n_victims, cpl);
+    compact_place_kernel<<<grid, kCmpThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl);
+    compact_blocks_kernel<<<ctx.dims.lanes, 1024, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl);
+  }
+  cudaError_t e = launch_allocate(ctx, layer, stream);
   if (e != cudaSuccess) return e;
+  {
+    const int cpl = cmp_ctas_per_lane(ctx.dims);
+    const dim3 grid(cpl, ctx.dims.lanes);
+    compact_reloc_count_kernel<<<grid, kCmpThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl);
+    if (ctx.dims.dtype == KVEVICT_BF16)
+      compact_reloc_move_kernel<__nv_bfloat16><<<grid, kCmpThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl, moves);
+    else
+      compact_reloc_move_kernel<float><<<grid, kCmpThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl, moves);
+    compact_reloc_finish_kernel<<<ctx.dims.lanes, 1024, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl);
+  }
   compact_finalize_kernel<<<1, 1024, 0, stream>>>(ctx.ws, ctx.dims, freed, n_freed, n_moves);
   return cudaGetLastError();
 }
