@@ -66,6 +66,44 @@ struct AttendArgs {
 
 constexpr int kMaxLanesSmem = 1024;   // lanes per layer (validated at create)
 
+// The layer's T tiles are cut into one contiguous range per warp, skewed:
+// warp gw of W starts at floor(T (x + c x (1 - x))), x = gw / W (fp32, exact
+// at both ends), so early warps take more tiles than late ones.  Every warp issues its first
+// copy stages at launch, and the copy engine serves that burst roughly in
+// launch order: a warp of the last CTAs receives its first tile several
+// microseconds after one of the first CTAs, and with equal ranges finishes
+// that much later.  c is chosen so the skew is about kSkewTiles tiles between
+// the first and the last warp (the stages in flight at launch, times the
+// ratio of streaming to burst bandwidth, measured on the 70B-shaped layer),
+// and no smaller than a lane's split-K segment bound allows.  Consecutive
+// starts are at least two tiles apart, so the fp32 rounding (T 2^-23 at most)
+// cannot reorder them below 2^23 tiles per layer.
+constexpr int kSkewTiles = 2;
+
+struct Split {
+  int T, W;
+  float c, rW;
+  __device__ __forceinline__ int begin(int gw) const {
+    if (gw >= W) return T;
+    const float x = static_cast<float>(gw) * rW;
+    return min(T, __float2int_rd(static_cast<float>(T) * fmaf(c * x, 1.f - x, x)));
+  }
+  // the warp whose range holds tile t (the last warp starting at or before
+  // it): the quadratic inverted in fp32, then corrected against begin()
+  __device__ __forceinline__ int warp_of(int t) const {
+    const float y = static_cast<float>(t) / static_cast<float>(T);
+    float x = y;
+    if (c > 0.f) {
+      const float b = 1.f + c;
+      x = (b - sqrtf(fmaxf(0.f, b * b - 4.f * c * y))) / (2.f * c);
+    }
+    int g = min(W - 1, max(0, __float2int_rd(x * static_cast<float>(W))));
+    while (g + 1 < W && begin(g + 1) <= t) ++g;
+    while (g > 0 && begin(g) > t) --g;
+    return g;
+  }
+};
+
 // ---------------------------------------------------------------------------
 // bf16 tensor-core kernel
 //
@@ -102,7 +140,7 @@ __device__ __forceinline__ void mma_bf16a(float* c, const uint32_t* a, uint32_t 
 }
 
 template <int D, int NT>
-__device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_prefix, const int tp, const int gw,
+__device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_prefix, const Split& sp, const int gw,
                                             const int t_begin, const int t_end, unsigned char* wbuf,
                                             uint64_t* bars);
 
@@ -143,21 +181,33 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) attend_bf16_kernel(Atten
   int max_tiles = 0;
   for (int w = 0; w < kAttendWarps; ++w) max_tiles = max(max_tiles, sh_scan[w]);
   const int total = sh_prefix[lanes];
+  // warps in use: every warp's range must hold at least `need` tiles, so a
+  // lane spans at most kMaxSeg - 1 ranges (plus one for a partial start)
+  const int need = max(1, (max_tiles + kMaxSeg - 2) / (kMaxSeg - 1));
   const int warps_total = gridDim.x * kAttendWarps;
-  int tp = (total + warps_total - 1) / warps_total;
-  tp = max(tp, (max_tiles + kMaxSeg - 2) / (kMaxSeg - 1));
-  tp = max(tp, 1);
-  if (blockIdx.x == 0) {
+  Split sp;
+  sp.T = total;
+  sp.W = max(1, min(warps_total, total / (need + 1)));   // mean >= need + 1: fp32 rounding keeps ranges >= need
+  sp.rW = 1.f / static_cast<float>(sp.W);
+  {
+    // skew: about kSkewTiles tiles first to last, while the smallest range,
+    // mean (1 - c), keeps at least need + 1 tiles; c <= 1/2
+    const float mean = static_cast<float>(total) * sp.rW;
+    const float cmax = mean > static_cast<float>(need + 1) ? 1.f - static_cast<float>(need + 1) / mean : 0.f;
+    sp.c = fmaxf(0.f, fminf(fminf(static_cast<float>(kSkewTiles) / mean, cmax), 0.5f));
+  }
+  // the split-K segment count of each lane, by the CTA with the fewest tiles
+  if (blockIdx.x == gridDim.x - 1) {
     for (int l = tid; l < lanes; l += blockDim.x) {
-      int s = sh_prefix[l], e = sh_prefix[l + 1];
-      a.lane_nseg[l] = (e - 1) / tp - s / tp + 1;
+      const int s = sh_prefix[l], e = sh_prefix[l + 1];
+      a.lane_nseg[l] = sp.warp_of(e - 1) - sp.warp_of(s) + 1;
     }
   }
 
   const int gw = blockIdx.x * kAttendWarps + warp;
-  const int t_begin = gw * tp;
-  const int t_end = min(total, t_begin + tp);
-  if (t_begin < t_end) attend_warp<D, NT>(a, sh_prefix, tp, gw, t_begin, t_end, smem + warp * C::kWarpBytes,
+  const int t_begin = gw < sp.W ? sp.begin(gw) : total;
+  const int t_end = gw < sp.W ? sp.begin(gw + 1) : total;
+  if (t_begin < t_end) attend_warp<D, NT>(a, sh_prefix, sp, gw, t_begin, t_end, smem + warp * C::kWarpBytes,
                                           sh_bar[warp]);
   // the next kernel in the stream may start now; this grid completes only
   // after its predecessor did (so completion orders everything before it)
@@ -167,7 +217,7 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) attend_bf16_kernel(Atten
 
 // One warp's range of tiles [t_begin, t_end) (stream-K split of the layer).
 template <int D, int NT>
-__device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_prefix, const int tp, const int gw,
+__device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_prefix, const Split& sp, const int gw,
                                             const int t_begin, const int t_end, unsigned char* wbuf,
                                             uint64_t* bars) {
   using C = Bf16Cfg<D, NT>;
@@ -334,7 +384,7 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
         }
       }
       cur_lane = cons_lane;
-      seg = gw - sh_prefix[cur_lane] / tp;
+      seg = gw - sp.warp_of(sh_prefix[cur_lane]);
       cur_n = min(max(a.count[cur_lane], 0), a.cap - 1);
       reset_acc();
     }
