@@ -9,6 +9,10 @@ DropKV explainer:
   1 / (c (1 - eps)(1 - k eps)) times the best set's when the candidates have
   small weights and their residuals lie in one cone.
 * Worked example: weights (.5, .3, .15, .05), values (5, 5, 15, 5).
+* Decode variant (a reading: the explainer scores a window of queries; at
+  decode time the window is the current query of each head of the group,
+  and the per-step scores go through the SnapKV history ring, whose window
+  sums are the eviction keys).
 """
 import itertools
 
@@ -72,6 +76,23 @@ def window_scores(q_rows, q_pos, K, V, kpos, token_idx=None):
     for i in range(p.shape[0]):
         total += token_scores(p[i, idx], V[idx], a[i])
     return total, lse, a
+
+
+def decode_scores(p, A, V, n_kept):
+    """DropKV decode variant, one step of one KV head: for each kept token j,
+    the sum over the group's query heads h of || p_hj / (1 - p_hj) (a_h - v_j) ||.
+
+    p [g, n] are the step's weights over the kept tokens and the new token
+    (the new token last), A [g, d] the heads' outputs, V [n, d] the values;
+    returns [n_kept] (the new token is not scored).  +inf where 1 - p <= 0.
+    """
+    p = np.atleast_2d(np.asarray(p, dtype=np.float64))
+    A = np.atleast_2d(np.asarray(A, dtype=np.float64))
+    V = np.asarray(V, dtype=np.float64)
+    total = np.zeros(n_kept, dtype=np.float64)
+    for h in range(p.shape[0]):
+        total += token_scores(p[h, :n_kept], V[:n_kept], A[h])
+    return total
 
 
 def greedy_set(scores, k):

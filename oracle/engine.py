@@ -7,10 +7,12 @@ Algorithm 1, whose only policy-specific line is SelectVictims):
 1. attend: the g query heads of the group attend the kept tokens and the new
    token (the new token's K/V come with the call);
 2. score: H2O adds the group's weights to the kept tokens' cumulative
-   scores; SnapKV writes them into the history ring and advances it; a null
-   query is inert (SnapKV, "How it works");
-3. keys: H2O uses the scores, SnapKV the pooled window sums, over the kept
-   tokens plus the new token (score 0, zero history);
+   scores; SnapKV writes them into the history ring and advances it; DropKV
+   (decode variant) writes each kept token's residual-output score of this
+   step into the same kind of ring; a null query is inert (SnapKV, "How it
+   works");
+3. keys: H2O uses the scores, SnapKV and DropKV the pooled window sums, over
+   the kept tokens plus the new token (score 0, zero history);
 4. select: k = max(0, n + 1 - budget) victims among tokens older than the
    recent window, smallest (key, position) first, ascending output;
 5. evict: victims leave the token table, their slots die, empty blocks go
@@ -27,7 +29,7 @@ import numpy as np
 
 from . import h2o, snapkv
 from .attention import decode_attention
-from .dropkv import window_scores
+from .dropkv import decode_scores, window_scores
 from .paged import PagedLayer
 from .select import select_lane
 
@@ -43,7 +45,7 @@ class Engine:
         self.cfg = cfg
         self.g = cfg.num_q_heads // cfg.num_kv_heads
         self.n_lanes = cfg.batch * cfg.num_kv_heads
-        W = cfg.obs_window if cfg.policy == SNAPKV else 1
+        W = cfg.obs_window if cfg.policy in (SNAPKV, DROPKV) and cfg.obs_window >= 1 else 1
         wanted = range(cfg.num_layers) if layers is None else layers
         self.layers = {l: PagedLayer(self.n_lanes, cfg.blocks_per_pool, cfg.head_dim, W, store_kv)
                        for l in wanted}
@@ -62,7 +64,7 @@ class Engine:
     def lane_keys(self, L, n_new=1):
         """Eviction keys over the kept tokens followed by the new token."""
         c = self.cfg
-        if c.policy == SNAPKV:
+        if c.policy in (SNAPKV, DROPKV):
             hist = np.vstack([L.hist, np.zeros((n_new, L.hist.shape[1]), np.float32)])
             return snapkv.keys(hist, c.pool_kernel)
         return np.concatenate([L.score, np.zeros(n_new)])
@@ -95,6 +97,8 @@ class Engine:
                     L.score = h2o.accumulate(L.score, p)
                 elif c.policy == SNAPKV:
                     L.ring_slot = snapkv.ring_write(L.hist, L.ring_slot, h2o.group_weights(p)[:n])
+                elif c.policy == DROPKV:
+                    L.ring_slot = snapkv.ring_write(L.hist, L.ring_slot, decode_scores(p, o, Va, n))
             keys = self.lane_keys(L)
             pos_all = np.append(L.pos, np.int64(new_pos))
             vict = select_lane(keys, pos_all, c.budget, c.recent_window)

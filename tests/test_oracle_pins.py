@@ -11,7 +11,7 @@ import pytest
 import torch
 
 from oracle import attention, dropkv, h2o, paged, select, snapkv
-from oracle.engine import Engine, H2O, SNAPKV
+from oracle.engine import DROPKV, Engine, H2O, SNAPKV
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 
@@ -318,6 +318,64 @@ def test_window_scores_against_bruteforce_removal():
 def test_token_score_p_one_is_never_evicted():
     s = dropkv.token_scores(np.array([1.0, 0.0]), np.array([[1.0], [2.0]]))
     assert s[0] == np.inf and s[1] == 0.0
+
+
+def test_dropkv_decode_scores_equal_a_one_row_window():
+    """A decode step's DropKV scores are the window scores of a window that
+    holds just the current query of each head (every key visible), on the
+    kept tokens; the window scorer is pinned to brute-force removal above."""
+    rng = np.random.default_rng(12)
+    for g, n, d in ((4, 13, 8), (1, 5, 3), (8, 30, 16)):
+        q = 2.0 * rng.standard_normal((g, d))
+        K = rng.standard_normal((n + 1, d))
+        V = rng.standard_normal((n + 1, d))
+        o, _, p = attention.decode_attention(q, K, V)
+        got = dropkv.decode_scores(p, o, V, n)
+        ref, _, _ = dropkv.window_scores(q, np.full(g, n), K, V, np.arange(n + 1))
+        np.testing.assert_allclose(got, ref[:n], rtol=1e-12)
+
+
+def test_dropkv_decode_step_evicts_least_output_shift():
+    """With a one-step history (obsWindow 1, no pooling) a DropKV decode step
+    evicts, among the candidates, the tokens whose single removal (weights
+    renormalised, computed by brute force) moves the group's outputs least in
+    summed norm; the new token enters with an empty history."""
+    rng = np.random.default_rng(13)
+    d, g = 16, 4
+    E = Engine(_cfg(policy=DROPKV, budget=10, recent_window=3, obs_window=1, pool_kernel=1))
+    E.prefill(0, rng.standard_normal((1, 1, 12, d)), rng.standard_normal((1, 1, 12, d)))
+    for t in range(15):
+        L = E.layers[0].lanes[0]
+        Kk, Vk = E.layers[0].rows(0)
+        q = 2.0 * rng.standard_normal((1, g, d))
+        k = rng.standard_normal((1, 1, d))
+        v = rng.standard_normal((1, 1, d))
+        Ka, Va = np.vstack([Kk, k[0]]), np.vstack([Vk, v[0]])
+        _, _, p = attention.decode_attention(q[0], Ka, Va)
+        n = Kk.shape[0]
+        shift = [sum(np.linalg.norm(dropkv.removal_shift(p[h], Va, [j])) for h in range(g)) for j in range(n)]
+        keys = np.append(np.array(shift, np.float32).astype(np.float64), 0.0)
+        pos = np.append(L.pos, 12 + t)
+        expect = select.select_lane(keys, pos, 10, 3)
+        r = E.decode_step(0, q, k, v, 12 + t)
+        np.testing.assert_array_equal(r["victims"][0], expect)
+    E.layers[0].check_invariants()
+
+
+def test_dropkv_decode_null_query_is_inert():
+    rng = np.random.default_rng(14)
+    d = 16
+    E = Engine(_cfg(policy=DROPKV, budget=20, recent_window=3, obs_window=3, pool_kernel=1))
+    E.prefill(0, rng.standard_normal((1, 1, 12, d)), rng.standard_normal((1, 1, 12, d)))
+    E.decode_step(0, rng.standard_normal((1, 4, d)), rng.standard_normal((1, 1, d)),
+                  rng.standard_normal((1, 1, d)), 12)
+    L = E.layers[0].lanes[0]
+    hist, slot = L.hist.copy(), L.ring_slot
+    assert slot == 1 and np.all(hist[:12, 0] > 0)
+    E.decode_step(0, None, rng.standard_normal((1, 1, d)), rng.standard_normal((1, 1, d)), 13)
+    L = E.layers[0].lanes[0]
+    assert L.ring_slot == slot
+    np.testing.assert_array_equal(L.hist[:13], hist[:13])
 
 
 def test_greedy_within_bound_when_cone_holds():
