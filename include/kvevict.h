@@ -26,7 +26,8 @@
  *   slots           [L][B*Hkv][C]   int32
  *   counts          [L][B*Hkv]      int32, kept tokens per lane
  *   scores          [L][B*Hkv][C]   fp32, H2O cumulative scores
- *   ring            [L][B*Hkv][C][obs_window] fp32 (SnapKV only, else NULL)
+ *   ring            [L][B*Hkv][C][obs_window] fp32 (SnapKV, and DropKV with
+ *                   obs_window >= 1; else NULL)
  *   ring_slot       [L][B*Hkv]      int32
  *   block_owner     [L][P]          int32, owning lane or -1 when free
  *   block_mask      [L][P]          int32, bit o set = offset o holds a live token
@@ -106,7 +107,8 @@ typedef struct {
   int32_t max_tokens;      /* C: token-table capacity per lane */
   int32_t budget;          /* tokens kept per lane after each step */
   int32_t recent_window;   /* the newest recent_window positions are never evicted */
-  int32_t obs_window;      /* SnapKV history ring length (ignored otherwise) */
+  int32_t obs_window;      /* history ring length: SnapKV (>= 1), DropKV decode (0 = no
+                              decode steps), ignored for H2O */
   int32_t pool_kernel;     /* SnapKV max-pool width, odd; 1 disables pooling */
   float theta_f;           /* relocation trigger on the lane's waste ratio */
   int32_t max_window;      /* DropKV scoring: largest w passed to kvevict_score
@@ -185,10 +187,15 @@ kvevict_status kvevict_prefill(kvevict_ctx* ctx, int layer, const void* k_ctx, c
  *   score    H2O: score_j += sum over the group of p_hj for every kept j
  *            ("Formulating Cumulative Attention Scores"); SnapKV: the
  *            group's weights go into ring slot ring_slot, which then advances
- *            (SnapKV, "How it works");
- *   keys     H2O: the scores; SnapKV: max over kept neighbours i-r..i+r
- *            (r = (pool_kernel-1)/2, clamped) of the float64 window sums
- *            taken in slot order 0 upward; the new token has key 0;
+ *            (SnapKV, "How it works"); DropKV (decode variant, obs_window
+ *            >= 1): each kept token's residual-output score of this step,
+ *            sum over the group's heads h of p_hj / (1 - p_hj) * ||a_h - v_j||
+ *            with a_h the head's output (+inf where 1 - p_hj <= 0; DropKV
+ *            explainer, Lemma 1, with the window reduced to the current
+ *            query), goes into the ring the same way;
+ *   keys     H2O: the scores; SnapKV and DropKV: max over kept neighbours
+ *            i-r..i+r (r = (pool_kernel-1)/2, clamped) of the float64 window
+ *            sums taken in slot order 0 upward; the new token has key 0;
  *   select   k = max(0, counts+1 - budget) victims among tokens with
  *            position < new_pos - recent_window + 1, smallest (key,
  *            position) first (SnapKV, "Tie-breaking"); written ascending to
@@ -206,7 +213,8 @@ kvevict_status kvevict_prefill(kvevict_ctx* ctx, int layer, const void* k_ctx, c
  * q == NULL is inert for the scores and the ring (SnapKV, "How it works":
  * a null attention vector writes nothing and does not advance the ring);
  * out/lse are then not written; admission and eviction still run.
- * new_pos must exceed every kept position of every lane (ST_POSITION). */
+ * new_pos must exceed every kept position of every lane (ST_POSITION).
+ * DropKV without a ring (obs_window 0) is refused (KVEVICT_E_INVALID_ARG). */
 kvevict_status kvevict_decode_step(kvevict_ctx* ctx, int layer, const void* q, const void* k_new,
                                    const void* v_new, int32_t new_pos, float* out, float* lse,
                                    int32_t* victims, int32_t* n_victims, void* stream);

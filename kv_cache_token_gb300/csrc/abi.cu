@@ -15,6 +15,12 @@ inline size_t up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 inline size_t es_of(int dtype) { return dtype == KVEVICT_BF16 ? 2 : 4; }
 }  // namespace
 
+// A history ring per kept token: SnapKV always, DropKV (decode variant) when
+// obs_window >= 1.
+bool has_ring(const kvevict_config& c) {
+  return c.policy == KVEVICT_SNAPKV || (c.policy == KVEVICT_DROPKV && c.obs_window >= 1);
+}
+
 Dims make_dims(const kvevict_config& c) {
   Dims d;
   d.policy = c.policy;
@@ -28,7 +34,7 @@ Dims make_dims(const kvevict_config& c) {
   d.P = c.blocks_per_pool;
   d.cap = c.max_tokens;
   d.lanes = c.batch * c.num_kv_heads;
-  d.W = c.policy == KVEVICT_SNAPKV ? c.obs_window : 1;
+  d.W = has_ring(c) ? c.obs_window : 1;
   d.budget = c.budget;
   d.R = c.recent_window;
   d.pool_kernel = c.pool_kernel;
@@ -57,7 +63,7 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base) {
     w.part_ml_buf[c] = reinterpret_cast<float*>(take(lanes * kMaxSeg * g * 2 * 4));
     w.lane_nseg_buf[c] = reinterpret_cast<int32_t*>(take(lanes * 4));
   }
-  const bool snap = c.policy == KVEVICT_SNAPKV;
+  const bool snap = has_ring(c);
   w.keys64 = snap ? reinterpret_cast<double*>(take(lanes * cap * 8)) : nullptr;
   w.pooled64 = snap ? reinterpret_cast<double*>(take(lanes * cap * 8)) : nullptr;
   w.need_admit = reinterpret_cast<int32_t*>(take(lanes * 4));
@@ -73,6 +79,7 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base) {
   w.cmp_pos = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
   w.cmp_slot = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
   w.cmp_score = reinterpret_cast<float*>(take(lanes * cap * 4));
+  w.cmp_ring = has_ring(c) ? reinterpret_cast<float*>(take(lanes * cap * static_cast<size_t>(dm.W) * 4)) : nullptr;
   w.cmp_cnt = reinterpret_cast<int32_t*>(take(lanes * static_cast<size_t>(cmp_ctas_per_lane(dm) + 1) * 4));
   w.epi_done = reinterpret_cast<int32_t*>(take(4));
   if (dm.max_window > 0 && dm.dtype == KVEVICT_BF16 && dm.d == 128) {
@@ -105,7 +112,7 @@ LayerState layer_state(const Ctx& ctx, int layer) {
   s.slot = b.slots + L * lanes * cap;
   s.count = b.counts + L * lanes;
   s.score = b.scores + L * lanes * cap;
-  s.ring = (dm.policy == KVEVICT_SNAPKV && b.ring) ? b.ring + L * lanes * cap * dm.W : nullptr;
+  s.ring = (has_ring(ctx.cfg) && b.ring) ? b.ring + L * lanes * cap * dm.W : nullptr;
   s.ring_slot = b.ring_slot + L * lanes;
   s.owner = b.block_owner + L * P;
   s.mask = b.block_mask + L * P;
@@ -127,7 +134,7 @@ cudaError_t launch_reset(const Ctx& ctx, cudaStream_t st) {
   ms(b.slots, 0xFF, sz(KVEVICT_BUF_SLOTS));
   ms(b.counts, 0, sz(KVEVICT_BUF_COUNTS));
   ms(b.scores, 0, sz(KVEVICT_BUF_SCORES));
-  if (c.policy == KVEVICT_SNAPKV) ms(b.ring, 0, sz(KVEVICT_BUF_RING));
+  if (has_ring(c)) ms(b.ring, 0, sz(KVEVICT_BUF_RING));
   ms(b.ring_slot, 0, sz(KVEVICT_BUF_RING_SLOT));
   ms(b.block_owner, 0xFF, sz(KVEVICT_BUF_BLOCK_OWNER));
   ms(b.block_mask, 0, sz(KVEVICT_BUF_BLOCK_MASK));
@@ -170,6 +177,8 @@ kvevict_status kvevict_validate(const kvevict_config* c) {
     return KVEVICT_E_INVALID_ARG;
   if (c->policy == KVEVICT_SNAPKV && (c->obs_window < 1 || c->obs_window > kve::kMaxW ))
     return KVEVICT_E_INVALID_ARG;
+  if (c->policy == KVEVICT_DROPKV && (c->obs_window < 0 || c->obs_window > kve::kMaxW))
+    return KVEVICT_E_INVALID_ARG;
   // 16-token blocks are addressed with int32 slots
   if (static_cast<long long>(c->blocks_per_pool) * 16 >= (1ll << 31)) return KVEVICT_E_INVALID_ARG;
   return KVEVICT_OK;
@@ -191,7 +200,7 @@ size_t kvevict_buffer_size(const kvevict_config* c, int which) {
     case KVEVICT_BUF_RING_SLOT:
     case KVEVICT_BUF_LANE_NBLOCKS: return L * lanes * 4;
     case KVEVICT_BUF_RING:
-      return c->policy == KVEVICT_SNAPKV ? L * lanes * cap * static_cast<size_t>(c->obs_window) * 4 : 0;
+      return kve::has_ring(*c) ? L * lanes * cap * static_cast<size_t>(c->obs_window) * 4 : 0;
     case KVEVICT_BUF_BLOCK_OWNER:
     case KVEVICT_BUF_BLOCK_MASK: return L * P * 4;
     case KVEVICT_BUF_STATS: return L * KVEVICT_NSTATS * 8;
@@ -212,7 +221,7 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   if (!bufs || !bufs->k_pool || !bufs->v_pool || !bufs->positions || !bufs->slots || !bufs->counts ||
       !bufs->scores || !bufs->ring_slot || !bufs->block_owner || !bufs->block_mask || !bufs->lane_blocks ||
       !bufs->lane_nblocks || !bufs->stats || !bufs->workspace ||
-      (cfg->policy == KVEVICT_SNAPKV && !bufs->ring))
+      (kve::has_ring(*cfg) && !bufs->ring))
     return KVEVICT_E_INVALID_ARG;
   if (reinterpret_cast<uintptr_t>(bufs->workspace) % 256 != 0 || reinterpret_cast<uintptr_t>(bufs->k_pool) % 16 != 0 ||
       reinterpret_cast<uintptr_t>(bufs->v_pool) % 16 != 0)
@@ -266,7 +275,7 @@ kvevict_status kvevict_decode_step(kvevict_ctx* ctx, int layer, const void* q, c
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !k_new || !v_new || !victims || !n_victims || new_pos < 0)
     return KVEVICT_E_INVALID_ARG;
   if (q && (!out || !lse)) return KVEVICT_E_INVALID_ARG;
-  if (ctx->c.dims.policy == KVEVICT_DROPKV) return KVEVICT_E_INVALID_ARG;
+  if (ctx->c.dims.policy == KVEVICT_DROPKV && !kve::has_ring(ctx->c.cfg)) return KVEVICT_E_INVALID_ARG;
   const cudaError_t e = kve::launch_decode(ctx->c, layer, q, k_new, v_new, new_pos, out, lse, victims, n_victims,
                                            static_cast<cudaStream_t>(stream));
   ctx->c.last_layer = layer;
@@ -276,7 +285,7 @@ kvevict_status kvevict_decode_step(kvevict_ctx* ctx, int layer, const void* q, c
 kvevict_status kvevict_attend(kvevict_ctx* ctx, int layer, const void* q, const void* k_new, const void* v_new,
                               void* stream) {
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !k_new || !v_new) return KVEVICT_E_INVALID_ARG;
-  if (ctx->c.dims.policy == KVEVICT_DROPKV) return KVEVICT_E_INVALID_ARG;
+  if (ctx->c.dims.policy == KVEVICT_DROPKV && !kve::has_ring(ctx->c.cfg)) return KVEVICT_E_INVALID_ARG;
   if (!q) return KVEVICT_OK;
   const cudaError_t e = kve::launch_attend(ctx->c, layer, q, k_new, v_new, static_cast<cudaStream_t>(stream));
   ctx->c.last_layer = layer;
@@ -289,7 +298,7 @@ kvevict_status kvevict_finish_step(kvevict_ctx* ctx, int layer, const void* q, c
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !k_new || !v_new || !victims || !n_victims || new_pos < 0)
     return KVEVICT_E_INVALID_ARG;
   if (q && (!out || !lse)) return KVEVICT_E_INVALID_ARG;
-  if (ctx->c.dims.policy == KVEVICT_DROPKV) return KVEVICT_E_INVALID_ARG;
+  if (ctx->c.dims.policy == KVEVICT_DROPKV && !kve::has_ring(ctx->c.cfg)) return KVEVICT_E_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = kve::launch_epilogue(ctx->c, layer, q != nullptr, new_pos, k_new, v_new, out, lse, victims,
                                        n_victims, st);

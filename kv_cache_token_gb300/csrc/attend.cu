@@ -82,15 +82,18 @@ constexpr int kSkewTiles = 2;
 
 struct Split {
   int T, W;
+  int tp;          // > 0: equal ranges of tp tiles (small layers), no skew
   float c, rW;
   __device__ __forceinline__ int begin(int gw) const {
     if (gw >= W) return T;
+    if (tp > 0) return min(T, gw * tp);
     const float x = static_cast<float>(gw) * rW;
     return min(T, __float2int_rd(static_cast<float>(T) * fmaf(c * x, 1.f - x, x)));
   }
   // the warp whose range holds tile t (the last warp starting at or before
   // it): the quadratic inverted in fp32, then corrected against begin()
   __device__ __forceinline__ int warp_of(int t) const {
+    if (tp > 0) return min(W - 1, t / tp);
     const float y = static_cast<float>(t) / static_cast<float>(T);
     float x = y;
     if (c > 0.f) {
@@ -187,9 +190,19 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) attend_bf16_kernel(Atten
   const int warps_total = gridDim.x * kAttendWarps;
   Split sp;
   sp.T = total;
-  sp.W = max(1, min(warps_total, total / (need + 1)));   // mean >= need + 1: fp32 rounding keeps ranges >= need
-  sp.rW = 1.f / static_cast<float>(sp.W);
-  {
+  if (total < (need + 2) * warps_total) {
+    // a small layer: equal ranges of at least `need` tiles, integer
+    // boundaries, no skew
+    sp.tp = max(need, (total + warps_total - 1) / warps_total);
+    sp.W = (total + sp.tp - 1) / sp.tp;
+    sp.rW = 0.f;
+    sp.c = 0.f;
+  } else {
+    // every warp; the mean range is at least need + 2 tiles, so fp32
+    // rounding keeps every skewed range at or above need
+    sp.tp = 0;
+    sp.W = warps_total;
+    sp.rW = 1.f / static_cast<float>(sp.W);
     // skew: about kSkewTiles tiles first to last, while the smallest range,
     // mean (1 - c), keeps at least need + 1 tiles; c <= 1/2
     const float mean = static_cast<float>(total) * sp.rW;

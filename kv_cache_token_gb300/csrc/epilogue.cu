@@ -62,6 +62,52 @@ __device__ __forceinline__ float hw_exp2(float x) {
   return y;
 }
 
+// DropKV decode variant: this step's residual-output score of one kept
+// token, sum over the group's heads h of p / (1 - p) * ||a_h - v|| (DropKV
+// explainer, Lemma 1, with the window reduced to the current query of each
+// head).  a [g][d] are the heads' outputs (shared memory), v the token's V
+// row; the distance is taken directly in fp32 (no expansion, so no
+// cancellation when a_h is close to v), 1 - p from expm1 when p > 1/2, and
+// the term is +inf where 1 - p <= 0.  lg: the token's base-2 scaled logits,
+// one per head, lcap apart.  Out of line, so the token loop that SnapKV and
+// H2O run stays small.
+template <typename KT>
+__device__ __noinline__ float dropkv_step_score(const float* a, const KT* v, int g, int d, const float* lg,
+                                                   int lcap, const float* lse2) {
+  float dist[kMaxG];
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) dist[h] = 0.f;
+  constexpr int kPer = 16 / static_cast<int>(sizeof(KT));    // elements per 16-byte load
+  for (int e0 = 0; e0 < d; e0 += kPer) {
+    const uint4 raw = *reinterpret_cast<const uint4*>(v + e0);
+    const KT* pv = reinterpret_cast<const KT*>(&raw);
+#pragma unroll
+    for (int u = 0; u < kPer; ++u) {
+      const float x = static_cast<float>(pv[u]);
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h) {
+        if (h < g) {
+          const float df = a[h * d + e0 + u] - x;
+          dist[h] = fmaf(df, df, dist[h]);
+        }
+      }
+    }
+  }
+  float sc = 0.f;
+#pragma unroll
+  for (int h = 0; h < kMaxG; ++h) {
+    if (h < g) {
+      const float x = lg[static_cast<size_t>(h) * lcap] - lse2[h];
+      const float p = exp2f(x);
+      if (p > 0.f) {
+        const float om = p > 0.5f ? -expm1f(x * kLn2) : 1.f - p;
+        sc += om > 0.f ? p / om * sqrtf(dist[h]) : INFINITY;
+      }
+    }
+  }
+  return sc;
+}
+
 // Marks this lane's epilogue done (thread 0 only).  The per-lane requests
 // the allocator reads (need_admit, want_dst, plan_tlive, count, released
 // block owners) are written before (by any thread of the CTA, ordered by a
@@ -546,14 +592,18 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       float acc = 0.f;
 #pragma unroll 8
       for (int s = 0; s < nseg; ++s) acc = fmaf(po[(static_cast<size_t>(s) * g + h) * d + e], sh_scale[s][h], acc);
-      A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = acc / sh_L[h];
+      const float o = acc / sh_L[h];
+      A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = o;
+      sh_rows[he] = o;    // the heads' outputs, for the DropKV scores below
     }
+    __syncthreads();
   }
 
   // ---- weights -> score state; SnapKV window sums ----------------------------
   const int policy = dm.policy;
+  const bool ringp = policy != KVEVICT_H2O;   // SnapKV, DropKV decode variant: history ring keys
   const int W = dm.W;
-  const int rs = policy == KVEVICT_SNAPKV ? A.ls.ring_slot[l] : 0;
+  const int rs = ringp ? A.ls.ring_slot[l] : 0;
   double* keys64 = A.ws.keys64 ? A.ws.keys64 + static_cast<size_t>(l) * dm.cap : nullptr;
   double* pooled64 = A.ws.pooled64 ? A.ws.pooled64 + static_cast<size_t>(l) * dm.cap : nullptr;
   const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
@@ -568,9 +618,19 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   for (int i = tid; i < n; i += blockDim.x) {
     float w = 0.f;
     if (A.has_q) {
-      for (int h = 0; h < g; ++h) w += exp2f(lg[static_cast<size_t>(h) * dm.lcap + i] - sh_lse2[h]);
+      if (policy == KVEVICT_DROPKV) {
+        const int s = L.slot[i];
+        if (s >= 0 && s < dm.P * kBlock) {
+          w = dropkv_step_score<KT>(sh_rows, static_cast<const KT*>(A.ls.v_pool) + static_cast<size_t>(s) * d, g, d,
+                                    lg + i, dm.lcap, sh_lse2);
+        } else {
+          set_status(A.ws.status, ST_BAD_INDEX);
+        }
+      } else {
+        for (int h = 0; h < g; ++h) w += exp2f(lg[static_cast<size_t>(h) * dm.lcap + i] - sh_lse2[h]);
+      }
     }
-    if (policy == KVEVICT_SNAPKV) {
+    if (ringp) {
       float* row = L.ring + static_cast<size_t>(i) * W;
       if (A.has_q) row[rs] = w;
       double sum = 0.0;
@@ -593,9 +653,9 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       }
     }
   }
-  if (policy == KVEVICT_SNAPKV && tid == 0) keys64[n] = 0.0;
+  if (ringp && tid == 0) keys64[n] = 0.0;
   __syncthreads();
-  if (policy == KVEVICT_SNAPKV) {
+  if (ringp) {
     if (A.has_q && tid == 0) A.ls.ring_slot[l] = (rs + 1) % W;
     // sliding max over kept neighbours [i-r, i+r], clamped to [0, n]
     const int r = (dm.pool_kernel - 1) / 2;
@@ -637,7 +697,7 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
     }
   } else if (k > 1) {
     SelectResult sel;
-    if (policy == KVEVICT_SNAPKV) {
+    if (ringp) {
       auto keyf = [&](int i) { return mono_key(pooled64[i]); };
       sel = block_bottom_k(n, k, 64, keyf, posf, candf, sh_hist, sh_misc);
       auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };

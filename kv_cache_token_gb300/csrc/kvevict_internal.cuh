@@ -88,6 +88,7 @@ struct Workspace {
   int32_t* cmp_pos;                // [lanes][cap]  forced compaction: survivors of each CTA's range,
   int32_t* cmp_slot;               //               compacted at the range start
   float* cmp_score;                // [lanes][cap]
+  float* cmp_ring;                 // [lanes][cap][W]  history rows of the survivors (ring policies)
   int32_t* cmp_cnt;                // [lanes][cmp_ctas_per_lane + 1]  survivors per CTA, entries before
 };
 
@@ -113,6 +114,7 @@ struct Ctx {
 };
 
 // workspace layout (host)
+bool has_ring(const kvevict_config& c);
 size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base);
 Dims make_dims(const kvevict_config& c);
 LayerState layer_state(const Ctx& ctx, int layer);

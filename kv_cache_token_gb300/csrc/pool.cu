@@ -284,97 +284,15 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelClThre
 // ---------------------------------------------------------------------------
 // forced compaction
 // ---------------------------------------------------------------------------
-// Victim test against an ascending victim list: per chunk of table entries
-// the list's slice that can match (it starts at the first victim position
-// not below the chunk's first position) is staged in shared memory, and
-// each entry is looked up there.  The slice start only moves forward.
-struct SegVictims {
-  const int32_t* vl;
-  int k;
-  const int32_t* pos;
-  int* seg;
-  int* sh_len;
-  int start, len;
-  __device__ void prepare(int base) {
-    if (base > 0) {
-      // drop the slice entries below this chunk's first position
-      const int p0 = pos[base];
-      for (;;) {
-        const int c = __syncthreads_count(static_cast<int>(threadIdx.x) < len && seg[threadIdx.x] < p0);
-        start += c;
-        if (c < len || start >= k) break;
-        // the whole slice was below p0 (victims not in the table): next slice
-        len = min(static_cast<int>(blockDim.x), k - start);
-        if (static_cast<int>(threadIdx.x) < len) seg[threadIdx.x] = vl[start + threadIdx.x];
-        __syncthreads();
-      }
-    }
-    len = min(static_cast<int>(blockDim.x), max(0, k - start));
-    __syncthreads();
-    if (static_cast<int>(threadIdx.x) < len) seg[threadIdx.x] = vl[start + threadIdx.x];
-    __syncthreads();
-  }
-  __device__ bool operator()(int i) const {
-    const int p = pos[i];
-    int lo = 0, hi = len;
-    while (lo < hi) {
-      const int mid = (lo + hi) >> 1;
-      if (seg[mid] < p) lo = mid + 1; else hi = mid;
-    }
-    return lo < len && seg[lo] == p;
-  }
-};
-
-__global__ void __launch_bounds__(kThreads) compact_evict_kernel(LayerState ls, Workspace ws, Dims dm,
-                                                                const int32_t* victims,
-                                                                const int32_t* n_victims) {
-  __shared__ int sh_scan[40];
-  __shared__ int sh_seg[kThreads];
-  __shared__ int sh_seg_len;
-  __shared__ int sh_idx[kThreads];
-  __shared__ __align__(16) float sh_rows[128 * kMaxW];
-  const int l = blockIdx.x, tid = threadIdx.x;
-  LaneRefs L = lane_refs(ls, dm, l);
-  const int n = ls.count[l];
-  if (n < 0 || n > dm.cap) {
-    if (tid == 0) { set_status(ws.status, ST_BAD_INDEX); ws.want_dst[l] = 0; ws.need_admit[l] = 0; }
-    return;
-  }
-  const int k = max(0, min(n_victims[l], n));
-  SegVictims isv;
-  isv.vl = victims + static_cast<size_t>(l) * dm.cap;
-  isv.k = k;
-  isv.pos = L.pos;
-  isv.seg = sh_seg;
-  isv.sh_len = &sh_seg_len;
-  isv.start = 0;
-  isv.len = 0;
-  int dead = 0;
-  const int vcount = lane_remove(L, n, isv, nullptr, ws.freed_flag, &dead, dm.P, ws.status, sh_scan, sh_idx,
-                                 sh_rows);
-  const int m = n - vcount;
-  if (tid == 0) ls.count[l] = m;
-  const int nb = lane_prune_blocks(L, l, sh_scan);
-  int t_live = 0;
-  const int ndst = lane_plan(L, nb, m, true, dm.theta_f, false, &t_live, sh_scan);
-  if (tid == 0) {
-    ws.need_admit[l] = 0;
-    ws.want_dst[l] = ndst;
-    ws.plan_tlive[l] = t_live;
-    if (ndst > 0) atomicOr(ws.work_flag, 1);
-    atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_VICTIMS]), (unsigned long long)vcount);
-    if (dead) atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_FREED_DEAD]), (unsigned long long)dead);
-  }
-}
-
-// Removal for tables without history rows, cmp_ctas_per_lane CTAs per lane
+// Removal, cmp_ctas_per_lane CTAs per lane
 // over contiguous ranges of the table (one wave at 128K instead of one CTA
 // per lane).  compact_remove_kernel: each CTA finds the slice of the
 // ascending victim list that can match its range (positions between its
 // first and last entry; extra positions match nothing, as in the oracle's
 // membership test), stages it in shared memory when it fits, tests each
 // entry by binary search, clears the victims' live bits and writes its
-// survivors, in order, to scratch at the range start, with their count.
+// survivors (with their history rows, for the ring policies), in order, to
+// scratch at the range start, with their count.
 // compact_place_kernel: each CTA copies its survivors to their final index
 // (the counts of the lane's earlier CTAs before it; the lane's entry count
 // before the removal comes from scratch).
@@ -417,6 +335,7 @@ __global__ void __launch_bounds__(kCmpThreads) compact_remove_kernel(LayerState 
                                                                     const int32_t* n_victims, int cpl) {
   __shared__ int sh_vic[kCmpStage];
   __shared__ int sh_scan[40];
+  __shared__ int sh_src[kCmpThreads];
   __shared__ int sh_v0, sh_v1;
   const int l = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
   LaneRefs L = lane_refs(ls, dm, l);
@@ -469,6 +388,7 @@ __global__ void __launch_bounds__(kCmpThreads) compact_remove_kernel(LayerState 
       ws.cmp_pos[o] = p;
       ws.cmp_slot[o] = sl;
       ws.cmp_score[o] = sc;
+      if (L.ring) sh_src[ex2 & 0xFFFF] = i;
     }
     if (isv) {
       if (sl >= 0 && sl < dm.P * kBlock) {
@@ -476,6 +396,15 @@ __global__ void __launch_bounds__(kCmpThreads) compact_remove_kernel(LayerState 
       } else if (sl >= 0) {
         set_status(ws.status, ST_BAD_INDEX);
       }
+    }
+    if (L.ring) {
+      // the chunk's survivors' history rows, W floats each, to scratch
+      __syncthreads();
+      const int W = L.W, kept = tot2 & 0xFFFF;
+      float* dst = ws.cmp_ring + (lo_off + s + kept_total) * W;
+      for (int e2 = tid; e2 < kept * W; e2 += blockDim.x)
+        dst[e2] = L.ring[static_cast<size_t>(sh_src[e2 / W]) * W + e2 % W];
+      __syncthreads();
     }
     kept_total += tot2 & 0xFFFF;
     vict_total += tot2 >> 16;
@@ -511,6 +440,11 @@ __global__ void __launch_bounds__(kCmpThreads) compact_place_kernel(LayerState l
     L.pos[off + j] = ws.cmp_pos[lo_off + s + j];
     L.slot[off + j] = ws.cmp_slot[lo_off + s + j];
     if (L.score) L.score[off + j] = ws.cmp_score[lo_off + s + j];
+  }
+  if (L.ring) {
+    const size_t W = L.W;
+    for (size_t e = tid; e < static_cast<size_t>(mine) * W; e += blockDim.x)
+      L.ring[static_cast<size_t>(off) * W + e] = ws.cmp_ring[(lo_off + s) * W + e];
   }
 }
 
@@ -896,9 +830,7 @@ cudaError_t launch_compact(const Ctx& ctx, int layer, const int32_t* victims, co
                            int32_t* freed, int32_t* n_freed, int32_t* moves, int32_t* n_moves,
                            cudaStream_t stream) {
   LayerState ls = layer_state(ctx, layer);
-  if (ls.ring) {
-    compact_evict_kernel<<<ctx.dims.lanes, kThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, victims, n_victims);
-  } else {
+  {
     const int cpl = cmp_ctas_per_lane(ctx.dims);
     const dim3 grid(cpl, ctx.dims.lanes);
     compact_remove_kernel<<<grid, kCmpThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, victims, n_victims, cpl);

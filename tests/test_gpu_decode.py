@@ -76,6 +76,24 @@ def test_h2o_group8_below_budget_growth():
     run_decode(shp, 40)
 
 
+def test_dropkv_decode_variant():
+    """DropKV decode variant: each step's residual-output scores (sum over the
+    group of p / (1 - p) ||a_h - v_j||) go through a history ring of 4 steps;
+    keys are the window sums (no pooling); heavy-tailed keys."""
+    shp = scaled("dropkv_prefill", ctx=600, num_kv_heads=2, num_q_heads=8, steps=12, budget=200,
+                 recent_window=40, obs_window=4, pool_kernel=1, kind="decode")
+    run_decode(shp, 12)
+
+
+def test_dropkv_decode_variant_pooled_with_null_steps_fp32():
+    shp = scaled("dropkv_prefill", ctx=400, num_kv_heads=2, num_q_heads=8, steps=10, budget=150,
+                 recent_window=20, obs_window=3, pool_kernel=3, kind="decode")
+    run_decode(shp, 10, null_steps=(2, 5))
+    shp = scaled("h2o_toy", policy=2, ctx=300, steps=12, budget=100, recent_window=20, obs_window=2,
+                 pool_kernel=1)
+    run_decode(shp, 12)
+
+
 def test_null_query_is_inert():
     shp = scaled("snapkv_decode", batch=1, num_kv_heads=2, num_q_heads=8, ctx=300, steps=6,
                  budget=200, recent_window=20, obs_window=4, pool_kernel=3)
