@@ -50,7 +50,7 @@ def parse():
                          "32K and 128K, selection, forced compaction, the SnapKV and toy decode steps), one "
                          "JSON line each, instead of the decode-step bench line")
     ap.add_argument("--only", default="",
-                    help="with --kernel-table: comma-separated subset of d3_32k, d3_128k, snapkv, toy")
+                    help="with --kernel-table: comma-separated subset of d3_32k, d3_128k, snapkv, dropkv_decode, toy")
     return ap.parse_args()
 
 
@@ -604,10 +604,16 @@ def run_kernel_table(args):
         torch.cuda.empty_cache()
 
     # decode steps of the SnapKV workload and of the H2O toy (latency-bound)
-    for tag, name, first in (("snapkv", "snapkv_decode", 1), ("toy", "h2o_toy", 1)):
+    # the DropKV decode variant runs on the SnapKV workload's data (same
+    # prompts, queries and new tokens), with its residual-output scores in a
+    # 32-step ring and no pooling
+    import dataclasses
+    variants = {"dropkv_decode": lambda: dataclasses.replace(shape("snapkv_decode"), policy=2, pool_kernel=1)}
+    for tag, name, first in (("snapkv", "snapkv_decode", 1), ("dropkv_decode", "dropkv_decode", 1),
+                             ("toy", "h2o_toy", 1)):
         if only and tag not in only:
             continue
-        shp = shape(name)
+        shp = variants[name]() if name in variants else shape(name)
         wl = Workload(shp)
         eng = Engine(config_from(shp))
         eng.reset()
@@ -642,7 +648,11 @@ def run_kernel_table(args):
         ms = e0.elapsed_time(e1) / len(timed_steps)
         lanes = eng.lanes
         es = 2 if shp.kv_dtype == "bf16" else 4
-        per_tok = 2 * d * es + (4 + 4 * shp.obs_window + 8 if shp.policy == 1 else 8)
+        # K and V rows; the ring policies add the ring write, the window
+        # sum's reads and the key, and the DropKV variant a second V read
+        per_tok = 2 * d * es + (8 if shp.policy == 0 else 4 + 4 * shp.obs_window + 8)
+        if shp.policy == 2:
+            per_tok += d * es
         emit("decode step (attention, score epilogue, selection, eviction, admission)", name, ms, ms, ms,
              nbytes=(n_before + lanes) * per_tok,
              extra={"steps_timed": len(timed_steps), "us_per_step": round(ms * 1e3, 2),
