@@ -26,8 +26,10 @@
  *   slots           [L][B*Hkv][C]   int32
  *   counts          [L][B*Hkv]      int32, kept tokens per lane
  *   scores          [L][B*Hkv][C]   fp32, H2O cumulative scores
- *   ring            [L][B*Hkv][C][obs_window] fp32 (SnapKV, and DropKV with
- *                   obs_window >= 1; else NULL)
+ *   ring            [L][P][16][obs_window] fp32 (SnapKV, and DropKV with
+ *                   obs_window >= 1; else NULL): a kept token's history row
+ *                   sits at its slot and moves with its K/V rows, so that
+ *                   removing a token from a table moves no history
  *   ring_slot       [L][B*Hkv]      int32
  *   block_owner     [L][P]          int32, owning lane or -1 when free
  *   block_mask      [L][P]          int32, bit o set = offset o holds a live token

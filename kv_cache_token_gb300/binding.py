@@ -149,7 +149,8 @@ class Engine:
         self.slots = buf(BUF_SLOTS, (Lr, lanes, C), torch.int32)
         self.counts = buf(BUF_COUNTS, (Lr, lanes), torch.int32)
         self.scores = buf(BUF_SCORES, (Lr, lanes, C), torch.float32)
-        self.ring = (buf(BUF_RING, (Lr, lanes, C, c.obs_window), torch.float32)
+        # history rows sit at the tokens' slots: ring[layer][slot] (slot = block * 16 + offset)
+        self.ring = (buf(BUF_RING, (Lr, P * 16, c.obs_window), torch.float32)
                      if c.policy == SNAPKV or (c.policy == DROPKV and c.obs_window >= 1) else None)
         self.ring_slot = buf(BUF_RING_SLOT, (Lr, lanes), torch.int32)
         self.block_owner = buf(BUF_BLOCK_OWNER, (Lr, P), torch.int32)

@@ -64,8 +64,8 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base) {
     w.lane_nseg_buf[c] = reinterpret_cast<int32_t*>(take(lanes * 4));
   }
   const bool snap = has_ring(c);
-  w.keys64 = snap ? reinterpret_cast<double*>(take(lanes * cap * 8)) : nullptr;
-  w.pooled64 = snap ? reinterpret_cast<double*>(take(lanes * cap * 8)) : nullptr;
+  w.keys64 = snap ? reinterpret_cast<unsigned long long*>(take(lanes * cap * 8)) : nullptr;
+  w.pooled64 = snap ? reinterpret_cast<unsigned long long*>(take(lanes * cap * 8)) : nullptr;
   w.need_admit = reinterpret_cast<int32_t*>(take(lanes * 4));
   w.want_dst = reinterpret_cast<int32_t*>(take(lanes * 4));
   w.admit_block = reinterpret_cast<int32_t*>(take(lanes * 4));
@@ -79,7 +79,6 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base) {
   w.cmp_pos = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
   w.cmp_slot = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
   w.cmp_score = reinterpret_cast<float*>(take(lanes * cap * 4));
-  w.cmp_ring = has_ring(c) ? reinterpret_cast<float*>(take(lanes * cap * static_cast<size_t>(dm.W) * 4)) : nullptr;
   w.cmp_cnt = reinterpret_cast<int32_t*>(take(lanes * static_cast<size_t>(cmp_ctas_per_lane(dm) + 1) * 4));
   w.epi_done = reinterpret_cast<int32_t*>(take(4));
   if (dm.max_window > 0 && dm.dtype == KVEVICT_BF16 && dm.d == 128) {
@@ -112,7 +111,7 @@ LayerState layer_state(const Ctx& ctx, int layer) {
   s.slot = b.slots + L * lanes * cap;
   s.count = b.counts + L * lanes;
   s.score = b.scores + L * lanes * cap;
-  s.ring = (has_ring(ctx.cfg) && b.ring) ? b.ring + L * lanes * cap * dm.W : nullptr;
+  s.ring = (has_ring(ctx.cfg) && b.ring) ? b.ring + L * P * kBlock * dm.W : nullptr;
   s.ring_slot = b.ring_slot + L * lanes;
   s.owner = b.block_owner + L * P;
   s.mask = b.block_mask + L * P;
@@ -200,7 +199,7 @@ size_t kvevict_buffer_size(const kvevict_config* c, int which) {
     case KVEVICT_BUF_RING_SLOT:
     case KVEVICT_BUF_LANE_NBLOCKS: return L * lanes * 4;
     case KVEVICT_BUF_RING:
-      return kve::has_ring(*c) ? L * lanes * cap * static_cast<size_t>(c->obs_window) * 4 : 0;
+      return kve::has_ring(*c) ? L * P * kve::kBlock * static_cast<size_t>(c->obs_window) * 4 : 0;
     case KVEVICT_BUF_BLOCK_OWNER:
     case KVEVICT_BUF_BLOCK_MASK: return L * P * 4;
     case KVEVICT_BUF_STATS: return L * KVEVICT_NSTATS * 8;

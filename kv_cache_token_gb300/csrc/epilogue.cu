@@ -48,7 +48,7 @@ __device__ __forceinline__ void copy_row(KT* dst, const KT* src, int d) {
   for (int e = threadIdx.x; e < d; e += blockDim.x) dst[e] = src[e];
 }
 
-template <typename KT>
+template <typename KT, bool kRing>
 __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n, unsigned char* dsm,
                                           int* sh_work);
 __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const Dims& dm, int* sh_scan,
@@ -62,50 +62,255 @@ __device__ __forceinline__ float hw_exp2(float x) {
   return y;
 }
 
-// DropKV decode variant: this step's residual-output score of one kept
-// token, sum over the group's heads h of p / (1 - p) * ||a_h - v|| (DropKV
-// explainer, Lemma 1, with the window reduced to the current query of each
-// head).  a [g][d] are the heads' outputs (shared memory), v the token's V
-// row; the distance is taken directly in fp32 (no expansion, so no
-// cancellation when a_h is close to v), 1 - p from expm1 when p > 1/2, and
-// the term is +inf where 1 - p <= 0.  lg: the token's base-2 scaled logits,
-// one per head, lcap apart.  Out of line, so the token loop that SnapKV and
-// H2O run stays small.
+// DropKV decode variant: this step's residual-output score of every kept
+// token, written to column rs of its history-ring row: the sum over the
+// group's heads of p / (1 - p) * ||a_h - v|| (DropKV explainer, Lemma 1, with
+// the window reduced to the current query of each head), 1 - p from expm1
+// when p > 1/2, +inf where 1 - p <= 0, no term where p = 0.  sh_a holds the
+// heads' outputs a_h (g x d floats), lg the base-2 scaled logits (one row of
+// lcap per head).  The ring row of a token is the one at its slot; hrows
+// (if not null) holds the kept tokens' rows in shared memory, ld apart, and
+// gets the scores too.
+//
+// Eight lanes share a token: each loads CPL 16-byte pieces of its V row
+// (lanes side by side, so a group reads 128 contiguous bytes per load) and
+// the group keeps kU tokens' rows in flight before any arithmetic.  The
+// distances are taken directly in fp32 (no expansion, so no cancellation when
+// a_h is close to v), four heads at a time, summed across the group; the
+// p / (1 - p) factors of a token's four heads are spread over its lanes.
+// The monotone image (mono_key) of +0.0.
+constexpr unsigned long long kKeyZero = 0x8000000000000000ull;
+
+// The window sum of one history row (column rs replaced by w when rs >= 0),
+// as its monotone key: the float64 sum in slot order 0 upward (SnapKV, "How
+// it works").  When the row's nonzero entries are finite, normal and their
+// exponents lie within `spread` of each other (spread + 24 + log2 W <= 53),
+// every partial sum of that order is exact in float64, so the sum is the
+// exact one; it is then taken in 64-bit integer arithmetic (significands
+// aligned to the smallest exponent) and converted once, exactly.  Other rows
+// are summed in float64.
+template <int kW>   // kW > 0: the row length at compile time; 0: W at run time
+__device__ __forceinline__ unsigned long long window_key(const float* row, const int Wr, const int rs, const float w,
+                                                        const int spread) {
+  const int W = kW > 0 ? kW : Wr;
+  unsigned umax = 0u, umin1 = 0xFFFFFFFFu;     // umin1: smallest nonzero bit pattern minus 1
+#pragma unroll
+  for (int t = 0; t < W; ++t) {
+    const unsigned u = __float_as_uint(t == rs ? w : row[t]);
+    umax = max(umax, u);
+    umin1 = min(umin1, u - 1u);
+  }
+  if (umax == 0u) return kKeyZero;
+  const int emax = static_cast<int>(umax >> 23), emin = static_cast<int>((umin1 + 1u) >> 23);
+  if (umax < 0x7F800000u && emin >= 1 && emax - emin <= spread) {
+    unsigned long long acc = 0ull;
+#pragma unroll
+    for (int t = 0; t < W; ++t) {
+      const unsigned u = __float_as_uint(t == rs ? w : row[t]);
+      const unsigned long long m = u != 0u ? static_cast<unsigned long long>((u & 0x7FFFFFu) | 0x800000u) : 0ull;
+      acc += m << max(static_cast<int>(u >> 23) - emin, 0);
+    }
+    // acc < 2^53: exact as a double; the scale 2^(emin - 150) is a normal power of two
+    const double v = static_cast<double>(acc) * __longlong_as_double(static_cast<long long>(emin - 150 + 1023) << 52);
+    return static_cast<unsigned long long>(__double_as_longlong(v)) | kKeyZero;
+  }
+  double sum = 0.0;
+  for (int t = 0; t < W; ++t) sum += static_cast<double>(t == rs ? w : row[t]);
+  return mono_key(sum);
+}
+
+// Starts asynchronous copies of the history rows of a lane's n kept tokens
+// (at their slots; W a multiple of 4) to rows[i * ld + t], t < W, in 16-byte
+// pieces, consecutive lanes on consecutive pieces; a row whose slot is out
+// of range is zero.  The slots go through sh_slot (n ints) first, so no copy
+// waits on a slot load.  All threads of the CTA take part.
+__device__ __forceinline__ void stage_history_async(const LaneRefs& L, const int n, const int W, const int ld,
+                                                    const int nslot, float* rows, int* sh_slot) {
+  for (int i = threadIdx.x; i < n; i += blockDim.x) {
+    const int s = L.slot[i];
+    sh_slot[i] = (s >= 0 && s < nslot) ? s : -1;
+  }
+  __syncthreads();
+  const int pr = W / 4;     // pieces per row
+  for (int e = threadIdx.x; e < n * pr; e += blockDim.x) {
+    const int i = e / pr, c = (e - i * pr) * 4;
+    const int s = sh_slot[i];
+    float* dst = rows + i * ld + c;
+    if (s >= 0) {
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                   "l"(L.ring + static_cast<size_t>(s) * W + c) : "memory");
+    } else {
+      *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+  }
+  cp_async_commit();
+}
+
+// window_key of a 16-byte aligned row with W a multiple of 4 (no column
+// replaced), read four floats at a time.
+template <int kW>
+__device__ __forceinline__ unsigned long long window_key4(const float* row, const int Wr, const int spread) {
+  const int W4 = (kW > 0 ? kW : Wr) / 4;
+  const uint4* r4 = reinterpret_cast<const uint4*>(row);
+  unsigned umax = 0u, umin1 = 0xFFFFFFFFu;
+#pragma unroll
+  for (int q = 0; q < W4; ++q) {
+    const uint4 v = r4[q];
+    umax = max(max(umax, max(v.x, v.y)), max(v.z, v.w));
+    umin1 = min(min(umin1, min(v.x - 1u, v.y - 1u)), min(v.z - 1u, v.w - 1u));
+  }
+  if (umax == 0u) return kKeyZero;
+  const int emax = static_cast<int>(umax >> 23), emin = static_cast<int>((umin1 + 1u) >> 23);
+  if (umax < 0x7F800000u && emin >= 1 && emax - emin <= spread) {
+    unsigned long long acc = 0ull;
+    auto add = [&](const unsigned u) {
+      const unsigned long long m = u != 0u ? static_cast<unsigned long long>((u & 0x7FFFFFu) | 0x800000u) : 0ull;
+      acc += m << max(static_cast<int>(u >> 23) - emin, 0);
+    };
+#pragma unroll
+    for (int q = 0; q < W4; ++q) {
+      const uint4 v = r4[q];
+      add(v.x); add(v.y); add(v.z); add(v.w);
+    }
+    const double v = static_cast<double>(acc) * __longlong_as_double(static_cast<long long>(emin - 150 + 1023) << 52);
+    return static_cast<unsigned long long>(__double_as_longlong(v)) | kKeyZero;
+  }
+  double sum = 0.0;
+  for (int t = 0; t < 4 * W4; ++t) sum += static_cast<double>(row[t]);
+  return mono_key(sum);
+}
+
+// One 16-byte piece of a K or V row as floats (8 bf16 or 4 fp32).
 template <typename KT>
-__device__ __noinline__ float dropkv_step_score(const float* a, const KT* v, int g, int d, const float* lg,
-                                                   int lcap, const float* lse2) {
-  float dist[kMaxG];
+__device__ __forceinline__ void piece_to_float(const uint4 w, float* x);
+template <>
+__device__ __forceinline__ void piece_to_float<__nv_bfloat16>(const uint4 w, float* x) {
+  const unsigned u[4] = {w.x, w.y, w.z, w.w};
 #pragma unroll
-  for (int h = 0; h < kMaxG; ++h) dist[h] = 0.f;
-  constexpr int kPer = 16 / static_cast<int>(sizeof(KT));    // elements per 16-byte load
-  for (int e0 = 0; e0 < d; e0 += kPer) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(v + e0);
-    const KT* pv = reinterpret_cast<const KT*>(&raw);
+  for (int k = 0; k < 4; ++k) {
+    x[2 * k] = __uint_as_float(u[k] << 16);
+    x[2 * k + 1] = __uint_as_float(u[k] & 0xFFFF0000u);
+  }
+}
+template <>
+__device__ __forceinline__ void piece_to_float<float>(const uint4 w, float* x) {
+  x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y); x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
+}
+
+template <typename KT, int CPL>
+__device__ __forceinline__ void dropkv_ring_scores(const EpiArgs& A, const LaneRefs& L, const int n, const float* sh_a,
+                                                const float* lg, const float* sh_lse2, const int W, const int rs,
+                                                float* hrows, const int ld) {
+  constexpr int kEpc = 16 / static_cast<int>(sizeof(KT));   // elements per 16-byte piece
+  constexpr int kU = 8 / CPL;                                // tokens per group and pass
+  constexpr int kPairs = kU / 2;                             // (token, head) terms per lane
+  constexpr int kTokLanes = 4 / kPairs;                      // lanes holding one token's terms
+  const Dims& dm = A.dm;
+  const int g = dm.g, d = dm.d;
+  const int tid = threadIdx.x, sub = tid & 7, grp = tid >> 3, ngrp = blockDim.x >> 3;
+  const uint4* vp = static_cast<const uint4*>(A.ls.v_pool);
+  const int rowc = d / kEpc;
+  const int nslot = dm.P * kBlock;
+  const int stride = ngrp * kU;
+  const int npass = (n + stride - 1) / stride;    // the same for every thread (shuffles below)
+  for (int ps = 0; ps < npass; ++ps) {
+    const int base = ps * stride + grp;
+    uint4 v[kU][CPL];
+    int sl[kU];
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
-      const float x = static_cast<float>(pv[u]);
-#pragma unroll
-      for (int h = 0; h < kMaxG; ++h) {
-        if (h < g) {
-          const float df = a[h * d + e0 + u] - x;
-          dist[h] = fmaf(df, df, dist[h]);
+    for (int u = 0; u < kU; ++u) {
+      const int i = base + u * ngrp;
+      int s = -1;
+      if (i < n) {
+        s = L.slot[i];
+        if (s < 0 || s >= nslot) {
+          if (sub == 0) set_status(A.ws.status, ST_BAD_INDEX);
+          s = -1;
         }
       }
-    }
-  }
-  float sc = 0.f;
+      sl[u] = s;
 #pragma unroll
-  for (int h = 0; h < kMaxG; ++h) {
-    if (h < g) {
-      const float x = lg[static_cast<size_t>(h) * lcap] - lse2[h];
-      const float p = exp2f(x);
-      if (p > 0.f) {
-        const float om = p > 0.5f ? -expm1f(x * kLn2) : 1.f - p;
-        sc += om > 0.f ? p / om * sqrtf(dist[h]) : INFINITY;
+      for (int c = 0; c < CPL; ++c)
+        v[u][c] = s >= 0 ? vp[static_cast<size_t>(s) * rowc + sub + 8 * c] : make_uint4(0u, 0u, 0u, 0u);
+    }
+    float sc = 0.f;
+    for (int h0 = 0; h0 < g; h0 += 4) {
+      // this lane's factors p / (1 - p), loaded before the distance arithmetic
+      float f[kPairs];
+#pragma unroll
+      for (int j = 0; j < kPairs; ++j) {
+        const int q = sub * kPairs + j, h = h0 + (q & 3), i = base + (q >> 2) * ngrp;
+        f[j] = 0.f;
+        if (h < g && i < n) {
+          const float x = lg[static_cast<size_t>(h) * dm.lcap + i] - sh_lse2[h];
+          const float p = exp2f(x);
+          if (p > 0.f) {
+            const float om = p > 0.5f ? -expm1f(x * kLn2) : 1.f - p;
+            f[j] = om > 0.f ? p / om : INFINITY;
+          }
+        }
       }
+      float dist[kU][4];
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+#pragma unroll
+        for (int hq = 0; hq < 4; ++hq) dist[u][hq] = 0.f;
+#pragma unroll
+      for (int c = 0; c < CPL; ++c) {
+        const int e0 = (sub + 8 * c) * kEpc;
+#pragma unroll
+        for (int hq = 0; hq < 4; ++hq) {
+          if (h0 + hq < g) {
+            float a[kEpc];
+            const float4* ap = reinterpret_cast<const float4*>(sh_a + (h0 + hq) * d + e0);
+#pragma unroll
+            for (int e = 0; e < kEpc / 4; ++e) {
+              const float4 t = ap[e];
+              a[4 * e] = t.x; a[4 * e + 1] = t.y; a[4 * e + 2] = t.z; a[4 * e + 3] = t.w;
+            }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+              float x[kEpc];
+              piece_to_float<KT>(v[u][c], x);
+#pragma unroll
+              for (int e = 0; e < kEpc; ++e) {
+                const float df = a[e] - x[e];
+                dist[u][hq] = fmaf(df, df, dist[u][hq]);
+              }
+            }
+          }
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u)
+#pragma unroll
+        for (int hq = 0; hq < 4; ++hq)
+#pragma unroll
+          for (int o = 1; o < 8; o <<= 1) dist[u][hq] += __shfl_xor_sync(0xffffffffu, dist[u][hq], o);
+      float t = 0.f;
+#pragma unroll
+      for (int j = 0; j < kPairs; ++j) {
+        const int q = sub * kPairs + j;
+        float dd = 0.f;
+#pragma unroll
+        for (int qq = 0; qq < kU * 4; ++qq)
+          if (qq == q) dd = dist[qq >> 2][qq & 3];
+        if (f[j] != 0.f) t += f[j] == INFINITY ? INFINITY : f[j] * sqrtf(dd);
+      }
+#pragma unroll
+      for (int o = 1; o < kTokLanes; o <<= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
+      sc += t;
+    }
+    int s = -1;
+#pragma unroll
+    for (int u = 0; u < kU; ++u)
+      if (u == sub / kTokLanes) s = sl[u];
+    const int it = base + (sub / kTokLanes) * ngrp;
+    if (sub % kTokLanes == 0 && it < n) {
+      if (s >= 0) L.ring[static_cast<size_t>(s) * W + rs] = sc;
+      if (hrows) hrows[it * ld + rs] = sc;
     }
   }
-  return sc;
 }
 
 // Marks this lane's epilogue done (thread 0 only).  The per-lane requests
@@ -485,7 +690,9 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
   }
 }
 
-template <typename KT>
+// kRing: the policy keeps a history ring (SnapKV, DropKV decode variant);
+// the H2O instantiation carries none of that code.
+template <typename KT, bool kRing>
 __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs A) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ int sh_scan[40];
@@ -505,11 +712,10 @@ __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs
       set_status(A.ws.status, ST_CAPACITY);
       A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
     }
-  } else if (dm.policy == KVEVICT_H2O && n + 1 - dm.budget <= 1 && n <= kFastN && dm.g <= 8 && dm.d <= 128 &&
-             (dm.d & 1) == 0) {
+  } else if (!kRing && n + 1 - dm.budget <= 1 && n <= kFastN && dm.g <= 8 && dm.d <= 128 && (dm.d & 1) == 0) {
     h2o_fast_step<KT>(A, L, n, dsm, &sh_sig, &sh_last, &sh_flag);
   } else {
-    lane_step<KT>(A, L, n, dsm, &sh_work);
+    lane_step<KT, kRing>(A, L, n, dsm, &sh_work);
   }
   __syncthreads();
   if (!sh_sig) {
@@ -530,28 +736,44 @@ __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs
 }
 
 // One lane's step after the attention kernel (all threads of the CTA).
-template <typename KT>
+template <typename KT, bool kRing>
 __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n, unsigned char* dsm,
                                           int* sh_work) {
   __shared__ float sh_M[kMaxG], sh_L[kMaxG], sh_lse2[kMaxG];
   __shared__ __align__(16) int sh_hist[256];   // also read as 64-bit words
   __shared__ int sh_misc[40];
   __shared__ int sh_scan[40];
-  __shared__ int sh_idx[kEpiThreads];
   __shared__ unsigned sh_min[32];
-  __shared__ int sh_nan;
+  __shared__ int sh_nan, sh_ncand;
   __shared__ float sh_scale[kMaxSeg][kMaxG];
   float* sh_rows = reinterpret_cast<float*>(dsm);      // general path: 128 * kMaxW floats
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
   const int cbuf = A.layer & 1;
+  const int policy = dm.policy;
+  constexpr bool ringp = kRing;   // SnapKV, DropKV decode variant: history ring keys
+  const int W = dm.W;
+  // history rows staged whole in shared memory: ld = 4 (mod 32) floats, so
+  // the 16-byte reads of eight lanes on eight consecutive rows hit distinct banks
+  const int ld = ((W + 27) / 32) * 32 + 4;
+
+  // ---- history rows, before the dependency wait ---------------------------------
+  // The ring is not written by the attention kernel, and every kernel before
+  // it is complete once it lets this one start, so the rows of all kept
+  // tokens are copied to shared memory (when they fit beside the heads'
+  // outputs and the keys) while the attention kernel drains.
+  float* hrows = sh_rows + kMaxG * 128;
+  const size_t hkeys_off = ((static_cast<size_t>(kMaxG) * 128 + static_cast<size_t>(n) * ld) * 4 + 7) & ~static_cast<size_t>(7);
+  const bool staged_all = ringp && n > 0 && (W & 3) == 0 && hkeys_off + static_cast<size_t>(n + 1) * 8 <= kEpiDynSmem;
+  if (staged_all) stage_history_async(L, n, W, ld, dm.P * kBlock, hrows, reinterpret_cast<int*>(dsm + hkeys_off));
 
   // ---- general path ------------------------------------------------------------
   grid_dep_wait();      // the attention kernel's results are complete and visible
   grid_dep_launch();
-  if (tid == 0) sh_nan = 0;
+  if (tid == 0) { sh_nan = 0; sh_ncand = 0; }
   if (n > 0 && L.pos[n - 1] >= A.new_pos) {
+    if (staged_all) cp_async_wait_all();
     if (tid == 0) {
       set_status(A.ws.status, ST_POSITION);
       A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
@@ -600,12 +822,13 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   }
 
   // ---- weights -> score state; SnapKV window sums ----------------------------
-  const int policy = dm.policy;
-  const bool ringp = policy != KVEVICT_H2O;   // SnapKV, DropKV decode variant: history ring keys
-  const int W = dm.W;
+  if (staged_all) {
+    cp_async_wait_all();
+    __syncthreads();
+  }
   const int rs = ringp ? A.ls.ring_slot[l] : 0;
-  double* keys64 = A.ws.keys64 ? A.ws.keys64 + static_cast<size_t>(l) * dm.cap : nullptr;
-  double* pooled64 = A.ws.pooled64 ? A.ws.pooled64 + static_cast<size_t>(l) * dm.cap : nullptr;
+  unsigned long long* kbuf = A.ws.keys64 ? A.ws.keys64 + static_cast<size_t>(l) * dm.cap : nullptr;
+  unsigned long long* pooled = A.ws.pooled64 ? A.ws.pooled64 + static_cast<size_t>(l) * dm.cap : nullptr;
   const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
   const int k = max(0, n + 1 - dm.budget);
   const int cut = A.new_pos - dm.R + 1;
@@ -615,29 +838,108 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   uint32_t best_p = 0xFFFFFFFFu;
   int best_i = -1;
   int nan_count = 0;
-  for (int i = tid; i < n; i += blockDim.x) {
-    float w = 0.f;
-    if (A.has_q) {
-      if (policy == KVEVICT_DROPKV) {
-        const int s = L.slot[i];
-        if (s >= 0 && s < dm.P * kBlock) {
-          w = dropkv_step_score<KT>(sh_rows, static_cast<const KT*>(A.ls.v_pool) + static_cast<size_t>(s) * d, g, d,
-                                    lg + i, dm.lcap, sh_lse2);
-        } else {
-          set_status(A.ws.status, ST_BAD_INDEX);
-        }
-      } else {
+  if (ringp && policy == KVEVICT_DROPKV && A.has_q) {
+    // this step's residual-output scores straight into ring column rs
+    constexpr int kEpc = 16 / static_cast<int>(sizeof(KT));
+    float* hr = staged_all ? hrows : nullptr;
+    if (d == 128) dropkv_ring_scores<KT, 128 / kEpc / 8>(A, L, n, sh_rows, lg, sh_lse2, W, rs, hr, ld);
+    else dropkv_ring_scores<KT, 64 / kEpc / 8>(A, L, n, sh_rows, lg, sh_lse2, W, rs, hr, ld);
+    __syncthreads();
+  }
+  int lw = 0;
+  while ((1 << lw) < W) ++lw;
+  const int spread = 29 - lw;    // exact-sum bound: spread + 24 + log2(W) <= 53
+  if (staged_all) {
+    // every row is in shared memory: a thread per token; SnapKV's new weight
+    // goes into column rs of the staged row and of the ring (the DropKV
+    // variant's scores are already in both)
+    kbuf = reinterpret_cast<unsigned long long*>(dsm + hkeys_off);
+    const bool fresh = A.has_q && policy == KVEVICT_SNAPKV;
+    int ncand = 0;
+    for (int i = tid; i < n; i += blockDim.x) {
+      float* row = hrows + i * ld;
+      if (fresh) {
+        float w = 0.f;
         for (int h = 0; h < g; ++h) w += exp2f(lg[static_cast<size_t>(h) * dm.lcap + i] - sh_lse2[h]);
+        row[rs] = w;
+        const int s = L.slot[i];
+        if (s >= 0 && s < dm.P * kBlock) L.ring[static_cast<size_t>(s) * W + rs] = w;
+        else set_status(A.ws.status, ST_BAD_INDEX);
       }
+      const unsigned long long key = W == 32 ? window_key4<32>(row, 32, spread) : window_key4<0>(row, W, spread);
+      kbuf[i] = key;
+      if (key == ~0ull) ++nan_count;
+      ncand += L.pos[i] < cut ? 1 : 0;
     }
-    if (ringp) {
-      float* row = L.ring + static_cast<size_t>(i) * W;
-      if (A.has_q) row[rs] = w;
-      double sum = 0.0;
-      for (int t = 0; t < W; ++t) sum += static_cast<double>((A.has_q && t == rs) ? w : row[t]);
-      keys64[i] = sum;
-      if (sum != sum) ++nan_count;
-    } else {
+    ncand = warp_sum(ncand);
+    if ((tid & 31) == 0 && ncand) atomicAdd(&sh_ncand, ncand);
+  } else if (ringp) {
+    // window sums: each warp stages 32 tokens' history rows in shared memory
+    // (one row per load instruction, coalesced), then each lane takes its own
+    // token's sum (window_key); SnapKV's new weight enters the sum (and the
+    // ring) at column rs
+    const int lane = tid & 31, warp = tid >> 5, nw = blockDim.x >> 5;
+    const int ld = W + 1;    // padded row: the lanes' row reads hit distinct banks
+    float* stg = sh_rows + kMaxG * 128 + warp * 32 * ld;
+    const bool fresh = A.has_q && policy == KVEVICT_SNAPKV;
+    // the keys stay in shared memory when they fit beside the staging rows
+    const size_t used = (static_cast<size_t>(kMaxG) * 128 + static_cast<size_t>(nw) * 32 * ld) * 4;
+    if (used + static_cast<size_t>(n + 1) * 8 <= kEpiDynSmem) kbuf = reinterpret_cast<unsigned long long*>(dsm + used);
+    // slots one chunk ahead; a chunk's position, weight and row loads are
+    // all issued before its arithmetic (the ring write of column rs comes
+    // after the row loads: the sums take w for that column anyway)
+    int ncand = 0;     // this thread's candidates (positions below the cut: a prefix of the table)
+    int s_next = warp * 32 + lane < n ? L.slot[warp * 32 + lane] : -1;
+    for (int base = warp * 32; base < n; base += nw * 32) {
+      const int i = base + lane;
+      int s = s_next;
+      if (i < n && (s < 0 || s >= dm.P * kBlock)) {
+        set_status(A.ws.status, ST_BAD_INDEX);
+        s = -1;
+      }
+      const int inext = i + nw * 32;
+      s_next = inext < n ? L.slot[inext] : -1;
+      const int p = i < n ? L.pos[i] : 0;
+      float lgv[kMaxG];
+#pragma unroll
+      for (int h = 0; h < kMaxG; ++h)
+        lgv[h] = (fresh && h < g && i < n) ? lg[static_cast<size_t>(h) * dm.lcap + i] : 0.f;
+      for (int c = lane; c - lane < W; c += 32) {
+        float x[32];
+#pragma unroll
+        for (int r = 0; r < 32; ++r) {
+          const int sr = __shfl_sync(0xffffffffu, s, r);
+          x[r] = (sr >= 0 && c < W) ? L.ring[static_cast<size_t>(sr) * W + c] : 0.f;
+        }
+        if (c < W) {
+#pragma unroll
+          for (int r = 0; r < 32; ++r) stg[r * ld + c] = x[r];
+        }
+      }
+      float w = 0.f;
+      if (fresh) {
+#pragma unroll
+        for (int h = 0; h < kMaxG; ++h)
+          if (h < g) w += exp2f(lgv[h] - sh_lse2[h]);
+        if (s >= 0) L.ring[static_cast<size_t>(s) * W + rs] = w;
+      }
+      ncand += (i < n && p < cut) ? 1 : 0;
+      __syncwarp();
+      if (i < n) {
+        const unsigned long long key = W == 32 ? window_key<32>(stg + lane * ld, 32, fresh ? rs : -1, w, spread)
+                                               : window_key<0>(stg + lane * ld, W, fresh ? rs : -1, w, spread);
+        kbuf[i] = key;
+        if (key == ~0ull) ++nan_count;
+      }
+      __syncwarp();
+    }
+    ncand = warp_sum(ncand);
+    if (lane == 0 && ncand) atomicAdd(&sh_ncand, ncand);
+  } else {
+    for (int i = tid; i < n; i += blockDim.x) {
+      float w = 0.f;
+      if (A.has_q)
+        for (int h = 0; h < g; ++h) w += exp2f(lg[static_cast<size_t>(h) * dm.lcap + i] - sh_lse2[h]);
       float sc = L.score[i];
       if (A.has_q) {
         sc += w;
@@ -653,32 +955,27 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       }
     }
   }
-  if (ringp && tid == 0) keys64[n] = 0.0;
+  if (ringp && tid == 0) kbuf[n] = kKeyZero;     // the new token's sum
   __syncthreads();
   if (ringp) {
     if (A.has_q && tid == 0) A.ls.ring_slot[l] = (rs + 1) % W;
-    // sliding max over kept neighbours [i-r, i+r], clamped to [0, n]
+    // max over kept neighbours [i-r, i+r], clamped to [0, n], on the keys'
+    // monotone images (a NaN sum, the largest image, wins the max); each
+    // thread takes a run of consecutive entries
+    // (candidates are the first ncand entries; positions ascend with the
+    // index, so the index breaks ties in the position's place)
     const int r = (dm.pool_kernel - 1) / 2;
-    const int span = 32 - 2 * r;
-    const int lane = tid & 31, warp = tid >> 5, nwarps = blockDim.x >> 5;
     const int nn = n + 1;
-    for (int base = warp * span; base < nn; base += nwarps * span) {
-      const int idx = base - r + lane;
-      const double v = (idx >= 0 && idx < nn) ? keys64[idx] : -INFINITY;
-      double m = v;
-      for (int o = 1; o <= r; ++o) {
-        m = fmax(m, __shfl_down_sync(0xffffffffu, v, o));
-        m = fmax(m, __shfl_up_sync(0xffffffffu, v, o));
-      }
-      if (lane >= r && lane < 32 - r && idx >= 0 && idx < nn) {
-        pooled64[idx] = m;
-        if (k == 1 && idx < n) {
-          const int p = L.pos[idx];
-          const unsigned long long kk = mono_key(m);
-          if (p < cut && (kk < best_k || (kk == best_k && static_cast<uint32_t>(p) < best_p))) {
-            best_k = kk; best_p = static_cast<uint32_t>(p); best_i = idx;
-          }
-        }
+    const int ncand = sh_ncand;
+    const int per = (nn + static_cast<int>(blockDim.x) - 1) / static_cast<int>(blockDim.x);
+    const int j1 = min(nn, (tid + 1) * per);
+    for (int j = tid * per; j < j1; ++j) {
+      unsigned long long m = 0;
+      const int qa = max(0, j - r), qb = min(nn - 1, j + r);
+      for (int q = qa; q <= qb; ++q) m = max(m, kbuf[q]);
+      if (k > 1) pooled[j] = m;
+      if (k == 1 && j < ncand && (m < best_k || (m == best_k && static_cast<uint32_t>(j) < best_p))) {
+        best_k = m; best_p = static_cast<uint32_t>(j); best_i = j;
       }
     }
     __syncthreads();
@@ -693,22 +990,20 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
     const int v = block_argmin3(best_k, best_p, best_i, sh_hist, sh_misc);
     if (v >= 0) {
       vcount = 1;
-      dead = lane_remove_one(L, n, v, vout, dm.P, A.ws.status, sh_misc, sh_rows);
+      dead = lane_remove_one(L, n, v, vout, dm.P, A.ws.status, sh_misc);
     }
   } else if (k > 1) {
     SelectResult sel;
     if (ringp) {
-      auto keyf = [&](int i) { return mono_key(pooled64[i]); };
+      auto keyf = [&](int i) { return pooled[i]; };
       sel = block_bottom_k(n, k, 64, keyf, posf, candf, sh_hist, sh_misc);
       auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
-      vcount = lane_remove(L, n, plain_victims(isv), vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx,
-                           sh_rows);
+      vcount = lane_remove(L, n, plain_victims(isv), vout, nullptr, &dead, dm.P, A.ws.status, sh_scan);
     } else {
       auto keyf = [&](int i) { return mono_key(L.score[i]); };
       sel = block_bottom_k(n, k, 32, keyf, posf, candf, sh_hist, sh_misc);
       auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
-      vcount = lane_remove(L, n, plain_victims(isv), vout, nullptr, &dead, dm.P, A.ws.status, sh_scan, sh_idx,
-                           sh_rows);
+      vcount = lane_remove(L, n, plain_victims(isv), vout, nullptr, &dead, dm.P, A.ws.status, sh_scan);
     }
   }
   const int m = n - vcount;
@@ -732,6 +1027,8 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
     KT* vp = static_cast<KT*>(A.ls.v_pool);
     copy_row(kp + static_cast<size_t>(best) * d, static_cast<const KT*>(A.k_new) + static_cast<size_t>(l) * d, d);
     copy_row(vp + static_cast<size_t>(best) * d, static_cast<const KT*>(A.v_new) + static_cast<size_t>(l) * d, d);
+    if (L.ring)
+      for (int t = tid; t < W; t += blockDim.x) L.ring[static_cast<size_t>(best) * W + t] = 0.f;
     if (tid == 0) atomicOr(&L.mask[best >> 4], 1 << (best & 15));
   }
   if (tid == 0) {
@@ -742,8 +1039,6 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
     if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
     A.n_victims[l] = vcount;
   }
-  if (L.ring)
-    for (int t = tid; t < W; t += blockDim.x) L.ring[static_cast<size_t>(m) * W + t] = 0.f;
   __syncthreads();
 
   // ---- relocation plan ---------------------------------------------------------
@@ -870,7 +1165,7 @@ __global__ void __launch_bounds__(1024) allocate_kernel(LayerState ls, Workspace
 // apply: one CTA per lane
 // ---------------------------------------------------------------------------
 template <typename KT>
-__global__ void __launch_bounds__(kApplyThreads) apply_kernel(LayerState ls, Workspace ws, Dims dm,
+__global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(LayerState ls, Workspace ws, Dims dm,
                                                            const void* k_new, const void* v_new,
                                                            int mark_freed, int32_t* moves) {
   __shared__ int sh_scan[40];
@@ -892,6 +1187,8 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(LayerState ls, Wor
     const size_t s = static_cast<size_t>(blk) * kBlock;
     copy_row(kp + s * d, static_cast<const KT*>(k_new) + static_cast<size_t>(l) * d, d);
     copy_row(vp + s * d, static_cast<const KT*>(v_new) + static_cast<size_t>(l) * d, d);
+    if (L.ring)
+      for (int t = tid; t < L.W; t += blockDim.x) L.ring[s * L.W + t] = 0.f;
     if (tid == 0) {
       L.mask[blk] = 1;
       L.slot[m - 1] = blk * kBlock;
@@ -973,6 +1270,7 @@ __global__ void __launch_bounds__(kApplyThreads) apply_kernel(LayerState ls, Wor
         for (int u = 0; u < kCopyBatch; ++u)
           if (dst[u]) *reinterpret_cast<uint4*>(dst[u]) = v[u];
       }
+      if (L.ring) move_history_rows(L.ring, L.W, sh_mv_src, sh_mv_dst, tot);
       __syncthreads();
       q_total += tot;
     }
@@ -1024,19 +1322,22 @@ cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, 
   // the last step's apply, whose epilogue may still be writing that layer's
   // tables, which this kernel reads before its dependency wait.
   const bool pdl = has_q || ctx.last_layer != layer;
+  const bool ring = ctx.dims.policy != KVEVICT_H2O;
+  const dim3 grid(ctx.dims.lanes), block(kEpiThreads);
   if (ctx.dims.dtype == KVEVICT_BF16)
-    return launch_k(decode_epilogue_kernel<__nv_bfloat16>, dim3(ctx.dims.lanes), dim3(kEpiThreads), kEpiDynSmem,
-                    stream, pdl, A);
-  return launch_k(decode_epilogue_kernel<float>, dim3(ctx.dims.lanes), dim3(kEpiThreads), kEpiDynSmem, stream,
-                  pdl, A);
+    return ring ? launch_k(decode_epilogue_kernel<__nv_bfloat16, true>, grid, block, kEpiDynSmem, stream, pdl, A)
+                : launch_k(decode_epilogue_kernel<__nv_bfloat16, false>, grid, block, kEpiDynSmem, stream, pdl, A);
+  return ring ? launch_k(decode_epilogue_kernel<float, true>, grid, block, kEpiDynSmem, stream, pdl, A)
+              : launch_k(decode_epilogue_kernel<float, false>, grid, block, kEpiDynSmem, stream, pdl, A);
 }
 
 cudaError_t prepare_epilogue() {
-  cudaError_t e = cudaFuncSetAttribute(decode_epilogue_kernel<__nv_bfloat16>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kEpiDynSmem));
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(decode_epilogue_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(kEpiDynSmem));
+  const int bytes = static_cast<int>(kEpiDynSmem);
+  const cudaFuncAttribute a = cudaFuncAttributeMaxDynamicSharedMemorySize;
+  cudaError_t e = cudaFuncSetAttribute(decode_epilogue_kernel<__nv_bfloat16, false>, a, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_kernel<__nv_bfloat16, true>, a, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_kernel<float, false>, a, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_kernel<float, true>, a, bytes);
   return e;
 }
 

@@ -65,8 +65,8 @@ struct Workspace {
   float* part_o_buf[2];            // [lanes][kMaxSeg][g][d]
   float* part_ml_buf[2];           // [lanes][kMaxSeg][g][2]  (max, sum), base 2
   int32_t* lane_nseg_buf[2];       // [lanes]
-  double* keys64;                  // [lanes][cap]  SnapKV window sums
-  double* pooled64;                // [lanes][cap]  SnapKV pooled keys
+  unsigned long long* keys64;      // [lanes][cap]  window sums (monotone images), when not in shared memory
+  unsigned long long* pooled64;    // [lanes][cap]  pooled keys (monotone images), several victims
   int32_t* need_admit;             // [lanes]
   int32_t* want_dst;               // [lanes]
   int32_t* admit_block;            // [lanes]
@@ -88,7 +88,6 @@ struct Workspace {
   int32_t* cmp_pos;                // [lanes][cap]  forced compaction: survivors of each CTA's range,
   int32_t* cmp_slot;               //               compacted at the range start
   float* cmp_score;                // [lanes][cap]
-  float* cmp_ring;                 // [lanes][cap][W]  history rows of the survivors (ring policies)
   int32_t* cmp_cnt;                // [lanes][cmp_ctas_per_lane + 1]  survivors per CTA, entries before
 };
 
@@ -187,6 +186,13 @@ __device__ __forceinline__ uint32_t smem_u32(const void* p) {
 }
 
 __device__ __forceinline__ void set_status(uint32_t* st, uint32_t bits) { atomicOr(st, bits); }
+
+// 4-byte asynchronous global -> shared copies (completion: cp_async_wait_all)
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
 
 // mbarrier and bulk-copy (TMA, untiled) primitives
 __device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {

@@ -9,7 +9,8 @@
 namespace kve {
 
 struct LaneRefs {
-  int32_t* pos; int32_t* slot; float* score; float* ring;   // lane slices
+  int32_t* pos; int32_t* slot; float* score;                // lane slices
+  float* ring;                                              // layer: history row per slot
   int32_t* blocks; int32_t* nblocks;                        // lane block list
   int32_t* owner; int32_t* mask;                            // layer pool
   int W;
@@ -21,7 +22,7 @@ __device__ __forceinline__ LaneRefs lane_refs(const LayerState& ls, const Dims& 
   r.pos = ls.pos + off;
   r.slot = ls.slot + off;
   r.score = ls.score ? ls.score + off : nullptr;
-  r.ring = ls.ring ? ls.ring + off * dm.W : nullptr;
+  r.ring = ls.ring;
   r.blocks = ls.lane_blocks + off;
   r.nblocks = ls.lane_nblocks + l;
   r.owner = ls.owner;
@@ -47,11 +48,12 @@ __device__ __forceinline__ PlainVictims<F> plain_victims(F f) { return PlainVict
 // held one before) is released (owner -1) and, if freed_flag is given,
 // flagged.  is_victim.prepare(base) runs on every thread at the start of each
 // chunk of blockDim entries, before any entry of the chunk is tested.
-// Returns the number of victims.  sh_scan: 40 ints, sh_idx: blockDim ints.
+// Returns the number of victims.  sh_scan: 40 ints.  History rows stay at
+// their slots.
 template <typename VictimFn>
 __device__ __forceinline__ int lane_remove(const LaneRefs& L, int n, VictimFn is_victim, int32_t* vout,
                            int32_t* freed_flag, int* n_dead, int P, uint32_t* status,
-                           int* sh_scan, int* sh_idx, float* sh_rows) {
+                           int* sh_scan) {
   int kept_total = 0, vict_total = 0;
   for (int base = 0; base < n; base += blockDim.x) {
     is_victim.prepare(base);
@@ -72,7 +74,6 @@ __device__ __forceinline__ int lane_remove(const LaneRefs& L, int n, VictimFn is
     const int kex = ex2 & 0xFFFF, vex = ex2 >> 16;
     const int ktot = tot2 & 0xFFFF, vtot = tot2 >> 16;
     const int ni = kept_total + kex;
-    sh_idx[threadIdx.x] = keep ? ni : -1;
     // every read of this chunk happened before the scans' barriers
     if (keep) {
       L.pos[ni] = p;
@@ -88,22 +89,6 @@ __device__ __forceinline__ int lane_remove(const LaneRefs& L, int n, VictimFn is
       }
     }
     __syncthreads();
-    if (L.ring) {
-      // move history rows of survivors: read a group of rows, barrier, write
-      const int W = L.W;
-      const int cnt = min(static_cast<int>(blockDim.x), n - base);
-      for (int g0 = 0; g0 < cnt; g0 += 128) {
-        const int rows = min(128, cnt - g0);
-        for (int e = threadIdx.x; e < rows * W; e += blockDim.x)
-          sh_rows[e] = L.ring[static_cast<size_t>(base + g0) * W + e];
-        __syncthreads();
-        for (int e = threadIdx.x; e < rows * W; e += blockDim.x) {
-          const int dst = sh_idx[g0 + e / W];
-          if (dst >= 0) L.ring[static_cast<size_t>(dst) * W + e % W] = sh_rows[e];
-        }
-        __syncthreads();
-      }
-    }
     kept_total += ktot;
     vict_total += vtot;
   }
@@ -152,12 +137,28 @@ __device__ __forceinline__ int block_argmin3(unsigned long long bk, uint32_t bp,
   return bi;
 }
 
+// History rows (ring policies) of tot moved tokens, W floats each, from
+// slot src[j] to slot dst[j] (src -1: not moved).  Destinations are fresh
+// blocks, never a source of the same plan, so each row is read before any
+// write can reach it.
+__device__ __forceinline__ void move_history_rows(float* ring, const int W, const int* src, const int* dst,
+                                                  const int tot) {
+  // a warp per row
+  const int lane = threadIdx.x & 31, nw = blockDim.x >> 5;
+  for (int j = threadIdx.x >> 5; j < tot; j += nw) {
+    const int so = src[j];
+    if (so < 0) continue;
+    const size_t a = static_cast<size_t>(so) * W, b = static_cast<size_t>(dst[j]) * W;
+    for (int t = lane; t < W; t += 32) ring[b + t] = ring[a + t];
+  }
+}
+
 // Removes the single entry v (the step's only victim): its position goes to
 // vout[0], its live bit clears (an emptied block is released and dropped
 // from the lane's block list by swapping in the last entry), and entries
 // v+1 .. n-1 shift down by one.  Returns 1 if a block was released.
 __device__ __forceinline__ int lane_remove_one(const LaneRefs& L, int n, int v, int32_t* vout, int P,
-                                               uint32_t* status, int* sh_b, float* sh_rows) {
+                                               uint32_t* status, int* sh_b) {
   if (threadIdx.x == 0) {
     const int s = L.slot[v];
     vout[0] = L.pos[v];
@@ -190,16 +191,6 @@ __device__ __forceinline__ int lane_remove_one(const LaneRefs& L, int n, int v, 
       L.pos[i - 1] = p;
       L.slot[i - 1] = s;
       if (L.score) L.score[i - 1] = sc;
-    }
-  }
-  if (L.ring) {
-    const int W = L.W;
-    for (int base = v + 1; base < n; base += 128) {
-      const int rows = min(128, n - base);
-      __syncthreads();
-      for (int e = threadIdx.x; e < rows * W; e += blockDim.x) sh_rows[e] = L.ring[static_cast<size_t>(base) * W + e];
-      __syncthreads();
-      for (int e = threadIdx.x; e < rows * W; e += blockDim.x) L.ring[static_cast<size_t>(base - 1) * W + e] = sh_rows[e];
     }
   }
   __syncthreads();

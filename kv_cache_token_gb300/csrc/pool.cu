@@ -79,9 +79,12 @@ __global__ void __launch_bounds__(kThreads) prefill_fill_kernel(LayerState ls, W
     if (ls.score) ls.score[lo + i] = 0.f;
   }
   if (ls.ring) {
-    float* r = ls.ring + lo * dm.W;
-    for (size_t e = static_cast<size_t>(t0) * dm.W + threadIdx.x; e < static_cast<size_t>(t1) * dm.W; e += blockDim.x)
-      r[e] = 0.f;
+    // empty histories, at the tokens' slots
+    for (int e = threadIdx.x; e < (t1 - t0) * dm.W; e += blockDim.x) {
+      const int i = t0 + e / dm.W, t = e % dm.W;
+      const int blk = ws.alloc_ids[l * need + i / kBlock];
+      ls.ring[(static_cast<size_t>(blk) * kBlock + i % kBlock) * dm.W + t] = 0.f;
+    }
   }
   const int vec = 16 / sizeof(KT);               // elements per 16-byte piece
   const int per_row = dm.d / vec;
@@ -291,7 +294,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelClThre
 // first and last entry; extra positions match nothing, as in the oracle's
 // membership test), stages it in shared memory when it fits, tests each
 // entry by binary search, clears the victims' live bits and writes its
-// survivors (with their history rows, for the ring policies), in order, to
+// survivors, in order, to
 // scratch at the range start, with their count.
 // compact_place_kernel: each CTA copies its survivors to their final index
 // (the counts of the lane's earlier CTAs before it; the lane's entry count
@@ -335,7 +338,6 @@ __global__ void __launch_bounds__(kCmpThreads) compact_remove_kernel(LayerState 
                                                                     const int32_t* n_victims, int cpl) {
   __shared__ int sh_vic[kCmpStage];
   __shared__ int sh_scan[40];
-  __shared__ int sh_src[kCmpThreads];
   __shared__ int sh_v0, sh_v1;
   const int l = blockIdx.y, c = blockIdx.x, tid = threadIdx.x;
   LaneRefs L = lane_refs(ls, dm, l);
@@ -388,7 +390,6 @@ __global__ void __launch_bounds__(kCmpThreads) compact_remove_kernel(LayerState 
       ws.cmp_pos[o] = p;
       ws.cmp_slot[o] = sl;
       ws.cmp_score[o] = sc;
-      if (L.ring) sh_src[ex2 & 0xFFFF] = i;
     }
     if (isv) {
       if (sl >= 0 && sl < dm.P * kBlock) {
@@ -396,15 +397,6 @@ __global__ void __launch_bounds__(kCmpThreads) compact_remove_kernel(LayerState 
       } else if (sl >= 0) {
         set_status(ws.status, ST_BAD_INDEX);
       }
-    }
-    if (L.ring) {
-      // the chunk's survivors' history rows, W floats each, to scratch
-      __syncthreads();
-      const int W = L.W, kept = tot2 & 0xFFFF;
-      float* dst = ws.cmp_ring + (lo_off + s + kept_total) * W;
-      for (int e2 = tid; e2 < kept * W; e2 += blockDim.x)
-        dst[e2] = L.ring[static_cast<size_t>(sh_src[e2 / W]) * W + e2 % W];
-      __syncthreads();
     }
     kept_total += tot2 & 0xFFFF;
     vict_total += tot2 >> 16;
@@ -440,11 +432,6 @@ __global__ void __launch_bounds__(kCmpThreads) compact_place_kernel(LayerState l
     L.pos[off + j] = ws.cmp_pos[lo_off + s + j];
     L.slot[off + j] = ws.cmp_slot[lo_off + s + j];
     if (L.score) L.score[off + j] = ws.cmp_score[lo_off + s + j];
-  }
-  if (L.ring) {
-    const size_t W = L.W;
-    for (size_t e = tid; e < static_cast<size_t>(mine) * W; e += blockDim.x)
-      L.ring[static_cast<size_t>(off) * W + e] = ws.cmp_ring[(lo_off + s) * W + e];
   }
 }
 
@@ -568,7 +555,7 @@ __global__ void __launch_bounds__(kCmpThreads) compact_reloc_count_kernel(LayerS
 }
 
 template <typename KT>
-__global__ void __launch_bounds__(kCmpThreads) compact_reloc_move_kernel(LayerState ls, Workspace ws, Dims dm,
+__global__ void __launch_bounds__(kCmpThreads, 1) compact_reloc_move_kernel(LayerState ls, Workspace ws, Dims dm,
                                                                         int cpl, int32_t* moves) {
   constexpr int kBatch = 8;
   __shared__ int sh_scan[40];
@@ -648,6 +635,7 @@ __global__ void __launch_bounds__(kCmpThreads) compact_reloc_move_kernel(LayerSt
       for (int u = 0; u < kBatch; ++u)
         if (dst[u]) *reinterpret_cast<uint4*>(dst[u]) = v[u];
     }
+    if (L.ring) move_history_rows(L.ring, L.W, sh_src, sh_dst, tot);
     __syncthreads();
     q_run += tot;
   }

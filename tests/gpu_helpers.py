@@ -76,7 +76,7 @@ def gpu_state(eng, layer):
         n = int(counts[l])
         s = slots[l, :n]
         st["lanes"].append(dict(pos=pos[l, :n], slot=s, score=scores[l, :n],
-                                hist=None if ring is None else ring[l, :n],
+                                hist=None if ring is None else ring[s],
                                 blocks=set(lb[l, :nb[l]].tolist()), K=K[s], V=V[s]))
     return st
 

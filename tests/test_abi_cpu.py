@@ -73,7 +73,7 @@ def test_sizes(lib):
     sz = lambda w: lib.kvevict_buffer_size(ctypes.byref(c), w)
     assert sz(binding.BUF_K_POOL) == P * 16 * 128 * 2
     assert sz(binding.BUF_POSITIONS) == lanes * C * 4
-    assert sz(binding.BUF_RING) == lanes * C * 32 * 4
+    assert sz(binding.BUF_RING) == P * 16 * 32 * 4      # a history row per slot
     assert sz(binding.BUF_STATS) == binding.NSTATS * 8
     assert sz(binding.BUF_WORKSPACE) == lib.kvevict_workspace_size(ctypes.byref(c)) > 0
     assert sz(binding.BUF_RING) > 0

@@ -73,7 +73,8 @@ def run_sampled_decode(shp, lanes, steps):
             if shp.policy == 0:
                 assert_scores_close(eng.scores[0, lane, :n].cpu().numpy(), L.score, "step %d lane %d scores" % (t, lane))
             else:
-                assert_scores_close(eng.ring[0, lane, :n].cpu().numpy().ravel(), L.hist.ravel(),
+                slots = eng.slots[0, lane, :n].long()
+                assert_scores_close(eng.ring[0][slots].cpu().numpy().ravel(), L.hist.ravel(),
                                     "step %d lane %d history" % (t, lane))
     assert eng.last_error()[0] == 0
     assert len(live) >= len(lanes) // 2, "too many near-tie swaps: %d" % swaps
