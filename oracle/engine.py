@@ -28,7 +28,7 @@ compaction are the other calls.
 import numpy as np
 
 from . import h2o, snapkv
-from .attention import decode_attention
+from .attention import causal_attention, decode_attention
 from .dropkv import decode_scores, window_scores
 from .paged import PagedLayer
 from .select import select_lane
@@ -153,6 +153,38 @@ class Engine:
             a[b, h * g:(h + 1) * g] = aa.reshape(g, w, c.head_dim)
             scores[lane] = sc
         return dict(lse=lse, a=a, scores=scores)
+
+    def score_mass(self, layer, q_win, q_pos, kind, lanes=None):
+        """Prefill-window attention mass of each kept token (no values).
+
+        kind SNAPKV: the one-shot SnapKV prefill keys (window sums over the
+        rows that see the token, pooled with pool_kernel); kind H2O: the
+        causal-prefill cumulative scores (rows strictly after the token).
+        q_win [B, Hq, w, d]; q_pos [w].  Returns dict(lse [B, Hq, w],
+        scores: list per lane); q_win None is inert (returns None)."""
+        c = self.cfg
+        PL = self.layers[layer]
+        g = self.g
+        if q_win is None:
+            return None
+        w = q_win.shape[2]
+        lse = np.zeros((c.batch, c.num_q_heads, w))
+        scores = {}
+        for lane in (range(self.n_lanes) if lanes is None else lanes):
+            b, h = divmod(lane, c.num_kv_heads)
+            L = PL.lanes[lane]
+            K, V = PL.rows(lane)
+            rows = np.asarray(q_win[b, h * g:(h + 1) * g], np.float64).reshape(g * w, c.head_dim)
+            qp = np.tile(np.asarray(q_pos, np.int64), g)
+            _, ls, p = causal_attention(rows, qp, K, V, L.pos)
+            lse[b, h * g:(h + 1) * g] = ls.reshape(g, w)
+            if kind == SNAPKV:
+                scores[lane] = snapkv.prefill_keys(p, qp, L.pos, c.pool_kernel)
+            elif kind == H2O:
+                scores[lane] = h2o.prefill_scores(p, qp, L.pos)
+            else:
+                raise ValueError("kind must be SNAPKV or H2O")
+        return dict(lse=lse, scores=scores)
 
     def compact(self, layer, victims):
         """Forced compaction: evict ``victims`` (list per lane of positions),

@@ -37,3 +37,21 @@ def cumulative_scores_from_rows(A):
         for t in range(j + 1, R):
             S[j] += np.sum(A[:, t, j])
     return S
+
+
+def prefill_scores(p, q_pos, kpos):
+    """Causal-prefill initialisation of the cumulative scores: S_j = sum over
+    the prompt query rows t at positions after j of A[t, j] (the score
+    equation sums t >= j + 1: a token's weight on itself is not counted).
+
+    p [r, n] are the causal softmax weights of the rows (every query of the
+    window, for every query head of the group) over the kept keys at
+    positions kpos [n]; rows at positions q_pos [r].  With every prompt
+    position in the window this is the equation's S_j after the prompt; with
+    the last w positions only, it is that sum restricted to those rows."""
+    p = np.asarray(p, dtype=np.float64)
+    later = np.asarray(kpos)[None, :] < np.asarray(q_pos)[:, None]
+    S = np.zeros(p.shape[1], dtype=np.float64)
+    for t in range(p.shape[0]):
+        S = S + np.where(later[t], p[t], 0.0)
+    return S

@@ -67,3 +67,27 @@ def validate(budget, recent_window, obs_window, pool_kernel):
     if obs_window == 0:
         return "obs_window_zero"
     return None
+
+
+def prefill_sums(p, q_pos, kpos):
+    """SnapKV as the paper runs it ("On the adaptation"): one shot over a
+    prompt, the attention the last few prompt queries pay to each key.
+
+    p [r, n] are the causal softmax weights of every (window query, query
+    head of the group) row over the kept keys at positions kpos [n], rows at
+    positions q_pos [r] (a row gives weight 0 to keys after it).  Returns
+    sums[j] = sum over rows of p[row, j], accumulated in float64 row by row
+    in row order.  These are the window sums of the prefill observation."""
+    p = np.asarray(p, dtype=np.float64)
+    vis = np.asarray(kpos)[None, :] <= np.asarray(q_pos)[:, None]
+    s = np.zeros(p.shape[1], dtype=np.float64)
+    for i in range(p.shape[0]):
+        s = s + np.where(vis[i], p[i], 0.0)
+    return s
+
+
+def prefill_keys(p, q_pos, kpos, pool_kernel):
+    """Eviction keys of the one-shot prefill selection: the prefill window
+    sums, max-pooled over kept neighbours with the same clamped window as the
+    decode-time keys ("How it works")."""
+    return max_pool(prefill_sums(p, q_pos, kpos), pool_kernel)

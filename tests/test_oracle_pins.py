@@ -114,6 +114,109 @@ def test_h2o_boosted_token_survives():
     E.layers[0].check_invariants()
 
 
+def _equal_key_prompt(n, g, w, d=8):
+    """A prompt whose keys are all equal: every query spreads its weight
+    evenly over the keys it sees.  Rows are (head, window position) for the
+    last w positions of n, every head's query random (the logits stay equal)."""
+    rng = np.random.default_rng(7)
+    K = np.tile(rng.standard_normal(d), (n, 1))
+    q = rng.standard_normal((g * w, d))
+    qpos = np.tile(np.arange(n - w, n), g)
+    kpos = np.arange(n)
+    _, _, p = attention.causal_attention(q, qpos, K, K, kpos)
+    return p, qpos, kpos
+
+
+def test_h2o_prefill_scores_closed_form():
+    """Causal-prefill S_j with equal keys: the row at position t gives
+    1/(t+1) to each of tokens 0..t, and S_j counts rows t >= j+1 only, so
+    S_j = g (h_n - h_{j+1}) over a whole-prompt window (h: harmonic numbers),
+    and every row's weight is counted except its own diagonal entry."""
+    n, g = 11, 3
+    p, qpos, kpos = _equal_key_prompt(n, g, n)
+    S = h2o.prefill_scores(p, qpos, kpos)
+    harm = lambda m: sum(1.0 / i for i in range(1, m + 1))
+    np.testing.assert_allclose(S, [g * (harm(n) - harm(j + 1)) for j in range(n)], rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(S.sum(), g * n - g * sum(1.0 / (t + 1) for t in range(n)), rtol=1e-13)
+    # the same S_j as the decode-time accumulation over the same queries
+    # (the H2O Guide's step-by-step rule run over the prompt)
+    A = np.zeros((g, n, n))
+    for t in range(n):
+        A[:, t, : t + 1] = 1.0 / (t + 1)
+    np.testing.assert_allclose(S, h2o.cumulative_scores_from_rows(A), rtol=1e-13, atol=1e-15)
+
+
+def test_h2o_prefill_scores_random_against_sdpa_weights():
+    """Random keys: S_j equals the column sums, over rows strictly after j,
+    of torch's causal softmax (its own masked softmax, float64)."""
+    rng = np.random.default_rng(8)
+    n, d, g = 40, 16, 2
+    K = rng.standard_normal((n, d))
+    q = rng.standard_normal((g, n, d))
+    mask = torch.tril(torch.ones(n, n, dtype=torch.bool))
+    logits = torch.tensor(q) @ torch.tensor(K).T / math.sqrt(d)
+    P = torch.softmax(logits.masked_fill(~mask, float("-inf")), dim=-1).numpy()
+    strict = np.tril(np.ones((n, n)), -1)
+    ref = (P * strict).sum(axis=(0, 1))
+    qpos = np.tile(np.arange(n), g)
+    _, _, p = attention.causal_attention(q.reshape(g * n, d), qpos, K, K, np.arange(n))
+    np.testing.assert_allclose(h2o.prefill_scores(p, qpos, np.arange(n)), ref, rtol=1e-12, atol=1e-14)
+
+
+def test_snapkv_prefill_sums_closed_form_and_mass():
+    """SnapKV prefill observation with equal keys: sums_j = g * sum over the
+    window positions t >= j of 1/(t+1); every row sums to one, so the sums
+    add up to the number of rows; poolKernel 1 leaves them unchanged."""
+    n, g, w = 30, 4, 6
+    p, qpos, kpos = _equal_key_prompt(n, g, w)
+    sums = snapkv.prefill_sums(p, qpos, kpos)
+    ref = [g * sum(1.0 / (t + 1) for t in range(max(j, n - w), n)) for j in range(n)]
+    np.testing.assert_allclose(sums, ref, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(sums.sum(), g * w, rtol=1e-13)
+    np.testing.assert_array_equal(snapkv.prefill_keys(p, qpos, kpos, 1), sums)
+
+
+def test_snapkv_prefill_one_row_is_last_query_softmax():
+    """A window of one query of one head: the keys are that query's softmax
+    weights (the SnapKV page's TOVA reduction, at prefill), checked against
+    torch.softmax; pooled with r = 1 they match a hand-clamped max."""
+    rng = np.random.default_rng(9)
+    n, d = 25, 16
+    K = rng.standard_normal((n, d))
+    q = rng.standard_normal((1, d))
+    _, _, p = attention.causal_attention(q, np.array([n - 1]), K, K, np.arange(n))
+    ref = torch.softmax(torch.tensor(q @ K.T / math.sqrt(d))[0], dim=0).numpy()
+    keys1 = snapkv.prefill_keys(p, np.array([n - 1]), np.arange(n), 1)
+    np.testing.assert_allclose(keys1, ref, rtol=1e-12)
+    keys3 = snapkv.prefill_keys(p, np.array([n - 1]), np.arange(n), 3)
+    hand = [max(ref[max(0, j - 1): j + 2]) for j in range(n)]
+    np.testing.assert_allclose(keys3, hand, rtol=1e-12)
+
+
+def test_engine_score_mass_dispatch():
+    """Engine.score_mass: SnapKV keys are the pooled window sums of the kept
+    tokens, H2O scores count only rows after the token; a null window is
+    inert."""
+    rng = np.random.default_rng(10)
+    cfg = _cfg(policy=SNAPKV, obs_window=4, pool_kernel=3, num_q_heads=2)
+    E = Engine(cfg)
+    n, d, w = 20, cfg.head_dim, 5
+    K = rng.standard_normal((1, 1, n, d)).astype(np.float32).astype(np.float64)   # the table stores fp32
+    E.prefill(0, K, rng.standard_normal((1, 1, n, d)))
+    qw = rng.standard_normal((1, 2, w, d))
+    qp = np.arange(n - w, n)
+    rows = qw[0].reshape(2 * w, d)
+    _, _, p = attention.causal_attention(rows, np.tile(qp, 2), K[0, 0], K[0, 0], np.arange(n))
+    snap = E.score_mass(0, qw, qp, SNAPKV)["scores"][0]
+    h2 = E.score_mass(0, qw, qp, H2O)["scores"][0]
+    vis = np.arange(n)[None, :] <= np.tile(qp, 2)[:, None]
+    later = np.arange(n)[None, :] < np.tile(qp, 2)[:, None]
+    sums = (p * vis).sum(axis=0)
+    np.testing.assert_allclose(snap, [sums[max(0, j - 1): j + 2].max() for j in range(n)], rtol=1e-13)
+    np.testing.assert_allclose(h2, (p * later).sum(axis=0), rtol=1e-13, atol=1e-16)
+    assert E.score_mass(0, None, qp, SNAPKV) is None
+
+
 # --------------------------------------------------------------------------
 # SnapKV
 # --------------------------------------------------------------------------

@@ -29,6 +29,14 @@ Workloads (shapes from the task's five configs; the constructions marked
    64 decode steps.
 5. paged_128k: as 3 with context 131072 (8192 blocks per lane), keep
    floor(5%) = 6553, then forced compaction.
+6. snapkv_prefill / snapkv_prefill_128k (SnapKV's own one-shot prefill
+   selection, which the SnapKV page describes; sizes chosen): B=1, Hq=32,
+   Hkv=8, d=128, bf16, context 32768 / 131072; keys and planted runs as in 2
+   (40 runs per 4096 tokens); the last 32 prompt positions are the
+   observation window (the H2O Guide's "last 32 prompt tokens"), their
+   queries q* + N(0,I) as in 2's decode queries; poolKernel 7; keep 1/16 of
+   the prompt (2048 / 8192, the H2O Guide's 64,000 -> 4,000 ratio) with the
+   window protected.
 """
 import dataclasses
 import math
@@ -103,6 +111,10 @@ SHAPES = {
                      3276, 1638, 1, 1, seed=4),
     "paged_128k": Shape("paged_128k", DROPKV, 1, 1, 32, 8, 128, "bf16", 131072, 0,
                         6553, 64, 1, 1, seed=5, window=64, kind="prefill"),
+    "snapkv_prefill": Shape("snapkv_prefill", SNAPKV, 1, 1, 32, 8, 128, "bf16", 32768, 0,
+                            2048, 32, 32, 7, seed=6, window=32, kind="prefill"),
+    "snapkv_prefill_128k": Shape("snapkv_prefill_128k", SNAPKV, 1, 1, 32, 8, 128, "bf16", 131072, 0,
+                                 8192, 32, 32, 7, seed=7, window=32, kind="prefill"),
 }
 
 
@@ -245,5 +257,8 @@ class Workload:
         """(q_win [B, Hq, w, d], q_pos [w] int32): the last w prompt positions."""
         s = self.s
         q = self._randn((s.batch, s.num_q_heads, s.window, s.head_dim), "win_q", layer, 0, device)
+        if s.name.startswith("snapkv"):
+            _, qstar = self._direction(layer, device)
+            q = q + qstar.repeat_interleave(s.group, dim=1)[:, :, None, :]
         pos = torch.arange(s.ctx - s.window, s.ctx, dtype=torch.int32, device=device)
         return self._store(q), pos
