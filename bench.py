@@ -50,7 +50,8 @@ def parse():
                          "32K and 128K, selection, forced compaction, the SnapKV and toy decode steps), one "
                          "JSON line each, instead of the decode-step bench line")
     ap.add_argument("--only", default="",
-                    help="with --kernel-table: comma-separated subset of d3_32k, d3_128k, snapkv, dropkv_decode, toy")
+                    help="with --kernel-table: comma-separated subset of d3_32k, d3_128k, snapkv_pf_32k, "
+                         "snapkv_pf_128k, snapkv, dropkv_decode, toy")
     return ap.parse_args()
 
 
@@ -598,6 +599,38 @@ def run_kernel_table(args):
             emit("D5 token-level compaction (plan, allocate, gather, release)", name, samples[1], samples[0],
                  samples[-1], nbytes=moved * 2 * d * 2 * 2 + int(nvic.sum().item()) * 3 * 4,
                  extra={"moved_tokens": moved, "freed_blocks": nf, "blocks_after": st[9], "live_after": st[10]})
+        code, msg = eng.last_error()
+        assert code == 0, msg
+        del eng
+        torch.cuda.empty_cache()
+
+    # SnapKV's one-shot prefill selection: window attention mass (K read in
+    # both passes, no V), pooled keys, bottom-k at 1/16 of the prompt
+    for tag, name in (("snapkv_pf_32k", "snapkv_prefill"), ("snapkv_pf_128k", "snapkv_prefill_128k")):
+        if only and tag not in only:
+            continue
+        shp = shape(name)
+        wl = Workload(shp)
+        eng = Engine(config_from(shp))
+        eng.reset()
+        K, V = wl.context(0, device="cuda")
+        eng.prefill(0, K, V)
+        del K, V
+        q, qp = wl.window(0, device="cuda")
+        lanes, w, g, d, n = eng.lanes, shp.window, shp.group, shp.head_dim, shp.ctx
+        lse = torch.empty((shp.batch, shp.num_q_heads, w), dtype=torch.float32, device="cuda")
+        scores = torch.zeros((lanes, shp.max_tokens), dtype=torch.float32, device="cuda")
+        ms, p10, p90 = timed(lambda: eng.score_mass(0, q, qp, 0, lse, scores), reps=10)
+        rows = g * w
+        emit("SnapKV prefill keys (LSE pass, attention-mass pass, pooling)", name, ms, p10, p90,
+             nbytes=2 * lanes * n * d * 2 + lanes * n * 4, flops=2 * 2 * lanes * rows * n * d)
+        pos, cnt = eng.positions[0], eng.counts[0]
+        victims = torch.full((lanes, shp.max_tokens), -1, dtype=torch.int32, device="cuda")
+        nvic = torch.zeros((lanes,), dtype=torch.int32, device="cuda")
+        ms, p10, p90 = timed(lambda: eng.select(scores, pos, cnt, shp.budget, shp.recent_window, victims, nvic),
+                             reps=10)
+        emit("D4 bottom-k selection (radix descent on (key, position))", name, ms, p10, p90,
+             nbytes=lanes * n * (4 + 4))
         code, msg = eng.last_error()
         assert code == 0, msg
         del eng

@@ -247,6 +247,35 @@ kvevict_status kvevict_score(kvevict_ctx* ctx, int layer, const void* q_win, int
                              const int32_t* q_pos, float* lse, float* a_out, float* scores,
                              void* stream);
 
+/* Prefill-window attention mass of one layer: how much attention the last w
+ * prompt queries pay to each kept token, values unused.  q_win [B][Hq][w][d]
+ * (kv_dtype, device, 16-byte aligned) at positions q_pos[w] (int32, device);
+ * every row attends the lane's kept tokens at positions <= its own (causal
+ * softmax, p_ij = exp(s_ij - LSE_i)).  Writes lse [B][Hq][w] (fp32, natural
+ * log) and, per lane, scores[lane][j] (fp32, [B*Hkv][max_tokens], kept
+ * order):
+ *   KVEVICT_MASS_SNAPKV  (SnapKV, "On the adaptation": the paper compresses a
+ *       prompt once from the attention its last few queries pay to each key,
+ *       then pools and selects; "How it works" for the pooling)
+ *       sums_j = sum over the group's rows with key position <= row position
+ *       of p_ij, then scores_j = max of sums over kept indices [j-r, j+r]
+ *       clamped to the lane, r = (pool_kernel - 1) / 2 from the config
+ *       (a NaN sum wins the max);
+ *   KVEVICT_MASS_H2O  (H2O Guide, "Formulating Cumulative Attention Scores":
+ *       S_j sums the rows t >= j + 1) scores_j = sum over the rows with key
+ *       position < row position of p_ij, no pooling.  With every prompt
+ *       position in the window this is the causal-prefill S_j; passing the
+ *       layer's slice of the score table as `scores` starts H2O decoding from
+ *       it.
+ * Sums are fp32 in an unspecified order.  Keep budget tokens with
+ * kvevict_select on these keys and kvevict_compact.  q_win == NULL is inert:
+ * nothing is written.  Needs kv_dtype bf16, head_dim 128 and
+ * g * w <= g * max_window (KVEVICT_E_DTYPE / KVEVICT_E_INVALID_ARG). */
+typedef enum { KVEVICT_MASS_SNAPKV = 0, KVEVICT_MASS_H2O = 1 } kvevict_mass_kind;
+kvevict_status kvevict_score_mass(kvevict_ctx* ctx, int layer, const void* q_win, int32_t w,
+                                  const int32_t* q_pos, int32_t kind, float* lse, float* scores,
+                                  void* stream);
+
 /* Bottom-k selection on given keys.  keys [n_lanes][stride] (fp32 or fp64,
  * device), positions [n_lanes][stride] ascending (int32, device), counts
  * [n_lanes] (int32, device).  Per lane: newest = positions[counts-1];

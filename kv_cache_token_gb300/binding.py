@@ -70,6 +70,7 @@ def lib():
         L.kvevict_attend.argtypes = [V, ctypes.c_int, V, V, V, V]
         L.kvevict_finish_step.argtypes = [V, ctypes.c_int, V, V, V, I, V, V, V, V, V]
         L.kvevict_score.argtypes = [V, ctypes.c_int, V, I, V, V, V, V, V]
+        L.kvevict_score_mass.argtypes = [V, ctypes.c_int, V, I, V, I, V, V, V]
         L.kvevict_attend_static.argtypes = [V, ctypes.c_int, V, V, V, V, V, V]
         L.kvevict_select.argtypes = [V, V, I, V, V, I, I, I, I, V, V, V]
         L.kvevict_compact.argtypes = [V, ctypes.c_int, V, V, V, V, V, V, V]
@@ -77,7 +78,7 @@ def lib():
         L.kvevict_last_error.argtypes = [V, ctypes.c_char_p, ctypes.c_size_t]
         for f in ("validate", "create", "reset", "prefill", "decode_step", "attend", "finish_step",
                   "attend_static",
-                  "score", "select",
+                  "score", "score_mass", "select",
                   "compact", "stats", "last_error"):
             getattr(L, "kvevict_" + f).restype = ctypes.c_int
         _LIB = L
@@ -254,6 +255,24 @@ class Engine:
         _check(lib().kvevict_score(self.h, layer, _ptr(q_win), w, _ptr(q_pos), _ptr(lse), _ptr(a_out),
                                    _ptr(scores), _stream(stream)), "kvevict_score")
         return lse, a_out, scores
+
+    def score_mass(self, layer, q_win, q_pos, kind, lse=None, scores=None, stream=None):
+        """kvevict_score_mass; kind 0 = SnapKV prefill keys, 1 = H2O
+        causal-prefill scores.  Returns (lse, scores) or None for q_win None."""
+        c = self.cfg
+        if q_win is None:
+            _check(lib().kvevict_score_mass(self.h, layer, None, 0, None, kind, None, None, _stream(stream)),
+                   "kvevict_score_mass")
+            return None
+        w = q_win.shape[2]
+        if lse is None:
+            lse = torch.empty((c.batch, c.num_q_heads, w), dtype=torch.float32, device=self.device)
+        if scores is None:
+            scores = torch.zeros((self.lanes, c.max_tokens), dtype=torch.float32, device=self.device)
+        assert q_win.is_contiguous() and q_pos.dtype == torch.int32
+        _check(lib().kvevict_score_mass(self.h, layer, _ptr(q_win), w, _ptr(q_pos), kind, _ptr(lse),
+                                        _ptr(scores), _stream(stream)), "kvevict_score_mass")
+        return lse, scores
 
     def select(self, keys, positions, counts, budget, recent_window, victims=None, n_victims=None,
                stream=None):

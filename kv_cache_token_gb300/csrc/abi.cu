@@ -318,6 +318,21 @@ kvevict_status kvevict_score(kvevict_ctx* ctx, int layer, const void* q_win, int
                                        static_cast<cudaStream_t>(stream)));
 }
 
+kvevict_status kvevict_score_mass(kvevict_ctx* ctx, int layer, const void* q_win, int32_t w, const int32_t* q_pos,
+                                  int32_t kind, float* lse, float* scores, void* stream) {
+  if (!ctx || layer < 0 || layer >= ctx->c.dims.L) return KVEVICT_E_INVALID_ARG;
+  if (kind != KVEVICT_MASS_SNAPKV && kind != KVEVICT_MASS_H2O) return KVEVICT_E_INVALID_ARG;
+  if (!q_win) return KVEVICT_OK;   // null attention is inert
+  if (w < 1 || w > ctx->c.dims.max_window || !q_pos || !lse || !scores) return KVEVICT_E_INVALID_ARG;
+  if (reinterpret_cast<uintptr_t>(q_win) % 16) return KVEVICT_E_INVALID_ARG;   // 16-byte row copies
+  if (ctx->c.dims.dtype != KVEVICT_BF16 || ctx->c.dims.d != 128) return KVEVICT_E_DTYPE;
+  const int pk = ctx->c.cfg.pool_kernel;
+  if (kind == KVEVICT_MASS_SNAPKV && (pk < 1 || pk % 2 == 0)) return KVEVICT_E_POOL_KERNEL_EVEN;
+  const int pool_r = kind == KVEVICT_MASS_SNAPKV && pk > 1 ? (pk - 1) / 2 : -1;
+  return cuda_status(kve::launch_score_mass(ctx->c, layer, q_win, w, q_pos, kind == KVEVICT_MASS_H2O, pool_r, lse,
+                                            scores, static_cast<cudaStream_t>(stream)));
+}
+
 kvevict_status kvevict_select(kvevict_ctx* ctx, const void* keys, int32_t key_dtype, const int32_t* positions,
                               const int32_t* counts, int32_t n_lanes, int32_t stride, int32_t budget,
                               int32_t recent_window, int32_t* victims, int32_t* n_victims, void* stream) {

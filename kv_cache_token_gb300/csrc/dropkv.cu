@@ -70,8 +70,17 @@ struct D3Args {
   const int32_t* qpos;      // [w]
   int w, rows, rows_cap, chunks, chunk_keys;   // chunk_keys: keys per CTA, a multiple of 64
   float* lse_out; float* a_out; float* scores;
+  float* col_out;   // where pass 2 leaves each key's column sum (scores, or scratch ahead of pooling)
   float scale2;
 };
+
+// What pass 2 sums per (row, key):
+//   kResidual  the DropKV term p / (1 - p) ||a - v||, keys at or before the row;
+//   kMassCausal  the weight p, keys at or before the row (SnapKV's prefill
+//                observation: the window rows' attention paid to each key);
+//   kMassLater   the weight p, keys strictly before the row (H2O's
+//                cumulative score, which sums the rows t >= j + 1).
+enum D3Mode { kResidual = 0, kMassCausal = 1, kMassLater = 2 };
 
 // Shared staging of one key tile: K rows, V rows, positions, |v|^2.
 struct Tile {
@@ -81,7 +90,9 @@ struct Tile {
   float vn[kKeyTile];
 };
 
-// Issue the cp.async copies of key tile [j0, j0 + 32) of lane l into t.
+// Issue the cp.async copies of key tile [j0, j0 + 32) of lane l into t
+// (K rows only when kV is false).
+template <bool kV = true>
 __device__ __forceinline__ void load_tile(Tile& t, const D3Args& A, int l, int n, int j0) {
   const __nv_bfloat16* kp = static_cast<const __nv_bfloat16*>(A.ls.k_pool);
   const __nv_bfloat16* vp = static_cast<const __nv_bfloat16*>(A.ls.v_pool);
@@ -91,6 +102,7 @@ __device__ __forceinline__ void load_tile(Tile& t, const D3Args& A, int l, int n
   for (int e = threadIdx.x; e < kKeyTile * 2 * 16; e += blockDim.x) {
     const int key = e >> 5, tens = (e >> 4) & 1, piece = e & 15;
     const int j = j0 + key;
+    if (!kV && tens) continue;
     unsigned char* dst = (tens ? t.v : t.k) + key * kRowStride + piece * 16;
     if (j < n) {
       int s = A.ls.slot[lo + j];
@@ -281,6 +293,8 @@ __global__ void __launch_bounds__(kWarps * 32) d3_pass1_kernel(D3Args A) {
 // (max, sum) in lanes of the warp, then each lane accumulates 4 of the d
 // columns over the chunks.
 // ---------------------------------------------------------------------------
+// kA false: the LSE alone (the chunks' partial outputs were not written).
+template <bool kA>
 __global__ void __launch_bounds__(256) d3_combine_kernel(D3Args A) {
   const int l = blockIdx.y;
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
@@ -304,7 +318,7 @@ __global__ void __launch_bounds__(256) d3_combine_kernel(D3Args A) {
     const float m = c < nch ? base[c * chunk_stride + kD] : -INFINITY;
     const float sc_mine = m == -INFINITY ? 0.f : exp2f(m - M);
     if (c < nch) Lp += base[c * chunk_stride + kD + 1] * sc_mine;
-    const int cnt = min(32, nch - c0);
+    const int cnt = kA ? min(32, nch - c0) : 0;
     const float* bc = base + static_cast<size_t>(c0) * chunk_stride + lane * 4;
 #pragma unroll 8
     for (int u = 0; u < cnt; ++u) {
@@ -322,6 +336,14 @@ __global__ void __launch_bounds__(256) d3_combine_kernel(D3Args A) {
   const float lse2 = M + log2f(Lp);
   const size_t orow = (static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i;
   const size_t wrow = static_cast<size_t>(l) * A.rows_cap + r;
+  if (!kA) {
+    if (lane == 0) {
+      A.lse_out[orow] = lse2 * kLn2;
+      A.ws.d3_rowc[wrow * 2 + 0] = lse2;
+      A.ws.d3_rowc[wrow * 2 + 1] = 0.f;
+    }
+    return;
+  }
   float nrm = 0.f;
   float av[4];
 #pragma unroll
@@ -369,7 +391,9 @@ __device__ __forceinline__ float residual_term(float x, float r2, const float* a
 // ---------------------------------------------------------------------------
 // pass 2
 // ---------------------------------------------------------------------------
+template <int kMode>
 __global__ void __launch_bounds__(kWarps * 32) d3_pass2_kernel(D3Args A) {
+  constexpr bool kRes = kMode == kResidual;
   __shared__ __align__(128) Tile tiles[2];
   __shared__ float colsum[kWarps][kKeyTile];
   const int chunk = blockIdx.x, l = blockIdx.y, rg = blockIdx.z;
@@ -383,8 +407,10 @@ __global__ void __launch_bounds__(kWarps * 32) d3_pass2_kernel(D3Args A) {
   const size_t wbase = static_cast<size_t>(l) * A.rows_cap;
   uint32_t qa[8][4], ah[8][4], al[8][4];
   load_afrag_q(qa, A, b, kh, r0);
-  load_afrag_rows(ah, A.ws.d3_ahi + wbase * kD, A.rows, r0);
-  load_afrag_rows(al, A.ws.d3_alo + wbase * kD, A.rows, r0);
+  if (kRes) {
+    load_afrag_rows(ah, A.ws.d3_ahi + wbase * kD, A.rows, r0);
+    load_afrag_rows(al, A.ws.d3_alo + wbase * kD, A.rows, r0);
+  }
   const int ra = r0 + gq, rb = r0 + gq + 8;
   const bool oka = ra < A.rows, okb = rb < A.rows;
   const int qpa = oka ? A.qpos[ra % A.w] : -1;
@@ -403,16 +429,16 @@ __global__ void __launch_bounds__(kWarps * 32) d3_pass2_kernel(D3Args A) {
   const float* arow_b = arow_of(rb, okb);
 
   const int ntiles = (j_end - j_begin + kKeyTile - 1) / kKeyTile;
-  load_tile(tiles[0], A, l, n, j_begin);
+  load_tile<kRes>(tiles[0], A, l, n, j_begin);
   cp_commit();
   for (int t = 0; t < ntiles; ++t) {
-    if (t + 1 < ntiles) load_tile(tiles[(t + 1) & 1], A, l, n, j_begin + (t + 1) * kKeyTile);
+    if (t + 1 < ntiles) load_tile<kRes>(tiles[(t + 1) & 1], A, l, n, j_begin + (t + 1) * kKeyTile);
     cp_commit();
     cp_wait<1>();
     __syncthreads();
     Tile& T = tiles[t & 1];
     // |v|^2 of the tile's keys (warp 0)
-    if (warp == 0) {
+    if (kRes && warp == 0) {
       const __nv_bfloat16* vr = reinterpret_cast<const __nv_bfloat16*>(T.v + lane * kRowStride);
       float acc = 0.f;
       for (int e = 0; e < kD; ++e) {
@@ -428,8 +454,10 @@ __global__ void __launch_bounds__(kWarps * 32) d3_pass2_kernel(D3Args A) {
       g[nt][0] = g[nt][1] = g[nt][2] = g[nt][3] = 0.f;
     }
     tile_rows_dot(s, qa, T.k);
-    tile_rows_dot(g, ah, T.v);
-    tile_rows_dot(g, al, T.v);
+    if (kRes) {
+      tile_rows_dot(g, ah, T.v);
+      tile_rows_dot(g, al, T.v);
+    }
     __syncthreads();   // |v|^2 ready
     float cs[4][2];
 #pragma unroll
@@ -440,10 +468,17 @@ __global__ void __launch_bounds__(kWarps * 32) d3_pass2_kernel(D3Args A) {
         const int kp = T.pos[key];
         const float vn = T.vn[key];
         float term = 0.f;
-        if (kp <= qpa) term += residual_term(s[nt][e] * A.scale2 - lsa, ana + vn - 2.f * g[nt][e], arow_a,
-                                             T.v + key * kRowStride);
-        if (kp <= qpb) term += residual_term(s[nt][2 + e] * A.scale2 - lsb, anb + vn - 2.f * g[nt][2 + e], arow_b,
-                                             T.v + key * kRowStride);
+        if (kRes) {
+          if (kp <= qpa) term += residual_term(s[nt][e] * A.scale2 - lsa, ana + vn - 2.f * g[nt][e], arow_a,
+                                               T.v + key * kRowStride);
+          if (kp <= qpb) term += residual_term(s[nt][2 + e] * A.scale2 - lsb, anb + vn - 2.f * g[nt][2 + e], arow_b,
+                                               T.v + key * kRowStride);
+        } else {
+          const bool ca = kMode == kMassLater ? kp < qpa : kp <= qpa;
+          const bool cb = kMode == kMassLater ? kp < qpb : kp <= qpb;
+          if (ca) term += exp2f(s[nt][e] * A.scale2 - lsa);
+          if (cb) term += exp2f(s[nt][2 + e] * A.scale2 - lsb);
+        }
         // sum over the 8 row groups of the warp (lanes with equal cq)
         term += __shfl_xor_sync(0xffffffffu, term, 4);
         term += __shfl_xor_sync(0xffffffffu, term, 8);
@@ -476,7 +511,35 @@ __global__ void __launch_bounds__(256) d3_finalize_kernel(D3Args A, int groups) 
     float tot = 0.f;
     for (int rg = 0; rg < groups; ++rg)
       tot += A.ws.d3_score_part[(static_cast<size_t>(rg) * A.dm.lanes + l) * A.dm.cap + j];
-    A.scores[static_cast<size_t>(l) * A.dm.cap + j] = tot;
+    A.col_out[static_cast<size_t>(l) * A.dm.cap + j] = tot;
+  }
+}
+
+// SnapKV pooling of the column sums (SnapKV, "How it works": pooled[i] =
+// max of sums[i - r .. i + r], clamped at the lane's ends; a NaN sum wins,
+// as a max over a set holding NaN is NaN).  One CTA per 1024 kept entries of
+// a lane, sums staged with a halo of r on each side.
+constexpr int kPoolTile = 1024;
+__global__ void __launch_bounds__(256) d3_pool_kernel(const float* __restrict__ sums, float* __restrict__ out,
+                                                      const int32_t* __restrict__ count, int cap, int r) {
+  extern __shared__ float pool_sm[];
+  const int l = blockIdx.y;
+  const int n = min(max(count[l], 0), cap);
+  const int j0 = blockIdx.x * kPoolTile;
+  if (j0 >= n) return;
+  const int lo = max(0, j0 - r), hi = min(n, j0 + kPoolTile + r);
+  const float* src = sums + static_cast<size_t>(l) * cap;
+  for (int j = lo + threadIdx.x; j < hi; j += blockDim.x) pool_sm[j - lo] = src[j];
+  __syncthreads();
+  const int jend = min(n, j0 + kPoolTile);
+  for (int j = j0 + threadIdx.x; j < jend; j += blockDim.x) {
+    const int a = max(0, j - r), b = min(n - 1, j + r);
+    float m = pool_sm[a - lo];
+    for (int i = a + 1; i <= b; ++i) {
+      const float x = pool_sm[i - lo];
+      if (x != x || x > m) m = x;
+    }
+    out[static_cast<size_t>(l) * cap + j] = m;
   }
 }
 
@@ -629,7 +692,7 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, i
 // In pass 2 it also retires each tile's column sums: once the tile's stage
 // is empty (its MMAs and the 8 row warps are done with it), the 8 warps'
 // partial sums are added in warp order and stored.
-template <bool kPass2>
+template <bool kPass2, bool kLoadV = true>
 __device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, int l,
                                            int j_begin, int j_end, int ntiles, unsigned char* sq, unsigned char* skv,
                                            int (*pos)[kTcKeys], float (*vn)[kTcKeys],
@@ -660,7 +723,7 @@ __device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, in
     if (s < 0 || s >= rows_max) { set_status(A.ws.status, ST_BAD_INDEX); s = 0; }
     sl = s;
     ps = A.ls.pos[lo + j];
-    if (kPass2) v = A.ws.d3_vn[lo + j];
+    if (kPass2 && kLoadV) v = A.ws.d3_vn[lo + j];
   };
   auto retire = [&](int u) {
     const int su = u % kTcStages;
@@ -671,7 +734,7 @@ __device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, in
 #pragma unroll
       for (int w8 = 0; w8 < kWsRowThreads / 32; ++w8) tot += col[su][w8][key];
       const int j = j_begin + u * kTcKeys + key;
-      if (j < j_end) A.scores[lo + j] = tot;
+      if (j < j_end) A.col_out[lo + j] = tot;
     }
   };
   int s0, s1, p0, p1;
@@ -687,7 +750,7 @@ __device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, in
     }
     pos[st][2 * lane] = p0;
     pos[st][2 * lane + 1] = p1;
-    if (kPass2) {
+    if (kPass2 && kLoadV) {
       vn[st][2 * lane] = v0;
       vn[st][2 * lane + 1] = v1;
     }
@@ -707,7 +770,7 @@ __device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, in
     const int gbase = __shfl_sync(0xffffffffu, qbase, 8 * grp);
     const bool grp_run = ((qrun >> (8 * grp)) & 0xFFu) == 0xFFu && gbase + 16 <= rows_max;
     __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(&bar.full[st], static_cast<uint32_t>(kTcKV));
+    if (lane == 0) mbar_arrive_expect_tx(&bar.full[st], static_cast<uint32_t>(kLoadV ? kTcKV : 2 * kTcHalf));
     __syncwarp();
     unsigned char* kst = skv + st * kTcKV;
     unsigned char* vst = kst + 2 * kTcHalf;
@@ -716,7 +779,7 @@ __device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, in
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           tma_rows(kst + hf * kTcHalf, &mp.m[4], hf * 64, tbase, &bar.full[st]);
-          tma_rows(vst + hf * kTcHalf, &mp.m[5], hf * 64, tbase, &bar.full[st]);
+          if (kLoadV) tma_rows(vst + hf * kTcHalf, &mp.m[5], hf * 64, tbase, &bar.full[st]);
         }
       }
     } else if (lane < kTcKeys / 4) {
@@ -725,14 +788,14 @@ __device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, in
 #pragma unroll
           for (int hf = 0; hf < 2; ++hf) {
             tma_rows(kst + hf * kTcHalf + grp * 2048, &mp.m[2], hf * 64, gbase, &bar.full[st]);
-            tma_rows(vst + hf * kTcHalf + grp * 2048, &mp.m[3], hf * 64, gbase, &bar.full[st]);
+            if (kLoadV) tma_rows(vst + hf * kTcHalf + grp * 2048, &mp.m[3], hf * 64, gbase, &bar.full[st]);
           }
         }
       } else {
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf) {
           tma_gather4(kst + hf * kTcHalf + lane * 512, &mp.m[0], hf * 64, g0, g1, g2, g3, &bar.full[st]);
-          tma_gather4(vst + hf * kTcHalf + lane * 512, &mp.m[1], hf * 64, g0, g1, g2, g3, &bar.full[st]);
+          if (kLoadV) tma_gather4(vst + hf * kTcHalf + lane * 512, &mp.m[1], hf * 64, g0, g1, g2, g3, &bar.full[st]);
         }
       }
     }
@@ -768,6 +831,9 @@ __device__ __forceinline__ void ws_init_bars(WsBars& bar, uint32_t full_count, u
 // S(t) done (b = t & 1); x_free[b]: P(t) written by the 8 row warps;
 // pv_done[b]: P V(t) done; empty[s]: P V and the 8 row warps (which also
 // take |v|^2 of the tile's keys for pass 2) are done with the stage.
+// Without V (kWithV false: the attention-mass scores need only the LSE) the
+// stages hold K alone, no P V is issued and the rows keep only (max, sum).
+template <bool kWithV>
 __global__ void __launch_bounds__(kWsThreads, 1)
     d3_tc_pass1_kernel(D3Args A, const __grid_constant__ D3Maps mp) {
   extern __shared__ unsigned char d3_dsm[];
@@ -791,7 +857,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   const uint32_t tl = sh_taddr;
 
   if (warp == kWsProducer) {
-    ws_produce<false>(A, mp, l, j_begin, j_end, ntiles, sq, skv, sh_pos, nullptr, nullptr, bar);
+    ws_produce<false, kWithV>(A, mp, l, j_begin, j_end, ntiles, sq, skv, sh_pos, nullptr, nullptr, bar);
   } else if (warp == kWsIssuer) {
     if ((tid & 31) == 0) {
       (void)mbar_wait_bounded(&bar.qfull, 0, A.ws.status);
@@ -813,7 +879,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         tc::fence_after();
         const uint32_t vbase = smem_u32(skv + st * kTcKV + 2 * kTcHalf);
 #pragma unroll
-        for (int mm = 0; mm < 2; ++mm) {
+        for (int mm = 0; mm < (kWithV ? 2 : 0); ++mm) {
           const uint32_t aP = tl + 256 + buf * 128 + mm * 64;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
@@ -875,7 +941,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         m_run = tmax;
         l_run *= factor;
       }
-      if (t > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
+      if (kWithV && t > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
         // P V(t - 1) must be complete before O is rescaled
         (void)mbar_wait_bounded(&bar.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, A.ws.status);
         tc::fence_after();
@@ -894,6 +960,19 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       // every key while the row has seen none (m = -inf, offset taken as 0)
       const float negm = m_run == -INFINITY ? 0.f : -m_run;
       float psum = 0.f;
+      if (!kWithV) {
+        // (max, sum) only: S has been read, the buffer and the stage are free
+        tc::fence_before();
+        __syncwarp();
+        if ((tid & 31) == 0) {
+          mbar_arrive1(&bar.x_free[buf]);
+          mbar_arrive1(&bar.empty[st]);
+        }
+#pragma unroll
+        for (int k = 0; k < kTcKeys; ++k) psum += hw_exp2(fmaf(s[k], A.scale2, negm));
+        l_run += psum;
+        continue;
+      }
       uint32_t hi[32], lo[32];
 #pragma unroll
       for (int k2 = 0; k2 < 32; ++k2) {
@@ -945,14 +1024,16 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       __syncwarp();
       if ((tid & 31) == 0) mbar_arrive1(&bar.empty[st]);
     }
-    (void)mbar_wait_bounded(&bar.pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, A.ws.status);
-    tc::fence_after();
     const size_t stride = kD + 2;
     float* part = A.ws.d3_part + (static_cast<size_t>(l) * A.chunks + chunk) * static_cast<size_t>(A.rows_cap) * stride +
                   static_cast<size_t>(r) * stride;
+    if (kWithV) {
+      (void)mbar_wait_bounded(&bar.pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, A.ws.status);
+      tc::fence_after();
+    }
     const uint32_t aO = tl + lane_off + m * 128;
 #pragma unroll
-    for (int q8 = 0; q8 < 8; ++q8) {
+    for (int q8 = 0; q8 < (kWithV ? 8 : 0); ++q8) {
       uint32_t v[16];
       tc::ld16(aO + q8 * 16, v);
       tc::wait_ld();
@@ -1009,6 +1090,9 @@ __device__ __noinline__ float residual_direct(float x, const float* arow, const 
 constexpr float kSmallLog2 = -7.f;   // p < 2^-7: p / (1 - p) = p + p^2 + p^3 within 2^-21
 constexpr float kR2Floor = 1e-30f;   // r2 floor: sqrt(r2) = r2 rsqrt(r2) stays finite (1e-15 for r2 = 0)
 
+// kMode (D3Mode): kResidual as above; the mass modes issue S alone, load no
+// V and sum the weights of the keys the row counts.
+template <int kMode>
 __global__ void __launch_bounds__(kWsThreads, 1)
     d3_tc_pass2_kernel(D3Args A, const __grid_constant__ D3Maps mp) {
   extern __shared__ unsigned char d3_dsm[];
@@ -1037,7 +1121,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   const bool row_ok = r < A.rows;
   const size_t wrow = static_cast<size_t>(l) * A.rows_cap + (row_ok ? r : 0);
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  if (warp < kWsProducer) {
+  if (kMode == kResidual && warp < kWsProducer) {
     // a of this row (bf16 hi and lo) into tensor memory
     const uint4* hsrc = reinterpret_cast<const uint4*>(A.ws.d3_ahi + wrow * kD);
     const uint4* lsrc = reinterpret_cast<const uint4*>(A.ws.d3_alo + wrow * kD);
@@ -1061,7 +1145,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   tc::fence_after();
 
   if (warp == kWsProducer) {
-    ws_produce<true>(A, mp, l, j_begin, j_end, ntiles, sq, skv, sh_pos, sh_vn, sh_col, bar);
+    ws_produce<true, kMode == kResidual>(A, mp, l, j_begin, j_end, ntiles, sq, skv, sh_pos, sh_vn, sh_col, bar);
   } else if (warp == kWsIssuer) {
     if (lane == 0) {
       (void)mbar_wait_bounded(&bar.qfull, 0, A.ws.status);
@@ -1077,7 +1161,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         for (int mm = 0; mm < 2; ++mm) {
           tc_issue_s(tl + 256 + mm * 64, sq, kst, mm);
 #pragma unroll
-          for (int ks = 0; ks < 8; ++ks) {
+          for (int ks = 0; ks < (kMode == kResidual ? 8 : 0); ++ks) {
             const int half = ks >> 2, kin = ks & 3;
             const uint64_t bd = tc::desc_sw128(smem_u32(vst + half * kTcHalf) + kin * 32, 16, 1024);
             tc::mma_ts(tl + 384 + mm * 64, tl + mm * 64 + ks * 8, bd, kIdS, ks > 0 ? 1u : 0u);
@@ -1098,6 +1182,67 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       arow = A.a_out + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i) * kD;
     }
     const int nkeys = j_end - j_begin;
+    if (kMode != kResidual) {
+#pragma unroll 1
+      for (int t = 0; t < ntiles; ++t) {
+        const int st = t % kTcStages;
+        (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);   // positions
+        (void)mbar_wait_bounded(&bar.x_full[0], t & 1, A.ws.status);
+        tc::fence_after();
+        float sv[kTcKeys];
+        {
+          uint32_t v[4][16];
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4) tc::ld16(tl + lane_off + 256 + m * 64 + q4 * 16, v[q4]);
+          tc::wait_ld();
+#pragma unroll
+          for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+            for (int k = 0; k < 16; ++k) sv[q4 * 16 + k] = __uint_as_float(v[q4][k]);
+        }
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(&bar.x_free[0]);
+        // the keys the row counts are a prefix of the tile (positions ascend)
+        int vis = 0;
+        if (row_ok) {
+          const int lim = min(kTcKeys, nkeys - t * kTcKeys);
+          auto counted = [&](int k) { return kMode == kMassLater ? sh_pos[st][k] < qp : sh_pos[st][k] <= qp; };
+          if (lim > 0 && counted(lim - 1)) {
+            vis = lim;
+          } else {
+            int lo = 0, hi = lim;
+            while (lo < hi) {
+              const int mid = (lo + hi) >> 1;
+              if (counted(mid)) lo = mid + 1; else hi = mid;
+            }
+            vis = lo;
+          }
+        }
+#pragma unroll 1
+        for (int hf = 0; hf < 2; ++hf) {
+          const int kv = vis - hf * 32;
+#pragma unroll
+          for (int k2 = 0; k2 < kTcKeys / 2; ++k2)
+            sv[k2] = k2 < kv ? hw_exp2(fmaf(sv[k2], A.scale2, -lse2)) : 0.f;
+#pragma unroll
+          for (int o = 16, cnt = kTcKeys / 2; o >= 1; o >>= 1, cnt >>= 1) {
+            const bool up = (lane & o) != 0;
+#pragma unroll
+            for (int i = 0; i < cnt / 2; ++i) {
+              const float send = up ? sv[i] : sv[cnt / 2 + i];
+              const float keep = up ? sv[cnt / 2 + i] : sv[i];
+              sv[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+            }
+          }
+          sh_col[st][warp][hf * 32 + lane] = sv[0];
+#pragma unroll
+          for (int k2 = 0; k2 < kTcKeys / 2; ++k2) sv[k2] = sv[kTcKeys / 2 + k2];
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(&bar.empty[st]);
+      }
+    } else {
 #pragma unroll 1
     for (int t = 0; t < ntiles; ++t) {
       const int st = t % kTcStages;
@@ -1224,6 +1369,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       __syncwarp();
       if (lane == 0) mbar_arrive1(&bar.empty[st]);    // this warp is done with the stage
     }
+    }
   }
   tc::fence_before();
   __syncthreads();
@@ -1235,10 +1381,16 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 int d3_rows_max(const Dims& dm) { return dm.g * dm.max_window; }
 
 cudaError_t prepare_dropkv() {
-  cudaError_t e = cudaFuncSetAttribute(d3_tc_pass1_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-  if (e == cudaSuccess)
-    e = cudaFuncSetAttribute(d3_tc_pass2_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
-  return e;
+  const void* fns[] = {reinterpret_cast<const void*>(d3_tc_pass1_kernel<true>),
+                       reinterpret_cast<const void*>(d3_tc_pass1_kernel<false>),
+                       reinterpret_cast<const void*>(d3_tc_pass2_kernel<kResidual>),
+                       reinterpret_cast<const void*>(d3_tc_pass2_kernel<kMassCausal>),
+                       reinterpret_cast<const void*>(d3_tc_pass2_kernel<kMassLater>)};
+  for (const void* f : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 // Keys per CTA: each lane's keys split over floor(SMs / lanes) CTAs (one
 // wave when the lanes are few), in whole 64-key tiles, at least kChunkMin.
@@ -1284,8 +1436,11 @@ cudaError_t prepare_tensor_maps(Ctx& ctx) {
   return cudaSuccess;
 }
 
-cudaError_t launch_score(const Ctx& ctx, int layer, const void* q_win, int w, const int32_t* q_pos,
-                         float* lse, float* a_out, float* scores, cudaStream_t stream) {
+// The window passes of one layer.  mode (D3Mode) picks the pass-2 term;
+// pool_r >= 0 max-pools the mass sums over kept neighbours (radius pool_r)
+// into scores, pool_r < 0 writes the sums themselves.
+static cudaError_t launch_window(const Ctx& ctx, int layer, const void* q_win, int w, const int32_t* q_pos,
+                                 int mode, int pool_r, float* lse, float* a_out, float* scores, cudaStream_t stream) {
   const Dims& dm = ctx.dims;
   D3Args A;
   A.ls = layer_state(ctx, layer);
@@ -1299,27 +1454,63 @@ cudaError_t launch_score(const Ctx& ctx, int layer, const void* q_win, int w, co
   A.chunk_keys = d3_chunk_keys(dm, ctx.sm_count);
   A.chunks = d3_chunks(dm, ctx.sm_count);
   A.lse_out = lse; A.a_out = a_out; A.scores = scores;
+  A.col_out = pool_r >= 0 ? ctx.ws.d3_score_part : scores;
   A.scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(dm.d));
   if (A.rows > A.rows_cap || A.rows > kMaxRowGroups * kRowsPerCta || dm.d != kD || dm.dtype != KVEVICT_BF16)
     return cudaErrorInvalidValue;
+  const bool res = mode == kResidual;
   if (A.rows <= kTcRows) {
     const dim3 grid(A.chunks, dm.lanes);
     if (!ctx.tmaps) return cudaErrorInvalidValue;
     D3Maps mp;
     for (int i = 0; i < kTmapsPerLayer; ++i) mp.m[i] = ctx.tmaps[static_cast<size_t>(layer) * kTmapsPerLayer + i];
-    d3_tc_pass1_kernel<<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
-    d3_combine_kernel<<<dim3((A.rows + 7) / 8, dm.lanes), 256, 0, stream>>>(A);
-    d3_tc_pass2_kernel<<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
-    return cudaGetLastError();
+    const dim3 cgrid((A.rows + 7) / 8, dm.lanes);
+    if (res) {
+      d3_tc_pass1_kernel<true><<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
+      d3_combine_kernel<true><<<cgrid, 256, 0, stream>>>(A);
+      d3_tc_pass2_kernel<kResidual><<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
+    } else {
+      d3_tc_pass1_kernel<false><<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
+      d3_combine_kernel<false><<<cgrid, 256, 0, stream>>>(A);
+      if (mode == kMassLater)
+        d3_tc_pass2_kernel<kMassLater><<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
+      else
+        d3_tc_pass2_kernel<kMassCausal><<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
+    }
+  } else {
+    const int groups = (A.rows + kRowsPerCta - 1) / kRowsPerCta;
+    dim3 grid(A.chunks, dm.lanes, groups);
+    d3_pass1_kernel<<<grid, kWarps * 32, 0, stream>>>(A);
+    if (res) {
+      d3_combine_kernel<true><<<dim3((A.rows + 7) / 8, dm.lanes), 256, 0, stream>>>(A);
+      d3_pass2_kernel<kResidual><<<grid, kWarps * 32, 0, stream>>>(A);
+    } else {
+      d3_combine_kernel<false><<<dim3((A.rows + 7) / 8, dm.lanes), 256, 0, stream>>>(A);
+      if (mode == kMassLater)
+        d3_pass2_kernel<kMassLater><<<grid, kWarps * 32, 0, stream>>>(A);
+      else
+        d3_pass2_kernel<kMassCausal><<<grid, kWarps * 32, 0, stream>>>(A);
+    }
+    dim3 fgrid((dm.cap + 255) / 256 < 64 ? (dm.cap + 255) / 256 : 64, dm.lanes);
+    d3_finalize_kernel<<<fgrid, 256, 0, stream>>>(A, groups);
   }
-  const int groups = (A.rows + kRowsPerCta - 1) / kRowsPerCta;
-  dim3 grid(A.chunks, dm.lanes, groups);
-  d3_pass1_kernel<<<grid, kWarps * 32, 0, stream>>>(A);
-  d3_combine_kernel<<<dim3((A.rows + 7) / 8, dm.lanes), 256, 0, stream>>>(A);
-  d3_pass2_kernel<<<grid, kWarps * 32, 0, stream>>>(A);
-  dim3 fgrid((dm.cap + 255) / 256 < 64 ? (dm.cap + 255) / 256 : 64, dm.lanes);
-  d3_finalize_kernel<<<fgrid, 256, 0, stream>>>(A, groups);
+  if (pool_r >= 0) {
+    const dim3 pgrid((dm.cap + kPoolTile - 1) / kPoolTile, dm.lanes);
+    const size_t sm = static_cast<size_t>(kPoolTile + 2 * pool_r) * sizeof(float);
+    d3_pool_kernel<<<pgrid, 256, sm, stream>>>(A.col_out, scores, A.ls.count, dm.cap, pool_r);
+  }
   return cudaGetLastError();
+}
+
+cudaError_t launch_score(const Ctx& ctx, int layer, const void* q_win, int w, const int32_t* q_pos,
+                         float* lse, float* a_out, float* scores, cudaStream_t stream) {
+  return launch_window(ctx, layer, q_win, w, q_pos, kResidual, -1, lse, a_out, scores, stream);
+}
+
+cudaError_t launch_score_mass(const Ctx& ctx, int layer, const void* q_win, int w, const int32_t* q_pos,
+                              bool later, int pool_r, float* lse, float* scores, cudaStream_t stream) {
+  return launch_window(ctx, layer, q_win, w, q_pos, later ? kMassLater : kMassCausal, pool_r, lse, nullptr,
+                       scores, stream);
 }
 
 }  // namespace kve

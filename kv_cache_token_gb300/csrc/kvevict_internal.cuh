@@ -142,6 +142,8 @@ cudaError_t launch_compact(const Ctx&, int layer, const int32_t* victims, const 
                            cudaStream_t);
 cudaError_t launch_score(const Ctx&, int layer, const void* q_win, int w, const int32_t* q_pos,
                          float* lse, float* a_out, float* scores, cudaStream_t);
+cudaError_t launch_score_mass(const Ctx&, int layer, const void* q_win, int w, const int32_t* q_pos,
+                              bool later, int pool_r, float* lse, float* scores, cudaStream_t);
 cudaError_t launch_stats(const Ctx&, int layer, long long* out, cudaStream_t);
 cudaError_t launch_attend_into(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
                                float* logits, float* part_o, float* part_ml, int32_t* lane_nseg, cudaStream_t);
