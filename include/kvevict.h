@@ -171,6 +171,18 @@ void kvevict_destroy(kvevict_ctx* ctx);
  * status word zero. */
 kvevict_status kvevict_reset(kvevict_ctx* ctx, void* stream);
 
+/* Per-layer budget (H2O Guide, "Asymmetric Layer Allocation": early layers
+ * want larger recent windows and fewer heavy hitters, deep layers larger
+ * heavy-hitter pools).  Sets the budget and recent window that later decode
+ * steps of `layer` use (the configuration's values until then); a host-side
+ * setting, read when a step is enqueued, so steps already enqueued (or
+ * captured in a CUDA graph) keep the values they were launched with.  Pool
+ * capacity stays the caller's sizing.  Refuses recent_window >= budget
+ * (KVEVICT_E_RECENT_GE_BUDGET, as create does), recent_window < 1 or a
+ * layer out of range (KVEVICT_E_INVALID_ARG).  kvevict_reset keeps it. */
+kvevict_status kvevict_set_layer_budget(kvevict_ctx* ctx, int layer, int32_t budget,
+                                        int32_t recent_window);
+
 /* Prompt admission (vToken review, Sec. 3.2 sync_new_tokens) for one layer:
  * every lane gets positions 0..n-1 with k_ctx/v_ctx [B][Hkv][n][d]
  * (kv_dtype, device), stored in ceil(n/16) blocks taken lowest-id first in

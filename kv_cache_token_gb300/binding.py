@@ -65,6 +65,7 @@ def lib():
         L.kvevict_destroy.argtypes = [V]
         L.kvevict_destroy.restype = None
         L.kvevict_reset.argtypes = [V, V]
+        L.kvevict_set_layer_budget.argtypes = [V, ctypes.c_int, I, I]
         L.kvevict_prefill.argtypes = [V, ctypes.c_int, V, V, I, V]
         L.kvevict_decode_step.argtypes = [V, ctypes.c_int, V, V, V, I, V, V, V, V, V]
         L.kvevict_attend.argtypes = [V, ctypes.c_int, V, V, V, V]
@@ -76,7 +77,7 @@ def lib():
         L.kvevict_compact.argtypes = [V, ctypes.c_int, V, V, V, V, V, V, V]
         L.kvevict_stats.argtypes = [V, ctypes.c_int, V, V]
         L.kvevict_last_error.argtypes = [V, ctypes.c_char_p, ctypes.c_size_t]
-        for f in ("validate", "create", "reset", "prefill", "decode_step", "attend", "finish_step",
+        for f in ("validate", "create", "reset", "set_layer_budget", "prefill", "decode_step", "attend", "finish_step",
                   "attend_static",
                   "score", "score_mass", "select",
                   "compact", "stats", "last_error"):
@@ -185,6 +186,9 @@ class Engine:
     # ---- C-ABI calls ----------------------------------------------------------
     def reset(self, stream=None):
         _check(lib().kvevict_reset(self.h, _stream(stream)), "kvevict_reset")
+
+    def set_layer_budget(self, layer, budget, recent_window):
+        _check(lib().kvevict_set_layer_budget(self.h, layer, budget, recent_window), "kvevict_set_layer_budget")
 
     def prefill(self, layer, k_ctx, v_ctx, stream=None):
         assert k_ctx.is_contiguous() and v_ctx.is_contiguous() and k_ctx.dtype == self.kv_dtype

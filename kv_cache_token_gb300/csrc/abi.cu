@@ -237,10 +237,24 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   ctx->c.device = dev;
   ctx->c.last_layer = -1;
   ctx->c.tmaps = nullptr;
+  ctx->c.layer_budget = new (std::nothrow) int[cfg->num_layers];
+  ctx->c.layer_recent = new (std::nothrow) int[cfg->num_layers];
+  if (!ctx->c.layer_budget || !ctx->c.layer_recent) {
+    delete[] ctx->c.layer_budget;
+    delete[] ctx->c.layer_recent;
+    delete ctx;
+    return KVEVICT_E_INVALID_ARG;
+  }
+  for (int l = 0; l < cfg->num_layers; ++l) {
+    ctx->c.layer_budget[l] = cfg->budget;
+    ctx->c.layer_recent[l] = cfg->recent_window;
+  }
   ctx->c.ws_bytes = kve::workspace_layout(*cfg, &ctx->c.ws, static_cast<char*>(bufs->workspace));
   if (kve::prepare_kernels(ctx->c) != cudaSuccess || ctx->c.attend_ctas_per_sm < 1 ||
       kve::prepare_tensor_maps(ctx->c) != cudaSuccess) {
     delete[] ctx->c.tmaps;
+    delete[] ctx->c.layer_budget;
+    delete[] ctx->c.layer_recent;
     delete ctx;
     return KVEVICT_E_CUDA;
   }
@@ -251,10 +265,20 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
 void kvevict_destroy(kvevict_ctx* ctx) {
   if (!ctx) return;
   delete[] ctx->c.tmaps;
+  delete[] ctx->c.layer_budget;
+  delete[] ctx->c.layer_recent;
   delete ctx;
 }
 
 static kvevict_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVEVICT_OK : KVEVICT_E_CUDA; }
+
+kvevict_status kvevict_set_layer_budget(kvevict_ctx* ctx, int layer, int32_t budget, int32_t recent_window) {
+  if (!ctx || layer < 0 || layer >= ctx->c.dims.L || recent_window < 1) return KVEVICT_E_INVALID_ARG;
+  if (recent_window >= budget) return KVEVICT_E_RECENT_GE_BUDGET;
+  ctx->c.layer_budget[layer] = budget;
+  ctx->c.layer_recent[layer] = recent_window;
+  return KVEVICT_OK;
+}
 
 kvevict_status kvevict_reset(kvevict_ctx* ctx, void* stream) {
   if (!ctx) return KVEVICT_E_INVALID_ARG;

@@ -1312,6 +1312,8 @@ cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, 
   A.ls = layer_state(ctx, layer);
   A.ws = ctx.ws;
   A.dm = ctx.dims;
+  A.dm.budget = ctx.layer_budget[layer];
+  A.dm.R = ctx.layer_recent[layer];
   A.has_q = has_q ? 1 : 0;
   A.new_pos = new_pos;
   A.layer = layer;

@@ -110,6 +110,11 @@ struct Ctx {
   // kTmapsPerLayer per layer, for the window scoring's row copies; null when
   // the configuration has no scoring window.
   CUtensorMap* tmaps;
+  // Per-layer budget and recent window ([L] each, host memory; the
+  // configuration's values until kvevict_set_layer_budget changes a layer).
+  // Only the decode epilogue reads them, from its launch arguments.
+  int* layer_budget;
+  int* layer_recent;
 };
 
 // workspace layout (host)

@@ -50,6 +50,15 @@ class Engine:
         self.layers = {l: PagedLayer(self.n_lanes, cfg.blocks_per_pool, cfg.head_dim, W, store_kv)
                        for l in wanted}
         self.deferred = 0
+        self.layer_budget = {}
+
+    def set_layer_budget(self, layer, budget, recent_window):
+        """Per-layer budget (H2O Guide, "Asymmetric Layer Allocation"): later
+        steps of ``layer`` keep ``budget`` tokens with a recent window of
+        ``recent_window``; the same refusals as the configuration."""
+        if recent_window < 1 or recent_window >= budget:
+            raise ValueError("recent_window must be in [1, budget)")
+        self.layer_budget[layer] = (budget, recent_window)
 
     def lane_of(self, b, kvh):
         return b * self.cfg.num_kv_heads + kvh
@@ -77,6 +86,7 @@ class Engine:
         c = self.cfg
         PL = self.layers[layer]
         g = self.g
+        budget, recent = self.layer_budget.get(layer, (c.budget, c.recent_window))
         out = np.zeros((c.batch, c.num_q_heads, c.head_dim))
         lse = np.zeros((c.batch, c.num_q_heads))
         victims, freed, pending, new_rows, all_keys, all_pos = [], [], [], {}, [], []
@@ -101,7 +111,7 @@ class Engine:
                     L.ring_slot = snapkv.ring_write(L.hist, L.ring_slot, decode_scores(p, o, Va, n))
             keys = self.lane_keys(L)
             pos_all = np.append(L.pos, np.int64(new_pos))
-            vict = select_lane(keys, pos_all, c.budget, c.recent_window)
+            vict = select_lane(keys, pos_all, budget, recent)
             assert new_pos not in vict
             all_keys.append(keys)
             all_pos.append(pos_all)

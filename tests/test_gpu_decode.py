@@ -13,9 +13,12 @@ from workloads import Workload, scaled, shape
 pytestmark = pytest.mark.gpu
 
 
-def run_decode(shp, steps, layers=(0,), check_state_every=1, null_steps=()):
+def run_decode(shp, steps, layers=(0,), check_state_every=1, null_steps=(), layer_budgets=None):
     wl = Workload(shp)
     eng, orc = make_pair(shp, layers=list(layers))
+    for layer, (budget, recent) in (layer_budgets or {}).items():
+        eng.set_layer_budget(layer, budget, recent)
+        orc.set_layer_budget(layer, budget, recent)
     for layer in layers:
         prefill_both(eng, orc, wl, layer)
         compare_states(gpu_state(eng, layer), oracle_state(orc, layer), shp.policy, "prefill")
@@ -194,3 +197,22 @@ def test_decode_steps_captured_in_a_cuda_graph():
         compare_states(gpu_state(eng, layer), oracle_state(orc, layer), shp.policy, "final layer %d" % layer)
     code, msg = eng.last_error()
     assert code == 0, msg
+
+
+def test_per_layer_budgets_h2o_and_snapkv():
+    """Per-layer budgets (H2O Guide, "Asymmetric Layer Allocation"): three
+    H2O layers with their own budgets and recent windows (one of them a
+    one-victim steady state, one still mass-evicting, one below its budget
+    and growing), then two SnapKV layers; every step against the oracle."""
+    shp = scaled("h2o_70b", num_layers=3, batch=2, num_kv_heads=2, num_q_heads=16, ctx=600, steps=8,
+                 budget=400, recent_window=100)
+    run_decode(shp, 8, layers=(0, 1, 2), layer_budgets={0: (599, 300), 1: (150, 20), 2: (640, 64)})
+    shp = scaled("snapkv_decode", num_layers=2, batch=1, num_kv_heads=2, num_q_heads=8, ctx=700, steps=6,
+                 budget=200, recent_window=40, obs_window=8, pool_kernel=5)
+    run_decode(shp, 6, layers=(0, 1), layer_budgets={1: (300, 100)})
+    eng, _ = make_pair(shp)
+    from kv_cache_token_gb300.binding import KvevictError
+    with pytest.raises(KvevictError):
+        eng.set_layer_budget(0, 50, 50)
+    with pytest.raises(KvevictError):
+        eng.set_layer_budget(2, 100, 10)

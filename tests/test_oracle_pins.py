@@ -601,3 +601,38 @@ def test_kv_bytes_formula():
     assert s.kv_bytes / 1e9 == pytest.approx(335.5, abs=0.05)
     from workloads import shape
     assert shape("h2o_70b").kv_bytes / 1e9 == pytest.approx(85.9, abs=0.05)
+
+
+def test_per_layer_budget_equals_uniform_engine_per_layer():
+    """H2O Guide, "Asymmetric Layer Allocation": a layer given its own budget
+    behaves exactly like an engine configured with that budget everywhere;
+    the other layers keep the configured one.  Kept counts stop at each
+    layer's budget, and the layer's recent window survives every step."""
+    rng = np.random.default_rng(12)
+    d, n0, steps = 16, 30, 25
+    base = _cfg(num_layers=2, num_q_heads=2, budget=20, recent_window=5)
+    E = Engine(base)
+    E.set_layer_budget(1, 12, 8)
+    ref0 = Engine(_cfg(num_layers=1, num_q_heads=2, budget=20, recent_window=5))
+    ref1 = Engine(_cfg(num_layers=1, num_q_heads=2, budget=12, recent_window=8))
+    with pytest.raises(ValueError):
+        E.set_layer_budget(0, 8, 8)
+    K = rng.standard_normal((2, 1, 1, n0, d))
+    V = rng.standard_normal((2, 1, 1, n0, d))
+    for layer in (0, 1):
+        E.prefill(layer, K[layer], V[layer])
+    ref0.prefill(0, K[0], V[0])
+    ref1.prefill(0, K[1], V[1])
+    for t in range(steps):
+        pos = n0 + t
+        for layer, R in ((0, ref0), (1, ref1)):
+            q = rng.standard_normal((1, 2, d))
+            kn = rng.standard_normal((1, 1, d))
+            vn = rng.standard_normal((1, 1, d))
+            a = E.decode_step(layer, q, kn, vn, pos)
+            b = R.decode_step(0, q, kn, vn, pos)
+            np.testing.assert_array_equal(a["victims"][0], b["victims"][0])
+            kept = E.layers[layer].lanes[0].pos
+            budget, recent = (20, 5) if layer == 0 else (12, 8)
+            assert kept.size == min(n0 + t + 1, budget)
+            assert set(range(pos - recent + 1, pos + 1)) <= set(kept.tolist())
