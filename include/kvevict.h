@@ -314,6 +314,28 @@ kvevict_status kvevict_compact(kvevict_ctx* ctx, int layer, const int32_t* victi
                                const int32_t* n_victims, int32_t* freed, int32_t* n_freed,
                                int32_t* moves, int32_t* n_moves, void* stream);
 
+/* Asynchronous reclamation (vToken review, Sec. 3.3 Stage 4: the relocation
+ * copy runs on its own stream after the step's forward pass, and the next
+ * step's attention waits on an event, not the host).
+ * kvevict_defer_relocation(ctx, 1): later decode steps evict and admit as
+ * before but plan no relocation (their Eq. (1) test is skipped); 0 restores
+ * in-step relocation.  A host-side setting read when a step is enqueued.
+ * kvevict_relocate(ctx, layer, ...): the relocation a decode step of `layer`
+ * would have run, now: every lane whose waste ratio F (Eq. (1)) exceeds
+ * theta_f and whose plan strictly lowers its block count (I4) packs the live
+ * tokens of its partly filled blocks into fresh lowest-id blocks (Stages 1
+ * and 3), in ascending position; outputs as kvevict_compact (freed [P]
+ * ascending, n_freed [1], moves [m][6], n_moves [1]; each may be NULL).  It
+ * has its own scratch, so it may run on another stream while decode steps
+ * of OTHER layers run; the caller orders it after the layer's last step
+ * (record an event on the step's stream, cudaStreamWaitEvent on the
+ * relocation stream) and makes that layer's next step wait for it (an event
+ * recorded after kvevict_relocate, waited on by the step's stream).  Two
+ * kvevict_relocate calls, or one and a kvevict_compact, must not overlap. */
+kvevict_status kvevict_defer_relocation(kvevict_ctx* ctx, int32_t deferred);
+kvevict_status kvevict_relocate(kvevict_ctx* ctx, int layer, int32_t* freed, int32_t* n_freed,
+                                int32_t* moves, int32_t* n_moves, void* stream);
+
 /* Attention output and log-sum-exp of one layer without any scratch from the
  * caller.  The pages have no counterpart to this call; it exists for callers
  * that cannot allocate device memory: code running during CUDA-graph stream

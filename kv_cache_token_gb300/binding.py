@@ -75,12 +75,14 @@ def lib():
         L.kvevict_attend_static.argtypes = [V, ctypes.c_int, V, V, V, V, V, V]
         L.kvevict_select.argtypes = [V, V, I, V, V, I, I, I, I, V, V, V]
         L.kvevict_compact.argtypes = [V, ctypes.c_int, V, V, V, V, V, V, V]
+        L.kvevict_defer_relocation.argtypes = [V, I]
+        L.kvevict_relocate.argtypes = [V, ctypes.c_int, V, V, V, V, V]
         L.kvevict_stats.argtypes = [V, ctypes.c_int, V, V]
         L.kvevict_last_error.argtypes = [V, ctypes.c_char_p, ctypes.c_size_t]
         for f in ("validate", "create", "reset", "set_layer_budget", "prefill", "decode_step", "attend", "finish_step",
                   "attend_static",
                   "score", "score_mass", "select",
-                  "compact", "stats", "last_error"):
+                  "compact", "defer_relocation", "relocate", "stats", "last_error"):
             getattr(L, "kvevict_" + f).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -306,6 +308,23 @@ class Engine:
             n_moves = torch.empty((1,), dtype=torch.int32, device=self.device)
         _check(lib().kvevict_compact(self.h, layer, _ptr(victims), _ptr(n_victims), _ptr(freed), _ptr(n_freed),
                                      _ptr(moves), _ptr(n_moves), _stream(stream)), "kvevict_compact")
+        return freed, n_freed, moves, n_moves
+
+    def defer_relocation(self, deferred=True):
+        _check(lib().kvevict_defer_relocation(self.h, 1 if deferred else 0), "kvevict_defer_relocation")
+
+    def relocate(self, layer, freed=None, n_freed=None, moves=None, n_moves=None, stream=None):
+        c = self.cfg
+        if freed is None:
+            freed = torch.empty((c.blocks_per_pool,), dtype=torch.int32, device=self.device)
+        if n_freed is None:
+            n_freed = torch.empty((1,), dtype=torch.int32, device=self.device)
+        if moves is None:
+            moves = torch.empty((self.lanes * c.max_tokens, 6), dtype=torch.int32, device=self.device)
+        if n_moves is None:
+            n_moves = torch.empty((1,), dtype=torch.int32, device=self.device)
+        _check(lib().kvevict_relocate(self.h, layer, _ptr(freed), _ptr(n_freed), _ptr(moves), _ptr(n_moves),
+                                      _stream(stream)), "kvevict_relocate")
         return freed, n_freed, moves, n_moves
 
     def stats(self, layer, stream=None):

@@ -45,7 +45,8 @@ Dims make_dims(const kvevict_config& c) {
 }
 
 // Carves the workspace; with base == nullptr only sizes it.
-size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base) {
+size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base, Workspace* ws_reloc,
+                        int32_t** no_victims) {
   const Dims dm = make_dims(c);
   size_t off = 0;
   auto take = [&](size_t bytes) -> char* {
@@ -94,7 +95,28 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base) {
     w.d3_part = nullptr; w.d3_ahi = nullptr; w.d3_alo = nullptr; w.d3_rowc = nullptr; w.d3_score_part = nullptr;
     w.d3_vn = nullptr;
   }
+  // kvevict_relocate's own compaction and allocator scratch
+  Workspace r = w;
+  r.work_flag = reinterpret_cast<int32_t*>(take(4));
+  r.need_admit = reinterpret_cast<int32_t*>(take(lanes * 4));
+  r.want_dst = reinterpret_cast<int32_t*>(take(lanes * 4));
+  r.admit_block = reinterpret_cast<int32_t*>(take(lanes * 4));
+  r.dst_begin = reinterpret_cast<int32_t*>(take(lanes * 4));
+  r.move_begin = reinterpret_cast<int32_t*>(take(lanes * 4));
+  r.plan_tlive = reinterpret_cast<int32_t*>(take(lanes * 4));
+  r.alloc_ids = reinterpret_cast<int32_t*>(take(P * 4));
+  r.freed_flag = reinterpret_cast<int32_t*>(take(P * 4));
+  r.blk_tag = reinterpret_cast<int32_t*>(take(P * 4));
+  r.counters = reinterpret_cast<int32_t*>(take(64));
+  r.cmp_pos = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
+  r.cmp_slot = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
+  r.cmp_score = reinterpret_cast<float*>(take(lanes * cap * 4));
+  r.cmp_cnt = reinterpret_cast<int32_t*>(take(lanes * static_cast<size_t>(cmp_ctas_per_lane(dm) + 1) * 4));
+  r.epi_done = reinterpret_cast<int32_t*>(take(4));
+  int32_t* nv = reinterpret_cast<int32_t*>(take(lanes * 4));
   if (ws) *ws = w;
+  if (ws_reloc) *ws_reloc = r;
+  if (no_victims) *no_victims = nv;
   return off;
 }
 
@@ -151,6 +173,16 @@ cudaError_t launch_reset(const Ctx& ctx, cudaStream_t st) {
   ms(w.blk_tag, 0, P * 4);
   ms(w.counters, 0, 64);
   ms(w.epi_done, 0, 4);
+  const Workspace& r = ctx.ws_reloc;
+  ms(r.work_flag, 0, 4);
+  ms(r.need_admit, 0, lanes * 4);
+  ms(r.want_dst, 0, lanes * 4);
+  ms(r.plan_tlive, 0, lanes * 4);
+  ms(r.freed_flag, 0, P * 4);
+  ms(r.blk_tag, 0, P * 4);
+  ms(r.counters, 0, 64);
+  ms(r.epi_done, 0, 4);
+  ms(ctx.no_victims, 0, lanes * 4);
   return e;
 }
 
@@ -249,7 +281,9 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
     ctx->c.layer_budget[l] = cfg->budget;
     ctx->c.layer_recent[l] = cfg->recent_window;
   }
-  ctx->c.ws_bytes = kve::workspace_layout(*cfg, &ctx->c.ws, static_cast<char*>(bufs->workspace));
+  ctx->c.defer_reloc = false;
+  ctx->c.ws_bytes = kve::workspace_layout(*cfg, &ctx->c.ws, static_cast<char*>(bufs->workspace), &ctx->c.ws_reloc,
+                                          &ctx->c.no_victims);
   if (kve::prepare_kernels(ctx->c) != cudaSuccess || ctx->c.attend_ctas_per_sm < 1 ||
       kve::prepare_tensor_maps(ctx->c) != cudaSuccess) {
     delete[] ctx->c.tmaps;
@@ -278,6 +312,19 @@ kvevict_status kvevict_set_layer_budget(kvevict_ctx* ctx, int layer, int32_t bud
   ctx->c.layer_budget[layer] = budget;
   ctx->c.layer_recent[layer] = recent_window;
   return KVEVICT_OK;
+}
+
+kvevict_status kvevict_defer_relocation(kvevict_ctx* ctx, int32_t deferred) {
+  if (!ctx) return KVEVICT_E_INVALID_ARG;
+  ctx->c.defer_reloc = deferred != 0;
+  return KVEVICT_OK;
+}
+
+kvevict_status kvevict_relocate(kvevict_ctx* ctx, int layer, int32_t* freed, int32_t* n_freed, int32_t* moves,
+                                int32_t* n_moves, void* stream) {
+  if (!ctx || layer < 0 || layer >= ctx->c.dims.L) return KVEVICT_E_INVALID_ARG;
+  return cuda_status(kve::launch_compact(ctx->c, ctx->c.ws_reloc, layer, ctx->c.no_victims, ctx->c.no_victims, true,
+                                         freed, n_freed, moves, n_moves, static_cast<cudaStream_t>(stream)));
 }
 
 kvevict_status kvevict_reset(kvevict_ctx* ctx, void* stream) {
@@ -372,7 +419,8 @@ kvevict_status kvevict_select(kvevict_ctx* ctx, const void* keys, int32_t key_dt
 kvevict_status kvevict_compact(kvevict_ctx* ctx, int layer, const int32_t* victims, const int32_t* n_victims,
                                int32_t* freed, int32_t* n_freed, int32_t* moves, int32_t* n_moves, void* stream) {
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !victims || !n_victims) return KVEVICT_E_INVALID_ARG;
-  return cuda_status(kve::launch_compact(ctx->c, layer, victims, n_victims, freed, n_freed, moves, n_moves,
+  return cuda_status(kve::launch_compact(ctx->c, ctx->c.ws, layer, victims, n_victims, false, freed, n_freed, moves,
+                                         n_moves,
                                          static_cast<cudaStream_t>(stream)));
 }
 

@@ -1314,6 +1314,8 @@ cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, 
   A.dm = ctx.dims;
   A.dm.budget = ctx.layer_budget[layer];
   A.dm.R = ctx.layer_recent[layer];
+  // deferred relocation: Eq. (1)'s test never passes here (F <= 1)
+  if (ctx.defer_reloc) A.dm.theta_f = INFINITY;
   A.has_q = has_q ? 1 : 0;
   A.new_pos = new_pos;
   A.layer = layer;
@@ -1343,8 +1345,8 @@ cudaError_t prepare_epilogue() {
   return e;
 }
 
-cudaError_t launch_allocate(const Ctx& ctx, int layer, cudaStream_t stream) {
-  allocate_kernel<<<1, 1024, 0, stream>>>(layer_state(ctx, layer), ctx.ws, ctx.dims);
+cudaError_t launch_allocate(const Ctx& ctx, const Workspace& ws, int layer, cudaStream_t stream) {
+  allocate_kernel<<<1, 1024, 0, stream>>>(layer_state(ctx, layer), ws, ctx.dims);
   return cudaGetLastError();
 }
 

@@ -115,11 +115,19 @@ struct Ctx {
   // Only the decode epilogue reads them, from its launch arguments.
   int* layer_budget;
   int* layer_recent;
+  // Relocation deferred to kvevict_relocate (decode steps then plan none).
+  bool defer_reloc;
+  // The compaction and allocator scratch of kvevict_relocate: a second copy
+  // of those workspace fields (the rest alias ws), so a relocation on
+  // another stream shares no scratch with decode steps of other layers.
+  Workspace ws_reloc;
+  int32_t* no_victims;   // [lanes] zeros: kvevict_relocate removes nothing
 };
 
 // workspace layout (host)
 bool has_ring(const kvevict_config& c);
-size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base);
+size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base, Workspace* ws_reloc = nullptr,
+                        int32_t** no_victims = nullptr);
 Dims make_dims(const kvevict_config& c);
 LayerState layer_state(const Ctx& ctx, int layer);
 int d3_chunks(const Dims& dm, int sm_count);
@@ -142,9 +150,9 @@ cudaError_t launch_decode(const Ctx&, int layer, const void* q, const void* k_ne
 cudaError_t launch_select(const Ctx&, const void* keys, int key_dtype, const int32_t* positions,
                           const int32_t* counts, int n_lanes, int stride, int budget, int recent,
                           int32_t* victims, int32_t* n_victims, cudaStream_t);
-cudaError_t launch_compact(const Ctx&, int layer, const int32_t* victims, const int32_t* n_victims,
-                           int32_t* freed, int32_t* n_freed, int32_t* moves, int32_t* n_moves,
-                           cudaStream_t);
+cudaError_t launch_compact(const Ctx&, const Workspace& ws, int layer, const int32_t* victims,
+                           const int32_t* n_victims, bool gated, int32_t* freed, int32_t* n_freed,
+                           int32_t* moves, int32_t* n_moves, cudaStream_t);
 cudaError_t launch_score(const Ctx&, int layer, const void* q_win, int w, const int32_t* q_pos,
                          float* lse, float* a_out, float* scores, cudaStream_t);
 cudaError_t launch_score_mass(const Ctx&, int layer, const void* q_win, int w, const int32_t* q_pos,
@@ -160,7 +168,7 @@ cudaError_t launch_attend(const Ctx&, int layer, const void* q, const void* k_ne
 cudaError_t launch_epilogue(const Ctx&, int layer, bool has_q, int new_pos, const void* k_new,
                             const void* v_new, float* out, float* lse, int32_t* victims,
                             int32_t* n_victims, cudaStream_t);
-cudaError_t launch_allocate(const Ctx&, int layer, cudaStream_t);
+cudaError_t launch_allocate(const Ctx&, const Workspace& ws, int layer, cudaStream_t);
 cudaError_t launch_allocate_apply(const Ctx&, int layer, const void* k_new, const void* v_new,
                                   bool mark_freed, int32_t* moves, cudaStream_t, bool with_allocate);
 

@@ -443,7 +443,8 @@ __global__ void __launch_bounds__(kCmpThreads) compact_place_kernel(LayerState l
 // (vToken review, Sec. 3.3 Stage 1).
 constexpr int kBlkPer = 8;
 
-__global__ void __launch_bounds__(1024) compact_blocks_kernel(LayerState ls, Workspace ws, Dims dm, int cpl) {
+__global__ void __launch_bounds__(1024) compact_blocks_kernel(LayerState ls, Workspace ws, Dims dm, int cpl,
+                                                              int gated) {
   __shared__ int sh_scan[40];
   __shared__ int sh_m;
   const int l = blockIdx.x, tid = threadIdx.x;
@@ -511,7 +512,8 @@ __global__ void __launch_bounds__(1024) compact_blocks_kernel(LayerState ls, Wor
     *L.nblocks = out;
     ls.count[l] = m;
     const int ndst = (tl_tot + kBlock - 1) / kBlock;
-    const int plan = (out > 0 && src_tot > ndst) ? ndst : 0;
+    const bool over = !gated || (out > 0 && frag_over(m, out, dm.theta_f));
+    const int plan = (out > 0 && over && src_tot > ndst) ? ndst : 0;
     ws.need_admit[l] = 0;
     ws.want_dst[l] = plan;
     ws.plan_tlive[l] = plan ? tl_tot : 0;
@@ -814,30 +816,33 @@ cudaError_t launch_select(const Ctx& ctx, const void* keys, int key_dtype, const
   return cudaGetLastError();
 }
 
-cudaError_t launch_compact(const Ctx& ctx, int layer, const int32_t* victims, const int32_t* n_victims,
-                           int32_t* freed, int32_t* n_freed, int32_t* moves, int32_t* n_moves,
-                           cudaStream_t stream) {
+// gated: plan only lanes whose Eq. (1) waste ratio exceeds theta_f (the
+// relocation a decode step would have run); otherwise every lane whose plan
+// frees blocks (forced).
+cudaError_t launch_compact(const Ctx& ctx, const Workspace& ws, int layer, const int32_t* victims,
+                           const int32_t* n_victims, bool gated, int32_t* freed, int32_t* n_freed,
+                           int32_t* moves, int32_t* n_moves, cudaStream_t stream) {
   LayerState ls = layer_state(ctx, layer);
   {
     const int cpl = cmp_ctas_per_lane(ctx.dims);
     const dim3 grid(cpl, ctx.dims.lanes);
-    compact_remove_kernel<<<grid, kCmpThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, victims, n_victims, cpl);
-    compact_place_kernel<<<grid, kCmpThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl);
-    compact_blocks_kernel<<<ctx.dims.lanes, 1024, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl);
+    compact_remove_kernel<<<grid, kCmpThreads, 0, stream>>>(ls, ws, ctx.dims, victims, n_victims, cpl);
+    compact_place_kernel<<<grid, kCmpThreads, 0, stream>>>(ls, ws, ctx.dims, cpl);
+    compact_blocks_kernel<<<ctx.dims.lanes, 1024, 0, stream>>>(ls, ws, ctx.dims, cpl, gated ? 1 : 0);
   }
-  cudaError_t e = launch_allocate(ctx, layer, stream);
+  cudaError_t e = launch_allocate(ctx, ws, layer, stream);
   if (e != cudaSuccess) return e;
   {
     const int cpl = cmp_ctas_per_lane(ctx.dims);
     const dim3 grid(cpl, ctx.dims.lanes);
-    compact_reloc_count_kernel<<<grid, kCmpThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl);
+    compact_reloc_count_kernel<<<grid, kCmpThreads, 0, stream>>>(ls, ws, ctx.dims, cpl);
     if (ctx.dims.dtype == KVEVICT_BF16)
-      compact_reloc_move_kernel<__nv_bfloat16><<<grid, kCmpThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl, moves);
+      compact_reloc_move_kernel<__nv_bfloat16><<<grid, kCmpThreads, 0, stream>>>(ls, ws, ctx.dims, cpl, moves);
     else
-      compact_reloc_move_kernel<float><<<grid, kCmpThreads, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl, moves);
-    compact_reloc_finish_kernel<<<ctx.dims.lanes, 1024, 0, stream>>>(ls, ctx.ws, ctx.dims, cpl);
+      compact_reloc_move_kernel<float><<<grid, kCmpThreads, 0, stream>>>(ls, ws, ctx.dims, cpl, moves);
+    compact_reloc_finish_kernel<<<ctx.dims.lanes, 1024, 0, stream>>>(ls, ws, ctx.dims, cpl);
   }
-  compact_finalize_kernel<<<1, 1024, 0, stream>>>(ctx.ws, ctx.dims, freed, n_freed, n_moves);
+  compact_finalize_kernel<<<1, 1024, 0, stream>>>(ws, ctx.dims, freed, n_freed, n_moves);
   return cudaGetLastError();
 }
 

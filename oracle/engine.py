@@ -51,6 +51,7 @@ class Engine:
                        for l in wanted}
         self.deferred = 0
         self.layer_budget = {}
+        self.defer_reloc = False
 
     def set_layer_budget(self, layer, budget, recent_window):
         """Per-layer budget (H2O Guide, "Asymmetric Layer Allocation"): later
@@ -120,16 +121,17 @@ class Engine:
                 pending.append(lane)
                 new_rows[lane] = (kn, vn)
             victims.append(vict)
-        moves, freed2, deferred = self._finish_layer(PL, pending, new_rows, forced=False)
+        moves, freed2, deferred = self._finish_layer(PL, pending, new_rows, forced=False,
+                                                     relocate=not self.defer_reloc)
         return dict(out=out, lse=lse, victims=victims, moves=moves,
                     freed=sorted(freed + freed2), deferred=deferred, keys=all_keys, pos=all_pos)
 
-    def _finish_layer(self, PL, pending, new_rows, forced):
+    def _finish_layer(self, PL, pending, new_rows, forced, relocate=True):
         """Layer-level end of a step: admissions that need a block, then the
         lanes' relocation plans (computed after those admissions)."""
         PL.allocate_admissions(pending, new_rows)
         plans = {}
-        for lane in range(self.n_lanes):
+        for lane in (range(self.n_lanes) if relocate else ()):
             p = PL.plan(lane, forced, self.cfg.theta_f)
             if p is not None:
                 plans[lane] = p
@@ -195,6 +197,14 @@ class Engine:
             else:
                 raise ValueError("kind must be SNAPKV or H2O")
         return dict(lse=lse, scores=scores)
+
+    def relocate(self, layer):
+        """Deferred relocation (vToken review, Sec. 3.3 Stage 4: the copy
+        runs after the step, on its own stream): the theta_F-gated plans a
+        decode step of ``layer`` would have run, now.  Returns dict(freed
+        ascending, moves, deferred)."""
+        moves, freed, deferred = self._finish_layer(self.layers[layer], [], {}, forced=False)
+        return dict(freed=sorted(freed), moves=moves, deferred=deferred)
 
     def compact(self, layer, victims):
         """Forced compaction: evict ``victims`` (list per lane of positions),

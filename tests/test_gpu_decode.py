@@ -216,3 +216,61 @@ def test_per_layer_budgets_h2o_and_snapkv():
         eng.set_layer_budget(0, 50, 50)
     with pytest.raises(KvevictError):
         eng.set_layer_budget(2, 100, 10)
+
+
+def test_deferred_relocation_on_side_stream():
+    """vToken review, Sec. 3.3 Stage 4: decode steps with relocation deferred,
+    each layer's kvevict_relocate on a second stream after an event on the
+    step's stream, and the layer's next step waiting on an event after it;
+    the next layer's step runs meanwhile.  Tables, blocks, K/V rows, freed
+    blocks and move lists against the oracle doing the same (mass eviction
+    at step 1 makes relocation fire)."""
+    shp = scaled("h2o_70b", num_layers=2, batch=2, num_kv_heads=2, num_q_heads=16, ctx=900, steps=5,
+                 budget=120, recent_window=40)
+    wl = Workload(shp)
+    layers = (0, 1)
+    eng, orc = make_pair(shp, layers=list(layers))
+    eng.defer_relocation(True)
+    orc.defer_reloc = True
+    for layer in layers:
+        prefill_both(eng, orc, wl, layer)
+    main = torch.cuda.current_stream()
+    side = torch.cuda.Stream()
+    done = {layer: None for layer in layers}
+    outs = []
+    moved = 0
+    for t in range(shp.steps):
+        for layer in layers:
+            if done[layer] is not None:
+                main.wait_event(done[layer])
+            q, kn, vn, pos = wl.step(layer, t)
+            out, lse, vic, nv = eng.decode_step(layer, q.cuda(), kn.cuda(), vn.cuda(), pos,
+                                                victims=torch.empty_like(eng.victims),
+                                                n_victims=torch.empty_like(eng.n_victims))
+            ref = orc.decode_step(layer, q.double().numpy(), kn.double().numpy(), vn.double().numpy(), pos)
+            stepped = torch.cuda.Event()
+            stepped.record(main)
+            side.wait_event(stepped)
+            res = eng.relocate(layer, stream=side)
+            done[layer] = torch.cuda.Event()
+            done[layer].record(side)
+            rref = orc.relocate(layer)
+            outs.append((t, layer, out, lse, vic, nv, res, ref, rref))
+    torch.cuda.synchronize()
+    for t, layer, out, lse, vic, nv, res, ref, rref in outs:
+        assert_rows_close(out.cpu().numpy(), ref["out"], "step %d layer %d out" % (t, layer))
+        for l, v in enumerate(victim_lists(nv, vic)):
+            np.testing.assert_array_equal(v, ref["victims"][l])
+        freed, n_freed, moves, n_moves = res
+        np.testing.assert_array_equal(freed[:int(n_freed.item())].cpu().numpy(),
+                                      np.array(rref["freed"], np.int32))
+        m = int(n_moves.item())
+        assert m == len(rref["moves"]), (t, layer)
+        if m:
+            np.testing.assert_array_equal(moves[:m].cpu().numpy(), np.array(rref["moves"], np.int32))
+        moved += m
+    for layer in layers:
+        compare_states(gpu_state(eng, layer), oracle_state(orc, layer), shp.policy, "layer %d" % layer)
+    assert moved > 0
+    code, msg = eng.last_error()
+    assert code == 0, msg

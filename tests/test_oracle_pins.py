@@ -636,3 +636,39 @@ def test_per_layer_budget_equals_uniform_engine_per_layer():
             budget, recent = (20, 5) if layer == 0 else (12, 8)
             assert kept.size == min(n0 + t + 1, budget)
             assert set(range(pos - recent + 1, pos + 1)) <= set(kept.tolist())
+
+
+def test_deferred_relocation_equals_in_step_relocation():
+    """vToken review, Sec. 3.3 Stage 4: moving the relocation copy to after
+    the step (its own stream) changes no outcome.  A step with relocation
+    deferred, then relocate(), leaves the same tables, blocks, K/V rows and
+    move list as the step that relocates inline; without relocate() the
+    deferred step moves nothing."""
+    rng = np.random.default_rng(13)
+    d, n0 = 16, 200
+    cfg = _cfg(num_q_heads=2, budget=40, recent_window=8, blocks_per_pool=64)
+    A, B = Engine(cfg), Engine(cfg)
+    B.defer_reloc = True
+    K = rng.standard_normal((1, 1, n0, d))
+    V = rng.standard_normal((1, 1, n0, d))
+    A.prefill(0, K, V)
+    B.prefill(0, K, V)
+    fired = 0
+    for t in range(6):
+        q = rng.standard_normal((1, 2, d))
+        kn = rng.standard_normal((1, 1, d))
+        vn = rng.standard_normal((1, 1, d))
+        ra = A.decode_step(0, q, kn, vn, n0 + t)
+        rb = B.decode_step(0, q, kn, vn, n0 + t)
+        assert rb["moves"] == []
+        rr = B.relocate(0)
+        assert ra["moves"] == rr["moves"]
+        fired += len(ra["moves"]) > 0
+        la, lb = A.layers[0], B.layers[0]
+        np.testing.assert_array_equal(la.lanes[0].pos, lb.lanes[0].pos)
+        np.testing.assert_array_equal(la.lanes[0].slot, lb.lanes[0].slot)
+        np.testing.assert_array_equal(la.live, lb.live)
+        np.testing.assert_array_equal(la.owner, lb.owner)
+        np.testing.assert_array_equal(la.K, lb.K)
+        la.check_invariants()
+    assert fired >= 1
