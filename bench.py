@@ -51,7 +51,7 @@ def parse():
                          "JSON line each, instead of the decode-step bench line")
     ap.add_argument("--only", default="",
                     help="with --kernel-table: comma-separated subset of d3_32k, d3_128k, snapkv_pf_32k, "
-                         "snapkv_pf_128k, snapkv, dropkv_decode, toy")
+                         "snapkv_pf_128k, snapkv, dropkv_decode, toy, reloc")
     return ap.parse_args()
 
 
@@ -690,6 +690,64 @@ def run_kernel_table(args):
              nbytes=(n_before + lanes) * per_tok,
              extra={"steps_timed": len(timed_steps), "us_per_step": round(ms * 1e3, 2),
                     "note": "the timed steps captured into one CUDA graph through the C ABI and replayed once"})
+        code, msg = eng.last_error()
+        assert code == 0, msg
+        del eng
+        torch.cuda.empty_cache()
+
+    # the mass-eviction step of the 70B-shaped workload (8 of its 80 layers,
+    # full lane count and context): relocation inside each layer's step
+    # versus deferred to a second stream behind events (vToken review,
+    # Sec. 3.3 Stage 4), where layer l's relocation overlaps layer l+1's step
+    if not only or "reloc" in only:
+        shp = dataclasses.replace(shape("h2o_70b"), num_layers=8)
+        wl = Workload(shp)
+        eng = Engine(config_from(shp))
+        L, B, Hq, d = shp.num_layers, shp.batch, shp.num_q_heads, shp.head_dim
+        first = [wl.step(l, 0, device="cuda") for l in range(L)]
+        out = torch.empty((B, Hq, d), dtype=torch.float32, device="cuda")
+        lse = torch.empty((B, Hq), dtype=torch.float32, device="cuda")
+        freed = torch.empty((shp.blocks_per_pool,), dtype=torch.int32, device="cuda")
+        moves = torch.empty((eng.lanes * shp.max_tokens, 6), dtype=torch.int32, device="cuda")
+        n_freed = torch.empty((1,), dtype=torch.int32, device="cuda")
+        n_moves = torch.empty((1,), dtype=torch.int32, device="cuda")
+        side = torch.cuda.Stream()
+        for mode in ("in_step", "side_stream"):
+            samples, moved = [], 0
+            for rep in range(3):
+                eng.reset()
+                for l in range(L):
+                    K, V = wl.context(l, device="cuda")
+                    eng.prefill(l, K, V)
+                    del K, V
+                eng.defer_relocation(mode != "in_step")
+                torch.cuda.synchronize()
+                e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                for l in range(L):
+                    q, kn, vn, p = first[l]
+                    eng.decode_step(l, q, kn, vn, p, out, lse)
+                    if mode != "in_step":
+                        ev = torch.cuda.Event()
+                        ev.record(stream)
+                        side.wait_event(ev)
+                        eng.relocate(l, freed, n_freed, moves, n_moves, stream=side)
+                if mode != "in_step":
+                    ev = torch.cuda.Event()
+                    ev.record(side)
+                    stream.wait_event(ev)
+                e1.record(stream)
+                torch.cuda.synchronize()
+                samples.append(e0.elapsed_time(e1))
+                moved = sum(int(eng.stats(l)[5].item()) for l in range(L))
+            eng.defer_relocation(False)
+            samples.sort()
+            attended = L * eng.lanes * (shp.ctx + 1)
+            emit("mass-eviction decode step, relocation " + ("in the step" if mode == "in_step"
+                                                            else "on a second stream (vToken Stage 4)"),
+                 "h2o_70b, 8 of 80 layers", samples[1], samples[0], samples[-1],
+                 nbytes=attended * 2 * d * 2 + moved * 2 * d * 2 * 2,
+                 extra={"moved_tokens": moved, "layers": L})
         code, msg = eng.last_error()
         assert code == 0, msg
         del eng

@@ -631,6 +631,11 @@ __device__ __forceinline__ void tc_issue_s(uint32_t dS, const unsigned char* sq,
 constexpr int kWsRowThreads = 256;
 constexpr int kWsThreads = kWsRowThreads + 64;
 constexpr int kWsProducer = 8, kWsIssuer = 9;
+constexpr int kPrefetch = 4;   // tiles of key slots / positions the producer has in flight
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
 
 __device__ __forceinline__ void cp_async16_zf(void* dst, const void* src, bool ok) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 16 : 0)
@@ -713,17 +718,40 @@ __device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, in
   cp_async_arrive(&bar.qfull);
   const size_t lo = static_cast<size_t>(l) * A.dm.cap;
   const int rows_max = A.dm.P * kBlock;
+  // The keys' slots, positions (and |v|^2) reach shared memory by 4-byte
+  // cp.async kPrefetch tiles ahead, one commit group per tile, so the
+  // producer does not wait a global round trip per tile before it can
+  // issue the tile's copies.  Each lane copies and later reads only its own
+  // two keys of a tile.
+  __shared__ int pf_slot[kPrefetch][kTcKeys], pf_pos[kPrefetch][kTcKeys];
+  __shared__ float pf_vn[kPrefetch][kTcKeys];
+  auto prefetch = [&](int t) {
+    if (t < ntiles) {
+      const int b = t % kPrefetch;
+#pragma unroll
+      for (int kk = 0; kk < 2; ++kk) {
+        const int key = 2 * lane + kk, j = j_begin + t * kTcKeys + key;
+        if (j < j_end) {
+          cp_async4(&pf_slot[b][key], A.ls.slot + lo + j);
+          cp_async4(&pf_pos[b][key], A.ls.pos + lo + j);
+          if (kPass2 && kLoadV) cp_async4(&pf_vn[b][key], A.ws.d3_vn + lo + j);
+        }
+      }
+    }
+    cp_commit();
+  };
   auto fetch = [&](int t, int key, int& sl, int& ps, float& v) {
     const int j = j_begin + t * kTcKeys + key;
     sl = rows_max;
     ps = 0x7FFFFFFF;
     v = 0.f;
     if (t >= ntiles || j >= j_end) return;
-    int s = A.ls.slot[lo + j];
+    const int b = t % kPrefetch;
+    int s = pf_slot[b][key];
     if (s < 0 || s >= rows_max) { set_status(A.ws.status, ST_BAD_INDEX); s = 0; }
     sl = s;
-    ps = A.ls.pos[lo + j];
-    if (kPass2 && kLoadV) v = A.ws.d3_vn[lo + j];
+    ps = pf_pos[b][key];
+    if (kPass2 && kLoadV) v = pf_vn[b][key];
   };
   auto retire = [&](int u) {
     const int su = u % kTcStages;
@@ -739,11 +767,14 @@ __device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, in
   };
   int s0, s1, p0, p1;
   float v0, v1;
-  fetch(0, 2 * lane, s0, p0, v0);
-  fetch(0, 2 * lane + 1, s1, p1, v1);
+#pragma unroll
+  for (int u = 0; u < kPrefetch; ++u) prefetch(u);
 #pragma unroll 1
   for (int t = 0; t < ntiles; ++t) {
     const int st = t % kTcStages;
+    cp_wait<kPrefetch - 1>();   // tile t's group has landed
+    fetch(t, 2 * lane, s0, p0, v0);
+    fetch(t, 2 * lane + 1, s1, p1, v1);
     if (t >= kTcStages) {
       (void)mbar_wait_bounded(&bar.empty[st], ((t / kTcStages) - 1) & 1, A.ws.status);
       if (kPass2) retire(t - kTcStages);
@@ -799,8 +830,7 @@ __device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, in
         }
       }
     }
-    fetch(t + 1, 2 * lane, s0, p0, v0);
-    fetch(t + 1, 2 * lane + 1, s1, p1, v1);
+    prefetch(t + kPrefetch);   // into the buffer tile t was read from (its values are in registers)
   }
   if (kPass2) {
 #pragma unroll 1
