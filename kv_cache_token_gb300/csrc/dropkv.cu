@@ -868,6 +868,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
     d3_tc_pass1_kernel(D3Args A, const __grid_constant__ D3Maps mp) {
   extern __shared__ unsigned char d3_dsm[];
   __shared__ int sh_pos[kTcStages][kTcKeys];
+  __shared__ float sh_ml[128][2];
   __shared__ __align__(8) WsBars bar;
   __shared__ uint32_t sh_taddr;
   const int chunk = blockIdx.x, l = blockIdx.y;
@@ -885,6 +886,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   __syncthreads();
   tc::fence_after();
   const uint32_t tl = sh_taddr;
+  // at most 128 rows without V: one row tile; warps w and w + 4 share its
+  // rows, each taking 32 keys of every tile
+  const bool split = !kWithV && A.rows <= 128;
 
   if (warp == kWsProducer) {
     ws_produce<false, kWithV>(A, mp, l, j_begin, j_end, ntiles, sq, skv, sh_pos, nullptr, nullptr, bar);
@@ -897,7 +901,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         tc::fence_after();
         const unsigned char* kst = skv + st * kTcKV;
         tc_issue_s(tl + 256 + buf * 128, sq, kst, 0);
-        tc_issue_s(tl + 256 + buf * 128 + 64, sq, kst, 1);
+        if (!split) tc_issue_s(tl + 256 + buf * 128 + 64, sq, kst, 1);
         tc::commit(&bar.x_full[buf]);
       };
       issue_s(0);
@@ -921,6 +925,105 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         tc::commit(&bar.empty[st]);
         tc::commit(&bar.pv_done[buf]);
       }
+    }
+  } else if (!kWithV) {
+    // row warps without V: each row's running (max, sum); split: rows
+    // tid & 127, keys [32 h0, 32 h0 + 32) of each tile with h0 = warp / 4
+    const int r = split ? (tid & 127) : tid, m = r >> 7, h0 = split ? (warp >> 2) : 0;
+    const bool row_ok = r < A.rows;
+    const int qp = row_ok ? A.qpos[r % A.w] : -1;
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int nkeys = j_end - j_begin;
+    float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll 1
+    for (int t = 0; t < ntiles; ++t) {
+      const int st = t % kTcStages, buf = t & 1;
+      (void)mbar_wait_bounded(&bar.x_full[buf], (t >> 1) & 1, A.ws.status);
+      (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);   // key positions
+      tc::fence_after();
+      const uint32_t aS = tl + lane_off + 256 + buf * 128 + m * 64;
+      float s[kTcKeys];
+      {
+        uint32_t v[4][16];
+        tc::ld16(aS + h0 * 32, v[0]);
+        tc::ld16(aS + h0 * 32 + 16, v[1]);
+        if (!split) {
+          tc::ld16(aS + 32, v[2]);
+          tc::ld16(aS + 48, v[3]);
+        }
+        tc::wait_ld();
+#pragma unroll
+        for (int q4 = 0; q4 < 4; ++q4)
+#pragma unroll
+          for (int k = 0; k < 16; ++k) s[q4 * 16 + k] = __uint_as_float(v[q4][k]);
+      }
+      // the keys at or before the row: a prefix of the tile (positions ascend)
+      int vis = 0;
+      if (row_ok) {
+        const int lim = min(kTcKeys, nkeys - t * kTcKeys);
+        if (lim > 0 && sh_pos[st][lim - 1] <= qp) {
+          vis = lim;
+        } else {
+          int lo = 0, hi = lim;
+          while (lo < hi) {
+            const int mid = (lo + hi) >> 1;
+            if (sh_pos[st][mid] <= qp) lo = mid + 1; else hi = mid;
+          }
+          vis = lo;
+        }
+      }
+      // S read, positions read: the buffer and the stage are free
+      tc::fence_before();
+      __syncwarp();
+      if ((tid & 31) == 0) {
+        mbar_arrive1(&bar.x_free[buf]);
+        mbar_arrive1(&bar.empty[st]);
+      }
+#pragma unroll 1
+      for (int hh = 0; hh < (split ? 1 : 2); ++hh) {
+        const int kv = vis - (h0 + hh) * 32;
+        float tmax = -INFINITY;
+#pragma unroll
+        for (int k = 0; k < 32; ++k) {
+          s[k] = k < kv ? s[k] : -INFINITY;
+          tmax = fmaxf(tmax, s[k]);
+        }
+        tmax *= A.scale2;
+        if (tmax > m_run + kTcRescale) {
+          l_run *= (m_run == -INFINITY) ? 0.f : exp2f(m_run - tmax);
+          m_run = tmax;
+        }
+        const float negm = m_run == -INFINITY ? 0.f : -m_run;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < 32; ++k) ps[k & 3] += hw_exp2(fmaf(s[k], A.scale2, negm));
+        l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+#pragma unroll
+        for (int k = 0; k < 32; ++k) s[k] = s[32 + k];
+      }
+    }
+    const size_t stride = kD + 2;
+    if (split) {
+      // merge the two key halves of each row (named barrier of the row warps)
+      if (h0 == 1) {
+        sh_ml[r][0] = m_run;
+        sh_ml[r][1] = l_run;
+      }
+      asm volatile("bar.sync 1, 256;" ::: "memory");
+      if (h0 == 0) {
+        const float m1 = sh_ml[r][0], l1 = sh_ml[r][1];
+        const float M = fmaxf(m_run, m1);
+        if (M != -INFINITY) {
+          l_run = l_run * exp2f(m_run - M) + l1 * exp2f(m1 - M);
+          m_run = M;
+        }
+      }
+    }
+    float* part = A.ws.d3_part + (static_cast<size_t>(l) * A.chunks + chunk) * static_cast<size_t>(A.rows_cap) * stride +
+                  static_cast<size_t>(r) * stride;
+    if (row_ok && h0 == 0) {
+      part[kD] = m_run;
+      part[kD + 1] = l_run;
     }
   } else {
     // row warps: one window row per thread
@@ -990,19 +1093,6 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       // every key while the row has seen none (m = -inf, offset taken as 0)
       const float negm = m_run == -INFINITY ? 0.f : -m_run;
       float psum = 0.f;
-      if (!kWithV) {
-        // (max, sum) only: S has been read, the buffer and the stage are free
-        tc::fence_before();
-        __syncwarp();
-        if ((tid & 31) == 0) {
-          mbar_arrive1(&bar.x_free[buf]);
-          mbar_arrive1(&bar.empty[st]);
-        }
-#pragma unroll
-        for (int k = 0; k < kTcKeys; ++k) psum += hw_exp2(fmaf(s[k], A.scale2, negm));
-        l_run += psum;
-        continue;
-      }
       uint32_t hi[32], lo[32];
 #pragma unroll
       for (int k2 = 0; k2 < 32; ++k2) {
@@ -1147,7 +1237,10 @@ __global__ void __launch_bounds__(kWsThreads, 1)
   tc::fence_after();
   const uint32_t tl = sh_taddr;
   const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
-  const int r = tid, m = r >> 7;
+  // mass modes with at most 128 rows: one row tile; warps w and w + 4 share
+  // its rows, warp w summing keys 0-31 of each tile and warp w + 4 keys 32-63
+  const bool split = kMode != kResidual && A.rows <= 128;
+  const int r = split ? (tid & 127) : tid, m = r >> 7, h0 = split && tid < kWsRowThreads ? (warp >> 2) : 0;
   const bool row_ok = r < A.rows;
   const size_t wrow = static_cast<size_t>(l) * A.rows_cap + (row_ok ? r : 0);
   const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
@@ -1189,6 +1282,7 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         const unsigned char* vst = kst + 2 * kTcHalf;
 #pragma unroll
         for (int mm = 0; mm < 2; ++mm) {
+          if (split && mm == 1) break;
           tc_issue_s(tl + 256 + mm * 64, sq, kst, mm);
 #pragma unroll
           for (int ks = 0; ks < (kMode == kResidual ? 8 : 0); ++ks) {
@@ -1222,8 +1316,13 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         float sv[kTcKeys];
         {
           uint32_t v[4][16];
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4) tc::ld16(tl + lane_off + 256 + m * 64 + q4 * 16, v[q4]);
+          const uint32_t aS = tl + lane_off + 256 + m * 64;
+          tc::ld16(aS + h0 * 32, v[0]);
+          tc::ld16(aS + h0 * 32 + 16, v[1]);
+          if (!split) {
+            tc::ld16(aS + 32, v[2]);
+            tc::ld16(aS + 48, v[3]);
+          }
           tc::wait_ld();
 #pragma unroll
           for (int q4 = 0; q4 < 4; ++q4)
@@ -1249,8 +1348,9 @@ __global__ void __launch_bounds__(kWsThreads, 1)
             vis = lo;
           }
         }
+        if (split) sh_col[st][warp][(1 - h0) * 32 + lane] = 0.f;   // the other warp of the pair sums those keys
 #pragma unroll 1
-        for (int hf = 0; hf < 2; ++hf) {
+        for (int hf = h0; hf < (split ? h0 + 1 : 2); ++hf) {
           const int kv = vis - hf * 32;
 #pragma unroll
           for (int k2 = 0; k2 < kTcKeys / 2; ++k2)
