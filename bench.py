@@ -203,6 +203,32 @@ def committed_traffic():
 
 
 # ---------------------------------------------------------------------------
+# ranks: one replica per GPU, no collective on the data path
+# ---------------------------------------------------------------------------
+def rank_shape(shp, rank):
+    """The workload of one rank: the same shapes with the rank's own seed
+    (lanes are independent, so each GPU serves its own sequences: weak
+    scaling); rank 0 keeps the single-GPU seed."""
+    import dataclasses
+    return shp if rank == 0 else dataclasses.replace(shp, seed=shp.seed + 7919 * rank)
+
+
+def aggregate_over_ranks(ms_per_step, step_bytes, attended_per_step, device="cpu"):
+    """Whole-job figures: the slowest rank's step time, and the bytes and
+    tokens every rank processed (timing only; nothing of the data moves)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return ms_per_step, step_bytes, attended_per_step
+    t = torch.tensor([ms_per_step, step_bytes, attended_per_step], dtype=torch.float64, device=device)
+    mx = t.clone()
+    dist.all_reduce(mx, op=dist.ReduceOp.MAX)
+    sm = t.clone()
+    dist.all_reduce(sm, op=dist.ReduceOp.SUM)
+    return float(mx[0]), float(sm[1]), float(sm[2])
+
+
+# ---------------------------------------------------------------------------
 # GPU arm
 # ---------------------------------------------------------------------------
 def run_gpu(args):
@@ -225,7 +251,7 @@ def run_gpu(args):
         if world > 1:
             dist.barrier()
 
-    shp = shape(args.workload)
+    shp = rank_shape(shape(args.workload), rank)
     if args.profile_layers:
         import dataclasses
         shp = dataclasses.replace(shp, num_layers=args.profile_layers)
@@ -399,17 +425,10 @@ def run_gpu(args):
         assert code == 0, msg
 
     # aggregate over ranks: units processed by all / max time
-    value = step_bytes / (ms_per_step * 1e-3) / 1e9
-    tokens_s = attended / args.steps / (ms_per_step * 1e-3)
-    if world > 1:
-        t = torch.tensor([ms_per_step, step_bytes, attended / args.steps], dtype=torch.float64, device="cuda")
-        mx = t.clone()
-        dist.all_reduce(mx, op=dist.ReduceOp.MAX)
-        sm = t.clone()
-        dist.all_reduce(sm, op=dist.ReduceOp.SUM)
-        ms_per_step = float(mx[0])
-        value = float(sm[1]) / (ms_per_step * 1e-3) / 1e9
-        tokens_s = float(sm[2]) / (ms_per_step * 1e-3)
+    ms_per_step, all_bytes, all_attended = aggregate_over_ranks(ms_per_step, step_bytes, attended / args.steps,
+                                                                device="cuda")
+    value = all_bytes / (ms_per_step * 1e-3) / 1e9
+    tokens_s = all_attended / (ms_per_step * 1e-3)
 
     cpu = None
     if rank == 0 and cpu_lanes is not None:
