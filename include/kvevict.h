@@ -361,6 +361,14 @@ kvevict_status kvevict_attend_static(kvevict_ctx* ctx, int layer, const void* q,
 /* Writes KVEVICT_NSTATS int64 counters of one layer to out (device). */
 kvevict_status kvevict_stats(kvevict_ctx* ctx, int layer, int64_t* out, void* stream);
 
+/* Self-check of the timeout reporting (no counterpart in the pages): one
+ * thread waits on a barrier that nothing completes, gives up after `polls`
+ * polls (1 .. 2^22; KVEVICT_E_INVALID_ARG otherwise) and sets the timeout
+ * bit, exactly as the library's own bounded waits do when a producer never
+ * arrives; the next kvevict_last_error then returns KVEVICT_E_TIMEOUT and
+ * the context stays usable.  Nothing faults or hangs. */
+kvevict_status kvevict_check_wait_timeout(kvevict_ctx* ctx, int32_t polls, void* stream);
+
 /* Synchronises the device, reads and clears the status word.  Returns
  * KVEVICT_OK if no fault bit was set, else KVEVICT_E_DEVICE (or
  * KVEVICT_E_TIMEOUT for a bounded wait) and a description in buf. */

@@ -79,10 +79,11 @@ def lib():
         L.kvevict_relocate.argtypes = [V, ctypes.c_int, V, V, V, V, V]
         L.kvevict_stats.argtypes = [V, ctypes.c_int, V, V]
         L.kvevict_last_error.argtypes = [V, ctypes.c_char_p, ctypes.c_size_t]
+        L.kvevict_check_wait_timeout.argtypes = [V, I, V]
         for f in ("validate", "create", "reset", "set_layer_budget", "prefill", "decode_step", "attend", "finish_step",
                   "attend_static",
                   "score", "score_mass", "select",
-                  "compact", "defer_relocation", "relocate", "stats", "last_error"):
+                  "compact", "defer_relocation", "relocate", "stats", "check_wait_timeout", "last_error"):
             getattr(L, "kvevict_" + f).restype = ctypes.c_int
         _LIB = L
     return _LIB
@@ -331,6 +332,9 @@ class Engine:
         out = torch.zeros((NSTATS,), dtype=torch.int64, device=self.device)
         _check(lib().kvevict_stats(self.h, layer, _ptr(out), _stream(stream)), "kvevict_stats")
         return out
+
+    def check_wait_timeout(self, polls, stream=None):
+        _check(lib().kvevict_check_wait_timeout(self.h, polls, _stream(stream)), "kvevict_check_wait_timeout")
 
     def last_error(self):
         buf = ctypes.create_string_buffer(256)

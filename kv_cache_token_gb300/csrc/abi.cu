@@ -430,6 +430,11 @@ kvevict_status kvevict_stats(kvevict_ctx* ctx, int layer, int64_t* out, void* st
                                        static_cast<cudaStream_t>(stream)));
 }
 
+kvevict_status kvevict_check_wait_timeout(kvevict_ctx* ctx, int32_t polls, void* stream) {
+  if (!ctx || polls < 1 || polls > (1 << 22)) return KVEVICT_E_INVALID_ARG;
+  return cuda_status(kve::launch_wait_check(ctx->c, polls, static_cast<cudaStream_t>(stream)));
+}
+
 kvevict_status kvevict_last_error(kvevict_ctx* ctx, char* buf, size_t len) {
   if (!ctx) return KVEVICT_E_INVALID_ARG;
   cudaError_t e = cudaDeviceSynchronize();

@@ -158,6 +158,7 @@ cudaError_t launch_score(const Ctx&, int layer, const void* q_win, int w, const 
 cudaError_t launch_score_mass(const Ctx&, int layer, const void* q_win, int w, const int32_t* q_pos,
                               bool later, int pool_r, float* lse, float* scores, cudaStream_t);
 cudaError_t launch_stats(const Ctx&, int layer, long long* out, cudaStream_t);
+cudaError_t launch_wait_check(const Ctx&, int polls, cudaStream_t);
 cudaError_t launch_attend_into(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
                                float* logits, float* part_o, float* part_ml, int32_t* lane_nseg, cudaStream_t);
 cudaError_t prepare_epilogue();     // one-time attributes of the epilogue kernels
@@ -229,8 +230,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 // Waits for phase `parity` of the barrier; gives up after a bounded number
 // of polls (each try_wait itself suspends for a while), records ST_TIMEOUT
 // and returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* status) {
-  for (int spins = 0; spins < (1 << 22); ++spins)
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, uint32_t* status,
+                                                  int max_polls = 1 << 22) {
+  for (int spins = 0; spins < max_polls; ++spins)
     if (mbar_try_wait(bar, parity)) return true;
   set_status(status, ST_TIMEOUT);
   return false;

@@ -786,7 +786,24 @@ __global__ void __launch_bounds__(1024) stats_kernel(LayerState ls, Dims dm, lon
   }
 }
 
+// The bounded-wait path on its own: one thread waits on a shared-memory
+// mbarrier that expects one arrival and gets none, gives up after `polls`
+// polls, and records ST_TIMEOUT in the status word, as every wait of the
+// library does when its producer never arrives.
+__global__ void wait_check_kernel(uint32_t* status, int polls) {
+  __shared__ __align__(8) uint64_t bar;
+  if (threadIdx.x != 0) return;
+  mbar_init(&bar, 1);
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  (void)mbar_wait_bounded(&bar, 0, status, polls);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_check(const Ctx& ctx, int polls, cudaStream_t stream) {
+  wait_check_kernel<<<1, 32, 0, stream>>>(ctx.ws.status, polls);
+  return cudaGetLastError();
+}
 
 cudaError_t launch_prefill(const Ctx& ctx, int layer, const void* k, const void* v, int n, cudaStream_t stream) {
   LayerState ls = layer_state(ctx, layer);
