@@ -461,7 +461,7 @@ def run_gpu(args):
         "cpu_baseline": cpu,
         "e2e": e2e,
         "clocks": clocks,
-        "gpu_launches": 3 * L * args.steps,
+        "gpu_launches": eng.kernels_per_decode_step() * L * args.steps,
     }
     if args.profile_layers:
         line["profile_only"] = "%d layers: for profiling, not a bench number" % L

@@ -80,6 +80,8 @@ def lib():
         L.kvevict_stats.argtypes = [V, ctypes.c_int, V, V]
         L.kvevict_last_error.argtypes = [V, ctypes.c_char_p, ctypes.c_size_t]
         L.kvevict_check_wait_timeout.argtypes = [V, I, V]
+        L.kvevict_kernels_per_decode_step.argtypes = [V]
+        L.kvevict_kernels_per_decode_step.restype = I
         for f in ("validate", "create", "reset", "set_layer_budget", "prefill", "decode_step", "attend", "finish_step",
                   "attend_static",
                   "score", "score_mass", "select",
@@ -332,6 +334,9 @@ class Engine:
         out = torch.zeros((NSTATS,), dtype=torch.int64, device=self.device)
         _check(lib().kvevict_stats(self.h, layer, _ptr(out), _stream(stream)), "kvevict_stats")
         return out
+
+    def kernels_per_decode_step(self):
+        return int(lib().kvevict_kernels_per_decode_step(self.h))
 
     def check_wait_timeout(self, polls, stream=None):
         _check(lib().kvevict_check_wait_timeout(self.h, polls, _stream(stream)), "kvevict_check_wait_timeout")

@@ -284,8 +284,12 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   ctx->c.defer_reloc = false;
   ctx->c.ws_bytes = kve::workspace_layout(*cfg, &ctx->c.ws, static_cast<char*>(bufs->workspace), &ctx->c.ws_reloc,
                                           &ctx->c.no_victims);
-  if (kve::prepare_kernels(ctx->c) != cudaSuccess || ctx->c.attend_ctas_per_sm < 1 ||
-      kve::prepare_tensor_maps(ctx->c) != cudaSuccess) {
+  const bool ok = kve::prepare_kernels(ctx->c) == cudaSuccess && ctx->c.attend_ctas_per_sm >= 1 &&
+                  kve::prepare_tensor_maps(ctx->c) == cudaSuccess;
+  // the epilogue applies admissions and relocations itself when all its
+  // CTAs (one per lane) are resident at once
+  ctx->c.epi_applies = ok && static_cast<long long>(kve::epilogue_ctas_per_sm()) * sms >= ctx->c.dims.lanes;
+  if (!ok) {
     delete[] ctx->c.tmaps;
     delete[] ctx->c.layer_budget;
     delete[] ctx->c.layer_recent;
@@ -372,7 +376,8 @@ kvevict_status kvevict_finish_step(kvevict_ctx* ctx, int layer, const void* q, c
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   cudaError_t e = kve::launch_epilogue(ctx->c, layer, q != nullptr, new_pos, k_new, v_new, out, lse, victims,
                                        n_victims, st);
-  if (e == cudaSuccess) e = kve::launch_allocate_apply(ctx->c, layer, k_new, v_new, false, nullptr, st, false);
+  if (e == cudaSuccess && !ctx->c.epi_applies)
+    e = kve::launch_allocate_apply(ctx->c, layer, k_new, v_new, false, nullptr, st, false);
   ctx->c.last_layer = layer;
   return cuda_status(e);
 }
@@ -428,6 +433,11 @@ kvevict_status kvevict_stats(kvevict_ctx* ctx, int layer, int64_t* out, void* st
   if (!ctx || !out || layer < 0 || layer >= ctx->c.dims.L) return KVEVICT_E_INVALID_ARG;
   return cuda_status(kve::launch_stats(ctx->c, layer, reinterpret_cast<long long*>(out),
                                        static_cast<cudaStream_t>(stream)));
+}
+
+int32_t kvevict_kernels_per_decode_step(const kvevict_ctx* ctx) {
+  if (!ctx) return 0;
+  return ctx->c.epi_applies ? 2 : 3;
 }
 
 kvevict_status kvevict_check_wait_timeout(kvevict_ctx* ctx, int32_t polls, void* stream) {

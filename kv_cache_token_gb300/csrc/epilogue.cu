@@ -39,9 +39,17 @@ struct EpiArgs {
   Workspace ws;
   Dims dm;
   int has_q, new_pos, layer;
+  int applies;   // admission and relocation done here (no apply kernel follows)
   const void* k_new; const void* v_new;
   float* out; float* lse; int32_t* victims; int32_t* n_victims;
 };
+
+constexpr int kGenCounter = 7;   // ws.counters slot: allocator results published (one increment per call)
+
+template <typename KT>
+__device__ void apply_lane(const LayerState& ls, const Workspace& ws, const Dims& dm, const int l,
+                           const void* k_new, const void* v_new, int mark_freed, int32_t* moves, int* sh_scan,
+                           int* sh_mv_src, int* sh_mv_dst);
 
 template <typename KT>
 __device__ __forceinline__ void copy_row(KT* dst, const KT* src, int d) {
@@ -696,7 +704,7 @@ template <typename KT, bool kRing>
 __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs A) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ int sh_scan[40];
-  __shared__ int sh_work, sh_last, sh_flag, sh_sig;
+  __shared__ int sh_work, sh_last, sh_flag, sh_sig, sh_gen, sh_apply;
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   LaneRefs L = lane_refs(A.ls, dm, l);
@@ -704,7 +712,9 @@ __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs
   // list) is not written by the attention kernel: it is read before the
   // dependency wait, while the attention kernel drains.
   const int n = __ldcg(A.ls.count + l);
-  if (tid == 0) { sh_work = 0; sh_sig = 0; }
+  // the allocator-result generation before this CTA signals (it changes only
+  // after every CTA of the grid has signalled)
+  if (tid == 0) { sh_work = 0; sh_sig = 0; sh_gen = A.applies ? __ldcg(A.ws.counters + kGenCounter) : 0; }
   if (n < 0 || n >= dm.cap) {
     grid_dep_wait();
     grid_dep_launch();
@@ -732,6 +742,28 @@ __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs
       __threadfence();
       allocate_layer(A.ls, A.ws, dm, sh_scan, &sh_flag);
     }
+  }
+  if (!A.applies) return;
+  // Admission into a fresh block and relocation, here instead of in an
+  // apply kernel: the last CTA publishes the allocator's result (release);
+  // a lane that asked for blocks waits for it (bounded) and applies.  Every
+  // CTA of the grid is resident at once (the host checked), so the last CTA
+  // always runs while the others wait.
+  if (sh_last) {
+    __syncthreads();   // the allocator's stores by every thread of this CTA
+    if (tid == 0) {
+      __threadfence();
+      st_release_gpu(A.ws.counters + kGenCounter, sh_gen + 1);
+    }
+  }
+  if (tid == 0) {
+    const bool mine = __ldcg(A.ws.need_admit + l) != 0 || __ldcg(A.ws.want_dst + l) > 0;
+    sh_apply = mine && wait_changed_bounded(A.ws.counters + kGenCounter, sh_gen, A.ws.status);
+  }
+  __syncthreads();
+  if (sh_apply) {
+    int* mv = reinterpret_cast<int*>(dsm);   // the step is done with the dynamic shared memory
+    apply_lane<KT>(A.ls, A.ws, dm, l, A.k_new, A.v_new, 0, nullptr, sh_scan, mv, mv + kApplyThreads);
   }
 }
 
@@ -1164,26 +1196,25 @@ __global__ void __launch_bounds__(1024) allocate_kernel(LayerState ls, Workspace
 // ---------------------------------------------------------------------------
 // apply: one CTA per lane
 // ---------------------------------------------------------------------------
+// One lane's admission into its fresh block and its relocation plan (vToken
+// review, Sec. 3.3 Stage 3), after the layer allocator assigned the blocks;
+// all threads of a kApplyThreads CTA.
 template <typename KT>
-__global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(LayerState ls, Workspace ws, Dims dm,
-                                                           const void* k_new, const void* v_new,
-                                                           int mark_freed, int32_t* moves) {
-  __shared__ int sh_scan[40];
-  __shared__ int sh_mv_src[kApplyThreads], sh_mv_dst[kApplyThreads];
-  grid_dep_launch();    // the next layer's attention may start (it touches other state)
-  grid_dep_wait();      // the epilogue and its allocator are complete
-  const int l = blockIdx.x, tid = threadIdx.x;
-  if (ws.counters[1] == 0) return;
-  const int need = ws.need_admit[l];
-  const int ndst = ws.want_dst[l];
+__device__ void apply_lane(const LayerState& ls, const Workspace& ws, const Dims& dm, const int l,
+                           const void* k_new, const void* v_new, int mark_freed, int32_t* moves, int* sh_scan,
+                           int* sh_mv_src, int* sh_mv_dst) {
+  const int tid = threadIdx.x;
+  // the allocator (another CTA) wrote these; read them from L2
+  const int need = __ldcg(ws.need_admit + l);
+  const int ndst = __ldcg(ws.want_dst + l);
   if (!need && ndst == 0) return;
   LaneRefs L = lane_refs(ls, dm, l);
   const int d = dm.d;
   KT* kp = static_cast<KT*>(ls.k_pool);
   KT* vp = static_cast<KT*>(ls.v_pool);
-  const int m = ls.count[l];
+  const int m = __ldcg(ls.count + l);
   if (need) {
-    const int blk = ws.admit_block[l];
+    const int blk = __ldcg(ws.admit_block + l);
     const size_t s = static_cast<size_t>(blk) * kBlock;
     copy_row(kp + s * d, static_cast<const KT*>(k_new) + static_cast<size_t>(l) * d, d);
     copy_row(vp + s * d, static_cast<const KT*>(v_new) + static_cast<size_t>(l) * d, d);
@@ -1210,8 +1241,8 @@ __global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(LayerState ls, 
     }
     int nsrc_tot;
     (void)block_excl_scan(nsrc, sh_scan, &nsrc_tot);
-    const int dbeg = ws.dst_begin[l];
-    const int mbeg = ws.move_begin[l];
+    const int dbeg = __ldcg(ws.dst_begin + l);
+    const int mbeg = __ldcg(ws.move_begin + l);
     const int cpr = d * static_cast<int>(sizeof(KT)) / 16;     // 16-byte pieces per K or V row
     const size_t row_bytes = static_cast<size_t>(d) * sizeof(KT);
     unsigned char* kpb = reinterpret_cast<unsigned char*>(kp);
@@ -1232,7 +1263,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(LayerState ls, 
         sh_mv_src[ex] = -1;
       } else if (src) {
         const int q = q_total + ex;
-        const int db = ws.alloc_ids[dbeg + q / kBlock];
+        const int db = __ldcg(ws.alloc_ids + dbeg + q / kBlock);
         const int dof = q % kBlock;
         const int ns = db * kBlock + dof;
         sh_mv_src[ex] = old;
@@ -1276,7 +1307,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(LayerState ls, 
     }
     __syncthreads();
     for (int j = tid; j < ndst; j += blockDim.x) {
-      const int db = ws.alloc_ids[dbeg + j];
+      const int db = __ldcg(ws.alloc_ids + dbeg + j);
       const int filled = min(kBlock, q_total - j * kBlock);
       L.mask[db] = filled >= kBlock ? 0xFFFF : ((1 << filled) - 1);
     }
@@ -1291,7 +1322,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(LayerState ls, 
     }
     __syncthreads();
     const int nb2 = lane_prune_blocks(L, l, sh_scan);
-    for (int j = tid; j < ndst; j += blockDim.x) L.blocks[nb2 + j] = ws.alloc_ids[dbeg + j];
+    for (int j = tid; j < ndst; j += blockDim.x) L.blocks[nb2 + j] = __ldcg(ws.alloc_ids + dbeg + j);
     __syncthreads();
     if (tid == 0) {
       *L.nblocks = nb2 + ndst;
@@ -1301,6 +1332,20 @@ __global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(LayerState ls, 
       atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_FREED_RELOC]), (unsigned long long)nsrc_tot);
     }
   }
+}
+
+// Admission into a fresh block and relocation of each lane, after the layer
+// allocator, when the epilogue does not do it itself.
+template <typename KT>
+__global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(LayerState ls, Workspace ws, Dims dm,
+                                                           const void* k_new, const void* v_new,
+                                                           int mark_freed, int32_t* moves) {
+  __shared__ int sh_scan[40];
+  __shared__ int sh_mv_src[kApplyThreads], sh_mv_dst[kApplyThreads];
+  grid_dep_launch();    // the next layer's attention may start (it touches other state)
+  grid_dep_wait();      // the epilogue and its allocator are complete
+  if (ws.counters[1] == 0) return;
+  apply_lane<KT>(ls, ws, dm, blockIdx.x, k_new, v_new, mark_freed, moves, sh_scan, sh_mv_src, sh_mv_dst);
 }
 
 }  // namespace
@@ -1317,6 +1362,7 @@ cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, 
   // deferred relocation: Eq. (1)'s test never passes here (F <= 1)
   if (ctx.defer_reloc) A.dm.theta_f = INFINITY;
   A.has_q = has_q ? 1 : 0;
+  A.applies = ctx.epi_applies ? 1 : 0;
   A.new_pos = new_pos;
   A.layer = layer;
   A.k_new = k_new; A.v_new = v_new;
@@ -1343,6 +1389,18 @@ cudaError_t prepare_epilogue() {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_kernel<float, false>, a, bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_kernel<float, true>, a, bytes);
   return e;
+}
+
+int epilogue_ctas_per_sm() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_epilogue_kernel<__nv_bfloat16, true>, kEpiThreads,
+                                                    kEpiDynSmem) != cudaSuccess)
+    return 0;
+  int m = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&m, decode_epilogue_kernel<float, false>, kEpiThreads,
+                                                    kEpiDynSmem) != cudaSuccess)
+    return 0;
+  return n < m ? n : m;
 }
 
 cudaError_t launch_allocate(const Ctx& ctx, const Workspace& ws, int layer, cudaStream_t stream) {

@@ -122,6 +122,10 @@ struct Ctx {
   // another stream shares no scratch with decode steps of other layers.
   Workspace ws_reloc;
   int32_t* no_victims;   // [lanes] zeros: kvevict_relocate removes nothing
+  // Every CTA of the decode epilogue fits on the device at once (one per
+  // lane): the epilogue then also applies its lane's admission and
+  // relocation after the layer allocator, and no apply kernel is launched.
+  bool epi_applies;
 };
 
 // workspace layout (host)
@@ -162,6 +166,7 @@ cudaError_t launch_wait_check(const Ctx&, int polls, cudaStream_t);
 cudaError_t launch_attend_into(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
                                float* logits, float* part_o, float* part_ml, int32_t* lane_nseg, cudaStream_t);
 cudaError_t prepare_epilogue();     // one-time attributes of the epilogue kernels
+int epilogue_ctas_per_sm();         // co-resident decode-epilogue CTAs per SM
 cudaError_t prepare_dropkv();       // one-time attributes of the window-scoring kernels
 cudaError_t prepare_kernels(Ctx&);   // one-time kernel attributes and occupancy (not stream work)
 cudaError_t launch_attend(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
@@ -265,6 +270,25 @@ __device__ __forceinline__ int atomic_add_release(int* p, int v) {
   int old;
   asm volatile("atom.release.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
+}
+
+__device__ __forceinline__ void st_release_gpu(int* p, int v) {
+  asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_acquire_gpu(const int* p) {
+  int v;
+  asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+// Waits until *p differs from `old` (acquire), with a bounded number of polls
+// (about a second); on giving up records ST_TIMEOUT and returns false.
+__device__ __forceinline__ bool wait_changed_bounded(const int* p, int old, uint32_t* status) {
+  for (int polls = 0; polls < (1 << 20); ++polls) {
+    if (ld_acquire_gpu(p) != old) return true;
+    __nanosleep(64);
+  }
+  set_status(status, ST_TIMEOUT);
+  return false;
 }
 
 __device__ __forceinline__ void fence_proxy_async() {

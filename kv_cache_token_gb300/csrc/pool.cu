@@ -878,7 +878,7 @@ cudaError_t launch_decode(const Ctx& ctx, int layer, const void* q, const void* 
     if (e != cudaSuccess) return e;
   }
   e = launch_epilogue(ctx, layer, q != nullptr, new_pos, k_new, v_new, out, lse, victims, n_victims, stream);
-  if (e != cudaSuccess) return e;
+  if (e != cudaSuccess || ctx.epi_applies) return e;
   return launch_allocate_apply(ctx, layer, k_new, v_new, false, nullptr, stream, false);
 }
 

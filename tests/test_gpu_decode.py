@@ -274,3 +274,13 @@ def test_deferred_relocation_on_side_stream():
     assert moved > 0
     code, msg = eng.last_error()
     assert code == 0, msg
+
+
+def test_more_lanes_than_resident_epilogue_ctas():
+    """160 lanes: more than the epilogue CTAs the device holds at once (one
+    per SM), so admissions and relocations go through the separate apply
+    kernel instead of the epilogue; every step against the oracle, with
+    mass eviction and relocation at step 1."""
+    shp = scaled("h2o_70b", num_layers=1, batch=20, num_kv_heads=8, num_q_heads=64, ctx=200, steps=4,
+                 budget=64, recent_window=16)
+    run_decode(shp, 4)
