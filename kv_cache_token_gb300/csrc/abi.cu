@@ -77,6 +77,7 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base, Work
   w.freed_flag = reinterpret_cast<int32_t*>(take(P * 4));
   w.blk_tag = reinterpret_cast<int32_t*>(take(P * 4));
   w.counters = reinterpret_cast<int32_t*>(take(64));
+  w.freed_part = reinterpret_cast<int32_t*>(take(kFreedRanges * 4));
   w.cmp_pos = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
   w.cmp_slot = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
   w.cmp_score = reinterpret_cast<float*>(take(lanes * cap * 4));
@@ -108,6 +109,7 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base, Work
   r.freed_flag = reinterpret_cast<int32_t*>(take(P * 4));
   r.blk_tag = reinterpret_cast<int32_t*>(take(P * 4));
   r.counters = reinterpret_cast<int32_t*>(take(64));
+  r.freed_part = reinterpret_cast<int32_t*>(take(kFreedRanges * 4));
   r.cmp_pos = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
   r.cmp_slot = reinterpret_cast<int32_t*>(take(lanes * cap * 4));
   r.cmp_score = reinterpret_cast<float*>(take(lanes * cap * 4));

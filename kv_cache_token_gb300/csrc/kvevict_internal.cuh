@@ -56,6 +56,8 @@ struct LayerState {
 };
 
 // Library scratch, carved out of the caller's workspace.
+constexpr int kFreedRanges = 256;   // most CTAs the freed-list kernels use
+
 struct Workspace {
   uint32_t* status;                // 1 word
   int32_t* work_flag;              // 1 word: any lane needs the allocator this call
@@ -77,6 +79,7 @@ struct Workspace {
   int32_t* freed_flag;             // [P]  1 = released during this call
   int32_t* blk_tag;                // [P]  1 = source block of a running plan
   int32_t* counters;               // [8] per-call scalars
+  int32_t* freed_part;             // [kFreedRanges] freed blocks per range of the pool (freed list)
   int32_t* epi_done;               // 1 word: epilogue CTAs finished this call
   // DropKV prefill-window scorer
   float* d3_part;                  // [lanes][chunks][rows_cap][d + 2]

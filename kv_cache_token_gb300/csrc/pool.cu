@@ -712,44 +712,82 @@ __global__ void __launch_bounds__(1024) compact_reloc_finish_kernel(LayerState l
   }
 }
 
-// The freed list: block ids with a set flag, ascending; each warp takes 512
-// consecutive flags per pass, 32 per coalesced load, and places its set
-// flags by ballot; one scan of the 32 warp counts per pass.  The flags are
-// cleared.
-__global__ void __launch_bounds__(1024) compact_finalize_kernel(Workspace ws, Dims dm, int32_t* freed,
-                                                               int32_t* n_freed, int32_t* n_moves) {
+// The freed list: block ids with a set flag, ascending, in two launches over
+// ranges of the pool (`span` flags per CTA, walked kFreedChunk at a time):
+// count the set flags of each range, then each range writes its ids after
+// the earlier ranges' counts, by warp ballots (32 flags per coalesced load),
+// and clears them.
+constexpr int kFreedPer = 8;                           // flags a thread takes per chunk
+constexpr int kFreedChunk = 1024 * kFreedPer;          // flags per CTA per chunk
+__global__ void __launch_bounds__(1024) freed_count_kernel(Workspace ws, Dims dm, int span) {
   __shared__ int sh_scan[40];
-  constexpr int kPer = 16;
+  const int b0 = blockIdx.x * span, b1 = min(dm.P, b0 + span);
+  int c = 0;
+  for (int base = b0; base < b1; base += kFreedChunk) {
+#pragma unroll
+    for (int u = 0; u < kFreedPer; ++u) {
+      const int idx = base + u * 1024 + threadIdx.x;
+      c += (idx < b1 && ws.freed_flag[idx] != 0) ? 1 : 0;
+    }
+  }
+  int tot;
+  (void)block_excl_scan(c, sh_scan, &tot);
+  if (threadIdx.x == 0) ws.freed_part[blockIdx.x] = tot;
+}
+
+__global__ void __launch_bounds__(1024) freed_write_kernel(Workspace ws, Dims dm, int span, int32_t* freed,
+                                                           int32_t* n_freed, int32_t* n_moves) {
+  __shared__ int sh_scan[40];
+  __shared__ int sh_off;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const unsigned lt = (1u << lane) - 1u;
-  int total = 0;
-  for (int base = 0; base < dm.P; base += blockDim.x * kPer) {
-    const int wb = base + warp * 32 * kPer;
-    unsigned bal[kPer];
+  if (warp == 0) {
+    // this range's offset (and, in CTA 0, the total) from the range counts
+    int off = 0, all = 0;
+    for (int r = lane; r < static_cast<int>(gridDim.x); r += 32) {
+      const int c = ws.freed_part[r];
+      if (r < static_cast<int>(blockIdx.x)) off += c;
+      all += c;
+    }
+    for (int o = 16; o > 0; o >>= 1) {
+      off += __shfl_xor_sync(0xffffffffu, off, o);
+      all += __shfl_xor_sync(0xffffffffu, all, o);
+    }
+    if (lane == 0) {
+      sh_off = off;
+      if (blockIdx.x == 0) {
+        if (n_freed) *n_freed = all;
+        if (n_moves) *n_moves = ws.counters[1] ? ws.counters[2] : 0;
+      }
+    }
+  }
+  __syncthreads();
+  const int b0 = blockIdx.x * span, b1 = min(dm.P, b0 + span);
+  int off = sh_off;
+  for (int base = b0; base < b1; base += kFreedChunk) {
+    // each warp: 32 * kFreedPer consecutive flags of the chunk
+    const int wb = base + warp * 32 * kFreedPer;
+    unsigned bal[kFreedPer];
     int wtot = 0;
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
+    for (int u = 0; u < kFreedPer; ++u) {
       const int idx = wb + u * 32 + lane;
-      bal[u] = __ballot_sync(0xffffffffu, idx < dm.P && ws.freed_flag[idx] != 0);
+      bal[u] = __ballot_sync(0xffffffffu, idx < b1 && ws.freed_flag[idx] != 0);
       wtot += __popc(bal[u]);
     }
     int tot;
     const int wex = block_excl_scan(lane == 0 ? wtot : 0, sh_scan, &tot);
-    int off = total + __shfl_sync(0xffffffffu, wex, 0);
+    int o = off + __shfl_sync(0xffffffffu, wex, 0);
 #pragma unroll
-    for (int u = 0; u < kPer; ++u) {
+    for (int u = 0; u < kFreedPer; ++u) {
       if ((bal[u] >> lane) & 1u) {
         const int idx = wb + u * 32 + lane;
-        if (freed) freed[off + __popc(bal[u] & lt)] = idx;
+        if (freed) freed[o + __popc(bal[u] & lt)] = idx;
         ws.freed_flag[idx] = 0;
       }
-      off += __popc(bal[u]);
+      o += __popc(bal[u]);
     }
-    total += tot;
-  }
-  if (threadIdx.x == 0) {
-    if (n_freed) *n_freed = total;
-    if (n_moves) *n_moves = ws.counters[1] ? ws.counters[2] : 0;
+    off += tot;
   }
 }
 
@@ -859,7 +897,11 @@ cudaError_t launch_compact(const Ctx& ctx, const Workspace& ws, int layer, const
       compact_reloc_move_kernel<float><<<grid, kCmpThreads, 0, stream>>>(ls, ws, ctx.dims, cpl, moves);
     compact_reloc_finish_kernel<<<ctx.dims.lanes, 1024, 0, stream>>>(ls, ws, ctx.dims, cpl);
   }
-  compact_finalize_kernel<<<1, 1024, 0, stream>>>(ws, ctx.dims, freed, n_freed, n_moves);
+  const int chunks = (ctx.dims.P + kFreedChunk - 1) / kFreedChunk;
+  const int ranges = chunks < kFreedRanges ? chunks : kFreedRanges;
+  const int span = (chunks + ranges - 1) / ranges * kFreedChunk;
+  freed_count_kernel<<<ranges, 1024, 0, stream>>>(ws, ctx.dims, span);
+  freed_write_kernel<<<ranges, 1024, 0, stream>>>(ws, ctx.dims, span, freed, n_freed, n_moves);
   return cudaGetLastError();
 }
 
