@@ -559,21 +559,44 @@ __global__ void __launch_bounds__(kF32Chunk) attend_f32_kernel(AttendArgs a, int
   const bool ok = i <= n;
   const float* krow = nullptr;
   const size_t pool_rows = static_cast<size_t>(a.P) * kBlock;
+  // the chunk's pool rows, read once (-1: the new token, whose rows come
+  // with the call), so the P V loop below has no dependent global loads
+  __shared__ int sh_slot[kF32Chunk];
   if (ok) {
     if (i < n) {
       int s = a.slot[static_cast<size_t>(l) * a.cap + i];
       if (s < 0 || static_cast<size_t>(s) >= pool_rows) { set_status(a.status, ST_BAD_INDEX); s = 0; }
       krow = static_cast<const float*>(a.k_pool) + static_cast<size_t>(s) * D;
+      sh_slot[tid] = s;
     } else {
       krow = static_cast<const float*>(a.k_new) + static_cast<size_t>(l) * D;
+      sh_slot[tid] = -1;
     }
   }
+  // pool rows are 16-byte aligned (D floats, base checked at create); the
+  // caller's new row may not be
+  const bool k_vec = ok && (reinterpret_cast<uintptr_t>(krow) & 15) == 0;
   __shared__ float swarp[kF32Chunk / 32];
   for (int h = 0; h < a.g; ++h) {
     float s = -INFINITY;
     if (ok) {
       float acc = 0.f;
-      for (int e = 0; e < D; ++e) acc = fmaf(sq[h * D + e], krow[e], acc);
+      if (k_vec) {
+        const float4* k4 = reinterpret_cast<const float4*>(krow);
+        const float4* q4 = reinterpret_cast<const float4*>(sq + h * D);
+        float c0 = 0.f, c1 = 0.f, c2 = 0.f, c3 = 0.f;
+#pragma unroll 4
+        for (int e4 = 0; e4 < D / 4; ++e4) {
+          const float4 kv = k4[e4], qv = q4[e4];
+          c0 = fmaf(qv.x, kv.x, c0);
+          c1 = fmaf(qv.y, kv.y, c1);
+          c2 = fmaf(qv.z, kv.z, c2);
+          c3 = fmaf(qv.w, kv.w, c3);
+        }
+        acc = (c0 + c1) + (c2 + c3);
+      } else {
+        for (int e = 0; e < D; ++e) acc = fmaf(sq[h * D + e], krow[e], acc);
+      }
       s = acc * a.scale2;
       a.logits[(static_cast<size_t>(l) * a.g + h) * a.lcap + i] = s;
     }
@@ -597,25 +620,30 @@ __global__ void __launch_bounds__(kF32Chunk) attend_f32_kernel(AttendArgs a, int
     }
     __syncthreads();
   }
-  // O[h][e] = sum_i p[h][i] v_i[e]
+  // O[h][e] = sum_i p[h][i] v_i[e]: consecutive threads read consecutive
+  // elements of one value row; the rows' addresses come from shared memory,
+  // so the unrolled loads of several tokens are in flight together
   const size_t base = (static_cast<size_t>(l) * kMaxSeg + chunk) * a.g;
+  const int cnt = min(kF32Chunk, n + 1 - chunk * kF32Chunk);
+  const float* vpool = static_cast<const float*>(a.v_pool);
+  const float* vnew = static_cast<const float*>(a.v_new) + static_cast<size_t>(l) * D;
   for (int he = tid; he < a.g * D; he += blockDim.x) {
     const int h = he / D, e = he % D;
-    float acc = 0.f;
-    const int cnt = min(kF32Chunk, n + 1 - chunk * kF32Chunk);
-    for (int t = 0; t < cnt; ++t) {
-      const int it = chunk * kF32Chunk + t;
-      const float* vr;
-      if (it < n) {
-        int s = a.slot[static_cast<size_t>(l) * a.cap + it];
-        if (s < 0 || static_cast<size_t>(s) >= pool_rows) s = 0;
-        vr = static_cast<const float*>(a.v_pool) + static_cast<size_t>(s) * D;
-      } else {
-        vr = static_cast<const float*>(a.v_new) + static_cast<size_t>(l) * D;
-      }
-      acc = fmaf(sp[h * kF32Chunk + t], vr[e], acc);
+    float acc0 = 0.f, acc1 = 0.f;
+    int t = 0;
+#pragma unroll 8
+    for (; t + 1 < cnt; t += 2) {
+      const int s0 = sh_slot[t], s1 = sh_slot[t + 1];
+      const float v0 = s0 >= 0 ? vpool[static_cast<size_t>(s0) * D + e] : vnew[e];
+      const float v1 = s1 >= 0 ? vpool[static_cast<size_t>(s1) * D + e] : vnew[e];
+      acc0 = fmaf(sp[h * kF32Chunk + t], v0, acc0);
+      acc1 = fmaf(sp[h * kF32Chunk + t + 1], v1, acc1);
     }
-    a.part_o[(base + h) * D + e] = acc;
+    if (t < cnt) {
+      const int s0 = sh_slot[t];
+      acc0 = fmaf(sp[h * kF32Chunk + t], s0 >= 0 ? vpool[static_cast<size_t>(s0) * D + e] : vnew[e], acc0);
+    }
+    a.part_o[(base + h) * D + e] = acc0 + acc1;
   }
   if (tid < a.g) {
     a.part_ml[(base + tid) * 2 + 0] = sred[tid * 2 + 0];
