@@ -605,8 +605,8 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
     A.ls.count[l] = m + 1;
     if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
     // The allocator reads a lane's requests (and its count) only when they
-    // are non-zero; between steps they hold zero (the apply kernel clears
-    // what it consumed).  A lane that asks for blocks, released a block or
+    // are non-zero; between steps they hold zero (applying them, here or in
+    // the apply kernel, clears what was consumed).  A lane that asks for blocks, released a block or
     // clears a request left over publishes with release semantics; the
     // writes of the others are of no concern to the allocator.
     const bool publish = work || dead_j >= 0 || stale_req;
