@@ -193,6 +193,7 @@ class Engine:
         _check(lib().kvevict_reset(self.h, _stream(stream)), "kvevict_reset")
 
     def set_layer_budget(self, layer, budget, recent_window):
+        """kvevict_set_layer_budget: later decode steps of `layer` keep `budget` tokens."""
         _check(lib().kvevict_set_layer_budget(self.h, layer, budget, recent_window), "kvevict_set_layer_budget")
 
     def prefill(self, layer, k_ctx, v_ctx, stream=None):
@@ -314,9 +315,11 @@ class Engine:
         return freed, n_freed, moves, n_moves
 
     def defer_relocation(self, deferred=True):
+        """kvevict_defer_relocation: decode steps plan no relocation while set."""
         _check(lib().kvevict_defer_relocation(self.h, 1 if deferred else 0), "kvevict_defer_relocation")
 
     def relocate(self, layer, freed=None, n_freed=None, moves=None, n_moves=None, stream=None):
+        """kvevict_relocate on `stream`; returns (freed, n_freed, moves, n_moves)."""
         c = self.cfg
         if freed is None:
             freed = torch.empty((c.blocks_per_pool,), dtype=torch.int32, device=self.device)
@@ -336,9 +339,11 @@ class Engine:
         return out
 
     def kernels_per_decode_step(self):
+        """kvevict_kernels_per_decode_step (2 or 3)."""
         return int(lib().kvevict_kernels_per_decode_step(self.h))
 
     def check_wait_timeout(self, polls, stream=None):
+        """kvevict_check_wait_timeout: the next last_error() reports a timeout."""
         _check(lib().kvevict_check_wait_timeout(self.h, polls, _stream(stream)), "kvevict_check_wait_timeout")
 
     def last_error(self):
