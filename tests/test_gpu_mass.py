@@ -133,9 +133,15 @@ def test_snapkv_prefill_select_compact_pipeline():
 
 def test_snapkv_prefill_keys_full_32k_sampled_lanes():
     """The 32K SnapKV prefill workload at full size, two lanes checked."""
-    run_mass(shape_full(), SNAP, lanes=[0, 5])
+    run_mass(shape_full("snapkv_prefill"), SNAP, lanes=[0, 5])
 
 
-def shape_full():
+def test_snapkv_prefill_keys_full_128k_sampled_lane():
+    """The 128K SnapKV prefill workload at full size (the launch the bench
+    times), one lane checked."""
+    run_mass(shape_full("snapkv_prefill_128k"), SNAP, lanes=[6])
+
+
+def shape_full(name):
     from workloads import shape
-    return shape("snapkv_prefill")
+    return shape(name)
