@@ -5,7 +5,20 @@
 #include <cstring>
 #include <new>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "kvevict_internal.cuh"
+
+namespace {
+// An NVTX range around a call's launches, named after the call, for
+// profilers and tracers (inert and nearly free when none is attached).
+struct CallRange {
+  explicit CallRange(const char* name) { nvtxRangePushA(name); }
+  ~CallRange() { nvtxRangePop(); }
+  CallRange(const CallRange&) = delete;
+  CallRange& operator=(const CallRange&) = delete;
+};
+}  // namespace
 
 namespace kve {
 
@@ -328,6 +341,7 @@ kvevict_status kvevict_defer_relocation(kvevict_ctx* ctx, int32_t deferred) {
 
 kvevict_status kvevict_relocate(kvevict_ctx* ctx, int layer, int32_t* freed, int32_t* n_freed, int32_t* moves,
                                 int32_t* n_moves, void* stream) {
+  const CallRange range("kvevict_relocate");
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L) return KVEVICT_E_INVALID_ARG;
   return cuda_status(kve::launch_compact(ctx->c, ctx->c.ws_reloc, layer, ctx->c.no_victims, ctx->c.no_victims, true,
                                          freed, n_freed, moves, n_moves, static_cast<cudaStream_t>(stream)));
@@ -340,6 +354,7 @@ kvevict_status kvevict_reset(kvevict_ctx* ctx, void* stream) {
 
 kvevict_status kvevict_prefill(kvevict_ctx* ctx, int layer, const void* k_ctx, const void* v_ctx, int32_t n,
                                void* stream) {
+  const CallRange range("kvevict_prefill");
   if (!ctx || !k_ctx || !v_ctx || layer < 0 || layer >= ctx->c.dims.L || n < 1 || n > ctx->c.dims.cap - 1)
     return KVEVICT_E_INVALID_ARG;
   return cuda_status(kve::launch_prefill(ctx->c, layer, k_ctx, v_ctx, n, static_cast<cudaStream_t>(stream)));
@@ -348,6 +363,7 @@ kvevict_status kvevict_prefill(kvevict_ctx* ctx, int layer, const void* k_ctx, c
 kvevict_status kvevict_decode_step(kvevict_ctx* ctx, int layer, const void* q, const void* k_new, const void* v_new,
                                    int32_t new_pos, float* out, float* lse, int32_t* victims, int32_t* n_victims,
                                    void* stream) {
+  const CallRange range("kvevict_decode_step");
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !k_new || !v_new || !victims || !n_victims || new_pos < 0)
     return KVEVICT_E_INVALID_ARG;
   if (q && (!out || !lse)) return KVEVICT_E_INVALID_ARG;
@@ -360,6 +376,7 @@ kvevict_status kvevict_decode_step(kvevict_ctx* ctx, int layer, const void* q, c
 
 kvevict_status kvevict_attend(kvevict_ctx* ctx, int layer, const void* q, const void* k_new, const void* v_new,
                               void* stream) {
+  const CallRange range("kvevict_attend");
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !k_new || !v_new) return KVEVICT_E_INVALID_ARG;
   if (ctx->c.dims.policy == KVEVICT_DROPKV && !kve::has_ring(ctx->c.cfg)) return KVEVICT_E_INVALID_ARG;
   if (!q) return KVEVICT_OK;
@@ -371,6 +388,7 @@ kvevict_status kvevict_attend(kvevict_ctx* ctx, int layer, const void* q, const 
 kvevict_status kvevict_finish_step(kvevict_ctx* ctx, int layer, const void* q, const void* k_new, const void* v_new,
                                    int32_t new_pos, float* out, float* lse, int32_t* victims, int32_t* n_victims,
                                    void* stream) {
+  const CallRange range("kvevict_finish_step");
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !k_new || !v_new || !victims || !n_victims || new_pos < 0)
     return KVEVICT_E_INVALID_ARG;
   if (q && (!out || !lse)) return KVEVICT_E_INVALID_ARG;
@@ -386,6 +404,7 @@ kvevict_status kvevict_finish_step(kvevict_ctx* ctx, int layer, const void* q, c
 
 kvevict_status kvevict_score(kvevict_ctx* ctx, int layer, const void* q_win, int32_t w, const int32_t* q_pos,
                              float* lse, float* a_out, float* scores, void* stream) {
+  const CallRange range("kvevict_score");
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L) return KVEVICT_E_INVALID_ARG;
   if (!q_win) return KVEVICT_OK;   // null attention is inert
   if (w < 1 || w > ctx->c.dims.max_window || !q_pos || !lse || !a_out || !scores) return KVEVICT_E_INVALID_ARG;
@@ -398,6 +417,7 @@ kvevict_status kvevict_score(kvevict_ctx* ctx, int layer, const void* q_win, int
 
 kvevict_status kvevict_score_mass(kvevict_ctx* ctx, int layer, const void* q_win, int32_t w, const int32_t* q_pos,
                                   int32_t kind, float* lse, float* scores, void* stream) {
+  const CallRange range("kvevict_score_mass");
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L) return KVEVICT_E_INVALID_ARG;
   if (kind != KVEVICT_MASS_SNAPKV && kind != KVEVICT_MASS_H2O) return KVEVICT_E_INVALID_ARG;
   if (!q_win) return KVEVICT_OK;   // null attention is inert
@@ -414,6 +434,7 @@ kvevict_status kvevict_score_mass(kvevict_ctx* ctx, int layer, const void* q_win
 kvevict_status kvevict_select(kvevict_ctx* ctx, const void* keys, int32_t key_dtype, const int32_t* positions,
                               const int32_t* counts, int32_t n_lanes, int32_t stride, int32_t budget,
                               int32_t recent_window, int32_t* victims, int32_t* n_victims, void* stream) {
+  const CallRange range("kvevict_select");
   if (!ctx || !keys || !positions || !counts || !victims || !n_victims || n_lanes < 0 || stride < 1 ||
       recent_window < 1 || budget < 0)
     return KVEVICT_E_INVALID_ARG;
@@ -425,6 +446,7 @@ kvevict_status kvevict_select(kvevict_ctx* ctx, const void* keys, int32_t key_dt
 
 kvevict_status kvevict_compact(kvevict_ctx* ctx, int layer, const int32_t* victims, const int32_t* n_victims,
                                int32_t* freed, int32_t* n_freed, int32_t* moves, int32_t* n_moves, void* stream) {
+  const CallRange range("kvevict_compact");
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !victims || !n_victims) return KVEVICT_E_INVALID_ARG;
   return cuda_status(kve::launch_compact(ctx->c, ctx->c.ws, layer, victims, n_victims, false, freed, n_freed, moves,
                                          n_moves,
