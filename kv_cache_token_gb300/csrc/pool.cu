@@ -140,13 +140,16 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(const KeyT* keys, c
   if (threadIdx.x == 0) n_victims[l] = total;
 }
 
-// Selection by a cluster of kSelCluster CTAs per lane: each CTA takes a
+// Selection by a cluster of kCl CTAs per lane (8, or 16 for tables of at
+// least kSelWideFrom entries, where the wider split measured faster): each CTA takes a
 // contiguous slice of the lane's entries; every radix pass merges the CTAs'
 // 256-bin histograms into the leader CTA's shared memory (distributed shared
 // memory atomics) and the leader's bucket choice is read back by all; the
 // victims are written ascending, each CTA at the offset of the lower ranks'
 // counts.  Same result as select_kernel.
-constexpr int kSelCluster = 8;
+constexpr int kSelCluster = 8;        // CTAs per lane below kSelWideFrom entries
+constexpr int kSelClusterWide = 16;   // at or above (a non-portable cluster size)
+constexpr int kSelWideFrom = 1 << 16;
 constexpr int kSelClThreads = 1024;
 
 struct SelState {
@@ -155,8 +158,8 @@ struct SelState {
   int k_rem, done, inclusive;
 };
 
-template <typename KeyT>
-__global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelClThreads)
+template <typename KeyT, int kCl>
+__global__ void __launch_bounds__(kSelClThreads)
     select_cluster_kernel(const KeyT* keys, const int32_t* positions, const int32_t* counts, int stride,
                           int budget, int R, int32_t* victims, int32_t* n_victims) {
   namespace cg = cooperative_groups;
@@ -167,7 +170,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelClThre
   __shared__ int sh_count;           // this CTA's number of victims
   __shared__ int sh_scan[40];
   const int rank = static_cast<int>(cluster.block_rank());
-  const int l = blockIdx.x / kSelCluster;
+  const int l = blockIdx.x / kCl;
   const int tid = threadIdx.x;
   const int n = max(0, min(counts[l], stride));
   const int k = max(0, n - budget);
@@ -178,7 +181,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelClThre
   const KeyT* kk = keys + static_cast<size_t>(l) * stride;
   const int32_t* pp = positions + static_cast<size_t>(l) * stride;
   const int cut = pp[n - 1] - R + 1;
-  const int chunk = (n + kSelCluster - 1) / kSelCluster;
+  const int chunk = (n + kCl - 1) / kCl;
   const int i_begin = min(n, rank * chunk), i_end = min(n, i_begin + chunk);
   int* lead_hist = cluster.map_shared_rank(sh_hist, 0);
   SelState* lead = cluster.map_shared_rank(&sh_state, 0);
@@ -261,7 +264,7 @@ __global__ void __cluster_dims__(kSelCluster, 1, 1) __launch_bounds__(kSelClThre
   if (tid == 0) sh_count = tot;
   cluster.sync();
   int offset = 0, all = 0;
-  for (int q = 0; q < kSelCluster; ++q) {
+  for (int q = 0; q < kCl; ++q) {
     const int cq = *cluster.map_shared_rank(&sh_count, q);
     if (q < rank) offset += cq;
     all += cq;
@@ -857,18 +860,47 @@ cudaError_t launch_prefill(const Ctx& ctx, int layer, const void* k, const void*
   return cudaGetLastError();
 }
 
+// One cluster of kCl CTAs per lane (thread-block cluster launch attribute;
+// sizes above 8 need the non-portable opt-in).
+template <typename KeyT, int kCl>
+static cudaError_t launch_sel(int n_lanes, cudaStream_t stream, const KeyT* keys, const int32_t* positions,
+                              const int32_t* counts, int stride, int budget, int recent, int32_t* victims,
+                              int32_t* n_victims) {
+  const auto fn = select_cluster_kernel<KeyT, kCl>;
+  if (kCl > 8) {
+    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+    if (e != cudaSuccess) return e;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(n_lanes * kCl);
+  cfg.blockDim = dim3(kSelClThreads);
+  cfg.stream = stream;
+  cudaLaunchAttribute at[1];
+  at[0].id = cudaLaunchAttributeClusterDimension;
+  at[0].val.clusterDim.x = kCl;
+  at[0].val.clusterDim.y = 1;
+  at[0].val.clusterDim.z = 1;
+  cfg.attrs = at;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, fn, keys, positions, counts, stride, budget, recent, victims, n_victims);
+}
+
 cudaError_t launch_select(const Ctx& ctx, const void* keys, int key_dtype, const int32_t* positions,
                           const int32_t* counts, int n_lanes, int stride, int budget, int recent,
                           int32_t* victims, int32_t* n_victims, cudaStream_t stream) {
   (void)ctx;
   if (n_lanes <= 0) return cudaSuccess;
   if (key_dtype == KVEVICT_KEY_F64)
-    select_cluster_kernel<double><<<n_lanes * kSelCluster, kSelClThreads, 0, stream>>>(
-        static_cast<const double*>(keys), positions, counts, stride, budget, recent, victims, n_victims);
-  else
-    select_cluster_kernel<float><<<n_lanes * kSelCluster, kSelClThreads, 0, stream>>>(
-        static_cast<const float*>(keys), positions, counts, stride, budget, recent, victims, n_victims);
-  return cudaGetLastError();
+    return stride >= kSelWideFrom
+               ? launch_sel<double, kSelClusterWide>(n_lanes, stream, static_cast<const double*>(keys), positions,
+                                                     counts, stride, budget, recent, victims, n_victims)
+               : launch_sel<double, kSelCluster>(n_lanes, stream, static_cast<const double*>(keys), positions, counts,
+                                                 stride, budget, recent, victims, n_victims);
+  return stride >= kSelWideFrom
+             ? launch_sel<float, kSelClusterWide>(n_lanes, stream, static_cast<const float*>(keys), positions, counts,
+                                                  stride, budget, recent, victims, n_victims)
+             : launch_sel<float, kSelCluster>(n_lanes, stream, static_cast<const float*>(keys), positions, counts,
+                                              stride, budget, recent, victims, n_victims);
 }
 
 // gated: plan only lanes whose Eq. (1) waste ratio exceeds theta_f (the
