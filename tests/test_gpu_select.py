@@ -29,10 +29,12 @@ def _run(eng, keys, pos, counts, budget, R):
         np.testing.assert_array_equal(got[l], ref[l], err_msg="lane %d" % l)
 
 
-@pytest.mark.parametrize("dtype", [np.float32, np.float64])
-def test_random_with_ties(eng, dtype):
+@pytest.mark.parametrize("dtype,lanes,stride", [(np.float32, 37, 3000), (np.float64, 37, 3000),
+                                                (np.float32, 8, 70000)])
+def test_random_with_ties(eng, dtype, lanes, stride):
+    """Ties, NaN, -0 and tiny keys; 70,000-entry tables take the 16-CTA
+    cluster path (64K entries and more), the others the 8-CTA one."""
     rng = np.random.default_rng(11)
-    lanes, stride = 37, 3000
     keys = np.zeros((lanes, stride), dtype)
     pos = np.zeros((lanes, stride), np.int32)
     counts = rng.integers(0, stride + 1, lanes)
@@ -50,7 +52,7 @@ def test_random_with_ties(eng, dtype):
             keys[l, ::7] = -0.0
             keys[l, 3::7] = 0.0
         pos[l] = np.sort(rng.choice(10 * stride, stride, replace=False))
-    for budget, R in [(100, 10), (2999, 1), (500, 50), (10, 3)]:
+    for budget, R in [(100, 10), (stride - 1, 1), (500, 50), (10, 3)]:
         _run(eng, keys, pos, counts, budget, R)
 
 
