@@ -518,6 +518,7 @@ def tensor_peak():
 
 
 def run_kernel_table(args):
+    import numpy as np
     import torch
     import __graft_entry__
     __graft_entry__.build()
@@ -600,6 +601,29 @@ def run_kernel_table(args):
                     del K, V
                     eng.score(0, q, qp, lse, a_out, scores)
                     eng.select(scores, pos, cnt, shp.budget, shp.recent_window, victims, nvic)
+                if rep == 0:
+                    # the block-granular counterfactual of the same eviction
+                    # (vToken review, Sec. 2 and Eq. (1)): only blocks whose 16
+                    # tokens all died are freed, nothing moves
+                    torch.cuda.synchronize()
+                    slots_h = eng.slots[0].cpu().numpy()
+                    cnt_h = eng.counts[0].cpu().numpy()
+                    pos_h = eng.positions[0].cpu().numpy()
+                    vic_h, nv_h = victims.cpu().numpy(), nvic.cpu().numpy()
+                    bg = {"freed_blocks": 0, "blocks": 0, "live": 0, "half_empty": 0}
+                    blocks_before = 0
+                    for l in range(lanes):
+                        n_l = int(cnt_h[l])
+                        dead = np.isin(pos_h[l, :n_l], vic_h[l, :int(nv_h[l])])
+                        blk = slots_h[l, :n_l] // 16
+                        live = np.bincount(blk[~dead], minlength=int(blk.max()) + 1)
+                        held = np.bincount(blk, minlength=live.size) > 0
+                        blocks_before += int(held.sum())
+                        bg["freed_blocks"] += int((held & (live == 0)).sum())
+                        bg["blocks"] += int((held & (live > 0)).sum())
+                        bg["live"] += int(live.sum())
+                        bg["half_empty"] += int((held & (live > 0) & (live <= 8)).sum())
+                    bg["waste_F"] = round(1.0 - bg["live"] / (16.0 * bg["blocks"]), 4) if bg["blocks"] else 0.0
                 # outputs allocated outside the timed call
                 freed = torch.empty((shp.blocks_per_pool,), dtype=torch.int32, device="cuda")
                 moves = torch.empty((lanes * shp.max_tokens, 6), dtype=torch.int32, device="cuda")
@@ -617,7 +641,12 @@ def run_kernel_table(args):
             samples.sort()
             emit("D5 token-level compaction (plan, allocate, gather, release)", name, samples[1], samples[0],
                  samples[-1], nbytes=moved * 2 * d * 2 * 2 + int(nvic.sum().item()) * 3 * 4,
-                 extra={"moved_tokens": moved, "freed_blocks": nf, "blocks_after": st[9], "live_after": st[10]})
+                 extra={"moved_tokens": moved, "freed_blocks": nf, "blocks_after": st[9], "live_after": st[10],
+                        "blocks_before": blocks_before,
+                        "token_level": {"freed_blocks": blocks_before - st[9], "blocks": st[9], "live": st[10],
+                                        "half_empty": st[11],
+                                        "waste_F": round(1.0 - st[10] / (16.0 * st[9]), 4) if st[9] else 0.0},
+                        "block_granular": bg})
         code, msg = eng.last_error()
         assert code == 0, msg
         del eng
