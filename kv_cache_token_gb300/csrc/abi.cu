@@ -300,7 +300,7 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   ctx->c.ws_bytes = kve::workspace_layout(*cfg, &ctx->c.ws, static_cast<char*>(bufs->workspace), &ctx->c.ws_reloc,
                                           &ctx->c.no_victims);
   const bool ok = kve::prepare_kernels(ctx->c) == cudaSuccess && ctx->c.attend_ctas_per_sm >= 1 &&
-                  kve::prepare_tensor_maps(ctx->c) == cudaSuccess;
+                  kve::prepare_select() == cudaSuccess && kve::prepare_tensor_maps(ctx->c) == cudaSuccess;
   // the epilogue applies admissions and relocations itself when all its
   // CTAs (one per lane) are resident at once
   ctx->c.epi_applies = ok && static_cast<long long>(kve::epilogue_ctas_per_sm()) * sms >= ctx->c.dims.lanes;

@@ -170,6 +170,7 @@ cudaError_t launch_attend_into(const Ctx&, int layer, const void* q, const void*
                                float* logits, float* part_o, float* part_ml, int32_t* lane_nseg, cudaStream_t);
 cudaError_t prepare_epilogue();     // one-time attributes of the epilogue kernels
 int epilogue_ctas_per_sm();         // co-resident decode-epilogue CTAs per SM
+cudaError_t prepare_select();       // one-time attributes of the selection kernels
 cudaError_t prepare_dropkv();       // one-time attributes of the window-scoring kernels
 cudaError_t prepare_kernels(Ctx&);   // one-time kernel attributes and occupancy (not stream work)
 cudaError_t launch_attend(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,

@@ -867,10 +867,6 @@ static cudaError_t launch_sel(int n_lanes, cudaStream_t stream, const KeyT* keys
                               const int32_t* counts, int stride, int budget, int recent, int32_t* victims,
                               int32_t* n_victims) {
   const auto fn = select_cluster_kernel<KeyT, kCl>;
-  if (kCl > 8) {
-    const cudaError_t e = cudaFuncSetAttribute(fn, cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
-    if (e != cudaSuccess) return e;
-  }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(n_lanes * kCl);
   cfg.blockDim = dim3(kSelClThreads);
@@ -883,6 +879,17 @@ static cudaError_t launch_sel(int n_lanes, cudaStream_t stream, const KeyT* keys
   cfg.attrs = at;
   cfg.numAttrs = 1;
   return cudaLaunchKernelEx(&cfg, fn, keys, positions, counts, stride, budget, recent, victims, n_victims);
+}
+
+// Opt-in to the non-portable cluster size of the wide selection (once per
+// context creation).
+cudaError_t prepare_select() {
+  cudaError_t e = cudaFuncSetAttribute(select_cluster_kernel<float, kSelClusterWide>,
+                                       cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(select_cluster_kernel<double, kSelClusterWide>,
+                             cudaFuncAttributeNonPortableClusterSizeAllowed, 1);
+  return e;
 }
 
 cudaError_t launch_select(const Ctx& ctx, const void* keys, int key_dtype, const int32_t* positions,
