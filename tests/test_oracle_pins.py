@@ -246,6 +246,35 @@ def test_snapkv_window_sum_slot_order_and_null_inert():
     np.testing.assert_array_equal(hist[:, 0], 2.0)
 
 
+def test_snapkv_window_sum_is_float64_in_slot_order():
+    """SnapKV, "How it works" (sums recomputed afresh, slot 0 upward) and
+    "Complexity" (float32 history, the sums are doubles).  Two float32 rows
+    whose float64 sum depends on the order, with the slot-order results
+    written out as exact binary values:
+    row 0 = (1, 2^-53, 2^-53, 2^-53): slot order rounds 1 + 2^-53 to 1 three
+    times (ties to even) -> exactly 1.  Pairwise order gives 1 + 2^-52,
+    reverse order 1 + 2^-51, the exact sum rounds to 1 + 2^-51.
+    row 1 = (1, 2^-24, 2^-24, 0): float64 holds 1 + 2^-23 exactly, while a
+    float32 accumulation rounds 1 + 2^-24 back to 1 twice."""
+    t53, t24 = 2.0 ** -53, 2.0 ** -24
+    hist = np.array([[1.0, t53, t53, t53], [1.0, t24, t24, 0.0]], dtype=np.float32)
+    assert np.all(hist.astype(np.float64) == np.array([[1.0, t53, t53, t53], [1.0, t24, t24, 0.0]]))
+    sums = snapkv.window_sums(hist)
+    assert sums.dtype == np.float64
+    assert sums[0] == 1.0
+    assert sums[1] == 1.0 + 2.0 ** -23
+    # the orders and precisions a mistake would take give other values
+    assert (1.0 + t53) + (t53 + t53) == 1.0 + 2.0 ** -52
+    assert ((t53 + t53) + t53) + 1.0 == 1.0 + 2.0 ** -51
+    assert math.fsum([1.0, t53, t53, t53]) == 1.0 + 2.0 ** -51
+    f32 = np.float32(0.0)
+    for x in hist[1]:
+        f32 = np.float32(f32 + x)
+    assert float(f32) == 1.0
+    # the eviction keys with pooling off are these sums
+    np.testing.assert_array_equal(snapkv.keys(hist, 1), [1.0, 1.0 + 2.0 ** -23])
+
+
 def test_snapkv_refusals():
     assert snapkv.validate(1024, 256, 32, 6) == "pool_kernel_even"
     assert snapkv.validate(256, 256, 32, 7) == "recent_ge_budget"
@@ -481,6 +510,29 @@ def test_dropkv_decode_null_query_is_inert():
     np.testing.assert_array_equal(L.hist[:13], hist[:13])
 
 
+def test_bound_constants_by_hand():
+    """The reading of the explainer's undefined c and eps, on a 2-D example
+    computed by hand.  Weights p = (.5, .1, .2, .2), values v0 = (.6, .8),
+    v1 = (-1, 0), v2 = (0, -1), v3 = (-1, -1): the output a = sum p v = 0, so
+    the candidates' residuals a - v are (1, 0), (0, 1), (1, 1) (token 0 is
+    protected).  Their unit directions average to the direction (1, 1)/sqrt 2,
+    so u = (1, 1)/sqrt 2 and c = min(1/sqrt 2, 1/sqrt 2, 1) = 1/sqrt 2;
+    eps = the largest candidate weight = .2 (not token 0's .5); with k = 2
+    the bound is 1/(c (1 - .2)(1 - .4)) = sqrt 2 / .48."""
+    p = np.array([0.5, 0.1, 0.2, 0.2])
+    V = np.array([[0.6, 0.8], [-1.0, 0.0], [0.0, -1.0], [-1.0, -1.0]])
+    c, eps, bound = dropkv.bound_constants(p, V, [1, 2, 3], 2)
+    assert c == pytest.approx(1.0 / math.sqrt(2.0), abs=1e-12)
+    assert eps == 0.2
+    assert bound == pytest.approx(math.sqrt(2.0) / 0.48, rel=1e-12)
+    # k eps >= 1: the guarantee does not apply
+    assert dropkv.bound_constants(p, V, [1, 2, 3], 5) is None
+    # residuals (1, 0) and (-1, 0) lie in no common cone: no c > 0
+    p2 = np.array([0.5, 0.25, 0.25])
+    V2 = np.array([[0.0, 0.0], [-1.0, 0.0], [1.0, 0.0]])
+    assert dropkv.bound_constants(p2, V2, [1, 2], 1) is None
+
+
 def test_greedy_within_bound_when_cone_holds():
     """Exhaustive best-k on <= 12 tokens; whenever the reading's c > 0 and
     k eps < 1 hold, greedy's shift is within 1/(c(1-eps)(1-k eps)) of the best."""
@@ -592,6 +644,54 @@ def test_admission_reuses_lowest_evicted_slot():
     assert PL.admit(0, 42, np.ones(2), np.ones(2))
     assert PL.lanes[0].slot[-1] == 2 * 16 + 8    # then the tail block
     PL.check_invariants()
+
+
+def test_new_blocks_go_to_waiting_lanes_lowest_id_first():
+    """Reading of the vToken review, Sec. 3.2-3.3 (the pages leave the order
+    open): new blocks are the lowest free ids, handed to the lanes whose new
+    token found no free slot in ascending lane order, the token at offset 0.
+    Hand-built pool of 8 blocks: lane 1 holds block 0, lane 3 holds blocks 2
+    and 5, so the free ids are 1, 3, 4, 6, 7; lanes 0, 2 and 3 wait."""
+    d = 2
+    PL = paged.PagedLayer(4, 8, d)
+    for blk, lane in ((0, 1), (2, 3), (5, 3)):
+        PL.assign(blk, lane)
+        PL.live[blk, :] = True
+    np.testing.assert_array_equal(PL.free_blocks(), [1, 3, 4, 6, 7])
+    rows = {}
+    for lane in (0, 2, 3):
+        PL.lanes[lane].append(100 + lane, -1)           # admitted, waiting for a block
+        rows[lane] = (np.full(d, 10.0 + lane), np.full(d, 20.0 + lane))
+    PL.allocate_admissions([0, 2, 3], rows)
+    expect = {0: 1, 2: 3, 3: 4}                         # lane -> block, by hand
+    for lane, blk in expect.items():
+        assert PL.owner[blk] == lane
+        assert blk in PL.lanes[lane].blocks
+        assert PL.lanes[lane].slot[-1] == blk * 16      # offset 0 (Eq. (2))
+        np.testing.assert_array_equal(PL.live[blk], [True] + [False] * 15)
+        np.testing.assert_array_equal(PL.K[blk, 0], rows[lane][0])
+        np.testing.assert_array_equal(PL.V[blk, 0], rows[lane][1])
+    np.testing.assert_array_equal(PL.free_blocks(), [6, 7])
+    # a pool with fewer free blocks than waiting lanes refuses the admission
+    for lane in (0, 1):
+        PL.lanes[lane].append(200 + lane, -1)
+    PL.assign(7, 2)
+    with pytest.raises(paged.NoBlocks):
+        PL.allocate_admissions([0, 1], {0: rows[0], 1: rows[0]})
+
+
+def test_stats_counts_half_full_blocks_by_hand():
+    """vToken review, Sec. 2 (Fig. 1: blocks at 50% utilisation or less) and
+    Eq. (1).  Owned blocks with live counts 8, 9, 16, 1 and one free block:
+    N = 4, live = 34, F = 1 - 34/64, and the blocks at <= 50% are the ones
+    with 8 and 1 live tokens (8/16 is exactly one half; 9/16 is above)."""
+    PL = paged.PagedLayer(2, 5, 2)
+    for blk, lane, n_live in ((0, 0, 8), (1, 0, 9), (2, 1, 16), (4, 1, 1)):
+        PL.assign(blk, lane)
+        PL.live[blk, :n_live] = True
+    N, live, F, half = PL.stats()
+    assert (N, live, half) == (4, 34, 2)
+    assert F == 1.0 - 34.0 / 64.0
 
 
 def test_kv_bytes_formula():
