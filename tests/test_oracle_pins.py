@@ -512,15 +512,17 @@ def test_dropkv_decode_null_query_is_inert():
 
 def test_bound_constants_by_hand():
     """The reading of the explainer's undefined c and eps, on a 2-D example
-    computed by hand.  Weights p = (.5, .1, .2, .2), values v0 = (.6, .8),
-    v1 = (-1, 0), v2 = (0, -1), v3 = (-1, -1): the output a = sum p v = 0, so
-    the candidates' residuals a - v are (1, 0), (0, 1), (1, 1) (token 0 is
-    protected).  Their unit directions average to the direction (1, 1)/sqrt 2,
-    so u = (1, 1)/sqrt 2 and c = min(1/sqrt 2, 1/sqrt 2, 1) = 1/sqrt 2;
+    computed by hand.  Weights p = (.5, .1, .2, .2), values v0 = (.8, 1.6),
+    v1 = (-2, 0), v2 = (0, -3), v3 = (-1, -1): the output a = sum p v = 0, so
+    the candidates' residuals a - v are (2, 0), (0, 3), (1, 1) (token 0 is
+    protected).  Their unit directions (1, 0), (0, 1), (1, 1)/sqrt 2 average
+    to the direction (1, 1)/sqrt 2, so u = (1, 1)/sqrt 2 and
+    c = min(1/sqrt 2, 1/sqrt 2, 1) = 1/sqrt 2 (the unnormalised residuals
+    would give sqrt 2, and their mean direction u = (3, 4)/5 would give .6);
     eps = the largest candidate weight = .2 (not token 0's .5); with k = 2
     the bound is 1/(c (1 - .2)(1 - .4)) = sqrt 2 / .48."""
     p = np.array([0.5, 0.1, 0.2, 0.2])
-    V = np.array([[0.6, 0.8], [-1.0, 0.0], [0.0, -1.0], [-1.0, -1.0]])
+    V = np.array([[0.8, 1.6], [-2.0, 0.0], [0.0, -3.0], [-1.0, -1.0]])
     c, eps, bound = dropkv.bound_constants(p, V, [1, 2, 3], 2)
     assert c == pytest.approx(1.0 / math.sqrt(2.0), abs=1e-12)
     assert eps == 0.2
