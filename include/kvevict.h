@@ -351,7 +351,9 @@ kvevict_status kvevict_relocate(kvevict_ctx* ctx, int layer, int32_t* freed, int
  * needing more returns KVEVICT_E_SCRATCH_LIMIT before anything is enqueued.
  * It calls no cudaMalloc and no allocating routine.  The first call on a
  * device looks up that array's device address (cudaGetSymbolAddress) with
- * the device current; make that first call before any stream capture.
+ * the device current; make that first call before any stream capture.  The
+ * address is kept with the CUDA context it belongs to and looked up again
+ * when another context is current (after cudaDeviceReset, for example).
  * Every call shares the array and it keeps the last call's contents (no
  * part of it needs to start at zero); calls that overlap on the GPU race. */
 #define KVEVICT_STATIC_SCRATCH_BYTES (16u << 20)

@@ -71,7 +71,7 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base, Work
   Workspace w;
   w.status = reinterpret_cast<uint32_t*>(take(4));
   w.work_flag = reinterpret_cast<int32_t*>(take(4));
-  for (int c = 0; c < 2; ++c) {
+  for (int c = 0; c < kScratchBufs; ++c) {
     w.logits_buf[c] = reinterpret_cast<float*>(take(lanes * g * dm.lcap * 4));
     w.part_o_buf[c] = reinterpret_cast<float*>(take(lanes * kMaxSeg * g * d * 4));
     w.part_ml_buf[c] = reinterpret_cast<float*>(take(lanes * kMaxSeg * g * 2 * 4));
@@ -96,6 +96,8 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base, Work
   w.cmp_score = reinterpret_cast<float*>(take(lanes * cap * 4));
   w.cmp_cnt = reinterpret_cast<int32_t*>(take(lanes * static_cast<size_t>(cmp_ctas_per_lane(dm) + 1) * 4));
   w.epi_done = reinterpret_cast<int32_t*>(take(4));
+  w.reads_done = reinterpret_cast<uint32_t*>(take(kScratchBufs * 4));
+  w.apply_list = reinterpret_cast<int32_t*>(take(lanes * 4));
   if (dm.max_window > 0 && dm.dtype == KVEVICT_BF16 && dm.d == 128) {
     const size_t rows = static_cast<size_t>(d3_rows_max(dm));
     const size_t chunks = static_cast<size_t>(d3_chunks(dm, 0));
@@ -128,6 +130,7 @@ size_t workspace_layout(const kvevict_config& c, Workspace* ws, char* base, Work
   r.cmp_score = reinterpret_cast<float*>(take(lanes * cap * 4));
   r.cmp_cnt = reinterpret_cast<int32_t*>(take(lanes * static_cast<size_t>(cmp_ctas_per_lane(dm) + 1) * 4));
   r.epi_done = reinterpret_cast<int32_t*>(take(4));
+  r.apply_list = reinterpret_cast<int32_t*>(take(lanes * 4));
   int32_t* nv = reinterpret_cast<int32_t*>(take(lanes * 4));
   if (ws) *ws = w;
   if (ws_reloc) *ws_reloc = r;
@@ -188,6 +191,7 @@ cudaError_t launch_reset(const Ctx& ctx, cudaStream_t st) {
   ms(w.blk_tag, 0, P * 4);
   ms(w.counters, 0, 64);
   ms(w.epi_done, 0, 4);
+  ms(w.reads_done, 0, kScratchBufs * 4);
   const Workspace& r = ctx.ws_reloc;
   ms(r.work_flag, 0, 4);
   ms(r.need_admit, 0, lanes * 4);
@@ -283,18 +287,25 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   ctx->c.sm_count = sms;
   ctx->c.device = dev;
   ctx->c.last_layer = -1;
+  ctx->c.last_kind = kve::kLaunchOther;
+  for (int c = 0; c < kve::kScratchBufs; ++c) ctx->c.epi_launches[c] = 0u;
   ctx->c.tmaps = nullptr;
   ctx->c.layer_budget = new (std::nothrow) int[cfg->num_layers];
   ctx->c.layer_recent = new (std::nothrow) int[cfg->num_layers];
-  if (!ctx->c.layer_budget || !ctx->c.layer_recent) {
+  ctx->c.layer_steady = new (std::nothrow) bool[cfg->num_layers];
+  if (!ctx->c.layer_budget || !ctx->c.layer_recent || !ctx->c.layer_steady) {
     delete[] ctx->c.layer_budget;
     delete[] ctx->c.layer_recent;
+    delete[] ctx->c.layer_steady;
     delete ctx;
     return KVEVICT_E_INVALID_ARG;
   }
   for (int l = 0; l < cfg->num_layers; ++l) {
     ctx->c.layer_budget[l] = cfg->budget;
     ctx->c.layer_recent[l] = cfg->recent_window;
+    // unknown contents (the buffers may hold a saved state): the large
+    // epilogue until a decode step or a reset says otherwise
+    ctx->c.layer_steady[l] = false;
   }
   ctx->c.defer_reloc = false;
   ctx->c.ws_bytes = kve::workspace_layout(*cfg, &ctx->c.ws, static_cast<char*>(bufs->workspace), &ctx->c.ws_reloc,
@@ -304,10 +315,15 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   // the epilogue applies admissions and relocations itself when all its
   // CTAs (one per lane) are resident at once
   ctx->c.epi_applies = ok && static_cast<long long>(kve::epilogue_ctas_per_sm()) * sms >= ctx->c.dims.lanes;
+  // the lean H2O epilogue: bf16 pools, groups of at most 8 heads, at most one
+  // lane per SM (one lean CTA fits beside the attention kernel's CTAs)
+  ctx->c.lean_epi = ok && cfg->policy == KVEVICT_H2O && cfg->kv_dtype == KVEVICT_BF16 && ctx->c.dims.g <= 8 &&
+                    ctx->c.dims.lanes <= sms && ctx->c.lean_coresident && kve::lean_epilogue_ctas_per_sm() >= 1;
   if (!ok) {
     delete[] ctx->c.tmaps;
     delete[] ctx->c.layer_budget;
     delete[] ctx->c.layer_recent;
+    delete[] ctx->c.layer_steady;
     delete ctx;
     return KVEVICT_E_CUDA;
   }
@@ -320,6 +336,7 @@ void kvevict_destroy(kvevict_ctx* ctx) {
   delete[] ctx->c.tmaps;
   delete[] ctx->c.layer_budget;
   delete[] ctx->c.layer_recent;
+  delete[] ctx->c.layer_steady;
   delete ctx;
 }
 
@@ -328,6 +345,8 @@ static kvevict_status cuda_status(cudaError_t e) { return e == cudaSuccess ? KVE
 kvevict_status kvevict_set_layer_budget(kvevict_ctx* ctx, int layer, int32_t budget, int32_t recent_window) {
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || recent_window < 1) return KVEVICT_E_INVALID_ARG;
   if (recent_window >= budget) return KVEVICT_E_RECENT_GE_BUDGET;
+  // a smaller budget: the next step may evict more than one token per lane
+  if (budget < ctx->c.layer_budget[layer]) ctx->c.layer_steady[layer] = false;
   ctx->c.layer_budget[layer] = budget;
   ctx->c.layer_recent[layer] = recent_window;
   return KVEVICT_OK;
@@ -343,12 +362,17 @@ kvevict_status kvevict_relocate(kvevict_ctx* ctx, int layer, int32_t* freed, int
                                 int32_t* n_moves, void* stream) {
   const CallRange range("kvevict_relocate");
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L) return KVEVICT_E_INVALID_ARG;
+  kve::note_other(ctx->c);
   return cuda_status(kve::launch_compact(ctx->c, ctx->c.ws_reloc, layer, ctx->c.no_victims, ctx->c.no_victims, true,
                                          freed, n_freed, moves, n_moves, static_cast<cudaStream_t>(stream)));
 }
 
 kvevict_status kvevict_reset(kvevict_ctx* ctx, void* stream) {
   if (!ctx) return KVEVICT_E_INVALID_ARG;
+  kve::note_other(ctx->c);
+  for (int l = 0; l < ctx->c.dims.L; ++l) ctx->c.layer_steady[l] = true;   // every lane empty
+  // the reset zeroes the epilogue counts of the scratch copies
+  for (int c = 0; c < kve::kScratchBufs; ++c) ctx->c.epi_launches[c] = 0u;
   return cuda_status(kve::launch_reset(ctx->c, static_cast<cudaStream_t>(stream)));
 }
 
@@ -357,6 +381,8 @@ kvevict_status kvevict_prefill(kvevict_ctx* ctx, int layer, const void* k_ctx, c
   const CallRange range("kvevict_prefill");
   if (!ctx || !k_ctx || !v_ctx || layer < 0 || layer >= ctx->c.dims.L || n < 1 || n > ctx->c.dims.cap - 1)
     return KVEVICT_E_INVALID_ARG;
+  kve::note_other(ctx->c);
+  ctx->c.layer_steady[layer] = ctx->c.layer_steady[layer] && n <= ctx->c.layer_budget[layer];
   return cuda_status(kve::launch_prefill(ctx->c, layer, k_ctx, v_ctx, n, static_cast<cudaStream_t>(stream)));
 }
 
@@ -370,7 +396,6 @@ kvevict_status kvevict_decode_step(kvevict_ctx* ctx, int layer, const void* q, c
   if (ctx->c.dims.policy == KVEVICT_DROPKV && !kve::has_ring(ctx->c.cfg)) return KVEVICT_E_INVALID_ARG;
   const cudaError_t e = kve::launch_decode(ctx->c, layer, q, k_new, v_new, new_pos, out, lse, victims, n_victims,
                                            static_cast<cudaStream_t>(stream));
-  ctx->c.last_layer = layer;
   return cuda_status(e);
 }
 
@@ -380,8 +405,8 @@ kvevict_status kvevict_attend(kvevict_ctx* ctx, int layer, const void* q, const 
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !k_new || !v_new) return KVEVICT_E_INVALID_ARG;
   if (ctx->c.dims.policy == KVEVICT_DROPKV && !kve::has_ring(ctx->c.cfg)) return KVEVICT_E_INVALID_ARG;
   if (!q) return KVEVICT_OK;
-  const cudaError_t e = kve::launch_attend(ctx->c, layer, q, k_new, v_new, static_cast<cudaStream_t>(stream));
-  ctx->c.last_layer = layer;
+  const cudaError_t e = kve::launch_attend(ctx->c, layer, q, k_new, v_new, static_cast<cudaStream_t>(stream), false);
+  if (e == cudaSuccess) kve::note_attend(ctx->c, layer);
   return cuda_status(e);
 }
 
@@ -394,11 +419,17 @@ kvevict_status kvevict_finish_step(kvevict_ctx* ctx, int layer, const void* q, c
   if (q && (!out || !lse)) return KVEVICT_E_INVALID_ARG;
   if (ctx->c.dims.policy == KVEVICT_DROPKV && !kve::has_ring(ctx->c.cfg)) return KVEVICT_E_INVALID_ARG;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
+  bool apply_kernel = false;
   cudaError_t e = kve::launch_epilogue(ctx->c, layer, q != nullptr, new_pos, k_new, v_new, out, lse, victims,
-                                       n_victims, st);
-  if (e == cudaSuccess && !ctx->c.epi_applies)
+                                       n_victims, st, &apply_kernel);
+  if (e == cudaSuccess) {
+    kve::note_epilogue(ctx->c, layer);
+    ctx->c.layer_steady[layer] = true;
+  }
+  if (e == cudaSuccess && apply_kernel) {
     e = kve::launch_allocate_apply(ctx->c, layer, k_new, v_new, false, nullptr, st, false);
-  ctx->c.last_layer = layer;
+    kve::note_apply(ctx->c);
+  }
   return cuda_status(e);
 }
 
@@ -411,6 +442,7 @@ kvevict_status kvevict_score(kvevict_ctx* ctx, int layer, const void* q_win, int
   if (reinterpret_cast<uintptr_t>(q_win) % 16 || reinterpret_cast<uintptr_t>(a_out) % 16)
     return KVEVICT_E_INVALID_ARG;   // 16-byte row copies and stores
   if (ctx->c.dims.dtype != KVEVICT_BF16 || ctx->c.dims.d != 128) return KVEVICT_E_DTYPE;
+  kve::note_other(ctx->c);
   return cuda_status(kve::launch_score(ctx->c, layer, q_win, w, q_pos, lse, a_out, scores,
                                        static_cast<cudaStream_t>(stream)));
 }
@@ -427,6 +459,7 @@ kvevict_status kvevict_score_mass(kvevict_ctx* ctx, int layer, const void* q_win
   const int pk = ctx->c.cfg.pool_kernel;
   if (kind == KVEVICT_MASS_SNAPKV && (pk < 1 || pk % 2 == 0)) return KVEVICT_E_POOL_KERNEL_EVEN;
   const int pool_r = kind == KVEVICT_MASS_SNAPKV && pk > 1 ? (pk - 1) / 2 : -1;
+  kve::note_other(ctx->c);
   return cuda_status(kve::launch_score_mass(ctx->c, layer, q_win, w, q_pos, kind == KVEVICT_MASS_H2O, pool_r, lse,
                                             scores, static_cast<cudaStream_t>(stream)));
 }
@@ -440,6 +473,7 @@ kvevict_status kvevict_select(kvevict_ctx* ctx, const void* keys, int32_t key_dt
     return KVEVICT_E_INVALID_ARG;
   if (key_dtype != KVEVICT_KEY_F32 && key_dtype != KVEVICT_KEY_F64) return KVEVICT_E_DTYPE;
   if (n_lanes == 0) return KVEVICT_OK;
+  kve::note_other(ctx->c);
   return cuda_status(kve::launch_select(ctx->c, keys, key_dtype, positions, counts, n_lanes, stride, budget,
                                         recent_window, victims, n_victims, static_cast<cudaStream_t>(stream)));
 }
@@ -448,6 +482,7 @@ kvevict_status kvevict_compact(kvevict_ctx* ctx, int layer, const int32_t* victi
                                int32_t* freed, int32_t* n_freed, int32_t* moves, int32_t* n_moves, void* stream) {
   const CallRange range("kvevict_compact");
   if (!ctx || layer < 0 || layer >= ctx->c.dims.L || !victims || !n_victims) return KVEVICT_E_INVALID_ARG;
+  kve::note_other(ctx->c);
   return cuda_status(kve::launch_compact(ctx->c, ctx->c.ws, layer, victims, n_victims, false, freed, n_freed, moves,
                                          n_moves,
                                          static_cast<cudaStream_t>(stream)));
@@ -455,17 +490,19 @@ kvevict_status kvevict_compact(kvevict_ctx* ctx, int layer, const int32_t* victi
 
 kvevict_status kvevict_stats(kvevict_ctx* ctx, int layer, int64_t* out, void* stream) {
   if (!ctx || !out || layer < 0 || layer >= ctx->c.dims.L) return KVEVICT_E_INVALID_ARG;
+  kve::note_other(ctx->c);
   return cuda_status(kve::launch_stats(ctx->c, layer, reinterpret_cast<long long*>(out),
                                        static_cast<cudaStream_t>(stream)));
 }
 
 int32_t kvevict_kernels_per_decode_step(const kvevict_ctx* ctx) {
   if (!ctx) return 0;
-  return ctx->c.epi_applies ? 2 : 3;
+  return (ctx->c.epi_applies || ctx->c.lean_epi) ? 2 : 3;
 }
 
 kvevict_status kvevict_check_wait_timeout(kvevict_ctx* ctx, int32_t polls, void* stream) {
   if (!ctx || polls < 1 || polls > (1 << 22)) return KVEVICT_E_INVALID_ARG;
+  kve::note_other(ctx->c);
   return cuda_status(kve::launch_wait_check(ctx->c, polls, static_cast<cudaStream_t>(stream)));
 }
 

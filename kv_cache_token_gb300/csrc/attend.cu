@@ -62,6 +62,12 @@ struct AttendArgs {
   uint32_t* status;
   int lanes, g, Hkv, Hq, cap, lcap, P;
   float scale2;   // log2(e) / sqrt(d)
+  int early_trigger;   // let the successor (the decode epilogue) be scheduled at once
+  // Before writing its scratch copy the kernel waits (acquire) until
+  // *reads_done has reached reads_expect (wrapping): every epilogue launched
+  // on the copy before has finished with it.  Null: no such wait.
+  const uint32_t* reads_done;
+  uint32_t reads_expect;
 };
 
 constexpr int kMaxLanesSmem = 1024;   // lanes per layer (validated at create)
@@ -126,7 +132,10 @@ struct Bf16Cfg {
   static constexpr int kStageBytes = 2 * 16 * kRowStride;      // K rows then V rows
   static constexpr int kPBytes = NT * 2 * 8 * 32;              // [NT][hi, lo][8 heads][16 tokens] bf16
   static constexpr int kWarpBytes = kAttStages * kStageBytes + kPBytes;
-  static constexpr int kSmem = kAttendWarps * kWarpBytes;
+  static constexpr int kSmem = kAttendWarps * kWarpBytes;      // warp buffers; the lane prefix follows
+  // dynamic shared memory of a launch over `lanes` lanes: the warp buffers,
+  // then the lanes' tile prefix (lanes + 1 ints)
+  static constexpr int smem_for(int lanes) { return kSmem + ((lanes + 1) * 4 + 15) / 16 * 16; }
   static constexpr int kKs = D / 16;                           // k-steps over d (QK^T)
   static constexpr int kDt = D / 16;                           // 16-row tiles of d (PV)
 };
@@ -143,20 +152,54 @@ __device__ __forceinline__ void mma_bf16a(float* c, const uint32_t* a, uint32_t 
 }
 
 template <int D, int NT>
-__device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_prefix, const Split& sp, const int gw,
+__device__ __forceinline__ bool attend_warp(const AttendArgs& a, const int* sh_prefix, const Split& sp, const int gw,
                                             const int t_begin, const int t_end, unsigned char* wbuf,
                                             uint64_t* bars);
 
+// With one head tile, three CTAs of this kernel (12 warps) fill an SM's
+// register file only to three quarters (128 registers a thread), and their
+// shared memory leaves about 12 KB: one CTA of the lean decode epilogue fits
+// beside them, so the epilogue of one layer runs on the same SMs while the
+// next layer streams.  (Two head tiles need more registers.)
 template <int D, int NT>
-__global__ void __launch_bounds__(kAttendWarps * 32, 3) attend_bf16_kernel(AttendArgs a) {
+__global__ void __launch_bounds__(kAttendWarps * 32, NT == 1 ? 4 : 3) attend_bf16_kernel(AttendArgs a) {
   using C = Bf16Cfg<D, NT>;
   extern __shared__ __align__(128) unsigned char smem[];
-  __shared__ int sh_prefix[kMaxLanesSmem + 1];
   __shared__ int sh_scan[40];
   __shared__ uint64_t sh_bar[kAttendWarps][kAttStages];
 
   const int tid = threadIdx.x, lane_id = tid & 31, warp = tid >> 5;
   const int lanes = a.lanes;
+  int* sh_prefix = reinterpret_cast<int*>(smem + C::kSmem);   // [lanes + 1]
+  // The kernel may have started before earlier kernels in the stream
+  // finished: it touches nothing until every epilogue launched before on its
+  // scratch copy has finished (which orders every earlier epilogue of its
+  // layer, and everything each of those waited for, before it).  Thread 0
+  // polls, bounded; past the bound the dependency wait covers it instead.
+  if (a.reads_done) {
+    if (tid == 0) {
+      int ok = 0;
+      for (int polls = 0; polls < (1 << 14); ++polls) {
+        if (static_cast<int>(static_cast<uint32_t>(ld_acquire_gpu(reinterpret_cast<const int*>(a.reads_done))) -
+                             a.reads_expect) >= 0) {
+          ok = 1;
+          break;
+        }
+        __nanosleep(128);
+      }
+      sh_scan[0] = ok;
+    }
+    __syncthreads();
+    const int ok = sh_scan[0];
+    __syncthreads();
+    if (!ok) grid_dep_wait();
+  }
+  // Inside a decode step the kernel that consumes these results (the decode
+  // epilogue) may be scheduled from now on: it reads only what this kernel
+  // does not write before its own dependency wait, which returns once this
+  // grid is complete.  Otherwise the successor is unknown and starts only
+  // once every CTA of this grid is at its end.
+  if (a.early_trigger) grid_dep_launch();
 
   // --- lane tile prefix (every CTA computes the same table) ---------------
   int my_max = 0;
@@ -220,17 +263,18 @@ __global__ void __launch_bounds__(kAttendWarps * 32, 3) attend_bf16_kernel(Atten
   const int gw = blockIdx.x * kAttendWarps + warp;
   const int t_begin = gw < sp.W ? sp.begin(gw) : total;
   const int t_end = gw < sp.W ? sp.begin(gw + 1) : total;
-  if (t_begin < t_end) attend_warp<D, NT>(a, sh_prefix, sp, gw, t_begin, t_end, smem + warp * C::kWarpBytes,
-                                          sh_bar[warp]);
-  // the next kernel in the stream may start now; this grid completes only
-  // after its predecessor did (so completion orders everything before it)
+  if (t_begin < t_end)
+    (void)attend_warp<D, NT>(a, sh_prefix, sp, gw, t_begin, t_end, smem + warp * C::kWarpBytes, sh_bar[warp]);
+  // this grid completes only after its predecessor did (so completion
+  // orders everything before it)
   grid_dep_wait();
-  grid_dep_launch();
+  if (!a.early_trigger) grid_dep_launch();
 }
 
-// One warp's range of tiles [t_begin, t_end) (stream-K split of the layer).
+// One warp's range of tiles [t_begin, t_end) (stream-K split of the layer);
+// false if a bounded wait gave up.
 template <int D, int NT>
-__device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_prefix, const Split& sp, const int gw,
+__device__ __forceinline__ bool attend_warp(const AttendArgs& a, const int* sh_prefix, const Split& sp, const int gw,
                                             const int t_begin, const int t_end, unsigned char* wbuf,
                                             uint64_t* bars) {
   using C = Bf16Cfg<D, NT>;
@@ -410,7 +454,7 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
     {
       int spins = 0;
       while (!mbar_try_wait(&bars[st], par)) {
-        if (++spins > (1 << 22)) { set_status(a.status, ST_TIMEOUT); return; }
+        if (++spins > (1 << 22)) { set_status(a.status, ST_TIMEOUT); return false; }
       }
     }
     __syncwarp();
@@ -530,6 +574,7 @@ __device__ __forceinline__ void attend_warp(const AttendArgs& a, const int* sh_p
     __syncwarp();
   }
   flush();
+  return true;
 }
 
 // ---------------------------------------------------------------------------
@@ -657,17 +702,44 @@ __global__ void __launch_bounds__(kF32Chunk) attend_f32_kernel(AttendArgs a, int
 
 template <int D, int NT>
 static cudaError_t set_attr() {
-  return cudaFuncSetAttribute(attend_bf16_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                              Bf16Cfg<D, NT>::kSmem);
+  cudaError_t e = cudaFuncSetAttribute(attend_bf16_kernel<D, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Bf16Cfg<D, NT>::smem_for(kMaxLanesSmem));
+  if (e == cudaSuccess)
+    e = cudaFuncSetAttribute(attend_bf16_kernel<D, NT>, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+  return e;
 }
 
 template <int D, int NT>
-static int ctas_per_sm() {
+static int ctas_per_sm(int lanes) {
   int n = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, attend_bf16_kernel<D, NT>, kAttendWarps * 32,
-                                                    Bf16Cfg<D, NT>::kSmem) != cudaSuccess)
+                                                    Bf16Cfg<D, NT>::smem_for(lanes)) != cudaSuccess)
     return 0;
   return n;
+}
+
+// Whether one CTA of the lean H2O epilogue fits on an SM beside `n` CTAs of
+// this attention kernel launched over `lanes` lanes.
+template <int D, int NT>
+static bool lean_fits_beside(int dev, int n, int lanes) {
+  cudaFuncAttributes fa, fl;
+  int lean_threads = 0;
+  if (cudaFuncGetAttributes(&fa, attend_bf16_kernel<D, NT>) != cudaSuccess) return false;
+  if (lean_epilogue_attributes(&fl, &lean_threads) != cudaSuccess) return false;
+  int smem_sm = 0, reserved = 0, regs_sm = 0, threads_sm = 0;
+  if (cudaDeviceGetAttribute(&smem_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&regs_sm, cudaDevAttrMaxRegistersPerMultiprocessor, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&threads_sm, cudaDevAttrMaxThreadsPerMultiProcessor, dev) != cudaSuccess)
+    return false;
+  // registers are granted per warp, in units of 8 a thread
+  auto regs = [](const cudaFuncAttributes& f, int threads) { return (f.numRegs + 7) / 8 * 8 * threads; };
+  const long long smem = static_cast<long long>(n) *
+                             (static_cast<long long>(fa.sharedSizeBytes) + Bf16Cfg<D, NT>::smem_for(lanes) + reserved) +
+                         static_cast<long long>(fl.sharedSizeBytes) + reserved;
+  const long long r = static_cast<long long>(n) * regs(fa, kAttendWarps * 32) + regs(fl, lean_threads);
+  const int threads = n * kAttendWarps * 32 + lean_threads;
+  return smem <= smem_sm && r <= regs_sm && threads <= threads_sm;
 }
 
 cudaError_t prepare_kernels(Ctx& ctx) {
@@ -682,42 +754,53 @@ cudaError_t prepare_kernels(Ctx& ctx) {
   const int nt = dm.g > 8 ? 2 : 1;
   ctx.attend_ctas_per_sm = 1;
   if (dm.dtype == KVEVICT_BF16) {
-    if (dm.d == 128) ctx.attend_ctas_per_sm = nt == 1 ? ctas_per_sm<128, 1>() : ctas_per_sm<128, 2>();
-    else ctx.attend_ctas_per_sm = nt == 1 ? ctas_per_sm<64, 1>() : ctas_per_sm<64, 2>();
+    if (dm.d == 128) ctx.attend_ctas_per_sm = nt == 1 ? ctas_per_sm<128, 1>(dm.lanes) : ctas_per_sm<128, 2>(dm.lanes);
+    else ctx.attend_ctas_per_sm = nt == 1 ? ctas_per_sm<64, 1>(dm.lanes) : ctas_per_sm<64, 2>(dm.lanes);
+  }
+  ctx.lean_coresident = false;
+  if (dm.dtype == KVEVICT_BF16 && ctx.attend_ctas_per_sm >= 1) {
+    const int n = ctx.attend_ctas_per_sm;
+    if (dm.d == 128)
+      ctx.lean_coresident = nt == 1 ? lean_fits_beside<128, 1>(ctx.device, n, dm.lanes)
+                                    : lean_fits_beside<128, 2>(ctx.device, n, dm.lanes);
+    else
+      ctx.lean_coresident = nt == 1 ? lean_fits_beside<64, 1>(ctx.device, n, dm.lanes)
+                                    : lean_fits_beside<64, 2>(ctx.device, n, dm.lanes);
   }
   return cudaGetLastError();
 }
 
 cudaError_t launch_attend(const Ctx& ctx, int layer, const void* q, const void* k_new, const void* v_new,
-                          cudaStream_t stream) {
+                          cudaStream_t stream, bool early_trigger) {
   const Dims& dm = ctx.dims;
   LayerState ls = layer_state(ctx, layer);
   AttendArgs a;
   a.k_pool = ls.k_pool; a.v_pool = ls.v_pool; a.slot = ls.slot; a.count = ls.count;
   a.q = q; a.k_new = k_new; a.v_new = v_new;
-  const int c = layer & 1;
+  const int c = layer % kScratchBufs;
   a.logits = ctx.ws.logits_buf[c]; a.part_o = ctx.ws.part_o_buf[c]; a.part_ml = ctx.ws.part_ml_buf[c];
   a.lane_nseg = ctx.ws.lane_nseg_buf[c]; a.status = ctx.ws.status;
+  a.reads_done = ctx.ws.reads_done + c;
+  a.reads_expect = ctx.epi_launches[c] * static_cast<uint32_t>(dm.lanes);
   a.lanes = dm.lanes; a.g = dm.g; a.Hkv = dm.Hkv; a.Hq = dm.Hq; a.cap = dm.cap; a.lcap = dm.lcap;
   a.P = dm.P;
   a.scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(dm.d));
-  // The previous attention, epilogue and apply launches may still run when
-  // this kernel starts early: allowed only when they work on the other
-  // scratch parity (and so on another layer).
-  const bool pdl = ctx.last_layer < 0 || ((ctx.last_layer ^ layer) & 1) != 0;
+  a.early_trigger = early_trigger ? 1 : 0;
+  // early start: see attend_early_ok (the kernel guards itself)
+  const bool pdl = attend_early_ok(ctx);
   if (dm.dtype == KVEVICT_BF16) {
     if (dm.lanes > kMaxLanesSmem) return cudaErrorInvalidValue;
     const int grid = ctx.sm_count * ctx.attend_ctas_per_sm;
     const int nt = dm.g > 8 ? 2 : 1;
     const dim3 blk(kAttendWarps * 32);
     if (dm.d == 128 && nt == 1)
-      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, Bf16Cfg<128, 1>::kSmem, stream, pdl, a);
+      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, Bf16Cfg<128, 1>::smem_for(dm.lanes), stream, pdl, a);
     else if (dm.d == 128)
-      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, Bf16Cfg<128, 2>::kSmem, stream, pdl, a);
+      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, Bf16Cfg<128, 2>::smem_for(dm.lanes), stream, pdl, a);
     else if (nt == 1)
-      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, Bf16Cfg<64, 1>::kSmem, stream, pdl, a);
+      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, Bf16Cfg<64, 1>::smem_for(dm.lanes), stream, pdl, a);
     else
-      return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, Bf16Cfg<64, 2>::kSmem, stream, pdl, a);
+      return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, Bf16Cfg<64, 2>::smem_for(dm.lanes), stream, pdl, a);
   } else {
     const int chunks = (dm.cap + kF32Chunk) / kF32Chunk;   // enough for n = cap - 1 plus the new token
     if (chunks > kMaxSeg) return cudaErrorInvalidValue;
@@ -743,18 +826,21 @@ cudaError_t launch_attend_into(const Ctx& ctx, int layer, const void* q, const v
   a.lanes = dm.lanes; a.g = dm.g; a.Hkv = dm.Hkv; a.Hq = dm.Hq; a.cap = dm.cap; a.lcap = dm.lcap;
   a.P = dm.P;
   a.scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(dm.d));
+  a.early_trigger = 0;
+  a.reads_done = nullptr;   // its own scratch, launched without early start
+  a.reads_expect = 0u;
   if (dm.dtype == KVEVICT_BF16) {
     if (dm.lanes > kMaxLanesSmem) return cudaErrorInvalidValue;
     const int grid = ctx.sm_count * ctx.attend_ctas_per_sm;
     const int nt = dm.g > 8 ? 2 : 1;
     const dim3 blk(kAttendWarps * 32);
     if (dm.d == 128 && nt == 1)
-      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, Bf16Cfg<128, 1>::kSmem, stream, false, a);
+      return launch_k(attend_bf16_kernel<128, 1>, dim3(grid), blk, Bf16Cfg<128, 1>::smem_for(dm.lanes), stream, false, a);
     else if (dm.d == 128)
-      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, Bf16Cfg<128, 2>::kSmem, stream, false, a);
+      return launch_k(attend_bf16_kernel<128, 2>, dim3(grid), blk, Bf16Cfg<128, 2>::smem_for(dm.lanes), stream, false, a);
     else if (nt == 1)
-      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, Bf16Cfg<64, 1>::kSmem, stream, false, a);
-    return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, Bf16Cfg<64, 2>::kSmem, stream, false, a);
+      return launch_k(attend_bf16_kernel<64, 1>, dim3(grid), blk, Bf16Cfg<64, 1>::smem_for(dm.lanes), stream, false, a);
+    return launch_k(attend_bf16_kernel<64, 2>, dim3(grid), blk, Bf16Cfg<64, 2>::smem_for(dm.lanes), stream, false, a);
   }
   const int chunks = (dm.cap + kF32Chunk) / kF32Chunk;
   if (chunks > kMaxSeg) return cudaErrorInvalidValue;

@@ -12,9 +12,15 @@
 // lane's relocation plan.
 // allocate: one CTA hands out the lowest free block ids, ascending lanes,
 // first to admissions that found no slot, then to relocation destinations.
-// apply: one CTA per lane writes those admissions and runs the relocation
+// apply: the admissions and relocations of the lanes that asked for blocks
 // (vToken review, Sec. 3.3 Stage 3: fill each destination completely, in
-// ascending position, and release the sources).
+// ascending position, and release the sources), claimed lane by lane by the
+// epilogue's CTAs once the allocator has published its result, or one CTA per
+// lane in a separate kernel.
+// Two epilogue kernels: a large one (512 threads, 180 KB of shared memory)
+// for every policy and step, and a lean H2O one (128 threads, no dynamic
+// shared memory) that fits on an SM beside three CTAs of the attention
+// kernel, so the epilogue of one layer runs while the next layer streams.
 #include "lane_ops.cuh"
 
 namespace kve {
@@ -45,6 +51,12 @@ struct EpiArgs {
 };
 
 constexpr int kGenCounter = 7;   // ws.counters slot: allocator results published (one increment per call)
+constexpr int kApplyCount = 8;   // ws.counters slot: lanes in ws.apply_list this call
+constexpr int kApplyClaim = 9;   // ws.counters slot: next entry of ws.apply_list to claim
+constexpr int kLeanThreads = 128;   // lean H2O epilogue: threads per CTA (one lane)
+constexpr int kLeanWarps = kLeanThreads / 32;
+constexpr int kLeanU = 4;           // lean H2O epilogue: tokens a thread has in flight in the weight pass
+constexpr int kShiftU = 8;          // lean H2O epilogue: table entries a thread moves per round of the shift
 
 template <typename KT>
 __device__ void apply_lane(const LayerState& ls, const Workspace& ws, const Dims& dm, const int l,
@@ -58,7 +70,7 @@ __device__ __forceinline__ void copy_row(KT* dst, const KT* src, int d) {
 
 template <typename KT, bool kRing>
 __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n, unsigned char* dsm,
-                                          int* sh_work);
+                                          int* sh_work, int* sh_gen);
 __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const Dims& dm, int* sh_scan,
                                int* sh_flag);
 
@@ -332,23 +344,32 @@ __device__ __forceinline__ void signal_done(const Workspace& ws, bool work, int*
   *sh_flag = (old >> kWorkShift) + (work ? 1 : 0);
 }
 
+// Right after the dependency wait (thread 0): the allocator-result
+// generation before this CTA signals (it changes only after every CTA of the
+// grid has signalled, and the previous layer's epilogue, which also
+// publishes one, is complete by now).
+__device__ __forceinline__ void read_generation(const EpiArgs& A, int* sh_gen) {
+  if (threadIdx.x == 0) *sh_gen = A.applies ? __ldcg(A.ws.counters + kGenCounter) : 0;
+}
+
 // H2O with at most one victim (the steady state of a full cache), all
 // threads of the CTA.  Before the dependency wait: the lane's token table
 // (kFastPer tokens a thread), its block list with the live masks (kFastPer
 // blocks a thread) and the new token's K/V row, none of which the attention
-// kernel writes; from the masks, each warp's lowest free slot.  After it:
-// logits and split-K partial outputs by bulk copy into shared memory,
-// split-K statistics by plain loads.  The minimum (key, position) and its
-// slot come from three warp reductions and one barrier; the holder of the
-// victim's block decides from the mask it already holds whether the block
-// empties.  The fragmentation test of Eq. (1) is evaluated before the wait
-// for each of the eight outcomes the scoring can have (double division is
-// slow on this part).  The allocator's requests and the done counter go out
-// before the table is rewritten, so the counter's release does not wait for
-// those stores, and the counter's old value is read only at the end.
+// kernel or another layer's epilogue writes; from the masks, each warp's
+// lowest free slot.  After it: logits and split-K partial outputs by bulk
+// copy into shared memory, split-K statistics by plain loads.  The minimum
+// (key, position) and its slot come from three warp reductions and one
+// barrier; the holder of the victim's block decides from the mask it already
+// holds whether the block empties.  The fragmentation test of Eq. (1) is
+// evaluated before the wait for each of the eight outcomes the scoring can
+// have (double division is slow on this part).  The done counter goes out
+// (release) once the table is rewritten: another CTA may apply this lane's
+// admission or relocation, which reads the table.
 template <typename KT>
 __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& L, const int n, unsigned char* dsm,
-                                              int* sh_sig, int* sh_last, int* sh_flag) {
+                                              int* sh_sig, int* sh_last, int* sh_flag, int* sh_gen,
+                                              int* sh_work) {
   __shared__ float sh_rL[8], sh_lse2[8];
   __shared__ __align__(16) float sh_scale[8][kMaxSeg];   // per head, per split-K segment
   __shared__ unsigned sh_over;
@@ -361,7 +382,7 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
-  const int cbuf = A.layer & 1;
+  const int cbuf = A.layer % kScratchBufs;
   const int k = max(0, n + 1 - dm.budget);          // 0 or 1
   const int cut = A.new_pos - dm.R + 1;
 
@@ -395,8 +416,6 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
     bm[j] = bk[j] >= 0 ? (__ldcg(L.mask + bk[j]) & 0xFFFF) : 0xFFFF;
   }
   if (bad_blk) set_status(A.ws.status, ST_BAD_INDEX);
-  // a request of this lane left non-zero (the invariant is that none is)
-  const bool stale_req = tid == 0 && (__ldcg(A.ws.need_admit + l) | __ldcg(A.ws.want_dst + l)) != 0;
   if (tid == 0) {
     sh_nan = 0;
     sh_dead = -1;
@@ -429,6 +448,9 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
 
   grid_dep_wait();      // the attention kernel's results are complete and visible
   grid_dep_launch();
+  read_generation(A, sh_gen);
+  // a request of this lane left non-zero (the invariant is that none is)
+  const bool stale_req = tid == 0 && (__ldcg(A.ws.need_admit + l) | __ldcg(A.ws.want_dst + l)) != 0;
 
   // split-K statistics of all kMaxSeg segments (in bounds), masked below
   const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
@@ -598,26 +620,22 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
   const int outcome = vcount | (dead_j >= 0 ? 2 : 0) | (need ? 4 : 0);
   const int ndst = lane_plan_given(L, nb2, ((sh_over >> outcome) & 1u) != 0, false, need, &t_live, sh_scan2);
   const bool work = need || ndst > 0;
-  // the done counter's old value is only needed at the end: its round trip
-  // overlaps the table rewrite and the output combine
-  int done_old = 0;
+  // The allocator reads a lane's requests (and its count) only when they are
+  // non-zero; between steps they hold zero (applying them clears what was
+  // consumed).  A lane that asks for blocks, released a block or clears a
+  // request left over signals with release semantics once its table is
+  // rewritten; the writes of the others are of no concern to the allocator.
+  const bool publish = work || dead_j >= 0 || stale_req;
   if (tid == 0) {
     A.ls.count[l] = m + 1;
     if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
-    // The allocator reads a lane's requests (and its count) only when they
-    // are non-zero; between steps they hold zero (applying them, here or in
-    // the apply kernel, clears what was consumed).  A lane that asks for blocks, released a block or
-    // clears a request left over publishes with release semantics; the
-    // writes of the others are of no concern to the allocator.
-    const bool publish = work || dead_j >= 0 || stale_req;
     if (work || stale_req) {
       A.ws.need_admit[l] = need ? 1 : 0;
       A.ws.want_dst[l] = ndst;
       A.ws.plan_tlive[l] = t_live;
     }
     if (work) atomicOr(A.ws.work_flag, 1);
-    const int inc = 1 + (work ? kWorkUnit : 0);
-    done_old = publish ? atomic_add_release(A.ws.epi_done, inc) : atomicAdd(A.ws.epi_done, inc);
+    *sh_work = work ? 1 : 0;
   }
   // ---- the table: survivors shift over the victim; the new token goes last -----------
 #pragma unroll
@@ -650,6 +668,15 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
     if (dead_j >= 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_FREED_DEAD]), 1ull);
     if (sh_nan) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_NAN_KEYS]), (unsigned long long)sh_nan);
     if (l == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_STEPS]), 1ull);
+  }
+  // the done counter, once every thread's table writes are ordered before it;
+  // its old value is only needed at the end, so its round trip overlaps the
+  // output combine
+  __syncthreads();
+  int done_old = 0;
+  if (tid == 0) {
+    const int inc = 1 + (work ? kWorkUnit : 0);
+    done_old = publish ? atomic_add_release(A.ws.epi_done, inc) : atomicAdd(A.ws.epi_done, inc);
   }
   // ---- output: combine the split-K partial outputs (the first kPoSeg from
   // shared memory); a thread owns two adjacent elements of one head, so the
@@ -698,13 +725,96 @@ __device__ __forceinline__ void h2o_fast_step(const EpiArgs& A, const LaneRefs& 
   }
 }
 
+// Waits until *p differs from `old` (acquire), for a bounded number of polls;
+// false if it did not change (not an error: see epilogue_tail).
+__device__ __forceinline__ bool wait_changed_quiet(const int* p, int old) {
+  for (int polls = 0; polls < (1 << 20); ++polls) {
+    if (ld_acquire_gpu(p) != old) return true;
+    __nanosleep(64);
+  }
+  return false;
+}
+
+// Applies lanes of ws.apply_list until none is left unclaimed (all threads of
+// the CTA; the list and its count are published).
+template <typename KT>
+__device__ __forceinline__ void apply_claimed(const EpiArgs& A, int* sh_scan, int* mv_src, int* mv_dst) {
+  __shared__ int sh_claim;
+  const int total = __ldcg(A.ws.counters + kApplyCount);
+  for (;;) {
+    if (threadIdx.x == 0) sh_claim = atomicAdd(A.ws.counters + kApplyClaim, 1);
+    __syncthreads();
+    const int c = sh_claim;
+    __syncthreads();
+    if (c >= total) break;
+    apply_lane<KT>(A.ls, A.ws, A.dm, __ldcg(A.ws.apply_list + c), A.k_new, A.v_new, 0, nullptr, sh_scan, mv_src,
+                   mv_dst);
+    __syncthreads();
+  }
+}
+
+// The end of every epilogue CTA (all threads), after its lane's step.  The
+// last CTA of the grid to finish runs the layer allocator, if any lane asked
+// for blocks.  With A.applies, admissions into fresh blocks and relocations
+// are applied here instead of in an apply kernel: the last CTA publishes the
+// allocator's result (a release store of the generation counter), then
+// claims the listed lanes one by one; a CTA whose own lane asked for blocks
+// waits for that result (bounded) and claims lanes too.  A waiter that gives
+// up simply leaves: whatever nobody else claims, the last CTA applies, so no
+// lane is left half-applied whatever else occupies the GPU.
+template <typename KT>
+__device__ __forceinline__ void epilogue_tail(const EpiArgs& A, int* sh_scan, int* sh_work, int* sh_last,
+                                              int* sh_flag, const int* sh_sig, const int* sh_gen, int* mv_src,
+                                              int* mv_dst) {
+  __shared__ int sh_go;
+  const int l = blockIdx.x, tid = threadIdx.x;
+  __syncthreads();
+  if (!*sh_sig) {
+    if (tid == 0) signal_done(A.ws, *sh_work != 0, sh_last, sh_flag);
+    __syncthreads();
+  }
+  if (*sh_last) {
+    if (*sh_flag == 0) {
+      if (tid == 0) {
+        *A.ws.epi_done = 0;
+        A.ws.counters[1] = 0; A.ws.counters[2] = 0; A.ws.counters[kApplyCount] = 0;
+      }
+    } else {
+      if (tid == 0) *A.ws.epi_done = 0;
+      __threadfence();
+      allocate_layer(A.ls, A.ws, A.dm, sh_scan, sh_flag);
+    }
+  }
+  if (!A.applies) return;
+  if (*sh_last) {
+    __syncthreads();   // the allocator's stores by every thread of this CTA
+    if (tid == 0) {
+      __threadfence();
+      st_release_gpu(A.ws.counters + kGenCounter, *sh_gen + 1);
+    }
+    apply_claimed<KT>(A, sh_scan, mv_src, mv_dst);
+    return;
+  }
+  if (tid == 0) sh_go = *sh_work != 0 && wait_changed_quiet(A.ws.counters + kGenCounter, *sh_gen);
+  __syncthreads();
+  if (sh_go) apply_claimed<KT>(A, sh_scan, mv_src, mv_dst);
+}
+
+// The end of an epilogue CTA: it is done with its scratch copy and with its
+// layer's tables (release, after every thread's last access), for the
+// attention kernels that guard themselves on the copy's count.
+__device__ __forceinline__ void scratch_released(const EpiArgs& A) {
+  __syncthreads();
+  if (threadIdx.x == 0) (void)atomic_add_release(reinterpret_cast<int*>(A.ws.reads_done) + A.layer % kScratchBufs, 1);
+}
+
 // kRing: the policy keeps a history ring (SnapKV, DropKV decode variant);
 // the H2O instantiation carries none of that code.
 template <typename KT, bool kRing>
 __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs A) {
   extern __shared__ __align__(128) unsigned char dsm[];
   __shared__ int sh_scan[40];
-  __shared__ int sh_work, sh_last, sh_flag, sh_sig, sh_gen, sh_apply;
+  __shared__ int sh_work, sh_last, sh_flag, sh_sig, sh_gen;
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   LaneRefs L = lane_refs(A.ls, dm, l);
@@ -712,65 +822,453 @@ __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs
   // list) is not written by the attention kernel: it is read before the
   // dependency wait, while the attention kernel drains.
   const int n = __ldcg(A.ls.count + l);
-  // the allocator-result generation before this CTA signals (it changes only
-  // after every CTA of the grid has signalled)
-  if (tid == 0) { sh_work = 0; sh_sig = 0; sh_gen = A.applies ? __ldcg(A.ws.counters + kGenCounter) : 0; }
+  if (tid == 0) { sh_work = 0; sh_sig = 0; sh_gen = 0; }
   if (n < 0 || n >= dm.cap) {
     grid_dep_wait();
     grid_dep_launch();
+    read_generation(A, &sh_gen);
     if (tid == 0) {
       set_status(A.ws.status, ST_CAPACITY);
       A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
     }
   } else if (!kRing && n + 1 - dm.budget <= 1 && n <= kFastN && dm.g <= 8 && dm.d <= 128 && (dm.d & 1) == 0) {
-    h2o_fast_step<KT>(A, L, n, dsm, &sh_sig, &sh_last, &sh_flag);
+    h2o_fast_step<KT>(A, L, n, dsm, &sh_sig, &sh_last, &sh_flag, &sh_gen, &sh_work);
   } else {
-    lane_step<KT, kRing>(A, L, n, dsm, &sh_work);
+    lane_step<KT, kRing>(A, L, n, dsm, &sh_work, &sh_gen);
   }
-  __syncthreads();
-  if (!sh_sig) {
-    if (tid == 0) signal_done(A.ws, sh_work != 0, &sh_last, &sh_flag);
-    __syncthreads();
-  }
-  // The last CTA of the grid to finish runs the layer allocator, if any lane
-  // asked for blocks.
-  if (sh_last) {
-    if (sh_flag == 0) {
-      if (tid == 0) { *A.ws.epi_done = 0; A.ws.counters[1] = 0; A.ws.counters[2] = 0; }
-    } else {
-      if (tid == 0) *A.ws.epi_done = 0;
-      __threadfence();
-      allocate_layer(A.ls, A.ws, dm, sh_scan, &sh_flag);
+  // the step is done with the dynamic shared memory: the relocation's move
+  // lists go there
+  int* mv = reinterpret_cast<int*>(dsm);
+  epilogue_tail<KT>(A, sh_scan, &sh_work, &sh_last, &sh_flag, &sh_sig, &sh_gen, mv, mv + kApplyThreads);
+  scratch_released(A);
+}
+
+// H2O with at most one victim (the steady state of a full cache) in a CTA of
+// kLeanThreads threads with no dynamic shared memory (the lean epilogue).
+// Before the dependency wait it reads only what neither the attention kernel
+// nor another layer's epilogue writes: the lane's
+// scores (kLeanPer a thread, in registers), its positions (the candidates
+// outside the recent window are a prefix of the table, since positions
+// ascend: it counts them), its block list and live masks (each warp's lowest
+// free slot), the new token's K/V row; and it pulls the lane's slots into L2.
+// After it: the split-K statistics give each head's log-sum-exp; one pass
+// reads each token's logits from L2 (kLeanU tokens a thread in flight), adds
+// its group weight to its score (written in place) and keeps the minimum
+// candidate (key, index: the index orders like the position); the victim's
+// live bit is cleared (an emptied block is released and dropped from the
+// list); the new token takes the lowest free slot; the entries after the
+// victim move down one place; the done counter goes out (release) once the
+// table is written; then the split-K output combine, 8 elements of one head
+// a thread, eight segments in flight.  The same results as h2o_fast_step.
+constexpr int kLeanPer = 32;   // tokens a thread holds: lanes of up to kLeanPer * kLeanThreads tokens
+template <typename KT>
+__device__ __forceinline__ void h2o_lean_step(const EpiArgs& A, const LaneRefs& L, const int n, int* sh_sig,
+                                              int* sh_last, int* sh_flag, int* sh_gen, int* sh_work) {
+  __shared__ float sh_rL[8], sh_lse2[8];
+  __shared__ float sh_scale[8][kMaxSeg];   // per head, per split-K segment
+  __shared__ unsigned sh_over;
+  __shared__ unsigned sh_wkey[kLeanWarps], sh_widx[kLeanWarps];
+  __shared__ unsigned sh_wfree[kLeanWarps], sh_wfree2[kLeanWarps];
+  __shared__ int sh_ncand[kLeanWarps];
+  __shared__ int sh_nan, sh_late, sh_dead, sh_dead_j, sh_vpos, sh_vslot;
+  __shared__ int sh_scan2[40];
+  constexpr unsigned kNone = 0xFFFFFFFFu;
+  const Dims& dm = A.dm;
+  const int l = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
+  const int cbuf = A.layer % kScratchBufs;
+  const int k = max(0, n + 1 - dm.budget);          // 0 or 1
+  const int cut = A.new_pos - dm.R + 1;
+
+  // ---- before the dependency wait -----------------------------------------------
+  if (tid == 0) { sh_nan = 0; sh_late = 0; sh_dead = -1; sh_dead_j = -1; }
+  float sc[kLeanPer];
+  int ncand = 0;
+#pragma unroll
+  for (int j = 0; j < kLeanPer; ++j) {
+    const int i = tid + j * kLeanThreads;
+    sc[j] = 0.f;
+    if (i < n) {
+      sc[j] = __ldcg(L.score + i);
+      ncand += __ldcg(L.pos + i) < cut ? 1 : 0;
+      if (lane == 0 || lane == 31) prefetch_l2(L.slot + i);
     }
   }
-  if (!A.applies) return;
-  // Admission into a fresh block and relocation, here instead of in an
-  // apply kernel: the last CTA publishes the allocator's result (release);
-  // a lane that asked for blocks waits for it (bounded) and applies.  Every
-  // CTA of the grid is resident at once (the host checked), so the last CTA
-  // always runs while the others wait.
-  if (sh_last) {
-    __syncthreads();   // the allocator's stores by every thread of this CTA
+  ncand = warp_sum(ncand);
+  if (lane == 0) sh_ncand[warp] = ncand;
+  const int nb = min(max(__ldcg(L.nblocks), 0), dm.cap);
+  {
+    // lowest free slot of the lane's blocks before this step's eviction
+    unsigned fr = kNone;
+    bool bad_blk = false;
+    for (int j = tid; j < nb; j += kLeanThreads) {
+      const int blk = __ldcg(L.blocks + j);
+      if (blk < 0 || blk >= dm.P) { bad_blk = true; continue; }
+      const int mk = __ldcg(L.mask + blk) & 0xFFFF;
+      if (mk != 0xFFFF) fr = min(fr, static_cast<unsigned>(blk * kBlock + (__ffs(~mk) - 1)));
+    }
+    if (bad_blk) set_status(A.ws.status, ST_BAD_INDEX);
+    fr = __reduce_min_sync(0xffffffffu, fr);
+    if (lane == 0) sh_wfree[warp] = fr;
+  }
+  // Eq. (1)'s test for each outcome the scoring has yet to decide: a victim
+  // or none (bit 0), its block emptied or not (bit 1), the new token waiting
+  // for a fresh block or not (bit 2); one lane per outcome
+  if (warp == 0) {
+    const int vc = lane & 1, dead = (lane >> 1) & 1, fresh = (lane >> 2) & 1;
+    const int N = nb - dead + fresh;
+    const bool o = lane < 8 && N > 0 && frag_over(n - vc + 1, N, dm.theta_f);
+    const unsigned bits = __ballot_sync(0xffffffffu, o);
+    if (lane == 0) sh_over = bits;
+  }
+  KT knv{}, vnv{};
+  if (tid < d) {
+    knv = static_cast<const KT*>(A.k_new)[static_cast<size_t>(l) * d + tid];
+    vnv = static_cast<const KT*>(A.v_new)[static_cast<size_t>(l) * d + tid];
+  }
+  // the last kept token must precede the new one
+  const bool late = tid == 0 && n > 0 && __ldcg(L.pos + n - 1) >= A.new_pos;
+
+  grid_dep_wait();      // the attention kernel's results are complete and visible
+  grid_dep_launch();
+  read_generation(A, sh_gen);
+  // a request of this lane left non-zero (the invariant is that none is)
+  const bool stale_req = tid == 0 && (__ldcg(A.ws.need_admit + l) | __ldcg(A.ws.want_dst + l)) != 0;
+  // split-K statistics of all kMaxSeg segments (in bounds), masked below
+  const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
+  float2 m0[2], m1[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) {
+    const int h = warp + r * kLeanWarps;
+    m0[r] = (A.has_q && h < g) ? __ldcg(ml + lane * g + h) : make_float2(-INFINITY, 0.f);
+    m1[r] = (A.has_q && h < g) ? __ldcg(ml + (lane + 32) * g + h) : make_float2(-INFINITY, 0.f);
+  }
+  const int nseg = A.has_q ? min(__ldcg(A.ws.lane_nseg_buf[cbuf] + l), kMaxSeg) : 0;
+  // the first round of logits goes out with the statistics (it does not need
+  // the log-sum-exp)
+  const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
+  float lv0[kLeanU][8];
+#pragma unroll
+  for (int u = 0; u < kLeanU; ++u) {
+    const int i = tid + u * kLeanThreads;
+#pragma unroll
+    for (int h = 0; h < 8; ++h)
+      lv0[u][h] = (A.has_q && h < g && i < n) ? __ldcg(lg + static_cast<size_t>(h) * dm.lcap + i) : 0.f;
+  }
+  if (__syncthreads_or(late)) {
     if (tid == 0) {
-      __threadfence();
-      st_release_gpu(A.ws.counters + kGenCounter, sh_gen + 1);
+      set_status(A.ws.status, ST_POSITION);
+      A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
+    }
+    return;
+  }
+  ncand = 0;
+#pragma unroll
+  for (int w = 0; w < kLeanWarps; ++w) ncand += sh_ncand[w];
+  // ---- per-head log-sum-exp of the split-K segments (a warp per head) ------------
+  if (A.has_q) {
+#pragma unroll
+    for (int r = 0; r < 2; ++r) {
+      const int h = warp + r * kLeanWarps;
+      if (h < g) {
+        if (lane >= nseg) m0[r] = make_float2(-INFINITY, 0.f);
+        if (lane + 32 >= nseg) m1[r] = make_float2(-INFINITY, 0.f);
+        const float M = warp_max(fmaxf(m0[r].x, m1[r].x));
+        const float s0 = m0[r].x == -INFINITY ? 0.f : exp2f(m0[r].x - M);
+        const float s1 = m1[r].x == -INFINITY ? 0.f : exp2f(m1[r].x - M);
+        sh_scale[h][lane] = s0;
+        sh_scale[h][lane + 32] = s1;
+        float Ls = m0[r].y * s0 + m1[r].y * s1;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+        if (lane == 0) {
+          sh_rL[h] = 1.f / Ls;
+          const float lse2 = M + log2f(Ls);
+          sh_lse2[h] = lse2;
+          A.lse[static_cast<size_t>(b) * dm.Hq + kh * g + h] = lse2 * kLn2;
+        }
+      }
+    }
+  }
+  __syncthreads();
+
+  // ---- weights -> scores (in place); candidate minimum (key, index) ---------------
+  unsigned ck = kNone, ci = kNone;
+  int nan_count = 0;
+#pragma unroll
+  for (int j0 = 0; j0 < kLeanPer; j0 += kLeanU) {
+    if (tid + j0 * kLeanThreads < n) {
+      float lv[kLeanU][8];
+#pragma unroll
+      for (int u = 0; u < kLeanU; ++u) {
+        const int i = tid + (j0 + u) * kLeanThreads;
+#pragma unroll
+        for (int h = 0; h < 8; ++h)
+          lv[u][h] = j0 == 0 ? lv0[u][h]
+                             : (A.has_q && h < g && i < n) ? __ldcg(lg + static_cast<size_t>(h) * dm.lcap + i) : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < kLeanU; ++u) {
+        const int i = tid + (j0 + u) * kLeanThreads;
+        if (i < n) {
+          float s = sc[j0 + u];
+          if (A.has_q) {
+            float w = 0.f;
+#pragma unroll
+            for (int h = 0; h < 8; ++h)
+              if (h < g) w += hw_exp2(lv[u][h] - sh_lse2[h]);
+            s += w;
+            L.score[i] = s;
+          }
+          if (s != s) ++nan_count;
+          if (k == 1 && i < ncand) {
+            const unsigned kk = static_cast<unsigned>(mono_key(s));
+            if (kk < ck) { ck = kk; ci = static_cast<unsigned>(i); }   // ascending i: ties keep the lower index
+          }
+        }
+      }
+    }
+  }
+  {
+    const unsigned wk = __reduce_min_sync(0xffffffffu, ck);
+    const unsigned wi = __reduce_min_sync(0xffffffffu, ck == wk ? ci : kNone);
+    if (lane == 0) { sh_wkey[warp] = wk; sh_widx[warp] = wi; }
+  }
+  nan_count = warp_sum(nan_count);
+  if (lane == 0 && nan_count) atomicAdd(&sh_nan, nan_count);
+  __syncthreads();
+  unsigned vidx;
+  {
+    const bool in = lane < kLeanWarps;
+    const unsigned k1 = in ? sh_wkey[lane] : kNone;
+    const unsigned vkey = __reduce_min_sync(0xffffffffu, k1);
+    vidx = __reduce_min_sync(0xffffffffu, (in && k1 == vkey) ? sh_widx[lane] : kNone);
+  }
+  const bool has_victim = k == 1 && vidx != kNone;
+  const int vi = static_cast<int>(vidx);
+  // the first round of the table shift (entries after the victim) goes out
+  // before the eviction's round trips
+  int sp[kShiftU], ssl[kShiftU];
+  float ssc[kShiftU];
+#pragma unroll
+  for (int u = 0; u < kShiftU; ++u) {
+    const int i = vi + 1 + u * kLeanThreads + tid;
+    if (has_victim && i < n) { sp[u] = __ldcg(L.pos + i); ssl[u] = __ldcg(L.slot + i); ssc[u] = L.score[i]; }
+  }
+  // ---- eviction: the victim's slot is released; an emptied block is freed ---------
+  if (tid == 0) {
+    int vslot = -1, vpos = -1;
+    if (has_victim) {
+      vpos = __ldcg(L.pos + vi);
+      vslot = __ldcg(L.slot + vi);
+      if (vslot >= 0 && vslot < dm.P * kBlock) {
+        const int vb = vslot >> 4, vbit = 1 << (vslot & 15);
+        const int old = atomicAnd(&L.mask[vb], ~vbit);
+        if (((old & 0xFFFF) & ~vbit) == 0) {
+          L.owner[vb] = -1;
+          sh_dead = vb;
+        }
+      } else if (vslot >= 0) {
+        set_status(A.ws.status, ST_BAD_INDEX);
+      }
+    }
+    sh_vpos = vpos;
+    sh_vslot = vslot;
+  }
+  __syncthreads();
+  const int dead_blk = sh_dead;
+  const int vslot = sh_vslot;
+  const bool vslot_ok = has_victim && vslot >= 0 && vslot < dm.P * kBlock;
+  const int vcount = has_victim ? 1 : 0;
+  int nb2 = nb;
+  unsigned best;
+  if (dead_blk < 0) {
+    // the victim's slot is now free too
+    unsigned pre = lane < kLeanWarps ? sh_wfree[lane] : kNone;
+    pre = __reduce_min_sync(0xffffffffu, pre);
+    best = min(pre, vslot_ok ? static_cast<unsigned>(vslot) : kNone);
+  } else {
+    // rare: the victim emptied its block; drop it from the list (the last
+    // entry moves into its place) and look for a free slot in the others
+    unsigned fr = kNone;
+    for (int j = tid; j < nb; j += kLeanThreads) {
+      const int blk = __ldcg(L.blocks + j);
+      if (blk == dead_blk) {
+        sh_dead_j = j;
+      } else if (blk >= 0 && blk < dm.P) {
+        const int mk = __ldcg(L.mask + blk) & 0xFFFF;
+        if (mk != 0xFFFF) fr = min(fr, static_cast<unsigned>(blk * kBlock + (__ffs(~mk) - 1)));
+      }
+    }
+    fr = __reduce_min_sync(0xffffffffu, fr);
+    if (lane == 0) sh_wfree2[warp] = fr;
+    __syncthreads();
+    if (tid == 0 && sh_dead_j >= 0) {
+      L.blocks[sh_dead_j] = __ldcg(L.blocks + nb - 1);
+      *L.nblocks = nb - 1;
+    }
+    best = lane < kLeanWarps ? sh_wfree2[lane] : kNone;
+    best = __reduce_min_sync(0xffffffffu, best);
+    nb2 = sh_dead_j >= 0 ? nb - 1 : nb;
+    __syncthreads();
+  }
+  const bool need = best == kNone;
+  const int m = n - vcount;
+  // ---- admission into the lowest free slot; relocation plan --------------------------
+  if (!need && tid == 0) atomicOr(&L.mask[best >> 4], 1 << (best & 15));
+  __syncthreads();
+  int t_live = 0;
+  const int outcome = vcount | (dead_blk >= 0 ? 2 : 0) | (need ? 4 : 0);
+  const int ndst = lane_plan_given(L, nb2, ((sh_over >> outcome) & 1u) != 0, false, need, &t_live, sh_scan2);
+  const bool work = need || ndst > 0;
+  // the allocator reads a lane's requests only when they are non-zero (see
+  // h2o_fast_step)
+  const bool publish = work || dead_blk >= 0 || stale_req;
+  if (tid == 0) {
+    A.ls.count[l] = m + 1;
+    if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
+    if (work || stale_req) {
+      A.ws.need_admit[l] = need ? 1 : 0;
+      A.ws.want_dst[l] = ndst;
+      A.ws.plan_tlive[l] = t_live;
+    }
+    if (work) atomicOr(A.ws.work_flag, 1);
+    *sh_work = work ? 1 : 0;
+  }
+  // ---- the table: entries after the victim move down one place; every read of a
+  // round precedes its barrier, the round's writes (one index lower) follow it -------
+  if (has_victim) {
+    if (tid == 0) A.victims[static_cast<size_t>(l) * dm.cap] = sh_vpos;
+    // round 0 was read before the eviction's barriers
+#pragma unroll
+    for (int u = 0; u < kShiftU; ++u) {
+      const int i = vi + 1 + u * kLeanThreads + tid;
+      if (i < n) { L.pos[i - 1] = sp[u]; L.slot[i - 1] = ssl[u]; L.score[i - 1] = ssc[u]; }
+    }
+    for (int base = vi + 1 + kLeanThreads * kShiftU; base < n; base += kLeanThreads * kShiftU) {
+#pragma unroll
+      for (int u = 0; u < kShiftU; ++u) {
+        const int i = base + u * kLeanThreads + tid;
+        if (i < n) { sp[u] = __ldcg(L.pos + i); ssl[u] = __ldcg(L.slot + i); ssc[u] = L.score[i]; }
+      }
+      __syncthreads();
+#pragma unroll
+      for (int u = 0; u < kShiftU; ++u) {
+        const int i = base + u * kLeanThreads + tid;
+        if (i < n) { L.pos[i - 1] = sp[u]; L.slot[i - 1] = ssl[u]; L.score[i - 1] = ssc[u]; }
+      }
+    }
+  }
+  __syncthreads();
+  if (!need && tid < d) {
+    static_cast<KT*>(A.ls.k_pool)[static_cast<size_t>(best) * d + tid] = knv;
+    static_cast<KT*>(A.ls.v_pool)[static_cast<size_t>(best) * d + tid] = vnv;
+  }
+  if (tid == 0) {
+    L.pos[m] = A.new_pos;
+    L.slot[m] = need ? -1 : static_cast<int>(best);
+    L.score[m] = 0.f;
+    A.n_victims[l] = vcount;
+    if (vcount) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_VICTIMS]), 1ull);
+    if (dead_blk >= 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_FREED_DEAD]), 1ull);
+    if (sh_nan) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_NAN_KEYS]), (unsigned long long)sh_nan);
+    if (l == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_STEPS]), 1ull);
+  }
+  // the done counter, once every thread's table writes are ordered before it
+  __syncthreads();
+  int done_old = 0;
+  if (tid == 0) {
+    const int inc = 1 + (work ? kWorkUnit : 0);
+    done_old = publish ? atomic_add_release(A.ws.epi_done, inc) : atomicAdd(A.ws.epi_done, inc);
+  }
+  // ---- output: combine the split-K partial outputs; a thread owns 8 adjacent
+  // elements of one head, four segments' loads in flight ----------------------------
+  if (A.has_q) {
+    const float* po = A.ws.part_o_buf[cbuf] + static_cast<size_t>(l) * kMaxSeg * g * d;
+    const bool out16 = (reinterpret_cast<uintptr_t>(A.out) & 15) == 0;
+    for (int q8 = tid; q8 < (g * d) >> 3; q8 += kLeanThreads) {
+      const int he = q8 * 8, h = he / d, e = he - h * d;
+      float acc[8];
+#pragma unroll
+      for (int t = 0; t < 8; ++t) acc[t] = 0.f;
+      for (int s0 = 0; s0 < nseg; s0 += 8) {
+        float4 x[8][2];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const int s2 = s0 + u;
+          const float4* src = reinterpret_cast<const float4*>(po + (static_cast<size_t>(s2) * g + h) * d + e);
+          x[u][0] = s2 < nseg ? __ldcg(src) : make_float4(0.f, 0.f, 0.f, 0.f);
+          x[u][1] = s2 < nseg ? __ldcg(src + 1) : make_float4(0.f, 0.f, 0.f, 0.f);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          const float c = s0 + u < nseg ? sh_scale[h][s0 + u] : 0.f;
+          acc[0] = fmaf(x[u][0].x, c, acc[0]); acc[1] = fmaf(x[u][0].y, c, acc[1]);
+          acc[2] = fmaf(x[u][0].z, c, acc[2]); acc[3] = fmaf(x[u][0].w, c, acc[3]);
+          acc[4] = fmaf(x[u][1].x, c, acc[4]); acc[5] = fmaf(x[u][1].y, c, acc[5]);
+          acc[6] = fmaf(x[u][1].z, c, acc[6]); acc[7] = fmaf(x[u][1].w, c, acc[7]);
+        }
+      }
+      const float r = sh_rL[h];
+      float* o = A.out + (static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e;
+      if (out16) {
+        reinterpret_cast<float4*>(o)[0] = make_float4(acc[0] * r, acc[1] * r, acc[2] * r, acc[3] * r);
+        reinterpret_cast<float4*>(o)[1] = make_float4(acc[4] * r, acc[5] * r, acc[6] * r, acc[7] * r);
+      } else {
+#pragma unroll
+        for (int t = 0; t < 8; ++t) o[t] = acc[t] * r;
+      }
     }
   }
   if (tid == 0) {
-    const bool mine = __ldcg(A.ws.need_admit + l) != 0 || __ldcg(A.ws.want_dst + l) > 0;
-    sh_apply = mine && wait_changed_bounded(A.ws.counters + kGenCounter, sh_gen, A.ws.status);
-  }
-  __syncthreads();
-  if (sh_apply) {
-    int* mv = reinterpret_cast<int*>(dsm);   // the step is done with the dynamic shared memory
-    apply_lane<KT>(A.ls, A.ws, dm, l, A.k_new, A.v_new, 0, nullptr, sh_scan, mv, mv + kApplyThreads);
+    *sh_last = (done_old & (kWorkUnit - 1)) == static_cast<int>(gridDim.x) - 1;
+    *sh_flag = (done_old >> kWorkShift) + (work ? 1 : 0);
+    *sh_sig = 1;
   }
 }
 
-// One lane's step after the attention kernel (all threads of the CTA).
+// The lean H2O epilogue: one CTA of kLeanThreads threads per lane, at most
+// 128 registers a thread and no dynamic shared memory, so that one of its
+// CTAs shares an SM with three CTAs of the attention kernel (which lets it
+// be scheduled from its start): the epilogue of a layer then runs while the
+// next layer's attention streams.  Lanes with more than one victim take the
+// general step (correct, slower with fewer threads).
+template <typename KT>
+__global__ void __launch_bounds__(kLeanThreads, 4) decode_epilogue_lean_kernel(EpiArgs A) {
+  __shared__ int sh_scan[40];
+  __shared__ int sh_work, sh_last, sh_flag, sh_sig, sh_gen;
+  __shared__ int sh_mv[2 * kLeanThreads];
+  const Dims& dm = A.dm;
+  const int l = blockIdx.x, tid = threadIdx.x;
+  // The next layer's attention may start now: it works on another layer and
+  // another scratch copy, and guards its copy itself.
+  grid_dep_launch();
+  LaneRefs L = lane_refs(A.ls, dm, l);
+  const int n = __ldcg(A.ls.count + l);
+  if (tid == 0) { sh_work = 0; sh_sig = 0; sh_gen = 0; }
+  if (n < 0 || n >= dm.cap) {
+    grid_dep_wait();
+    grid_dep_launch();
+    read_generation(A, &sh_gen);
+    if (tid == 0) {
+      set_status(A.ws.status, ST_CAPACITY);
+      A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
+    }
+  } else if (n + 1 - dm.budget <= 1 && n <= kLeanPer * kLeanThreads && dm.g <= 8 && dm.d <= kLeanThreads &&
+             (dm.d & 7) == 0) {
+    h2o_lean_step<KT>(A, L, n, &sh_sig, &sh_last, &sh_flag, &sh_gen, &sh_work);
+  } else {
+    lane_step<KT, false>(A, L, n, nullptr, &sh_work, &sh_gen);
+  }
+  epilogue_tail<KT>(A, sh_scan, &sh_work, &sh_last, &sh_flag, &sh_sig, &sh_gen, sh_mv, sh_mv + kLeanThreads);
+  scratch_released(A);
+}
+
+// One lane's step after the attention kernel (all threads of the CTA).  dsm
+// (the ring policies' row buffer, kEpiDynSmem bytes) is used only with kRing.
 template <typename KT, bool kRing>
 __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n, unsigned char* dsm,
-                                          int* sh_work) {
+                                          int* sh_work, int* sh_gen) {
   __shared__ float sh_M[kMaxG], sh_L[kMaxG], sh_lse2[kMaxG];
   __shared__ __align__(16) int sh_hist[256];   // also read as 64-bit words
   __shared__ int sh_misc[40];
@@ -782,7 +1280,7 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   const Dims& dm = A.dm;
   const int l = blockIdx.x, tid = threadIdx.x;
   const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
-  const int cbuf = A.layer & 1;
+  const int cbuf = A.layer % kScratchBufs;
   const int policy = dm.policy;
   constexpr bool ringp = kRing;   // SnapKV, DropKV decode variant: history ring keys
   const int W = dm.W;
@@ -795,7 +1293,7 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   // it is complete once it lets this one start, so the rows of all kept
   // tokens are copied to shared memory (when they fit beside the heads'
   // outputs and the keys) while the attention kernel drains.
-  float* hrows = sh_rows + kMaxG * 128;
+  float* hrows = kRing ? sh_rows + kMaxG * 128 : nullptr;
   const size_t hkeys_off = ((static_cast<size_t>(kMaxG) * 128 + static_cast<size_t>(n) * ld) * 4 + 7) & ~static_cast<size_t>(7);
   const bool staged_all = ringp && n > 0 && (W & 3) == 0 && hkeys_off + static_cast<size_t>(n + 1) * 8 <= kEpiDynSmem;
   if (staged_all) stage_history_async(L, n, W, ld, dm.P * kBlock, hrows, reinterpret_cast<int*>(dsm + hkeys_off));
@@ -803,6 +1301,7 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   // ---- general path ------------------------------------------------------------
   grid_dep_wait();      // the attention kernel's results are complete and visible
   grid_dep_launch();
+  read_generation(A, sh_gen);
   if (tid == 0) { sh_nan = 0; sh_ncand = 0; }
   if (n > 0 && L.pos[n - 1] >= A.new_pos) {
     if (staged_all) cp_async_wait_all();
@@ -848,7 +1347,7 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       for (int s = 0; s < nseg; ++s) acc = fmaf(po[(static_cast<size_t>(s) * g + h) * d + e], sh_scale[s][h], acc);
       const float o = acc / sh_L[h];
       A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = o;
-      sh_rows[he] = o;    // the heads' outputs, for the DropKV scores below
+      if constexpr (kRing) sh_rows[he] = o;    // the heads' outputs, for the DropKV scores below
     }
     __syncthreads();
   }
@@ -1108,7 +1607,7 @@ __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const 
   }
   __syncthreads();
   if (*sh_flag == 0) {
-    if (tid == 0) { ws.counters[1] = 0; ws.counters[2] = 0; }
+    if (tid == 0) { ws.counters[1] = 0; ws.counters[2] = 0; ws.counters[kApplyCount] = 0; }
     return;
   }
   // exclusive prefixes over lanes: admissions, destinations, moved tokens
@@ -1179,9 +1678,22 @@ __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const 
       ls.owner[ws.alloc_ids[totA + q]] = lo - 1;
     }
   }
+  // the lanes left with work for apply, ascending (each thread reads the
+  // requests of the lanes it updated above)
+  int nwork = 0;
+  for (int base = 0; base < dm.lanes; base += blockDim.x) {
+    const int l = base + tid;
+    const int has = (l < dm.lanes && (__ldcg(ws.need_admit + l) != 0 || __ldcg(ws.want_dst + l) > 0)) ? 1 : 0;
+    int tot;
+    const int ex = block_excl_scan(has, sh_scan, &tot);
+    if (has) ws.apply_list[nwork + ex] = l;
+    nwork += tot;
+  }
   if (tid == 0) {
     ws.counters[1] = 1;
     ws.counters[2] = deferred ? 0 : totM;
+    ws.counters[kApplyCount] = nwork;
+    ws.counters[kApplyClaim] = 0;
     if (deferred && totD > 0)
       atomicAdd(reinterpret_cast<unsigned long long*>(&ls.stats[SC_DEFERRED]), 1ull);
   }
@@ -1352,7 +1864,7 @@ __global__ void __launch_bounds__(kApplyThreads, 1) apply_kernel(LayerState ls, 
 
 cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, const void* k_new,
                             const void* v_new, float* out, float* lse, int32_t* victims,
-                            int32_t* n_victims, cudaStream_t stream) {
+                            int32_t* n_victims, cudaStream_t stream, bool* needs_apply_kernel) {
   EpiArgs A;
   A.ls = layer_state(ctx, layer);
   A.ws = ctx.ws;
@@ -1362,18 +1874,25 @@ cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, 
   // deferred relocation: Eq. (1)'s test never passes here (F <= 1)
   if (ctx.defer_reloc) A.dm.theta_f = INFINITY;
   A.has_q = has_q ? 1 : 0;
-  A.applies = ctx.epi_applies ? 1 : 0;
   A.new_pos = new_pos;
   A.layer = layer;
   A.k_new = k_new; A.v_new = v_new;
   A.out = out; A.lse = lse; A.victims = victims; A.n_victims = n_victims;
-  // After this layer's attention launch the predecessor triggers only once
-  // its own predecessors are complete; without one, the predecessor may be
-  // the last step's apply, whose epilogue may still be writing that layer's
-  // tables, which this kernel reads before its dependency wait.
-  const bool pdl = has_q || ctx.last_layer != layer;
+  // Early start (programmatic dependent launch) only right after this
+  // layer's attention launch: the epilogue then reads, before its dependency
+  // wait, tables no running kernel writes.  A query-less epilogue waits for
+  // its predecessor.
+  const bool pdl = has_q && ctx.last_kind == kLaunchAttend && ctx.last_layer == layer;
   const bool ring = ctx.dims.policy != KVEVICT_H2O;
-  const dim3 grid(ctx.dims.lanes), block(kEpiThreads);
+  const dim3 grid(ctx.dims.lanes);
+  // the lean H2O epilogue when every lane is within its budget (a hint from
+  // the host's record of the layer; either kernel is correct in every case)
+  const bool lean = !ring && ctx.lean_epi && ctx.layer_steady[layer];
+  A.applies = (lean || ctx.epi_applies) ? 1 : 0;
+  if (needs_apply_kernel) *needs_apply_kernel = !A.applies;
+  if (lean)   // bf16 pools only (see kvevict_create)
+    return launch_k(decode_epilogue_lean_kernel<__nv_bfloat16>, grid, dim3(kLeanThreads), 0, stream, pdl, A);
+  const dim3 block(kEpiThreads);
   if (ctx.dims.dtype == KVEVICT_BF16)
     return ring ? launch_k(decode_epilogue_kernel<__nv_bfloat16, true>, grid, block, kEpiDynSmem, stream, pdl, A)
                 : launch_k(decode_epilogue_kernel<__nv_bfloat16, false>, grid, block, kEpiDynSmem, stream, pdl, A);
@@ -1388,19 +1907,40 @@ cudaError_t prepare_epilogue() {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_kernel<__nv_bfloat16, true>, a, bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_kernel<float, false>, a, bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_kernel<float, true>, a, bytes);
+  // the lean kernel shares SMs with the attention kernel, which needs the
+  // largest shared-memory carveout: ask for the same one
+  const cudaFuncAttribute c = cudaFuncAttributePreferredSharedMemoryCarveout;
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_lean_kernel<__nv_bfloat16>, c, 100);
   return e;
 }
 
+// The smallest occupancy over the large kernel's four instantiations (any
+// of them may run a decode step).
 int epilogue_ctas_per_sm() {
+  int best = 1 << 30;
+  auto take = [&](auto kernel) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kEpiThreads, kEpiDynSmem) != cudaSuccess) n = 0;
+    best = n < best ? n : best;
+  };
+  take(decode_epilogue_kernel<__nv_bfloat16, false>);
+  take(decode_epilogue_kernel<__nv_bfloat16, true>);
+  take(decode_epilogue_kernel<float, false>);
+  take(decode_epilogue_kernel<float, true>);
+  return best;
+}
+
+cudaError_t lean_epilogue_attributes(cudaFuncAttributes* a, int* threads) {
+  *threads = kLeanThreads;
+  return cudaFuncGetAttributes(a, decode_epilogue_lean_kernel<__nv_bfloat16>);
+}
+
+int lean_epilogue_ctas_per_sm() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_epilogue_kernel<__nv_bfloat16, true>, kEpiThreads,
-                                                    kEpiDynSmem) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_epilogue_lean_kernel<__nv_bfloat16>, kLeanThreads,
+                                                    0) != cudaSuccess)
     return 0;
-  int m = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&m, decode_epilogue_kernel<float, false>, kEpiThreads,
-                                                    kEpiDynSmem) != cudaSuccess)
-    return 0;
-  return n < m ? n : m;
+  return n;
 }
 
 cudaError_t launch_allocate(const Ctx& ctx, const Workspace& ws, int layer, cudaStream_t stream) {

@@ -18,6 +18,7 @@ constexpr int kMaxW = 64;           // largest SnapKV obsWindow supported
 constexpr int kMaxG = 16;           // largest GQA group
 constexpr int kAttendWarps = 4;     // warps per CTA of the decode kernel
 constexpr int kStages = 3;          // copy stages per warp of the decode kernel
+constexpr int kScratchBufs = 3;     // copies of the decode split-K scratch (layer l uses copy l % 3)
 
 // device status bits (read and cleared by kvevict_last_error)
 enum : uint32_t {
@@ -61,12 +62,16 @@ constexpr int kFreedRanges = 256;   // most CTAs the freed-list kernels use
 struct Workspace {
   uint32_t* status;                // 1 word
   int32_t* work_flag;              // 1 word: any lane needs the allocator this call
-  // split-K scratch, two copies: layer l uses copy l & 1, so the attention of
-  // layer l+1 may overlap the epilogue of layer l
-  float* logits_buf[2];            // [lanes][g][lcap] base-2 scaled logits
-  float* part_o_buf[2];            // [lanes][kMaxSeg][g][d]
-  float* part_ml_buf[2];           // [lanes][kMaxSeg][g][2]  (max, sum), base 2
-  int32_t* lane_nseg_buf[2];       // [lanes]
+  // split-K scratch, kScratchBufs copies: layer l uses copy l % kScratchBufs,
+  // so the attention of layer l+1 may run beside the epilogues of layers l and
+  // l-1.  reads_done[c] counts the epilogue CTAs that have finished with copy
+  // c (monotonic, wrapping); an attention writes copy c only once every
+  // epilogue launched on it before has finished.
+  float* logits_buf[kScratchBufs];       // [lanes][g][lcap] base-2 scaled logits
+  float* part_o_buf[kScratchBufs];       // [lanes][kMaxSeg][g][d]
+  float* part_ml_buf[kScratchBufs];      // [lanes][kMaxSeg][g][2]  (max, sum), base 2
+  int32_t* lane_nseg_buf[kScratchBufs];  // [lanes]
+  uint32_t* reads_done;                  // [kScratchBufs]
   unsigned long long* keys64;      // [lanes][cap]  window sums (monotone images), when not in shared memory
   unsigned long long* pooled64;    // [lanes][cap]  pooled keys (monotone images), several victims
   int32_t* need_admit;             // [lanes]
@@ -78,9 +83,10 @@ struct Workspace {
   int32_t* alloc_ids;              // [P]
   int32_t* freed_flag;             // [P]  1 = released during this call
   int32_t* blk_tag;                // [P]  1 = source block of a running plan
-  int32_t* counters;               // [8] per-call scalars
+  int32_t* counters;               // [16] per-call scalars
   int32_t* freed_part;             // [kFreedRanges] freed blocks per range of the pool (freed list)
   int32_t* epi_done;               // 1 word: epilogue CTAs finished this call
+  int32_t* apply_list;             // [lanes]  lanes left with an admission or a relocation to apply
   // DropKV prefill-window scorer
   float* d3_part;                  // [lanes][chunks][rows_cap][d + 2]
   __nv_bfloat16* d3_ahi;           // [lanes][rows][d]
@@ -103,11 +109,16 @@ struct Ctx {
   int device;
   size_t ws_bytes;
   int attend_ctas_per_sm;
-  // Layer of the most recent attention or decode-step launch (-1: none).
-  // Those kernels may still run when the next kernel starts under
-  // programmatic dependent launch, so a launch that would touch that layer's
-  // tables or its parity's scratch is not launched early.
+  // One CTA of the lean H2O epilogue fits on an SM beside attend_ctas_per_sm
+  // CTAs of the attention kernel (registers, shared memory, threads).
+  bool lean_coresident;
+  // Launch history for programmatic dependent launch: the most recent launch
+  // (kLaunch*, its layer), and per scratch copy the number of decode
+  // epilogues launched on it (wrapping), whose CTAs the next attention on
+  // that copy waits for (Workspace::reads_done).
   int last_layer;
+  int last_kind;
+  uint32_t epi_launches[kScratchBufs];
   // TMA tensor maps over each layer's K and V pool ([P * 16 rows][d], bf16,
   // 128-byte swizzle, boxes of one 64-element half row x 1, 16 or 64 rows),
   // kTmapsPerLayer per layer, for the window scoring's row copies; null when
@@ -129,7 +140,39 @@ struct Ctx {
   // lane): the epilogue then also applies its lane's admission and
   // relocation after the layer allocator, and no apply kernel is launched.
   bool epi_applies;
+  // The lean H2O epilogue (one small CTA per lane, beside the attention
+  // kernel's CTAs) can serve this configuration.
+  bool lean_epi;
+  // Per layer [L] (host): every lane of the layer holds at most its budget,
+  // so a decode step evicts at most one token per lane and the lean
+  // epilogue is the right kernel.  A performance hint only: both epilogue
+  // kernels handle every case.
+  bool* layer_steady;
 };
+
+enum : int { kLaunchOther = 0, kLaunchAttend = 1, kLaunchEpilogue = 2, kLaunchApply = 3 };
+
+// Launch-history rules (host).  An attention kernel checks on the device,
+// before it writes anything, that every decode epilogue launched earlier on
+// its scratch copy has finished (which also covers every earlier epilogue of
+// its own layer, which uses the same copy), so it may start early after any
+// kernel but a separate apply kernel, which rewrites a layer's tables after
+// its epilogue has finished.  The epilogue starts early only right after its
+// layer's attention launch.
+inline bool attend_early_ok(const Ctx& c) { return c.last_kind != kLaunchApply; }
+inline void note_attend(Ctx& c, int layer) {
+  c.last_kind = kLaunchAttend;
+  c.last_layer = layer;
+}
+inline void note_epilogue(Ctx& c, int layer) {
+  c.epi_launches[layer % kScratchBufs] += 1u;
+  c.last_kind = kLaunchEpilogue;
+  c.last_layer = layer;
+}
+inline void note_apply(Ctx& c) { c.last_kind = kLaunchApply; }
+// Kernels launched without early start (they never let a successor start
+// before they complete).
+inline void note_other(Ctx& c) { c.last_kind = kLaunchOther; }
 
 // workspace layout (host)
 bool has_ring(const kvevict_config& c);
@@ -151,7 +194,7 @@ cudaError_t prepare_tensor_maps(Ctx& ctx);
 // kernel launchers (host)
 cudaError_t launch_reset(const Ctx&, cudaStream_t);
 cudaError_t launch_prefill(const Ctx&, int layer, const void* k, const void* v, int n, cudaStream_t);
-cudaError_t launch_decode(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
+cudaError_t launch_decode(Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
                           int new_pos, float* out, float* lse, int32_t* victims, int32_t* n_victims,
                           cudaStream_t);
 cudaError_t launch_select(const Ctx&, const void* keys, int key_dtype, const int32_t* positions,
@@ -169,15 +212,19 @@ cudaError_t launch_wait_check(const Ctx&, int polls, cudaStream_t);
 cudaError_t launch_attend_into(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
                                float* logits, float* part_o, float* part_ml, int32_t* lane_nseg, cudaStream_t);
 cudaError_t prepare_epilogue();     // one-time attributes of the epilogue kernels
-int epilogue_ctas_per_sm();         // co-resident decode-epilogue CTAs per SM
+int epilogue_ctas_per_sm();         // co-resident decode-epilogue CTAs per SM (the large kernel)
+int lean_epilogue_ctas_per_sm();    // the same for the lean H2O epilogue
+cudaError_t lean_epilogue_attributes(cudaFuncAttributes*, int* threads);
 cudaError_t prepare_select();       // one-time attributes of the selection kernels
 cudaError_t prepare_dropkv();       // one-time attributes of the window-scoring kernels
 cudaError_t prepare_kernels(Ctx&);   // one-time kernel attributes and occupancy (not stream work)
+// early_trigger: the successor in the stream is this layer's decode
+// epilogue, which may be scheduled as soon as the attention starts.
 cudaError_t launch_attend(const Ctx&, int layer, const void* q, const void* k_new, const void* v_new,
-                          cudaStream_t);
+                          cudaStream_t, bool early_trigger);
 cudaError_t launch_epilogue(const Ctx&, int layer, bool has_q, int new_pos, const void* k_new,
                             const void* v_new, float* out, float* lse, int32_t* victims,
-                            int32_t* n_victims, cudaStream_t);
+                            int32_t* n_victims, cudaStream_t, bool* used_apply_kernel = nullptr);
 cudaError_t launch_allocate(const Ctx&, const Workspace& ws, int layer, cudaStream_t);
 cudaError_t launch_allocate_apply(const Ctx&, int layer, const void* k_new, const void* v_new,
                                   bool mark_freed, int32_t* moves, cudaStream_t, bool with_allocate);
@@ -293,6 +340,11 @@ __device__ __forceinline__ bool wait_changed_bounded(const int* p, int old, uint
   }
   set_status(status, ST_TIMEOUT);
   return false;
+}
+
+// Pulls the 128-byte line holding p into L2 (no registers, no completion).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+  asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
 __device__ __forceinline__ void fence_proxy_async() {

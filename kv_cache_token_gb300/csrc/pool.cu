@@ -950,17 +950,26 @@ cudaError_t launch_stats(const Ctx& ctx, int layer, long long* out, cudaStream_t
   return cudaGetLastError();
 }
 
-cudaError_t launch_decode(const Ctx& ctx, int layer, const void* q, const void* k_new, const void* v_new,
+cudaError_t launch_decode(Ctx& ctx, int layer, const void* q, const void* k_new, const void* v_new,
                           int new_pos, float* out, float* lse, int32_t* victims, int32_t* n_victims,
                           cudaStream_t stream) {
   cudaError_t e;
   if (q) {
-    e = launch_attend(ctx, layer, q, k_new, v_new, stream);
+    e = launch_attend(ctx, layer, q, k_new, v_new, stream, true);
     if (e != cudaSuccess) return e;
+    note_attend(ctx, layer);
   }
-  e = launch_epilogue(ctx, layer, q != nullptr, new_pos, k_new, v_new, out, lse, victims, n_victims, stream);
-  if (e != cudaSuccess || ctx.epi_applies) return e;
-  return launch_allocate_apply(ctx, layer, k_new, v_new, false, nullptr, stream, false);
+  bool apply_kernel = false;
+  e = launch_epilogue(ctx, layer, q != nullptr, new_pos, k_new, v_new, out, lse, victims, n_victims, stream,
+                      &apply_kernel);
+  if (e != cudaSuccess) return e;
+  note_epilogue(ctx, layer);
+  // every lane of the layer is now within its budget
+  ctx.layer_steady[layer] = true;
+  if (!apply_kernel) return e;
+  e = launch_allocate_apply(ctx, layer, k_new, v_new, false, nullptr, stream, false);
+  note_apply(ctx);
+  return e;
 }
 
 }  // namespace kve

@@ -15,7 +15,10 @@
 // loads the library until the process exits.  Host code cannot use the
 // array's name as a device address, so the first call on each device looks
 // the address up (cudaGetSymbolAddress) with that device current and keeps
-// it; that first call should therefore happen before any stream capture.
+// it, together with the CUDA context it belongs to; that first call should
+// therefore happen before any stream capture.  A later call that finds
+// another context current on the device (after cudaDeviceReset, say) looks
+// the address up again.
 // All calls share the one array: calls whose kernels overlap on the GPU (two
 // streams, or two host threads) race on it and give undefined results.
 // Nothing in it needs to start at zero: every scratch word a call reads was
@@ -33,6 +36,24 @@ static __device__ __align__(256) unsigned char g_attend_scratch[kStaticBytes];
 
 std::mutex g_mu;
 void* g_scratch_addr[kMaxDevices] = {};
+CUcontext g_scratch_ctx[kMaxDevices] = {};
+
+// The calling thread's current CUDA context (null if none or not known),
+// through the runtime's driver entry point.
+CUcontext current_context() {
+  using GetCurrent = CUresult (*)(CUcontext*);
+  static GetCurrent fn = [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+    if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &f, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      f = nullptr;
+    return reinterpret_cast<GetCurrent>(f);
+  }();
+  CUcontext c = nullptr;
+  if (!fn || fn(&c) != CUDA_SUCCESS) return nullptr;
+  return c;
+}
 
 inline size_t up256(size_t x) { return (x + 255) / 256 * 256; }
 
@@ -97,10 +118,12 @@ extern "C" kvevict_status kvevict_attend_static(kvevict_ctx* ctx, int layer, con
   char* base = nullptr;
   {
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_scratch_addr[dev]) {
+    const CUcontext cur = current_context();
+    if (!g_scratch_addr[dev] || !cur || cur != g_scratch_ctx[dev]) {
       void* p = nullptr;
       if (cudaGetSymbolAddress(&p, g_attend_scratch) != cudaSuccess || !p) return KVEVICT_E_CUDA;
       g_scratch_addr[dev] = p;
+      g_scratch_ctx[dev] = current_context();   // the lookup made the device's context current
     }
     base = static_cast<char*>(g_scratch_addr[dev]);
   }
