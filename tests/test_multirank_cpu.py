@@ -63,3 +63,22 @@ def test_two_gloo_ranks_aggregate_timing_and_own_workloads():
 def test_single_process_aggregation_is_identity():
     import bench
     assert bench.aggregate_over_ranks(3.0, 7.0, 2.0) == (3.0, 7.0, 2.0)
+
+
+def test_bench_gpus_flag_launches_ranks_itself():
+    """`bench.py --gpus 2` started without a launcher re-runs itself as two
+    ranks (torch.distributed.run, 127.0.0.1 rendezvous); rank 0 prints one
+    line aggregated over both (here on CPU ranks with stand-in work)."""
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    env = {k: v for k, v in os.environ.items() if k not in ("WORLD_SIZE", "RANK", "LOCAL_RANK")}
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--gpus", "2", "--selftest-cpu"],
+                       capture_output=True, text=True, timeout=240, env=env, cwd=root)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [l for l in r.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1, r.stdout
+    d = json.loads(lines[0])
+    assert d["n_gpus"] == 2 and d["config"]["ranks"] == 2
+    assert d["value"] > 0 and d["ms_per_step"] > 0
