@@ -128,3 +128,25 @@ def near_tie(ref_keys, ref_pos, got_v, ref_v, rtol=RTOL):
     chosen = [key_of[p] for p in b]
     thr = max(chosen) if chosen else 0.0
     return all(abs(key_of[p] - thr) <= rtol * abs(thr) + 1e-12 for p in diff)
+
+
+def count_tie_swaps(ref_keys, ref_pos, got_v, ref_v, what, rtol=RTOL, floor=SCORE_FLOOR):
+    """Number of victims the GPU chose that the oracle did not (as many the
+    other way round), after checking that every such token's oracle key lies
+    within the score tolerance of the oracle's selection threshold (the
+    largest key the oracle evicted): a swap between near-equal keys, which
+    fp32 against fp64 scoring may order differently.  Raises otherwise."""
+    a, b = set(np.asarray(got_v).tolist()), set(np.asarray(ref_v).tolist())
+    assert len(a) == len(b), "%s: %d victims against %d" % (what, len(a), len(b))
+    if a == b:
+        return 0
+    keys = np.asarray(ref_keys, dtype=np.float64)
+    key_of = dict(zip(np.asarray(ref_pos).tolist(), keys.tolist()))
+    thr = max(key_of[p] for p in b)
+    fin = keys[np.isfinite(keys)]
+    scale = float(np.max(np.abs(fin))) if fin.size else 0.0
+    for p in a ^ b:
+        k = key_of[p]
+        assert abs(k - thr) <= rtol * abs(thr) + floor * scale, \
+            "%s: position %d (oracle key %r) differs from the threshold %r beyond the tolerance" % (what, p, k, thr)
+    return len(a - b)

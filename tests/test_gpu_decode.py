@@ -284,3 +284,44 @@ def test_more_lanes_than_resident_epilogue_ctas():
     shp = scaled("h2o_70b", num_layers=1, batch=20, num_kv_heads=8, num_q_heads=64, ctx=200, steps=4,
                  budget=64, recent_window=16)
     run_decode(shp, 4)
+
+
+def test_decode_steps_while_another_stream_holds_the_sms():
+    """The epilogue applies admissions into fresh blocks and relocations
+    itself, lane by lane, claimed by its CTAs once the layer allocator has
+    published its result; a CTA that gave up waiting leaves its lane to the
+    others.  Here a second stream keeps every SM busy with long matrix
+    products while the decode steps run (the first step is a mass eviction
+    with a relocation in every lane, the later ones the steady state): every
+    step's outputs, victims and tables still match the oracle."""
+    shp = scaled("h2o_70b", num_layers=2, batch=4, num_kv_heads=8, num_q_heads=64, ctx=1200, steps=6,
+                 budget=300, recent_window=100)
+    wl = Workload(shp)
+    eng, orc = make_pair(shp, layers=[0, 1])
+    for layer in (0, 1):
+        prefill_both(eng, orc, wl, layer)
+    side = torch.cuda.Stream()
+    a = torch.randn((8192, 8192), dtype=torch.bfloat16, device="cuda")
+    bmat = torch.randn((8192, 8192), dtype=torch.bfloat16, device="cuda")
+    torch.cuda.synchronize()
+    for t in range(shp.steps):
+        with torch.cuda.stream(side):
+            for _ in range(4):
+                torch.matmul(a, bmat)          # ~ms of work on every SM, concurrent with the step
+        for layer in (0, 1):
+            q, kn, vn, pos = wl.step(layer, t)
+            out, lse, vic, nv = eng.decode_step(layer, q.cuda(), kn.cuda(), vn.cuda(), pos)
+            ref = orc.decode_step(layer, q.double().numpy(), kn.double().numpy(), vn.double().numpy(), pos)
+            torch.cuda.synchronize()
+            assert_rows_close(out.cpu().numpy(), ref["out"], "step %d layer %d out" % (t, layer))
+            got = victim_lists(nv, vic)
+            for l in range(eng.lanes):
+                assert np.array_equal(got[l], ref["victims"][l]) or \
+                    near_tie(ref["keys"][l], ref["pos"][l], got[l], ref["victims"][l]), \
+                    "step %d layer %d lane %d victims" % (t, layer, l)
+            compare_states(gpu_state(eng, layer), oracle_state(orc, layer), shp.policy,
+                           "step %d layer %d" % (t, layer))
+    st = eng.stats(0).cpu().numpy()
+    assert st[5] > 0, "the first step relocated tokens"
+    code, msg = eng.last_error()
+    assert code == 0, msg

@@ -5,8 +5,8 @@ import numpy as np
 import pytest
 import torch
 
-from tests.gpu_helpers import (assert_rows_close, assert_scores_close, compare_states, gpu_state,
-                               make_pair, oracle_state, prefill_both)
+from tests.gpu_helpers import (assert_rows_close, assert_scores_close, compare_states, count_tie_swaps,
+                               gpu_state, make_pair, oracle_state, prefill_both)
 from workloads import Workload, scaled
 
 pytestmark = pytest.mark.gpu
@@ -136,3 +136,26 @@ def test_window_scores_scattered_slots():
         assert_scores_close(sc[l, :n].cpu().numpy(), ref["scores"][l], "lane %d scores" % l)
     code, msg = eng.last_error()
     assert code == 0, msg
+
+
+def test_victims_from_gpu_scores_end_to_end():
+    """The whole chain on the GPU (window scores, then the budgeted selection
+    on those scores) against the oracle's selection on its own float64
+    scores: the victim sets are equal except for swaps between tokens whose
+    oracle keys are within the score tolerance of the threshold (DropKV
+    explainer: drop the k lowest-scoring tokens); the swap count is printed
+    and bounded."""
+    shp = scaled("dropkv_prefill", ctx=6000, num_kv_heads=2, num_q_heads=8, budget=300, recent_window=64)
+    eng, orc, sc, ref = run_score(shp)
+    v, nv = eng.select(sc, eng.positions[0].contiguous(), eng.counts[0].contiguous(), shp.budget,
+                       shp.recent_window)
+    torch.cuda.synchronize()
+    from oracle.select import select_lane
+    swaps = 0
+    for l in range(eng.lanes):
+        L = orc.layers[0].lanes[l]
+        r = select_lane(np.asarray(ref["scores"][l], np.float64), L.pos, shp.budget, shp.recent_window)
+        got = v[l, :int(nv[l])].cpu().numpy()
+        swaps += count_tie_swaps(ref["scores"][l], L.pos, got, r, "lane %d" % l)
+    print("NEAR-TIE swaps, DropKV window scoring + selection (6000 tokens x %d lanes): %d" % (eng.lanes, swaps))
+    assert swaps <= 2

@@ -13,8 +13,8 @@ import torch
 
 from kv_cache_token_gb300 import Engine, config_from
 from oracle.engine import Engine as Oracle
-from tests.gpu_helpers import (assert_rows_close, assert_scores_close, compare_states, gpu_state, near_tie,
-                               oracle_state, victim_lists)
+from tests.gpu_helpers import (assert_rows_close, assert_scores_close, compare_states, count_tie_swaps,
+                               gpu_state, near_tie, oracle_state, victim_lists)
 from workloads import Workload, shape
 
 pytestmark = pytest.mark.gpu
@@ -77,7 +77,8 @@ def run_sampled_decode(shp, lanes, steps):
                 assert_scores_close(eng.ring[0][slots].cpu().numpy().ravel(), L.hist.ravel(),
                                     "step %d lane %d history" % (t, lane))
     assert eng.last_error()[0] == 0
-    assert len(live) >= len(lanes) // 2, "too many near-tie swaps: %d" % swaps
+    print("NEAR-TIE swaps, %s: %d of %d sampled lanes over %d steps" % (shp.name, swaps, len(lanes), steps))
+    assert swaps <= 1, "near-tie swaps: %d" % swaps
     return swaps
 
 
@@ -166,4 +167,36 @@ def test_paged_128k_compaction_full_size():
     assert nf > freed_block_gran and F < Fb
     print("128K: freed token-level %d vs block-granular %d; F %.3f vs %.3f; blocks <=50%% %d vs %d"
           % (nf, freed_block_gran, F, Fb, half, half_b))
+    assert eng.last_error()[0] == 0
+
+
+@pytest.mark.parametrize("name", ["dropkv_prefill", "paged_128k"])
+def test_victims_from_gpu_scores_full_lane(name):
+    """Configurations 3 and 5 end to end on one full lane: the GPU's window
+    scores of all 8 lanes, the GPU's selection to the budget on them, and
+    lane 0's victim set against the oracle's selection on its float64 scores
+    of the whole lane (swaps only between near-equal keys; counted)."""
+    shp = shape(name)
+    wl = Workload(shp)
+    eng = Engine(config_from(shp))
+    eng.reset()
+    K, V = wl.context(0, device="cuda")
+    eng.prefill(0, K, V)
+    q, qp = wl.window(0, device="cuda")
+    lse, a, sc = eng.score(0, q, qp)
+    v, nv = eng.select(sc, eng.positions[0].contiguous(), eng.counts[0].contiguous(), shp.budget,
+                       shp.recent_window)
+    torch.cuda.synchronize()
+    g, lane = shp.group, 0
+    o = lane_oracle(shp, K[0, 0].double().cpu().numpy(), V[0, 0].double().cpu().numpy())
+    del K, V
+    r = o.score(0, q[0:1, 0:g].double().cpu().numpy(), qp.cpu().numpy())
+    from oracle.select import select_lane
+    L = o.layers[0].lanes[0]
+    ref_v = select_lane(np.asarray(r["scores"][0], np.float64), L.pos, shp.budget, shp.recent_window)
+    got = v[lane, :int(nv[lane])].cpu().numpy()
+    assert got.size == ref_v.size == shp.ctx - shp.budget
+    swaps = count_tie_swaps(r["scores"][0], L.pos, got, ref_v, "%s lane 0" % name)
+    print("NEAR-TIE swaps, %s lane 0 (%d victims of %d tokens): %d" % (name, ref_v.size, shp.ctx, swaps))
+    assert swaps <= 4
     assert eng.last_error()[0] == 0
