@@ -361,9 +361,11 @@ kvevict_status kvevict_attend_static(kvevict_ctx* ctx, int layer, const void* q,
                                      const void* v_new, float* out, float* lse, void* stream);
 
 /* Kernels one kvevict_decode_step with a query launches: 2 (attention, then
- * the epilogue, which also applies admissions into fresh blocks and
- * relocations, when all its one-CTA-per-lane grid fits on the device at
- * once) or 3 (an apply kernel follows); 0 for a NULL context. */
+ * one epilogue: the small one that runs beside the next layer's attention
+ * when it fits on the SMs the attention leaves free, or the larger one that
+ * also applies admissions into fresh blocks and relocations when all its
+ * one-CTA-per-lane grid fits on the device at once) or 3 (an apply kernel
+ * follows); 0 for a NULL context. */
 int32_t kvevict_kernels_per_decode_step(const kvevict_ctx* ctx);
 
 /* Writes KVEVICT_NSTATS int64 counters of one layer to out (device). */
