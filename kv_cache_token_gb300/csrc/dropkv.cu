@@ -68,7 +68,7 @@ struct D3Args {
   Dims dm;
   const __nv_bfloat16* q;   // [B][Hq][w][d]
   const int32_t* qpos;      // [w]
-  int w, rows, rows_cap, chunks, chunk_keys;   // chunk_keys: keys per CTA, a multiple of 64
+  int w, rows, rows_cap, chunks, chunk_keys;   // chunk_keys: keys per CTA, a multiple of 128
   float* lse_out; float* a_out; float* scores;
   float* col_out;   // where pass 2 leaves each key's column sum (scores, or scratch ahead of pooling)
   float scale2;
@@ -544,43 +544,61 @@ __global__ void __launch_bounds__(256) d3_pool_kernel(const float* __restrict__ 
 }
 
 // ---------------------------------------------------------------------------
-// tcgen05 path: all window rows of a lane (up to 256 = two 128-row tiles) per
-// CTA, one thread per row, accumulators in tensor memory.
+// tcgen05 path.  A CTA owns one 128-row tile of a lane's window rows (rows
+// 0-127, and 128-255 when there are more) and one chunk of the lane's keys;
+// the CTAs of the two row tiles of a chunk are grid neighbours, run side by
+// side and read the same K and V rows (the second read is served by L2).
 //
-// pass 1, per 64-key tile:  S = Q K^T (Q and K in shared memory, 128-byte
-//   swizzle); each thread masks and exponentiates its row (lazy rescale of
-//   the running max), writes P as bf16 hi + lo over S in tensor memory, and
-//   O += P V takes P from tensor memory and V (MN-major) from shared memory.
-//   Tensor-memory columns: O of tile 0 / 1 at 0 / 128; S-P double buffer at
-//   256 + 128 * (t & 1) (+ 64 for row tile 1).  The row warps also take
-//   |v|^2 of every key for pass 2.
-// pass 2, per 64-key tile:  S = Q K^T and G = a V^T (a as bf16 hi + lo held
-//   in tensor memory); each thread copies its row of S and G to registers,
-//   which frees the buffer for the next tile's MMAs, and turns them into
-//   residual terms (32 keys at a time through one copy of the code); each warp sums its 32 rows per key
-//   by a butterfly, and the producer adds the 8 warp sums in a fixed order
-//   when the tile's stage is recycled and writes the final scores.  While
-//   every weight of a warp's rows is below 2^-7, p / (1 - p) is the series
-//   p (1 + p (1 + p)) instead of a reciprocal.
-//   Tensor-memory columns: a hi 0 / 64, a lo 128 / 192, S 256 / 320,
-//   G 384 / 448 (row tile 0 / 1).  (MMAs of 32 keys, which would let two
-//   buffers fit, re-read Q from shared memory for half the keys and ran
-//   at a fraction of the rate.)
-// K/V rows arrive by TMA gathers (four pool rows per copy, 128-byte swizzle
-// applied by the copy engine) into a four-stage ring.
+// pass 1, per 64-key tile: S = Q K^T on the tensor cores.  Two groups of four
+//   row warps (one thread per row) take alternate tiles.  Each group keeps its
+//   own running max and sum per row and its own output accumulator O_g in
+//   tensor memory; the two are merged at the end like two chunks, so no two
+//   threads ever share a row's softmax state.  A thread masks and
+//   exponentiates its row of S (lazy rescale of the running max), writes P as
+//   bf16 hi + lo over S, and O_g += P V takes P from tensor memory and V
+//   (MN-major) from shared memory.  The group also takes |v|^2 of the tile's
+//   keys for pass 2.  Tensor-memory columns: O_A 0, O_B 128, four S/P buffers
+//   at 256 + 64 b (tile t in b = t % 4); S runs three tiles ahead of P V.  K
+//   and V have rings of their own: a K stage is free once its S is computed,
+//   a V stage once P V and the |v|^2 job are done with it.
+// pass 2, per 128-key tile: S^T = K Q^T and G^T = V a^T (a as bf16 hi + lo;
+//   Q, a hi and a lo stay in shared memory).  Tensor-memory lanes are keys
+//   and columns rows, so a thread owns one key and sums its terms over 64
+//   rows in a register: no reduction across threads.  The two warps sharing a
+//   key add their sums in a fixed order; with two row tiles both CTAs add
+//   theirs into the output, which pass 1 zeroed (two addends onto zero: the
+//   result is the same whichever lands first).  Tensor-memory columns:
+//   buffer b (tile t % 2) holds S^T at 256 b and G^T at 256 b + 128.
+// The attention-mass modes skip V: pass 1 keeps (max, sum) per row and
+// pass 2 sums the weights p themselves.
+// K and V rows arrive by TMA: a 64-row box per 64 consecutive slots (the
+// layout a prefill leaves), 16-row boxes for runs of 16, else gathers of four
+// rows; the copy engine applies the 128-byte swizzle the MMAs read.
 // ---------------------------------------------------------------------------
-constexpr int kTcKeys = 64;
-constexpr int kTcStages = 4;
-constexpr int kTcRows = 256;
-constexpr int kTcHalf = kTcKeys * 128;                 // one d half of a K or V tile (8 KB)
-constexpr int kTcKV = 4 * kTcHalf;                     // K (2 halves) then V (2 halves)
-constexpr int kTcQ = 2 * 2 * 128 * 128;                // [row tile][d half][128 rows][128 B]
-constexpr int kTcSmem = kTcQ + kTcStages * kTcKV + 1024;
-constexpr uint32_t kTcCols = 512;
+constexpr int kTcRows = 256;                 // window rows per lane on this path (two row tiles)
+constexpr int kRowTile = 128;
+constexpr int kQBytes = 2 * kRowTile * 128;  // [d half][128 rows][128 B]
+constexpr int kP1Keys = 64;
+constexpr int kP1KSt = 5, kP1VSt = 5;        // K and V ring depths
+constexpr int kP1Bufs = 4;                   // S/P buffers in tensor memory
+constexpr int kP1Ahead = kP1Bufs - 1;        // tiles S runs ahead of P V
+constexpr int kP1Tile = kP1Keys * 256;       // one K or V tile (16 KB)
+constexpr int kP1Smem = kQBytes + (kP1KSt + kP1VSt) * kP1Tile + 1024;
+constexpr int kP1KProd = 8, kP1VProd = 9, kP1Issuer = 10;
+constexpr int kP1Depth = 4;                  // tiles of slots the producers read ahead
+constexpr int kP1Threads = 11 * 32;
+constexpr int kP2Keys = 128;
+constexpr int kP2St = 2;                     // K/V stages
+constexpr int kP2Tile = kP2Keys * 256;       // one K or V tile (32 KB)
+constexpr int kP2RowWarps = 16;             // 4 per lane quarter, 32 rows each
+constexpr int kP2Producer = 16, kP2Issuer = 17;
+constexpr int kP2Threads = 18 * 32;
+constexpr int kTileKeys = kP2Keys;           // chunks hold whole tiles of both passes
 constexpr float kTcRescale = 8.f;
-constexpr uint32_t kIdS = tc::idesc_bf16(128, kTcKeys, 0);
+constexpr uint32_t kIdS64 = tc::idesc_bf16(128, kP1Keys, 0);
 constexpr uint32_t kIdPV = tc::idesc_bf16(128, kD, 1);
-static_assert(kChunkMin % kTcKeys == 0, "chunks hold whole tiles");
+constexpr uint32_t kId128 = tc::idesc_bf16(128, 128, 0);
+static_assert(kChunkMin % kTileKeys == 0, "chunks hold whole tiles");
 
 // Hardware approximations (PTX ex2/rcp/sqrt .approx.ftz, relative error
 // about 2^-22; results below 2^-126 flush to zero).
@@ -609,50 +627,32 @@ __device__ __forceinline__ unsigned char* align1024(unsigned char* p) {
   const uint32_t a = smem_u32(p);
   return p + (((a + 1023u) & ~1023u) - a);
 }
-// byte offset of bf16 element e of key row k in a swizzled K or V tile
+// byte offset of bf16 element e of key row k in a swizzled tile of kKeys rows
+// ([d half][kKeys rows][128 B])
+template <int kKeys>
 __device__ __forceinline__ int sw_off(int k, int e) {
-  return (e >> 6) * kTcHalf + k * 128 + ((((e & 63) >> 3) ^ (k & 7)) << 4) + (e & 7) * 2;
+  return (e >> 6) * (kKeys * 128) + k * 128 + ((((e & 63) >> 3) ^ (k & 7)) << 4) + (e & 7) * 2;
 }
-
-// S[row tile mm] = Q K^T for stage st into tensor-memory column dS (thread 0)
-__device__ __forceinline__ void tc_issue_s(uint32_t dS, const unsigned char* sq, const unsigned char* kst, int mm) {
-#pragma unroll
-  for (int ks = 0; ks < 8; ++ks) {
-    const int half = ks >> 2, kin = ks & 3;
-    const uint64_t ad = tc::desc_sw128(smem_u32(sq + mm * 32768 + half * 16384) + kin * 32, 16, 1024);
-    const uint64_t bd = tc::desc_sw128(smem_u32(kst + half * kTcHalf) + kin * 32, 16, 1024);
-    tc::mma_ss(dS, ad, bd, kIdS, ks > 0 ? 1u : 0u);
-  }
-}
-
-// Warp roles of the tcgen05 passes: warps 0-7 own one window row per thread,
-// warp 8 produces (Q, then K/V tiles into the stage ring by TMA row gathers),
-// warp 9 lane 0 issues the MMAs.  Hand-offs are mbarriers only.
-constexpr int kWsRowThreads = 256;
-constexpr int kWsThreads = kWsRowThreads + 64;
-constexpr int kWsProducer = 8, kWsIssuer = 9;
-constexpr int kPrefetch = 4;   // tiles of key slots / positions the producer has in flight
-
-__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+// Orders this thread's generic-proxy shared-memory writes before later
+// async-proxy reads of them (the tensor cores reading an operand).
+__device__ __forceinline__ void fence_proxy_async() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void named_sync(int id, int threads) {
+  asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
 __device__ __forceinline__ void cp_async16_zf(void* dst, const void* src, bool ok) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(smem_u32(dst)), "l"(src), "r"(ok ? 16 : 0)
                : "memory");
 }
-// one arrival on the barrier once this thread's earlier cp.async copies land
-__device__ __forceinline__ void cp_async_arrive(uint64_t* bar) {
-  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+__device__ __forceinline__ void cp_async4i(int* dst, const int* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void named_arrive(int id, int threads) {
+  asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive1(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
-struct WsBars {
-  uint64_t qfull;
-  uint64_t full[kTcStages], empty[kTcStages];
-  uint64_t x_full[2], x_free[2], pv_done[2];
-};
 
 // The K and V pool tensor maps of one layer (see kTmapsPerLayer).
 struct D3Maps {
@@ -684,363 +684,318 @@ __device__ __forceinline__ void tma_gather4(void* dst, const CUtensorMap* map, i
       : "memory");
 }
 
-// Producer warp.  Q rows first (8 per lane, 16-byte cp.async, once); then per
-// tile the K and V rows of its 64 keys by TMA, after the keys' positions
-// (and in pass 2 their |v|^2), loaded one tile ahead, are stored to the
-// stage and lane 0 has armed the stage's full barrier with the tile's bytes.
-// A tile whose 64 slots are consecutive (the layout a prefill leaves) takes
-// one 64-row copy per tensor and row half; otherwise each group of 16 keys
-// in consecutive slots takes a 16-row copy, and the other keys are gathered
-// four rows per copy (lanes 0-15, four keys each; a key past the chunk
-// gathers a row past the pool, which reads as zeros).  A TMA instruction
-// costs tens of nanoseconds to issue, so the fewer the better.
-// In pass 2 it also retires each tile's column sums: once the tile's stage
-// is empty (its MMAs and the 8 row warps are done with it), the 8 warps'
-// partial sums are added in warp order and stored.
-template <bool kPass2, bool kLoadV = true>
-__device__ __forceinline__ void ws_produce(const D3Args& A, const D3Maps& mp, int l,
-                                           int j_begin, int j_end, int ntiles, unsigned char* sq, unsigned char* skv,
-                                           int (*pos)[kTcKeys], float (*vn)[kTcKeys],
-                                           float (*col)[kWsRowThreads / 32][kTcKeys], WsBars& bar) {
+// One producer warp streaming the chunk's tiles of kKeys keys into a ring of
+// kStages stages.  A stage holds the K tile (kK) and then the V tile (kV),
+// each [d half][kKeys rows][128 B]; with kPos the keys' positions go to
+// pos[stage][key] for the row warps.  Per tile: wait until the stage is
+// empty, store the positions, arm the stage's full barrier with the bytes to
+// come, issue the copies.  The keys' slots (and positions) are read ahead, so
+// the producer does not wait a global round trip per tile: kDepth > 0 tiles
+// ahead by 4-byte cp.async into pf_s / pf_p ([kDepth][kKeys], one commit
+// group per tile; each lane copies and reads back only its own keys), or,
+// with kDepth 0, one tile ahead into registers (enough when the producer
+// mostly waits for empty stages).  A key past the chunk reads a pool row past
+// the end: zeros.  A tile whose keys sit
+// in consecutive slots takes one 64-row copy per 64 keys, tensor and d half;
+// otherwise each 16-key group in consecutive slots takes a 16-row copy and
+// the rest are gathered four rows per copy (a TMA instruction costs tens of
+// nanoseconds to issue, so the fewer the better).
+template <int kKeys, int kStages, bool kK, bool kV, bool kPos, int kDepth>
+__device__ __forceinline__ void d3_produce(const D3Args& A, const D3Maps& mp, int l, int j_begin, int j_end,
+                                           int ntiles, unsigned char* ring, uint64_t* full, uint64_t* empty,
+                                           int* pos, int* pf_s, int* pf_p) {
+  constexpr int kpl = kKeys / 32;   // keys per lane
+  constexpr int kHalfB = kKeys * 128;
+  constexpr int kTileB = 2 * kHalfB;
+  constexpr uint32_t kStageB = (kK ? kTileB : 0) + (kV ? kTileB : 0);
+  constexpr int kGl = kKeys / 4;    // gather lanes: lane L < kGl takes keys 4L .. 4L + 3
   const int lane = threadIdx.x & 31;
-  const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
-#pragma unroll 1
-  for (int q = 0; q < 8; ++q) {
-    const int r = lane * 8 + q, rr = r & 127;
-    unsigned char* row = sq + (r >> 7) * 32768 + rr * 128;
-    const bool ok = r < A.rows;
-    const int h = ok ? r / A.w : 0, i = ok ? r % A.w : 0;
-    const __nv_bfloat16* src = A.q + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i) * kD;
-#pragma unroll
-    for (int c = 0; c < 16; ++c)
-      cp_async16_zf(row + (c >> 3) * 16384 + (((c & 7) ^ (rr & 7)) << 4), ok ? src + c * 8 : A.q, ok);
-  }
-  cp_async_arrive(&bar.qfull);
   const size_t lo = static_cast<size_t>(l) * A.dm.cap;
   const int rows_max = A.dm.P * kBlock;
-  // The keys' slots, positions (and |v|^2) reach shared memory by 4-byte
-  // cp.async kPrefetch tiles ahead, one commit group per tile, so the
-  // producer does not wait a global round trip per tile before it can
-  // issue the tile's copies.  Each lane copies and later reads only its own
-  // two keys of a tile.
-  __shared__ int pf_slot[kPrefetch][kTcKeys], pf_pos[kPrefetch][kTcKeys];
-  __shared__ float pf_vn[kPrefetch][kTcKeys];
+  int sl[kpl], ps[kpl];
+  auto read = [&](int t, int (&s)[kpl], int (&p)[kpl]) {
+#pragma unroll
+    for (int i = 0; i < kpl; ++i) {
+      const int j = j_begin + t * kKeys + kpl * lane + i;
+      const bool ok = t < ntiles && j < j_end;
+      s[i] = ok ? A.ls.slot[lo + j] : rows_max;
+      p[i] = (kPos && ok) ? A.ls.pos[lo + j] : 0x7FFFFFFF;
+    }
+  };
   auto prefetch = [&](int t) {
     if (t < ntiles) {
-      const int b = t % kPrefetch;
+      const int bb = t % (kDepth > 0 ? kDepth : 1);
 #pragma unroll
-      for (int kk = 0; kk < 2; ++kk) {
-        const int key = 2 * lane + kk, j = j_begin + t * kTcKeys + key;
+      for (int i = 0; i < kpl; ++i) {
+        const int key = kpl * lane + i, j = j_begin + t * kKeys + key;
         if (j < j_end) {
-          cp_async4(&pf_slot[b][key], A.ls.slot + lo + j);
-          cp_async4(&pf_pos[b][key], A.ls.pos + lo + j);
-          if (kPass2 && kLoadV) cp_async4(&pf_vn[b][key], A.ws.d3_vn + lo + j);
+          cp_async4i(pf_s + bb * kKeys + key, A.ls.slot + lo + j);
+          if (kPos) cp_async4i(pf_p + bb * kKeys + key, A.ls.pos + lo + j);
         }
       }
     }
     cp_commit();
   };
-  auto fetch = [&](int t, int key, int& sl, int& ps, float& v) {
-    const int j = j_begin + t * kTcKeys + key;
-    sl = rows_max;
-    ps = 0x7FFFFFFF;
-    v = 0.f;
-    if (t >= ntiles || j >= j_end) return;
-    const int b = t % kPrefetch;
-    int s = pf_slot[b][key];
-    if (s < 0 || s >= rows_max) { set_status(A.ws.status, ST_BAD_INDEX); s = 0; }
-    sl = s;
-    ps = pf_pos[b][key];
-    if (kPass2 && kLoadV) v = pf_vn[b][key];
-  };
-  auto retire = [&](int u) {
-    const int su = u % kTcStages;
+  if (kDepth > 0) {
 #pragma unroll
-    for (int kk = 0; kk < 2; ++kk) {
-      const int key = 2 * lane + kk;
-      float tot = 0.f;
-#pragma unroll
-      for (int w8 = 0; w8 < kWsRowThreads / 32; ++w8) tot += col[su][w8][key];
-      const int j = j_begin + u * kTcKeys + key;
-      if (j < j_end) A.col_out[lo + j] = tot;
-    }
-  };
-  int s0, s1, p0, p1;
-  float v0, v1;
-#pragma unroll
-  for (int u = 0; u < kPrefetch; ++u) prefetch(u);
+    for (int u = 0; u < kDepth; ++u) prefetch(u);
+  } else {
+    read(0, sl, ps);
+  }
 #pragma unroll 1
   for (int t = 0; t < ntiles; ++t) {
-    const int st = t % kTcStages;
-    cp_wait<kPrefetch - 1>();   // tile t's group has landed
-    fetch(t, 2 * lane, s0, p0, v0);
-    fetch(t, 2 * lane + 1, s1, p1, v1);
-    if (t >= kTcStages) {
-      (void)mbar_wait_bounded(&bar.empty[st], ((t / kTcStages) - 1) & 1, A.ws.status);
-      if (kPass2) retire(t - kTcStages);
-    }
-    pos[st][2 * lane] = p0;
-    pos[st][2 * lane + 1] = p1;
-    if (kPass2 && kLoadV) {
-      vn[st][2 * lane] = v0;
-      vn[st][2 * lane + 1] = v1;
-    }
-    // lane g < 16 takes keys 4g .. 4g + 3, held by lanes 2g and 2g + 1
-    const int g0 = __shfl_sync(0xffffffffu, s0, (2 * lane) & 31);
-    const int g1 = __shfl_sync(0xffffffffu, s1, (2 * lane) & 31);
-    const int g2 = __shfl_sync(0xffffffffu, s0, (2 * lane + 1) & 31);
-    const int g3 = __shfl_sync(0xffffffffu, s1, (2 * lane + 1) & 31);
-    // consecutive slots: the whole tile (lane 0's key 0 first), and each
-    // 16-key group q (keys 16q.., held by lanes 8q .. 8q + 7)
-    const int tbase = __shfl_sync(0xffffffffu, s0, 0);
-    const bool tile_run = __all_sync(0xffffffffu, s0 == tbase + 2 * lane && s1 == tbase + 2 * lane + 1) &&
-                          tbase + kTcKeys <= rows_max;
-    const int qbase = __shfl_sync(0xffffffffu, s0, lane & ~7);
-    const unsigned qrun = __ballot_sync(0xffffffffu, s0 == qbase + 2 * (lane & 7) && s1 == qbase + 2 * (lane & 7) + 1);
-    const int grp = (lane >> 2) & 3;                                  // the group of lane g < 16
-    const int gbase = __shfl_sync(0xffffffffu, qbase, 8 * grp);
-    const bool grp_run = ((qrun >> (8 * grp)) & 0xFFu) == 0xFFu && gbase + 16 <= rows_max;
-    __syncwarp();
-    if (lane == 0) mbar_arrive_expect_tx(&bar.full[st], static_cast<uint32_t>(kLoadV ? kTcKV : 2 * kTcHalf));
-    __syncwarp();
-    unsigned char* kst = skv + st * kTcKV;
-    unsigned char* vst = kst + 2 * kTcHalf;
-    if (tile_run) {
-      if (lane == 0) {
+    int sn[kpl], pn[kpl];
+    if (kDepth > 0) {
+      cp_wait<(kDepth > 0 ? kDepth - 1 : 0)>();   // tile t's group has landed
+      const int bb = t % (kDepth > 0 ? kDepth : 1);
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          tma_rows(kst + hf * kTcHalf, &mp.m[4], hf * 64, tbase, &bar.full[st]);
-          if (kLoadV) tma_rows(vst + hf * kTcHalf, &mp.m[5], hf * 64, tbase, &bar.full[st]);
-        }
+      for (int i = 0; i < kpl; ++i) {
+        const int key = kpl * lane + i, j = j_begin + t * kKeys + key;
+        sl[i] = j < j_end ? pf_s[bb * kKeys + key] : rows_max;
+        ps[i] = (kPos && j < j_end) ? pf_p[bb * kKeys + key] : 0x7FFFFFFF;
       }
-    } else if (lane < kTcKeys / 4) {
-      if (grp_run) {
-        if ((lane & 3) == 0) {
+      prefetch(t + kDepth);   // into the buffer just read (its values are in registers)
+    } else {
+      read(t + 1, sn, pn);
+    }
+    const int st = t % kStages;
+    if (t >= kStages) (void)mbar_wait_bounded(&empty[st], ((t / kStages) - 1) & 1, A.ws.status);
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            tma_rows(kst + hf * kTcHalf + grp * 2048, &mp.m[2], hf * 64, gbase, &bar.full[st]);
-            if (kLoadV) tma_rows(vst + hf * kTcHalf + grp * 2048, &mp.m[3], hf * 64, gbase, &bar.full[st]);
+    for (int i = 0; i < kpl; ++i) {
+      const int j = j_begin + t * kKeys + kpl * lane + i;
+      if (j < j_end && (sl[i] < 0 || sl[i] >= rows_max)) {
+        set_status(A.ws.status, ST_BAD_INDEX);
+        sl[i] = 0;
+      }
+      if (kPos) pos[st * kKeys + kpl * lane + i] = ps[i];
+    }
+    if (kK || kV) {
+      // consecutive slots: the whole tile, and each 16-key group
+      const int tbase = __shfl_sync(0xffffffffu, sl[0], 0);
+      const int g16 = (kpl * lane) >> 4;   // this lane's 16-key group
+      const int gfirst = __shfl_sync(0xffffffffu, sl[0], (16 * g16) / kpl);
+      bool run_t = true, run_g = true;
+#pragma unroll
+      for (int i = 0; i < kpl; ++i) {
+        run_t = run_t && sl[i] == tbase + kpl * lane + i;
+        run_g = run_g && sl[i] == gfirst + kpl * lane + i - 16 * g16;
+      }
+      const bool tile_run = __all_sync(0xffffffffu, run_t) && tbase + kKeys <= rows_max;
+      const unsigned runs = __ballot_sync(0xffffffffu, run_g);
+      const int gl = lane % kGl;             // lanes past kGl compute harmless copies of lane gl's values
+      const int ggrp = gl >> 2;              // the gather lane's 16-key group
+      const unsigned gmask = ((1u << (16 / kpl)) - 1u) << ((16 * ggrp) / kpl);
+      const int gbase = __shfl_sync(0xffffffffu, sl[0], (16 * ggrp) / kpl);
+      const bool grp_run = (runs & gmask) == gmask && gbase + 16 <= rows_max;
+      int g4[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) g4[i] = __shfl_sync(0xffffffffu, sl[i % kpl], (4 * gl + i) / kpl);
+      __syncwarp();
+      if (lane == 0) mbar_arrive_expect_tx(&full[st], kStageB);
+      __syncwarp();
+      unsigned char* stage = ring + static_cast<size_t>(st) * kStageB;
+#pragma unroll
+      for (int ten = 0; ten < 2; ++ten) {
+        if ((ten == 0 && !kK) || (ten == 1 && !kV)) continue;
+        unsigned char* dst = stage + ((ten == 1 && kK) ? kTileB : 0);
+        const int mg = ten, m16 = 2 + ten, m64 = 4 + ten;
+        if (tile_run) {
+          if (lane == 0) {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+#pragma unroll
+              for (int c = 0; c < kKeys / 64; ++c)
+                tma_rows(dst + hf * kHalfB + c * 8192, &mp.m[m64], hf * 64, tbase + 64 * c, &full[st]);
+          }
+        } else if (lane < kGl) {
+          if (grp_run) {
+            if ((lane & 3) == 0) {
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf)
+                tma_rows(dst + hf * kHalfB + ggrp * 2048, &mp.m[m16], hf * 64, gbase, &full[st]);
+            }
+          } else {
+#pragma unroll
+            for (int hf = 0; hf < 2; ++hf)
+              tma_gather4(dst + hf * kHalfB + lane * 512, &mp.m[mg], hf * 64, g4[0], g4[1], g4[2], g4[3],
+                          &full[st]);
           }
         }
-      } else {
+      }
+    } else {
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&full[st]);   // positions only
+    }
+    if (kDepth == 0) {
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          tma_gather4(kst + hf * kTcHalf + lane * 512, &mp.m[0], hf * 64, g0, g1, g2, g3, &bar.full[st]);
-          if (kLoadV) tma_gather4(vst + hf * kTcHalf + lane * 512, &mp.m[1], hf * 64, g0, g1, g2, g3, &bar.full[st]);
-        }
+      for (int i = 0; i < kpl; ++i) {
+        sl[i] = sn[i];
+        ps[i] = pn[i];
       }
     }
-    prefetch(t + kPrefetch);   // into the buffer tile t was read from (its values are in registers)
   }
-  if (kPass2) {
-#pragma unroll 1
-    for (int u = ntiles > kTcStages ? ntiles - kTcStages : 0; u < ntiles; ++u) {
-      (void)mbar_wait_bounded(&bar.empty[u % kTcStages], (u / kTcStages) & 1, A.ws.status);
-      retire(u);
+}
+
+// The CTA's 128 window rows of Q (which = 0) or of a hi / a lo (1 / 2) into
+// shared memory at dst in the UMMA 128-byte K-major layout, by 16-byte
+// cp.async pieces (zeros past the rows), split over `threads` threads.
+__device__ __forceinline__ void stage_rows(unsigned char* dst, int which, const D3Args& A, int l, int rt, int tid,
+                                           int threads) {
+  const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
+  for (int e = tid; e < kRowTile * 16; e += threads) {
+    const int rr = e >> 4, c = e & 15, r = rt * kRowTile + rr;
+    const bool ok = r < A.rows;
+    const __nv_bfloat16* src = A.q;
+    if (ok) {
+      if (which == 0)
+        src = A.q + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + r / A.w) * A.w + r % A.w) * kD + c * 8;
+      else
+        src = (which == 1 ? A.ws.d3_ahi : A.ws.d3_alo) + (static_cast<size_t>(l) * A.rows_cap + r) * kD + c * 8;
     }
+    cp_async16_zf(dst + (c >> 3) * 16384 + rr * 128 + (((c & 7) ^ (rr & 7)) << 4), src, ok);
   }
 }
 
-__device__ __forceinline__ void ws_init_bars(WsBars& bar, uint32_t full_count, uint32_t empty_count,
-                                             uint32_t free_count) {
-  mbar_init(&bar.qfull, 32);
-  for (int s = 0; s < kTcStages; ++s) {
-    mbar_init(&bar.full[s], full_count);
-    mbar_init(&bar.empty[s], empty_count);
-  }
-  for (int b = 0; b < 2; ++b) {
-    mbar_init(&bar.x_full[b], 1);
-    mbar_init(&bar.x_free[b], free_count);
-    mbar_init(&bar.pv_done[b], 1);
-  }
-  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
+struct P1Bars {
+  uint64_t qfull;
+  uint64_t kfull[kP1KSt], kempty[kP1KSt];
+  uint64_t vfull[kP1VSt], vempty[kP1VSt];
+  uint64_t x_full[kP1Bufs], x_free[kP1Bufs], pv_done[kP1Bufs];
+};
 
-// pass 1.  Issue order S(0), then per tile S(t+1), P V(t): the tensor core
-// computes the next scores while the row warps exponentiate.  x_full[b]:
-// S(t) done (b = t & 1); x_free[b]: P(t) written by the 8 row warps;
-// pv_done[b]: P V(t) done; empty[s]: P V and the 8 row warps (which also
-// take |v|^2 of the tile's keys for pass 2) are done with the stage.
-// Without V (kWithV false: the attention-mass scores need only the LSE) the
-// stages hold K alone, no P V is issued and the rows keep only (max, sum).
+// pass 1.  Barriers: x_full[b] S(t) done; x_free[b] the four row warps of
+// tile t's group have read S (and written P); pv_done[b] P V(t) done;
+// kfull / kempty and vfull / vempty the two rings (a V stage also carries
+// the keys' positions).  Issue order: S(0 .. 2), then per tile P V(t),
+// S(t + 3): S(t + 3) reuses the buffer of P(t - 1), which P V(t - 1) read
+// before it in the tensor core's order.
 template <bool kWithV>
-__global__ void __launch_bounds__(kWsThreads, 1)
-    d3_tc_pass1_kernel(D3Args A, const __grid_constant__ D3Maps mp) {
+__global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __grid_constant__ D3Maps mp) {
   extern __shared__ unsigned char d3_dsm[];
-  __shared__ int sh_pos[kTcStages][kTcKeys];
-  __shared__ float sh_ml[128][2];
-  __shared__ __align__(8) WsBars bar;
+  __shared__ __align__(8) P1Bars bar;
+  __shared__ int sh_pos[kP1VSt * kP1Keys];
+  __shared__ float sh_ml[2][kRowTile][2];
+  __shared__ int pf_k[kP1Depth * kP1Keys], pf_v[kP1Depth * kP1Keys], pf_p[kP1Depth * kP1Keys];
   __shared__ uint32_t sh_taddr;
-  const int chunk = blockIdx.x, l = blockIdx.y;
+  const int nrt = (A.rows + kRowTile - 1) / kRowTile;
+  const int rt = blockIdx.x % nrt, chunk = blockIdx.x / nrt, l = blockIdx.y;
   const int n = min(max(A.ls.count[l], 0), A.dm.cap);
   const int j_begin = chunk * A.chunk_keys;
   if (j_begin >= n) return;
   const int j_end = min(n, j_begin + A.chunk_keys);
-  const int ntiles = (j_end - j_begin + kTcKeys - 1) / kTcKeys;
+  const int ntiles = (j_end - j_begin + kP1Keys - 1) / kP1Keys;
   unsigned char* sq = align1024(d3_dsm);
-  unsigned char* skv = sq + kTcQ;
-  const int tid = threadIdx.x, warp = tid >> 5;
-  if (warp == kWsIssuer) tc::alloc(&sh_taddr, kTcCols);
-  if (tid == 0) ws_init_bars(bar, 1, 1 + kWsRowThreads / 32, kWsRowThreads / 32);
+  unsigned char* skr = sq + kQBytes;
+  unsigned char* svr = skr + kP1KSt * kP1Tile;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (warp == kP1Issuer) tc::alloc(&sh_taddr, 512);
+  if (tid == 0) {
+    mbar_init(&bar.qfull, 8);
+    for (int s = 0; s < kP1KSt; ++s) {
+      mbar_init(&bar.kfull[s], 1);
+      mbar_init(&bar.kempty[s], 1);
+    }
+    for (int s = 0; s < kP1VSt; ++s) {
+      mbar_init(&bar.vfull[s], 1);
+      mbar_init(&bar.vempty[s], kWithV ? 5 : 4);
+    }
+    for (int b = 0; b < kP1Bufs; ++b) {
+      mbar_init(&bar.x_full[b], 1);
+      mbar_init(&bar.x_free[b], 4);
+      mbar_init(&bar.pv_done[b], 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
   const uint32_t tl = sh_taddr;
-  // at most 128 rows without V: one row tile; warps w and w + 4 share its
-  // rows, each taking 32 keys of every tile
-  const bool split = !kWithV && A.rows <= 128;
+  const size_t lo = static_cast<size_t>(l) * A.dm.cap;
 
-  if (warp == kWsProducer) {
-    ws_produce<false, kWithV>(A, mp, l, j_begin, j_end, ntiles, sq, skv, sh_pos, nullptr, nullptr, bar);
-  } else if (warp == kWsIssuer) {
-    if ((tid & 31) == 0) {
+  if (warp == kP1KProd) {
+    d3_produce<kP1Keys, kP1KSt, true, false, false, kP1Depth>(A, mp, l, j_begin, j_end, ntiles, skr, bar.kfull,
+                                                              bar.kempty, nullptr, pf_k, nullptr);
+  } else if (warp == kP1VProd) {
+    d3_produce<kP1Keys, kP1VSt, false, kWithV, true, kP1Depth>(A, mp, l, j_begin, j_end, ntiles, svr, bar.vfull,
+                                                               bar.vempty, sh_pos, pf_v, pf_p);
+  } else if (warp == kP1Issuer) {
+    if (lane == 0) {
+      // descriptors built once; each MMA advances one by a constant
+      const uint64_t dq = tc::desc_sw128(smem_u32(sq), 16, 1024);
+      const uint64_t dk0 = tc::desc_sw128(smem_u32(skr), 16, 1024);
+      const uint64_t dv0 = tc::desc_sw128(smem_u32(svr), kP1Keys * 128, 1024);
       (void)mbar_wait_bounded(&bar.qfull, 0, A.ws.status);
-      auto issue_s = [&](int t) {
-        const int st = t % kTcStages, buf = t & 1;
-        (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);
+      auto issue_s = [&](int u) {
+        const int ks = u % kP1KSt;
+        // without P V, the rows' reading of S(u - 4) is what frees its buffer
+        // (with it, P V(u - 4) read that buffer before S(u) in issue order)
+        if (!kWithV && u >= kP1Bufs)
+          (void)mbar_wait_bounded(&bar.x_free[u % kP1Bufs], ((u / kP1Bufs) - 1) & 1, A.ws.status);
+        (void)mbar_wait_bounded(&bar.kfull[ks], (u / kP1KSt) & 1, A.ws.status);
         tc::fence_after();
-        const unsigned char* kst = skv + st * kTcKV;
-        tc_issue_s(tl + 256 + buf * 128, sq, kst, 0);
-        if (!split) tc_issue_s(tl + 256 + buf * 128 + 64, sq, kst, 1);
-        tc::commit(&bar.x_full[buf]);
+        const uint64_t dk = tc::desc_add(dk0, ks * kP1Tile);
+        const uint32_t dS = tl + 256 + (u % kP1Bufs) * 64;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const int half = kk >> 2, kin = kk & 3;
+          tc::mma_ss(dS, tc::desc_add(dq, half * 16384 + kin * 32),
+                     tc::desc_add(dk, half * (kP1Keys * 128) + kin * 32), kIdS64, kk > 0 ? 1u : 0u);
+        }
+        tc::commit(&bar.x_full[u % kP1Bufs]);
+        tc::commit(&bar.kempty[ks]);
       };
-      issue_s(0);
+      for (int u = 0; u < min(kP1Ahead, ntiles); ++u) issue_s(u);
 #pragma unroll 1
       for (int t = 0; t < ntiles; ++t) {
-        if (t + 1 < ntiles) issue_s(t + 1);
-        const int st = t % kTcStages, buf = t & 1;
-        (void)mbar_wait_bounded(&bar.x_free[buf], (t >> 1) & 1, A.ws.status);
-        tc::fence_after();
-        const uint32_t vbase = smem_u32(skv + st * kTcKV + 2 * kTcHalf);
-#pragma unroll
-        for (int mm = 0; mm < (kWithV ? 2 : 0); ++mm) {
-          const uint32_t aP = tl + 256 + buf * 128 + mm * 64;
+        const int b = t % kP1Bufs;
+        if (kWithV) {
+          const int vs = t % kP1VSt;
+          (void)mbar_wait_bounded(&bar.x_free[b], (t / kP1Bufs) & 1, A.ws.status);
+          (void)mbar_wait_bounded(&bar.vfull[vs], (t / kP1VSt) & 1, A.ws.status);
+          tc::fence_after();
+          const uint64_t dv = tc::desc_add(dv0, vs * kP1Tile);
+          const uint32_t aP = tl + 256 + b * 64, dO = tl + (t & 1) * 128;
+          const uint32_t acc0 = t >= 2 ? 1u : 0u;
 #pragma unroll
           for (int ks = 0; ks < 4; ++ks) {
-            const uint64_t bd = tc::desc_sw128(vbase + ks * 2048, kTcHalf, 1024);
-            tc::mma_ts(tl + mm * 128, aP + ks * 8, bd, kIdPV, (t > 0 || ks > 0) ? 1u : 0u);
-            tc::mma_ts(tl + mm * 128, aP + 32 + ks * 8, bd, kIdPV, 1u);
+            const uint64_t bd = tc::desc_add(dv, ks * 2048);
+            tc::mma_ts(dO, aP + ks * 8, bd, kIdPV, ks > 0 ? 1u : acc0);
+            tc::mma_ts(dO, aP + 32 + ks * 8, bd, kIdPV, 1u);
           }
+          tc::commit(&bar.pv_done[b]);
+          tc::commit(&bar.vempty[vs]);
         }
-        tc::commit(&bar.empty[st]);
-        tc::commit(&bar.pv_done[buf]);
+        if (t + kP1Ahead < ntiles) issue_s(t + kP1Ahead);
       }
-    }
-  } else if (!kWithV) {
-    // row warps without V: each row's running (max, sum); split: rows
-    // tid & 127, keys [32 h0, 32 h0 + 32) of each tile with h0 = warp / 4
-    const int r = split ? (tid & 127) : tid, m = r >> 7, h0 = split ? (warp >> 2) : 0;
-    const bool row_ok = r < A.rows;
-    const int qp = row_ok ? A.qpos[r % A.w] : -1;
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int nkeys = j_end - j_begin;
-    float m_run = -INFINITY, l_run = 0.f;
-#pragma unroll 1
-    for (int t = 0; t < ntiles; ++t) {
-      const int st = t % kTcStages, buf = t & 1;
-      (void)mbar_wait_bounded(&bar.x_full[buf], (t >> 1) & 1, A.ws.status);
-      (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);   // key positions
-      tc::fence_after();
-      const uint32_t aS = tl + lane_off + 256 + buf * 128 + m * 64;
-      float s[kTcKeys];
-      {
-        uint32_t v[4][16];
-        tc::ld16(aS + h0 * 32, v[0]);
-        tc::ld16(aS + h0 * 32 + 16, v[1]);
-        if (!split) {
-          tc::ld16(aS + 32, v[2]);
-          tc::ld16(aS + 48, v[3]);
-        }
-        tc::wait_ld();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-          for (int k = 0; k < 16; ++k) s[q4 * 16 + k] = __uint_as_float(v[q4][k]);
-      }
-      // the keys at or before the row: a prefix of the tile (positions ascend)
-      int vis = 0;
-      if (row_ok) {
-        const int lim = min(kTcKeys, nkeys - t * kTcKeys);
-        if (lim > 0 && sh_pos[st][lim - 1] <= qp) {
-          vis = lim;
-        } else {
-          int lo = 0, hi = lim;
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (sh_pos[st][mid] <= qp) lo = mid + 1; else hi = mid;
-          }
-          vis = lo;
-        }
-      }
-      // S read, positions read: the buffer and the stage are free
-      tc::fence_before();
-      __syncwarp();
-      if ((tid & 31) == 0) {
-        mbar_arrive1(&bar.x_free[buf]);
-        mbar_arrive1(&bar.empty[st]);
-      }
-#pragma unroll 1
-      for (int hh = 0; hh < (split ? 1 : 2); ++hh) {
-        const int kv = vis - (h0 + hh) * 32;
-        float tmax = -INFINITY;
-#pragma unroll
-        for (int k = 0; k < 32; ++k) {
-          s[k] = k < kv ? s[k] : -INFINITY;
-          tmax = fmaxf(tmax, s[k]);
-        }
-        tmax *= A.scale2;
-        if (tmax > m_run + kTcRescale) {
-          l_run *= (m_run == -INFINITY) ? 0.f : exp2f(m_run - tmax);
-          m_run = tmax;
-        }
-        const float negm = m_run == -INFINITY ? 0.f : -m_run;
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k = 0; k < 32; ++k) ps[k & 3] += hw_exp2(fmaf(s[k], A.scale2, negm));
-        l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-#pragma unroll
-        for (int k = 0; k < 32; ++k) s[k] = s[32 + k];
-      }
-    }
-    const size_t stride = kD + 2;
-    if (split) {
-      // merge the two key halves of each row (named barrier of the row warps)
-      if (h0 == 1) {
-        sh_ml[r][0] = m_run;
-        sh_ml[r][1] = l_run;
-      }
-      asm volatile("bar.sync 1, 256;" ::: "memory");
-      if (h0 == 0) {
-        const float m1 = sh_ml[r][0], l1 = sh_ml[r][1];
-        const float M = fmaxf(m_run, m1);
-        if (M != -INFINITY) {
-          l_run = l_run * exp2f(m_run - M) + l1 * exp2f(m1 - M);
-          m_run = M;
-        }
-      }
-    }
-    float* part = A.ws.d3_part + (static_cast<size_t>(l) * A.chunks + chunk) * static_cast<size_t>(A.rows_cap) * stride +
-                  static_cast<size_t>(r) * stride;
-    if (row_ok && h0 == 0) {
-      part[kD] = m_run;
-      part[kD + 1] = l_run;
     }
   } else {
-    // row warps: one window row per thread
-    const int r = tid, m = r >> 7;
+    // row warps: group grp = warp / 4 takes tiles t = grp, grp + 2, ...; one row per thread
+    const int grp = warp >> 2, qd = warp & 3;
+    const int rr = qd * 32 + lane, r = rt * kRowTile + rr;
     const bool row_ok = r < A.rows;
     const int qp = row_ok ? A.qpos[r % A.w] : -1;
-    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const int nkeys = j_end - j_begin;
+    stage_rows(sq, 0, A, l, rt, tid, 256);
+    cp_commit();
+    cp_wait<0>();
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive1(&bar.qfull);
+    // pass 2 adds both row tiles' sums into the output: zero it first
+    if (nrt > 1 && rt == 0)
+      for (int j = j_begin + tid; j < j_end; j += 256) A.col_out[lo + j] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
+    const int gt = tid & 127;   // thread within the group
 #pragma unroll 1
-    for (int t = 0; t < ntiles; ++t) {
-      const int st = t % kTcStages, buf = t & 1;
-      (void)mbar_wait_bounded(&bar.x_full[buf], (t >> 1) & 1, A.ws.status);
-      (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);   // key positions
+    for (int t = grp; t < ntiles; t += 2) {
+      const int b = t % kP1Bufs, vs = t % kP1VSt;
+      (void)mbar_wait_bounded(&bar.x_full[b], (t / kP1Bufs) & 1, A.ws.status);
+      (void)mbar_wait_bounded(&bar.vfull[vs], (t / kP1VSt) & 1, A.ws.status);   // positions (and V)
       tc::fence_after();
-      const uint32_t aS = tl + lane_off + 256 + buf * 128 + m * 64;
-      float s[kTcKeys];
+      const int* tpos = sh_pos + vs * kP1Keys;
+      const uint32_t aS = tl + lane_off + 256 + b * 64;
+      float s[kP1Keys];
       {
         uint32_t v[4][16];
 #pragma unroll
@@ -1052,33 +1007,48 @@ __global__ void __launch_bounds__(kWsThreads, 1)
           for (int k = 0; k < 16; ++k) s[q4 * 16 + k] = __uint_as_float(v[q4][k]);
       }
       // a full tile whose last (largest) position precedes the row is wholly visible
-      const bool all_vis = row_ok && (t + 1) * kTcKeys <= nkeys && sh_pos[st][kTcKeys - 1] <= qp;
-      // the largest raw score of the tile (scale2 > 0 keeps the order; the
-      // scale is applied once, and inside the exponent's FMA below)
-      float tmax = -INFINITY;
+      const bool all_vis = row_ok && (t + 1) * kP1Keys <= nkeys && tpos[kP1Keys - 1] <= qp;
+      // the largest raw score (scale2 > 0 keeps the order; the scale is
+      // applied once, and inside the exponent's FMA below); four partial maxima
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
       if (all_vis) {
 #pragma unroll
-        for (int k = 0; k < kTcKeys; ++k) tmax = fmaxf(tmax, s[k]);
+        for (int k = 0; k < kP1Keys; ++k) mx[k & 3] = fmaxf(mx[k & 3], s[k]);
       } else {
 #pragma unroll
-        for (int k = 0; k < kTcKeys; ++k) {
-          const bool ok = row_ok && t * kTcKeys + k < nkeys && sh_pos[st][k] <= qp;
+        for (int k = 0; k < kP1Keys; ++k) {
+          const bool ok = row_ok && t * kP1Keys + k < nkeys && tpos[k] <= qp;
           s[k] = ok ? s[k] : -INFINITY;
-          tmax = fmaxf(tmax, s[k]);
+          mx[k & 3] = fmaxf(mx[k & 3], s[k]);
         }
       }
-      tmax *= A.scale2;
+      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * A.scale2;
       float factor = 1.f;
       if (tmax > m_run + kTcRescale) {
         factor = (m_run == -INFINITY) ? 0.f : exp2f(m_run - tmax);
         m_run = tmax;
         l_run *= factor;
       }
-      if (kWithV && t > 0 && __any_sync(0xffffffffu, factor != 1.f)) {
-        // P V(t - 1) must be complete before O is rescaled
-        (void)mbar_wait_bounded(&bar.pv_done[(t - 1) & 1], ((t - 1) >> 1) & 1, A.ws.status);
+      if (!kWithV) {
+        // S and the positions are read: release the buffer and the stage
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive1(&bar.x_free[b]);
+          mbar_arrive1(&bar.vempty[vs]);
+        }
+        const float negm = m_run == -INFINITY ? 0.f : -m_run;
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < kP1Keys; ++k) ps[k & 3] += hw_exp2(fmaf(s[k], A.scale2, negm));
+        l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        continue;
+      }
+      if (t >= 2 && __any_sync(0xffffffffu, factor != 1.f)) {
+        // P V of the group's previous tile must be complete before O_g is rescaled
+        (void)mbar_wait_bounded(&bar.pv_done[(t - 2) % kP1Bufs], ((t - 2) / kP1Bufs) & 1, A.ws.status);
         tc::fence_after();
-        const uint32_t aO = tl + lane_off + m * 128;
+        const uint32_t aO = tl + lane_off + grp * 128;
 #pragma unroll 1
         for (int q8 = 0; q8 < 8; ++q8) {
           uint32_t v[16];
@@ -1092,16 +1062,16 @@ __global__ void __launch_bounds__(kWsThreads, 1)
       // p = 2^(s scale2 - m); a masked key (s = -inf) gives 0, and so does
       // every key while the row has seen none (m = -inf, offset taken as 0)
       const float negm = m_run == -INFINITY ? 0.f : -m_run;
-      float psum = 0.f;
-      uint32_t hi[32], lo[32];
+      float psum[2] = {0.f, 0.f};
+      uint32_t hi[32], lo2[32];
 #pragma unroll
       for (int k2 = 0; k2 < 32; ++k2) {
         const float p0 = hw_exp2(fmaf(s[2 * k2], A.scale2, negm));
         const float p1 = hw_exp2(fmaf(s[2 * k2 + 1], A.scale2, negm));
-        psum += p0 + p1;
-        split_bf16(p0, p1, hi[k2], lo[k2]);
+        psum[k2 & 1] += p0 + p1;
+        split_bf16(p0, p1, hi[k2], lo2[k2]);
       }
-      l_run += psum;
+      l_run += psum[0] + psum[1];
       {
         uint32_t v[16];
 #pragma unroll
@@ -1111,80 +1081,124 @@ __global__ void __launch_bounds__(kWsThreads, 1)
         for (int k = 0; k < 16; ++k) v[k] = hi[16 + k];
         tc::st16(aS + 16, v);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = lo[k];
+        for (int k = 0; k < 16; ++k) v[k] = lo2[k];
         tc::st16(aS + 32, v);
 #pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = lo[16 + k];
+        for (int k = 0; k < 16; ++k) v[k] = lo2[16 + k];
         tc::st16(aS + 48, v);
       }
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
-      if ((tid & 31) == 0) mbar_arrive1(&bar.x_free[buf]);
-      // |v|^2 of the tile's keys for pass 2: four threads per key, 32 elements each
+      if (lane == 0) mbar_arrive1(&bar.x_free[b]);
+      // |v|^2 of the tile's keys for pass 2 (with two row tiles each CTA
+      // takes half the keys): 2 or 4 threads per key
       {
-        const int key = tid >> 2, part = tid & 3;
-        const unsigned char* vst = skv + st * kTcKV + 2 * kTcHalf;
+        const unsigned char* vst = svr + vs * kP1Tile;
         float acc = 0.f;
+        int key;
+        bool lead;
+        if (nrt == 1) {
+          key = gt >> 1;
+          const int part = gt & 1;
+          float acc2 = 0.f;
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          const uint4 x = *reinterpret_cast<const uint4*>(vst + sw_off(key, (part * 4 + c) * 8));
-          const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&x);
+          for (int c = 0; c < 8; ++c) {
+            const uint4 x = *reinterpret_cast<const uint4*>(vst + sw_off<kP1Keys>(key, (part * 8 + c) * 8));
+            const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&x);
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float2 f = __bfloat1622float2(pr[u]);
-            acc = fmaf(f.x, f.x, fmaf(f.y, f.y, acc));
+            for (int u = 0; u < 4; ++u) {
+              const float2 f = __bfloat1622float2(pr[u]);
+              acc = fmaf(f.x, f.x, acc);
+              acc2 = fmaf(f.y, f.y, acc2);
+            }
           }
+          acc += acc2;
+          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+          lead = part == 0;
+        } else {
+          key = rt * 32 + (gt >> 2);
+          const int part = gt & 3;
+          float acc2 = 0.f;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            const uint4 x = *reinterpret_cast<const uint4*>(vst + sw_off<kP1Keys>(key, (part * 4 + c) * 8));
+            const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float2 f = __bfloat1622float2(pr[u]);
+              acc = fmaf(f.x, f.x, acc);
+              acc2 = fmaf(f.y, f.y, acc2);
+            }
+          }
+          acc += acc2;
+          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+          lead = part == 0;
         }
-        acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-        acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-        const int j = j_begin + t * kTcKeys + key;
-        if (part == 0 && j < j_end) A.ws.d3_vn[static_cast<size_t>(l) * A.dm.cap + j] = acc;
+        const int j = j_begin + t * kP1Keys + key;
+        if (lead && j < j_end) A.ws.d3_vn[lo + j] = acc;
       }
       __syncwarp();
-      if ((tid & 31) == 0) mbar_arrive1(&bar.empty[st]);
+      if (lane == 0) mbar_arrive1(&bar.vempty[vs]);
     }
+    // merge the two groups' (max, sum, O) per row, like two chunks
+    sh_ml[grp][rr][0] = m_run;
+    sh_ml[grp][rr][1] = l_run;
+    named_sync(1, 256);
+    const float m0 = sh_ml[0][rr][0], l0 = sh_ml[0][rr][1], m1 = sh_ml[1][rr][0], l1 = sh_ml[1][rr][1];
+    const float M = fmaxf(m0, m1);
+    const float s0 = m0 == -INFINITY ? 0.f : exp2f(m0 - M);
+    const float s1 = m1 == -INFINITY ? 0.f : exp2f(m1 - M);
     const size_t stride = kD + 2;
     float* part = A.ws.d3_part + (static_cast<size_t>(l) * A.chunks + chunk) * static_cast<size_t>(A.rows_cap) * stride +
-                  static_cast<size_t>(r) * stride;
+                  static_cast<size_t>(row_ok ? r : 0) * stride;
     if (kWithV) {
-      (void)mbar_wait_bounded(&bar.pv_done[(ntiles - 1) & 1], ((ntiles - 1) >> 1) & 1, A.ws.status);
+      // every P V is complete once the last one is (each commit covers all earlier MMAs)
+      (void)mbar_wait_bounded(&bar.pv_done[(ntiles - 1) % kP1Bufs], ((ntiles - 1) / kP1Bufs) & 1, A.ws.status);
       tc::fence_after();
-    }
-    const uint32_t aO = tl + lane_off + m * 128;
+      const bool two = ntiles >= 2;   // O_B holds nothing when the chunk has one tile
 #pragma unroll
-    for (int q8 = 0; q8 < (kWithV ? 8 : 0); ++q8) {
-      uint32_t v[16];
-      tc::ld16(aO + q8 * 16, v);
-      tc::wait_ld();
-      if (row_ok) {
+      for (int q4 = 0; q4 < 4; ++q4) {
+        const int c0 = grp * 64 + q4 * 16;   // this thread writes columns [64 grp, 64 grp + 64) of its row
+        uint32_t va[16], vb[16];
+        tc::ld16(tl + lane_off + c0, va);
+        if (two) tc::ld16(tl + lane_off + 128 + c0, vb);
+        tc::wait_ld();
+        if (row_ok) {
 #pragma unroll
-        for (int k = 0; k < 16; k += 2)
-          *reinterpret_cast<float2*>(part + q8 * 16 + k) = make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1]));
+          for (int k = 0; k < 16; k += 2) {
+            float2 o;
+            o.x = s0 * __uint_as_float(va[k]) + (two ? s1 * __uint_as_float(vb[k]) : 0.f);
+            o.y = s0 * __uint_as_float(va[k + 1]) + (two ? s1 * __uint_as_float(vb[k + 1]) : 0.f);
+            *reinterpret_cast<float2*>(part + c0 + k) = o;
+          }
+        }
       }
     }
-    if (row_ok) {
-      part[kD] = m_run;
-      part[kD + 1] = l_run;
+    if (row_ok && grp == 0) {
+      part[kD] = M;
+      part[kD + 1] = s0 * l0 + s1 * l1;
     }
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == kWsIssuer) tc::dealloc(tl, kTcCols);
+  if (warp == kP1Issuer) tc::dealloc(tl, 512);
 }
 
-// p / (1 - p) * ||a - v|| for the one key of a row with p > 1/2, x = log2 p:
-// the distance directly from the fp32 a row and the swizzled V tile (the
-// expansion would cancel), 1 - p from expm1.
-__device__ __noinline__ float residual_direct(float x, const float* arow, const unsigned char* vtile, int key) {
+// p / (1 - p) * ||a - v|| for a (row, key) pair with p > 1/2, x = log2 p:
+// the distance directly from the fp32 a row and the key's bf16 V row in the
+// pool (the expansion would cancel there), 1 - p from expm1.
+__device__ __noinline__ float residual_direct(float x, const float* arow, const __nv_bfloat16* vrow) {
   const float p = exp2f(x);
   const float om = -expm1f(x * kLn2);
   if (!(om > 0.f)) return INFINITY;
   const float4* a4 = reinterpret_cast<const float4*>(arow);
+  const uint4* v8 = reinterpret_cast<const uint4*>(vrow);
   float acc = 0.f;
 #pragma unroll 4
   for (int c = 0; c < kD / 8; ++c) {
-    const uint4 raw = *reinterpret_cast<const uint4*>(vtile + sw_off(key, c * 8));
+    const uint4 raw = v8[c];
     const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
     const float4 x0 = a4[c * 2], x1 = a4[c * 2 + 1];
     const float2 v0 = __bfloat1622float2(pr[0]), v1 = __bfloat1622float2(pr[1]);
@@ -1202,308 +1216,282 @@ __device__ __noinline__ float residual_direct(float x, const float* arow, const 
   return p / om * sqrtf(acc);
 }
 
-// pass 2.  x_full[0]: S(t) and G(t) done; x_free[0]: the 8 row warps have
-// read them (the buffer may be overwritten); empty[s]: the MMAs and the 8 row
-// warps are done with the stage.  Each row warp leaves its 32 rows' sum per
-// key of the tile in col[stage][warp]; the producer adds the 8 when it
-// recycles the stage.
 constexpr float kSmallLog2 = -7.f;   // p < 2^-7: p / (1 - p) = p + p^2 + p^3 within 2^-21
 constexpr float kR2Floor = 1e-30f;   // r2 floor: sqrt(r2) = r2 rsqrt(r2) stays finite (1e-15 for r2 = 0)
 
-// kMode (D3Mode): kResidual as above; the mass modes issue S alone, load no
-// V and sum the weights of the keys the row counts.
+// Pass-2 state past the big operands, in dynamic shared memory (the operands
+// fill all but a few KB of it).
+struct P2Small {
+  uint64_t full[kP2St], empty[kP2St], x_full[2], x_free[2], qfull;
+  uint32_t taddr, pad;
+  float lse2[kRowTile];    // per row of the CTA: LSE (base 2; +inf past the rows) and |a|^2
+  float an[kRowTile];
+};
+constexpr int p2_smem(bool res) {
+  return (res ? 3 : 1) * kQBytes + kP2St * (res ? 2 : 1) * kP2Tile + static_cast<int>(sizeof(P2Small)) + 1008;
+}
+
+// pass 2.  Barriers: full / empty the K/V stages (empty: the tile's MMAs are
+// done with it); x_full[b] S^T and G^T of tile t done; x_free[b] the 8 row
+// warps have read them into registers; qfull the resident operands staged.
 template <int kMode>
-__global__ void __launch_bounds__(kWsThreads, 1)
-    d3_tc_pass2_kernel(D3Args A, const __grid_constant__ D3Maps mp) {
+__global__ void __launch_bounds__(kP2Threads, 1) d3_p2_kernel(D3Args A, const __grid_constant__ D3Maps mp) {
+  constexpr bool kRes = kMode == kResidual;
+  constexpr int kStageB = (kRes ? 2 : 1) * kP2Tile;
+  constexpr uint32_t kCols = kRes ? 512 : 256;
+  constexpr int kBufCols = kRes ? 256 : 128;
   extern __shared__ unsigned char d3_dsm[];
-  __shared__ int sh_pos[kTcStages][kTcKeys];
-  __shared__ __align__(16) float sh_vn[kTcStages][kTcKeys];
-  __shared__ float sh_col[kTcStages][kWsRowThreads / 32][kTcKeys];
-  __shared__ __align__(8) WsBars bar;
-  __shared__ uint32_t sh_taddr;
-  const int chunk = blockIdx.x, l = blockIdx.y;
+  const int nrt = (A.rows + kRowTile - 1) / kRowTile;
+  const int rt = blockIdx.x % nrt, chunk = blockIdx.x / nrt, l = blockIdx.y;
   const int n = min(max(A.ls.count[l], 0), A.dm.cap);
   const int j_begin = chunk * A.chunk_keys;
   if (j_begin >= n) return;
   const int j_end = min(n, j_begin + A.chunk_keys);
-  const int ntiles = (j_end - j_begin + kTcKeys - 1) / kTcKeys;
+  const int ntiles = (j_end - j_begin + kP2Keys - 1) / kP2Keys;
   unsigned char* sq = align1024(d3_dsm);
-  unsigned char* skv = sq + kTcQ;
+  unsigned char* sah = sq + kQBytes;
+  unsigned char* sal = sah + kQBytes;
+  unsigned char* ring = sq + (kRes ? 3 : 1) * kQBytes;
+  P2Small& sm = *reinterpret_cast<P2Small*>(ring + kP2St * kStageB);
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  if (warp == kWsIssuer) tc::alloc(&sh_taddr, kTcCols);
-  if (tid == 0) ws_init_bars(bar, 1, 1 + kWsRowThreads / 32, kWsRowThreads / 32);
-  tc::fence_before();
-  __syncthreads();
-  tc::fence_after();
-  const uint32_t tl = sh_taddr;
-  const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
-  // mass modes with at most 128 rows: one row tile; warps w and w + 4 share
-  // its rows, warp w summing keys 0-31 of each tile and warp w + 4 keys 32-63
-  const bool split = kMode != kResidual && A.rows <= 128;
-  const int r = split ? (tid & 127) : tid, m = r >> 7, h0 = split && tid < kWsRowThreads ? (warp >> 2) : 0;
-  const bool row_ok = r < A.rows;
-  const size_t wrow = static_cast<size_t>(l) * A.rows_cap + (row_ok ? r : 0);
-  const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-  if (kMode == kResidual && warp < kWsProducer) {
-    // a of this row (bf16 hi and lo) into tensor memory
-    const uint4* hsrc = reinterpret_cast<const uint4*>(A.ws.d3_ahi + wrow * kD);
-    const uint4* lsrc = reinterpret_cast<const uint4*>(A.ws.d3_alo + wrow * kD);
-#pragma unroll
-    for (int q4 = 0; q4 < 4; ++q4) {
-      uint32_t vh[16], vl[16];
-#pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        const uint4 x = row_ok ? hsrc[q4 * 4 + u] : make_uint4(0, 0, 0, 0);
-        const uint4 y = row_ok ? lsrc[q4 * 4 + u] : make_uint4(0, 0, 0, 0);
-        vh[u * 4 + 0] = x.x; vh[u * 4 + 1] = x.y; vh[u * 4 + 2] = x.z; vh[u * 4 + 3] = x.w;
-        vl[u * 4 + 0] = y.x; vl[u * 4 + 1] = y.y; vl[u * 4 + 2] = y.z; vl[u * 4 + 3] = y.w;
-      }
-      tc::st16(tl + lane_off + m * 64 + q4 * 16, vh);
-      tc::st16(tl + lane_off + 128 + m * 64 + q4 * 16, vl);
+  if (warp == kP2Issuer) tc::alloc(&sm.taddr, kCols);
+  if (tid == 0) {
+    for (int s = 0; s < kP2St; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
     }
-    tc::wait_st();
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.x_full[b], 1);
+      mbar_init(&sm.x_free[b], kP2RowWarps);
+    }
+    mbar_init(&sm.qfull, kP2RowWarps);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   tc::fence_before();
   __syncthreads();
   tc::fence_after();
+  const uint32_t tl = sm.taddr;
+  const size_t lo = static_cast<size_t>(l) * A.dm.cap;
 
-  if (warp == kWsProducer) {
-    ws_produce<true, kMode == kResidual>(A, mp, l, j_begin, j_end, ntiles, sq, skv, sh_pos, sh_vn, sh_col, bar);
-  } else if (warp == kWsIssuer) {
+  if (warp == kP2Producer) {
+    d3_produce<kP2Keys, kP2St, true, kRes, false, 0>(A, mp, l, j_begin, j_end, ntiles, ring, sm.full, sm.empty,
+                                                     nullptr, nullptr, nullptr);
+  } else if (warp == kP2Issuer) {
     if (lane == 0) {
-      (void)mbar_wait_bounded(&bar.qfull, 0, A.ws.status);
+      // descriptors built once; each MMA advances one by a constant
+      const uint64_t dq = tc::desc_sw128(smem_u32(sq), 16, 1024);
+      const uint64_t dah = tc::desc_sw128(smem_u32(sah), 16, 1024);
+      const uint64_t dal = tc::desc_sw128(smem_u32(sal), 16, 1024);
+      const uint64_t dr0 = tc::desc_sw128(smem_u32(ring), 16, 1024);
+      (void)mbar_wait_bounded(&sm.qfull, 0, A.ws.status);
 #pragma unroll 1
       for (int t = 0; t < ntiles; ++t) {
-        const int st = t % kTcStages;
-        (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);
-        if (t > 0) (void)mbar_wait_bounded(&bar.x_free[0], (t - 1) & 1, A.ws.status);
+        const int st = t & 1;
+        (void)mbar_wait_bounded(&sm.full[st], (t >> 1) & 1, A.ws.status);
+        if (t >= 2) (void)mbar_wait_bounded(&sm.x_free[st], ((t >> 1) - 1) & 1, A.ws.status);
         tc::fence_after();
-        const unsigned char* kst = skv + st * kTcKV;
-        const unsigned char* vst = kst + 2 * kTcHalf;
+        const uint64_t dk = tc::desc_add(dr0, st * kStageB), dv = tc::desc_add(dk, kP2Tile);
+        const uint32_t dS = tl + st * kBufCols, dG = dS + 128;
 #pragma unroll
-        for (int mm = 0; mm < 2; ++mm) {
-          if (split && mm == 1) break;
-          tc_issue_s(tl + 256 + mm * 64, sq, kst, mm);
+        for (int kk = 0; kk < 8; ++kk) {
+          const int off = (kk >> 2) * (kP2Keys * 128) + (kk & 3) * 32;   // d half, 16-element step
+          tc::mma_ss(dS, tc::desc_add(dk, off), tc::desc_add(dq, off), kId128, kk > 0 ? 1u : 0u);
+        }
+        if (kRes) {
 #pragma unroll
-          for (int ks = 0; ks < (kMode == kResidual ? 8 : 0); ++ks) {
-            const int half = ks >> 2, kin = ks & 3;
-            const uint64_t bd = tc::desc_sw128(smem_u32(vst + half * kTcHalf) + kin * 32, 16, 1024);
-            tc::mma_ts(tl + 384 + mm * 64, tl + mm * 64 + ks * 8, bd, kIdS, ks > 0 ? 1u : 0u);
-            tc::mma_ts(tl + 384 + mm * 64, tl + 128 + mm * 64 + ks * 8, bd, kIdS, 1u);
+          for (int kk = 0; kk < 8; ++kk) {
+            const int off = (kk >> 2) * (kP2Keys * 128) + (kk & 3) * 32;
+            tc::mma_ss(dG, tc::desc_add(dv, off), tc::desc_add(dah, off), kId128, kk > 0 ? 1u : 0u);
+          }
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk) {
+            const int off = (kk >> 2) * (kP2Keys * 128) + (kk & 3) * 32;
+            tc::mma_ss(dG, tc::desc_add(dv, off), tc::desc_add(dal, off), kId128, 1u);
           }
         }
-        tc::commit(&bar.x_full[0]);
-        tc::commit(&bar.empty[st]);
+        tc::commit(&sm.x_full[st]);
+        tc::commit(&sm.empty[st]);
       }
     }
   } else {
-    const int qp = row_ok ? A.qpos[r % A.w] : -1;
-    const float lse2 = row_ok ? A.ws.d3_rowc[wrow * 2] : 0.f;
-    const float an = row_ok ? A.ws.d3_rowc[wrow * 2 + 1] : 0.f;
-    const float* arow = A.a_out;
-    if (row_ok) {
-      const int h = r / A.w, i = r % A.w;
-      arow = A.a_out + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + h) * A.w + i) * kD;
+    // row warps: warp w owns keys 32 (w % 4) .. + 31 of every tile (its
+    // tensor-memory lanes) and the CTA's rows 32 (w / 4) .. + 31 (columns)
+    constexpr int kRowThreads = kP2RowWarps * 32;
+    const int qd = warp & 3, c = warp >> 2;
+    const int kk = qd * 32 + lane;
+    const int r0 = rt * kRowTile + c * 32;   // first row of this warp
+    const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
+    const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
+    stage_rows(sq, 0, A, l, rt, tid, kRowThreads);
+    if (kRes) {
+      stage_rows(sah, 1, A, l, rt, tid, kRowThreads);
+      stage_rows(sal, 2, A, l, rt, tid, kRowThreads);
     }
-    const int nkeys = j_end - j_begin;
-    if (kMode != kResidual) {
-#pragma unroll 1
-      for (int t = 0; t < ntiles; ++t) {
-        const int st = t % kTcStages;
-        (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);   // positions
-        (void)mbar_wait_bounded(&bar.x_full[0], t & 1, A.ws.status);
-        tc::fence_after();
-        float sv[kTcKeys];
-        {
-          uint32_t v[4][16];
-          const uint32_t aS = tl + lane_off + 256 + m * 64;
-          tc::ld16(aS + h0 * 32, v[0]);
-          tc::ld16(aS + h0 * 32 + 16, v[1]);
-          if (!split) {
-            tc::ld16(aS + 32, v[2]);
-            tc::ld16(aS + 48, v[3]);
-          }
-          tc::wait_ld();
-#pragma unroll
-          for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-            for (int k = 0; k < 16; ++k) sv[q4 * 16 + k] = __uint_as_float(v[q4][k]);
-        }
-        tc::fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive1(&bar.x_free[0]);
-        // the keys the row counts are a prefix of the tile (positions ascend)
-        int vis = 0;
-        if (row_ok) {
-          const int lim = min(kTcKeys, nkeys - t * kTcKeys);
-          auto counted = [&](int k) { return kMode == kMassLater ? sh_pos[st][k] < qp : sh_pos[st][k] <= qp; };
-          if (lim > 0 && counted(lim - 1)) {
-            vis = lim;
-          } else {
-            int lo = 0, hi = lim;
-            while (lo < hi) {
-              const int mid = (lo + hi) >> 1;
-              if (counted(mid)) lo = mid + 1; else hi = mid;
-            }
-            vis = lo;
-          }
-        }
-        if (split) sh_col[st][warp][(1 - h0) * 32 + lane] = 0.f;   // the other warp of the pair sums those keys
-#pragma unroll 1
-        for (int hf = h0; hf < (split ? h0 + 1 : 2); ++hf) {
-          const int kv = vis - hf * 32;
-#pragma unroll
-          for (int k2 = 0; k2 < kTcKeys / 2; ++k2)
-            sv[k2] = k2 < kv ? hw_exp2(fmaf(sv[k2], A.scale2, -lse2)) : 0.f;
-#pragma unroll
-          for (int o = 16, cnt = kTcKeys / 2; o >= 1; o >>= 1, cnt >>= 1) {
-            const bool up = (lane & o) != 0;
-#pragma unroll
-            for (int i = 0; i < cnt / 2; ++i) {
-              const float send = up ? sv[i] : sv[cnt / 2 + i];
-              const float keep = up ? sv[cnt / 2 + i] : sv[i];
-              sv[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-            }
-          }
-          sh_col[st][warp][hf * 32 + lane] = sv[0];
-#pragma unroll
-          for (int k2 = 0; k2 < kTcKeys / 2; ++k2) sv[k2] = sv[kTcKeys / 2 + k2];
-        }
-        __syncwarp();
-        if (lane == 0) mbar_arrive1(&bar.empty[st]);
-      }
-    } else {
+    if (tid < kRowTile) {
+      const int r = rt * kRowTile + tid;
+      const size_t wrow = static_cast<size_t>(l) * A.rows_cap + r;
+      // a row past the window's rows: +inf LSE, so every weight of it is 0
+      sm.lse2[tid] = r < A.rows ? A.ws.d3_rowc[wrow * 2] : INFINITY;
+      sm.an[tid] = (kRes && r < A.rows) ? A.ws.d3_rowc[wrow * 2 + 1] : 0.f;
+    }
+    cp_commit();
+    cp_wait<0>();
+    fence_proxy_async();
+    named_sync(1, kRowThreads);
+    if (lane == 0) mbar_arrive1(&sm.qfull);
+    // the query position of row r0 + lane, and the warp's minimum: a key at
+    // or before it is seen by all of the warp's rows
+    const int qp_mine = r0 + lane < A.rows ? A.qpos[(r0 + lane) % A.w] : 0x7FFFFFFF;
+    const int qmin = __reduce_min_sync(0xffffffffu, qp_mine);
+    const int nv = min(32, A.rows - r0);   // rows of this warp (<= 0: none)
+    const int nch = nv <= 0 ? 0 : (nv + 15) >> 4;
+    auto meta = [&](int t, int& p, float& v) {
+      const int j = j_begin + t * kP2Keys + kk;
+      const bool ok = t < ntiles && j < j_end;
+      p = ok ? A.ls.pos[lo + j] : 0x7FFFFFFF;
+      v = (kRes && ok) ? A.ws.d3_vn[lo + j] : 0.f;
+    };
+    int pj;
+    float vj;
+    meta(0, pj, vj);
 #pragma unroll 1
     for (int t = 0; t < ntiles; ++t) {
-      const int st = t % kTcStages;
-      const unsigned char* vst = skv + st * kTcKV + 2 * kTcHalf;
-      (void)mbar_wait_bounded(&bar.full[st], (t / kTcStages) & 1, A.ws.status);   // positions, |v|^2, V
-      // S and G of the tile's 64 keys; once read, the next tile's MMAs may
-      // overwrite them
-      (void)mbar_wait_bounded(&bar.x_full[0], t & 1, A.ws.status);
+      const int st = t & 1;
+      const int j = j_begin + t * kP2Keys + kk;
+      const bool key_ok = j < j_end;
+      int pj_n;
+      float vj_n;
+      meta(t + 1, pj_n, vj_n);   // in flight while this tile is scored
+      // every (row, key) pair of the warp counted: no mask (a key past the
+      // chunk has position INT_MAX)
+      const int wmax = __reduce_max_sync(0xffffffffu, pj);
+      const bool no_mask = kMode == kMassLater ? wmax < qmin : wmax <= qmin;
+      (void)mbar_wait_bounded(&sm.x_full[st], (t >> 1) & 1, A.ws.status);
       tc::fence_after();
-      float sv[kTcKeys], gv[kTcKeys];
-      {
-        uint32_t v[4][16], w[4][16];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) {
-          tc::ld16(tl + lane_off + 256 + m * 64 + q4 * 16, v[q4]);
-          tc::ld16(tl + lane_off + 384 + m * 64 + q4 * 16, w[q4]);
-        }
-        tc::wait_ld();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            sv[q4 * 16 + k] = __uint_as_float(v[q4][k]);
-            gv[q4 * 16 + k] = __uint_as_float(w[q4][k]);
-          }
-      }
-      tc::fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive1(&bar.x_free[0]);
-      // keys visible to the row: positions ascend within the tile, so they
-      // are a prefix (binary search of the row's query position)
-      int vis = 0;
-      if (row_ok) {
-        const int lim = min(kTcKeys, nkeys - t * kTcKeys);
-        if (lim > 0 && sh_pos[st][lim - 1] <= qp) {
-          vis = lim;
-        } else {
-          int lo = 0, hi = lim;   // first key with position > qp lies in [lo, hi)
-          while (lo < hi) {
-            const int mid = (lo + hi) >> 1;
-            if (sh_pos[st][mid] <= qp) lo = mid + 1; else hi = mid;
-          }
-          vis = lo;
-        }
-      }
-      // the two halves go through one copy of the code (the row loop is long
-      // and instruction fetch stalls when it is duplicated); after the first,
-      // the second half's registers move down
+      const uint32_t aS = tl + lane_off + st * kBufCols + c * 32;
+      float acc = 0.f;
+      // 16 rows at a time: the chunk's S^T (and G^T) columns into registers
 #pragma unroll 1
-      for (int hf = 0; hf < 2; ++hf) {
-        const int kv = vis - hf * 32;   // visible keys of this half: k2 < kv
-        // weights p = 2^x of the half's keys in place of S (x = -inf, p = 0
-        // where not visible), and the largest x
-        float xmax = -INFINITY;
-        if (__all_sync(0xffffffffu, kv >= kTcKeys / 2)) {
+      for (int ch = 0; ch < nch; ++ch) {
+        uint32_t v[16], g[16];
+        tc::ld16(aS + ch * 16, v);
+        if (kRes) tc::ld16(aS + 128 + ch * 16, g);
+        tc::wait_ld();
+        const float* lse_c = sm.lse2 + c * 32 + ch * 16;
+        const float* an_c = sm.an + c * 32 + ch * 16;
+        float x[16];
+        float xm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-          for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
-            const float x = fmaf(sv[k2], A.scale2, -lse2);
-            xmax = fmaxf(xmax, x);
-            sv[k2] = hw_exp2(x);
-          }
-        } else {
+        for (int k4 = 0; k4 < 4; ++k4) {
+          const float4 L4 = *reinterpret_cast<const float4*>(lse_c + 4 * k4);
+          const float Ls[4] = {L4.x, L4.y, L4.z, L4.w};
 #pragma unroll
-          for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
-            const float x = k2 < kv ? fmaf(sv[k2], A.scale2, -lse2) : -INFINITY;
-            xmax = fmaxf(xmax, x);
-            sv[k2] = hw_exp2(x);
+          for (int u = 0; u < 4; ++u) {
+            const int k = 4 * k4 + u;
+            float xv = fmaf(__uint_as_float(v[k]), A.scale2, -Ls[u]);
+            if (!no_mask) {
+              const int qpr = __shfl_sync(0xffffffffu, qp_mine, ch * 16 + k);
+              const bool vis = key_ok && (kMode == kMassLater ? pj < qpr : pj <= qpr);
+              xv = vis ? xv : -INFINITY;
+            }
+            x[k] = xv;
+            xm[u] = fmaxf(xm[u], xv);
           }
         }
-        if (!__any_sync(0xffffffffu, xmax >= kSmallLog2)) {
-          // every weight of the warp's rows is small: no reciprocal, and
-          // sqrt(r2) = r2 rsqrt(r2) (a key that is not visible has p = 0)
-          const float4* vn4 = reinterpret_cast<const float4*>(&sh_vn[st][hf * 32]);
+        if (!kRes) {
 #pragma unroll
-          for (int k4 = 0; k4 < kTcKeys / 8; ++k4) {
-            const float4 vq = vn4[k4];
-            const float vv[4] = {vq.x, vq.y, vq.z, vq.w};
+          for (int k = 0; k < 16; ++k) acc += hw_exp2(x[k]);
+          continue;
+        }
+        const float xmax = fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3]));
+        if (!__any_sync(0xffffffffu, xmax >= kSmallLog2)) {
+          // every weight of the warp's pairs is small: no reciprocal, and
+          // sqrt(r2) = r2 rsqrt(r2) (a pair not counted has p = 0)
+#pragma unroll
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 N4 = *reinterpret_cast<const float4*>(an_c + 4 * k4);
+            const float Ns[4] = {N4.x, N4.y, N4.z, N4.w};
 #pragma unroll
             for (int u = 0; u < 4; ++u) {
-              const int k2 = k4 * 4 + u;
-              const float p = sv[k2];
-              const float r2 = fmaxf(kR2Floor, fmaf(-2.f, gv[k2], an + vv[u]));
+              const int k = 4 * k4 + u;
+              const float p = hw_exp2(x[k]);
+              const float r2 = fmaxf(kR2Floor, fmaf(-2.f, __uint_as_float(g[k]), Ns[u] + vj));
               const float q = fmaf(fmaf(p, p, p), p, p);   // p + p^2 + p^3
-              sv[k2] = q * r2 * hw_rsqrt(r2);
+              acc = fmaf(q * r2, hw_rsqrt(r2), acc);
             }
           }
         } else {
-          int xk = -1;
+          unsigned big = 0;
 #pragma unroll
-          for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
-            const float p = sv[k2];
-            const float r2 = fmaxf(0.f, fmaf(-2.f, gv[k2], an + sh_vn[st][hf * 32 + k2]));
-            float tm = p * hw_rcp(1.f - p) * hw_sqrt(r2);
-            if (p > 0.5f) { xk = k2; tm = 0.f; }
-            sv[k2] = p > 0.f ? tm : 0.f;
+          for (int k4 = 0; k4 < 4; ++k4) {
+            const float4 N4 = *reinterpret_cast<const float4*>(an_c + 4 * k4);
+            const float Ns[4] = {N4.x, N4.y, N4.z, N4.w};
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const int k = 4 * k4 + u;
+              const float p = hw_exp2(x[k]);
+              const float r2 = fmaxf(0.f, fmaf(-2.f, __uint_as_float(g[k]), Ns[u] + vj));
+              const float tm = p * hw_rcp(1.f - p) * hw_sqrt(r2);
+              if (p > 0.5f) big |= 1u << k;
+              acc += (p > 0.f && p <= 0.5f) ? tm : 0.f;
+            }
           }
-          // the one key of the row with p > 1/2 (the largest x): direct
-          // distance, out of line
-          if (xk >= 0) {
-            const float dterm = residual_direct(xmax, arow, vst, hf * 32 + xk);
+          // pairs with p > 1/2 (at most one key per row has one): direct distance
+          while (big) {
+            const int k = __ffs(big) - 1;
+            big &= big - 1;
+            float xk = 0.f;
 #pragma unroll
-            for (int k2 = 0; k2 < kTcKeys / 2; ++k2)
-              if (k2 == xk) sv[k2] = dterm;
+            for (int k2 = 0; k2 < 16; ++k2)
+              if (k2 == k) xk = x[k2];
+            const int r = r0 + ch * 16 + k;
+            const float* arow =
+                A.a_out + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + r / A.w) * A.w + r % A.w) * kD;
+            int slot = A.ls.slot[lo + j];
+            if (slot < 0 || slot >= A.dm.P * kBlock) {
+              set_status(A.ws.status, ST_BAD_INDEX);
+              slot = 0;
+            }
+            const __nv_bfloat16* vrow = static_cast<const __nv_bfloat16*>(A.ls.v_pool) + static_cast<size_t>(slot) * kD;
+            acc += residual_direct(xk, arow, vrow);
           }
-        }
-        // butterfly: each lane ends with the warp's sum of one key
-#pragma unroll
-        for (int o = 16, cnt = kTcKeys / 2; o >= 1; o >>= 1, cnt >>= 1) {
-          const bool up = (lane & o) != 0;
-#pragma unroll
-          for (int i = 0; i < cnt / 2; ++i) {
-            const float send = up ? sv[i] : sv[cnt / 2 + i];
-            const float keep = up ? sv[cnt / 2 + i] : sv[i];
-            sv[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-          }
-        }
-        sh_col[st][warp][hf * 32 + lane] = sv[0];
-#pragma unroll
-        for (int k2 = 0; k2 < kTcKeys / 2; ++k2) {
-          sv[k2] = sv[kTcKeys / 2 + k2];
-          gv[k2] = gv[kTcKeys / 2 + k2];
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive1(&bar.empty[st]);    // this warp is done with the stage
-    }
+      // the four warps sharing these keys: warps c = 1..3 leave their sums in
+      // the first (already read) S^T column of their rows, warp c = 0 adds
+      // them to its own in order c = 0..3; a barrier per tile parity, so a
+      // warp a tile ahead cannot arrive on the one still being waited on
+      const int hb = 2 + qd + 4 * (t & 1);
+      if (c != 0) {
+        tc::st1(aS, __float_as_uint(acc));
+        tc::wait_st();
+        tc::fence_before();
+        named_arrive(hb, 128);
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(&sm.x_free[st]);
+      } else {
+        named_sync(hb, 128);
+        tc::fence_after();
+        const uint32_t a1 = tc::ld1(aS + 32), a2 = tc::ld1(aS + 64), a3 = tc::ld1(aS + 96);
+        tc::wait_ld();
+        const float tot = ((acc + __uint_as_float(a1)) + __uint_as_float(a2)) + __uint_as_float(a3);
+        tc::fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(&sm.x_free[st]);
+        if (key_ok) {
+          if (nrt == 1)
+            A.col_out[lo + j] = tot;
+          else
+            atomicAdd(A.col_out + lo + j, tot);
+        }
+      }
+      pj = pj_n;
+      vj = vj_n;
     }
   }
   tc::fence_before();
   __syncthreads();
-  if (warp == kWsIssuer) tc::dealloc(tl, kTcCols);
+  if (warp == kP2Issuer) tc::dealloc(tl, kCols);
 }
 
 }  // namespace
@@ -1511,27 +1499,31 @@ __global__ void __launch_bounds__(kWsThreads, 1)
 int d3_rows_max(const Dims& dm) { return dm.g * dm.max_window; }
 
 cudaError_t prepare_dropkv() {
-  const void* fns[] = {reinterpret_cast<const void*>(d3_tc_pass1_kernel<true>),
-                       reinterpret_cast<const void*>(d3_tc_pass1_kernel<false>),
-                       reinterpret_cast<const void*>(d3_tc_pass2_kernel<kResidual>),
-                       reinterpret_cast<const void*>(d3_tc_pass2_kernel<kMassCausal>),
-                       reinterpret_cast<const void*>(d3_tc_pass2_kernel<kMassLater>)};
-  for (const void* f : fns) {
-    const cudaError_t e = cudaFuncSetAttribute(f, cudaFuncAttributeMaxDynamicSharedMemorySize, kTcSmem);
+  struct {
+    const void* f;
+    int smem;
+  } fns[] = {{reinterpret_cast<const void*>(d3_p1_kernel<true>), kP1Smem},
+             {reinterpret_cast<const void*>(d3_p1_kernel<false>), kP1Smem},
+             {reinterpret_cast<const void*>(d3_p2_kernel<kResidual>), p2_smem(true)},
+             {reinterpret_cast<const void*>(d3_p2_kernel<kMassCausal>), p2_smem(false)},
+             {reinterpret_cast<const void*>(d3_p2_kernel<kMassLater>), p2_smem(false)}};
+  for (const auto& x : fns) {
+    const cudaError_t e = cudaFuncSetAttribute(x.f, cudaFuncAttributeMaxDynamicSharedMemorySize, x.smem);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
 }
-// Keys per CTA: each lane's keys split over floor(SMs / lanes) CTAs (one
-// wave when the lanes are few), in whole 64-key tiles, at least kChunkMin.
-// sm_count 0 gives the most chunks any device can use (workspace sizing).
-static int d3_chunk_keys(const Dims& dm, int sm_count) {
-  const int per_lane = sm_count > 0 ? max(1, sm_count / max(1, dm.lanes)) : 1 << 30;
+// Keys per CTA: each lane's keys split over floor(SMs / (lanes x row tiles))
+// CTAs (one wave when the lanes are few), in whole 128-key tiles, at least
+// kChunkMin.  sm_count 0 gives the most chunks any device can use
+// (workspace sizing).
+static int d3_chunk_keys(const Dims& dm, int sm_count, int row_tiles) {
+  const int per_lane = sm_count > 0 ? max(1, sm_count / max(1, dm.lanes * row_tiles)) : 1 << 30;
   const int k = (dm.cap + per_lane - 1) / per_lane;
-  return max(kChunkMin, (k + kTcKeys - 1) / kTcKeys * kTcKeys);
+  return max(kChunkMin, (k + kTileKeys - 1) / kTileKeys * kTileKeys);
 }
 int d3_chunks(const Dims& dm, int sm_count) {
-  const int ck = d3_chunk_keys(dm, sm_count);
+  const int ck = d3_chunk_keys(dm, sm_count, 1);
   return (dm.cap + ck - 1) / ck;
 }
 
@@ -1550,7 +1542,7 @@ cudaError_t prepare_tensor_maps(Ctx& ctx) {
   // bytes) by 1, 16 or 64 rows
   const cuuint64_t gdim[2] = {static_cast<cuuint64_t>(kD), static_cast<cuuint64_t>(dm.P) * kBlock};
   const cuuint64_t gstride[1] = {static_cast<cuuint64_t>(kD) * 2};
-  const cuuint32_t box_rows[3] = {1, 16, static_cast<cuuint32_t>(kTcKeys)};
+  const cuuint32_t box_rows[3] = {1, 16, 64};
   const cuuint32_t estride[2] = {1, 1};
   for (int layer = 0; layer < dm.L; ++layer) {
     const LayerState ls = layer_state(ctx, layer);
@@ -1581,31 +1573,34 @@ static cudaError_t launch_window(const Ctx& ctx, int layer, const void* q_win, i
   A.w = w;
   A.rows = dm.g * w;
   A.rows_cap = d3_rows_max(dm);
-  A.chunk_keys = d3_chunk_keys(dm, ctx.sm_count);
-  A.chunks = d3_chunks(dm, ctx.sm_count);
+  // the tensor-core path splits the rows into 128-row tiles, one CTA each
+  const bool tcp = A.rows <= kTcRows;
+  const int nrt = tcp ? (A.rows + kRowTile - 1) / kRowTile : 1;
+  A.chunk_keys = d3_chunk_keys(dm, ctx.sm_count, nrt);
+  A.chunks = (dm.cap + A.chunk_keys - 1) / A.chunk_keys;
   A.lse_out = lse; A.a_out = a_out; A.scores = scores;
   A.col_out = pool_r >= 0 ? ctx.ws.d3_score_part : scores;
   A.scale2 = 1.4426950408889634f / sqrtf(static_cast<float>(dm.d));
   if (A.rows > A.rows_cap || A.rows > kMaxRowGroups * kRowsPerCta || dm.d != kD || dm.dtype != KVEVICT_BF16)
     return cudaErrorInvalidValue;
   const bool res = mode == kResidual;
-  if (A.rows <= kTcRows) {
-    const dim3 grid(A.chunks, dm.lanes);
+  if (tcp) {
+    const dim3 grid(nrt * A.chunks, dm.lanes);
     if (!ctx.tmaps) return cudaErrorInvalidValue;
     D3Maps mp;
     for (int i = 0; i < kTmapsPerLayer; ++i) mp.m[i] = ctx.tmaps[static_cast<size_t>(layer) * kTmapsPerLayer + i];
     const dim3 cgrid((A.rows + 7) / 8, dm.lanes);
     if (res) {
-      d3_tc_pass1_kernel<true><<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
+      d3_p1_kernel<true><<<grid, kP1Threads, kP1Smem, stream>>>(A, mp);
       d3_combine_kernel<true><<<cgrid, 256, 0, stream>>>(A);
-      d3_tc_pass2_kernel<kResidual><<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
+      d3_p2_kernel<kResidual><<<grid, kP2Threads, p2_smem(true), stream>>>(A, mp);
     } else {
-      d3_tc_pass1_kernel<false><<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
+      d3_p1_kernel<false><<<grid, kP1Threads, kP1Smem, stream>>>(A, mp);
       d3_combine_kernel<false><<<cgrid, 256, 0, stream>>>(A);
       if (mode == kMassLater)
-        d3_tc_pass2_kernel<kMassLater><<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
+        d3_p2_kernel<kMassLater><<<grid, kP2Threads, p2_smem(false), stream>>>(A, mp);
       else
-        d3_tc_pass2_kernel<kMassCausal><<<grid, kWsThreads, kTcSmem, stream>>>(A, mp);
+        d3_p2_kernel<kMassCausal><<<grid, kP2Threads, p2_smem(false), stream>>>(A, mp);
     }
   } else {
     const int groups = (A.rows + kRowsPerCta - 1) / kRowsPerCta;

@@ -46,6 +46,14 @@ __device__ __forceinline__ uint64_t desc_sw128(uint32_t sa, uint32_t lbo, uint32
   return d;
 }
 
+// The descriptor of the same matrix `bytes` further on (a multiple of 16):
+// the start address field holds address / 16 in 14 bits, and shared-memory
+// addresses stay below 2^18, so the add never carries out of the field.
+// Lets an MMA issue loop advance precomputed descriptors with one add
+// instead of rebuilding them (the issuing thread's instruction chain, not
+// the tensor core, bounds the rate of small MMAs otherwise).
+__device__ __forceinline__ uint64_t desc_add(uint64_t d, uint32_t bytes) { return d + (bytes >> 4); }
+
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 accumulator, A
 // K-major, B K-major (b_mn = 0) or MN-major (b_mn = 1), shape M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, int b_mn) {
@@ -82,6 +90,15 @@ __device__ __forceinline__ void ld16(uint32_t taddr, uint32_t (&v)[16]) {
       : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]),
         "=r"(v[8]), "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
       : "r"(taddr));
+}
+// One 32-bit column of this thread's lane (warp-collective).
+__device__ __forceinline__ uint32_t ld1(uint32_t taddr) {
+  uint32_t v;
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x1.b32 {%0}, [%1];" : "=r"(v) : "r"(taddr));
+  return v;
+}
+__device__ __forceinline__ void st1(uint32_t taddr, uint32_t v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(taddr), "r"(v) : "memory");
 }
 __device__ __forceinline__ void wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void st16(uint32_t taddr, const uint32_t (&v)[16]) {
