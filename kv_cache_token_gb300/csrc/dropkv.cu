@@ -15,6 +15,7 @@
 // finalize: scores = sum of the row-group partials.
 #include <cudaTypedefs.h>
 #include <new>
+#include <type_traits>
 
 #include "kvevict_internal.cuh"
 #include "tcgen05.cuh"
@@ -60,6 +61,19 @@ __device__ __forceinline__ void split_bf16(float p0, float p1, uint32_t& hi, uin
   __nv_bfloat162 l = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
   hi = *reinterpret_cast<uint32_t*>(&h);
   lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+// The same split with integer and add instructions only (the conversion
+// instructions run at a fraction of the rate): hi is p truncated to bf16 (its
+// upper 16 bits), lo = p - hi exactly in fp32, rounded to the nearest bf16
+// (ties away from zero) by adding half an ulp to its bits; hi + lo is p to
+// 2^-16 relative.  For finite p >= 0 (attention weights).
+__device__ __forceinline__ void split_bf16_fast(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+  hi = __byte_perm(b0, b1, 0x7632);
+  const float l0 = p0 - __uint_as_float(b0 & 0xFFFF0000u);
+  const float l1 = p1 - __uint_as_float(b1 & 0xFFFF0000u);
+  lo = __byte_perm(__float_as_uint(l0) + 0x8000u, __float_as_uint(l1) + 0x8000u, 0x7632);
 }
 
 struct D3Args {
@@ -578,15 +592,14 @@ __global__ void __launch_bounds__(256) d3_pool_kernel(const float* __restrict__ 
 constexpr int kTcRows = 256;                 // window rows per lane on this path (two row tiles)
 constexpr int kRowTile = 128;
 constexpr int kQBytes = 2 * kRowTile * 128;  // [d half][128 rows][128 B]
-constexpr int kP1Keys = 64;
-constexpr int kP1KSt = 5, kP1VSt = 5;        // K and V ring depths
-constexpr int kP1Bufs = 4;                   // S/P buffers in tensor memory
-constexpr int kP1Ahead = kP1Bufs - 1;        // tiles S runs ahead of P V
-constexpr int kP1Tile = kP1Keys * 256;       // one K or V tile (16 KB)
+constexpr int kP1Keys = 128;
+constexpr int kP1Bufs = 2;                   // S/P buffers in tensor memory (after O_0, O_1)
+constexpr int kP1KSt = 3, kP1VSt = 2;        // K and V ring depths
+constexpr int kP1Tile = kP1Keys * 256;       // one K or V tile (32 KB)
 constexpr int kP1Smem = kQBytes + (kP1KSt + kP1VSt) * kP1Tile + 1024;
-constexpr int kP1KProd = 8, kP1VProd = 9, kP1Issuer = 10;
-constexpr int kP1Depth = 4;                  // tiles of slots the producers read ahead
-constexpr int kP1Threads = 11 * 32;
+constexpr int kP1KProd = 8, kP1VProd = 9, kP1Issuer = 10, kP1VnWarp0 = 11, kP1VnWarps = 2;
+constexpr int kP1Depth = 3;                  // tiles of slots the producers read ahead
+constexpr int kP1Threads = 13 * 32;
 constexpr int kP2Keys = 128;
 constexpr int kP2St = 2;                     // K/V stages
 constexpr int kP2Tile = kP2Keys * 256;       // one K or V tile (32 KB)
@@ -595,7 +608,6 @@ constexpr int kP2Producer = 16, kP2Issuer = 17;
 constexpr int kP2Threads = 18 * 32;
 constexpr int kTileKeys = kP2Keys;           // chunks hold whole tiles of both passes
 constexpr float kTcRescale = 8.f;
-constexpr uint32_t kIdS64 = tc::idesc_bf16(128, kP1Keys, 0);
 constexpr uint32_t kIdPV = tc::idesc_bf16(128, kD, 1);
 constexpr uint32_t kId128 = tc::idesc_bf16(128, 128, 0);
 static_assert(kChunkMin % kTileKeys == 0, "chunks hold whole tiles");
@@ -860,20 +872,21 @@ struct P1Bars {
   uint64_t qfull;
   uint64_t kfull[kP1KSt], kempty[kP1KSt];
   uint64_t vfull[kP1VSt], vempty[kP1VSt];
-  uint64_t x_full[kP1Bufs], x_free[kP1Bufs], pv_done[kP1Bufs];
+  uint64_t x_full[kP1Bufs], x_free[kP1Bufs];
 };
 
-// pass 1.  Barriers: x_full[b] S(t) done; x_free[b] the four row warps of
-// tile t's group have read S (and written P); pv_done[b] P V(t) done;
-// kfull / kempty and vfull / vempty the two rings (a V stage also carries
-// the keys' positions).  Issue order: S(0 .. 2), then per tile P V(t),
-// S(t + 3): S(t + 3) reuses the buffer of P(t - 1), which P V(t - 1) read
-// before it in the tensor core's order.
+// pass 1.  Barriers: x_full[b] S(t) done (b = t % 2); x_free[b] the 8 row
+// warps have read S(t) and written P(t); kfull / kempty and vfull / vempty
+// the two rings (a K stage also carries the keys' positions, released by
+// S(t) and the rows; vempty[s] completes once P V(t) and the |v|^2 warps are
+// done with V stage s, which also tells the rows that P V(t) is complete).  Issue order: S(0),
+// then per tile S(t + 1), P V(t): S(t + 1) reuses the buffer of P(t - 1),
+// which P V(t - 1) read before it in the tensor core's order.
 template <bool kWithV>
 __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __grid_constant__ D3Maps mp) {
   extern __shared__ unsigned char d3_dsm[];
   __shared__ __align__(8) P1Bars bar;
-  __shared__ int sh_pos[kP1VSt * kP1Keys];
+  __shared__ int sh_pos[kP1KSt * kP1Keys];
   __shared__ float sh_ml[2][kRowTile][2];
   __shared__ int pf_k[kP1Depth * kP1Keys], pf_v[kP1Depth * kP1Keys], pf_p[kP1Depth * kP1Keys];
   __shared__ uint32_t sh_taddr;
@@ -893,16 +906,15 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
     mbar_init(&bar.qfull, 8);
     for (int s = 0; s < kP1KSt; ++s) {
       mbar_init(&bar.kfull[s], 1);
-      mbar_init(&bar.kempty[s], 1);
+      mbar_init(&bar.kempty[s], 1 + 8);   // S(t) and the 8 row warps (the keys' positions)
     }
     for (int s = 0; s < kP1VSt; ++s) {
       mbar_init(&bar.vfull[s], 1);
-      mbar_init(&bar.vempty[s], kWithV ? 5 : 4);
+      mbar_init(&bar.vempty[s], 1 + kP1VnWarps);   // P V(t) and the |v|^2 warps
     }
     for (int b = 0; b < kP1Bufs; ++b) {
       mbar_init(&bar.x_full[b], 1);
-      mbar_init(&bar.x_free[b], 4);
-      mbar_init(&bar.pv_done[b], 1);
+      mbar_init(&bar.x_free[b], 8);
     }
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
@@ -913,11 +925,12 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
   const size_t lo = static_cast<size_t>(l) * A.dm.cap;
 
   if (warp == kP1KProd) {
-    d3_produce<kP1Keys, kP1KSt, true, false, false, kP1Depth>(A, mp, l, j_begin, j_end, ntiles, skr, bar.kfull,
-                                                              bar.kempty, nullptr, pf_k, nullptr);
+    d3_produce<kP1Keys, kP1KSt, true, false, true, kP1Depth>(A, mp, l, j_begin, j_end, ntiles, skr, bar.kfull,
+                                                             bar.kempty, sh_pos, pf_k, pf_p);
   } else if (warp == kP1VProd) {
-    d3_produce<kP1Keys, kP1VSt, false, kWithV, true, kP1Depth>(A, mp, l, j_begin, j_end, ntiles, svr, bar.vfull,
-                                                               bar.vempty, sh_pos, pf_v, pf_p);
+    if (kWithV)
+      d3_produce<kP1Keys, kP1VSt, false, true, false, kP1Depth>(A, mp, l, j_begin, j_end, ntiles, svr, bar.vfull,
+                                                                bar.vempty, nullptr, pf_v, nullptr);
   } else if (warp == kP1Issuer) {
     if (lane == 0) {
       // descriptors built once; each MMA advances one by a constant
@@ -926,51 +939,87 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
       const uint64_t dv0 = tc::desc_sw128(smem_u32(svr), kP1Keys * 128, 1024);
       (void)mbar_wait_bounded(&bar.qfull, 0, A.ws.status);
       auto issue_s = [&](int u) {
-        const int ks = u % kP1KSt;
-        // without P V, the rows' reading of S(u - 4) is what frees its buffer
-        // (with it, P V(u - 4) read that buffer before S(u) in issue order)
+        const int b = u % kP1Bufs, ks = u % kP1KSt;
+        // without P V, the rows' reading of S(u - 2) is what frees its buffer
+        // (with it, P V(u - 2) read that buffer before S(u) in issue order)
         if (!kWithV && u >= kP1Bufs)
-          (void)mbar_wait_bounded(&bar.x_free[u % kP1Bufs], ((u / kP1Bufs) - 1) & 1, A.ws.status);
+          (void)mbar_wait_bounded(&bar.x_free[b], ((u / kP1Bufs) - 1) & 1, A.ws.status);
         (void)mbar_wait_bounded(&bar.kfull[ks], (u / kP1KSt) & 1, A.ws.status);
         tc::fence_after();
         const uint64_t dk = tc::desc_add(dk0, ks * kP1Tile);
-        const uint32_t dS = tl + 256 + (u % kP1Bufs) * 64;
+        const uint32_t dS = tl + 256 + b * kP1Keys;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-          const int half = kk >> 2, kin = kk & 3;
-          tc::mma_ss(dS, tc::desc_add(dq, half * 16384 + kin * 32),
-                     tc::desc_add(dk, half * (kP1Keys * 128) + kin * 32), kIdS64, kk > 0 ? 1u : 0u);
+          const int off = (kk >> 2) * (kP1Keys * 128) + (kk & 3) * 32;   // d half, 16-element step
+          tc::mma_ss(dS, tc::desc_add(dq, off), tc::desc_add(dk, off), kId128, kk > 0 ? 1u : 0u);
         }
-        tc::commit(&bar.x_full[u % kP1Bufs]);
+        tc::commit(&bar.x_full[b]);
         tc::commit(&bar.kempty[ks]);
       };
-      for (int u = 0; u < min(kP1Ahead, ntiles); ++u) issue_s(u);
+      if (ntiles > 0) issue_s(0);
 #pragma unroll 1
       for (int t = 0; t < ntiles; ++t) {
-        const int b = t % kP1Bufs;
+        if (t + 1 < ntiles) issue_s(t + 1);
         if (kWithV) {
-          const int vs = t % kP1VSt;
+          const int b = t % kP1Bufs, vs = t % kP1VSt;
           (void)mbar_wait_bounded(&bar.x_free[b], (t / kP1Bufs) & 1, A.ws.status);
           (void)mbar_wait_bounded(&bar.vfull[vs], (t / kP1VSt) & 1, A.ws.status);
           tc::fence_after();
           const uint64_t dv = tc::desc_add(dv0, vs * kP1Tile);
-          const uint32_t aP = tl + 256 + b * 64, dO = tl + (t & 1) * 128;
-          const uint32_t acc0 = t >= 2 ? 1u : 0u;
+          const uint32_t aP = tl + 256 + b * kP1Keys;
 #pragma unroll
-          for (int ks = 0; ks < 4; ++ks) {
+          for (int ks = 0; ks < kP1Keys / 16; ++ks) {
+            // keys 16 ks ..: half h = ks / 4 accumulates into O_h; P hi at
+            // column 16 ks of the buffer, lo at 16 ks + 8
+            const int hh = ks >> 2, kin = ks & 3;
+            const uint32_t ac = aP + ks * 16;
             const uint64_t bd = tc::desc_add(dv, ks * 2048);
-            tc::mma_ts(dO, aP + ks * 8, bd, kIdPV, ks > 0 ? 1u : acc0);
-            tc::mma_ts(dO, aP + 32 + ks * 8, bd, kIdPV, 1u);
+            tc::mma_ts(tl + hh * 128, ac, bd, kIdPV, (t > 0 || kin > 0) ? 1u : 0u);
+            tc::mma_ts(tl + hh * 128, ac + 8, bd, kIdPV, 1u);
           }
-          tc::commit(&bar.pv_done[b]);
           tc::commit(&bar.vempty[vs]);
         }
-        if (t + kP1Ahead < ntiles) issue_s(t + kP1Ahead);
+      }
+    }
+  } else if (warp >= kP1VnWarp0) {
+    // |v|^2 of every tile's keys for pass 2 (with two row tiles each CTA
+    // takes half of them), a key per thread (two with one row tile)
+    if (kWithV) {
+      const int vt = tid - kP1VnWarp0 * 32;   // 0 .. 63
+      const int kpc = kP1Keys / nrt;
+#pragma unroll 1
+      for (int t = 0; t < ntiles; ++t) {
+        const int vs = t % kP1VSt;
+        (void)mbar_wait_bounded(&bar.vfull[vs], (t / kP1VSt) & 1, A.ws.status);
+        const unsigned char* vst = svr + vs * kP1Tile;
+#pragma unroll 1
+        for (int key = rt * kpc + vt; key < (rt + 1) * kpc; key += 64) {
+          float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 4
+          for (int c = 0; c < 16; ++c) {
+            const uint4 x = *reinterpret_cast<const uint4*>(vst + sw_off<kP1Keys>(key, c * 8));
+            const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&x);
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+              const float2 f = __bfloat1622float2(pr[u]);
+              acc[(2 * u) & 3] = fmaf(f.x, f.x, acc[(2 * u) & 3]);
+              acc[(2 * u + 1) & 3] = fmaf(f.y, f.y, acc[(2 * u + 1) & 3]);
+            }
+          }
+          const int j = j_begin + t * kP1Keys + key;
+          if (j < j_end) A.ws.d3_vn[lo + j] = (acc[0] + acc[1]) + (acc[2] + acc[3]);
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive1(&bar.vempty[vs]);
       }
     }
   } else {
-    // row warps: group grp = warp / 4 takes tiles t = grp, grp + 2, ...; one row per thread
-    const int grp = warp >> 2, qd = warp & 3;
+    // row warps: warps w and w + 4 share rows 32 (w % 4) .. + 31 (their
+    // tensor-memory lanes); warp w / 4 = h takes keys 64 h .. 64 h + 63 of
+    // every tile with its own running max and sum and its own output
+    // accumulator O_h (columns 128 h ..): the two key halves are two
+    // sub-chunks, merged at the end
+    const int qd = warp & 3, h = warp >> 2;
     const int rr = qd * 32 + lane, r = rt * kRowTile + rr;
     const bool row_ok = r < A.rows;
     const int qp = row_ok ? A.qpos[r % A.w] : -1;
@@ -986,42 +1035,50 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
     if (nrt > 1 && rt == 0)
       for (int j = j_begin + tid; j < j_end; j += 256) A.col_out[lo + j] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
-    const int gt = tid & 127;   // thread within the group
 #pragma unroll 1
-    for (int t = grp; t < ntiles; t += 2) {
-      const int b = t % kP1Bufs, vs = t % kP1VSt;
+    for (int t = 0; t < ntiles; ++t) {
+      const int b = t % kP1Bufs, ks = t % kP1KSt;
       (void)mbar_wait_bounded(&bar.x_full[b], (t / kP1Bufs) & 1, A.ws.status);
-      (void)mbar_wait_bounded(&bar.vfull[vs], (t / kP1VSt) & 1, A.ws.status);   // positions (and V)
+      (void)mbar_wait_bounded(&bar.kfull[ks], (t / kP1KSt) & 1, A.ws.status);   // positions
       tc::fence_after();
-      const int* tpos = sh_pos + vs * kP1Keys;
-      const uint32_t aS = tl + lane_off + 256 + b * 64;
-      float s[kP1Keys];
-      {
-        uint32_t v[4][16];
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4) tc::ld16(aS + q4 * 16, v[q4]);
-        tc::wait_ld();
-#pragma unroll
-        for (int q4 = 0; q4 < 4; ++q4)
-#pragma unroll
-          for (int k = 0; k < 16; ++k) s[q4 * 16 + k] = __uint_as_float(v[q4][k]);
-      }
-      // a full tile whose last (largest) position precedes the row is wholly visible
-      const bool all_vis = row_ok && (t + 1) * kP1Keys <= nkeys && tpos[kP1Keys - 1] <= qp;
-      // the largest raw score (scale2 > 0 keeps the order; the scale is
-      // applied once, and inside the exponent's FMA below); four partial maxima
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-      if (all_vis) {
-#pragma unroll
-        for (int k = 0; k < kP1Keys; ++k) mx[k & 3] = fmaxf(mx[k & 3], s[k]);
-      } else {
-#pragma unroll
-        for (int k = 0; k < kP1Keys; ++k) {
-          const bool ok = row_ok && t * kP1Keys + k < nkeys && tpos[k] <= qp;
-          s[k] = ok ? s[k] : -INFINITY;
-          mx[k & 3] = fmaxf(mx[k & 3], s[k]);
+      const int* tpos = sh_pos + ks * kP1Keys + h * 64;
+      const uint32_t aS = tl + lane_off + 256 + b * kP1Keys + h * 64;
+      // the half's keys the row sees: a prefix (positions ascend), found by
+      // a binary search unless the last one already precedes the row
+      const int k0 = t * kP1Keys + h * 64;   // first key of the half within the chunk
+      int vis = 0;
+      if (row_ok) {
+        const int lim = max(0, min(64, nkeys - k0));
+        if (lim > 0 && tpos[lim - 1] <= qp) {
+          vis = lim;
+        } else {
+          int lo_ = 0, hi_ = lim;
+          while (lo_ < hi_) {
+            const int mid = (lo_ + hi_) >> 1;
+            if (tpos[mid] <= qp) lo_ = mid + 1; else hi_ = mid;
+          }
+          vis = lo_;
         }
       }
+      __syncwarp();
+      if (lane == 0) mbar_arrive1(&bar.kempty[ks]);   // the positions are read
+      // The row loops stay compact (16 keys at a time, not unrolled over the
+      // tile): the kernel's warp roles share the instruction cache, and fully
+      // unrolled code stalled them on instruction fetch.  S is read twice,
+      // for the max and then for P.
+      const bool full = __all_sync(0xffffffffu, vis == 64);   // no key of the half masked for the warp
+      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[16];
+        tc::ld16(aS + c * 16, v);
+        tc::wait_ld();
+        const int vc = full ? 16 : vis - 16 * c;
+#pragma unroll
+        for (int k = 0; k < 16; ++k) mx[k & 3] = fmaxf(mx[k & 3], k < vc ? __uint_as_float(v[k]) : -INFINITY);
+      }
+      // the largest raw score (scale2 > 0 keeps the order; the scale is
+      // applied once, and inside the exponent's FMA below)
       const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * A.scale2;
       float factor = 1.f;
       if (tmax > m_run + kTcRescale) {
@@ -1029,26 +1086,32 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
         m_run = tmax;
         l_run *= factor;
       }
+      const float negm = m_run == -INFINITY ? 0.f : -m_run;
       if (!kWithV) {
-        // S and the positions are read: release the buffer and the stage
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[16];
+          tc::ld16(aS + c * 16, v);
+          tc::wait_ld();
+          const int vc = vis - 16 * c;
+#pragma unroll
+          for (int k = 0; k < 16; ++k)
+            ps[k & 3] += hw_exp2(k < vc ? fmaf(__uint_as_float(v[k]), A.scale2, negm) : -INFINITY);
+        }
+        l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        // S is read: release the buffer
         tc::fence_before();
         __syncwarp();
-        if (lane == 0) {
-          mbar_arrive1(&bar.x_free[b]);
-          mbar_arrive1(&bar.vempty[vs]);
-        }
-        const float negm = m_run == -INFINITY ? 0.f : -m_run;
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int k = 0; k < kP1Keys; ++k) ps[k & 3] += hw_exp2(fmaf(s[k], A.scale2, negm));
-        l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        if (lane == 0) mbar_arrive1(&bar.x_free[b]);
         continue;
       }
-      if (t >= 2 && __any_sync(0xffffffffu, factor != 1.f)) {
-        // P V of the group's previous tile must be complete before O_g is rescaled
-        (void)mbar_wait_bounded(&bar.pv_done[(t - 2) % kP1Bufs], ((t - 2) / kP1Bufs) & 1, A.ws.status);
+      if (t >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
+        // P V(t - 1) must be complete before O_h is rescaled
+        const int tp = t - 1, vp = tp % kP1VSt;
+        (void)mbar_wait_bounded(&bar.vempty[vp], (tp / kP1VSt) & 1, A.ws.status);
         tc::fence_after();
-        const uint32_t aO = tl + lane_off + grp * 128;
+        const uint32_t aO = tl + lane_off + h * 128;
 #pragma unroll 1
         for (int q8 = 0; q8 < 8; ++q8) {
           uint32_t v[16];
@@ -1059,92 +1122,49 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
           tc::st16(aO + q8 * 16, v);
         }
       }
-      // p = 2^(s scale2 - m); a masked key (s = -inf) gives 0, and so does
-      // every key while the row has seen none (m = -inf, offset taken as 0)
-      const float negm = m_run == -INFINITY ? 0.f : -m_run;
+      // p = 2^(s scale2 - m); a key the row does not see gives 0, and so does
+      // every key while the row has seen none (m = -inf, offset taken as 0).
+      // P of the 16 keys of chunk c goes over their own (already read) S
+      // columns: hi in the first 8, lo in the next 8.
       float psum[2] = {0.f, 0.f};
-      uint32_t hi[32], lo2[32];
+      auto p_chunk = [&](int c, auto masked) {
+        uint32_t v[16];
+        tc::ld16(aS + c * 16, v);
+        tc::wait_ld();
+        const int vc = vis - 16 * c;
+        uint32_t hi[8], lo2[8];
 #pragma unroll
-      for (int k2 = 0; k2 < 32; ++k2) {
-        const float p0 = hw_exp2(fmaf(s[2 * k2], A.scale2, negm));
-        const float p1 = hw_exp2(fmaf(s[2 * k2 + 1], A.scale2, negm));
-        psum[k2 & 1] += p0 + p1;
-        split_bf16(p0, p1, hi[k2], lo2[k2]);
+        for (int k2 = 0; k2 < 8; ++k2) {
+          float x0 = fmaf(__uint_as_float(v[2 * k2]), A.scale2, negm);
+          float x1 = fmaf(__uint_as_float(v[2 * k2 + 1]), A.scale2, negm);
+          if (decltype(masked)::value) {
+            x0 = 2 * k2 < vc ? x0 : -INFINITY;
+            x1 = 2 * k2 + 1 < vc ? x1 : -INFINITY;
+          }
+          const float p0 = hw_exp2(x0), p1 = hw_exp2(x1);
+          psum[k2 & 1] += p0 + p1;
+          split_bf16_fast(p0, p1, hi[k2], lo2[k2]);
+        }
+        tc::st8(aS + c * 16, hi);
+        tc::st8(aS + c * 16 + 8, lo2);
+      };
+      if (full) {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) p_chunk(c, std::false_type{});
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) p_chunk(c, std::true_type{});
       }
       l_run += psum[0] + psum[1];
-      {
-        uint32_t v[16];
-#pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = hi[k];
-        tc::st16(aS, v);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = hi[16 + k];
-        tc::st16(aS + 16, v);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = lo2[k];
-        tc::st16(aS + 32, v);
-#pragma unroll
-        for (int k = 0; k < 16; ++k) v[k] = lo2[16 + k];
-        tc::st16(aS + 48, v);
-      }
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive1(&bar.x_free[b]);
-      // |v|^2 of the tile's keys for pass 2 (with two row tiles each CTA
-      // takes half the keys): 2 or 4 threads per key
-      {
-        const unsigned char* vst = svr + vs * kP1Tile;
-        float acc = 0.f;
-        int key;
-        bool lead;
-        if (nrt == 1) {
-          key = gt >> 1;
-          const int part = gt & 1;
-          float acc2 = 0.f;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 x = *reinterpret_cast<const uint4*>(vst + sw_off<kP1Keys>(key, (part * 8 + c) * 8));
-            const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float2 f = __bfloat1622float2(pr[u]);
-              acc = fmaf(f.x, f.x, acc);
-              acc2 = fmaf(f.y, f.y, acc2);
-            }
-          }
-          acc += acc2;
-          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-          lead = part == 0;
-        } else {
-          key = rt * 32 + (gt >> 2);
-          const int part = gt & 3;
-          float acc2 = 0.f;
-#pragma unroll
-          for (int c = 0; c < 4; ++c) {
-            const uint4 x = *reinterpret_cast<const uint4*>(vst + sw_off<kP1Keys>(key, (part * 4 + c) * 8));
-            const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&x);
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const float2 f = __bfloat1622float2(pr[u]);
-              acc = fmaf(f.x, f.x, acc);
-              acc2 = fmaf(f.y, f.y, acc2);
-            }
-          }
-          acc += acc2;
-          acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-          acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-          lead = part == 0;
-        }
-        const int j = j_begin + t * kP1Keys + key;
-        if (lead && j < j_end) A.ws.d3_vn[lo + j] = acc;
-      }
-      __syncwarp();
-      if (lane == 0) mbar_arrive1(&bar.vempty[vs]);
     }
-    // merge the two groups' (max, sum, O) per row, like two chunks
-    sh_ml[grp][rr][0] = m_run;
-    sh_ml[grp][rr][1] = l_run;
+    // merge the two key halves' (max, sum, O) per row, like two chunks;
+    // this thread writes output columns [64 h, 64 h + 64)
+    sh_ml[h][rr][0] = m_run;
+    sh_ml[h][rr][1] = l_run;
     named_sync(1, 256);
     const float m0 = sh_ml[0][rr][0], l0 = sh_ml[0][rr][1], m1 = sh_ml[1][rr][0], l1 = sh_ml[1][rr][1];
     const float M = fmaxf(m0, m1);
@@ -1154,29 +1174,28 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
     float* part = A.ws.d3_part + (static_cast<size_t>(l) * A.chunks + chunk) * static_cast<size_t>(A.rows_cap) * stride +
                   static_cast<size_t>(row_ok ? r : 0) * stride;
     if (kWithV) {
-      // every P V is complete once the last one is (each commit covers all earlier MMAs)
-      (void)mbar_wait_bounded(&bar.pv_done[(ntiles - 1) % kP1Bufs], ((ntiles - 1) / kP1Bufs) & 1, A.ws.status);
+      // every P V is complete once the last one is (its commit covers all earlier MMAs)
+      (void)mbar_wait_bounded(&bar.vempty[(ntiles - 1) % kP1VSt], ((ntiles - 1) / kP1VSt) & 1, A.ws.status);
       tc::fence_after();
-      const bool two = ntiles >= 2;   // O_B holds nothing when the chunk has one tile
 #pragma unroll
       for (int q4 = 0; q4 < 4; ++q4) {
-        const int c0 = grp * 64 + q4 * 16;   // this thread writes columns [64 grp, 64 grp + 64) of its row
+        const int c0 = h * 64 + q4 * 16;
         uint32_t va[16], vb[16];
         tc::ld16(tl + lane_off + c0, va);
-        if (two) tc::ld16(tl + lane_off + 128 + c0, vb);
+        tc::ld16(tl + lane_off + 128 + c0, vb);
         tc::wait_ld();
         if (row_ok) {
 #pragma unroll
           for (int k = 0; k < 16; k += 2) {
             float2 o;
-            o.x = s0 * __uint_as_float(va[k]) + (two ? s1 * __uint_as_float(vb[k]) : 0.f);
-            o.y = s0 * __uint_as_float(va[k + 1]) + (two ? s1 * __uint_as_float(vb[k + 1]) : 0.f);
+            o.x = s0 * __uint_as_float(va[k]) + s1 * __uint_as_float(vb[k]);
+            o.y = s0 * __uint_as_float(va[k + 1]) + s1 * __uint_as_float(vb[k + 1]);
             *reinterpret_cast<float2*>(part + c0 + k) = o;
           }
         }
       }
     }
-    if (row_ok && grp == 0) {
+    if (row_ok && h == 0) {
       part[kD] = M;
       part[kD + 1] = s0 * l0 + s1 * l1;
     }
