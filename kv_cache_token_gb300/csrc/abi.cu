@@ -319,6 +319,9 @@ kvevict_status kvevict_create(const kvevict_config* cfg, const kvevict_buffers* 
   // lane per SM (one lean CTA fits beside the attention kernel's CTAs)
   ctx->c.lean_epi = ok && cfg->policy == KVEVICT_H2O && cfg->kv_dtype == KVEVICT_BF16 && ctx->c.dims.g <= 8 &&
                     ctx->c.dims.lanes <= sms && ctx->c.lean_coresident && kve::lean_epilogue_ctas_per_sm() >= 1;
+  // ring policies: the cluster epilogue when every lane's cluster is resident at once
+  const int rcc = ok && cfg->policy != KVEVICT_H2O ? kve::ring_cluster_ctas() : 0;
+  ctx->c.ring_cluster = rcc > 0 && static_cast<long long>(ctx->c.dims.lanes) * rcc <= sms;
   if (!ok) {
     delete[] ctx->c.tmaps;
     delete[] ctx->c.layer_budget;

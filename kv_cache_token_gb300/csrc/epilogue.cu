@@ -23,8 +23,11 @@
 // kernel, so the epilogue of one layer runs while the next layer streams.
 #include "lane_ops.cuh"
 
+#include <cooperative_groups.h>
+
 namespace kve {
 namespace {
+namespace cg = cooperative_groups;
 
 constexpr int kEpiThreads = 512;
 constexpr int kFastPer = 7;     // tokens per thread on the one-victim H2O path
@@ -69,8 +72,8 @@ __device__ __forceinline__ void copy_row(KT* dst, const KT* src, int d) {
 }
 
 template <typename KT, bool kRing>
-__device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n, unsigned char* dsm,
-                                          int* sh_work, int* sh_gen);
+__device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int l, const int n,
+                                          unsigned char* dsm, int* sh_work, int* sh_gen);
 __device__ void allocate_layer(const LayerState& ls, const Workspace& ws, const Dims& dm, int* sh_scan,
                                int* sh_flag);
 
@@ -217,8 +220,11 @@ __device__ __forceinline__ void piece_to_float<float>(const uint4 w, float* x) {
   x[0] = __uint_as_float(w.x); x[1] = __uint_as_float(w.y); x[2] = __uint_as_float(w.z); x[3] = __uint_as_float(w.w);
 }
 
+// Tokens i_lo .. i_hi - 1: the score goes to ring column rs of the tokens in
+// [own_lo, own_hi) and to row i - i_lo of hrows (if given) for all of them.
 template <typename KT, int CPL>
-__device__ __forceinline__ void dropkv_ring_scores(const EpiArgs& A, const LaneRefs& L, const int n, const float* sh_a,
+__device__ __forceinline__ void dropkv_ring_scores(const EpiArgs& A, const LaneRefs& L, const int i_lo, const int i_hi,
+                                                const int own_lo, const int own_hi, const float* sh_a,
                                                 const float* lg, const float* sh_lse2, const int W, const int rs,
                                                 float* hrows, const int ld) {
   constexpr int kEpc = 16 / static_cast<int>(sizeof(KT));   // elements per 16-byte piece
@@ -232,9 +238,10 @@ __device__ __forceinline__ void dropkv_ring_scores(const EpiArgs& A, const LaneR
   const int rowc = d / kEpc;
   const int nslot = dm.P * kBlock;
   const int stride = ngrp * kU;
-  const int npass = (n + stride - 1) / stride;    // the same for every thread (shuffles below)
+  const int n = i_hi;
+  const int npass = (i_hi - i_lo + stride - 1) / stride;    // the same for every thread (shuffles below)
   for (int ps = 0; ps < npass; ++ps) {
-    const int base = ps * stride + grp;
+    const int base = i_lo + ps * stride + grp;
     uint4 v[kU][CPL];
     int sl[kU];
 #pragma unroll
@@ -327,20 +334,20 @@ __device__ __forceinline__ void dropkv_ring_scores(const EpiArgs& A, const LaneR
       if (u == sub / kTokLanes) s = sl[u];
     const int it = base + (sub / kTokLanes) * ngrp;
     if (sub % kTokLanes == 0 && it < n) {
-      if (s >= 0) L.ring[static_cast<size_t>(s) * W + rs] = sc;
-      if (hrows) hrows[it * ld + rs] = sc;
+      if (s >= 0 && it >= own_lo && it < own_hi) L.ring[static_cast<size_t>(s) * W + rs] = sc;
+      if (hrows) hrows[(it - i_lo) * ld + rs] = sc;
     }
   }
 }
 
-// Marks this lane's epilogue done (thread 0 only).  The per-lane requests
+// Marks this lane's epilogue done (thread 0 only; nsig CTAs signal, one a lane).  The per-lane requests
 // the allocator reads (need_admit, want_dst, plan_tlive, count, released
 // block owners) are written before (by any thread of the CTA, ordered by a
 // barrier before this call); the release makes them visible to the last CTA.  The done counter carries the number of lanes asking for blocks
 // in its upper bits, so the common no-work case needs no further atomic.
-__device__ __forceinline__ void signal_done(const Workspace& ws, bool work, int* sh_last, int* sh_flag) {
+__device__ __forceinline__ void signal_done(const Workspace& ws, bool work, int* sh_last, int* sh_flag, int nsig) {
   const int old = atomic_add_release(ws.epi_done, 1 + (work ? kWorkUnit : 0));
-  *sh_last = (old & (kWorkUnit - 1)) == static_cast<int>(gridDim.x) - 1;
+  *sh_last = (old & (kWorkUnit - 1)) == nsig - 1;
   *sh_flag = (old >> kWorkShift) + (work ? 1 : 0);
 }
 
@@ -765,12 +772,12 @@ __device__ __forceinline__ void apply_claimed(const EpiArgs& A, int* sh_scan, in
 template <typename KT>
 __device__ __forceinline__ void epilogue_tail(const EpiArgs& A, int* sh_scan, int* sh_work, int* sh_last,
                                               int* sh_flag, const int* sh_sig, const int* sh_gen, int* mv_src,
-                                              int* mv_dst) {
+                                              int* mv_dst, int nsig) {
   __shared__ int sh_go;
-  const int l = blockIdx.x, tid = threadIdx.x;
+  const int tid = threadIdx.x;
   __syncthreads();
   if (!*sh_sig) {
-    if (tid == 0) signal_done(A.ws, *sh_work != 0, sh_last, sh_flag);
+    if (tid == 0) signal_done(A.ws, *sh_work != 0, sh_last, sh_flag, nsig);
     __syncthreads();
   }
   if (*sh_last) {
@@ -834,12 +841,13 @@ __global__ void __launch_bounds__(kEpiThreads, 1) decode_epilogue_kernel(EpiArgs
   } else if (!kRing && n + 1 - dm.budget <= 1 && n <= kFastN && dm.g <= 8 && dm.d <= 128 && (dm.d & 1) == 0) {
     h2o_fast_step<KT>(A, L, n, dsm, &sh_sig, &sh_last, &sh_flag, &sh_gen, &sh_work);
   } else {
-    lane_step<KT, kRing>(A, L, n, dsm, &sh_work, &sh_gen);
+    lane_step<KT, kRing>(A, L, l, n, dsm, &sh_work, &sh_gen);
   }
   // the step is done with the dynamic shared memory: the relocation's move
   // lists go there
   int* mv = reinterpret_cast<int*>(dsm);
-  epilogue_tail<KT>(A, sh_scan, &sh_work, &sh_last, &sh_flag, &sh_sig, &sh_gen, mv, mv + kApplyThreads);
+  epilogue_tail<KT>(A, sh_scan, &sh_work, &sh_last, &sh_flag, &sh_sig, &sh_gen, mv, mv + kApplyThreads,
+                    static_cast<int>(gridDim.x));
   scratch_released(A);
 }
 
@@ -1258,27 +1266,124 @@ __global__ void __launch_bounds__(kLeanThreads, 4) decode_epilogue_lean_kernel(E
              (dm.d & 7) == 0) {
     h2o_lean_step<KT>(A, L, n, &sh_sig, &sh_last, &sh_flag, &sh_gen, &sh_work);
   } else {
-    lane_step<KT, false>(A, L, n, nullptr, &sh_work, &sh_gen);
+    lane_step<KT, false>(A, L, l, n, nullptr, &sh_work, &sh_gen);
   }
-  epilogue_tail<KT>(A, sh_scan, &sh_work, &sh_last, &sh_flag, &sh_sig, &sh_gen, sh_mv, sh_mv + kLeanThreads);
+  epilogue_tail<KT>(A, sh_scan, &sh_work, &sh_last, &sh_flag, &sh_sig, &sh_gen, sh_mv, sh_mv + kLeanThreads,
+                    static_cast<int>(gridDim.x));
   scratch_released(A);
 }
 
 // One lane's step after the attention kernel (all threads of the CTA).  dsm
 // (the ring policies' row buffer, kEpiDynSmem bytes) is used only with kRing.
+// The lane's block list, live masks and new K/V row as read before the
+// dependency wait (nothing running writes them), and what the step's single
+// eviction changed since: the victim's slot (its live bit is clear now) and
+// the block it released (-1: none; that block left the list).
+template <typename KT>
+struct LanePrefetch {
+  const int* blocks;
+  const int* masks;
+  int nb;
+  int victim_slot;
+  int dead_blk;
+  const KT* k_new;
+  const KT* v_new;
+};
+
+// After the victims are out (vcount of them; dead: blocks their removal
+// released): admission of the new token into the lowest free slot of the
+// lane's blocks, the table's new tail, the relocation plan and the
+// per-lane requests and statistics (all threads of the CTA owning the lane).
+// pf (optional): the block state and new row read ahead (one victim at most).
+template <typename KT>
+__device__ __forceinline__ void lane_finish(const EpiArgs& A, const LaneRefs& L, const int l, const int n,
+                                            const int k, const int vcount, const int dead, const int nan_count,
+                                            int* sh_work, int* sh_scan, const LanePrefetch<KT>* pf = nullptr) {
+  __shared__ unsigned sh_min[32];
+  __shared__ int sh_nan;
+  const Dims& dm = A.dm;
+  const int tid = threadIdx.x, d = dm.d, W = dm.W;
+  if (tid == 0) sh_nan = 0;
+  const int m = n - vcount;
+  const int nb = (k > 1 && dead > 0) ? lane_prune_blocks(L, l, sh_scan) : *L.nblocks;
+
+  // ---- admission: lowest free slot among the lane's blocks --------------------
+  unsigned best = 0xFFFFFFFFu;
+  if (pf) {
+    for (int j = tid; j < pf->nb; j += blockDim.x) {
+      const int blk = pf->blocks[j];
+      if (blk == pf->dead_blk) continue;
+      int mk = pf->masks[j] & 0xFFFF;
+      if (pf->victim_slot >= 0 && (pf->victim_slot >> 4) == blk) mk &= ~(1 << (pf->victim_slot & 15));
+      if (mk != 0xFFFF) best = min(best, static_cast<unsigned>(blk * kBlock + (__ffs(~mk) - 1)));
+    }
+  } else {
+    for (int j = tid; j < nb; j += blockDim.x) {
+      const int blk = L.blocks[j];
+      const int mk = L.mask[blk] & 0xFFFF;
+      if (mk != 0xFFFF) best = min(best, static_cast<unsigned>(blk * kBlock + (__ffs(~mk) - 1)));
+    }
+  }
+  best = warp_min(best);
+  if ((tid & 31) == 0) sh_min[tid >> 5] = best;
+  __syncthreads();
+  best = 0xFFFFFFFFu;
+  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) best = min(best, sh_min[w]);
+  const bool need = best == 0xFFFFFFFFu;
+  if (!need) {
+    KT* kp = static_cast<KT*>(A.ls.k_pool);
+    KT* vp = static_cast<KT*>(A.ls.v_pool);
+    copy_row(kp + static_cast<size_t>(best) * d,
+             pf ? pf->k_new : static_cast<const KT*>(A.k_new) + static_cast<size_t>(l) * d, d);
+    copy_row(vp + static_cast<size_t>(best) * d,
+             pf ? pf->v_new : static_cast<const KT*>(A.v_new) + static_cast<size_t>(l) * d, d);
+    if (L.ring)
+      for (int t = tid; t < W; t += blockDim.x) L.ring[static_cast<size_t>(best) * W + t] = 0.f;
+    if (tid == 0) atomicOr(&L.mask[best >> 4], 1 << (best & 15));
+  }
+  if (tid == 0) {
+    L.pos[m] = A.new_pos;
+    L.slot[m] = need ? -1 : static_cast<int>(best);
+    if (L.score) L.score[m] = 0.f;
+    A.ls.count[l] = m + 1;
+    if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
+    A.n_victims[l] = vcount;
+  }
+  __syncthreads();
+
+  // ---- relocation plan ---------------------------------------------------------
+  int t_live = 0;
+  const int ndst = lane_plan(L, nb, m + 1, false, dm.theta_f, need, &t_live, sh_scan);
+  if (nan_count) atomicAdd(&sh_nan, nan_count);
+  __syncthreads();
+  const int nan_tot = sh_nan;
+  if (tid == 0) {
+    A.ws.need_admit[l] = need ? 1 : 0;
+    A.ws.want_dst[l] = ndst;
+    A.ws.plan_tlive[l] = t_live;
+    if (need || ndst > 0) {
+      atomicOr(A.ws.work_flag, 1);
+      *sh_work = 1;
+    }
+    atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_VICTIMS]), (unsigned long long)vcount);
+    if (dead) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_FREED_DEAD]), (unsigned long long)dead);
+    if (nan_tot) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_NAN_KEYS]), (unsigned long long)nan_tot);
+    if (l == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_STEPS]), 1ull);
+  }
+}
+
 template <typename KT, bool kRing>
-__device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int n, unsigned char* dsm,
-                                          int* sh_work, int* sh_gen) {
+__device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, const int l, const int n,
+                                          unsigned char* dsm, int* sh_work, int* sh_gen) {
   __shared__ float sh_M[kMaxG], sh_L[kMaxG], sh_lse2[kMaxG];
   __shared__ __align__(16) int sh_hist[256];   // also read as 64-bit words
   __shared__ int sh_misc[40];
   __shared__ int sh_scan[40];
-  __shared__ unsigned sh_min[32];
-  __shared__ int sh_nan, sh_ncand;
+  __shared__ int sh_ncand;
   __shared__ float sh_scale[kMaxSeg][kMaxG];
   float* sh_rows = reinterpret_cast<float*>(dsm);      // general path: 128 * kMaxW floats
   const Dims& dm = A.dm;
-  const int l = blockIdx.x, tid = threadIdx.x;
+  const int tid = threadIdx.x;
   const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d;
   const int cbuf = A.layer % kScratchBufs;
   const int policy = dm.policy;
@@ -1302,7 +1407,7 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
   grid_dep_wait();      // the attention kernel's results are complete and visible
   grid_dep_launch();
   read_generation(A, sh_gen);
-  if (tid == 0) { sh_nan = 0; sh_ncand = 0; }
+  if (tid == 0) sh_ncand = 0;
   if (n > 0 && L.pos[n - 1] >= A.new_pos) {
     if (staged_all) cp_async_wait_all();
     if (tid == 0) {
@@ -1373,8 +1478,8 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
     // this step's residual-output scores straight into ring column rs
     constexpr int kEpc = 16 / static_cast<int>(sizeof(KT));
     float* hr = staged_all ? hrows : nullptr;
-    if (d == 128) dropkv_ring_scores<KT, 128 / kEpc / 8>(A, L, n, sh_rows, lg, sh_lse2, W, rs, hr, ld);
-    else dropkv_ring_scores<KT, 64 / kEpc / 8>(A, L, n, sh_rows, lg, sh_lse2, W, rs, hr, ld);
+    if (d == 128) dropkv_ring_scores<KT, 128 / kEpc / 8>(A, L, 0, n, 0, n, sh_rows, lg, sh_lse2, W, rs, hr, ld);
+    else dropkv_ring_scores<KT, 64 / kEpc / 8>(A, L, 0, n, 0, n, sh_rows, lg, sh_lse2, W, rs, hr, ld);
     __syncthreads();
   }
   int lw = 0;
@@ -1537,60 +1642,468 @@ __device__ __forceinline__ void lane_step(const EpiArgs& A, const LaneRefs& L, c
       vcount = lane_remove(L, n, plain_victims(isv), vout, nullptr, &dead, dm.P, A.ws.status, sh_scan);
     }
   }
-  const int m = n - vcount;
-  const int nb = (k > 1 && dead > 0) ? lane_prune_blocks(L, l, sh_scan) : *L.nblocks;
+  lane_finish<KT>(A, L, l, n, k, vcount, dead, nan_count, sh_work, sh_scan);
+}
 
-  // ---- admission: lowest free slot among the lane's blocks --------------------
-  unsigned best = 0xFFFFFFFFu;
-  for (int j = tid; j < nb; j += blockDim.x) {
-    const int blk = L.blocks[j];
-    const int mk = L.mask[blk] & 0xFFFF;
-    if (mk != 0xFFFF) best = min(best, static_cast<unsigned>(blk * kBlock + (__ffs(~mk) - 1)));
-  }
-  best = warp_min(best);
-  if ((tid & 31) == 0) sh_min[tid >> 5] = best;
-  __syncthreads();
-  best = 0xFFFFFFFFu;
-  for (int w = 0; w < (int)(blockDim.x >> 5); ++w) best = min(best, sh_min[w]);
-  const bool need = best == 0xFFFFFFFFu;
-  if (!need) {
-    KT* kp = static_cast<KT*>(A.ls.k_pool);
-    KT* vp = static_cast<KT*>(A.ls.v_pool);
-    copy_row(kp + static_cast<size_t>(best) * d, static_cast<const KT*>(A.k_new) + static_cast<size_t>(l) * d, d);
-    copy_row(vp + static_cast<size_t>(best) * d, static_cast<const KT*>(A.v_new) + static_cast<size_t>(l) * d, d);
-    if (L.ring)
-      for (int t = tid; t < W; t += blockDim.x) L.ring[static_cast<size_t>(best) * W + t] = 0.f;
-    if (tid == 0) atomicOr(&L.mask[best >> 4], 1 << (best & 15));
-  }
-  if (tid == 0) {
-    L.pos[m] = A.new_pos;
-    L.slot[m] = need ? -1 : static_cast<int>(best);
-    if (L.score) L.score[m] = 0.f;
-    A.ls.count[l] = m + 1;
-    if (m + 1 >= dm.cap) set_status(A.ws.status, ST_CAPACITY);
-    A.n_victims[l] = vcount;
-  }
-  __syncthreads();
+// ---------------------------------------------------------------------------
+// Ring policies (SnapKV, DropKV decode variant) with one lane per cluster of
+// kRingCluster CTAs, each owning a quarter of the lane's tokens: the lane's
+// step has few lanes to spread over the GPU otherwise (one CTA a lane left
+// most SMs idle).  Before the dependency wait each rank stages the history
+// rows of its tokens and of a pooling halo (pool radius on each side).
+// After it: every rank derives the heads' log-sum-exp; each combines a
+// quarter of the split-K outputs (the DropKV scores need all of them: the
+// ranks read one another's quarter from distributed shared memory); each
+// scores and keys its range, writing the ring's new column only for the
+// tokens it owns; each pools and takes the minimum candidate over the
+// tokens it owns, and the lane's minimum is the smallest (key, index) over
+// the ranks.  The table shift after the victim is split over the ranks
+// (every read before a cluster barrier, the writes after it).  Rank 0 then
+// does the rest (the victim's live bit, admission, the relocation plan, the
+// per-lane requests).  Several victims (k > 1): the ranks publish their
+// pooled keys and rank 0 selects and removes them.
+// ---------------------------------------------------------------------------
+constexpr int kRingCluster = 4;
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
-  // ---- relocation plan ---------------------------------------------------------
-  int t_live = 0;
-  const int ndst = lane_plan(L, nb, m + 1, false, dm.theta_f, need, &t_live, sh_scan);
-  if (nan_count) atomicAdd(&sh_nan, nan_count);
+// History rows of tokens lo .. hi - 1 to rows[(i - lo) * ld + t] (W a
+// multiple of 4), as stage_history_async; their raw slots and positions to
+// sh_slot and sh_pos (hi - lo ints each).
+__device__ __forceinline__ void stage_history_range_async(const LaneRefs& L, const int lo, const int hi, const int W,
+                                                          const int ld, const int nslot, float* rows, int* sh_slot,
+                                                          int* sh_pos) {
+  for (int i = lo + threadIdx.x; i < hi; i += blockDim.x) {
+    sh_slot[i - lo] = L.slot[i];
+    sh_pos[i - lo] = L.pos[i];
+  }
   __syncthreads();
-  const int nan_tot = sh_nan;
-  if (tid == 0) {
-    A.ws.need_admit[l] = need ? 1 : 0;
-    A.ws.want_dst[l] = ndst;
-    A.ws.plan_tlive[l] = t_live;
-    if (need || ndst > 0) {
-      atomicOr(A.ws.work_flag, 1);
-      *sh_work = 1;
+  const int pr = W / 4;
+  for (int e = threadIdx.x; e < (hi - lo) * pr; e += blockDim.x) {
+    const int i = e / pr, c = (e - i * pr) * 4;
+    const int s = sh_slot[i] >= 0 && sh_slot[i] < nslot ? sh_slot[i] : -1;
+    float* dst = rows + i * ld + c;
+    if (s >= 0) {
+      asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)),
+                   "l"(L.ring + static_cast<size_t>(s) * W + c) : "memory");
+    } else {
+      *reinterpret_cast<float4*>(dst) = make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_VICTIMS]), (unsigned long long)vcount);
-    if (dead) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_FREED_DEAD]), (unsigned long long)dead);
-    if (nan_tot) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_NAN_KEYS]), (unsigned long long)nan_tot);
-    if (l == 0) atomicAdd(reinterpret_cast<unsigned long long*>(&A.ls.stats[SC_STEPS]), 1ull);
   }
+  cp_async_commit();
+}
+
+// Layout of the dynamic shared memory of one rank: the heads' outputs, the
+// staged rows, their slots, the keys.  Returns the bytes needed (the caller
+// checks them against kEpiDynSmem).
+constexpr int kPfBlocks = kEpiThreads;   // block list entries rank 0 reads ahead (more: read at admission)
+struct RingClusterSmem {
+  float* sh_a;
+  float* rows;
+  int* slots;        // raw slots of tokens lo .. hi - 1
+  int* pos;          // their positions
+  unsigned long long* keys;
+  int* pf_blocks;    // rank 0: the lane's block list and live masks, the new K/V row
+  int* pf_masks;
+  unsigned char* pf_row;
+  size_t bytes;
+};
+__device__ __forceinline__ size_t ring_cluster_bytes(int span, int ld) {
+  size_t off = static_cast<size_t>(kMaxG) * 128 * 4 + static_cast<size_t>(span) * ld * 4;
+  off += 2 * ((static_cast<size_t>(span) * 4 + 7) & ~static_cast<size_t>(7));
+  off += static_cast<size_t>(span + 1) * 8;
+  off += 2 * static_cast<size_t>(kPfBlocks) * 4 + 2 * 128 * 4;
+  return off;
+}
+__device__ __forceinline__ RingClusterSmem ring_cluster_smem(unsigned char* dsm, int span, int ld) {
+  RingClusterSmem m;
+  size_t off = 0;
+  m.sh_a = reinterpret_cast<float*>(dsm + off);
+  off += static_cast<size_t>(kMaxG) * 128 * 4;
+  m.rows = reinterpret_cast<float*>(dsm + off);
+  off += static_cast<size_t>(span) * ld * 4;
+  m.slots = reinterpret_cast<int*>(dsm + off);
+  off += (static_cast<size_t>(span) * 4 + 7) & ~static_cast<size_t>(7);
+  m.pos = reinterpret_cast<int*>(dsm + off);
+  off += (static_cast<size_t>(span) * 4 + 7) & ~static_cast<size_t>(7);
+  m.keys = reinterpret_cast<unsigned long long*>(dsm + off);
+  off += static_cast<size_t>(span + 1) * 8;
+  m.pf_blocks = reinterpret_cast<int*>(dsm + off);
+  off += static_cast<size_t>(kPfBlocks) * 4;
+  m.pf_masks = reinterpret_cast<int*>(dsm + off);
+  off += static_cast<size_t>(kPfBlocks) * 4;
+  m.pf_row = dsm + off;
+  off += 2 * 128 * 4;
+  m.bytes = off;
+  return m;
+}
+
+// The largest range (owned tokens and halo) any rank of a lane of n tokens
+// stages, and whether the cluster step applies (every rank's owned tokens
+// within one pass of the CTA's threads, W a multiple of 4, the staging in
+// shared memory).  The same answer on every rank.
+__device__ __forceinline__ bool ring_cluster_fits(const Dims& dm, const int n) {
+  const int R = (dm.pool_kernel - 1) / 2;
+  const int own = (n + kRingCluster - 1) / kRingCluster;
+  const int span = own + 2 * R;
+  const int ld = ((dm.W + 27) / 32) * 32 + 4;
+  const size_t bytes = ring_cluster_bytes(span, ld);
+  return n > 0 && (dm.W & 3) == 0 && own <= kEpiThreads && dm.g <= kMaxG && dm.d <= 128 && bytes <= kEpiDynSmem;
+}
+
+template <typename KT>
+__device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRefs& L, const int l, const int rank,
+                                                  const int n, unsigned char* dsm, int* sh_work, int* sh_gen) {
+  __shared__ float sh_L[kMaxG], sh_lse2[kMaxG];
+  __shared__ float sh_scale[kMaxSeg][kMaxG];
+  __shared__ __align__(16) int sh_hist[256];
+  __shared__ int sh_misc[40];
+  __shared__ int sh_scan[40];
+  __shared__ unsigned long long sh_bk;   // this rank's minimum candidate key, and its index (-1: none)
+  __shared__ int sh_bi, sh_nanr;
+  __shared__ int sh_vslot, sh_dead;     // rank 0: the victim's raw slot and the block it released (from its owner)
+  __shared__ int sh_pfnb;
+  cg::cluster_group cluster = cg::this_cluster();
+  const Dims& dm = A.dm;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int b = l / dm.Hkv, kh = l % dm.Hkv, g = dm.g, d = dm.d, W = dm.W;
+  const int cbuf = A.layer % kScratchBufs;
+  const int policy = dm.policy;
+  const int R = (dm.pool_kernel - 1) / 2;
+  const int i0 = (n * rank) / kRingCluster, i1 = (n * (rank + 1)) / kRingCluster;   // owned tokens
+  const int lo = max(0, i0 - R), hi = min(n, i1 + R);                              // with the halo
+  const int ld = ((W + 27) / 32) * 32 + 4;
+  const RingClusterSmem sm = ring_cluster_smem(dsm, hi - lo, ld);
+
+  // ---- before the dependency wait: history rows, slots and positions of the
+  // range; rank 0 also the lane's block list with its live masks and the new
+  // token's K/V row (none of which the attention kernel writes)
+  if (tid == 0) { sh_vslot = -1; sh_dead = -1; }
+  const int rs = A.ls.ring_slot[l];   // written by this layer's previous epilogue only
+  stage_history_range_async(L, lo, hi, W, ld, dm.P * kBlock, sm.rows, sm.slots, sm.pos);
+  if (rank == 0) {
+    const int nb0 = *L.nblocks;
+    if (tid == 0) sh_pfnb = nb0;
+    if (nb0 <= kPfBlocks) {
+      for (int j = tid; j < nb0; j += blockDim.x) {
+        const int blk = L.blocks[j];
+        sm.pf_blocks[j] = blk;
+        sm.pf_masks[j] = L.mask[blk];
+      }
+    }
+    // element by element: the new rows carry no alignment promise
+    KT* row = reinterpret_cast<KT*>(sm.pf_row);
+    for (int e = tid; e < 2 * d; e += blockDim.x)
+      row[e] = e < d ? static_cast<const KT*>(A.k_new)[static_cast<size_t>(l) * d + e]
+                     : static_cast<const KT*>(A.v_new)[static_cast<size_t>(l) * d + e - d];
+  }
+  grid_dep_wait();      // the attention kernel's results are complete and visible
+  grid_dep_launch();
+  if (rank == 0) read_generation(A, sh_gen);
+  if (tid == 0) { sh_bi = -1; sh_bk = ~0ull; sh_nanr = 0; }
+  if (L.pos[n - 1] >= A.new_pos) {
+    cp_async_wait_all();
+    if (rank == 0 && tid == 0) {
+      set_status(A.ws.status, ST_POSITION);
+      A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
+    }
+    return;
+  }
+
+  // ---- combine the split-K partials: a quarter of the outputs per rank -----------
+  if (A.has_q) {
+    const int nseg = min(A.ws.lane_nseg_buf[cbuf][l], kMaxSeg);
+    const float2* ml = reinterpret_cast<const float2*>(A.ws.part_ml_buf[cbuf]) + static_cast<size_t>(l) * kMaxSeg * g;
+    if (warp < g) {
+      const int h = warp;
+      const float2 v0 = lane < nseg ? ml[lane * g + h] : make_float2(-INFINITY, 0.f);
+      const float2 v1 = lane + 32 < nseg ? ml[(lane + 32) * g + h] : make_float2(-INFINITY, 0.f);
+      const float M = warp_max(fmaxf(v0.x, v1.x));
+      const float s0 = v0.x == -INFINITY ? 0.f : exp2f(v0.x - M);
+      const float s1 = v1.x == -INFINITY ? 0.f : exp2f(v1.x - M);
+      if (lane < nseg) sh_scale[lane][h] = s0;
+      if (lane + 32 < nseg) sh_scale[lane + 32][h] = s1;
+      float Ls = v0.y * s0 + v1.y * s1;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+      if (lane == 0) {
+        sh_L[h] = Ls;
+        const float lse2 = M + log2f(Ls);
+        sh_lse2[h] = lse2;
+        if (rank == 0) A.lse[static_cast<size_t>(b) * dm.Hq + kh * g + h] = lse2 * kLn2;
+      }
+    }
+    __syncthreads();
+    const int ghd = g * d, per = (ghd + kRingCluster - 1) / kRingCluster;
+    const float* po = A.ws.part_o_buf[cbuf] + static_cast<size_t>(l) * kMaxSeg * g * d;
+    // four threads per output, each a quarter of the segments (fewer loads in
+    // a chain), their sums added by two shuffles
+    const int e0 = rank * per, cnt = max(0, min(ghd, e0 + per) - e0);
+    for (int base = 0; base < 4 * cnt; base += blockDim.x) {
+      const int x = base + tid, q = x & 3;
+      const bool act = x < 4 * cnt;
+      const int he = e0 + (x >> 2);
+      const int h = act ? he / d : 0, e = act ? he - h * d : 0;
+      float acc = 0.f;
+      if (act) {
+#pragma unroll 4
+        for (int s = q; s < nseg; s += 4) acc = fmaf(po[(static_cast<size_t>(s) * g + h) * d + e], sh_scale[s][h], acc);
+      }
+      acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+      acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+      if (act && q == 0) {
+        const float o = acc / sh_L[h];
+        A.out[(static_cast<size_t>(b) * dm.Hq + kh * g + h) * d + e] = o;
+        sm.sh_a[he] = o;
+      }
+    }
+    if (policy == KVEVICT_DROPKV) {
+      cluster.sync();   // every rank's quarter of the outputs is in its shared memory
+      for (int rr = 0; rr < kRingCluster; ++rr) {
+        if (rr == rank) continue;
+        const float* ra = cluster.map_shared_rank(sm.sh_a, rr);
+        for (int he = rr * per + tid; he < min(ghd, (rr + 1) * per); he += blockDim.x) sm.sh_a[he] = ra[he];
+      }
+    }
+    __syncthreads();
+  }
+
+  // ---- scores of this step into the ring, window-sum keys of lo .. hi - 1 --------
+  cp_async_wait_all();
+  __syncthreads();
+  const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
+  const int k = max(0, n + 1 - dm.budget);
+  const int cut = A.new_pos - dm.R + 1;
+  if (policy == KVEVICT_DROPKV && A.has_q) {
+    constexpr int kEpc = 16 / static_cast<int>(sizeof(KT));
+    if (d == 128) dropkv_ring_scores<KT, 128 / kEpc / 8>(A, L, lo, hi, i0, i1, sm.sh_a, lg, sh_lse2, W, rs, sm.rows, ld);
+    else dropkv_ring_scores<KT, 64 / kEpc / 8>(A, L, lo, hi, i0, i1, sm.sh_a, lg, sh_lse2, W, rs, sm.rows, ld);
+    __syncthreads();
+  }
+  int lw = 0;
+  while ((1 << lw) < W) ++lw;
+  const int spread = 29 - lw;    // exact-sum bound: spread + 24 + log2(W) <= 53
+  const bool fresh = A.has_q && policy == KVEVICT_SNAPKV;
+  int nan_count = 0;
+  for (int i = lo + tid; i < hi; i += blockDim.x) {
+    float* row = sm.rows + (i - lo) * ld;
+    const bool own = i >= i0 && i < i1;
+    if (fresh) {
+      float w = 0.f;
+      for (int h = 0; h < g; ++h) w += exp2f(lg[static_cast<size_t>(h) * dm.lcap + i] - sh_lse2[h]);
+      row[rs] = w;
+      if (own) {
+        const int s = sm.slots[i - lo];
+        if (s >= 0 && s < dm.P * kBlock) L.ring[static_cast<size_t>(s) * W + rs] = w;
+        else set_status(A.ws.status, ST_BAD_INDEX);
+      }
+    }
+    const unsigned long long key = W == 32 ? window_key4<32>(row, 32, spread) : window_key4<0>(row, W, spread);
+    sm.keys[i - lo] = key;
+    if (own && key == ~0ull) ++nan_count;
+  }
+  if (tid == 0 && hi == n) sm.keys[n - lo] = kKeyZero;     // the new token's sum
+  if (nan_count) atomicAdd(&sh_nanr, nan_count);
+  __syncthreads();
+
+  // ---- max-pool over kept neighbours, minimum candidate of the owned tokens -------
+  unsigned long long* pooled = A.ws.pooled64 ? A.ws.pooled64 + static_cast<size_t>(l) * dm.cap : nullptr;
+  unsigned long long best_k = ~0ull;
+  uint32_t best_p = 0xFFFFFFFFu;
+  int best_i = -1;
+  for (int j = i0 + tid; j < i1; j += blockDim.x) {
+    unsigned long long m = 0;
+    const int qa = max(0, j - R), qb = min(n, j + R);
+    for (int q = qa; q <= qb; ++q) m = max(m, sm.keys[q - lo]);
+    if (k > 1) pooled[j] = m;
+    if (k == 1 && sm.pos[j - lo] < cut && (m < best_k || (m == best_k && static_cast<uint32_t>(j) < best_p))) {
+      best_k = m; best_p = static_cast<uint32_t>(j); best_i = j;
+    }
+  }
+  int vcount = 0, dead = 0;
+  int32_t* vout = A.victims + static_cast<size_t>(l) * dm.cap;
+  if (k == 1) {
+    const int v_local = block_argmin3(best_k, best_p, best_i, sh_hist, sh_misc);
+    if (tid == 0 && v_local >= 0) {
+      unsigned long long m = 0;
+      const int qa = max(0, v_local - R), qb = min(n, v_local + R);
+      for (int q = qa; q <= qb; ++q) m = max(m, sm.keys[q - lo]);
+      sh_bk = m;
+      sh_bi = v_local;
+    }
+    cluster.sync();   // every rank's minimum and NaN count is in its shared memory
+    unsigned long long gk = ~0ull;
+    int v = -1, vr = 0;
+    for (int rr = 0; rr < kRingCluster; ++rr) {
+      const int ri = *cluster.map_shared_rank(&sh_bi, rr);
+      const unsigned long long rk = *cluster.map_shared_rank(&sh_bk, rr);
+      if (ri >= 0 && (v < 0 || rk < gk || (rk == gk && ri < v))) { gk = rk; v = ri; vr = rr; }
+    }
+    int nan_all = 0;
+    if (rank == 0 && tid == 0)
+      for (int rr = 0; rr < kRingCluster; ++rr) nan_all += *cluster.map_shared_rank(&sh_nanr, rr);
+    if (v >= 0) {
+      // rank 0 takes the victim's slot and position from the rank owning it;
+      // every rank reads the entries it moves down one place
+      if (rank == 0 && tid == 0) {
+        // the owner's layout: its arrays' offsets depend on its span
+        const int olo = max(0, (n * vr) / kRingCluster - R), ohi = min(n, (n * (vr + 1)) / kRingCluster + R);
+        const RingClusterSmem osm = ring_cluster_smem(dsm, ohi - olo, ld);
+        sh_vslot = cluster.map_shared_rank(osm.slots, vr)[v - olo];
+        vout[0] = cluster.map_shared_rank(osm.pos, vr)[v - olo];
+      }
+      const int i = max(i0, v + 1) + tid;
+      const bool mv = i < i1;
+      int p = 0, s = 0;
+      float sc = 0.f;
+      if (mv) {
+        p = sm.pos[i - lo];
+        s = sm.slots[i - lo];
+        if (L.score) sc = L.score[i];
+      }
+      cluster.sync();   // every read is done: no rank touches another's shared memory after this
+      if (mv) {
+        L.pos[i - 1] = p;
+        L.slot[i - 1] = s;
+        if (L.score) L.score[i - 1] = sc;
+      }
+      vcount = 1;
+      if (rank == 0) {
+        // the victim's live bit (an emptied block is released and leaves the
+        // list), from the live masks read ahead when the list fitted
+        const int vs = sh_vslot;
+        if (vs >= 0 && vs < dm.P * kBlock) {
+          const int blk = vs >> 4, bit = 1 << (vs & 15);
+          if (sh_pfnb <= kPfBlocks) {
+            for (int j = tid; j < sh_pfnb; j += blockDim.x) {
+              if (sm.pf_blocks[j] == blk) {
+                const int old = sm.pf_masks[j];
+                atomicAnd(&L.mask[blk], ~bit);
+                if ((old & ~bit) == 0 && (old & bit)) {
+                  L.owner[blk] = -1;
+                  sh_dead = blk;
+                }
+              }
+            }
+          } else if (tid == 0) {
+            const int old = atomicAnd(&L.mask[blk], ~bit);
+            if ((old & ~bit) == 0 && (old & bit)) {
+              L.owner[blk] = -1;
+              sh_dead = blk;
+            }
+          }
+        } else if (vs >= 0 && tid == 0) {
+          set_status(A.ws.status, ST_BAD_INDEX);
+        }
+        __syncthreads();
+        const int dead_blk = sh_dead;
+        if (dead_blk >= 0) {
+          const int nb = *L.nblocks;
+          for (int j = tid; j < nb; j += blockDim.x) {
+            if (L.blocks[j] == dead_blk) {
+              L.blocks[j] = L.blocks[nb - 1];
+              *L.nblocks = nb - 1;
+            }
+          }
+          dead = 1;
+        }
+        __syncthreads();
+      }
+    } else {
+      cluster.sync();   // no rank touches another's shared memory after this
+    }
+    // the table writes of every rank are done before rank 0 signals for the
+    // lane (arrive here, wait before the signal)
+    cluster_arrive();
+    if (rank != 0) {
+      cluster_wait();
+      return;
+    }
+    if (A.has_q && tid == 0) A.ls.ring_slot[l] = (rs + 1) % W;
+    LanePrefetch<KT> pf;
+    pf.blocks = sm.pf_blocks;
+    pf.masks = sm.pf_masks;
+    pf.nb = sh_pfnb;
+    pf.victim_slot = vcount == 1 ? sh_vslot : -1;
+    pf.dead_blk = vcount == 1 ? sh_dead : -1;
+    pf.k_new = reinterpret_cast<const KT*>(sm.pf_row);
+    pf.v_new = reinterpret_cast<const KT*>(sm.pf_row) + d;
+    lane_finish<KT>(A, L, l, n, k, vcount, dead, nan_all, sh_work, sh_scan,
+                    sh_pfnb <= kPfBlocks ? &pf : nullptr);
+    cluster_wait();
+    return;
+  } else if (k > 1) {
+    cluster.sync();   // every rank's pooled keys are written
+    if (rank == 0) {
+      auto candf = [&](int i) { return L.pos[i] < cut; };
+      auto posf = [&](int i) { return static_cast<uint32_t>(L.pos[i]); };
+      auto keyf = [&](int i) { return pooled[i]; };
+      const SelectResult sel = block_bottom_k(n, k, 64, keyf, posf, candf, sh_hist, sh_misc);
+      auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
+      vcount = lane_remove(L, n, plain_victims(isv), vout, nullptr, &dead, dm.P, A.ws.status, sh_scan);
+    }
+  }
+  // the ranks' NaN counts (final once a cluster barrier followed the keys:
+  // the selection's, or one here); nothing reads another rank's shared
+  // memory after the last barrier
+  if (k == 0) cluster.sync();
+  int nan_tot = 0;
+  if (rank == 0 && tid == 0)
+    for (int rr = 0; rr < kRingCluster; ++rr) nan_tot += *cluster.map_shared_rank(&sh_nanr, rr);
+  cluster.sync();
+  if (rank != 0) return;
+  if (A.has_q && tid == 0) A.ls.ring_slot[l] = (rs + 1) % W;
+  // admission from the block state read ahead when at most one token left
+  // (its live bit and released block known) and the list fitted
+  LanePrefetch<KT> pf;
+  pf.blocks = sm.pf_blocks;
+  pf.masks = sm.pf_masks;
+  pf.nb = sh_pfnb;
+  pf.victim_slot = vcount == 1 ? sh_vslot : -1;
+  pf.dead_blk = vcount == 1 ? sh_dead : -1;
+  pf.k_new = reinterpret_cast<const KT*>(sm.pf_row);
+  pf.v_new = reinterpret_cast<const KT*>(sm.pf_row) + d;
+  const bool use_pf = k <= 1 && sh_pfnb <= kPfBlocks;
+  lane_finish<KT>(A, L, l, n, k, vcount, dead, nan_tot, sh_work, sh_scan, use_pf ? &pf : nullptr);
+}
+
+template <typename KT>
+__global__ void __cluster_dims__(kRingCluster, 1, 1) __launch_bounds__(kEpiThreads, 1)
+    decode_epilogue_ring_cluster_kernel(EpiArgs A) {
+  extern __shared__ __align__(128) unsigned char dsm[];
+  __shared__ int sh_scan[40];
+  __shared__ int sh_work, sh_last, sh_flag, sh_sig, sh_gen;
+  const Dims& dm = A.dm;
+  const int rank = static_cast<int>(cg::this_cluster().block_rank());
+  const int l = blockIdx.x / kRingCluster, tid = threadIdx.x;
+  LaneRefs L = lane_refs(A.ls, dm, l);
+  const int n = __ldcg(A.ls.count + l);
+  if (tid == 0) { sh_work = 0; sh_sig = 0; sh_gen = 0; }
+  if (n < 0 || n >= dm.cap) {
+    grid_dep_wait();
+    grid_dep_launch();
+    if (rank == 0) {
+      read_generation(A, &sh_gen);
+      if (tid == 0) {
+        set_status(A.ws.status, ST_CAPACITY);
+        A.n_victims[l] = 0; A.ws.need_admit[l] = 0; A.ws.want_dst[l] = 0; A.ws.plan_tlive[l] = 0;
+      }
+    }
+  } else if (ring_cluster_fits(dm, n)) {
+    lane_step_cluster<KT>(A, L, l, rank, n, dsm, &sh_work, &sh_gen);
+  } else if (rank == 0) {
+    lane_step<KT, true>(A, L, l, n, dsm, &sh_work, &sh_gen);
+  } else {
+    grid_dep_wait();
+    grid_dep_launch();
+  }
+  if (rank != 0) return;
+  // rank 0 signals for the lane (the others are done with the scratch copy:
+  // the step's last cluster barrier follows their last read)
+  int* mv = reinterpret_cast<int*>(dsm);
+  epilogue_tail<KT>(A, sh_scan, &sh_work, &sh_last, &sh_flag, &sh_sig, &sh_gen, mv, mv + kApplyThreads,
+                    static_cast<int>(gridDim.x) / kRingCluster);
+  scratch_released(A);
 }
 
 // ---------------------------------------------------------------------------
@@ -1893,6 +2406,12 @@ cudaError_t launch_epilogue(const Ctx& ctx, int layer, bool has_q, int new_pos, 
   if (lean)   // bf16 pools only (see kvevict_create)
     return launch_k(decode_epilogue_lean_kernel<__nv_bfloat16>, grid, dim3(kLeanThreads), 0, stream, pdl, A);
   const dim3 block(kEpiThreads);
+  if (ring && ctx.ring_cluster) {
+    const dim3 cgrid(ctx.dims.lanes * kRingCluster);
+    if (ctx.dims.dtype == KVEVICT_BF16)
+      return launch_k(decode_epilogue_ring_cluster_kernel<__nv_bfloat16>, cgrid, block, kEpiDynSmem, stream, pdl, A);
+    return launch_k(decode_epilogue_ring_cluster_kernel<float>, cgrid, block, kEpiDynSmem, stream, pdl, A);
+  }
   if (ctx.dims.dtype == KVEVICT_BF16)
     return ring ? launch_k(decode_epilogue_kernel<__nv_bfloat16, true>, grid, block, kEpiDynSmem, stream, pdl, A)
                 : launch_k(decode_epilogue_kernel<__nv_bfloat16, false>, grid, block, kEpiDynSmem, stream, pdl, A);
@@ -1907,6 +2426,8 @@ cudaError_t prepare_epilogue() {
   if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_kernel<__nv_bfloat16, true>, a, bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_kernel<float, false>, a, bytes);
   if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_kernel<float, true>, a, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_ring_cluster_kernel<__nv_bfloat16>, a, bytes);
+  if (e == cudaSuccess) e = cudaFuncSetAttribute(decode_epilogue_ring_cluster_kernel<float>, a, bytes);
   // the lean kernel shares SMs with the attention kernel, which needs the
   // largest shared-memory carveout: ask for the same one
   const cudaFuncAttribute c = cudaFuncAttributePreferredSharedMemoryCarveout;
@@ -1928,6 +2449,16 @@ int epilogue_ctas_per_sm() {
   take(decode_epilogue_kernel<float, false>);
   take(decode_epilogue_kernel<float, true>);
   return best;
+}
+
+// kRingCluster when a cluster of the ring epilogue can be resident (one
+// CTA per SM of a cluster), else 0.
+int ring_cluster_ctas() {
+  int n = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_epilogue_ring_cluster_kernel<__nv_bfloat16>,
+                                                    kEpiThreads, kEpiDynSmem) != cudaSuccess)
+    return 0;
+  return n >= 1 ? kRingCluster : 0;
 }
 
 cudaError_t lean_epilogue_attributes(cudaFuncAttributes* a, int* threads) {

@@ -143,6 +143,9 @@ struct Ctx {
   // The lean H2O epilogue (one small CTA per lane, beside the attention
   // kernel's CTAs) can serve this configuration.
   bool lean_epi;
+  // Ring policies: a cluster of four CTAs per lane runs the lane's step (all
+  // of them resident at once, one per SM).
+  bool ring_cluster;
   // Per layer [L] (host): every lane of the layer holds at most its budget,
   // so a decode step evicts at most one token per lane and the lean
   // epilogue is the right kernel.  A performance hint only: both epilogue
@@ -214,6 +217,7 @@ cudaError_t launch_attend_into(const Ctx&, int layer, const void* q, const void*
 cudaError_t prepare_epilogue();     // one-time attributes of the epilogue kernels
 int epilogue_ctas_per_sm();         // co-resident decode-epilogue CTAs per SM (the large kernel)
 int lean_epilogue_ctas_per_sm();    // the same for the lean H2O epilogue
+int ring_cluster_ctas();             // CTAs of a ring policy's cluster epilogue per lane (0: unavailable)
 cudaError_t lean_epilogue_attributes(cudaFuncAttributes*, int* threads);
 cudaError_t prepare_select();       // one-time attributes of the selection kernels
 cudaError_t prepare_dropkv();       // one-time attributes of the window-scoring kernels
