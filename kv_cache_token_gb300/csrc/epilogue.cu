@@ -203,6 +203,58 @@ __device__ __forceinline__ unsigned long long window_key4(const float* row, cons
   return mono_key(sum);
 }
 
+// window_key in two parts, for a row whose column rs changes last: the
+// part over the other columns (before the new value is known), then the key
+// once it is (merge).  merge returns exactly window_key(row with column rs
+// = w): the exact-sum condition of the whole row implies the others' one,
+// so their aligned integer sum is valid and re-aligns exactly to the
+// row's smallest exponent; otherwise it sums the row in float64 in slot
+// order as window_key does.
+struct WindowPart {
+  unsigned long long acc;   // the others' significands aligned to their smallest exponent (valid when the row's test passes)
+  unsigned umax, umin1;     // largest bit pattern, smallest nonzero one minus 1, over the other columns
+};
+__device__ __forceinline__ WindowPart window_part(const float* row, const int W, const int rs, const int spread) {
+  WindowPart p;
+  p.umax = 0u;
+  p.umin1 = 0xFFFFFFFFu;
+  for (int t = 0; t < W; ++t) {
+    if (t == rs) continue;
+    const unsigned u = __float_as_uint(row[t]);
+    p.umax = max(p.umax, u);
+    p.umin1 = min(p.umin1, u - 1u);
+  }
+  p.acc = 0ull;
+  if (p.umax == 0u) return p;
+  const int emax = static_cast<int>(p.umax >> 23), emin = static_cast<int>((p.umin1 + 1u) >> 23);
+  if (p.umax < 0x7F800000u && emin >= 1 && emax - emin <= spread) {
+    for (int t = 0; t < W; ++t) {
+      if (t == rs) continue;
+      const unsigned u = __float_as_uint(row[t]);
+      const unsigned long long m = u != 0u ? static_cast<unsigned long long>((u & 0x7FFFFFu) | 0x800000u) : 0ull;
+      p.acc += m << max(static_cast<int>(u >> 23) - emin, 0);
+    }
+  }
+  return p;
+}
+__device__ __forceinline__ unsigned long long window_merge(const WindowPart& p, const float w, const float* row,
+                                                           const int W, const int rs, const int spread) {
+  const unsigned uw = __float_as_uint(w);
+  const unsigned umax = max(p.umax, uw), umin1 = min(p.umin1, uw - 1u);
+  if (umax == 0u) return kKeyZero;
+  const int emax = static_cast<int>(umax >> 23), emin = static_cast<int>((umin1 + 1u) >> 23);
+  if (umax < 0x7F800000u && emin >= 1 && emax - emin <= spread) {
+    unsigned long long acc = 0ull;
+    if (p.umax != 0u) acc = p.acc << (static_cast<int>((p.umin1 + 1u) >> 23) - emin);
+    if (uw != 0u) acc += static_cast<unsigned long long>((uw & 0x7FFFFFu) | 0x800000u) << (static_cast<int>(uw >> 23) - emin);
+    const double v = static_cast<double>(acc) * __longlong_as_double(static_cast<long long>(emin - 150 + 1023) << 52);
+    return static_cast<unsigned long long>(__double_as_longlong(v)) | kKeyZero;
+  }
+  double sum = 0.0;
+  for (int t = 0; t < W; ++t) sum += static_cast<double>(t == rs ? w : row[t]);
+  return mono_key(sum);
+}
+
 // One 16-byte piece of a K or V row as floats (8 bf16 or 4 fp32).
 template <typename KT>
 __device__ __forceinline__ void piece_to_float(const uint4 w, float* x);
@@ -1703,6 +1755,7 @@ struct RingClusterSmem {
   int* slots;        // raw slots of tokens lo .. hi - 1
   int* pos;          // their positions
   unsigned long long* keys;
+  WindowPart* parts; // window sums of tokens lo .. hi - 1 without column rs (before the wait)
   int* pf_blocks;    // rank 0: the lane's block list and live masks, the new K/V row
   int* pf_masks;
   unsigned char* pf_row;
@@ -1712,6 +1765,7 @@ __device__ __forceinline__ size_t ring_cluster_bytes(int span, int ld) {
   size_t off = static_cast<size_t>(kMaxG) * 128 * 4 + static_cast<size_t>(span) * ld * 4;
   off += 2 * ((static_cast<size_t>(span) * 4 + 7) & ~static_cast<size_t>(7));
   off += static_cast<size_t>(span + 1) * 8;
+  off += static_cast<size_t>(span) * sizeof(WindowPart);
   off += 2 * static_cast<size_t>(kPfBlocks) * 4 + 2 * 128 * 4;
   return off;
 }
@@ -1728,6 +1782,8 @@ __device__ __forceinline__ RingClusterSmem ring_cluster_smem(unsigned char* dsm,
   off += (static_cast<size_t>(span) * 4 + 7) & ~static_cast<size_t>(7);
   m.keys = reinterpret_cast<unsigned long long*>(dsm + off);
   off += static_cast<size_t>(span + 1) * 8;
+  m.parts = reinterpret_cast<WindowPart*>(dsm + off);
+  off += static_cast<size_t>(span) * sizeof(WindowPart);
   m.pf_blocks = reinterpret_cast<int*>(dsm + off);
   off += static_cast<size_t>(kPfBlocks) * 4;
   m.pf_masks = reinterpret_cast<int*>(dsm + off);
@@ -1761,8 +1817,11 @@ __device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRe
   __shared__ int sh_scan[40];
   __shared__ unsigned long long sh_bk;   // this rank's minimum candidate key, and its index (-1: none)
   __shared__ int sh_bi, sh_nanr;
-  __shared__ int sh_vslot, sh_dead;     // rank 0: the victim's raw slot and the block it released (from its owner)
+  __shared__ int sh_vslot, sh_dead;     // rank 0: the victim's raw slot and the block it released
+  __shared__ int sh_vpos;               // rank 0: the victim's position (from its owner)
   __shared__ int sh_pfnb;
+  __shared__ unsigned long long sh_ck[kRingCluster];   // every rank's minimum candidate (pushed by each rank)
+  __shared__ int sh_ci[kRingCluster], sh_cn[kRingCluster];   // its index (-1: none), its NaN count
   cg::cluster_group cluster = cg::this_cluster();
   const Dims& dm = A.dm;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1797,6 +1856,14 @@ __device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRe
       row[e] = e < d ? static_cast<const KT*>(A.k_new)[static_cast<size_t>(l) * d + e]
                      : static_cast<const KT*>(A.v_new)[static_cast<size_t>(l) * d + e - d];
   }
+  int lw = 0;
+  while ((1 << lw) < W) ++lw;
+  const int spread = 29 - lw;    // exact-sum bound: spread + 24 + log2(W) <= 53
+  // the window sums without column rs, while the attention kernel drains
+  // (column rs takes this step's value after the wait)
+  cp_async_wait_all();
+  __syncthreads();
+  for (int i = lo + tid; i < hi; i += blockDim.x) sm.parts[i - lo] = window_part(sm.rows + (i - lo) * ld, W, A.has_q ? rs : -1, spread);
   grid_dep_wait();      // the attention kernel's results are complete and visible
   grid_dep_launch();
   if (rank == 0) read_generation(A, sh_gen);
@@ -1834,11 +1901,17 @@ __device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRe
       }
     }
     __syncthreads();
-    const int ghd = g * d, per = (ghd + kRingCluster - 1) / kRingCluster;
+  }
+  // The split-K output combine of outputs e0 .. e0 + cnt - 1 (all threads):
+  // four threads per output, each a quarter of the segments (fewer loads in a
+  // chain), their sums added by two shuffles.  The DropKV scores need every
+  // output first (a quarter per rank, then exchanged); SnapKV's step does
+  // not, so ranks 1..3 combine a third each after the eviction, while rank 0
+  // finishes the lane.
+  const int ghd = g * d;
+  auto combine = [&](const int e0, const int cnt) {
+    const int nseg = min(A.ws.lane_nseg_buf[cbuf][l], kMaxSeg);
     const float* po = A.ws.part_o_buf[cbuf] + static_cast<size_t>(l) * kMaxSeg * g * d;
-    // four threads per output, each a quarter of the segments (fewer loads in
-    // a chain), their sums added by two shuffles
-    const int e0 = rank * per, cnt = max(0, min(ghd, e0 + per) - e0);
     for (int base = 0; base < 4 * cnt; base += blockDim.x) {
       const int x = base + tid, q = x & 3;
       const bool act = x < 4 * cnt;
@@ -1857,7 +1930,11 @@ __device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRe
         sm.sh_a[he] = o;
       }
     }
-    if (policy == KVEVICT_DROPKV) {
+  };
+  if (A.has_q && policy == KVEVICT_DROPKV) {
+    const int per = (ghd + kRingCluster - 1) / kRingCluster;
+    combine(rank * per, max(0, min(ghd, rank * per + per) - rank * per));
+    {
       cluster.sync();   // every rank's quarter of the outputs is in its shared memory
       for (int rr = 0; rr < kRingCluster; ++rr) {
         if (rr == rank) continue;
@@ -1869,8 +1946,6 @@ __device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRe
   }
 
   // ---- scores of this step into the ring, window-sum keys of lo .. hi - 1 --------
-  cp_async_wait_all();
-  __syncthreads();
   const float* lg = A.ws.logits_buf[cbuf] + static_cast<size_t>(l) * g * dm.lcap;
   const int k = max(0, n + 1 - dm.budget);
   const int cut = A.new_pos - dm.R + 1;
@@ -1880,9 +1955,6 @@ __device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRe
     else dropkv_ring_scores<KT, 64 / kEpc / 8>(A, L, lo, hi, i0, i1, sm.sh_a, lg, sh_lse2, W, rs, sm.rows, ld);
     __syncthreads();
   }
-  int lw = 0;
-  while ((1 << lw) < W) ++lw;
-  const int spread = 29 - lw;    // exact-sum bound: spread + 24 + log2(W) <= 53
   const bool fresh = A.has_q && policy == KVEVICT_SNAPKV;
   int nan_count = 0;
   for (int i = lo + tid; i < hi; i += blockDim.x) {
@@ -1898,7 +1970,9 @@ __device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRe
         else set_status(A.ws.status, ST_BAD_INDEX);
       }
     }
-    const unsigned long long key = W == 32 ? window_key4<32>(row, 32, spread) : window_key4<0>(row, W, spread);
+    // this step's column rs joins the sum taken before the wait
+    const unsigned long long key = window_merge(sm.parts[i - lo], A.has_q ? row[rs] : 0.f, row, W,
+                                                A.has_q ? rs : -1, spread);
     sm.keys[i - lo] = key;
     if (own && key == ~0ull) ++nan_count;
   }
@@ -1924,33 +1998,35 @@ __device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRe
   int32_t* vout = A.victims + static_cast<size_t>(l) * dm.cap;
   if (k == 1) {
     const int v_local = block_argmin3(best_k, best_p, best_i, sh_hist, sh_misc);
-    if (tid == 0 && v_local >= 0) {
-      unsigned long long m = 0;
-      const int qa = max(0, v_local - R), qb = min(n, v_local + R);
-      for (int q = qa; q <= qb; ++q) m = max(m, sm.keys[q - lo]);
-      sh_bk = m;
-      sh_bi = v_local;
+    // each rank pushes its minimum (and NaN count) into every rank's shared
+    // memory: after the barrier every rank reads them locally
+    if (tid < kRingCluster) {
+      unsigned long long m = ~0ull;
+      if (v_local >= 0) {
+        m = 0;
+        const int qa = max(0, v_local - R), qb = min(n, v_local + R);
+        for (int q = qa; q <= qb; ++q) m = max(m, sm.keys[q - lo]);
+      }
+      cluster.map_shared_rank(sh_ck, tid)[rank] = m;
+      cluster.map_shared_rank(sh_ci, tid)[rank] = v_local;
+      cluster.map_shared_rank(sh_cn, tid)[rank] = sh_nanr;
     }
-    cluster.sync();   // every rank's minimum and NaN count is in its shared memory
+    cluster.sync();   // every rank's minimum and NaN count is in every rank's shared memory
     unsigned long long gk = ~0ull;
-    int v = -1, vr = 0;
-    for (int rr = 0; rr < kRingCluster; ++rr) {
-      const int ri = *cluster.map_shared_rank(&sh_bi, rr);
-      const unsigned long long rk = *cluster.map_shared_rank(&sh_bk, rr);
-      if (ri >= 0 && (v < 0 || rk < gk || (rk == gk && ri < v))) { gk = rk; v = ri; vr = rr; }
-    }
+    int v = -1;
     int nan_all = 0;
-    if (rank == 0 && tid == 0)
-      for (int rr = 0; rr < kRingCluster; ++rr) nan_all += *cluster.map_shared_rank(&sh_nanr, rr);
+    for (int rr = 0; rr < kRingCluster; ++rr) {
+      const int ri = sh_ci[rr];
+      const unsigned long long rk = sh_ck[rr];
+      if (ri >= 0 && (v < 0 || rk < gk || (rk == gk && ri < v))) { gk = rk; v = ri; }
+      nan_all += sh_cn[rr];
+    }
     if (v >= 0) {
-      // rank 0 takes the victim's slot and position from the rank owning it;
+      // the rank owning the victim pushes its slot and position to rank 0;
       // every rank reads the entries it moves down one place
-      if (rank == 0 && tid == 0) {
-        // the owner's layout: its arrays' offsets depend on its span
-        const int olo = max(0, (n * vr) / kRingCluster - R), ohi = min(n, (n * (vr + 1)) / kRingCluster + R);
-        const RingClusterSmem osm = ring_cluster_smem(dsm, ohi - olo, ld);
-        sh_vslot = cluster.map_shared_rank(osm.slots, vr)[v - olo];
-        vout[0] = cluster.map_shared_rank(osm.pos, vr)[v - olo];
+      if (v >= i0 && v < i1 && tid == 0) {
+        *cluster.map_shared_rank(&sh_vslot, 0) = sm.slots[v - lo];
+        *cluster.map_shared_rank(&sh_vpos, 0) = sm.pos[v - lo];
       }
       const int i = max(i0, v + 1) + tid;
       const bool mv = i < i1;
@@ -1969,6 +2045,7 @@ __device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRe
       }
       vcount = 1;
       if (rank == 0) {
+        if (tid == 0) vout[0] = sh_vpos;
         // the victim's live bit (an emptied block is released and leaves the
         // list), from the live masks read ahead when the list fitted
         const int vs = sh_vslot;
@@ -2012,8 +2089,13 @@ __device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRe
     } else {
       cluster.sync();   // no rank touches another's shared memory after this
     }
-    // the table writes of every rank are done before rank 0 signals for the
-    // lane (arrive here, wait before the signal)
+    if (A.has_q && policy != KVEVICT_DROPKV && rank != 0) {
+      const int per3 = (ghd + kRingCluster - 2) / (kRingCluster - 1);
+      const int e0 = (rank - 1) * per3;
+      combine(e0, max(0, min(ghd, e0 + per3) - e0));
+    }
+    // the table writes (and outputs) of every rank are done before rank 0
+    // signals for the lane (arrive here, wait before the signal)
     cluster_arrive();
     if (rank != 0) {
       cluster_wait();
@@ -2042,6 +2124,10 @@ __device__ __forceinline__ void lane_step_cluster(const EpiArgs& A, const LaneRe
       auto isv = [&](int i) { return candf(i) && select_is_victim(sel, keyf(i), posf(i)); };
       vcount = lane_remove(L, n, plain_victims(isv), vout, nullptr, &dead, dm.P, A.ws.status, sh_scan);
     }
+  }
+  if (A.has_q && policy != KVEVICT_DROPKV) {
+    const int per = (ghd + kRingCluster - 1) / kRingCluster;
+    combine(rank * per, max(0, min(ghd, rank * per + per) - rank * per));
   }
   // the ranks' NaN counts (final once a cluster barrier followed the keys:
   // the selection's, or one here); nothing reads another rank's shared
