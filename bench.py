@@ -68,11 +68,11 @@ def parse():
                     help="profiling only: run the workload with this many layers (not a bench number)")
     ap.add_argument("--kernel-table", action="store_true",
                     help="time the engine's other kernels on their own workloads (DropKV window scoring at "
-                         "32K and 128K, selection, forced compaction, the SnapKV and toy decode steps), one "
-                         "JSON line each, instead of the decode-step bench line")
+                         "32K and 128K, selection, forced compaction, SnapKV prefill selection, relocation), "
+                         "one JSON line each, instead of the decode-step bench line")
     ap.add_argument("--only", default="",
                     help="with --kernel-table: comma-separated subset of d3_32k, d3_128k, snapkv_pf_32k, "
-                         "snapkv_pf_128k, snapkv, dropkv_decode, toy, reloc")
+                         "snapkv_pf_128k, reloc")
     ap.add_argument("--selftest-cpu", action="store_true",
                     help="the rank launcher and the cross-rank aggregation on CPU ranks (gloo) with a tiny "
                          "stand-in numpy step per rank; prints the aggregated line, no GPU")
