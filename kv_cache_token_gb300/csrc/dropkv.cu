@@ -1062,24 +1062,51 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
       }
       __syncwarp();
       if (lane == 0) mbar_arrive1(&bar.kempty[ks]);   // the positions are read
-      // The row loops stay compact (16 keys at a time, not unrolled over the
-      // tile): the kernel's warp roles share the instruction cache, and fully
-      // unrolled code stalled them on instruction fetch.  S is read twice,
-      // for the max and then for P.
+      // The row loops stay compact (16 keys at a time, S read twice: max,
+      // then P): the kernel's warp roles share the instruction cache, and
+      // fully unrolled loops stalled them on instruction fetch.  Without P V
+      // a half whose 64 keys the whole warp sees (every tile but the last
+      // few) is read once, into registers, and summed from there.
       const bool full = __all_sync(0xffffffffu, vis == 64);   // no key of the half masked for the warp
-      float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[16];
-        tc::ld16(aS + c * 16, v);
+      const bool regs = !kWithV && full;
+      uint32_t s0[16], s1[16], s2[16], s3[16];
+      float tmax;
+      if (regs) {
+        tc::ld16(aS, s0);
+        tc::ld16(aS + 16, s1);
+        tc::ld16(aS + 32, s2);
+        tc::ld16(aS + 48, s3);
         tc::wait_ld();
-        const int vc = full ? 16 : vis - 16 * c;
+        tc::hold16(s0);
+        tc::hold16(s1);
+        tc::hold16(s2);
+        tc::hold16(s3);
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int k = 0; k < 16; ++k) mx[k & 3] = fmaxf(mx[k & 3], k < vc ? __uint_as_float(v[k]) : -INFINITY);
+        for (int k = 0; k < 16; k += 2) {
+          mq[0] = fmaxf(mq[0], fmaxf(__uint_as_float(s0[k]), __uint_as_float(s0[k + 1])));
+          mq[1] = fmaxf(mq[1], fmaxf(__uint_as_float(s1[k]), __uint_as_float(s1[k + 1])));
+          mq[2] = fmaxf(mq[2], fmaxf(__uint_as_float(s2[k]), __uint_as_float(s2[k + 1])));
+          mq[3] = fmaxf(mq[3], fmaxf(__uint_as_float(s3[k]), __uint_as_float(s3[k + 1])));
+        }
+        tmax = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      } else {
+        float mx[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[16];
+          tc::ld16(aS + c * 16, v);
+          tc::wait_ld();
+          tc::hold16(v);
+          const int vc = full ? 16 : vis - 16 * c;
+#pragma unroll
+          for (int k = 0; k < 16; ++k) mx[k & 3] = fmaxf(mx[k & 3], k < vc ? __uint_as_float(v[k]) : -INFINITY);
+        }
+        tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
       }
       // the largest raw score (scale2 > 0 keeps the order; the scale is
       // applied once, and inside the exponent's FMA below)
-      const float tmax = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])) * A.scale2;
+      tmax *= A.scale2;
       float factor = 1.f;
       if (tmax > m_run + kTcRescale) {
         factor = (m_run == -INFINITY) ? 0.f : exp2f(m_run - tmax);
@@ -1089,15 +1116,26 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
       const float negm = m_run == -INFINITY ? 0.f : -m_run;
       if (!kWithV) {
         float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[16];
-          tc::ld16(aS + c * 16, v);
-          tc::wait_ld();
-          const int vc = vis - 16 * c;
+        if (regs) {
 #pragma unroll
-          for (int k = 0; k < 16; ++k)
-            ps[k & 3] += hw_exp2(k < vc ? fmaf(__uint_as_float(v[k]), A.scale2, negm) : -INFINITY);
+          for (int k = 0; k < 16; ++k) {
+            ps[0] += hw_exp2(fmaf(__uint_as_float(s0[k]), A.scale2, negm));
+            ps[1] += hw_exp2(fmaf(__uint_as_float(s1[k]), A.scale2, negm));
+            ps[2] += hw_exp2(fmaf(__uint_as_float(s2[k]), A.scale2, negm));
+            ps[3] += hw_exp2(fmaf(__uint_as_float(s3[k]), A.scale2, negm));
+          }
+        } else {
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[16];
+            tc::ld16(aS + c * 16, v);
+            tc::wait_ld();
+            tc::hold16(v);
+            const int vc = vis - 16 * c;
+#pragma unroll
+            for (int k = 0; k < 16; ++k)
+              ps[k & 3] += hw_exp2(k < vc ? fmaf(__uint_as_float(v[k]), A.scale2, negm) : -INFINITY);
+          }
         }
         l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
         // S is read: release the buffer
@@ -1117,6 +1155,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
           uint32_t v[16];
           tc::ld16(aO + q8 * 16, v);
           tc::wait_ld();
+          tc::hold16(v);
 #pragma unroll
           for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * factor);
           tc::st16(aO + q8 * 16, v);
@@ -1127,11 +1166,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
       // P of the 16 keys of chunk c goes over their own (already read) S
       // columns: hi in the first 8, lo in the next 8.
       float psum[2] = {0.f, 0.f};
-      auto p_chunk = [&](int c, auto masked) {
-        uint32_t v[16];
-        tc::ld16(aS + c * 16, v);
-        tc::wait_ld();
-        const int vc = vis - 16 * c;
+      auto p_store = [&](int c, const uint32_t (&v)[16], int vc, auto masked) {
         uint32_t hi[8], lo2[8];
 #pragma unroll
         for (int k2 = 0; k2 < 8; ++k2) {
@@ -1150,10 +1185,22 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
       };
       if (full) {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) p_chunk(c, std::false_type{});
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[16];
+          tc::ld16(aS + c * 16, v);
+          tc::wait_ld();
+          tc::hold16(v);
+          p_store(c, v, 16, std::false_type{});
+        }
       } else {
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) p_chunk(c, std::true_type{});
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[16];
+          tc::ld16(aS + c * 16, v);
+          tc::wait_ld();
+          tc::hold16(v);
+          p_store(c, v, vis - 16 * c, std::true_type{});
+        }
       }
       l_run += psum[0] + psum[1];
       tc::wait_st();
@@ -1396,6 +1443,8 @@ __global__ void __launch_bounds__(kP2Threads, 1) d3_p2_kernel(D3Args A, const __
         tc::ld16(aS + ch * 16, v);
         if (kRes) tc::ld16(aS + 128 + ch * 16, g);
         tc::wait_ld();
+        tc::hold16(v);
+        if (kRes) tc::hold16(g);
         const float* lse_c = sm.lse2 + c * 32 + ch * 16;
         const float* an_c = sm.an + c * 32 + ch * 16;
         float x[16];
