@@ -1035,43 +1035,78 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
     if (nrt > 1 && rt == 0)
       for (int j = j_begin + tid; j < j_end; j += 256) A.col_out[lo + j] = 0.f;
     float m_run = -INFINITY, l_run = 0.f;
+    // the position of the last key of this half of tile t, read from the
+    // table a tile ahead (INT_MAX when the half runs past the chunk): a row
+    // at or after it sees the whole half, and needs no staged positions
+    auto half_last = [&](int t) {
+      const int k0 = t * kP1Keys + h * 64;
+      return (t < ntiles && k0 + 64 <= nkeys) ? A.ls.pos[lo + j_begin + k0 + 63] : 0x7FFFFFFF;
+    };
+    int last_next = half_last(0);
 #pragma unroll 1
     for (int t = 0; t < ntiles; ++t) {
       const int b = t % kP1Bufs, ks = t % kP1KSt;
+      const int last = last_next;
+      last_next = half_last(t + 1);
       (void)mbar_wait_bounded(&bar.x_full[b], (t / kP1Bufs) & 1, A.ws.status);
-      (void)mbar_wait_bounded(&bar.kfull[ks], (t / kP1KSt) & 1, A.ws.status);   // positions
       tc::fence_after();
-      const int* tpos = sh_pos + ks * kP1Keys + h * 64;
       const uint32_t aS = tl + lane_off + 256 + b * kP1Keys + h * 64;
-      // the half's keys the row sees: a prefix (positions ascend), found by
-      // a binary search unless the last one already precedes the row
-      const int k0 = t * kP1Keys + h * 64;   // first key of the half within the chunk
-      int vis = 0;
-      if (row_ok) {
-        const int lim = max(0, min(64, nkeys - k0));
-        if (lim > 0 && tpos[lim - 1] <= qp) {
-          vis = lim;
-        } else {
-          int lo_ = 0, hi_ = lim;
-          while (lo_ < hi_) {
-            const int mid = (lo_ + hi_) >> 1;
-            if (tpos[mid] <= qp) lo_ = mid + 1; else hi_ = mid;
+      const bool full = __all_sync(0xffffffffu, row_ok && last <= qp);   // no key of the half masked for the warp
+      int vis = 64;
+      if (!full) {
+        // the half's keys the row sees: a prefix (positions ascend), found
+        // by a binary search of the staged positions
+        (void)mbar_wait_bounded(&bar.kfull[ks], (t / kP1KSt) & 1, A.ws.status);
+        const int* tpos = sh_pos + ks * kP1Keys + h * 64;
+        const int k0 = t * kP1Keys + h * 64;   // first key of the half within the chunk
+        vis = 0;
+        if (row_ok) {
+          const int lim = max(0, min(64, nkeys - k0));
+          if (lim > 0 && tpos[lim - 1] <= qp) {
+            vis = lim;
+          } else {
+            int lo_ = 0, hi_ = lim;
+            while (lo_ < hi_) {
+              const int mid = (lo_ + hi_) >> 1;
+              if (tpos[mid] <= qp) lo_ = mid + 1; else hi_ = mid;
+            }
+            vis = lo_;
           }
-          vis = lo_;
         }
       }
+      // the stage is free once S(t) is done (x_full) and the rows are past
+      // its positions
       __syncwarp();
-      if (lane == 0) mbar_arrive1(&bar.kempty[ks]);   // the positions are read
+      if (lane == 0) mbar_arrive1(&bar.kempty[ks]);
       // The row loops stay compact (16 keys at a time, S read twice: max,
       // then P): the kernel's warp roles share the instruction cache, and
       // fully unrolled loops stalled them on instruction fetch.  Without P V
       // a half whose 64 keys the whole warp sees (every tile but the last
       // few) is read once, into registers, and summed from there.
-      const bool full = __all_sync(0xffffffffu, vis == 64);   // no key of the half masked for the warp
       const bool regs = !kWithV && full;
       uint32_t s0[16], s1[16], s2[16], s3[16];
       float tmax;
       if (regs) {
+        tc::ld16(aS, s0);
+        tc::ld16(aS + 16, s1);
+        tc::ld16(aS + 32, s2);
+        tc::ld16(aS + 48, s3);
+        tc::wait_ld();
+        tc::hold16(s0);
+        tc::hold16(s1);
+        tc::hold16(s2);
+        tc::hold16(s3);
+        float mq[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int k = 0; k < 16; k += 2) {
+          mq[0] = fmaxf(mq[0], fmaxf(__uint_as_float(s0[k]), __uint_as_float(s0[k + 1])));
+          mq[1] = fmaxf(mq[1], fmaxf(__uint_as_float(s1[k]), __uint_as_float(s1[k + 1])));
+          mq[2] = fmaxf(mq[2], fmaxf(__uint_as_float(s2[k]), __uint_as_float(s2[k + 1])));
+          mq[3] = fmaxf(mq[3], fmaxf(__uint_as_float(s3[k]), __uint_as_float(s3[k + 1])));
+        }
+        tmax = fmaxf(fmaxf(mq[0], mq[1]), fmaxf(mq[2], mq[3]));
+      } else if (full) {
+        // every key visible: the four 16-column loads in flight at once
         tc::ld16(aS, s0);
         tc::ld16(aS + 16, s1);
         tc::ld16(aS + 32, s2);
@@ -1151,14 +1186,28 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
         tc::fence_after();
         const uint32_t aO = tl + lane_off + h * 128;
 #pragma unroll 1
-        for (int q8 = 0; q8 < 8; ++q8) {
-          uint32_t v[16];
-          tc::ld16(aO + q8 * 16, v);
+        for (int q = 0; q < 2; ++q) {
+          uint32_t o0[16], o1[16], o2[16], o3[16];
+          tc::ld16(aO + q * 64, o0);
+          tc::ld16(aO + q * 64 + 16, o1);
+          tc::ld16(aO + q * 64 + 32, o2);
+          tc::ld16(aO + q * 64 + 48, o3);
           tc::wait_ld();
-          tc::hold16(v);
+          tc::hold16(o0);
+          tc::hold16(o1);
+          tc::hold16(o2);
+          tc::hold16(o3);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) v[k] = __float_as_uint(__uint_as_float(v[k]) * factor);
-          tc::st16(aO + q8 * 16, v);
+          for (int k = 0; k < 16; ++k) {
+            o0[k] = __float_as_uint(__uint_as_float(o0[k]) * factor);
+            o1[k] = __float_as_uint(__uint_as_float(o1[k]) * factor);
+            o2[k] = __float_as_uint(__uint_as_float(o2[k]) * factor);
+            o3[k] = __float_as_uint(__uint_as_float(o3[k]) * factor);
+          }
+          tc::st16(aO + q * 64, o0);
+          tc::st16(aO + q * 64 + 16, o1);
+          tc::st16(aO + q * 64 + 32, o2);
+          tc::st16(aO + q * 64 + 48, o3);
         }
       }
       // p = 2^(s scale2 - m); a key the row does not see gives 0, and so does
