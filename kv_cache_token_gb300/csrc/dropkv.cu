@@ -1179,37 +1179,6 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
         if (lane == 0) mbar_arrive1(&bar.x_free[b]);
         continue;
       }
-      if (t >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
-        // P V(t - 1) must be complete before O_h is rescaled
-        const int tp = t - 1, vp = tp % kP1VSt;
-        (void)mbar_wait_bounded(&bar.vempty[vp], (tp / kP1VSt) & 1, A.ws.status);
-        tc::fence_after();
-        const uint32_t aO = tl + lane_off + h * 128;
-#pragma unroll 1
-        for (int q = 0; q < 2; ++q) {
-          uint32_t o0[16], o1[16], o2[16], o3[16];
-          tc::ld16(aO + q * 64, o0);
-          tc::ld16(aO + q * 64 + 16, o1);
-          tc::ld16(aO + q * 64 + 32, o2);
-          tc::ld16(aO + q * 64 + 48, o3);
-          tc::wait_ld();
-          tc::hold16(o0);
-          tc::hold16(o1);
-          tc::hold16(o2);
-          tc::hold16(o3);
-#pragma unroll
-          for (int k = 0; k < 16; ++k) {
-            o0[k] = __float_as_uint(__uint_as_float(o0[k]) * factor);
-            o1[k] = __float_as_uint(__uint_as_float(o1[k]) * factor);
-            o2[k] = __float_as_uint(__uint_as_float(o2[k]) * factor);
-            o3[k] = __float_as_uint(__uint_as_float(o3[k]) * factor);
-          }
-          tc::st16(aO + q * 64, o0);
-          tc::st16(aO + q * 64 + 16, o1);
-          tc::st16(aO + q * 64 + 32, o2);
-          tc::st16(aO + q * 64 + 48, o3);
-        }
-      }
       // p = 2^(s scale2 - m); a key the row does not see gives 0, and so does
       // every key while the row has seen none (m = -inf, offset taken as 0).
       // P of the 16 keys of chunk c goes over their own (already read) S
@@ -1249,6 +1218,39 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
           tc::wait_ld();
           tc::hold16(v);
           p_store(c, v, vis - 16 * c, std::true_type{});
+        }
+      }
+      // O_h is rescaled after P(t) is written, so that P V(t - 1), which
+      // must be complete first, has run meanwhile; P V(t) is issued only
+      // once the rows are past this point (x_free)
+      if (t >= 1 && __any_sync(0xffffffffu, factor != 1.f)) {
+        const int tp = t - 1, vp = tp % kP1VSt;
+        (void)mbar_wait_bounded(&bar.vempty[vp], (tp / kP1VSt) & 1, A.ws.status);
+        tc::fence_after();
+        const uint32_t aO = tl + lane_off + h * 128;
+#pragma unroll 1
+        for (int q = 0; q < 2; ++q) {
+          uint32_t o0[16], o1[16], o2[16], o3[16];
+          tc::ld16(aO + q * 64, o0);
+          tc::ld16(aO + q * 64 + 16, o1);
+          tc::ld16(aO + q * 64 + 32, o2);
+          tc::ld16(aO + q * 64 + 48, o3);
+          tc::wait_ld();
+          tc::hold16(o0);
+          tc::hold16(o1);
+          tc::hold16(o2);
+          tc::hold16(o3);
+#pragma unroll
+          for (int k = 0; k < 16; ++k) {
+            o0[k] = __float_as_uint(__uint_as_float(o0[k]) * factor);
+            o1[k] = __float_as_uint(__uint_as_float(o1[k]) * factor);
+            o2[k] = __float_as_uint(__uint_as_float(o2[k]) * factor);
+            o3[k] = __float_as_uint(__uint_as_float(o3[k]) * factor);
+          }
+          tc::st16(aO + q * 64, o0);
+          tc::st16(aO + q * 64 + 16, o1);
+          tc::st16(aO + q * 64 + 32, o2);
+          tc::st16(aO + q * 64 + 48, o3);
         }
       }
       l_run += psum[0] + psum[1];
