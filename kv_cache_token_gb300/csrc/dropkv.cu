@@ -1303,34 +1303,14 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
   if (warp == kP1Issuer) tc::dealloc(tl, 512);
 }
 
-// p / (1 - p) * ||a - v|| for a (row, key) pair with p > 1/2, x = log2 p:
-// the distance directly from the fp32 a row and the key's bf16 V row in the
-// pool (the expansion would cancel there), 1 - p from expm1.
-__device__ __noinline__ float residual_direct(float x, const float* arow, const __nv_bfloat16* vrow) {
+// p / (1 - p) * sqrt(d2) for a (row, key) pair with p > 1/2, x = log2 p, d2
+// = ||a - v||^2 taken directly (the expansion would cancel there); 1 - p
+// from expm1.
+__device__ __forceinline__ float direct_term(float x, float d2) {
   const float p = exp2f(x);
   const float om = -expm1f(x * kLn2);
   if (!(om > 0.f)) return INFINITY;
-  const float4* a4 = reinterpret_cast<const float4*>(arow);
-  const uint4* v8 = reinterpret_cast<const uint4*>(vrow);
-  float acc = 0.f;
-#pragma unroll 4
-  for (int c = 0; c < kD / 8; ++c) {
-    const uint4 raw = v8[c];
-    const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&raw);
-    const float4 x0 = a4[c * 2], x1 = a4[c * 2 + 1];
-    const float2 v0 = __bfloat1622float2(pr[0]), v1 = __bfloat1622float2(pr[1]);
-    const float2 v2 = __bfloat1622float2(pr[2]), v3 = __bfloat1622float2(pr[3]);
-    float d;
-    d = x0.x - v0.x; acc = fmaf(d, d, acc);
-    d = x0.y - v0.y; acc = fmaf(d, d, acc);
-    d = x0.z - v1.x; acc = fmaf(d, d, acc);
-    d = x0.w - v1.y; acc = fmaf(d, d, acc);
-    d = x1.x - v2.x; acc = fmaf(d, d, acc);
-    d = x1.y - v2.y; acc = fmaf(d, d, acc);
-    d = x1.z - v3.x; acc = fmaf(d, d, acc);
-    d = x1.w - v3.y; acc = fmaf(d, d, acc);
-  }
-  return p / om * sqrtf(acc);
+  return p / om * sqrtf(d2);
 }
 
 constexpr float kSmallLog2 = -7.f;   // p < 2^-7: p / (1 - p) = p + p^2 + p^3 within 2^-21
@@ -1462,23 +1442,24 @@ __global__ void __launch_bounds__(kP2Threads, 1) d3_p2_kernel(D3Args A, const __
     const int qmin = __reduce_min_sync(0xffffffffu, qp_mine);
     const int nv = min(32, A.rows - r0);   // rows of this warp (<= 0: none)
     const int nch = nv <= 0 ? 0 : (nv + 15) >> 4;
-    auto meta = [&](int t, int& p, float& v) {
+    auto meta = [&](int t, int& p, float& v, int& sl) {
       const int j = j_begin + t * kP2Keys + kk;
       const bool ok = t < ntiles && j < j_end;
       p = ok ? A.ls.pos[lo + j] : 0x7FFFFFFF;
       v = (kRes && ok) ? A.ws.d3_vn[lo + j] : 0.f;
+      sl = (kRes && ok) ? A.ls.slot[lo + j] : 0;
     };
-    int pj;
+    int pj, sj;
     float vj;
-    meta(0, pj, vj);
+    meta(0, pj, vj, sj);
 #pragma unroll 1
     for (int t = 0; t < ntiles; ++t) {
       const int st = t & 1;
       const int j = j_begin + t * kP2Keys + kk;
       const bool key_ok = j < j_end;
-      int pj_n;
+      int pj_n, sj_n;
       float vj_n;
-      meta(t + 1, pj_n, vj_n);   // in flight while this tile is scored
+      meta(t + 1, pj_n, vj_n, sj_n);   // in flight while this tile is scored
       // every (row, key) pair of the warp counted: no mask (a key past the
       // chunk has position INT_MAX)
       const int wmax = __reduce_max_sync(0xffffffffu, pj);
@@ -1555,24 +1536,43 @@ __global__ void __launch_bounds__(kP2Threads, 1) d3_p2_kernel(D3Args A, const __
               acc += (p > 0.f && p <= 0.5f) ? tm : 0.f;
             }
           }
-          // pairs with p > 1/2 (at most one key per row has one): direct distance
-          while (big) {
-            const int k = __ffs(big) - 1;
-            big &= big - 1;
+          // pairs with p > 1/2 (at most one key per row has one): the direct
+          // distance, each pair's 128 elements shared by the warp's lanes, so
+          // its loads (the fp32 a row, just written by the combine, and the
+          // key's V row, just copied for the tile) take one round trip
+          unsigned pend = __ballot_sync(0xffffffffu, big != 0);
+          while (pend) {
+            const int src = __ffs(pend) - 1;
+            const int k = __ffs(__shfl_sync(0xffffffffu, big, src)) - 1;
             float xk = 0.f;
 #pragma unroll
             for (int k2 = 0; k2 < 16; ++k2)
               if (k2 == k) xk = x[k2];
-            const int r = r0 + ch * 16 + k;
-            const float* arow =
-                A.a_out + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + r / A.w) * A.w + r % A.w) * kD;
-            int slot = A.ls.slot[lo + j];
+            xk = __shfl_sync(0xffffffffu, xk, src);
+            int slot = __shfl_sync(0xffffffffu, sj, src);
             if (slot < 0 || slot >= A.dm.P * kBlock) {
-              set_status(A.ws.status, ST_BAD_INDEX);
+              if (lane == 0) set_status(A.ws.status, ST_BAD_INDEX);
               slot = 0;
             }
-            const __nv_bfloat16* vrow = static_cast<const __nv_bfloat16*>(A.ls.v_pool) + static_cast<size_t>(slot) * kD;
-            acc += residual_direct(xk, arow, vrow);
+            const int r = r0 + ch * 16 + k;
+            const float4 av = *reinterpret_cast<const float4*>(
+                A.a_out + ((static_cast<size_t>(b) * A.dm.Hq + kh * A.dm.g + r / A.w) * A.w + r % A.w) * kD + 4 * lane);
+            const uint2 vr = *reinterpret_cast<const uint2*>(static_cast<const __nv_bfloat16*>(A.ls.v_pool) +
+                                                             static_cast<size_t>(slot) * kD + 4 * lane);
+            const float2 v01 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vr.x));
+            const float2 v23 = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&vr.y));
+            float d, d2 = 0.f;
+            d = av.x - v01.x; d2 = fmaf(d, d, d2);
+            d = av.y - v01.y; d2 = fmaf(d, d, d2);
+            d = av.z - v23.x; d2 = fmaf(d, d, d2);
+            d = av.w - v23.y; d2 = fmaf(d, d, d2);
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+            if (lane == src) {
+              acc += direct_term(xk, d2);
+              big &= big - 1;
+            }
+            pend = __ballot_sync(0xffffffffu, big != 0);
           }
         }
       }
@@ -1606,6 +1606,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) d3_p2_kernel(D3Args A, const __
       }
       pj = pj_n;
       vj = vj_n;
+      sj = sj_n;
     }
   }
   tc::fence_before();
