@@ -63,19 +63,6 @@ __device__ __forceinline__ void split_bf16(float p0, float p1, uint32_t& hi, uin
   lo = *reinterpret_cast<uint32_t*>(&l);
 }
 
-// The same split with integer and add instructions only (the conversion
-// instructions run at a fraction of the rate): hi is p truncated to bf16 (its
-// upper 16 bits), lo = p - hi exactly in fp32, rounded to the nearest bf16
-// (ties away from zero) by adding half an ulp to its bits; hi + lo is p to
-// 2^-16 relative.  For finite p >= 0 (attention weights).
-__device__ __forceinline__ void split_bf16_fast(float p0, float p1, uint32_t& hi, uint32_t& lo) {
-  const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-  hi = __byte_perm(b0, b1, 0x7632);
-  const float l0 = p0 - __uint_as_float(b0 & 0xFFFF0000u);
-  const float l1 = p1 - __uint_as_float(b1 & 0xFFFF0000u);
-  lo = __byte_perm(__float_as_uint(l0) + 0x8000u, __float_as_uint(l1) + 0x8000u, 0x7632);
-}
-
 struct D3Args {
   LayerState ls;
   Workspace ws;
@@ -618,6 +605,40 @@ __device__ __forceinline__ float hw_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+// Two fp32 lanes per instruction (the packed .f32x2 arithmetic): each lane
+// is rounded exactly as the scalar fmaf, + or * rounds it.
+__device__ __forceinline__ float2 f2_fma(float2 a, float2 b, float2 c) {
+  float2 d;
+  asm("{\n .reg .b64 a, b, c, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mov.b64 c, {%6, %7};\n"
+      " fma.rn.f32x2 d, a, b, c;\n mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+  return d;
+}
+__device__ __forceinline__ float2 f2_add(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n add.rn.f32x2 d, a, b;\n"
+      " mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 f2_sub(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n sub.rn.f32x2 d, a, b;\n"
+      " mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
+}
+__device__ __forceinline__ float2 f2_mul(float2 a, float2 b) {
+  float2 d;
+  asm("{\n .reg .b64 a, b, d;\n mov.b64 a, {%2, %3};\n mov.b64 b, {%4, %5};\n mul.rn.f32x2 d, a, b;\n"
+      " mov.b64 {%0, %1}, d;\n}"
+      : "=f"(d.x), "=f"(d.y)
+      : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+  return d;
 }
 __device__ __forceinline__ float hw_rcp(float x) {
   float y;
@@ -1183,20 +1204,30 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
       // every key while the row has seen none (m = -inf, offset taken as 0).
       // P of the 16 keys of chunk c goes over their own (already read) S
       // columns: hi in the first 8, lo in the next 8.
-      float psum[2] = {0.f, 0.f};
+      float2 psum = make_float2(0.f, 0.f);
       auto p_store = [&](int c, const uint32_t (&v)[16], int vc, auto masked) {
         uint32_t hi[8], lo2[8];
 #pragma unroll
         for (int k2 = 0; k2 < 8; ++k2) {
-          float x0 = fmaf(__uint_as_float(v[2 * k2]), A.scale2, negm);
-          float x1 = fmaf(__uint_as_float(v[2 * k2 + 1]), A.scale2, negm);
+          float2 xx = f2_fma(make_float2(__uint_as_float(v[2 * k2]), __uint_as_float(v[2 * k2 + 1])),
+                             make_float2(A.scale2, A.scale2), make_float2(negm, negm));
           if (decltype(masked)::value) {
-            x0 = 2 * k2 < vc ? x0 : -INFINITY;
-            x1 = 2 * k2 + 1 < vc ? x1 : -INFINITY;
+            xx.x = 2 * k2 < vc ? xx.x : -INFINITY;
+            xx.y = 2 * k2 + 1 < vc ? xx.y : -INFINITY;
           }
-          const float p0 = hw_exp2(x0), p1 = hw_exp2(x1);
-          psum[k2 & 1] += p0 + p1;
-          split_bf16_fast(p0, p1, hi[k2], lo2[k2]);
+          const float2 pp = make_float2(hw_exp2(xx.x), hw_exp2(xx.y));
+          psum = f2_add(psum, pp);
+          // the split into bf16 hi + lo by integer and add instructions
+          // only (the conversion instructions run at a fraction of the
+          // rate): hi is p truncated to bf16 (its upper 16 bits), lo = p - hi
+          // exactly in fp32, rounded to the nearest bf16 (ties away from
+          // zero) by adding half an ulp to its bits; hi + lo is p to 2^-16
+          // relative (p finite and >= 0)
+          const uint32_t b0 = __float_as_uint(pp.x), b1 = __float_as_uint(pp.y);
+          hi[k2] = __byte_perm(b0, b1, 0x7632);
+          const float2 rem =
+              f2_sub(pp, make_float2(__uint_as_float(b0 & 0xFFFF0000u), __uint_as_float(b1 & 0xFFFF0000u)));
+          lo2[k2] = __byte_perm(__float_as_uint(rem.x) + 0x8000u, __float_as_uint(rem.y) + 0x8000u, 0x7632);
         }
         tc::st8(aS + c * 16, hi);
         tc::st8(aS + c * 16 + 8, lo2);
@@ -1253,7 +1284,7 @@ __global__ void __launch_bounds__(kP1Threads, 1) d3_p1_kernel(D3Args A, const __
           tc::st16(aO + q * 64 + 48, o3);
         }
       }
-      l_run += psum[0] + psum[1];
+      l_run += psum.x + psum.y;
       tc::wait_st();
       tc::fence_before();
       __syncwarp();
@@ -1321,7 +1352,7 @@ constexpr float kR2Floor = 1e-30f;   // r2 floor: sqrt(r2) = r2 rsqrt(r2) stays 
 struct P2Small {
   uint64_t full[kP2St], empty[kP2St], x_full[2], x_free[2], qfull;
   uint32_t taddr, pad;
-  float lse2[kRowTile];    // per row of the CTA: LSE (base 2; +inf past the rows) and |a|^2
+  float nlse2[kRowTile];   // per row of the CTA: -LSE (base 2; -inf past the rows) and |a|^2
   float an[kRowTile];
 };
 constexpr int p2_smem(bool res) {
@@ -1428,7 +1459,7 @@ __global__ void __launch_bounds__(kP2Threads, 1) d3_p2_kernel(D3Args A, const __
       const int r = rt * kRowTile + tid;
       const size_t wrow = static_cast<size_t>(l) * A.rows_cap + r;
       // a row past the window's rows: +inf LSE, so every weight of it is 0
-      sm.lse2[tid] = r < A.rows ? A.ws.d3_rowc[wrow * 2] : INFINITY;
+      sm.nlse2[tid] = r < A.rows ? -A.ws.d3_rowc[wrow * 2] : -INFINITY;
       sm.an[tid] = (kRes && r < A.rows) ? A.ws.d3_rowc[wrow * 2 + 1] : 0.f;
     }
     cp_commit();
@@ -1477,49 +1508,53 @@ __global__ void __launch_bounds__(kP2Threads, 1) d3_p2_kernel(D3Args A, const __
         tc::wait_ld();
         tc::hold16(v);
         if (kRes) tc::hold16(g);
-        const float* lse_c = sm.lse2 + c * 32 + ch * 16;
+        const float* nlse_c = sm.nlse2 + c * 32 + ch * 16;
         const float* an_c = sm.an + c * 32 + ch * 16;
+        // two rows per packed instruction
         float x[16];
         float xm[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
-        for (int k4 = 0; k4 < 4; ++k4) {
-          const float4 L4 = *reinterpret_cast<const float4*>(lse_c + 4 * k4);
-          const float Ls[4] = {L4.x, L4.y, L4.z, L4.w};
-#pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const int k = 4 * k4 + u;
-            float xv = fmaf(__uint_as_float(v[k]), A.scale2, -Ls[u]);
-            if (!no_mask) {
-              const int qpr = __shfl_sync(0xffffffffu, qp_mine, ch * 16 + k);
-              const bool vis = key_ok && (kMode == kMassLater ? pj < qpr : pj <= qpr);
-              xv = vis ? xv : -INFINITY;
-            }
-            x[k] = xv;
-            xm[u] = fmaxf(xm[u], xv);
+        for (int k = 0; k < 16; k += 2) {
+          const float2 nl = *reinterpret_cast<const float2*>(nlse_c + k);
+          float2 xx = f2_fma(make_float2(__uint_as_float(v[k]), __uint_as_float(v[k + 1])),
+                             make_float2(A.scale2, A.scale2), nl);
+          if (!no_mask) {
+            const int qp0 = __shfl_sync(0xffffffffu, qp_mine, ch * 16 + k);
+            const int qp1 = __shfl_sync(0xffffffffu, qp_mine, ch * 16 + k + 1);
+            const bool vis0 = key_ok && (kMode == kMassLater ? pj < qp0 : pj <= qp0);
+            const bool vis1 = key_ok && (kMode == kMassLater ? pj < qp1 : pj <= qp1);
+            xx.x = vis0 ? xx.x : -INFINITY;
+            xx.y = vis1 ? xx.y : -INFINITY;
           }
+          x[k] = xx.x;
+          x[k + 1] = xx.y;
+          xm[k & 3] = fmaxf(xm[k & 3], xx.x);
+          xm[(k + 1) & 3] = fmaxf(xm[(k + 1) & 3], xx.y);
         }
         if (!kRes) {
+          float2 a2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int k = 0; k < 16; ++k) acc += hw_exp2(x[k]);
+          for (int k = 0; k < 16; k += 2) a2 = f2_add(a2, make_float2(hw_exp2(x[k]), hw_exp2(x[k + 1])));
+          acc += a2.x + a2.y;
           continue;
         }
         const float xmax = fmaxf(fmaxf(xm[0], xm[1]), fmaxf(xm[2], xm[3]));
         if (!__any_sync(0xffffffffu, xmax >= kSmallLog2)) {
           // every weight of the warp's pairs is small: no reciprocal, and
           // sqrt(r2) = r2 rsqrt(r2) (a pair not counted has p = 0)
+          float2 a2 = make_float2(0.f, 0.f);
 #pragma unroll
-          for (int k4 = 0; k4 < 4; ++k4) {
-            const float4 N4 = *reinterpret_cast<const float4*>(an_c + 4 * k4);
-            const float Ns[4] = {N4.x, N4.y, N4.z, N4.w};
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-              const int k = 4 * k4 + u;
-              const float p = hw_exp2(x[k]);
-              const float r2 = fmaxf(kR2Floor, fmaf(-2.f, __uint_as_float(g[k]), Ns[u] + vj));
-              const float q = fmaf(fmaf(p, p, p), p, p);   // p + p^2 + p^3
-              acc = fmaf(q * r2, hw_rsqrt(r2), acc);
-            }
+          for (int k = 0; k < 16; k += 2) {
+            const float2 n2 = *reinterpret_cast<const float2*>(an_c + k);
+            const float2 p = make_float2(hw_exp2(x[k]), hw_exp2(x[k + 1]));
+            float2 r2 = f2_fma(make_float2(__uint_as_float(g[k]), __uint_as_float(g[k + 1])), make_float2(-2.f, -2.f),
+                               f2_add(n2, make_float2(vj, vj)));
+            r2.x = fmaxf(kR2Floor, r2.x);
+            r2.y = fmaxf(kR2Floor, r2.y);
+            const float2 q = f2_fma(f2_fma(p, p, p), p, p);   // p + p^2 + p^3
+            a2 = f2_fma(f2_mul(q, r2), make_float2(hw_rsqrt(r2.x), hw_rsqrt(r2.y)), a2);
           }
+          acc += a2.x + a2.y;
         } else {
           unsigned big = 0;
 #pragma unroll
