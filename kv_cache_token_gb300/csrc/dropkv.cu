@@ -297,6 +297,11 @@ __global__ void __launch_bounds__(kWarps * 32) d3_pass1_kernel(D3Args A) {
 // kA false: the LSE alone (the chunks' partial outputs were not written).
 template <bool kA>
 __global__ void __launch_bounds__(256) d3_combine_kernel(D3Args A) {
+  // launched as a dependent of pass 1: its partials are complete past the
+  // wait; pass 2 may launch at once (all of this grid is resident, and pass
+  // 2 waits for it before reading what it writes)
+  grid_dep_wait();
+  grid_dep_launch();
   const int l = blockIdx.y;
   const int r = blockIdx.x * 8 + (threadIdx.x >> 5), lane = threadIdx.x & 31;
   if (r >= A.rows) return;
@@ -1451,6 +1456,10 @@ __global__ void __launch_bounds__(kP2Threads, 1) d3_p2_kernel(D3Args A, const __
     const uint32_t lane_off = static_cast<uint32_t>(qd * 32) << 16;
     const int b = l / A.dm.Hkv, kh = l % A.dm.Hkv;
     stage_rows(sq, 0, A, l, rt, tid, kRowThreads);
+    // launched as a dependent of the combine: everything above (the barriers,
+    // tensor memory, Q, and the producers' K/V copies) overlaps it; a, the
+    // row statistics, |v|^2 and the output are read or written past the wait
+    grid_dep_wait();
     if (kRes) {
       stage_rows(sah, 1, A, l, rt, tid, kRowThreads);
       stage_rows(sal, 2, A, l, rt, tid, kRowThreads);
@@ -1745,18 +1754,22 @@ static cudaError_t launch_window(const Ctx& ctx, int layer, const void* q_win, i
     D3Maps mp;
     for (int i = 0; i < kTmapsPerLayer; ++i) mp.m[i] = ctx.tmaps[static_cast<size_t>(layer) * kTmapsPerLayer + i];
     const dim3 cgrid((A.rows + 7) / 8, dm.lanes);
+    // the combine and pass 2 are dependent launches (each orders itself
+    // with griddepcontrol.wait before it reads its predecessor's results)
+    cudaError_t e;
     if (res) {
       d3_p1_kernel<true><<<grid, kP1Threads, kP1Smem, stream>>>(A, mp);
-      d3_combine_kernel<true><<<cgrid, 256, 0, stream>>>(A);
-      d3_p2_kernel<kResidual><<<grid, kP2Threads, p2_smem(true), stream>>>(A, mp);
+      e = launch_k(d3_combine_kernel<true>, cgrid, dim3(256), 0, stream, true, A);
+      if (e == cudaSuccess) e = launch_k(d3_p2_kernel<kResidual>, grid, dim3(kP2Threads), p2_smem(true), stream, true, A, mp);
     } else {
       d3_p1_kernel<false><<<grid, kP1Threads, kP1Smem, stream>>>(A, mp);
-      d3_combine_kernel<false><<<cgrid, 256, 0, stream>>>(A);
-      if (mode == kMassLater)
-        d3_p2_kernel<kMassLater><<<grid, kP2Threads, p2_smem(false), stream>>>(A, mp);
-      else
-        d3_p2_kernel<kMassCausal><<<grid, kP2Threads, p2_smem(false), stream>>>(A, mp);
+      e = launch_k(d3_combine_kernel<false>, cgrid, dim3(256), 0, stream, true, A);
+      if (e == cudaSuccess)
+        e = mode == kMassLater
+                ? launch_k(d3_p2_kernel<kMassLater>, grid, dim3(kP2Threads), p2_smem(false), stream, true, A, mp)
+                : launch_k(d3_p2_kernel<kMassCausal>, grid, dim3(kP2Threads), p2_smem(false), stream, true, A, mp);
     }
+    if (e != cudaSuccess) return e;
   } else {
     const int groups = (A.rows + kRowsPerCta - 1) / kRowsPerCta;
     dim3 grid(A.chunks, dm.lanes, groups);
