@@ -2538,13 +2538,17 @@ int epilogue_ctas_per_sm() {
 }
 
 // kRingCluster when a cluster of the ring epilogue can be resident (one
-// CTA per SM of a cluster), else 0.
+// CTA per SM of a cluster, for both storage types), else 0.
 int ring_cluster_ctas() {
-  int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_epilogue_ring_cluster_kernel<__nv_bfloat16>,
-                                                    kEpiThreads, kEpiDynSmem) != cudaSuccess)
-    return 0;
-  return n >= 1 ? kRingCluster : 0;
+  int best = 1 << 30;
+  auto take = [&](auto kernel) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, kEpiThreads, kEpiDynSmem) != cudaSuccess) n = 0;
+    best = n < best ? n : best;
+  };
+  take(decode_epilogue_ring_cluster_kernel<__nv_bfloat16>);
+  take(decode_epilogue_ring_cluster_kernel<float>);
+  return best >= 1 ? kRingCluster : 0;
 }
 
 cudaError_t lean_epilogue_attributes(cudaFuncAttributes* a, int* threads) {
