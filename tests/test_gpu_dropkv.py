@@ -33,6 +33,15 @@ def test_window_scores_scaled():
     run_score(shp)
 
 
+def test_window_scores_one_row_tile():
+    """128 window rows (group 4 x 32 positions): one row tile, so pass 2
+    writes each key's sum itself (no second tile adds into it); the context
+    spans several chunks and ends in a ragged tile."""
+    shp = scaled("dropkv_prefill", ctx=5001, num_kv_heads=2, num_q_heads=8, window=32, budget=250,
+                 recent_window=32)
+    run_score(shp)
+
+
 def test_window_scores_many_rows():
     """384 window rows per lane (group 8 x 48 positions): more rows than the
     two 128-row tensor-memory tiles, so the general kernel scores them."""
